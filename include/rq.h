@@ -1,0 +1,164 @@
+/*
+ * rq.h -- C ABI of the rotation-quantized KV cache library (librq.so), GB300 / sm_103a.
+ *
+ * The method ("SGLang 1-Bit Turbo" README, section "RotorQuant KV Cache Compression", and
+ * the TurboQuant section it is compared with): every K and V vector written to the cache
+ * keeps its L2 norm, is turned by a fixed data-oblivious rotation -- 2D Givens pairs
+ * (PlanarQuant) or 4D unit-quaternion blocks (IsoQuant) -- and each rotated coordinate is
+ * coded with a b-bit Lloyd-Max scalar quantizer (modes rq3/rq4 x planar/iso).  Attention
+ * reads the packed cache directly: because the rotation is orthogonal, a query is rotated
+ * once instead of un-rotating every key, values are summed in the rotated space and the
+ * output is rotated back once.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller; the library
+ *     never frees them.  Pointers marked "host" are read during the call only.
+ *   - fp16 means IEEE binary16 stored as 2-byte values.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls enqueue work and
+ *     return without synchronising; the caller keeps inputs alive until the stream passes.
+ *   - A context holds one split-K workspace: calls on the same context must not overlap on
+ *     the GPU (issue them on one stream, or order the streams).
+ *   - Return value: RQ_OK or an RQ_ERR_* code.  Argument errors are detected on the host
+ *     before anything is enqueued.  Nothing throws across this boundary.
+ *   - `d_status` (device int32, nullable): data-dependent range faults found by a kernel
+ *     (a page id outside [0, num_pages), a slot outside the pool, a sequence longer than
+ *     its block-table row) are OR-ed into *d_status as RQ_STATUS_* bits; the offending
+ *     index is clamped so no access leaves its buffer, and the outputs of the affected
+ *     sequence are unspecified.  The library never clears *d_status.
+ *
+ * Storage contract (the pages fix none of it; see the design doc for the readings):
+ *   page pool   : device bytes [num_pages][num_kv_heads][page_bytes]; the chunk of
+ *                 (page, kv head) is   K codes [P][vb] | V codes [P][vb] | K norms fp16 [P] |
+ *                 V norms fp16 [P],  vb = head_dim * bits / 8, page_bytes = P * (2 vb + 4).
+ *   4-bit codes : byte j = code[2j] | code[2j+1] << 4.
+ *   3-bit codes : per 32-dim group w, 12 bytes at 12w = little-endian words W0, W1, W2:
+ *                 W0 bits 2i.. = code[32w+i] & 3, W1 bits 2i.. = code[32w+16+i] & 3
+ *                 (i = 0..15), W2 bit p(i) = code[32w+i] >> 2 with i = 16h + 4k + r and
+ *                 p(i) = 8k + 2h + {4,5,0,1}[r].
+ *   code        : number of bin boundaries strictly below u = (R x)_i / ||x||, where the
+ *                 boundaries are midpoints of consecutive centroids; a vector of norm 0
+ *                 codes every coordinate as 2^(bits-1) - 1.
+ *   norm        : ||x|| rounded to fp16 (nearest even).
+ *   slot        : page * P + offset in page; block_table[b][i] is the page holding tokens
+ *                 i*P .. i*P+P-1 of sequence b.
+ */
+#ifndef RQ_H
+#define RQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes */
+#define RQ_OK 0
+#define RQ_ERR_INVALID 1       /* a NULL pointer, a negative size, inconsistent geometry */
+#define RQ_ERR_UNSUPPORTED 2   /* valid but not built: head_dim != 128, bits not 3/4, ... */
+#define RQ_ERR_CUDA 3          /* a CUDA call failed (allocation, copy or launch) */
+#define RQ_ERR_CAPACITY 4      /* batch, query tokens or block-table width above the context's limits */
+
+/* Bits of *d_status */
+#define RQ_STATUS_BAD_PAGE 1   /* block-table entry outside [0, num_pages) */
+#define RQ_STATUS_BAD_SLOT 2   /* slot_mapping entry >= num_pages * page_size */
+#define RQ_STATUS_BAD_LEN 4    /* seq_len < 0 or above max_pages * page_size, or below T */
+#define RQ_STATUS_NORM_OVERFLOW 8 /* a vector norm above the fp16 range (stored as inf) */
+
+/* Rotation families ("--kv-cache-dtype rq{3,4}_{planar,iso}") */
+#define RQ_PLANAR 0            /* PlanarQuant: 2D Givens rotation per dimension pair */
+#define RQ_ISO 1               /* IsoQuant: unit quaternion per 4-dimension block */
+
+typedef struct rq_ctx rq_ctx;  /* opaque, owned by the library */
+
+typedef struct {
+  int head_dim;              /* must be 128 */
+  int num_q_heads;           /* Hq, a multiple of num_kv_heads */
+  int num_kv_heads;          /* Hkv >= 1 */
+  int bits;                  /* 3 or 4 */
+  int mode;                  /* RQ_PLANAR or RQ_ISO */
+  int page_size;             /* P: a multiple of 16, at most 256 */
+  int num_pages;             /* pages in the caller's pool */
+  int max_batch;             /* largest B of an attention call */
+  int max_query_tokens;      /* largest T of a verify call (>= 1) */
+  int max_pages_per_seq;     /* largest block-table width (max_pages) of an attention call */
+  /* host float32 [num_kv_heads][head_dim]: planar -> [Hkv][d/2][2] = (cos t, sin t) of the
+     pair (2i, 2i+1), y_2i = c x_2i - s x_2i+1, y_2i+1 = s x_2i + c x_2i+1;
+     iso -> [Hkv][d/4][4] = unit quaternion (a, b, c, d) of block 4i..4i+3, y = q (x) x
+     (Hamilton product, q on the left).  rot_k turns keys and queries, rot_v values. */
+  const float *rot_k;
+  const float *rot_v;
+  /* host float32 [2^bits] ascending centroids, or NULL for the Lloyd-Max quantizer of
+     N(0, 1/head_dim) (the levels of N(0,1) divided by sqrt(head_dim)). */
+  const float *codebook;
+  float sm_scale;            /* softmax scale; 0 selects 1/sqrt(head_dim) */
+  int device;                /* CUDA device ordinal the context lives on; -1 = current */
+} rq_config;
+
+/* Validates cfg, copies the rotation tables and codebook to the device and allocates the
+   split-K workspace on cfg->device.  On success *out is a new context; on failure *out is
+   NULL and nothing stays allocated.  Errors: RQ_ERR_INVALID, RQ_ERR_UNSUPPORTED, RQ_ERR_CUDA. */
+int rq_create(rq_ctx **out, const rq_config *cfg);
+
+/* Releases everything rq_create allocated.  NULL-safe.  The caller must make sure no work of
+   this context is still running (synchronise its stream first). */
+void rq_free(rq_ctx *ctx);
+
+/* Bytes of one (page, kv head) chunk: page_size * (2 * head_dim * bits / 8 + 4).  0 for NULL. */
+size_t rq_page_bytes(const rq_ctx *ctx);
+
+/* Host only (no GPU needed): the default codebook -- ascending centroids of the Lloyd-Max
+   quantizer of N(0,1) with 2^bits levels, divided by sqrt(head_dim), rounded to float32 --
+   into centroids[2^bits].  bits in 1..8, head_dim >= 1.  Returns RQ_OK or RQ_ERR_INVALID. */
+int rq_lloyd_max_codebook(int bits, int head_dim, float *centroids);
+
+/* Host copies of the context's centroids [2^bits] and bin boundaries [2^bits - 1] (float32;
+   boundary j = float((centroid_j + centroid_{j+1}) / 2) computed in double).  Either may be NULL. */
+int rq_get_codebook(const rq_ctx *ctx, float *centroids, float *boundaries);
+
+/*
+ * Quantize-on-append (one fused kernel): for token t < n and kv head h, encode
+ * k[t][h][:] and v[t][h][:] (device fp16 [n][Hkv][head_dim]) into slot slot_mapping[t]
+ * (device int32 [n]) of the page pool kv_pages (device, see the storage contract).  A slot
+ * < 0 is skipped (padding); a slot >= num_pages * page_size sets RQ_STATUS_BAD_SLOT and is
+ * skipped.  Slots within one call must be distinct.  n = 0 is a no-op.
+ */
+int rq_quantize_append(rq_ctx *ctx, const void *k, const void *v, const int32_t *slot_mapping,
+                       int n, void *kv_pages, int32_t *d_status, void *stream);
+
+/*
+ * GQA decode attention over the packed cache (split-K flash-decode + log-sum-exp combine).
+ *   q           device fp16 [B][Hq][head_dim]
+ *   kv_pages    device page pool
+ *   block_table device int32 [B][max_pages]
+ *   seq_lens    device int32 [B]: tokens of sequence b, all attended (0 gives zeros)
+ *   out         device fp16 [B][Hq][head_dim]; head hq reads kv head hq / (Hq / Hkv)
+ * out = softmax(sm_scale * q K^T) V over the dequantised cache.  B may be 0.
+ * Errors: RQ_ERR_INVALID, RQ_ERR_CAPACITY (B > max_batch, max_pages > max_pages_per_seq),
+ * RQ_ERR_CUDA.
+ */
+int rq_decode_attention(rq_ctx *ctx, const void *q, const void *kv_pages, const int32_t *block_table,
+                        int max_pages, const int32_t *seq_lens, int B, void *out, int32_t *d_status,
+                        void *stream);
+
+/*
+ * Speculative chain-verify attention: T query tokens per sequence, the last T cached tokens
+ * being the drafts themselves (append them first).  Query row j (0 <= j < T) attends to
+ * positions 0 .. seq_lens[b] - T + j (causal over the draft tail).
+ *   q   device fp16 [B][T][Hq][head_dim],   out device fp16 [B][T][Hq][head_dim]
+ * Other arguments as rq_decode_attention; T = 1 is decode.  0 < seq_lens[b] < T sets
+ * RQ_STATUS_BAD_LEN.  Errors as rq_decode_attention, plus RQ_ERR_CAPACITY for
+ * T > max_query_tokens.
+ */
+int rq_verify_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
+                        const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
+                        void *out, int32_t *d_status, void *stream);
+
+/* Static English text for a return code (never NULL). */
+const char *rq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RQ_H */

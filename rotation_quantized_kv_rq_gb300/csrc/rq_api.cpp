@@ -1,0 +1,297 @@
+// Host side of the C ABI declared in include/rq.h: argument validation, the context (device
+// tables and split-K workspace), the default Lloyd-Max codebook and launch planning.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/rq.h"
+#include "rq_internal.h"
+
+struct rq_ctx {
+  rq_config cfg;          // host pointers cleared after creation
+  rq::Geometry g;
+  int device;
+  int num_sms;
+  float* d_tables;        // rot_k | rot_v | centroids | boundaries
+  float* d_ws;            // split-K partials
+  size_t ws_floats;
+  int max_splits;
+  int max_n_tiles;        // ceil(max_query_tokens * group / 8)
+  float centroids[256];
+  float boundaries[255];
+};
+
+namespace {
+
+constexpr int kMaxSplitsDefault = 64;
+constexpr int kMaxSplitPages = 1024;  // mirrors the kernel's staging buffer
+
+// Makes `dev` current for the scope and restores the previous device afterwards.
+class DeviceScope {
+ public:
+  explicit DeviceScope(int dev) {
+    ok_ = cudaGetDevice(&prev_) == cudaSuccess;
+    if (ok_ && dev >= 0 && dev != prev_) {
+      ok_ = cudaSetDevice(dev) == cudaSuccess;
+      switched_ = ok_;
+    }
+  }
+  ~DeviceScope() {
+    if (switched_) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = 0;
+  bool ok_ = false, switched_ = false;
+};
+
+// Lloyd-Max levels of the standard normal with 2^bits levels.  The quantizer is symmetric,
+// so only the positive half is iterated: cells [x_{k-1}, x_k) with x_0 = 0 and x_K = inf,
+// levels y_k = E[X | cell k] = (phi(x_{k-1}) - phi(x_k)) / (Q(x_{k-1}) - Q(x_k)) with Q the
+// upper tail, thresholds x_k = (y_k + y_{k+1}) / 2; repeated until the levels stop moving.
+void lloyd_max_positive_half(int levels, double* out_ascending) {
+  const int K = levels / 2;
+  double y[128], x[129];
+  for (int k = 0; k < K; ++k) y[k] = 4.0 * (k + 0.5) / K;
+  auto pdf = [](double v) { return std::exp(-0.5 * v * v) * 0.39894228040143267794; };
+  auto tail = [](double v) { return 0.5 * std::erfc(v * 0.70710678118654752440); };
+  for (int iter = 0; iter < 4000000; ++iter) {
+    x[0] = 0.0;
+    for (int k = 1; k < K; ++k) x[k] = 0.5 * (y[k - 1] + y[k]);
+    double change = 0.0;
+    for (int k = 0; k < K; ++k) {
+      const double a = x[k];
+      const double num = pdf(a) - (k + 1 < K ? pdf(x[k + 1]) : 0.0);
+      const double den = tail(a) - (k + 1 < K ? tail(x[k + 1]) : 0.0);
+      const double ny = num / den;
+      change = std::fmax(change, std::fabs(ny - y[k]));
+      y[k] = ny;
+    }
+    if (change < 1e-15) break;
+  }
+  for (int k = 0; k < K; ++k) {
+    out_ascending[K + k] = y[k];
+    out_ascending[K - 1 - k] = -y[k];
+  }
+}
+
+int check_geometry(const rq_config* c) {
+  if (c->head_dim <= 0 || c->num_q_heads <= 0 || c->num_kv_heads <= 0 || c->page_size <= 0 || c->num_pages <= 0 ||
+      c->max_batch <= 0 || c->max_query_tokens <= 0 || c->max_pages_per_seq <= 0)
+    return RQ_ERR_INVALID;
+  if (c->num_q_heads % c->num_kv_heads != 0) return RQ_ERR_INVALID;
+  if (c->mode != RQ_PLANAR && c->mode != RQ_ISO) return RQ_ERR_INVALID;
+  if (!c->rot_k || !c->rot_v) return RQ_ERR_INVALID;
+  if (c->head_dim != rq::kHeadDim) return RQ_ERR_UNSUPPORTED;
+  if (c->bits != 3 && c->bits != 4) return RQ_ERR_UNSUPPORTED;
+  if (c->page_size % 16 != 0 || c->page_size > 256) return RQ_ERR_UNSUPPORTED;
+  if ((long long)c->num_pages * c->page_size > INT32_MAX) return RQ_ERR_UNSUPPORTED;
+  if (!(c->sm_scale >= 0.0f) || std::isinf(c->sm_scale)) return RQ_ERR_INVALID;
+  return RQ_OK;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* rq_status_string(int status) {
+  switch (status) {
+    case RQ_OK: return "ok";
+    case RQ_ERR_INVALID: return "invalid argument";
+    case RQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case RQ_ERR_CUDA: return "CUDA error";
+    case RQ_ERR_CAPACITY: return "above the context's capacity";
+    default: return "unknown status";
+  }
+}
+
+int rq_lloyd_max_codebook(int bits, int head_dim, float* centroids) {
+  if (bits < 1 || bits > 8 || head_dim < 1 || !centroids) return RQ_ERR_INVALID;
+  const int L = 1 << bits;
+  double c[256];
+  lloyd_max_positive_half(L, c);
+  const double s = 1.0 / std::sqrt((double)head_dim);
+  for (int j = 0; j < L; ++j) centroids[j] = (float)(c[j] * s);
+  return RQ_OK;
+}
+
+int rq_create(rq_ctx** out, const rq_config* cfg) {
+  if (!out) return RQ_ERR_INVALID;
+  *out = nullptr;
+  if (!cfg) return RQ_ERR_INVALID;
+  int st = check_geometry(cfg);
+  if (st != RQ_OK) return st;
+
+  rq_ctx* ctx = new (std::nothrow) rq_ctx();
+  if (!ctx) return RQ_ERR_CUDA;
+  ctx->cfg = *cfg;
+  const int L = 1 << cfg->bits;
+  if (cfg->codebook) {
+    for (int j = 0; j < L; ++j) {
+      if (!std::isfinite(cfg->codebook[j]) || (j > 0 && !(cfg->codebook[j] > cfg->codebook[j - 1]))) {
+        delete ctx;
+        return RQ_ERR_INVALID;
+      }
+      ctx->centroids[j] = cfg->codebook[j];
+    }
+  } else {
+    rq_lloyd_max_codebook(cfg->bits, cfg->head_dim, ctx->centroids);
+  }
+  for (int j = 0; j + 1 < L; ++j)
+    ctx->boundaries[j] = (float)(0.5 * ((double)ctx->centroids[j] + (double)ctx->centroids[j + 1]));
+  ctx->cfg.rot_k = ctx->cfg.rot_v = ctx->cfg.codebook = nullptr;
+
+  int dev = cfg->device;
+  if (dev < 0 && cudaGetDevice(&dev) != cudaSuccess) {
+    delete ctx;
+    return RQ_ERR_CUDA;
+  }
+  ctx->device = dev;
+  DeviceScope scope(dev);
+  if (!scope.ok() || cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    delete ctx;
+    return RQ_ERR_CUDA;
+  }
+
+  const int hkv = cfg->num_kv_heads, d = cfg->head_dim;
+  const size_t rot = (size_t)hkv * d;
+  const size_t table_floats = 2 * rot + 256 + 256;
+  const int group = cfg->num_q_heads / hkv;
+  ctx->max_n_tiles = (cfg->max_query_tokens * group + 7) / 8;
+  ctx->max_splits = kMaxSplitsDefault;
+  const int need = (cfg->max_pages_per_seq + kMaxSplitPages - 1) / kMaxSplitPages;
+  if (need > ctx->max_splits) ctx->max_splits = need;
+  if (ctx->max_splits > cfg->max_pages_per_seq) ctx->max_splits = cfg->max_pages_per_seq;
+  ctx->ws_floats = (size_t)cfg->max_batch * hkv * ctx->max_n_tiles * ctx->max_splits * 8 * rq::kPartialStride;
+
+  cudaError_t e = cudaMalloc(&ctx->d_tables, table_floats * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_ws, ctx->ws_floats * sizeof(float));
+  float* host = nullptr;
+  if (e == cudaSuccess) {
+    host = (float*)std::calloc(table_floats, sizeof(float));
+    if (!host) e = cudaErrorMemoryAllocation;
+  }
+  if (e == cudaSuccess) {
+    std::memcpy(host, cfg->rot_k, rot * sizeof(float));
+    std::memcpy(host + rot, cfg->rot_v, rot * sizeof(float));
+    std::memcpy(host + 2 * rot, ctx->centroids, L * sizeof(float));
+    std::memcpy(host + 2 * rot + 256, ctx->boundaries, (L - 1) * sizeof(float));
+    e = cudaMemcpy(ctx->d_tables, host, table_floats * sizeof(float), cudaMemcpyHostToDevice);
+  }
+  std::free(host);
+  if (e == cudaSuccess) e = rq::attention_prepare();
+  if (e != cudaSuccess) {
+    cudaFree(ctx->d_tables);
+    cudaFree(ctx->d_ws);
+    delete ctx;
+    return RQ_ERR_CUDA;
+  }
+
+  rq::Geometry& g = ctx->g;
+  g.num_q_heads = cfg->num_q_heads;
+  g.num_kv_heads = hkv;
+  g.group = group;
+  g.bits = cfg->bits;
+  g.mode = cfg->mode;
+  g.page_size = cfg->page_size;
+  g.num_pages = cfg->num_pages;
+  g.vec_bytes = d * cfg->bits / 8;
+  g.page_bytes = cfg->page_size * (2 * g.vec_bytes + 4);
+  const float scale = cfg->sm_scale > 0.f ? cfg->sm_scale : (float)(1.0 / std::sqrt((double)d));
+  g.q_scale = (float)(scale * 1.44269504088896340736);
+  g.rot_k = ctx->d_tables;
+  g.rot_v = ctx->d_tables + rot;
+  g.centroids = ctx->d_tables + 2 * rot;
+  g.boundaries = ctx->d_tables + 2 * rot + 256;
+  *out = ctx;
+  return RQ_OK;
+}
+
+void rq_free(rq_ctx* ctx) {
+  if (!ctx) return;
+  {
+    DeviceScope scope(ctx->device);
+    cudaFree(ctx->d_tables);
+    cudaFree(ctx->d_ws);
+  }
+  delete ctx;
+}
+
+size_t rq_page_bytes(const rq_ctx* ctx) { return ctx ? (size_t)ctx->g.page_bytes : 0; }
+
+int rq_get_codebook(const rq_ctx* ctx, float* centroids, float* boundaries) {
+  if (!ctx) return RQ_ERR_INVALID;
+  const int L = 1 << ctx->g.bits;
+  if (centroids) std::memcpy(centroids, ctx->centroids, L * sizeof(float));
+  if (boundaries) std::memcpy(boundaries, ctx->boundaries, (L - 1) * sizeof(float));
+  return RQ_OK;
+}
+
+int rq_quantize_append(rq_ctx* ctx, const void* k, const void* v, const int32_t* slot_mapping, int n,
+                       void* kv_pages, int32_t* d_status, void* stream) {
+  if (!ctx || n < 0) return RQ_ERR_INVALID;
+  if (n == 0) return RQ_OK;
+  if (!k || !v || !slot_mapping || !kv_pages) return RQ_ERR_INVALID;
+  DeviceScope scope(ctx->device);
+  if (!scope.ok()) return RQ_ERR_CUDA;
+  return to_status(rq::launch_append(ctx->g, k, v, slot_mapping, n, (uint8_t*)kv_pages, d_status,
+                                     (cudaStream_t)stream));
+}
+
+int rq_verify_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages, const int32_t* block_table,
+                        int max_pages, const int32_t* seq_lens, int B, void* out, int32_t* d_status, void* stream) {
+  if (!ctx || B < 0 || T < 1 || max_pages < 1) return RQ_ERR_INVALID;
+  if (B == 0) return RQ_OK;
+  if (!q || !kv_pages || !block_table || !seq_lens || !out) return RQ_ERR_INVALID;
+  if (B > ctx->cfg.max_batch || T > ctx->cfg.max_query_tokens || max_pages > ctx->cfg.max_pages_per_seq)
+    return RQ_ERR_CAPACITY;
+  DeviceScope scope(ctx->device);
+  if (!scope.ok()) return RQ_ERR_CUDA;
+
+  rq::AttnArgs a;
+  a.q = q;
+  a.pages = (const uint8_t*)kv_pages;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.B = B;
+  a.T = T;
+  a.out = out;
+  a.status = d_status;
+  a.ws = ctx->d_ws;
+  a.rows = T * ctx->g.group;
+  a.n_tiles_n = (a.rows + 7) / 8;
+  a.max_splits = ctx->max_splits;
+
+  // Split planning: about 8 work items per resident CTA, each split a whole number of
+  // "one 16-token tile per warp" rounds.
+  const int P = ctx->g.page_size;
+  const long long units = (long long)B * ctx->g.num_kv_heads * a.n_tiles_n;
+  const long long target = 8LL * ctx->num_sms;
+  long long nsplit = (target + units - 1) / units;
+  if (nsplit < 1) nsplit = 1;
+  if (nsplit > ctx->max_splits) nsplit = ctx->max_splits;
+  const int quantum = 256 / P > 0 ? 256 / P : 1;
+  long long pps = (max_pages + nsplit - 1) / nsplit;
+  pps = (pps + quantum - 1) / quantum * quantum;
+  const long long min_pps = (max_pages + ctx->max_splits - 1) / ctx->max_splits;
+  if (pps < min_pps) pps = min_pps;
+  if (pps > kMaxSplitPages) pps = kMaxSplitPages;
+  if ((max_pages + pps - 1) / pps > ctx->max_splits) return RQ_ERR_CAPACITY;
+  a.pages_per_split = (int)pps;
+  return to_status(rq::launch_attention(ctx->g, a, ctx->num_sms, (cudaStream_t)stream));
+}
+
+int rq_decode_attention(rq_ctx* ctx, const void* q, const void* kv_pages, const int32_t* block_table, int max_pages,
+                        const int32_t* seq_lens, int B, void* out, int32_t* d_status, void* stream) {
+  return rq_verify_attention(ctx, q, 1, kv_pages, block_table, max_pages, seq_lens, B, out, d_status, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,646 @@
+// GQA decode / chain-verify attention that reads the packed cache directly, and the
+// log-sum-exp combine that merges the split-K partials and rotates the output back.
+//
+// Method ("SGLang 1-Bit Turbo" README, section "RotorQuant KV Cache Compression"): keys and
+// values are stored as norm * R^T c[code] with an orthogonal structured R.  Hence
+//   <q, k>  = n_k * <R_k q, c[code_k]>          (rotate q once, never un-rotate a key)
+//   sum p v = R_v^T sum p n_v c[code_v]          (sum in rotated space, rotate back once)
+//
+// Kernel design (sm_103a):
+//   * Persistent CTAs of 16 warps; work item = (sequence, kv head, query n-tile, split of
+//     the context).  The CTA stages the split's page ids in shared memory, every warp takes
+//     16-token tiles of the split round-robin, and the warps' (m, l, O) are merged through
+//     shared memory into one partial per item.
+//   * Per 16-token tile both contractions run on the tensor cores with mma.sync m16n8k16
+//     (fp16 in, fp32 accumulate): S^T[16 tok x 8 q] = K~[16 x 128] q~^T and
+//     O^T[128 x 8 q] += V~^T[128 x 16 tok] P^T.  The <= 8 query rows of a kv head (the GQA
+//     group, or group x drafts for verify) are the N = 8 side, so no query padding to 16.
+//   * Codes become fp16 centroids through a lane-replicated shared-memory table: one byte of
+//     codes (two 4-bit codes, or two 3-bit codes assembled from the 3-bit planes) indexes a
+//     half2 entry; each lane reads its own copy of the entry, so lookups never conflict.
+//   * P is moved from the S^T accumulator layout to the B-operand layout with movmatrix.
+//   * Scores are kept in base 2 (sm_scale * log2 e folded into q~).
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include "rq_internal.h"
+#include "../../include/rq.h"
+
+namespace rq {
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kLutBytes = 256 * 256;          // 256 index bytes x (2 tables x 32 lanes x 4 B)
+constexpr int kMaxSplitPages = 1024;          // page ids staged per item
+constexpr int kMergeFloats = kWarps * 8 * kPartialStride;
+constexpr size_t kSmemBytes = kLutBytes + (size_t)kMergeFloats * 4 + kMaxSplitPages * 4 + 64;
+
+// ---------------------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+template <uint32_t LUT>
+__device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, %4;" : "=r"(d) : "r"(a), "r"(b), "r"(c), "n"(LUT));
+  return d;
+}
+// (a & c) | (b & ~c)
+__device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t c) { return lop3<0xE2>(a, b, c); }
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
+}
+
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ldg_stream4(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ldg_stream2(const void* p) {
+  unsigned short r;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
+  return __half2float(__ushort_as_half((unsigned short)bits16));
+}
+
+// ---------------------------------------------------------------------------------------
+// Code tables.  Entry e of a table is the half2 (c[code_a], c[code_b]) of the two codes an
+// index byte e carries:
+//   T4 (4-bit):  code_a = e & 15,                       code_b = e >> 4
+//   T1 (3-bit):  code_a = (e & 3) | (e >> 4 & 1) << 2,   code_b = (e >> 2 & 3) | (e >> 5 & 1) << 2
+//   T2 (3-bit):  code_a = (e >> 4 & 3) | (e & 1) << 2,   code_b = (e >> 6 & 3) | (e >> 1 & 1) << 2
+// Row e holds 64 words: word l (l < 32) is the first table's entry for lane l, word 32 + l the
+// second table's (T2 for 3-bit; a copy of T4 for 4-bit).  A lookup address is
+// base + e * 256 + lane * 4 (+ 128 for the second table).
+// ---------------------------------------------------------------------------------------
+template <int BITS>
+__device__ void build_lut(uint32_t* lut, const float* centroids) {
+  __shared__ float cb[16];
+  if (threadIdx.x < (1 << BITS)) cb[threadIdx.x] = centroids[threadIdx.x];
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256 * 64; i += kThreads) {
+    const int e = i >> 6, second = (i >> 5) & 1;
+    int ca, cbx;
+    if (BITS == 4) {
+      ca = e & 15;
+      cbx = e >> 4;
+    } else if (!second) {
+      ca = (e & 3) | ((e >> 4) & 1) << 2;
+      cbx = ((e >> 2) & 3) | ((e >> 5) & 1) << 2;
+    } else {
+      ca = ((e >> 4) & 3) | (e & 1) << 2;
+      cbx = ((e >> 6) & 3) | ((e >> 1) & 1) << 2;
+    }
+    lut[i] = pack_half2(cb[ca], cb[cbx]);
+  }
+}
+
+// Half2 of the two codes in byte J of index word x (SECOND selects the second table).
+template <int J, int SECOND>
+__device__ __forceinline__ uint32_t lut(uint32_t x, uint32_t lane_off, uint32_t base) {
+  const uint32_t a = prmt(x, lane_off, 0x5504u | (J << 4));
+  return lds32(a + base + (SECOND ? 128u : 0u));
+}
+template <int SECOND>
+__device__ __forceinline__ uint32_t lut_dyn(uint32_t x, int j, uint32_t lane_off, uint32_t base) {
+  const uint32_t a = prmt(x, lane_off, 0x5504u | (j << 4));
+  return lds32(a + base + (SECOND ? 128u : 0u));
+}
+
+// ---------------------------------------------------------------------------------------
+// Raw tile data of one lane (lane = 4g + t):
+//   K rows g and g+8, the 32 dims 32t..32t+31 of each;
+//   V tokens 2t, 2t+1, 2t+8, 2t+9, the 16 dims 16g..16g+15 of each;
+//   the K and V norms of tokens g and g+8.
+// ---------------------------------------------------------------------------------------
+template <int BITS>
+struct Raw;
+
+template <>
+struct Raw<4> {
+  uint4 k[2];        // 16 bytes = 32 codes per K row
+  uint2 v[4];        // 8 bytes = 16 codes per V token
+  uint32_t nk, nv;   // fp16 norms of tokens g (low) and g+8 (high)
+};
+template <>
+struct Raw<3> {
+  uint32_t k[2][3];  // W0, W1, W2 of group t
+  uint32_t v[4][2];  // W(g&1) and W2 of group g/2
+  uint32_t nk, nv;
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_tile(Raw<BITS>& r, const uint8_t* chunk, int off, int P, int g, int t) {
+  constexpr int vb = BITS * 16;
+  const uint8_t* kb = chunk + (size_t)off * vb;
+  const uint8_t* vbp = chunk + (size_t)(P + off) * vb;
+  const uint8_t* nb = chunk + (size_t)2 * P * vb + 2 * off;
+  const int vt[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+  if constexpr (BITS == 4) {
+    r.k[0] = ldg_stream16(kb + g * 64 + 16 * t);
+    r.k[1] = ldg_stream16(kb + (g + 8) * 64 + 16 * t);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.v[i] = ldg_stream8(vbp + vt[i] * 64 + 8 * g);
+  } else {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int w = 0; w < 3; ++w) r.k[rr][w] = ldg_stream4(kb + (g + 8 * rr) * 48 + 12 * t + 4 * w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      r.v[i][0] = ldg_stream4(vbp + vt[i] * 48 + 12 * (g >> 1) + 4 * (g & 1));
+      r.v[i][1] = ldg_stream4(vbp + vt[i] * 48 + 12 * (g >> 1) + 8);
+    }
+  }
+  r.nk = ldg_stream2(nb + 2 * g) | (ldg_stream2(nb + 2 * (g + 8)) << 16);
+  r.nv = ldg_stream2(nb + 2 * P + 2 * g) | (ldg_stream2(nb + 2 * P + 2 * (g + 8)) << 16);
+}
+
+// A operand of S^T = K~ q~^T for k-chunk kc: rows g / g+8 hold tokens g / g+8, k-slots
+// 2t,2t+1 hold dim pair 2kc and 2t+8,2t+9 dim pair 2kc+1 of the lane's 32 dims.
+// 4-bit: pair j is byte j of the row's 16 bytes.
+// 3-bit: X0 = W0.lo | W2.hi (T1, pairs 2k), X1 = W2.lo | W0.hi (T2, pairs 2k+1),
+//        X2 = W1.lo | (W2>>2).hi (T1, pairs 8+2k), X3 = (W2>>2).lo | W1.hi (T2, pairs 9+2k).
+template <int BITS>
+__device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const uint32_t (&qf)[8][2],
+                                        uint32_t lane_off, uint32_t base) {
+  s[0] = s[1] = s[2] = s[3] = 0.f;
+  float s2[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (BITS == 4) {
+    const uint32_t k0[4] = {r.k[0].x, r.k[0].y, r.k[0].z, r.k[0].w};
+    const uint32_t k1[4] = {r.k[1].x, r.k[1].y, r.k[1].z, r.k[1].w};
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) {
+      const int w = kc >> 1, j0 = (2 * kc) & 3;
+      uint32_t a0, a1, a2, a3;
+      if (j0 == 0) {
+        a0 = lut<0, 0>(k0[w], lane_off, base);
+        a1 = lut<0, 0>(k1[w], lane_off, base);
+        a2 = lut<1, 0>(k0[w], lane_off, base);
+        a3 = lut<1, 0>(k1[w], lane_off, base);
+      } else {
+        a0 = lut<2, 0>(k0[w], lane_off, base);
+        a1 = lut<2, 0>(k1[w], lane_off, base);
+        a2 = lut<3, 0>(k0[w], lane_off, base);
+        a3 = lut<3, 0>(k1[w], lane_off, base);
+      }
+      if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+      else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+    }
+  } else {
+    uint32_t X[2][4];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const uint32_t w0 = r.k[rr][0], w1 = r.k[rr][1], w2 = r.k[rr][2], w2s = w2 >> 2;
+      X[rr][0] = bitsel(w0, w2, 0x0F0F0F0Fu);
+      X[rr][1] = bitsel(w2, w0, 0x0F0F0F0Fu);
+      X[rr][2] = bitsel(w1, w2s, 0x0F0F0F0Fu);
+      X[rr][3] = bitsel(w2s, w1, 0x0F0F0F0Fu);
+    }
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) {
+      const int hi = kc >> 2, byte = kc & 3;
+      const uint32_t a0 = lut_dyn<0>(X[0][2 * hi], byte, lane_off, base);
+      const uint32_t a1 = lut_dyn<0>(X[1][2 * hi], byte, lane_off, base);
+      const uint32_t a2 = lut_dyn<1>(X[0][2 * hi + 1], byte, lane_off, base);
+      const uint32_t a3 = lut_dyn<1>(X[1][2 * hi + 1], byte, lane_off, base);
+      if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+      else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s[i] += s2[i];
+}
+
+// A operand of O^T += V~^T P^T for m-tile mt: rows g / g+8 hold dims 16g+2mt / 16g+2mt+1,
+// k-slots 2t,2t+1 tokens (2t, 2t+1) and 2t+8,2t+9 tokens (2t+8, 2t+9).  Index bytes carry one
+// dim of two tokens, so the two tokens' code words are interleaved first.
+template <int BITS>
+__device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, uint32_t pb0, uint32_t pb1,
+                                        uint32_t lane_off, uint32_t base, int g) {
+  if constexpr (BITS == 4) {
+    uint32_t XE[2][2], XO[2][2];  // [token pair][word]
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const uint2 A = r.v[2 * pr], B = r.v[2 * pr + 1];
+      XE[pr][0] = bitsel(A.x, B.x << 4, 0x0F0F0F0Fu);
+      XE[pr][1] = bitsel(A.y, B.y << 4, 0x0F0F0F0Fu);
+      XO[pr][0] = bitsel(A.x >> 4, B.x, 0x0F0F0F0Fu);
+      XO[pr][1] = bitsel(A.y >> 4, B.y, 0x0F0F0F0Fu);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int w = mt >> 2, j = mt & 3;
+      const uint32_t a0 = lut_dyn<0>(XE[0][w], j, lane_off, base);
+      const uint32_t a1 = lut_dyn<0>(XO[0][w], j, lane_off, base);
+      const uint32_t a2 = lut_dyn<0>(XE[1][w], j, lane_off, base);
+      const uint32_t a3 = lut_dyn<0>(XO[1][w], j, lane_off, base);
+      mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+  } else {
+    const int sh = 2 * (g & 1);
+    uint32_t XE1[2], XE2[2], XO1[2], XO2[2];
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const uint32_t A = r.v[2 * pr][0], B = r.v[2 * pr + 1][0];
+      const uint32_t A2 = r.v[2 * pr][1], B2 = r.v[2 * pr + 1][1];
+      const uint32_t E = bitsel(A, B << 2, 0x33333333u);
+      const uint32_t O = bitsel(A >> 2, B, 0x33333333u);
+      const uint32_t M = bitsel(A2, B2 << 1, 0x55555555u) >> sh;
+      const uint32_t M2 = bitsel(A2 >> 1, B2, 0x55555555u) >> sh;
+      XE1[pr] = bitsel(E, M, 0x0F0F0F0Fu);
+      XE2[pr] = bitsel(M, E, 0x0F0F0F0Fu);
+      XO1[pr] = bitsel(O, M2, 0x0F0F0F0Fu);
+      XO2[pr] = bitsel(M2, O, 0x0F0F0F0Fu);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int j = mt >> 1;
+      uint32_t a0, a1, a2, a3;
+      if ((mt & 1) == 0) {
+        a0 = lut_dyn<0>(XE1[0], j, lane_off, base);
+        a1 = lut_dyn<0>(XO1[0], j, lane_off, base);
+        a2 = lut_dyn<0>(XE1[1], j, lane_off, base);
+        a3 = lut_dyn<0>(XO1[1], j, lane_off, base);
+      } else {
+        a0 = lut_dyn<1>(XE2[0], j, lane_off, base);
+        a1 = lut_dyn<1>(XO2[0], j, lane_off, base);
+        a2 = lut_dyn<1>(XE2[1], j, lane_off, base);
+        a3 = lut_dyn<1>(XO2[1], j, lane_off, base);
+      }
+      mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// The split-K kernel.
+// ---------------------------------------------------------------------------------------
+struct ItemInfo {
+  int b, h, nt, split;
+};
+
+__device__ __forceinline__ ItemInfo decode_item(int item, const Geometry& g, const AttnArgs& a, int nsplit) {
+  ItemInfo it;
+  it.split = item % nsplit;
+  int rest = item / nsplit;
+  it.nt = rest % a.n_tiles_n;
+  rest /= a.n_tiles_n;
+  it.h = rest % g.num_kv_heads;
+  it.b = rest / g.num_kv_heads;
+  return it;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_splitk_kernel(const Geometry g, const AttnArgs a, int nsplit, int n_items) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* lut_words = reinterpret_cast<uint32_t*>(smem);
+  float* merge = reinterpret_cast<float*>(smem + kLutBytes);
+  int* page_ids = reinterpret_cast<int*>(smem + kLutBytes + (size_t)kMergeFloats * 4);
+
+  build_lut<BITS>(lut_words, g.centroids);
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(lut_words);
+  const uint32_t lane_off = (uint32_t)lane * 4u;
+  const int P = g.page_size;
+  const int tiles_per_page = P / 16;
+  const __half* qh = reinterpret_cast<const __half*>(a.q);
+
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const ItemInfo it = decode_item(item, g, a, nsplit);
+    int len = a.seq_lens[it.b];
+    const int cap = a.max_pages * P;
+    if (len < 0 || len > cap || (len > 0 && len < a.T)) {
+      if (threadIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_LEN);
+      len = len < 0 ? 0 : (len > cap ? cap : len);
+    }
+    const int npages = (len + P - 1) / P;
+    const int p0 = it.split * a.pages_per_split;
+    int p1 = p0 + a.pages_per_split;
+    if (p1 > npages) p1 = npages;
+    if (p0 >= p1) continue;  // uniform across the CTA: the combine never reads this split
+
+    // Stage the split's page ids (clamped into the pool).
+    for (int i = threadIdx.x; i < p1 - p0; i += kThreads) {
+      int pg = a.block_table[(size_t)it.b * a.max_pages + p0 + i];
+      if (pg < 0 || pg >= g.num_pages) {
+        if (a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
+        pg = 0;
+      }
+      page_ids[i] = pg;
+    }
+
+    // q~ = R_k q * sm_scale * log2(e) for query column gq of this n-tile, the lane's 32 dims.
+    uint32_t qf[8][2];
+    const int row = it.nt * 8 + gq;  // query row of the kv head: draft j = row / group, head row % group
+    int last_pos[2];                  // last visible position of query columns 2tq, 2tq+1
+    {
+      float qv[32];
+      if (row < a.rows) {
+        const int j = row / g.group, head = it.h * g.group + row % g.group;
+        const __half* src = qh + (((size_t)it.b * a.T + j) * g.num_q_heads + head) * kHeadDim + 32 * tq;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(src + 8 * c);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+            qv[8 * c + 2 * e] = f.x;
+            qv[8 * c + 2 * e + 1] = f.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) qv[i] = 0.f;
+      }
+      const float4* rp = reinterpret_cast<const float4*>(g.rot_k + (size_t)it.h * kHeadDim + 32 * tq);
+      float y[32];
+#pragma unroll
+      for (int blk = 0; blk < 8; ++blk) {
+        const float4 p = __ldg(rp + blk);
+        const float* x = qv + 4 * blk;
+        if (g.mode == RQ_PLANAR) {
+          y[4 * blk + 0] = p.x * x[0] - p.y * x[1];
+          y[4 * blk + 1] = p.y * x[0] + p.x * x[1];
+          y[4 * blk + 2] = p.z * x[2] - p.w * x[3];
+          y[4 * blk + 3] = p.w * x[2] + p.z * x[3];
+        } else {
+          y[4 * blk + 0] = p.x * x[0] - p.y * x[1] - p.z * x[2] - p.w * x[3];
+          y[4 * blk + 1] = p.y * x[0] + p.x * x[1] - p.w * x[2] + p.z * x[3];
+          y[4 * blk + 2] = p.z * x[0] + p.w * x[1] + p.x * x[2] - p.y * x[3];
+          y[4 * blk + 3] = p.w * x[0] - p.z * x[1] + p.y * x[2] + p.x * x[3];
+        }
+      }
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        qf[kc][0] = pack_half2(y[4 * kc] * g.q_scale, y[4 * kc + 1] * g.q_scale);
+        qf[kc][1] = pack_half2(y[4 * kc + 2] * g.q_scale, y[4 * kc + 3] * g.q_scale);
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int rc = it.nt * 8 + 2 * tq + c;
+        const int j = rc < a.rows ? rc / g.group : a.T - 1;
+        last_pos[c] = len - a.T + j;
+      }
+    }
+    __syncthreads();  // page ids staged
+
+    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
+    float l_run[2] = {0.f, 0.f};
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    const int tile0 = p0 * tiles_per_page, tile1 = p1 * tiles_per_page;
+    const size_t head_off = (size_t)it.h * g.page_bytes;
+    int tile = tile0 + warp;
+    Raw<BITS> cur, nxt;
+    if (tile < tile1) {
+      const int pi = tile / tiles_per_page - p0, off = (tile % tiles_per_page) * 16;
+      load_tile<BITS>(cur, a.pages + (size_t)page_ids[pi] * g.num_kv_heads * g.page_bytes + head_off, off, P, gq, tq);
+    }
+    for (; tile < tile1; tile += kWarps) {
+      const int tn = tile + kWarps;
+      if (tn < tile1) {
+        const int pi = tn / tiles_per_page - p0, off = (tn % tiles_per_page) * 16;
+        load_tile<BITS>(nxt, a.pages + (size_t)page_ids[pi] * g.num_kv_heads * g.page_bytes + head_off, off, P, gq,
+                        tq);
+      }
+      // ---- scores (base 2) for tokens pos0 + gq and pos0 + gq + 8, query columns 2tq, 2tq+1
+      float s[4];
+      qk_tile<BITS>(s, cur, qf, lane_off, base);
+      const int pos0 = tile * 16;
+      const float nk0 = half_bits_to_float(cur.nk & 0xffffu), nk1 = half_bits_to_float(cur.nk >> 16);
+      const float nv0 = half_bits_to_float(cur.nv & 0xffffu), nv1 = half_bits_to_float(cur.nv >> 16);
+      const int r0 = pos0 + gq, r1 = pos0 + gq + 8;
+      float sc[4];
+      sc[0] = r0 <= last_pos[0] ? s[0] * nk0 : -CUDART_INF_F;
+      sc[1] = r0 <= last_pos[1] ? s[1] * nk0 : -CUDART_INF_F;
+      sc[2] = r1 <= last_pos[0] ? s[2] * nk1 : -CUDART_INF_F;
+      sc[3] = r1 <= last_pos[1] ? s[3] * nk1 : -CUDART_INF_F;
+      float pw[4];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float tmax = fmaxf(sc[c], sc[c + 2]);
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        const float m_new = fmaxf(m_run[c], tmax);
+        const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+        const float alpha = exp2f(m_run[c] - m_use);
+        const float p0v = exp2f(sc[c] - m_use), p1v = exp2f(sc[c + 2] - m_use);
+        l_run[c] = l_run[c] * alpha + p0v + p1v;
+        m_run[c] = m_new;
+        pw[c] = p0v;
+        pw[c + 2] = p1v;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][c] *= alpha;
+          o[mt][c + 2] *= alpha;
+        }
+      }
+      // P' = p * n_v (zero for masked tokens, whatever their stored norm)
+      const float q0 = sc[0] == -CUDART_INF_F ? 0.f : pw[0] * nv0;
+      const float q1 = sc[1] == -CUDART_INF_F ? 0.f : pw[1] * nv0;
+      const float q2 = sc[2] == -CUDART_INF_F ? 0.f : pw[2] * nv1;
+      const float q3 = sc[3] == -CUDART_INF_F ? 0.f : pw[3] * nv1;
+      const uint32_t pb0 = movmatrix_t(pack_half2(q0, q1));
+      const uint32_t pb1 = movmatrix_t(pack_half2(q2, q3));
+      pv_tile<BITS>(o, cur, pb0, pb1, lane_off, base, gq);
+      cur = nxt;
+    }
+
+    // ---- merge the warps' partial states of this item ----
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float l = l_run[c];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      l_run[c] = l;
+    }
+    float* mw = merge + (size_t)warp * 8 * kPartialStride;  // [col][132]: m, l, -, -, o[128]
+    if (gq == 0) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        mw[(2 * tq + c) * kPartialStride + 0] = m_run[c];
+        mw[(2 * tq + c) * kPartialStride + 1] = l_run[c];
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d0 = 16 * gq + 2 * mt;
+      mw[(2 * tq) * kPartialStride + 4 + d0] = o[mt][0];
+      mw[(2 * tq + 1) * kPartialStride + 4 + d0] = o[mt][1];
+      mw[(2 * tq) * kPartialStride + 4 + d0 + 1] = o[mt][2];
+      mw[(2 * tq + 1) * kPartialStride + 4 + d0 + 1] = o[mt][3];
+    }
+    __syncthreads();
+    {
+      const int cols = min(8, a.rows - it.nt * 8);
+      float* dst = a.ws + ((((size_t)it.b * g.num_kv_heads + it.h) * a.n_tiles_n + it.nt) * a.max_splits + it.split) *
+                              8 * kPartialStride;
+      for (int i = threadIdx.x; i < cols * 130; i += kThreads) {
+        const int c = i / 130, e = i % 130;
+        float M = -CUDART_INF_F;
+#pragma unroll 4
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, merge[((size_t)w * 8 + c) * kPartialStride]);
+        float acc = 0.f;
+        if (M != -CUDART_INF_F) {
+          const int src = e == 0 ? -1 : (e == 1 ? 1 : 4 + (e - 2));
+#pragma unroll 4
+          for (int w = 0; w < kWarps; ++w) {
+            const float* mwp = merge + ((size_t)w * 8 + c) * kPartialStride;
+            const float sc = exp2f(mwp[0] - M);
+            if (src >= 0) acc += mwp[src] * sc;
+          }
+        }
+        if (e == 0) dst[c * kPartialStride] = M;
+        else if (e == 1) dst[c * kPartialStride + 1] = acc;
+        else dst[c * kPartialStride + 4 + (e - 2)] = acc;
+      }
+    }
+    __syncthreads();  // merge buffer and page ids are reused by the next item
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Combine: one warp per output row (b, j, query head); lane l owns dims 4l..4l+3.
+//   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  o~ = sum_s O_s 2^(m_s - M) / L,
+//   out = R_v^T o~  (block-local: a Givens pair or a quaternion block per lane).
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(const Geometry g, const AttnArgs a, int nsplit) {
+  const int warp_global = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int total = a.B * a.T * g.num_q_heads;
+  if (warp_global >= total) return;
+  const int head = warp_global % g.num_q_heads;
+  const int j = (warp_global / g.num_q_heads) % a.T;
+  const int b = warp_global / (g.num_q_heads * a.T);
+  const int h = head / g.group;
+  const int row = j * g.group + head % g.group;
+  const int nt = row >> 3, col = row & 7;
+  const int P = g.page_size;
+  int len = a.seq_lens[b];
+  const int cap = a.max_pages * P;
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  const int npages = (len + P - 1) / P;
+  const int ns = min(nsplit, (npages + a.pages_per_split - 1) / a.pages_per_split);
+  const float* base = a.ws + (((size_t)b * g.num_kv_heads + h) * a.n_tiles_n + nt) * a.max_splits * 8 * kPartialStride +
+                      (size_t)col * kPartialStride;
+  float M = -CUDART_INF_F;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, base[(size_t)s * 8 * kPartialStride]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  if (M != -CUDART_INF_F && len >= a.T) {
+    for (int s = 0; s < ns; ++s) {
+      const float* ps = base + (size_t)s * 8 * kPartialStride;
+      const float w = exp2f(ps[0] - M);
+      L += ps[1] * w;
+      const float4 v = *reinterpret_cast<const float4*>(ps + 4 + 4 * lane);
+      acc.x += v.x * w;
+      acc.y += v.y * w;
+      acc.z += v.z * w;
+      acc.w += v.w * w;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float y[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+  const float4 p = __ldg(reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim) + lane);
+  float x[4];
+  if (g.mode == RQ_PLANAR) {
+    x[0] = p.x * y[0] + p.y * y[1];
+    x[1] = -p.y * y[0] + p.x * y[1];
+    x[2] = p.z * y[2] + p.w * y[3];
+    x[3] = -p.w * y[2] + p.z * y[3];
+  } else {  // L(q)^T y
+    const float qa = p.x, qb = p.y, qc = p.z, qd = p.w;
+    x[0] = qa * y[0] + qb * y[1] + qc * y[2] + qd * y[3];
+    x[1] = -qb * y[0] + qa * y[1] + qd * y[2] - qc * y[3];
+    x[2] = -qc * y[0] - qd * y[1] + qa * y[2] + qb * y[3];
+    x[3] = -qd * y[0] + qc * y[1] - qb * y[2] + qa * y[3];
+  }
+  __half2* out = reinterpret_cast<__half2*>(reinterpret_cast<__half*>(a.out) +
+                                            (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim + 4 * lane);
+  out[0] = __floats2half2_rn(x[0], x[1]);
+  out[1] = __floats2half2_rn(x[2], x[3]);
+}
+
+}  // namespace
+
+size_t attention_smem_bytes() { return kSmemBytes; }
+
+cudaError_t attention_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(attn_splitk_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_splitk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+}
+
+cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+  if (a.B <= 0) return cudaSuccess;
+  const int nsplit = (a.max_pages + a.pages_per_split - 1) / a.pages_per_split;
+  const long long n_items = (long long)a.B * g.num_kv_heads * a.n_tiles_n * nsplit;
+  if (n_items > 0) {
+    const int grid = (int)(n_items < num_ctas ? n_items : num_ctas);
+    if (g.bits == 4)
+      attn_splitk_kernel<4><<<grid, kThreads, kSmemBytes, stream>>>(g, a, nsplit, (int)n_items);
+    else
+      attn_splitk_kernel<3><<<grid, kThreads, kSmemBytes, stream>>>(g, a, nsplit, (int)n_items);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const long long rows = (long long)a.B * a.T * g.num_q_heads;
+  attn_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(g, a, nsplit);
+  return cudaGetLastError();
+}
+
+}  // namespace rq

@@ -1,0 +1,58 @@
+// Internal interface between the host API (rq_api.cpp) and the sm_103a kernels (*.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rq {
+
+constexpr int kHeadDim = 128;
+
+// Device-side copy of what every kernel needs to know about a context.
+struct Geometry {
+  int num_q_heads;
+  int num_kv_heads;
+  int group;           // Hq / Hkv
+  int bits;
+  int mode;            // 0 planar, 1 iso
+  int page_size;
+  int num_pages;
+  int vec_bytes;       // head_dim * bits / 8
+  int page_bytes;      // page_size * (2 * vec_bytes + 4)
+  float q_scale;       // sm_scale * log2(e): scores are kept in base 2
+  const float* rot_k;  // device [Hkv][128]
+  const float* rot_v;  // device [Hkv][128]
+  const float* centroids;   // device [2^bits]
+  const float* boundaries;  // device [2^bits - 1]
+};
+
+// One attention launch (decode is T = 1).
+struct AttnArgs {
+  const void* q;             // fp16 [B][T][Hq][128]
+  const uint8_t* pages;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  int B;
+  int T;
+  void* out;                 // fp16 [B][T][Hq][128]
+  int32_t* status;           // nullable
+  float* ws;                 // split-K partials
+  int rows;                  // T * group: query rows per kv head
+  int n_tiles_n;             // ceil(rows / 8)
+  int pages_per_split;
+  int max_splits;            // splits per (b, kv head) the workspace has room for
+};
+
+constexpr int kPartialStride = 132;   // floats per partial row: m, l, pad, pad, o[128]
+
+cudaError_t launch_append(const Geometry& g, const void* k, const void* v, const int32_t* slots,
+                          int n, uint8_t* pages, int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream);
+
+// Dynamic shared memory the attention kernel needs (set as the kernel's maximum once).
+size_t attention_smem_bytes();
+cudaError_t attention_prepare();
+
+}  // namespace rq

@@ -1,0 +1,186 @@
+"""GPU parity on small cases: the CUDA library (through the C ABI) against the fp64 oracle on
+the same seeded inputs.  Codes and norms bit-exact (near-boundary exceptions counted and
+bounded); attention within 2e-3 + 1e-3|ref| of the oracle's fp64 attention over the
+dequantised cache."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from rotation_quantized_kv_rq_gb300 import rq, synth
+from tests import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+PLANAR, ISO = synth.PLANAR, synth.ISO
+
+
+def make_case(mode, bits, hq, hkv, P, lens, T=1, seed=7, zero_tokens=(), permuted=True):
+    lens = np.asarray(lens, np.int32)
+    spec = synth.Spec("case", mode, bits, len(lens), int(max(lens.max(), 1)), hq, hkv, P, permuted=permuted,
+                      query_tokens=T, seed=seed)
+    rng = np.random.default_rng(seed)
+    rk = synth.rotation_params(mode, hkv, rng)
+    rv = synth.rotation_params(mode, hkv, rng)
+    bt, total = synth.block_table(spec, lens, extra_pages=3)
+    wl = synth.Workload(spec, rk, rv, lens, bt, total)
+    kv = []
+    for b, L in enumerate(lens):
+        if L == 0:
+            kv.append((np.zeros((0, hkv, 128), np.float16), np.zeros((0, hkv, 128), np.float16)))
+            continue
+        k, v = synth.kv_tokens(spec, b, 0, int(L))
+        k, v = k.numpy(), v.numpy()
+        for (zb, zt) in zero_tokens:
+            if zb == b and zt < L:
+                k[zt] = 0
+                v[zt] = 0
+        kv.append((k, v))
+    q = synth.queries(spec).numpy()
+    return wl, kv, q
+
+
+def run_both(wl, kv, q):
+    s = wl.spec
+    oc = PT.oracle_cache(wl)
+    margins, tokens = {}, []
+    flat_k, flat_v, flat_slots = [], [], []
+    ti = 0
+    for b, (k, v) in enumerate(kv):
+        L = k.shape[0]
+        if L == 0:
+            continue
+        slots = PT.positions_slots(wl, b, 0, L)
+        mk, mv = oc.append(k, v, slots, with_margins=True)
+        for t in range(L):
+            margins[ti + t] = (mk[t], mv[t])
+            for h in range(s.num_kv_heads):
+                tokens.append((int(slots[t]) // s.page_size, int(slots[t]) % s.page_size, h, ti + t))
+        flat_k.append(k)
+        flat_v.append(v)
+        flat_slots.append(slots)
+        ti += L
+    T = s.query_tokens
+    ref = oc.attention(q, wl.block_table, wl.seq_lens, T=T)
+
+    cache = rq.KVCache(s.mode, s.bits, s.num_q_heads, s.num_kv_heads, s.page_size, wl.num_pages, wl.rot_k, wl.rot_v,
+                       max_batch=s.batch, max_query_tokens=T, max_pages_per_seq=wl.block_table.shape[1])
+    K = np.concatenate(flat_k)
+    V = np.concatenate(flat_v)
+    cache.append(PT.to_dev(K), PT.to_dev(V), PT.to_dev(np.concatenate(flat_slots)))
+    bt, sl = PT.to_dev(wl.block_table), PT.to_dev(wl.seq_lens)
+    qd = PT.to_dev(q)
+    if T == 1:
+        out = cache.decode(qd[:, 0].contiguous(), bt, sl).unsqueeze(1)
+    else:
+        out = cache.verify(qd, bt, sl)
+    torch.cuda.synchronize()
+    gpu_pages = cache.pages.cpu().numpy()
+    status = int(cache.status.item())
+    out = out.cpu().numpy()
+
+    # decode alone, over the oracle's own packed bytes
+    cache.pages.copy_(torch.from_numpy(oc.pages.reshape(cache.pages.shape)))
+    out2 = (cache.decode(qd[:, 0].contiguous(), bt, sl).unsqueeze(1) if T == 1 else cache.verify(qd, bt, sl))
+    out2 = out2.cpu().numpy()
+    cache.close()
+    return dict(oc=oc, ref=ref, out=out, out_on_oracle_pages=out2, gpu_pages=gpu_pages, tokens=tokens,
+                margins=margins, inputs=(K, V), status=status)
+
+
+CASES = [
+    # mode, bits, Hq, Hkv, P, lens, T
+    (PLANAR, 4, 32, 8, 16, [1024], 1),
+    (PLANAR, 3, 32, 8, 16, [37, 16, 1, 160, 0, 15, 17, 33], 1),
+    (ISO, 4, 64, 8, 16, [300, 511, 129, 2], 1),
+    (ISO, 3, 32, 8, 16, [70, 100, 6, 7], 6),
+    (PLANAR, 3, 64, 8, 64, [200, 64, 65, 63], 1),
+    (ISO, 4, 16, 2, 32, [95, 1], 1),
+    (PLANAR, 4, 8, 8, 16, [40, 41], 1),
+    (ISO, 3, 24, 2, 16, [90, 33], 1),
+    (PLANAR, 4, 12, 4, 16, [48, 20], 3),
+    (ISO, 4, 32, 8, 16, [5000], 1),
+    (PLANAR, 3, 32, 8, 128, [700, 129], 2),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{'iso' if c[0] else 'planar'}{c[1]}_G{c[2] // c[3]}_P{c[4]}_T{c[6]}_n{len(c[5])}")
+def test_append_and_attention_match_oracle(case):
+    mode, bits, hq, hkv, P, lens, T = case
+    wl, kv, q = make_case(mode, bits, hq, hkv, P, lens, T, zero_tokens=[(0, 3)])
+    r = run_both(wl, kv, q)
+    assert r["status"] == 0
+    compared, in_band = PT.compare_chunks(r["gpu_pages"], r["oc"], r["tokens"], r["margins"], r["inputs"])
+    assert in_band <= max(2, compared // 100000), (in_band, compared)
+    PT.assert_close(r["out_on_oracle_pages"], r["ref"], "attention over the oracle's pages")
+    PT.assert_close(r["out"], r["ref"], "append + attention")
+
+
+def test_zero_length_sequences_give_zeros():
+    wl, kv, q = make_case(PLANAR, 4, 32, 8, 16, [0, 50, 0])
+    r = run_both(wl, kv, q)
+    assert not r["out"][0].any() and not r["out"][2].any()
+    PT.assert_close(r["out"], r["ref"])
+
+
+def test_status_flags_and_clamping():
+    """Out-of-range inputs set status bits instead of faulting; other sequences are unaffected."""
+    wl, kv, q = make_case(ISO, 3, 32, 8, 16, [40, 40])
+    s = wl.spec
+    cache = rq.KVCache(s.mode, s.bits, s.num_q_heads, s.num_kv_heads, s.page_size, wl.num_pages, wl.rot_k,
+                       wl.rot_v, max_batch=2, max_pages_per_seq=wl.block_table.shape[1])
+    k, v = kv[0]
+    bad_slot = np.array([wl.num_pages * s.page_size + 5], np.int32)
+    cache.append(PT.to_dev(k[:1]), PT.to_dev(v[:1]), PT.to_dev(bad_slot))
+    torch.cuda.synchronize()
+    assert cache.status.item() & rq.RQ_STATUS_BAD_SLOT
+    assert not cache.pages.any()                      # nothing written
+    cache.status.zero_()
+    skip = np.array([-1], np.int32)
+    cache.append(PT.to_dev(k[:1]), PT.to_dev(v[:1]), PT.to_dev(skip))
+    torch.cuda.synchronize()
+    assert cache.status.item() == 0 and not cache.pages.any()
+    bt = wl.block_table.copy()
+    bt[1, 1] = wl.num_pages + 100                     # bad page id in sequence 1
+    out = cache.decode(PT.to_dev(q[:, 0]), PT.to_dev(bt), PT.to_dev(wl.seq_lens))
+    torch.cuda.synchronize()
+    assert cache.status.item() & rq.RQ_STATUS_BAD_PAGE
+    cache.status.zero_()
+    lens = wl.seq_lens.copy()
+    lens[0] = bt.shape[1] * s.page_size + 1           # longer than its block-table row
+    cache.decode(PT.to_dev(q[:, 0]), PT.to_dev(wl.block_table), PT.to_dev(lens), out=out)
+    torch.cuda.synchronize()
+    assert cache.status.item() & rq.RQ_STATUS_BAD_LEN
+    cache.close()
+
+
+def test_capacity_and_argument_errors():
+    wl, kv, q = make_case(PLANAR, 4, 32, 8, 16, [20])
+    s = wl.spec
+    cache = rq.KVCache(s.mode, s.bits, s.num_q_heads, s.num_kv_heads, s.page_size, wl.num_pages, wl.rot_k,
+                       wl.rot_v, max_batch=1, max_pages_per_seq=wl.block_table.shape[1])
+    q2 = PT.to_dev(np.concatenate([q, q])[:, 0])
+    bt2 = PT.to_dev(np.concatenate([wl.block_table] * 2))
+    with pytest.raises(rq.RQError) as e:
+        cache.decode(q2, bt2, PT.to_dev(np.array([20, 20], np.int32)))
+    assert e.value.code == rq.RQ_ERR_CAPACITY
+    with pytest.raises(rq.RQError) as e:
+        cache.verify(PT.to_dev(np.repeat(q, 2, axis=1)), PT.to_dev(wl.block_table), PT.to_dev(wl.seq_lens))
+    assert e.value.code == rq.RQ_ERR_CAPACITY
+    cache.close()
+
+
+def test_repeated_calls_are_deterministic():
+    """Relaunching on the same inputs gives bitwise the same outputs (no races in the merges)."""
+    wl, kv, q = make_case(ISO, 4, 64, 8, 16, [3000, 1700, 20])
+    s = wl.spec
+    cache = rq.KVCache(s.mode, s.bits, s.num_q_heads, s.num_kv_heads, s.page_size, wl.num_pages, wl.rot_k,
+                       wl.rot_v, max_batch=3, max_pages_per_seq=wl.block_table.shape[1])
+    for b, (k, v) in enumerate(kv):
+        cache.append(PT.to_dev(k), PT.to_dev(v), PT.to_dev(PT.positions_slots(wl, b, 0, k.shape[0])))
+    qd, bt, sl = PT.to_dev(q[:, 0]), PT.to_dev(wl.block_table), PT.to_dev(wl.seq_lens)
+    first = cache.decode(qd, bt, sl).clone()
+    for _ in range(20):
+        again = cache.decode(qd, bt, sl)
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+    cache.close()
