@@ -1,0 +1,462 @@
+"""Benchmark of the rotation-quantized KV cache hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg1] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: the quantize-append of the step's
+new tokens, then split-K decode (or chain-verify) attention over the packed cache and the
+log-sum-exp combine.  Inputs are synthetic and seeded (rotation_quantized_kv_rq_gb300.synth);
+the packed cache is built before timing and stays resident in HBM.
+
+Default workload cfg1: rq3_planar, 16 sequences x 8192 context, 32 q / 8 kv heads, page 16,
+permuted block table, per-token K offset; each step appends 1 token per sequence and
+decodes.  Its packed cache (105 MB) fits in the 129 MB L2, so L2 is flushed (a 512 MB write)
+before every step, outside the per-step CUDA events.
+
+Prints one JSON line (rank 0).  `value` = query tokens per second over all ranks (weak
+scaling: every rank runs the full workload on its own GPU); `roofline` is the split-K
+attention kernel's achieved packed-KV bandwidth against the measured HBM copy peak;
+`cpu_baseline` / `--impl reference` time the fp64 CPU oracle on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rotation_quantized_kv_rq_gb300 import rq, synth  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+DESCRIPTIONS = {
+    "cfg0": "rq4_planar decode, 1 x 1024 ctx, 32 q / 8 kv heads, head_dim 128, page 16",
+    "cfg1": "rq3_planar decode, 16 x 8192 ctx, 32 q / 8 kv heads, head_dim 128, page 16, permuted pages, "
+            "append 1 token per sequence + decode",
+    "cfg2": "rq4_iso decode, 32 sequences x U[1024, 32768] ctx, 64 q / 8 kv heads, head_dim 128, page 16",
+    "cfg2_32k": "rq4_iso decode, 32 x 32768 ctx, 64 q / 8 kv heads, head_dim 128, page 16",
+    "cfg3": "rq3_iso chain verify, 8 x 16384 ctx + 6 drafts, 32 q / 8 kv heads, head_dim 128, page 16, "
+            "append 6 drafts + verify",
+    "cfg3_prefill": "rq3_iso quantize-append of 65536 tokens x 8 kv heads (K and V), page 16",
+    "cfg4": "rq3_planar decode, 64 x 65536 ctx, 64 q / 8 kv heads, head_dim 128, page 64",
+}
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing (replicas: no collective on the data path)
+# ---------------------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------
+# workload setup
+# ---------------------------------------------------------------------------------------
+class Bench:
+    def __init__(self, name, device):
+        self.name = name
+        self.device = device
+        self.prefill_only = name == "cfg3_prefill"
+        spec = synth.SPECS["cfg3" if self.prefill_only else name]
+        if self.prefill_only:
+            spec = synth.scaled(spec, batch=1, ctx=synth.PREFILL_TOKENS, query_tokens=1, appended=synth.PREFILL_TOKENS)
+        self.spec = spec
+        self.wl = synth.workload(spec)
+        s, wl = spec, self.wl
+        self.cache = rq.KVCache(s.mode, s.bits, s.num_q_heads, s.num_kv_heads, s.page_size, wl.num_pages, wl.rot_k,
+                                wl.rot_v, max_batch=s.batch, max_query_tokens=s.query_tokens,
+                                max_pages_per_seq=wl.block_table.shape[1], device=device)
+        self.bt = torch.from_numpy(wl.block_table).to(device)
+        self.lens = torch.from_numpy(wl.seq_lens).to(device)
+        # prefill everything except the step's own tokens
+        new_k, new_v, new_slots = [], [], []
+        for b in range(s.batch):
+            L = int(wl.seq_lens[b])
+            keep = L - s.appended
+            chunk = 16384
+            for st in range(0, keep, chunk):
+                cnt = min(chunk, keep - st)
+                k, v = synth.kv_tokens(s, b, st, cnt, device=device)
+                slots = torch.from_numpy(synth.slots_for(wl.block_table, b, np.arange(st, st + cnt), s.page_size))
+                self.cache.append(k, v, slots.to(device))
+            if s.appended:
+                k, v = synth.kv_tokens(s, b, keep, s.appended, device=device)
+                new_k.append(k)
+                new_v.append(v)
+                new_slots.append(synth.slots_for(wl.block_table, b, np.arange(keep, L), s.page_size))
+        if s.appended:
+            self.k_new = torch.cat(new_k).contiguous()
+            self.v_new = torch.cat(new_v).contiguous()
+            self.slots_new = torch.from_numpy(np.concatenate(new_slots)).to(device)
+        else:
+            self.k_new = self.v_new = self.slots_new = None
+        self.q = synth.queries(s, device=device).contiguous()
+        if s.query_tokens == 1:
+            self.q = self.q[:, 0].contiguous()
+        self.out = torch.empty_like(self.q)
+        torch.cuda.synchronize(device)
+        assert int(self.cache.status.item()) == 0, "range fault while building the cache"
+
+    def step(self):
+        s = self.spec
+        if self.k_new is not None:
+            self.cache.append(self.k_new, self.v_new, self.slots_new)
+        if self.prefill_only:
+            return
+        if s.query_tokens == 1:
+            self.cache.decode(self.q, self.bt, self.lens, out=self.out)
+        else:
+            self.cache.verify(self.q, self.bt, self.lens, out=self.out)
+
+    def launches_per_step(self):
+        n = 1 if self.k_new is not None else 0
+        return n if self.prefill_only else n + 2
+
+    def tokens_per_step(self):
+        if self.prefill_only:
+            return self.spec.ctx
+        return self.spec.batch * self.spec.query_tokens
+
+    def packed_bytes(self):
+        s = self.spec
+        per = 32 * s.bits + 4
+        return int(self.wl.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * per
+
+    def attention_algorithmic_bytes(self):
+        """Bytes the split-K kernel must move per launch: the packed cache of every attended
+        token-head, the queries, and the block-table entries it reads."""
+        s = self.spec
+        pages = int(((self.wl.seq_lens + s.page_size - 1) // s.page_size).sum())
+        return self.packed_bytes() + s.batch * s.query_tokens * s.num_q_heads * 256 + pages * 4
+
+    def append_algorithmic_bytes(self):
+        n = int(self.slots_new.numel()) if self.slots_new is not None else 0
+        per_vec = 256 + 16 * self.spec.bits + 2
+        return n * self.spec.num_kv_heads * 2 * per_vec + n * 4
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+CLOCK_Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+           "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+           "clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic(kernel_file, workload):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    src = os.path.join(ROOT, "rotation_quantized_kv_rq_gb300", "csrc", kernel_file)
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if d.get("source_sha256") != sha:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------------------
+# the oracle on the host (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------------------
+def oracle_step_rate(name, budget_s=10.0, max_seqs=None):
+    """Times the CPU oracle doing this workload's step on a sample of sequences: its own
+    packed cache is built first (untimed), then append + attention are timed per sequence
+    until the budget is spent.  Returns (tokens/s, description, seconds)."""
+    from oracle import oracle as O
+    prefill_only = name == "cfg3_prefill"
+    spec = synth.SPECS["cfg3" if prefill_only else name]
+    if prefill_only:
+        spec = synth.scaled(spec, batch=1, ctx=synth.PREFILL_TOKENS, query_tokens=1, appended=synth.PREFILL_TOKENS)
+    wl = synth.workload(spec)
+    q = synth.queries(spec).numpy()
+    timed, toks, seqs = 0.0, 0, 0
+    if prefill_only:
+        oc = O.Cache(spec.mode, spec.bits, spec.num_q_heads, spec.num_kv_heads, spec.page_size, wl.num_pages,
+                     wl.rot_k, wl.rot_v)
+        n = 0
+        while timed < budget_s and n < spec.ctx:
+            cnt = min(1024, spec.ctx - n)
+            k, v = synth.kv_tokens(spec, 0, n, cnt)
+            slots = synth.slots_for(wl.block_table, 0, np.arange(n, n + cnt), spec.page_size)
+            t0 = time.perf_counter()
+            oc.append(k.numpy(), v.numpy(), slots)
+            timed += time.perf_counter() - t0
+            n += cnt
+        return n / timed, f"quantize-append of the first {n} of {spec.ctx} tokens x {spec.num_kv_heads} kv heads", timed
+    for b in range(spec.batch):
+        if timed >= budget_s or (max_seqs and seqs >= max_seqs):
+            break
+        L = int(wl.seq_lens[b])
+        P = spec.page_size
+        npg = (L + P - 1) // P
+        bt = np.arange(npg, dtype=np.int32)[None, :]   # the sample's own compact pool
+        oc = O.Cache(spec.mode, spec.bits, spec.num_q_heads, spec.num_kv_heads, P, npg, wl.rot_k, wl.rot_v)
+        keep = L - spec.appended
+        for st in range(0, keep, 8192):
+            cnt = min(8192, keep - st)
+            k, v = synth.kv_tokens(spec, b, st, cnt)
+            oc.append(k.numpy(), v.numpy(), np.arange(st, st + cnt, dtype=np.int32))
+        if spec.appended:
+            k_new, v_new = synth.kv_tokens(spec, b, keep, spec.appended)
+        t0 = time.perf_counter()
+        if spec.appended:
+            oc.append(k_new.numpy(), v_new.numpy(), np.arange(keep, L, dtype=np.int32))
+        oc.attention(q[b:b + 1] if spec.query_tokens > 1 else q[b:b + 1, :1], bt, np.array([L], np.int32),
+                     T=spec.query_tokens)
+        timed += time.perf_counter() - t0
+        toks += spec.query_tokens
+        seqs += 1
+    return toks / timed, f"{seqs} of {spec.batch} sequences (full context each), one step each", timed
+
+
+# ---------------------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    rate, sample, secs = oracle_step_rate(args.workload, budget_s=args.ref_budget)
+    spec_tokens = synth.SPECS.get(args.workload, synth.SPECS["cfg3"])
+    line = {
+        "impl": "reference", "metric": "decode-attn tokens/s", "value": rate, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "the reference arm is the plain fp64 CPU oracle written from the pages (no implementation of "
+                "the method exists on the pages); it times the oracle on one host core",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    bench = Bench(args.workload, device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        bench.step()
+    torch.cuda.synchronize(device)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with sampler:
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            flush.fill_(float(i))
+            if not bench.prefill_only:
+                rq.rq_set_profile_events(bench.cache.ctx, kev[i][0], kev[i][1])
+            ev[i][0].record(stream)
+            bench.step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(device)
+        t_wall1 = time.perf_counter()
+        if not bench.prefill_only:
+            rq.rq_set_profile_events(bench.cache.ctx)
+        barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev] if not bench.prefill_only else step_ms
+    ms = sum(step_ms) / K
+    ms = max_over_ranks(ms, world)
+    tokens = bench.tokens_per_step()
+    value = world * tokens / (ms * 1e-3)
+    assert int(bench.cache.status.item()) == 0
+
+    # ---- end to end through the public API: pinned host inputs in, result back to the host
+    h_q = bench.q.cpu().pin_memory()
+    h_out = torch.empty_like(h_q, device="cpu").pin_memory()
+    d_q = torch.empty_like(bench.q)
+    h_k = bench.k_new.cpu().pin_memory() if bench.k_new is not None else None
+    h_v = bench.v_new.cpu().pin_memory() if bench.k_new is not None else None
+    h_s = bench.slots_new.cpu().pin_memory() if bench.k_new is not None else None
+    d_k = torch.empty_like(bench.k_new) if h_k is not None else None
+    d_v = torch.empty_like(bench.v_new) if h_k is not None else None
+    d_s = torch.empty_like(bench.slots_new) if h_k is not None else None
+    h2d = h_q.numel() * 2 + (h_k.numel() * 2 * 2 + h_s.numel() * 4 if h_k is not None else 0)
+    d2h = h_out.numel() * 2
+    e2e_times = []
+    n_e2e = max(3, min(K, 200))
+    for i in range(n_e2e + 2):
+        flush.fill_(float(i))
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        if h_k is not None:
+            d_k.copy_(h_k, non_blocking=True)
+            d_v.copy_(h_v, non_blocking=True)
+            d_s.copy_(h_s, non_blocking=True)
+            bench.cache.append(d_k, d_v, d_s)
+        if not bench.prefill_only:
+            d_q.copy_(h_q, non_blocking=True)
+            if bench.spec.query_tokens == 1:
+                bench.cache.decode(d_q, bench.bt, bench.lens, out=bench.out)
+            else:
+                bench.cache.verify(d_q, bench.bt, bench.lens, out=bench.out)
+            h_out.copy_(bench.out, non_blocking=True)
+        stream.synchronize()
+        if i >= 2:
+            e2e_times.append(time.perf_counter() - t0)
+    e2e_s = max_over_ranks(statistics.median(e2e_times), world)
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    kms = statistics.mean(kern_ms)
+    if bench.prefill_only:
+        alg = bench.append_algorithmic_bytes()
+        kname = "append_kernel"
+    else:
+        alg = bench.attention_algorithmic_bytes()
+        kname = "attn_splitk_kernel"
+    achieved = alg / (kms * 1e-3) / 1e9
+    traffic = committed_traffic("rq_attention.cu" if not bench.prefill_only else "rq_append.cu", args.workload)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "kernel": kname, "algorithmic_bytes_per_launch": alg,
+            "kernel_ms_mean": kms, "kernel_ms_median": statistics.median(kern_ms),
+            "peak_source": f"{peak_kind} hbm_gbs", "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, sample, secs = oracle_step_rate(args.workload, budget_s=args.cpu_budget)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+               "seconds": round(secs, 2)}
+    s = bench.spec
+    line = {
+        "metric": "decode-attn tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": f"u{s.bits} codes, f16 mma, f32 accumulate", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}", "batch": s.batch,
+                   "ctx": int(s.ctx), "query_tokens": s.query_tokens, "bits": s.bits,
+                   "mode": "planar" if s.mode == synth.PLANAR else "iso", "page_size": s.page_size,
+                   "packed_kv_bytes": bench.packed_bytes(),
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB write) outside the per-step events",
+                   "parallelism": f"replicas x{world}"},
+        "packed_kv_gbs": bench.packed_bytes() / (ms * 1e-3) / 1e9,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": bench.launches_per_step() * K,
+        "clocks": sampler.summary(),
+        "wall_s_timed_region": t_wall1 - t_wall0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="cfg1", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -154,6 +154,11 @@ int rq_verify_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
                         const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
                         void *out, int32_t *d_status, void *stream);
 
+/* Diagnostics.  While set, every attention call records ev_start on its stream just before
+   its split-K kernel and ev_end just after it (both cudaEvent_t created by the caller, who
+   reads the elapsed time); NULL, NULL stops recording.  Costs nothing when unset. */
+int rq_set_profile_events(rq_ctx *ctx, void *ev_start, void *ev_end);
+
 /* Static English text for a return code (never NULL). */
 const char *rq_status_string(int status);
 

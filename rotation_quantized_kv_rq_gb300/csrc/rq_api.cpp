@@ -21,6 +21,8 @@ struct rq_ctx {
   size_t ws_floats;
   int max_splits;
   int max_n_tiles;        // ceil(max_query_tokens * group / 8)
+  cudaEvent_t prof_start; // optional diagnostics events (caller-owned)
+  cudaEvent_t prof_end;
   float centroids[256];
   float boundaries[255];
 };
@@ -224,6 +226,13 @@ void rq_free(rq_ctx* ctx) {
   delete ctx;
 }
 
+int rq_set_profile_events(rq_ctx* ctx, void* ev_start, void* ev_end) {
+  if (!ctx || (!ev_start) != (!ev_end)) return RQ_ERR_INVALID;
+  ctx->prof_start = (cudaEvent_t)ev_start;
+  ctx->prof_end = (cudaEvent_t)ev_end;
+  return RQ_OK;
+}
+
 size_t rq_page_bytes(const rq_ctx* ctx) { return ctx ? (size_t)ctx->g.page_bytes : 0; }
 
 int rq_get_codebook(const rq_ctx* ctx, float* centroids, float* boundaries) {
@@ -286,7 +295,8 @@ int rq_verify_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages,
   if (pps > kMaxSplitPages) pps = kMaxSplitPages;
   if ((max_pages + pps - 1) / pps > ctx->max_splits) return RQ_ERR_CAPACITY;
   a.pages_per_split = (int)pps;
-  return to_status(rq::launch_attention(ctx->g, a, ctx->num_sms, (cudaStream_t)stream));
+  return to_status(
+      rq::launch_attention(ctx->g, a, ctx->num_sms, (cudaStream_t)stream, ctx->prof_start, ctx->prof_end));
 }
 
 int rq_decode_attention(rq_ctx* ctx, const void* q, const void* kv_pages, const int32_t* block_table, int max_pages,

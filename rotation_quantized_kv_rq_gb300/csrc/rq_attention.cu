@@ -625,18 +625,21 @@ cudaError_t attention_prepare() {
   return cudaFuncSetAttribute(attn_splitk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
 }
 
-cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream,
+                             cudaEvent_t ev_start, cudaEvent_t ev_end) {
   if (a.B <= 0) return cudaSuccess;
   const int nsplit = (a.max_pages + a.pages_per_split - 1) / a.pages_per_split;
   const long long n_items = (long long)a.B * g.num_kv_heads * a.n_tiles_n * nsplit;
   if (n_items > 0) {
     const int grid = (int)(n_items < num_ctas ? n_items : num_ctas);
+    if (ev_start) cudaEventRecord(ev_start, stream);
     if (g.bits == 4)
       attn_splitk_kernel<4><<<grid, kThreads, kSmemBytes, stream>>>(g, a, nsplit, (int)n_items);
     else
       attn_splitk_kernel<3><<<grid, kThreads, kSmemBytes, stream>>>(g, a, nsplit, (int)n_items);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (ev_end) cudaEventRecord(ev_end, stream);
   }
   const long long rows = (long long)a.B * a.T * g.num_q_heads;
   attn_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(g, a, nsplit);

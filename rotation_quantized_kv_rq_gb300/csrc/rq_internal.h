@@ -49,7 +49,8 @@ constexpr int kPartialStride = 132;   // floats per partial row: m, l, pad, pad,
 cudaError_t launch_append(const Geometry& g, const void* k, const void* v, const int32_t* slots,
                           int n, uint8_t* pages, int32_t* status, cudaStream_t stream);
 
-cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream);
+cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream,
+                             cudaEvent_t ev_start = nullptr, cudaEvent_t ev_end = nullptr);
 
 // Dynamic shared memory the attention kernel needs (set as the kernel's maximum once).
 size_t attention_smem_bytes();

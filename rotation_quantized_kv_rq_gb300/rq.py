@@ -23,7 +23,8 @@ RQ_PLANAR, RQ_ISO = 0, 1
 HEAD_DIM = 128
 
 EXPORTS = ["rq_create", "rq_free", "rq_page_bytes", "rq_lloyd_max_codebook", "rq_get_codebook",
-           "rq_quantize_append", "rq_decode_attention", "rq_verify_attention", "rq_status_string"]
+           "rq_quantize_append", "rq_decode_attention", "rq_verify_attention", "rq_set_profile_events",
+           "rq_status_string"]
 
 
 class RQError(RuntimeError):
@@ -70,6 +71,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             L.rq_verify_attention.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, vp,
                                               vp]
             L.rq_verify_attention.restype = ctypes.c_int
+            L.rq_set_profile_events.argtypes = [vp, vp, vp]
+            L.rq_set_profile_events.restype = ctypes.c_int
             L.rq_status_string.argtypes = [ctypes.c_int]
             L.rq_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -172,6 +175,13 @@ def rq_verify_attention(ctx, q: torch.Tensor, kv_pages: torch.Tensor, block_tabl
            lib().rq_verify_attention(ctx, _ptr(q), T, _ptr(kv_pages), _ptr(block_table), block_table.shape[-1],
                                      _ptr(seq_lens), B, _ptr(out), _ptr(status), _stream(stream, q.device)))
     return out
+
+
+def rq_set_profile_events(ctx, ev_start=None, ev_end=None) -> None:
+    """Record torch.cuda.Event pairs around the split-K attention kernel of later calls."""
+    a = ctypes.c_void_p(ev_start.cuda_event) if ev_start is not None else None
+    b = ctypes.c_void_p(ev_end.cuda_event) if ev_end is not None else None
+    _check("rq_set_profile_events", lib().rq_set_profile_events(ctx, a, b))
 
 
 class KVCache:

@@ -1,0 +1,127 @@
+"""Parity at the five workloads' full sizes, in the launch configuration bench.py times.
+
+For each workload the whole packed cache is built on the GPU, one bench step runs (append of
+the step's tokens + attention), and sampled sequences are re-encoded by the CPU oracle from
+the same inputs: their packed bytes must match (near-boundary codes excepted and bounded), and
+their attention outputs must agree within 2e-3 + 1e-3|ref|.  Fidelity against attention over
+the unquantised fp16 cache is reported as cosine similarity."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+from oracle import oracle as O
+from rotation_quantized_kv_rq_gb300 import synth
+from tests import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+
+def _sequence_inputs(spec, b, L, device):
+    ks, vs = [], []
+    for st in range(0, L, 16384):
+        k, v = synth.kv_tokens(spec, b, st, min(16384, L - st), device=device)
+        ks.append(k.cpu())
+        vs.append(v.cpu())
+    return torch.cat(ks).numpy(), torch.cat(vs).numpy()
+
+
+def _check_sequence(bn, b, out_gpu):
+    spec, wl = bn.spec, bn.wl
+    L = int(wl.seq_lens[b])
+    P = spec.page_size
+    npg = (L + P - 1) // P
+    k, v = _sequence_inputs(spec, b, L, bn.device)
+    oc = O.Cache(spec.mode, spec.bits, spec.num_q_heads, spec.num_kv_heads, P, npg, wl.rot_k, wl.rot_v)
+    oc.append(k, v, np.arange(L, dtype=np.int32))
+    # packed bytes of the sequence's pages, in order, against the oracle's compact pool
+    pages = torch.from_numpy(wl.block_table[b, :npg].astype(np.int64)).to(bn.device)
+    gpu = bn.cache.pages.index_select(0, pages).cpu().numpy()        # [npg][Hkv][page_bytes]
+    ora = oc.pages.reshape(npg, spec.num_kv_heads, -1)
+    # only the bytes of valid tokens are defined: mask the tail of the last page
+    vb = 16 * spec.bits
+    diff = np.argwhere(gpu != ora)
+    in_band = 0
+    for (pg, h, byte) in diff:
+        if byte < 2 * P * vb:
+            kv, rem = divmod(int(byte), P * vb)
+            off = rem // vb
+            norm = False
+        else:
+            kv, rem = divmod(int(byte) - 2 * P * vb, 2 * P)
+            off = rem // 2
+            norm = True
+        t = pg * P + off
+        if t >= L:
+            continue
+        x = (k if kv == 0 else v)[t, h]
+        if norm:
+            exact = float(np.linalg.norm(x.astype(np.float64)))
+            gn = int(gpu[pg, h, 2 * P * vb + kv * 2 * P + 2 * off]) | int(gpu[pg, h, 2 * P * vb + kv * 2 * P + 2 * off + 1]) << 8
+            on = int(ora[pg, h, 2 * P * vb + kv * 2 * P + 2 * off]) | int(ora[pg, h, 2 * P * vb + kv * 2 * P + 2 * off + 1]) << 8
+            mid = 0.5 * (O.half_to_double(gn) + O.half_to_double(on))
+            assert abs(exact - mid) <= 1e-6 * exact, ("norm", b, t, h, kv)
+            in_band += 1
+            continue
+        rot = (wl.rot_k if kv == 0 else wl.rot_v)[h]
+        codes, _, margin = O.encode(spec.mode, spec.bits, rot, oc.boundaries, x)
+        lo = (kv * P + off) * vb
+        gc = O.unpack(spec.bits, gpu[pg, h, lo:lo + vb])
+        bad = np.nonzero(gc != codes)[0]
+        assert np.all(margin[bad] < PT.BOUNDARY_BAND), ("code", b, t, h, kv, bad, margin[bad])
+        in_band += len(bad)
+    total_codes = L * spec.num_kv_heads * 2 * 128
+    assert in_band <= max(4, total_codes // 200000), (in_band, total_codes)
+
+    q = bn.q.cpu().numpy()
+    qb = q[b:b + 1] if spec.query_tokens > 1 else q[b:b + 1, None]
+    ref = oc.attention(qb, np.arange(npg, dtype=np.int32)[None], np.array([L], np.int32), T=spec.query_tokens)
+    got = out_gpu[b:b + 1] if spec.query_tokens > 1 else out_gpu[b:b + 1, None]
+    err = PT.assert_close(got, ref, f"{bn.name} seq {b}")
+    dense = O.attention_dense(qb, k[None], v[None], np.array([L], np.int32), spec.num_q_heads, spec.num_kv_heads,
+                              T=spec.query_tokens)
+    cos = PT.cosine_per_head(got, dense)
+    return err, in_band, total_codes, float(cos.min()), float(cos.mean())
+
+
+@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg2", "cfg2_32k", "cfg3", "cfg4", "cfg3_prefill"])
+def test_full_size_workload(name, capsys):
+    dev = torch.device("cuda", 0)
+    bn = bench.Bench(name, dev)
+    bn.step()
+    torch.cuda.synchronize(dev)
+    assert int(bn.cache.status.item()) == 0
+    if bn.prefill_only:
+        # the whole 65,536-token prefill: compare every chunk of a few sampled pages
+        spec, wl = bn.spec, bn.wl
+        k, v = _sequence_inputs(spec, 0, spec.ctx, dev)
+        rng = np.random.default_rng(0)
+        sample = rng.choice(wl.num_pages, size=64, replace=False)
+        oc = O.Cache(spec.mode, spec.bits, spec.num_q_heads, spec.num_kv_heads, spec.page_size, wl.num_pages,
+                     wl.rot_k, wl.rot_v)
+        pos = np.concatenate([np.arange(p * 16, p * 16 + 16) for p in range(spec.ctx // 16)
+                              if wl.block_table[0, p] in set(sample.tolist())])
+        mk, mv = oc.append(k[pos], v[pos], synth.slots_for(wl.block_table, 0, pos, 16), with_margins=True)
+        gpu = bn.cache.pages.cpu().numpy()
+        tokens, margins = [], {}
+        for i, t in enumerate(pos):
+            s = int(synth.slots_for(wl.block_table, 0, np.array([t]), 16)[0])
+            margins[i] = (mk[i], mv[i])
+            for h in range(spec.num_kv_heads):
+                tokens.append((s // 16, s % 16, h, i))
+        compared, in_band = PT.compare_chunks(gpu, oc, tokens, margins, (k[pos], v[pos]))
+        assert in_band <= max(4, compared // 200000)
+        with capsys.disabled():
+            print(f"\n{name}: {compared} codes compared, {in_band} within 1e-6 of a boundary")
+        bn.cache.close()
+        return
+    out = bn.out.cpu().numpy()
+    B = bn.spec.batch
+    lens = bn.wl.seq_lens
+    samples = sorted({0, B - 1, int(np.argmax(lens))})
+    for b in samples:
+        err, in_band, total, cmin, cmean = _check_sequence(bn, b, out)
+        with capsys.disabled():
+            print(f"\n{name} seq {b} (ctx {int(lens[b])}): max abs err {err:.2e}, near-boundary codes "
+                  f"{in_band}/{total}, cosine vs fp16 attention min {cmin:.5f} mean {cmean:.5f}")
+    bn.cache.close()
