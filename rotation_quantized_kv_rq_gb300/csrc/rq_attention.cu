@@ -52,7 +52,7 @@ __device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 // (a & c) | (b & ~c)
-__device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t c) { return lop3<0xE2>(a, b, c); }
+__device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t c) { return lop3<0xE4>(a, b, c); }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
