@@ -333,6 +333,11 @@ def run_ours(args, rank, world, local):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # torch creates an event's CUDA handle on its first record: record every profiling event
+    # once here, so the library can re-record the same handles around its kernel
+    for a, b in kev:
+        a.record(stream)
+        b.record(stream)
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize(device)
@@ -440,7 +445,7 @@ def run_ours(args, rank, world, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="cfg1", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

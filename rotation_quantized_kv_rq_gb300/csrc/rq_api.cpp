@@ -18,6 +18,7 @@ struct rq_ctx {
   int num_sms;
   float* d_tables;        // rot_k | rot_v | centroids | boundaries
   float* d_ws;            // split-K partials
+  int* d_counters;        // attention work-item counters (2 ints, zero between launches)
   size_t ws_floats;
   int max_splits;
   int max_n_tiles;        // ceil(max_query_tokens * group / 8)
@@ -175,6 +176,8 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
 
   cudaError_t e = cudaMalloc(&ctx->d_tables, table_floats * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&ctx->d_ws, ctx->ws_floats * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_counters, 2 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_counters, 0, 2 * sizeof(int));
   float* host = nullptr;
   if (e == cudaSuccess) {
     host = (float*)std::calloc(table_floats, sizeof(float));
@@ -192,6 +195,7 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   if (e != cudaSuccess) {
     cudaFree(ctx->d_tables);
     cudaFree(ctx->d_ws);
+    cudaFree(ctx->d_counters);
     delete ctx;
     return RQ_ERR_CUDA;
   }
@@ -222,6 +226,7 @@ void rq_free(rq_ctx* ctx) {
     DeviceScope scope(ctx->device);
     cudaFree(ctx->d_tables);
     cudaFree(ctx->d_ws);
+    cudaFree(ctx->d_counters);
   }
   delete ctx;
 }
@@ -279,22 +284,31 @@ int rq_verify_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages,
   a.n_tiles_n = (a.rows + 7) / 8;
   a.max_splits = ctx->max_splits;
 
-  // Split planning: about 8 work items per resident CTA, each split a whole number of
-  // "one 16-token tile per warp" rounds.
+  a.counters = ctx->d_counters;
+
+  // Split planning.  Each split is a whole number of "one 16-token tile per warp" rounds
+  // (256 tokens).  A CTA works through ceil(items / CTAs) items in the worst case, each
+  // costing its tile rounds plus about two rounds of fixed work (query rotation, merge,
+  // partial write), so pick the split count that minimises that product.
   const int P = ctx->g.page_size;
   const long long units = (long long)B * ctx->g.num_kv_heads * a.n_tiles_n;
-  const long long target = 8LL * ctx->num_sms;
-  long long nsplit = (target + units - 1) / units;
-  if (nsplit < 1) nsplit = 1;
-  if (nsplit > ctx->max_splits) nsplit = ctx->max_splits;
   const int quantum = 256 / P > 0 ? 256 / P : 1;
-  long long pps = (max_pages + nsplit - 1) / nsplit;
-  pps = (pps + quantum - 1) / quantum * quantum;
   const long long min_pps = (max_pages + ctx->max_splits - 1) / ctx->max_splits;
-  if (pps < min_pps) pps = min_pps;
-  if (pps > kMaxSplitPages) pps = kMaxSplitPages;
-  if ((max_pages + pps - 1) / pps > ctx->max_splits) return RQ_ERR_CAPACITY;
-  a.pages_per_split = (int)pps;
+  long long best_pps = -1, best_cost = -1;
+  for (int ns = 1; ns <= ctx->max_splits; ++ns) {
+    long long pps = (max_pages + ns - 1) / ns;
+    pps = (pps + quantum - 1) / quantum * quantum;
+    if (pps < min_pps) pps = (min_pps + quantum - 1) / quantum * quantum;
+    if (pps > kMaxSplitPages) continue;
+    const long long nsplit = (max_pages + pps - 1) / pps;
+    if (nsplit > ctx->max_splits) continue;
+    const long long rounds = (units * nsplit + ctx->num_sms - 1) / ctx->num_sms;
+    const long long tile_rounds = (pps * (P / 16) + 15) / 16;
+    const long long cost = rounds * (tile_rounds + 2);
+    if (best_cost < 0 || cost < best_cost) best_cost = cost, best_pps = pps;
+  }
+  if (best_pps < 0) return RQ_ERR_CAPACITY;
+  a.pages_per_split = (int)best_pps;
   return to_status(
       rq::launch_attention(ctx->g, a, ctx->num_sms, (cudaStream_t)stream, ctx->prof_start, ctx->prof_end));
 }

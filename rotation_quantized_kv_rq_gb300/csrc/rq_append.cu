@@ -2,11 +2,12 @@
 // Compression": norm, fixed data-oblivious rotation -- 2D Givens pairs or 4D quaternion
 // blocks -- then Lloyd-Max scalar codes, bit-packed into the paged cache).
 //
-// One warp encodes the K and the V vector of one (token, kv head).  Lane l owns dimensions
-// 4l..4l+3, which hold two whole Givens pairs or one whole quaternion block, so the rotation
-// needs no data from other lanes; only the squared norm is reduced across the warp.
-// The kernel is bound by HBM: 512 bytes of fp16 in, 2 * (16 * bits + 2) bytes out per
-// (token, head).
+// Work item = one (token, kv head).  A warp takes items in a grid-stride loop: lanes 0-15
+// encode the K vector and lanes 16-31 the V vector.  Lane j of a half owns dimensions
+// 8j..8j+7 -- four whole Givens pairs or two whole quaternion blocks -- so the rotation is
+// lane-local and only the squared norm is reduced (4 xor-shuffles within the half).  Each lane
+// reads 16 bytes, and the next item's 16 bytes are in flight while the current one is coded.
+// The kernel is bound by HBM: 512 bytes of fp16 in, 2 * (16 * bits + 2) bytes out per item.
 #include <cuda_fp16.h>
 
 #include "rq_internal.h"
@@ -15,13 +16,8 @@
 namespace rq {
 namespace {
 
-constexpr int kAppendWarps = 8;
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
+constexpr int kAppendThreads = 256;
+constexpr int kAppendWarps = kAppendThreads / 32;
 
 // Number of boundaries strictly below u: branchless binary search over the sorted table.
 template <int BITS>
@@ -33,8 +29,22 @@ __device__ __forceinline__ int code_of(float u, const float* bnd) {
   return lo;
 }
 
+struct Item {
+  int t, h, slot;
+  uint4 raw;  // 8 fp16 of this lane's half (K or V)
+};
+
+__device__ __forceinline__ void fetch(Item& it, long long item, const Geometry& g, const __half* src_k,
+                                      const __half* src_v, const int32_t* slots, int half, int j) {
+  it.t = (int)(item / g.num_kv_heads);
+  it.h = (int)(item % g.num_kv_heads);
+  it.slot = __ldg(slots + it.t);
+  const __half* src = (half ? src_v : src_k) + ((size_t)it.t * g.num_kv_heads + it.h) * kHeadDim + 8 * j;
+  it.raw = __ldg(reinterpret_cast<const uint4*>(src));
+}
+
 template <int BITS>
-__global__ void __launch_bounds__(kAppendWarps * 32)
+__global__ void __launch_bounds__(kAppendThreads)
 append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict__ v,
               const int32_t* __restrict__ slots, int n, uint8_t* __restrict__ pages,
               int32_t* __restrict__ status) {
@@ -43,78 +53,99 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
   __syncthreads();
 
   const int lane = threadIdx.x & 31;
-  const long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
-  if (item >= (long long)n * g.num_kv_heads) return;
-  const int t = (int)(item / g.num_kv_heads);
-  const int h = (int)(item % g.num_kv_heads);
-  const int slot = slots[t];
-  if (slot < 0) return;
-  if ((long long)slot >= (long long)g.num_pages * g.page_size) {
-    if (lane == 0 && status) atomicOr(status, RQ_STATUS_BAD_SLOT);
-    return;
-  }
-  const int page = slot / g.page_size, off = slot % g.page_size;
-  uint8_t* chunk = pages + ((size_t)page * g.num_kv_heads + h) * (size_t)g.page_bytes;
+  const int half = lane >> 4;        // 0: K, 1: V
+  const int j = lane & 15;           // dims 8j..8j+7
+  const long long items = (long long)n * g.num_kv_heads;
+  const long long stride = (long long)gridDim.x * kAppendWarps;
+  const float* rot = half ? g.rot_v : g.rot_k;
   const int vb = BITS * 16;
+  const long long pool_slots = (long long)g.num_pages * g.page_size;
 
-  // Issue both loads before any arithmetic.
-  const size_t src = ((size_t)t * g.num_kv_heads + h) * kHeadDim + 4 * lane;
-  uint2 raw[2];
-  raw[0] = __ldg(reinterpret_cast<const uint2*>(k + src));
-  raw[1] = __ldg(reinterpret_cast<const uint2*>(v + src));
+  long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+  if (item >= items) return;
+  Item cur, nxt;
+  fetch(cur, item, g, k, v, slots, half, j);
+  for (; item < items; item += stride) {
+    if (item + stride < items) fetch(nxt, item + stride, g, k, v, slots, half, j);
 
+    const int slot = cur.slot;
+    const bool bad = (long long)slot >= pool_slots;
+    if (bad && lane == 0 && status) atomicOr(status, RQ_STATUS_BAD_SLOT);
+    if (slot >= 0 && !bad) {  // uniform across the warp
+      const float4 p0 = __ldg(reinterpret_cast<const float4*>(rot + (size_t)cur.h * kHeadDim + 8 * j));
+      const float4 p1 = __ldg(reinterpret_cast<const float4*>(rot + (size_t)cur.h * kHeadDim + 8 * j + 4));
+      const uint32_t w[4] = {cur.raw.x, cur.raw.y, cur.raw.z, cur.raw.w};
+      float x[8];
 #pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const float4 p = __ldg(reinterpret_cast<const float4*>((which ? g.rot_v : g.rot_k) + (size_t)h * kHeadDim) + lane);
-    const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw[which].x));
-    const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&raw[which].y));
-    float x[4] = {x01.x, x01.y, x23.x, x23.y};
-    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
-    ss = warp_sum(ss);
-    const float nrm = __fsqrt_rn(ss);
-
-    float y[4];
-    if (g.mode == RQ_PLANAR) {
-      y[0] = p.x * x[0] - p.y * x[1];
-      y[1] = p.y * x[0] + p.x * x[1];
-      y[2] = p.z * x[2] - p.w * x[3];
-      y[3] = p.w * x[2] + p.z * x[3];
-    } else {  // Hamilton product (a,b,c,d) (x) (x0,x1,x2,x3)
-      const float a = p.x, b = p.y, c = p.z, d = p.w;
-      y[0] = a * x[0] - b * x[1] - c * x[2] - d * x[3];
-      y[1] = b * x[0] + a * x[1] - d * x[2] + c * x[3];
-      y[2] = c * x[0] + d * x[1] + a * x[2] - b * x[3];
-      y[3] = d * x[0] - c * x[1] + b * x[2] + a * x[3];
-    }
-    int code[4];
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+      }
+      float ss = 0.f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float u = nrm > 0.f ? __fdiv_rn(y[r], nrm) : 0.f;
-      code[r] = code_of<BITS>(u, bnd);
-    }
+      for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float nrm = __fsqrt_rn(ss);
 
-    uint8_t* dst = chunk + (size_t)which * g.page_size * vb + (size_t)off * vb;
-    if (BITS == 4) {
-      const uint16_t two = (uint16_t)(code[0] | (code[1] << 4) | (code[2] << 8) | (code[3] << 12));
-      *reinterpret_cast<uint16_t*>(dst + 2 * lane) = two;
-    } else {
-      // Lane l covers dims 4j..4j+3 of 32-dim group w = l/8 (j = l%8).  Its low bits form
-      // byte j of the group's W0|W1; its high bits go to byte j%4 of W2 at bits
-      // 2*(j/4) + {4,5,0,1}[r], shared with lane j^4.
-      const int w = lane >> 3, j = lane & 7, hh = j >> 2;
-      const uint32_t lo = (code[0] & 3) | ((code[1] & 3) << 2) | ((code[2] & 3) << 4) | ((code[3] & 3) << 6);
-      const uint32_t hib = ((code[0] >> 2) << (2 * hh + 4)) | ((code[1] >> 2) << (2 * hh + 5)) |
-                           ((code[2] >> 2) << (2 * hh)) | ((code[3] >> 2) << (2 * hh + 1));
-      const uint32_t partner = __shfl_down_sync(0xffffffffu, hib, 4);
-      dst[12 * w + j] = (uint8_t)lo;
-      if (hh == 0) dst[12 * w + 8 + j] = (uint8_t)(hib | partner);
+      float y[8];
+      const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      if (g.mode == RQ_PLANAR) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float c = pr[2 * q], s = pr[2 * q + 1];
+          y[2 * q] = c * x[2 * q] - s * x[2 * q + 1];
+          y[2 * q + 1] = s * x[2 * q] + c * x[2 * q + 1];
+        }
+      } else {  // Hamilton product (a,b,c,d) (x) (x0,x1,x2,x3)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float a = pr[4 * q], b = pr[4 * q + 1], c = pr[4 * q + 2], d = pr[4 * q + 3];
+          const float* xb = x + 4 * q;
+          y[4 * q + 0] = a * xb[0] - b * xb[1] - c * xb[2] - d * xb[3];
+          y[4 * q + 1] = b * xb[0] + a * xb[1] - d * xb[2] + c * xb[3];
+          y[4 * q + 2] = c * xb[0] + d * xb[1] + a * xb[2] - b * xb[3];
+          y[4 * q + 3] = d * xb[0] - c * xb[1] + b * xb[2] + a * xb[3];
+        }
+      }
+      int code[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) code[e] = code_of<BITS>(nrm > 0.f ? __fdiv_rn(y[e], nrm) : 0.f, bnd);
+
+      const int page = slot / g.page_size, off = slot % g.page_size;
+      uint8_t* chunk = pages + ((size_t)page * g.num_kv_heads + cur.h) * (size_t)g.page_bytes;
+      uint8_t* dst = chunk + (size_t)half * g.page_size * vb + (size_t)off * vb;
+      if (BITS == 4) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) word |= (uint32_t)code[e] << (4 * e);
+        *reinterpret_cast<uint32_t*>(dst + 4 * j) = word;
+      } else {
+        // Lane j covers dims 8m..8m+7 of 32-dim group w = j/4 (m = j%4).  Its low bits are
+        // bytes 2m, 2m+1 of the group's W0|W1; its high bits fill half of bytes 2(m&1) and
+        // 2(m&1)+1 of W2, shared with lane j^2 (same k, other h).
+        const int w = j >> 2, m = j & 3, hh = m >> 1;
+        uint32_t lo = 0, hib = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          lo |= (uint32_t)(code[e] & 3) << (2 * e);
+          const int r = e & 3, kk = e >> 2;  // dim 8m + e = 16hh + 4(2(m&1) + kk) + r
+          const int off_r = (r < 2) ? 4 + r : r - 2;
+          hib |= (uint32_t)(code[e] >> 2) << (8 * kk + 2 * hh + off_r);
+        }
+        const uint32_t partner = __shfl_xor_sync(0xffffffffu, hib, 2);
+        *reinterpret_cast<uint16_t*>(dst + 12 * w + 2 * m) = (uint16_t)lo;
+        if (hh == 0) *reinterpret_cast<uint16_t*>(dst + 12 * w + 8 + 2 * (m & 1)) = (uint16_t)(hib | partner);
+      }
+      if (j == 0) {
+        const __half n16 = __float2half_rn(nrm);
+        uint8_t* nb = chunk + (size_t)2 * g.page_size * vb + (size_t)half * 2 * g.page_size + 2 * off;
+        *reinterpret_cast<__half*>(nb) = n16;
+        if (status && __hisinf(n16)) atomicOr(status, RQ_STATUS_NORM_OVERFLOW);
+      }
     }
-    if (lane == 0) {
-      const __half n16 = __float2half_rn(nrm);
-      uint8_t* nb = chunk + (size_t)2 * g.page_size * vb + (size_t)which * 2 * g.page_size + 2 * off;
-      *reinterpret_cast<__half*>(nb) = n16;
-      if (status && __hisinf(n16)) atomicOr(status, RQ_STATUS_NORM_OVERFLOW);
-    }
+    cur = nxt;
   }
 }
 
@@ -123,14 +154,22 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
 cudaError_t launch_append(const Geometry& g, const void* k, const void* v, const int32_t* slots, int n,
                           uint8_t* pages, int32_t* status, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
+  static int max_blocks = 0;
+  if (max_blocks == 0) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    max_blocks = (sms > 0 ? sms : 132) * (2048 / kAppendThreads);
+  }
   const long long items = (long long)n * g.num_kv_heads;
-  const unsigned blocks = (unsigned)((items + kAppendWarps - 1) / kAppendWarps);
+  long long blocks = (items + kAppendWarps - 1) / kAppendWarps;
+  if (blocks > max_blocks) blocks = max_blocks;
   if (g.bits == 4)
-    append_kernel<4><<<blocks, kAppendWarps * 32, 0, stream>>>(g, (const __half*)k, (const __half*)v, slots, n,
-                                                               pages, status);
+    append_kernel<4><<<(unsigned)blocks, kAppendThreads, 0, stream>>>(g, (const __half*)k, (const __half*)v,
+                                                                     slots, n, pages, status);
   else
-    append_kernel<3><<<blocks, kAppendWarps * 32, 0, stream>>>(g, (const __half*)k, (const __half*)v, slots, n,
-                                                               pages, status);
+    append_kernel<3><<<(unsigned)blocks, kAppendThreads, 0, stream>>>(g, (const __half*)k, (const __half*)v,
+                                                                     slots, n, pages, status);
   return cudaGetLastError();
 }
 

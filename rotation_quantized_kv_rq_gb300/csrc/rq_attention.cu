@@ -323,20 +323,22 @@ struct ItemInfo {
   int b, h, nt, split;
 };
 
-__device__ __forceinline__ ItemInfo decode_item(int item, const Geometry& g, const AttnArgs& a, int nsplit) {
+// Items are ordered split-major, so every sequence's full-length splits come before the
+// (shorter or empty) last splits and the dynamic scheduler hands out long items first.
+__device__ __forceinline__ ItemInfo decode_item(int item, const Geometry& g, const AttnArgs& a) {
   ItemInfo it;
-  it.split = item % nsplit;
-  int rest = item / nsplit;
-  it.nt = rest % a.n_tiles_n;
-  rest /= a.n_tiles_n;
+  it.nt = item % a.n_tiles_n;
+  int rest = item / a.n_tiles_n;
   it.h = rest % g.num_kv_heads;
-  it.b = rest / g.num_kv_heads;
+  rest /= g.num_kv_heads;
+  it.b = rest % a.B;
+  it.split = rest / a.B;
   return it;
 }
 
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_splitk_kernel(const Geometry g, const AttnArgs a, int nsplit, int n_items) {
+attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* lut_words = reinterpret_cast<uint32_t*>(smem);
   float* merge = reinterpret_cast<float*>(smem + kLutBytes);
@@ -353,8 +355,11 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int nsplit, int n_items) 
   const int tiles_per_page = P / 16;
   const __half* qh = reinterpret_cast<const __half*>(a.q);
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const ItemInfo it = decode_item(item, g, a, nsplit);
+  __shared__ int s_item;
+  if (threadIdx.x == 0) s_item = atomicAdd(a.counters, 1);
+  __syncthreads();
+  for (int item = s_item; item < n_items;) {
+    const ItemInfo it = decode_item(item, g, a);
     int len = a.seq_lens[it.b];
     const int cap = a.max_pages * P;
     if (len < 0 || len > cap || (len > 0 && len < a.T)) {
@@ -365,7 +370,13 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int nsplit, int n_items) 
     const int p0 = it.split * a.pages_per_split;
     int p1 = p0 + a.pages_per_split;
     if (p1 > npages) p1 = npages;
-    if (p0 >= p1) continue;  // uniform across the CTA: the combine never reads this split
+    if (p0 >= p1) {  // uniform across the CTA: the combine never reads this split
+      __syncthreads();
+      if (threadIdx.x == 0) s_item = atomicAdd(a.counters, 1);
+      __syncthreads();
+      item = s_item;
+      continue;
+    }
 
     // Stage the split's page ids (clamped into the pool).
     for (int i = threadIdx.x; i < p1 - p0; i += kThreads) {
@@ -466,7 +477,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int nsplit, int n_items) 
       sc[1] = r0 <= last_pos[1] ? s[1] * nk0 : -CUDART_INF_F;
       sc[2] = r1 <= last_pos[0] ? s[2] * nk1 : -CUDART_INF_F;
       sc[3] = r1 <= last_pos[1] ? s[3] * nk1 : -CUDART_INF_F;
-      float pw[4];
+      float pw[4], alpha[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float tmax = fmaxf(sc[c], sc[c + 2]);
@@ -475,16 +486,22 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int nsplit, int n_items) 
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
         const float m_new = fmaxf(m_run[c], tmax);
         const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-        const float alpha = exp2f(m_run[c] - m_use);
+        alpha[c] = exp2f(m_run[c] - m_use);
         const float p0v = exp2f(sc[c] - m_use), p1v = exp2f(sc[c + 2] - m_use);
-        l_run[c] = l_run[c] * alpha + p0v + p1v;
+        l_run[c] = l_run[c] * alpha[c] + p0v + p1v;
         m_run[c] = m_new;
         pw[c] = p0v;
         pw[c + 2] = p1v;
+      }
+      // Rescale the accumulators only when some column's running max moved (rare after the
+      // first tiles); alpha is exactly 1 otherwise, so skipping changes nothing.
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          o[mt][c] *= alpha;
-          o[mt][c + 2] *= alpha;
+          o[mt][0] *= alpha[0];
+          o[mt][2] *= alpha[0];
+          o[mt][1] *= alpha[1];
+          o[mt][3] *= alpha[1];
         }
       }
       // P' = p * n_v (zero for masked tokens, whatever their stored norm)
@@ -549,6 +566,18 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int nsplit, int n_items) 
       }
     }
     __syncthreads();  // merge buffer and page ids are reused by the next item
+    if (threadIdx.x == 0) s_item = atomicAdd(a.counters, 1);
+    __syncthreads();
+    item = s_item;
+  }
+  // The last CTA to finish re-arms the work counter for the next launch on this stream.
+  // Nothing waits on it: every CTA has already drawn an out-of-range item.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.counters + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(a.counters, 0);
+      atomicExch(a.counters + 1, 0);
+    }
   }
 }
 
@@ -634,9 +663,9 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas,
     const int grid = (int)(n_items < num_ctas ? n_items : num_ctas);
     if (ev_start) cudaEventRecord(ev_start, stream);
     if (g.bits == 4)
-      attn_splitk_kernel<4><<<grid, kThreads, kSmemBytes, stream>>>(g, a, nsplit, (int)n_items);
+      attn_splitk_kernel<4><<<grid, kThreads, kSmemBytes, stream>>>(g, a, (int)n_items);
     else
-      attn_splitk_kernel<3><<<grid, kThreads, kSmemBytes, stream>>>(g, a, nsplit, (int)n_items);
+      attn_splitk_kernel<3><<<grid, kThreads, kSmemBytes, stream>>>(g, a, (int)n_items);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev_end) cudaEventRecord(ev_end, stream);

@@ -42,6 +42,7 @@ struct AttnArgs {
   int n_tiles_n;             // ceil(rows / 8)
   int pages_per_split;
   int max_splits;            // splits per (b, kv head) the workspace has room for
+  int* counters;             // [2] work-item and finished-CTA counters, zero between launches
 };
 
 constexpr int kPartialStride = 132;   // floats per partial row: m, l, pad, pad, o[128]
