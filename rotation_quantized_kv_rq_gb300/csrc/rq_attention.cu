@@ -34,7 +34,9 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kLutBytes = 256 * 256;          // 256 index bytes x (2 tables x 32 lanes x 4 B)
 constexpr int kMaxSplitPages = 1024;          // page ids staged per item
 constexpr int kMergeFloats = kWarps * 8 * kPartialStride;
-constexpr size_t kSmemBytes = kLutBytes + (size_t)kMergeFloats * 4 + kMaxSplitPages * 4 + 64;
+// The table must start at a 64 KB-aligned shared-window address (see `lut` below), so the
+// allocation reserves a worst-case 64 KB alignment gap in front of it.
+constexpr size_t kSmemBytes = 65536 + kLutBytes + (size_t)kMergeFloats * 4 + kMaxSplitPages * 4 + 128;
 
 // ---------------------------------------------------------------------------------------
 // PTX helpers
@@ -117,8 +119,7 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
 // base + e * 256 + lane * 4 (+ 128 for the second table).
 // ---------------------------------------------------------------------------------------
 template <int BITS>
-__device__ void build_lut(uint32_t* lut, const float* centroids) {
-  __shared__ float cb[16];
+__device__ void build_lut(uint32_t* lut, const float* centroids, float* cb) {
   if (threadIdx.x < (1 << BITS)) cb[threadIdx.x] = centroids[threadIdx.x];
   __syncthreads();
   for (int i = threadIdx.x; i < 256 * 64; i += kThreads) {
@@ -139,15 +140,23 @@ __device__ void build_lut(uint32_t* lut, const float* centroids) {
 }
 
 // Half2 of the two codes in byte J of index word x (SECOND selects the second table).
+// The table starts at a 64 KB-aligned shared address A, so an entry's address
+// A + e * 256 + lane * 4 (+ 128) has byte 0 = lane * 4 (+ 128), byte 1 = e and bytes 2-3 = A's:
+// one byte permute of (x, key) with key = A | lane * 4 (+ 128) forms it, with no add.
 template <int J, int SECOND>
-__device__ __forceinline__ uint32_t lut(uint32_t x, uint32_t lane_off, uint32_t base) {
-  const uint32_t a = prmt(x, lane_off, 0x5504u | (J << 4));
-  return lds32(a + base + (SECOND ? 128u : 0u));
+__device__ __forceinline__ uint32_t lut(uint32_t x, uint32_t key1, uint32_t key2) {
+  return lds32(prmt(x, SECOND ? key2 : key1, 0x7604u | (J << 4)));
 }
 template <int SECOND>
-__device__ __forceinline__ uint32_t lut_dyn(uint32_t x, int j, uint32_t lane_off, uint32_t base) {
-  const uint32_t a = prmt(x, lane_off, 0x5504u | (j << 4));
-  return lds32(a + base + (SECOND ? 128u : 0u));
+__device__ __forceinline__ uint32_t lut_dyn(uint32_t x, int j, uint32_t key1, uint32_t key2) {
+  return lds32(prmt(x, SECOND ? key2 : key1, 0x7604u | (j << 4)));
+}
+
+// 2^x on the SFU (x = -inf gives +0, which masked scores rely on).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -206,7 +215,7 @@ __device__ __forceinline__ void load_tile(Raw<BITS>& r, const uint8_t* chunk, in
 //        X2 = W1.lo | (W2>>2).hi (T1, pairs 8+2k), X3 = (W2>>2).lo | W1.hi (T2, pairs 9+2k).
 template <int BITS>
 __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const uint32_t (&qf)[8][2],
-                                        uint32_t lane_off, uint32_t base) {
+                                        uint32_t key1, uint32_t key2) {
   s[0] = s[1] = s[2] = s[3] = 0.f;
   float s2[4] = {0.f, 0.f, 0.f, 0.f};
   if constexpr (BITS == 4) {
@@ -217,15 +226,15 @@ __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const
       const int w = kc >> 1, j0 = (2 * kc) & 3;
       uint32_t a0, a1, a2, a3;
       if (j0 == 0) {
-        a0 = lut<0, 0>(k0[w], lane_off, base);
-        a1 = lut<0, 0>(k1[w], lane_off, base);
-        a2 = lut<1, 0>(k0[w], lane_off, base);
-        a3 = lut<1, 0>(k1[w], lane_off, base);
+        a0 = lut<0, 0>(k0[w], key1, key2);
+        a1 = lut<0, 0>(k1[w], key1, key2);
+        a2 = lut<1, 0>(k0[w], key1, key2);
+        a3 = lut<1, 0>(k1[w], key1, key2);
       } else {
-        a0 = lut<2, 0>(k0[w], lane_off, base);
-        a1 = lut<2, 0>(k1[w], lane_off, base);
-        a2 = lut<3, 0>(k0[w], lane_off, base);
-        a3 = lut<3, 0>(k1[w], lane_off, base);
+        a0 = lut<2, 0>(k0[w], key1, key2);
+        a1 = lut<2, 0>(k1[w], key1, key2);
+        a2 = lut<3, 0>(k0[w], key1, key2);
+        a3 = lut<3, 0>(k1[w], key1, key2);
       }
       if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
       else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
@@ -243,10 +252,10 @@ __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const
 #pragma unroll
     for (int kc = 0; kc < 8; ++kc) {
       const int hi = kc >> 2, byte = kc & 3;
-      const uint32_t a0 = lut_dyn<0>(X[0][2 * hi], byte, lane_off, base);
-      const uint32_t a1 = lut_dyn<0>(X[1][2 * hi], byte, lane_off, base);
-      const uint32_t a2 = lut_dyn<1>(X[0][2 * hi + 1], byte, lane_off, base);
-      const uint32_t a3 = lut_dyn<1>(X[1][2 * hi + 1], byte, lane_off, base);
+      const uint32_t a0 = lut_dyn<0>(X[0][2 * hi], byte, key1, key2);
+      const uint32_t a1 = lut_dyn<0>(X[1][2 * hi], byte, key1, key2);
+      const uint32_t a2 = lut_dyn<1>(X[0][2 * hi + 1], byte, key1, key2);
+      const uint32_t a3 = lut_dyn<1>(X[1][2 * hi + 1], byte, key1, key2);
       if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
       else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
     }
@@ -260,7 +269,7 @@ __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const
 // dim of two tokens, so the two tokens' code words are interleaved first.
 template <int BITS>
 __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, uint32_t pb0, uint32_t pb1,
-                                        uint32_t lane_off, uint32_t base, int g) {
+                                        uint32_t key1, uint32_t key2, int g) {
   if constexpr (BITS == 4) {
     uint32_t XE[2][2], XO[2][2];  // [token pair][word]
 #pragma unroll
@@ -274,10 +283,10 @@ __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, ui
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       const int w = mt >> 2, j = mt & 3;
-      const uint32_t a0 = lut_dyn<0>(XE[0][w], j, lane_off, base);
-      const uint32_t a1 = lut_dyn<0>(XO[0][w], j, lane_off, base);
-      const uint32_t a2 = lut_dyn<0>(XE[1][w], j, lane_off, base);
-      const uint32_t a3 = lut_dyn<0>(XO[1][w], j, lane_off, base);
+      const uint32_t a0 = lut_dyn<0>(XE[0][w], j, key1, key2);
+      const uint32_t a1 = lut_dyn<0>(XO[0][w], j, key1, key2);
+      const uint32_t a2 = lut_dyn<0>(XE[1][w], j, key1, key2);
+      const uint32_t a3 = lut_dyn<0>(XO[1][w], j, key1, key2);
       mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
     }
   } else {
@@ -301,15 +310,15 @@ __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, ui
       const int j = mt >> 1;
       uint32_t a0, a1, a2, a3;
       if ((mt & 1) == 0) {
-        a0 = lut_dyn<0>(XE1[0], j, lane_off, base);
-        a1 = lut_dyn<0>(XO1[0], j, lane_off, base);
-        a2 = lut_dyn<0>(XE1[1], j, lane_off, base);
-        a3 = lut_dyn<0>(XO1[1], j, lane_off, base);
+        a0 = lut_dyn<0>(XE1[0], j, key1, key2);
+        a1 = lut_dyn<0>(XO1[0], j, key1, key2);
+        a2 = lut_dyn<0>(XE1[1], j, key1, key2);
+        a3 = lut_dyn<0>(XO1[1], j, key1, key2);
       } else {
-        a0 = lut_dyn<1>(XE2[0], j, lane_off, base);
-        a1 = lut_dyn<1>(XO2[0], j, lane_off, base);
-        a2 = lut_dyn<1>(XE2[1], j, lane_off, base);
-        a3 = lut_dyn<1>(XO2[1], j, lane_off, base);
+        a0 = lut_dyn<1>(XE2[0], j, key1, key2);
+        a1 = lut_dyn<1>(XO2[0], j, key1, key2);
+        a2 = lut_dyn<1>(XE2[1], j, key1, key2);
+        a3 = lut_dyn<1>(XO2[1], j, key1, key2);
       }
       mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
     }
@@ -340,17 +349,21 @@ template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
   extern __shared__ __align__(16) uint8_t smem[];
-  uint32_t* lut_words = reinterpret_cast<uint32_t*>(smem);
-  float* merge = reinterpret_cast<float*>(smem + kLutBytes);
-  int* page_ids = reinterpret_cast<int*>(smem + kLutBytes + (size_t)kMergeFloats * 4);
+  const uint32_t dyn_base = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t lut_addr = (dyn_base + 0xFFFFu) & ~0xFFFFu;   // first 64 KB-aligned address
+  uint32_t* lut_words = reinterpret_cast<uint32_t*>(smem + (lut_addr - dyn_base));
+  uint8_t* high = smem + (lut_addr - dyn_base) + kLutBytes;
+  float* merge = reinterpret_cast<float*>(high);
+  int* page_ids = reinterpret_cast<int*>(high + (size_t)kMergeFloats * 4);
+  float* cb = reinterpret_cast<float*>(page_ids + kMaxSplitPages);
 
-  build_lut<BITS>(lut_words, g.centroids);
+  build_lut<BITS>(lut_words, g.centroids, cb);
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const uint32_t base = (uint32_t)__cvta_generic_to_shared(lut_words);
-  const uint32_t lane_off = (uint32_t)lane * 4u;
+  const uint32_t key1 = lut_addr | ((uint32_t)lane * 4u);
+  const uint32_t key2 = key1 + 128u;
   const int P = g.page_size;
   const int tiles_per_page = P / 16;
   const __half* qh = reinterpret_cast<const __half*>(a.q);
@@ -467,16 +480,26 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
       }
       // ---- scores (base 2) for tokens pos0 + gq and pos0 + gq + 8, query columns 2tq, 2tq+1
       float s[4];
-      qk_tile<BITS>(s, cur, qf, lane_off, base);
+      qk_tile<BITS>(s, cur, qf, key1, key2);
       const int pos0 = tile * 16;
       const float nk0 = half_bits_to_float(cur.nk & 0xffffu), nk1 = half_bits_to_float(cur.nk >> 16);
       const float nv0 = half_bits_to_float(cur.nv & 0xffffu), nv1 = half_bits_to_float(cur.nv >> 16);
       const int r0 = pos0 + gq, r1 = pos0 + gq + 8;
+      // Tiles wholly inside every column's visible range (all but the last one or two of a
+      // sequence) skip the per-element mask.
+      const bool interior = __all_sync(0xffffffffu, pos0 + 15 <= min(last_pos[0], last_pos[1]));
       float sc[4];
-      sc[0] = r0 <= last_pos[0] ? s[0] * nk0 : -CUDART_INF_F;
-      sc[1] = r0 <= last_pos[1] ? s[1] * nk0 : -CUDART_INF_F;
-      sc[2] = r1 <= last_pos[0] ? s[2] * nk1 : -CUDART_INF_F;
-      sc[3] = r1 <= last_pos[1] ? s[3] * nk1 : -CUDART_INF_F;
+      if (interior) {
+        sc[0] = s[0] * nk0;
+        sc[1] = s[1] * nk0;
+        sc[2] = s[2] * nk1;
+        sc[3] = s[3] * nk1;
+      } else {
+        sc[0] = r0 <= last_pos[0] ? s[0] * nk0 : -CUDART_INF_F;
+        sc[1] = r0 <= last_pos[1] ? s[1] * nk0 : -CUDART_INF_F;
+        sc[2] = r1 <= last_pos[0] ? s[2] * nk1 : -CUDART_INF_F;
+        sc[3] = r1 <= last_pos[1] ? s[3] * nk1 : -CUDART_INF_F;
+      }
       float pw[4], alpha[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -486,8 +509,8 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
         const float m_new = fmaxf(m_run[c], tmax);
         const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-        alpha[c] = exp2f(m_run[c] - m_use);
-        const float p0v = exp2f(sc[c] - m_use), p1v = exp2f(sc[c + 2] - m_use);
+        alpha[c] = ex2(m_run[c] - m_use);
+        const float p0v = ex2(sc[c] - m_use), p1v = ex2(sc[c + 2] - m_use);
         l_run[c] = l_run[c] * alpha[c] + p0v + p1v;
         m_run[c] = m_new;
         pw[c] = p0v;
@@ -505,13 +528,16 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
         }
       }
       // P' = p * n_v (zero for masked tokens, whatever their stored norm)
-      const float q0 = sc[0] == -CUDART_INF_F ? 0.f : pw[0] * nv0;
-      const float q1 = sc[1] == -CUDART_INF_F ? 0.f : pw[1] * nv0;
-      const float q2 = sc[2] == -CUDART_INF_F ? 0.f : pw[2] * nv1;
-      const float q3 = sc[3] == -CUDART_INF_F ? 0.f : pw[3] * nv1;
+      float q0 = pw[0] * nv0, q1 = pw[1] * nv0, q2 = pw[2] * nv1, q3 = pw[3] * nv1;
+      if (!interior) {
+        q0 = sc[0] == -CUDART_INF_F ? 0.f : q0;
+        q1 = sc[1] == -CUDART_INF_F ? 0.f : q1;
+        q2 = sc[2] == -CUDART_INF_F ? 0.f : q2;
+        q3 = sc[3] == -CUDART_INF_F ? 0.f : q3;
+      }
       const uint32_t pb0 = movmatrix_t(pack_half2(q0, q1));
       const uint32_t pb1 = movmatrix_t(pack_half2(q2, q3));
-      pv_tile<BITS>(o, cur, pb0, pb1, lane_off, base, gq);
+      pv_tile<BITS>(o, cur, pb0, pb1, key1, key2, gq);
       cur = nxt;
     }
 
