@@ -154,6 +154,34 @@ int rq_verify_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
                         const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
                         void *out, int32_t *d_status, void *stream);
 
+/*
+ * Decode attention that allocates nothing.  The pages have no counterpart to this entry point:
+ * it exists for callers that cannot call cudaMalloc -- for example code running inside a
+ * serving engine whose memory pool has already reserved the device's free memory (a raw
+ * allocation would fail or fragment the pool), or a plugin whose host framework forbids
+ * allocations outside its own allocator.  Such callers cannot create a context either, so
+ * everything comes in as arguments:
+ *   cfg         host; only head_dim, num_q_heads, num_kv_heads, bits, mode, page_size, num_pages
+ *               and sm_scale are read (the max_* limits, host tables, codebook and device are
+ *               ignored)
+ *   d_rot_k, d_rot_v   device float32 [Hkv][head_dim], laid out as rq_config.rot_k / rot_v
+ *   d_centroids        device float32 [2^bits], ascending (e.g. from rq_lloyd_max_codebook)
+ *   other arguments    as rq_decode_attention, on the CURRENT device
+ * The result equals rq_decode_attention's on the same inputs.
+ * Scratch: the split-K partials and work counters live in one file-scope 16 MiB device array
+ * that every GPU which loads the library holds until the process exits.  A call whose
+ * B * num_kv_heads * ceil(group / 8) exceeds 3,971 (not even one context split per sequence
+ * fits) returns RQ_ERR_CAPACITY; so does a block table wider than 65,536 pages.
+ * The first call on a device sets up that device (resolves the array's address, reads the SM
+ * count, sets the kernel's shared-memory limit); make that first call before any stream
+ * capture.  Every call shares the one array and re-zeroes its counters on `stream`, so calls
+ * that overlap on the GPU (different streams, or different host threads) race: serialise them.
+ */
+int rq_decode_attention_noalloc(const rq_config *cfg, const float *d_rot_k, const float *d_rot_v,
+                                const float *d_centroids, const void *q, const void *kv_pages,
+                                const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                                int B, void *out, int32_t *d_status, void *stream);
+
 /* Diagnostics.  While set, every attention call records ev_start on its stream just before
    its split-K kernel and ev_end just after it (both cudaEvent_t created by the caller, who
    reads the elapsed time); NULL, NULL stops recording.  Costs nothing when unset. */

@@ -24,7 +24,7 @@ HEAD_DIM = 128
 
 EXPORTS = ["rq_create", "rq_free", "rq_page_bytes", "rq_lloyd_max_codebook", "rq_get_codebook",
            "rq_quantize_append", "rq_decode_attention", "rq_verify_attention", "rq_set_profile_events",
-           "rq_status_string"]
+           "rq_decode_attention_noalloc", "rq_status_string"]
 
 
 class RQError(RuntimeError):
@@ -71,6 +71,9 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             L.rq_verify_attention.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, vp,
                                               vp]
             L.rq_verify_attention.restype = ctypes.c_int
+            L.rq_decode_attention_noalloc.argtypes = [ctypes.POINTER(rq_config), vp, vp, vp, vp, vp, vp,
+                                                      ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]
+            L.rq_decode_attention_noalloc.restype = ctypes.c_int
             L.rq_set_profile_events.argtypes = [vp, vp, vp]
             L.rq_set_profile_events.restype = ctypes.c_int
             L.rq_status_string.argtypes = [ctypes.c_int]
@@ -174,6 +177,29 @@ def rq_verify_attention(ctx, q: torch.Tensor, kv_pages: torch.Tensor, block_tabl
     _check("rq_verify_attention",
            lib().rq_verify_attention(ctx, _ptr(q), T, _ptr(kv_pages), _ptr(block_table), block_table.shape[-1],
                                      _ptr(seq_lens), B, _ptr(out), _ptr(status), _stream(stream, q.device)))
+    return out
+
+
+def rq_decode_attention_noalloc(mode: int, bits: int, num_q_heads: int, num_kv_heads: int, page_size: int,
+                                num_pages: int, d_rot_k: torch.Tensor, d_rot_v: torch.Tensor,
+                                d_centroids: torch.Tensor, q: torch.Tensor, kv_pages: torch.Tensor,
+                                block_table: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor,
+                                status: torch.Tensor | None = None, sm_scale: float = 0.0,
+                                stream=None) -> torch.Tensor:
+    """Decode attention with no allocation: tables as device float32 tensors, scratch in the
+    library's fixed device array (see include/rq.h)."""
+    for t in (d_rot_k, d_rot_v, d_centroids):
+        assert t.dtype == torch.float32 and t.is_contiguous() and t.is_cuda
+    assert q.dtype == torch.float16 and out.dtype == torch.float16 and q.is_contiguous() and out.is_contiguous()
+    assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32 and block_table.is_contiguous()
+    cfg = rq_config(HEAD_DIM, num_q_heads, num_kv_heads, bits, mode, page_size, num_pages, 0, 0, 0,
+                    ctypes.POINTER(ctypes.c_float)(), ctypes.POINTER(ctypes.c_float)(),
+                    ctypes.POINTER(ctypes.c_float)(), float(sm_scale), -1)
+    _check("rq_decode_attention_noalloc",
+           lib().rq_decode_attention_noalloc(ctypes.byref(cfg), _ptr(d_rot_k), _ptr(d_rot_v), _ptr(d_centroids),
+                                             _ptr(q), _ptr(kv_pages), _ptr(block_table), block_table.shape[-1],
+                                             _ptr(seq_lens), seq_lens.numel(), _ptr(out), _ptr(status),
+                                             _stream(stream, q.device)))
     return out
 
 
