@@ -64,6 +64,8 @@ extern "C" {
 #define RQ_STATUS_BAD_SLOT 2   /* slot_mapping entry >= num_pages * page_size */
 #define RQ_STATUS_BAD_LEN 4    /* seq_len < 0 or above max_pages * page_size, or below T */
 #define RQ_STATUS_NORM_OVERFLOW 8 /* a vector norm above the fp16 range (stored as inf) */
+#define RQ_STATUS_TIMEOUT 16   /* an attention kernel's staged page copy did not complete within
+                                  its bounded wait (outputs of that call are unspecified) */
 
 /* Rotation families ("--kv-cache-dtype rq{3,4}_{planar,iso}") */
 #define RQ_PLANAR 0            /* PlanarQuant: 2D Givens rotation per dimension pair */

@@ -19,14 +19,22 @@ namespace {
 constexpr int kAppendThreads = 256;
 constexpr int kAppendWarps = kAppendThreads / 32;
 
-// Number of boundaries strictly below u: branchless binary search over the sorted table.
-template <int BITS>
-__device__ __forceinline__ int code_of(float u, const float* bnd) {
-  int lo = 0;
-#pragma unroll
-  for (int step = (1 << BITS) / 2; step >= 1; step >>= 1)
-    if (bnd[lo + step - 1] < u) lo += step;
-  return lo;
+// Number of boundaries strictly below u (b ascending, in registers): a binary search written as
+// a select tree, one compare per level and no indexed memory.
+__device__ __forceinline__ int code_of(float u, const float (&b)[15], int bits) {
+  if (bits == 3) {
+    const bool s2 = u > b[3];
+    const bool s1 = u > (s2 ? b[5] : b[1]);
+    const bool s0 = u > (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
+    return (s2 ? 4 : 0) + (s1 ? 2 : 0) + (s0 ? 1 : 0);
+  }
+  const bool s3 = u > b[7];
+  const bool s2 = u > (s3 ? b[11] : b[3]);
+  const bool s1 = u > (s3 ? (s2 ? b[13] : b[9]) : (s2 ? b[5] : b[1]));
+  const float m0 = s3 ? (s2 ? (s1 ? b[14] : b[12]) : (s1 ? b[10] : b[8]))
+                      : (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
+  const bool s0 = u > m0;
+  return (s3 ? 8 : 0) + (s2 ? 4 : 0) + (s1 ? 2 : 0) + (s0 ? 1 : 0);
 }
 
 struct Item {
@@ -48,9 +56,9 @@ __global__ void __launch_bounds__(kAppendThreads)
 append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict__ v,
               const int32_t* __restrict__ slots, int n, uint8_t* __restrict__ pages,
               int32_t* __restrict__ status) {
-  __shared__ float bnd[16];
-  if (threadIdx.x < (1 << BITS) - 1) bnd[threadIdx.x] = g.boundaries[threadIdx.x];
-  __syncthreads();
+  float bnd[15];
+#pragma unroll
+  for (int i = 0; i < 15; ++i) bnd[i] = i < (1 << BITS) - 1 ? __ldg(g.boundaries + i) : 0.f;
 
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;        // 0: K, 1: V
@@ -109,9 +117,12 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
           y[4 * q + 3] = d * xb[0] - c * xb[1] + b * xb[2] + a * xb[3];
         }
       }
+      // u = y / n as y * (1/n): within an ulp of the quotient, so a code can differ from the
+      // quotient's only for u within ~1e-7 of a boundary.
+      const float rcp = nrm > 0.f ? __frcp_rn(nrm) : 0.f;
       int code[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) code[e] = code_of<BITS>(nrm > 0.f ? __fdiv_rn(y[e], nrm) : 0.f, bnd);
+      for (int e = 0; e < 8; ++e) code[e] = code_of(y[e] * rcp, bnd, BITS);
 
       const int page = slot / g.page_size, off = slot % g.page_size;
       uint8_t* chunk = pages + ((size_t)page * g.num_kv_heads + cur.h) * (size_t)g.page_bytes;

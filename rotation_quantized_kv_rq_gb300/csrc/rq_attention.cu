@@ -34,9 +34,28 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kLutBytes = 256 * 256;          // 256 index bytes x (2 tables x 32 lanes x 4 B)
 constexpr int kMaxSplitPages = 1024;          // page ids staged per item
 constexpr int kMergeFloats = kWarps * 8 * kPartialStride;
-// The table must start at a 64 KB-aligned shared-window address (see `lut` below), so the
-// allocation reserves a worst-case 64 KB alignment gap in front of it.
-constexpr size_t kSmemBytes = 65536 + kLutBytes + (size_t)kMergeFloats * 4 + kMaxSplitPages * 4 + 128;
+constexpr int kWaitLimit = 1 << 22;           // bounded mbarrier polling (about a second)
+
+// Per-warp ring of staged 16-token tiles.  A stage holds one tile exactly as a 16-token page
+// chunk is laid out: K codes [16][vb] | V codes [16][vb] | K norms fp16 [16] | V norms fp16 [16].
+template <int BITS>
+struct Ring {
+  static constexpr int VB = BITS * 16;
+  static constexpr int SB = 32 * VB + 64;           // stage bytes: 2112 (4-bit), 1600 (3-bit)
+  static constexpr int S = BITS == 4 ? 3 : 4;       // stages per warp
+  static constexpr int BYTES = kWarps * S * SB;     // 101,376 / 102,400
+};
+
+// Dynamic shared memory, from the start of the CTA's dynamic window at shared address `base`:
+//   rings [16 warps][S][SB]  (the warps' merge buffer aliases them between items)
+//   lookup table, 64 KB, at the first 64 KB-aligned address after the rings
+//   page ids int[1024] | mbarriers u64[16][S] | centroids float[16] | item slot int[4]
+template <int BITS>
+__host__ __device__ constexpr size_t smem_layout_end(uint32_t base) {
+  return (((size_t)base + Ring<BITS>::BYTES + 0xFFFF) & ~(size_t)0xFFFF) - base + kLutBytes + kMaxSplitPages * 4 +
+         kWarps * Ring<BITS>::S * 8 + 64 + 16;
+}
+static_assert(kMergeFloats * 4 <= Ring<4>::BYTES && kMergeFloats * 4 <= Ring<3>::BYTES, "merge buffer must fit the rings");
 
 // ---------------------------------------------------------------------------------------
 // PTX helpers
@@ -77,27 +96,34 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return d;
 }
 
-__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
+__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
 }
-__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
+__device__ __forceinline__ void mbar_expect_tx(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ uint32_t ldg_stream4(const void* p) {
-  uint32_t r;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
+__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok;
 }
-__device__ __forceinline__ uint32_t ldg_stream2(const void* p) {
-  unsigned short r;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
-  return r;
+// Polls an mbarrier phase at most kWaitLimit times; false if it never completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
+  for (int i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(addr, parity)) return true;
+  return false;
 }
+// 1-D bulk copy global -> this CTA's shared memory (TMA), completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
@@ -160,11 +186,18 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Raw tile data of one lane (lane = 4g + t):
-//   K rows g and g+8, the 32 dims 32t..32t+31 of each;
-//   V tokens 2t, 2t+1, 2t+8, 2t+9, the 16 dims 16g..16g+15 of each;
-//   the K and V norms of tokens g and g+8.
+// Raw tile data of one lane (lane = 4g + t), read from a staged tile in shared memory.
+// The MMA rows of a tile map to its tokens through rho(r) = r ^ ((r >> 1) & 1), a
+// permutation chosen so that the staged reads are conflict-free for K and at most 2-way for V:
+//   K rows g and g+8 -> tokens rho(g), rho(g) + 8, the 32 dims 32t..32t+31 of each;
+//   V k-slots 2t, 2t+1, 2t+8, 2t+9 -> tokens rho(2t), rho(2t+1), rho(2t) + 8, rho(2t+1) + 8,
+//     the 16 dims 16g..16g+15 of each;
+//   the K and V norms of tokens rho(g) and rho(g) + 8.
+// Both contractions sum over tokens, so any permutation gives the same result as long as the
+// score rows, the norms, the masks and the P^T operand use the same one.
 // ---------------------------------------------------------------------------------------
+__device__ __forceinline__ int rho(int r) { return r ^ ((r >> 1) & 1); }
+
 template <int BITS>
 struct Raw;
 
@@ -172,7 +205,7 @@ template <>
 struct Raw<4> {
   uint4 k[2];        // 16 bytes = 32 codes per K row
   uint2 v[4];        // 8 bytes = 16 codes per V token
-  uint32_t nk, nv;   // fp16 norms of tokens g (low) and g+8 (high)
+  uint32_t nk, nv;   // fp16 norms of the two K rows' tokens (low, high)
 };
 template <>
 struct Raw<3> {
@@ -182,33 +215,36 @@ struct Raw<3> {
 };
 
 template <int BITS>
-__device__ __forceinline__ void load_tile(Raw<BITS>& r, const uint8_t* chunk, int off, int P, int g, int t) {
+__device__ __forceinline__ void load_stage(Raw<BITS>& r, const uint8_t* st, int g, int t) {
   constexpr int vb = BITS * 16;
-  const uint8_t* kb = chunk + (size_t)off * vb;
-  const uint8_t* vbp = chunk + (size_t)(P + off) * vb;
-  const uint8_t* nb = chunk + (size_t)2 * P * vb + 2 * off;
-  const int vt[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+  const uint8_t* vbp = st + 16 * vb;
+  const uint8_t* nb = st + 32 * vb;
+  const int rk = rho(g);
+  const int va = rho(2 * t), vbt = rho(2 * t + 1);
+  const int vt[4] = {va, vbt, va + 8, vbt + 8};
   if constexpr (BITS == 4) {
-    r.k[0] = ldg_stream16(kb + g * 64 + 16 * t);
-    r.k[1] = ldg_stream16(kb + (g + 8) * 64 + 16 * t);
+    r.k[0] = *reinterpret_cast<const uint4*>(st + rk * 64 + 16 * t);
+    r.k[1] = *reinterpret_cast<const uint4*>(st + (rk + 8) * 64 + 16 * t);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) r.v[i] = ldg_stream8(vbp + vt[i] * 64 + 8 * g);
+    for (int i = 0; i < 4; ++i) r.v[i] = *reinterpret_cast<const uint2*>(vbp + vt[i] * 64 + 8 * g);
   } else {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-      for (int w = 0; w < 3; ++w) r.k[rr][w] = ldg_stream4(kb + (g + 8 * rr) * 48 + 12 * t + 4 * w);
+      for (int w = 0; w < 3; ++w)
+        r.k[rr][w] = *reinterpret_cast<const uint32_t*>(st + (rk + 8 * rr) * 48 + 12 * t + 4 * w);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      r.v[i][0] = ldg_stream4(vbp + vt[i] * 48 + 12 * (g >> 1) + 4 * (g & 1));
-      r.v[i][1] = ldg_stream4(vbp + vt[i] * 48 + 12 * (g >> 1) + 8);
+      r.v[i][0] = *reinterpret_cast<const uint32_t*>(vbp + vt[i] * 48 + 12 * (g >> 1) + 4 * (g & 1));
+      r.v[i][1] = *reinterpret_cast<const uint32_t*>(vbp + vt[i] * 48 + 12 * (g >> 1) + 8);
     }
   }
-  r.nk = ldg_stream2(nb + 2 * g) | (ldg_stream2(nb + 2 * (g + 8)) << 16);
-  r.nv = ldg_stream2(nb + 2 * P + 2 * g) | (ldg_stream2(nb + 2 * P + 2 * (g + 8)) << 16);
+  const uint16_t* n16 = reinterpret_cast<const uint16_t*>(nb);
+  r.nk = (uint32_t)n16[rk] | ((uint32_t)n16[rk + 8] << 16);
+  r.nv = (uint32_t)n16[16 + rk] | ((uint32_t)n16[16 + rk + 8] << 16);
 }
 
-// A operand of S^T = K~ q~^T for k-chunk kc: rows g / g+8 hold tokens g / g+8, k-slots
+// A operand of S^T = K~ q~^T for k-chunk kc: rows g / g+8 hold the two K rows, k-slots
 // 2t,2t+1 hold dim pair 2kc and 2t+8,2t+9 dim pair 2kc+1 of the lane's 32 dims.
 // 4-bit: pair j is byte j of the row's 16 bytes.
 // 3-bit: X0 = W0.lo | W2.hi (T1, pairs 2k), X1 = W2.lo | W0.hi (T2, pairs 2k+1),
@@ -265,7 +301,7 @@ __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const
 }
 
 // A operand of O^T += V~^T P^T for m-tile mt: rows g / g+8 hold dims 16g+2mt / 16g+2mt+1,
-// k-slots 2t,2t+1 tokens (2t, 2t+1) and 2t+8,2t+9 tokens (2t+8, 2t+9).  Index bytes carry one
+// k-slots 2t,2t+1 and 2t+8,2t+9 the lane's two V token pairs.  Index bytes carry one
 // dim of two tokens, so the two tokens' code words are interleaved first.
 template <int BITS>
 __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, uint32_t pb0, uint32_t pb1,
@@ -347,19 +383,25 @@ __device__ __forceinline__ ItemInfo decode_item(int item, const Geometry& g, con
 
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
-  extern __shared__ __align__(16) uint8_t smem[];
+attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_bytes) {
+  using R = Ring<BITS>;
+  extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t dyn_base = (uint32_t)__cvta_generic_to_shared(smem);
-  const uint32_t lut_addr = (dyn_base + 0xFFFFu) & ~0xFFFFu;   // first 64 KB-aligned address
+  if (smem_layout_end<BITS>(dyn_base) > (size_t)smem_bytes) {  // unexpected reserved shared memory
+    if (threadIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
+    return;
+  }
+  uint8_t* rings = smem;
+  const uint32_t lut_addr = (dyn_base + R::BYTES + 0xFFFFu) & ~0xFFFFu;
   uint32_t* lut_words = reinterpret_cast<uint32_t*>(smem + (lut_addr - dyn_base));
-  uint8_t* high = smem + (lut_addr - dyn_base) + kLutBytes;
-  float* merge = reinterpret_cast<float*>(high);
-  int* page_ids = reinterpret_cast<int*>(high + (size_t)kMergeFloats * 4);
-  float* cb = reinterpret_cast<float*>(page_ids + kMaxSplitPages);
+  uint8_t* tail = smem + (lut_addr - dyn_base) + kLutBytes;
+  int* page_ids = reinterpret_cast<int*>(tail);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(tail + kMaxSplitPages * 4);
+  float* cb = reinterpret_cast<float*>(mbar + kWarps * R::S);
+  int* s_item = reinterpret_cast<int*>(cb + 16);
+  float* merge = reinterpret_cast<float*>(rings);  // aliases the rings between items
 
-  build_lut<BITS>(lut_words, g.centroids, cb);
-  __syncthreads();
-
+  build_lut<BITS>(lut_words, g.centroids, cb);  // ends with the centroids staged; synced below
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const uint32_t key1 = lut_addr | ((uint32_t)lane * 4u);
@@ -367,11 +409,19 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
   const int P = g.page_size;
   const int tiles_per_page = P / 16;
   const __half* qh = reinterpret_cast<const __half*>(a.q);
+  uint8_t* my_ring = rings + (size_t)warp * R::S * R::SB;
+  const uint32_t ring_addr = dyn_base + (uint32_t)(warp * R::S * R::SB);
+  const uint32_t mbar_addr = (uint32_t)__cvta_generic_to_shared(mbar + warp * R::S);
+  if (lane == 0) {
+    for (int st = 0; st < R::S; ++st) mbar_init(mbar_addr + 8 * st, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  uint32_t phase = 0;  // bit st: parity of the next completion of stage st
+  bool broken = false;  // a staged copy never completed: stop using the ring
 
-  __shared__ int s_item;
-  if (threadIdx.x == 0) s_item = atomicAdd(a.counters, 1);
+  if (threadIdx.x == 0) *s_item = atomicAdd(a.counters, 1);
   __syncthreads();
-  for (int item = s_item; item < n_items;) {
+  for (int item = *s_item; item < n_items;) {
     const ItemInfo it = decode_item(item, g, a);
     int len = a.seq_lens[it.b];
     const int cap = a.max_pages * P;
@@ -385,9 +435,9 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
     if (p1 > npages) p1 = npages;
     if (p0 >= p1) {  // uniform across the CTA: the combine never reads this split
       __syncthreads();
-      if (threadIdx.x == 0) s_item = atomicAdd(a.counters, 1);
+      if (threadIdx.x == 0) *s_item = atomicAdd(a.counters, 1);
       __syncthreads();
-      item = s_item;
+      item = *s_item;
       continue;
     }
 
@@ -465,26 +515,54 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
 
     const int tile0 = p0 * tiles_per_page, tile1 = p1 * tiles_per_page;
     const size_t head_off = (size_t)it.h * g.page_bytes;
-    int tile = tile0 + warp;
-    Raw<BITS> cur, nxt;
-    if (tile < tile1) {
+    const int first = tile0 + warp;                       // this warp's tiles: first + k * kWarps
+    const int n_w = (first < tile1 && !broken) ? (tile1 - 1 - first) / kWarps + 1 : 0;
+    // Lane 0 stages the warp's k-th tile into stage k % S with TMA bulk copies: one copy when a
+    // page is one tile, else K codes, V codes and the two norm runs of the tile.
+    auto issue = [&](int k) {
+      const int tile = first + k * kWarps, st = k % R::S;
       const int pi = tile / tiles_per_page - p0, off = (tile % tiles_per_page) * 16;
-      load_tile<BITS>(cur, a.pages + (size_t)page_ids[pi] * g.num_kv_heads * g.page_bytes + head_off, off, P, gq, tq);
-    }
-    for (; tile < tile1; tile += kWarps) {
-      const int tn = tile + kWarps;
-      if (tn < tile1) {
-        const int pi = tn / tiles_per_page - p0, off = (tn % tiles_per_page) * 16;
-        load_tile<BITS>(nxt, a.pages + (size_t)page_ids[pi] * g.num_kv_heads * g.page_bytes + head_off, off, P, gq,
-                        tq);
+      const uint8_t* chunk = a.pages + (size_t)page_ids[pi] * g.num_kv_heads * g.page_bytes + head_off;
+      const uint32_t dst = ring_addr + st * R::SB, mb = mbar_addr + 8 * st;
+      mbar_expect_tx(mb, R::SB);
+      if (P == 16) {
+        bulk_g2s(dst, chunk, R::SB, mb);
+      } else {
+        bulk_g2s(dst, chunk + (size_t)off * R::VB, 16 * R::VB, mb);
+        bulk_g2s(dst + 16 * R::VB, chunk + (size_t)(P + off) * R::VB, 16 * R::VB, mb);
+        bulk_g2s(dst + 32 * R::VB, chunk + (size_t)2 * P * R::VB + 2 * off, 32, mb);
+        bulk_g2s(dst + 32 * R::VB + 32, chunk + (size_t)2 * P * R::VB + 2 * P + 2 * off, 32, mb);
       }
-      // ---- scores (base 2) for tokens pos0 + gq and pos0 + gq + 8, query columns 2tq, 2tq+1
+    };
+    if (lane == 0 && n_w > 0) {
+      fence_proxy_async();
+      for (int k = 0; k < min(R::S, n_w); ++k) issue(k);
+    }
+    int consumed = 0;
+    for (int k = 0; k < n_w; ++k) {
+      const int st = k % R::S;
+      const bool ok = mbar_wait_bounded(mbar_addr + 8 * st, (phase >> st) & 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        broken = true;
+        break;
+      }
+      phase ^= 1u << st;
+      consumed = k + 1;
+      Raw<BITS> cur;
+      load_stage<BITS>(cur, my_ring + st * R::SB, gq, tq);
+      __syncwarp();
+      if (k + R::S < n_w && lane == 0) {  // refill this stage while the tile is processed
+        fence_proxy_async();
+        issue(k + R::S);
+      }
+      const int tile = first + k * kWarps;
+      // ---- scores (base 2) of the lane's two K rows for query columns 2tq, 2tq+1
       float s[4];
       qk_tile<BITS>(s, cur, qf, key1, key2);
       const int pos0 = tile * 16;
       const float nk0 = half_bits_to_float(cur.nk & 0xffffu), nk1 = half_bits_to_float(cur.nk >> 16);
       const float nv0 = half_bits_to_float(cur.nv & 0xffffu), nv1 = half_bits_to_float(cur.nv >> 16);
-      const int r0 = pos0 + gq, r1 = pos0 + gq + 8;
+      const int r0 = pos0 + rho(gq), r1 = r0 + 8;
       // Tiles wholly inside every column's visible range (all but the last one or two of a
       // sequence) skip the per-element mask.
       const bool interior = __all_sync(0xffffffffu, pos0 + 15 <= min(last_pos[0], last_pos[1]));
@@ -538,10 +616,17 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
       const uint32_t pb0 = movmatrix_t(pack_half2(q0, q1));
       const uint32_t pb1 = movmatrix_t(pack_half2(q2, q3));
       pv_tile<BITS>(o, cur, pb0, pb1, key1, key2, gq);
-      cur = nxt;
+    }
+    if (broken) {
+      // A copy never landed: flag it, wait (bounded) for the copies still in flight so none
+      // lands in a reused buffer, and leave the ring alone from now on.
+      if (lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
+      for (int k = consumed; k < min(n_w, consumed + R::S); ++k)
+        mbar_wait_bounded(mbar_addr + 8 * (k % R::S), (phase >> (k % R::S)) & 1u);
     }
 
     // ---- merge the warps' partial states of this item ----
+    __syncthreads();  // every warp is done with its ring, which the merge buffer aliases
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       float l = l_run[c];
@@ -592,9 +677,9 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items) {
       }
     }
     __syncthreads();  // merge buffer and page ids are reused by the next item
-    if (threadIdx.x == 0) s_item = atomicAdd(a.counters, 1);
+    if (threadIdx.x == 0) *s_item = atomicAdd(a.counters, 1);
     __syncthreads();
-    item = s_item;
+    item = *s_item;
   }
   // The last CTA to finish re-arms the work counter for the next launch on this stream.
   // Nothing waits on it: every CTA has already drawn an out-of-range item.
@@ -672,12 +757,21 @@ attn_combine_kernel(const Geometry g, const AttnArgs a, int nsplit) {
 
 }  // namespace
 
-size_t attention_smem_bytes() { return kSmemBytes; }
+// Dynamic shared memory of a variant: its layout end for a window that starts right after the
+// driver's reserved shared memory (the kernels declare no static shared memory).
+static int smem_bytes_for(int bits) {
+  int dev = 0, reserved = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) reserved = 0;
+  return (int)(bits == 4 ? smem_layout_end<4>((uint32_t)reserved) : smem_layout_end<3>((uint32_t)reserved));
+}
+
+size_t attention_smem_bytes() { return (size_t)smem_bytes_for(4) > (size_t)smem_bytes_for(3) ? smem_bytes_for(4) : smem_bytes_for(3); }
 
 cudaError_t attention_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(attn_splitk_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(attn_splitk_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for(3));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_splitk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  return cudaFuncSetAttribute(attn_splitk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for(4));
 }
 
 cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream,
@@ -688,10 +782,11 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas,
   if (n_items > 0) {
     const int grid = (int)(n_items < num_ctas ? n_items : num_ctas);
     if (ev_start) cudaEventRecord(ev_start, stream);
+    const int smem = smem_bytes_for(g.bits);
     if (g.bits == 4)
-      attn_splitk_kernel<4><<<grid, kThreads, kSmemBytes, stream>>>(g, a, (int)n_items);
+      attn_splitk_kernel<4><<<grid, kThreads, smem, stream>>>(g, a, (int)n_items, smem);
     else
-      attn_splitk_kernel<3><<<grid, kThreads, kSmemBytes, stream>>>(g, a, (int)n_items);
+      attn_splitk_kernel<3><<<grid, kThreads, smem, stream>>>(g, a, (int)n_items, smem);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev_end) cudaEventRecord(ev_end, stream);

@@ -18,7 +18,7 @@ import torch
 from . import build as _build
 
 RQ_OK, RQ_ERR_INVALID, RQ_ERR_UNSUPPORTED, RQ_ERR_CUDA, RQ_ERR_CAPACITY = 0, 1, 2, 3, 4
-RQ_STATUS_BAD_PAGE, RQ_STATUS_BAD_SLOT, RQ_STATUS_BAD_LEN, RQ_STATUS_NORM_OVERFLOW = 1, 2, 4, 8
+RQ_STATUS_BAD_PAGE, RQ_STATUS_BAD_SLOT, RQ_STATUS_BAD_LEN, RQ_STATUS_NORM_OVERFLOW, RQ_STATUS_TIMEOUT = 1, 2, 4, 8, 16
 RQ_PLANAR, RQ_ISO = 0, 1
 HEAD_DIM = 128
 
