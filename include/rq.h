@@ -30,7 +30,10 @@
  *   page pool   : device bytes [num_pages][num_kv_heads][page_bytes]; the chunk of
  *                 (page, kv head) is   K codes [P][vb] | V codes [P][vb] | K norms fp16 [P] |
  *                 V norms fp16 [P],  vb = head_dim * bits / 8, page_bytes = P * (2 vb + 4).
- *   4-bit codes : byte j = code[2j] | code[2j+1] << 4.
+ *   4-bit codes : byte j = code[2j] | code[2j+1] << 4.  In the V-codes section of a chunk,
+ *                 tokens are stored as pairs: pair p = tokens (2p, 2p+1) fills 128 bytes and the
+ *                 8 bytes of 16-dim group c of token 2p + h sit at 16 * (c ^ (2p mod 8)) + 8h.
+ *                 K codes, and 3-bit V codes, are stored token after token.
  *   3-bit codes : per 32-dim group w, 12 bytes at 12w = little-endian words W0, W1, W2:
  *                 W0 bits 2i.. = code[32w+i] & 3, W1 bits 2i.. = code[32w+16+i] & 3
  *                 (i = 0..15), W2 bit p(i) = code[32w+i] >> 2 with i = 16h + 4k + r and

@@ -75,6 +75,8 @@ def lib():
             L.rqo_dequant.argtypes = [c_int, c_int, c_int, P(ctypes.c_float), P(ctypes.c_float),
                                       P(ctypes.c_uint8), ctypes.c_uint16, P(c_dbl)]
             L.rqo_dequant.restype = None
+            L.rqo_v_unit_offset.argtypes = [c_int, c_int, c_int, c_int]
+            L.rqo_v_unit_offset.restype = c_sz
             L.rqo_page_bytes.argtypes = [c_int, c_int, c_int]
             L.rqo_page_bytes.restype = c_sz
             L.rqo_append.argtypes = [c_int, c_int, c_int, c_int, c_int, P(ctypes.c_float), P(ctypes.c_float),
@@ -217,6 +219,19 @@ def dequant(mode: int, bits: int, rot_head, centroids, codes, n16: int):
 # ---------------------------------------------------------------------------------------
 # Paged cache and attention
 # ---------------------------------------------------------------------------------------
+def v_unit_offset(bits: int, off: int, unit: int, d: int = 128) -> int:
+    """Byte offset of 8-byte unit `unit` of V token `off` inside a chunk's V-codes section."""
+    return int(lib().rqo_v_unit_offset(bits, d, off, unit))
+
+
+def v_codes_of(bits: int, chunk: np.ndarray, page_size: int, off: int, d: int = 128) -> np.ndarray:
+    """The packed codes of V token `off` gathered from a chunk."""
+    vb = vector_bytes(bits, d)
+    base = page_size * vb
+    return np.concatenate([chunk[base + v_unit_offset(bits, off, u, d):base + v_unit_offset(bits, off, u, d) + 8]
+                           for u in range(vb // 8)])
+
+
 def page_bytes(bits: int, page_size: int, d: int = 128) -> int:
     return int(lib().rqo_page_bytes(bits, page_size, d))
 

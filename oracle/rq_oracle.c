@@ -348,7 +348,32 @@ void rqo_dequant(int mode, int bits, int d, const float *rot, const float *centr
 /* Paged cache.  One chunk per (page, kv head), at byte (page * Hkv + head) * page_bytes:   */
 /*   K codes [P][vb] | V codes [P][vb] | K norms fp16 [P] | V norms fp16 [P]               */
 /* with vb = d * bits / 8.  Slot s holds token offset s % P of page s / P.                 */
+/* K codes, and 3-bit V codes, are stored token after token.  4-bit V codes (d = 128) are   */
+/* stored as token pairs: pair p = tokens (2p, 2p+1) fills 128 bytes; its 8-byte unit for  */
+/* 16-dim group c of token 2p + h sits at byte 16 * (c ^ (2p mod 8)) + 8h of the pair.      */
 /* ------------------------------------------------------------------------------------- */
+
+/* Byte offset, inside the V-codes section, of the vb bytes (or the 8-byte unit `unit` of  */
+/* a 4-bit d = 128 vector) of token `off`. */
+static size_t v_unit_offset(int bits, int d, int off, int unit) {
+  size_t vb = rqo_vector_bytes(bits, d);
+  if (bits != 4 || d != 128) return (size_t)off * vb + (size_t)unit * 8;
+  int pair = off / 2, h = off % 2;
+  return (size_t)pair * 128 + (size_t)16 * (unit ^ ((2 * pair) % 8)) + (size_t)8 * h;
+}
+
+static void put_v(int bits, int d, uint8_t *vsec, int off, const uint8_t *packed) {
+  size_t vb = rqo_vector_bytes(bits, d);
+  for (size_t u = 0; u < vb / 8; ++u) memcpy(vsec + v_unit_offset(bits, d, off, (int)u), packed + 8 * u, 8);
+}
+
+static void get_v(int bits, int d, const uint8_t *vsec, int off, uint8_t *packed) {
+  size_t vb = rqo_vector_bytes(bits, d);
+  for (size_t u = 0; u < vb / 8; ++u) memcpy(packed + 8 * u, vsec + v_unit_offset(bits, d, off, (int)u), 8);
+}
+
+/* Exposed for tests: byte offset of 8-byte unit `unit` of V token `off` in its section. */
+size_t rqo_v_unit_offset(int bits, int d, int off, int unit) { return v_unit_offset(bits, d, off, unit); }
 
 size_t rqo_page_bytes(int bits, int page_size, int d) {
   return (size_t)page_size * (2 * rqo_vector_bytes(bits, d) + 4);
@@ -375,7 +400,9 @@ void rqo_append(int mode, int bits, int d, int hkv, int page_size,
       rqo_pack(bits, d, codes, chunk + off * vb);
       rqo_encode(mode, bits, d, rot_v + (size_t)h * d, boundaries, v + src, codes, &nv,
                  margin_v ? margin_v + src : NULL);
-      rqo_pack(bits, d, codes, chunk + page_size * vb + off * vb);
+      uint8_t packed[1024];
+      rqo_pack(bits, d, codes, packed);
+      put_v(bits, d, chunk + page_size * vb, off, packed);
       uint8_t *norms = chunk + 2 * page_size * vb;
       norms[2 * off] = (uint8_t)(nk & 0xff);
       norms[2 * off + 1] = (uint8_t)(nk >> 8);
@@ -399,7 +426,9 @@ static void load_token(int mode, int bits, int d, int hkv, int page_size, const 
   uint8_t codes[1024];
   rqo_unpack(bits, d, chunk + off * vb, codes);
   rqo_dequant(mode, bits, d, rot_k + (size_t)h * d, centroids, codes, nk, kh);
-  rqo_unpack(bits, d, chunk + page_size * vb + off * vb, codes);
+  uint8_t packed[1024];
+  get_v(bits, d, chunk + page_size * vb, off, packed);
+  rqo_unpack(bits, d, packed, codes);
   rqo_dequant(mode, bits, d, rot_v + (size_t)h * d, centroids, codes, nv, vh);
 }
 

@@ -131,7 +131,15 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
         uint32_t word = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) word |= (uint32_t)code[e] << (4 * e);
-        *reinterpret_cast<uint32_t*>(dst + 4 * j) = word;
+        if (half == 0) {
+          *reinterpret_cast<uint32_t*>(dst + 4 * j) = word;
+        } else {
+          // V: token pairs (2p, 2p+1) share 128 bytes; the 8-byte unit of 16-dim group c of
+          // token 2p + h sits at 16 * (c ^ (2p mod 8)) + 8h.  Lane j holds half of unit j / 2.
+          const int pair = off >> 1, hv = off & 1, c = j >> 1;
+          uint8_t* vsec = chunk + (size_t)g.page_size * vb;
+          *reinterpret_cast<uint32_t*>(vsec + pair * 128 + 16 * (c ^ ((2 * pair) & 7)) + 8 * hv + 4 * (j & 1)) = word;
+        }
       } else {
         // Lane j covers dims 8m..8m+7 of 32-dim group w = j/4 (m = j%4).  Its low bits are
         // bytes 2m, 2m+1 of the group's W0|W1; its high bits fill half of bytes 2(m&1) and

@@ -33,29 +33,55 @@ constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kLutBytes = 256 * 256;          // 256 index bytes x (2 tables x 32 lanes x 4 B)
 constexpr int kMaxSplitPages = 1024;          // page ids staged per item
-constexpr int kMergeFloats = kWarps * 8 * kPartialStride;
 constexpr int kWaitLimit = 1 << 22;           // bounded mbarrier polling (about a second)
 
-// Per-warp ring of staged 16-token tiles.  A stage holds one tile exactly as a 16-token page
-// chunk is laid out: K codes [16][vb] | V codes [16][vb] | K norms fp16 [16] | V norms fp16 [16].
+// Staged tiles.  A slot holds one 16-token tile exactly as a 16-token page chunk is laid out:
+// K codes [16][vb] | V codes [16][vb] | K norms fp16 [16] | V norms fp16 [16].  Each warp owns
+// kSlots slots used as kSlots/2 stages of two consecutive tiles (32 tokens); one mbarrier per
+// stage.  The slots sit on both sides of the 64 KB-aligned lookup table (see smem_plan).
 template <int BITS>
 struct Ring {
   static constexpr int VB = BITS * 16;
-  static constexpr int SB = 32 * VB + 64;           // stage bytes: 2112 (4-bit), 1600 (3-bit)
-  static constexpr int S = BITS == 4 ? 3 : 4;       // stages per warp
-  static constexpr int BYTES = kWarps * S * SB;     // 101,376 / 102,400
+  static constexpr int SB = 32 * VB + 64;     // slot bytes: 2112 (4-bit), 1600 (3-bit)
 };
+constexpr int kSlots = 4;                     // per warp: 2 stages x 2 tiles
+constexpr int kStages = kSlots / 2;
+constexpr int kSlotsTotal = kWarps * kSlots;  // 64
+constexpr int kMergeHalfBytes = kWarps * 4 * kPartialStride * 4;  // 4 query columns of all warps
 
-// Dynamic shared memory, from the start of the CTA's dynamic window at shared address `base`:
-//   rings [16 warps][S][SB]  (the warps' merge buffer aliases them between items)
-//   lookup table, 64 KB, at the first 64 KB-aligned address after the rings
-//   page ids int[1024] | mbarriers u64[16][S] | centroids float[16] | item slot int[4]
+// Shared-memory plan for a CTA whose dynamic window starts at shared address `base`:
+//   [base, lut)          low slots (as many whole slots as fit), or nothing
+//   [lut, lut + 64 KB)   lookup table; lut = first 64 KB-aligned address >= base
+//   [lut + 64 KB, ...)   the remaining slots, page ids int[1024], mbarriers u64[16][2],
+//                        centroids float[16], item slot int[4]
+// Between items the two halves of the merge buffer (query columns 0-3 and 4-7) reuse slot
+// space: the low region when it holds a half, else the high slots.
+struct SmemPlan {
+  uint32_t lut;        // shared address of the table
+  int n_lo;            // slots below the table
+  uint32_t hi;         // shared address of the first high slot
+  uint32_t tail;       // shared address of the page-id array
+  uint32_t merge_lo;   // shared address of merge half 0 (columns 0-3)
+  uint32_t merge_hi;   // shared address of merge half 1 (columns 4-7)
+  uint32_t end;        // one past the last byte used
+};
 template <int BITS>
-__host__ __device__ constexpr size_t smem_layout_end(uint32_t base) {
-  return (((size_t)base + Ring<BITS>::BYTES + 0xFFFF) & ~(size_t)0xFFFF) - base + kLutBytes + kMaxSplitPages * 4 +
-         kWarps * Ring<BITS>::S * 8 + 64 + 16;
+__host__ __device__ constexpr SmemPlan smem_plan(uint32_t base) {
+  SmemPlan p{};
+  p.lut = (base + 0xFFFFu) & ~0xFFFFu;
+  int n_lo = (int)((p.lut - base) / Ring<BITS>::SB);
+  if (n_lo > kSlotsTotal) n_lo = kSlotsTotal;
+  p.n_lo = n_lo;
+  p.hi = p.lut + kLutBytes;
+  const uint32_t hi_bytes = (uint32_t)(kSlotsTotal - n_lo) * Ring<BITS>::SB;
+  const bool lo_merge = (uint32_t)n_lo * Ring<BITS>::SB >= (uint32_t)kMergeHalfBytes;
+  p.merge_lo = lo_merge ? base : p.hi;
+  p.merge_hi = lo_merge ? p.hi : p.hi + kMergeHalfBytes;
+  const uint32_t hi_need = lo_merge ? kMergeHalfBytes : 2 * kMergeHalfBytes;
+  p.tail = p.hi + (hi_bytes > hi_need ? hi_bytes : hi_need);
+  p.end = p.tail + kMaxSplitPages * 4 + kWarps * kStages * 8 + 64 + 16;
+  return p;
 }
-static_assert(kMergeFloats * 4 <= Ring<4>::BYTES && kMergeFloats * 4 <= Ring<3>::BYTES, "merge buffer must fit the rings");
 
 // ---------------------------------------------------------------------------------------
 // PTX helpers
@@ -187,8 +213,9 @@ __device__ __forceinline__ float ex2(float x) {
 
 // ---------------------------------------------------------------------------------------
 // Raw tile data of one lane (lane = 4g + t), read from a staged tile in shared memory.
-// The MMA rows of a tile map to its tokens through rho(r) = r ^ ((r >> 1) & 1), a
-// permutation chosen so that the staged reads are conflict-free for K and at most 2-way for V:
+// The MMA rows of a tile map to its tokens through rho(r): the identity for 4-bit codes, whose
+// V token pairs are stored swizzled, and r ^ ((r >> 1) & 1) for 3-bit codes, a permutation
+// chosen so that the staged reads are conflict-free for K and at most 2-way for V:
 //   K rows g and g+8 -> tokens rho(g), rho(g) + 8, the 32 dims 32t..32t+31 of each;
 //   V k-slots 2t, 2t+1, 2t+8, 2t+9 -> tokens rho(2t), rho(2t+1), rho(2t) + 8, rho(2t+1) + 8,
 //     the 16 dims 16g..16g+15 of each;
@@ -196,7 +223,10 @@ __device__ __forceinline__ float ex2(float x) {
 // Both contractions sum over tokens, so any permutation gives the same result as long as the
 // score rows, the norms, the masks and the P^T operand use the same one.
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ int rho(int r) { return r ^ ((r >> 1) & 1); }
+template <int BITS>
+__device__ __forceinline__ int rho(int r) {
+  return BITS == 4 ? r : (r ^ ((r >> 1) & 1));
+}
 
 template <int BITS>
 struct Raw;
@@ -219,15 +249,22 @@ __device__ __forceinline__ void load_stage(Raw<BITS>& r, const uint8_t* st, int 
   constexpr int vb = BITS * 16;
   const uint8_t* vbp = st + 16 * vb;
   const uint8_t* nb = st + 32 * vb;
-  const int rk = rho(g);
-  const int va = rho(2 * t), vbt = rho(2 * t + 1);
-  const int vt[4] = {va, vbt, va + 8, vbt + 8};
+  const int rk = rho<BITS>(g);
   if constexpr (BITS == 4) {
     r.k[0] = *reinterpret_cast<const uint4*>(st + rk * 64 + 16 * t);
     r.k[1] = *reinterpret_cast<const uint4*>(st + (rk + 8) * 64 + 16 * t);
+    // V token pairs (2t, 2t+1) and (2t+8, 2t+9) are 128-byte pair rows t and t+4; the lane's
+    // 16-dim group g of both tokens is one 16-byte unit, at 16 * (g ^ 2t mod 8) in either row.
 #pragma unroll
-    for (int i = 0; i < 4; ++i) r.v[i] = *reinterpret_cast<const uint2*>(vbp + vt[i] * 64 + 8 * g);
+    for (int i = 0; i < 2; ++i) {
+      const int pair = t + 4 * i;
+      const uint4 u = *reinterpret_cast<const uint4*>(vbp + pair * 128 + 16 * (g ^ ((2 * pair) & 7)));
+      r.v[2 * i] = make_uint2(u.x, u.y);
+      r.v[2 * i + 1] = make_uint2(u.z, u.w);
+    }
   } else {
+    const int va = rho<BITS>(2 * t), vbt = rho<BITS>(2 * t + 1);
+    const int vt[4] = {va, vbt, va + 8, vbt + 8};
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
@@ -387,36 +424,40 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
   using R = Ring<BITS>;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t dyn_base = (uint32_t)__cvta_generic_to_shared(smem);
-  if (smem_layout_end<BITS>(dyn_base) > (size_t)smem_bytes) {  // unexpected reserved shared memory
+  const SmemPlan plan = smem_plan<BITS>(dyn_base);
+  if (plan.end - dyn_base > (uint32_t)smem_bytes) {  // unexpected reserved shared memory
     if (threadIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
     return;
   }
-  uint8_t* rings = smem;
-  const uint32_t lut_addr = (dyn_base + R::BYTES + 0xFFFFu) & ~0xFFFFu;
-  uint32_t* lut_words = reinterpret_cast<uint32_t*>(smem + (lut_addr - dyn_base));
-  uint8_t* tail = smem + (lut_addr - dyn_base) + kLutBytes;
-  int* page_ids = reinterpret_cast<int*>(tail);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(tail + kMaxSplitPages * 4);
-  float* cb = reinterpret_cast<float*>(mbar + kWarps * R::S);
+  auto at = [&](uint32_t addr) { return smem + (addr - dyn_base); };
+  uint32_t* lut_words = reinterpret_cast<uint32_t*>(at(plan.lut));
+  int* page_ids = reinterpret_cast<int*>(at(plan.tail));
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(page_ids + kMaxSplitPages);
+  float* cb = reinterpret_cast<float*>(mbar + kWarps * kStages);
   int* s_item = reinterpret_cast<int*>(cb + 16);
-  float* merge = reinterpret_cast<float*>(rings);  // aliases the rings between items
+  float* const merge_lo = reinterpret_cast<float*>(at(plan.merge_lo));
+  float* const merge_hi = reinterpret_cast<float*>(at(plan.merge_hi));
 
   build_lut<BITS>(lut_words, g.centroids, cb);  // ends with the centroids staged; synced below
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const uint32_t key1 = lut_addr | ((uint32_t)lane * 4u);
+  const uint32_t key1 = plan.lut | ((uint32_t)lane * 4u);
   const uint32_t key2 = key1 + 128u;
   const int P = g.page_size;
   const int tiles_per_page = P / 16;
   const __half* qh = reinterpret_cast<const __half*>(a.q);
-  uint8_t* my_ring = rings + (size_t)warp * R::S * R::SB;
-  const uint32_t ring_addr = dyn_base + (uint32_t)(warp * R::S * R::SB);
-  const uint32_t mbar_addr = (uint32_t)__cvta_generic_to_shared(mbar + warp * R::S);
+  // shared addresses of this warp's slots: stage st uses slots 2st (first tile) and 2st + 1
+  auto slot_of = [&](int i) -> uint32_t {
+    const int sl = warp * kSlots + i;
+    return sl < plan.n_lo ? dyn_base + (uint32_t)(sl * R::SB) : plan.hi + (uint32_t)((sl - plan.n_lo) * R::SB);
+  };
+  const uint32_t slot0 = slot_of(0), slot1 = slot_of(1), slot2 = slot_of(2), slot3 = slot_of(3);
+  const uint32_t mbar_addr = (uint32_t)__cvta_generic_to_shared(mbar + warp * kStages);
   if (lane == 0) {
-    for (int st = 0; st < R::S; ++st) mbar_init(mbar_addr + 8 * st, 1);
+    for (int st = 0; st < kStages; ++st) mbar_init(mbar_addr + 8 * st, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  uint32_t phase = 0;  // bit st: parity of the next completion of stage st
+  uint32_t phase = 0;   // bit st: parity of the next completion of stage st
   bool broken = false;  // a staged copy never completed: stop using the ring
 
   if (threadIdx.x == 0) *s_item = atomicAdd(a.counters, 1);
@@ -513,34 +554,42 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
+    // The split's tiles, taken two at a time: pair q = tiles tile0 + 2q and tile0 + 2q + 1
+    // (the second exists unless the split ends on an odd page); warp w takes pairs w + 16k.
     const int tile0 = p0 * tiles_per_page, tile1 = p1 * tiles_per_page;
+    const int n_pairs = (tile1 - tile0 + 1) / 2;
     const size_t head_off = (size_t)it.h * g.page_bytes;
-    const int first = tile0 + warp;                       // this warp's tiles: first + k * kWarps
-    const int n_w = (first < tile1 && !broken) ? (tile1 - 1 - first) / kWarps + 1 : 0;
-    // Lane 0 stages the warp's k-th tile into stage k % S with TMA bulk copies: one copy when a
-    // page is one tile, else K codes, V codes and the two norm runs of the tile.
+    const int n_w = (warp < n_pairs && !broken) ? (n_pairs - 1 - warp) / kWarps + 1 : 0;
+    // Lane 0 stages the warp's k-th pair into stage k % 2 (slots 2(k%2), 2(k%2)+1): per tile one
+    // bulk copy when a page is one tile, else K codes, V codes and the two norm runs.
     auto issue = [&](int k) {
-      const int tile = first + k * kWarps, st = k % R::S;
-      const int pi = tile / tiles_per_page - p0, off = (tile % tiles_per_page) * 16;
-      const uint8_t* chunk = a.pages + (size_t)page_ids[pi] * g.num_kv_heads * g.page_bytes + head_off;
-      const uint32_t dst = ring_addr + st * R::SB, mb = mbar_addr + 8 * st;
-      mbar_expect_tx(mb, R::SB);
-      if (P == 16) {
-        bulk_g2s(dst, chunk, R::SB, mb);
-      } else {
-        bulk_g2s(dst, chunk + (size_t)off * R::VB, 16 * R::VB, mb);
-        bulk_g2s(dst + 16 * R::VB, chunk + (size_t)(P + off) * R::VB, 16 * R::VB, mb);
-        bulk_g2s(dst + 32 * R::VB, chunk + (size_t)2 * P * R::VB + 2 * off, 32, mb);
-        bulk_g2s(dst + 32 * R::VB + 32, chunk + (size_t)2 * P * R::VB + 2 * P + 2 * off, 32, mb);
+      const int st = k % kStages;
+      const int tA = tile0 + 2 * (warp + k * kWarps);
+      const int nt_pair = tA + 1 < tile1 ? 2 : 1;
+      const uint32_t mb = mbar_addr + 8 * st;
+      mbar_expect_tx(mb, nt_pair * R::SB);
+      for (int h = 0; h < nt_pair; ++h) {
+        const int tile = tA + h;
+        const int pi = tile / tiles_per_page - p0, off = (tile % tiles_per_page) * 16;
+        const uint8_t* chunk = a.pages + (size_t)page_ids[pi] * g.num_kv_heads * g.page_bytes + head_off;
+        const uint32_t dst = st ? (h ? slot3 : slot2) : (h ? slot1 : slot0);
+        if (P == 16) {
+          bulk_g2s(dst, chunk, R::SB, mb);
+        } else {
+          bulk_g2s(dst, chunk + (size_t)off * R::VB, 16 * R::VB, mb);
+          bulk_g2s(dst + 16 * R::VB, chunk + (size_t)(P + off) * R::VB, 16 * R::VB, mb);
+          bulk_g2s(dst + 32 * R::VB, chunk + (size_t)2 * P * R::VB + 2 * off, 32, mb);
+          bulk_g2s(dst + 32 * R::VB + 32, chunk + (size_t)2 * P * R::VB + 2 * P + 2 * off, 32, mb);
+        }
       }
     };
     if (lane == 0 && n_w > 0) {
       fence_proxy_async();
-      for (int k = 0; k < min(R::S, n_w); ++k) issue(k);
+      for (int k = 0; k < min(kStages, n_w); ++k) issue(k);
     }
     int consumed = 0;
     for (int k = 0; k < n_w; ++k) {
-      const int st = k % R::S;
+      const int st = k % kStages;
       const bool ok = mbar_wait_bounded(mbar_addr + 8 * st, (phase >> st) & 1u);
       if (!__all_sync(0xffffffffu, ok)) {
         broken = true;
@@ -548,54 +597,63 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
       }
       phase ^= 1u << st;
       consumed = k + 1;
-      Raw<BITS> cur;
-      load_stage<BITS>(cur, my_ring + st * R::SB, gq, tq);
-      __syncwarp();
-      if (k + R::S < n_w && lane == 0) {  // refill this stage while the tile is processed
-        fence_proxy_async();
-        issue(k + R::S);
-      }
-      const int tile = first + k * kWarps;
-      // ---- scores (base 2) of the lane's two K rows for query columns 2tq, 2tq+1
-      float s[4];
-      qk_tile<BITS>(s, cur, qf, key1, key2);
-      const int pos0 = tile * 16;
-      const float nk0 = half_bits_to_float(cur.nk & 0xffffu), nk1 = half_bits_to_float(cur.nk >> 16);
-      const float nv0 = half_bits_to_float(cur.nv & 0xffffu), nv1 = half_bits_to_float(cur.nv >> 16);
-      const int r0 = pos0 + rho(gq), r1 = r0 + 8;
-      // Tiles wholly inside every column's visible range (all but the last one or two of a
-      // sequence) skip the per-element mask.
-      const bool interior = __all_sync(0xffffffffu, pos0 + 15 <= min(last_pos[0], last_pos[1]));
-      float sc[4];
-      if (interior) {
+      const uint8_t* stA = at(st ? slot2 : slot0);
+      const uint8_t* stB = at(st ? slot3 : slot1);
+      const int pos0 = (tile0 + 2 * (warp + k * kWarps)) * 16;  // first token of the pair
+
+      // ---- scores (base 2) of the lane's four K rows (two per tile) for columns 2tq, 2tq+1
+      float sc[8];  // [tile][row][col]
+      uint32_t nv_bits[2];
+      {
+        Raw<BITS> rk;
+        float s[4];
+        load_stage<BITS>(rk, stA, gq, tq);
+        qk_tile<BITS>(s, rk, qf, key1, key2);
+        nv_bits[0] = rk.nv;
+        const float nk0 = half_bits_to_float(rk.nk & 0xffffu), nk1 = half_bits_to_float(rk.nk >> 16);
         sc[0] = s[0] * nk0;
         sc[1] = s[1] * nk0;
         sc[2] = s[2] * nk1;
         sc[3] = s[3] * nk1;
-      } else {
-        sc[0] = r0 <= last_pos[0] ? s[0] * nk0 : -CUDART_INF_F;
-        sc[1] = r0 <= last_pos[1] ? s[1] * nk0 : -CUDART_INF_F;
-        sc[2] = r1 <= last_pos[0] ? s[2] * nk1 : -CUDART_INF_F;
-        sc[3] = r1 <= last_pos[1] ? s[3] * nk1 : -CUDART_INF_F;
+        load_stage<BITS>(rk, stB, gq, tq);
+        qk_tile<BITS>(s, rk, qf, key1, key2);
+        nv_bits[1] = rk.nv;
+        const float nk2 = half_bits_to_float(rk.nk & 0xffffu), nk3 = half_bits_to_float(rk.nk >> 16);
+        sc[4] = s[0] * nk2;
+        sc[5] = s[1] * nk2;
+        sc[6] = s[2] * nk3;
+        sc[7] = s[3] * nk3;
       }
-      float pw[4], alpha[2];
+      // Pairs wholly inside every column's visible range skip the per-element mask.
+      const bool interior = __all_sync(0xffffffffu, pos0 + 31 <= min(last_pos[0], last_pos[1]));
+      if (!interior) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int pos = pos0 + 16 * (e >> 2) + rho<BITS>(gq) + 8 * ((e >> 1) & 1);
+          if (pos > last_pos[e & 1]) sc[e] = -CUDART_INF_F;
+        }
+      }
+      float alpha[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        float tmax = fmaxf(sc[c], sc[c + 2]);
+        float tmax = fmaxf(fmaxf(sc[c], sc[c + 2]), fmaxf(sc[c + 4], sc[c + 6]));
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
         const float m_new = fmaxf(m_run[c], tmax);
         const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
         alpha[c] = ex2(m_run[c] - m_use);
-        const float p0v = ex2(sc[c] - m_use), p1v = ex2(sc[c + 2] - m_use);
-        l_run[c] = l_run[c] * alpha[c] + p0v + p1v;
+        float lsum = 0.f;
+#pragma unroll
+        for (int e = c; e < 8; e += 2) {
+          sc[e] = ex2(sc[e] - m_use);  // now p; masked entries give 0
+          lsum += sc[e];
+        }
+        l_run[c] = l_run[c] * alpha[c] + lsum;
         m_run[c] = m_new;
-        pw[c] = p0v;
-        pw[c + 2] = p1v;
       }
       // Rescale the accumulators only when some column's running max moved (rare after the
-      // first tiles); alpha is exactly 1 otherwise, so skipping changes nothing.
+      // first pairs); alpha is exactly 1 otherwise, so skipping changes nothing.
       if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
@@ -605,28 +663,43 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
           o[mt][3] *= alpha[1];
         }
       }
-      // P' = p * n_v (zero for masked tokens, whatever their stored norm)
-      float q0 = pw[0] * nv0, q1 = pw[1] * nv0, q2 = pw[2] * nv1, q3 = pw[3] * nv1;
-      if (!interior) {
-        q0 = sc[0] == -CUDART_INF_F ? 0.f : q0;
-        q1 = sc[1] == -CUDART_INF_F ? 0.f : q1;
-        q2 = sc[2] == -CUDART_INF_F ? 0.f : q2;
-        q3 = sc[3] == -CUDART_INF_F ? 0.f : q3;
+      // P' = p * n_v, zero for masked tokens whatever their stored norm; to the B layout.
+      uint32_t pb[2][2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float nva = half_bits_to_float(nv_bits[h] & 0xffffu), nvb = half_bits_to_float(nv_bits[h] >> 16);
+        float q0 = sc[4 * h + 0] * nva, q1 = sc[4 * h + 1] * nva, q2 = sc[4 * h + 2] * nvb, q3 = sc[4 * h + 3] * nvb;
+        if (!interior) {
+          q0 = sc[4 * h + 0] == 0.f ? 0.f : q0;
+          q1 = sc[4 * h + 1] == 0.f ? 0.f : q1;
+          q2 = sc[4 * h + 2] == 0.f ? 0.f : q2;
+          q3 = sc[4 * h + 3] == 0.f ? 0.f : q3;
+        }
+        pb[h][0] = movmatrix_t(pack_half2(q0, q1));
+        pb[h][1] = movmatrix_t(pack_half2(q2, q3));
       }
-      const uint32_t pb0 = movmatrix_t(pack_half2(q0, q1));
-      const uint32_t pb1 = movmatrix_t(pack_half2(q2, q3));
-      pv_tile<BITS>(o, cur, pb0, pb1, key1, key2, gq);
+      // ---- values: read both tiles' V codes, hand the stage back, accumulate
+      Raw<BITS> rvA, rvB;
+      load_stage<BITS>(rvA, stA, gq, tq);
+      load_stage<BITS>(rvB, stB, gq, tq);
+      __syncwarp();
+      if (k + kStages < n_w && lane == 0) {  // refill this stage while the pair is accumulated
+        fence_proxy_async();
+        issue(k + kStages);
+      }
+      pv_tile<BITS>(o, rvA, pb[0][0], pb[0][1], key1, key2, gq);
+      pv_tile<BITS>(o, rvB, pb[1][0], pb[1][1], key1, key2, gq);
     }
     if (broken) {
       // A copy never landed: flag it, wait (bounded) for the copies still in flight so none
       // lands in a reused buffer, and leave the ring alone from now on.
       if (lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
-      for (int k = consumed; k < min(n_w, consumed + R::S); ++k)
-        mbar_wait_bounded(mbar_addr + 8 * (k % R::S), (phase >> (k % R::S)) & 1u);
+      for (int k = consumed; k < min(n_w, consumed + kStages); ++k)
+        mbar_wait_bounded(mbar_addr + 8 * (k % kStages), (phase >> (k % kStages)) & 1u);
     }
 
     // ---- merge the warps' partial states of this item ----
-    __syncthreads();  // every warp is done with its ring, which the merge buffer aliases
+    __syncthreads();  // every warp is done with its slots, which the merge buffer reuses
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       float l = l_run[c];
@@ -635,21 +708,23 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
       l += __shfl_xor_sync(0xffffffffu, l, 16);
       l_run[c] = l;
     }
-    float* mw = merge + (size_t)warp * 8 * kPartialStride;  // [col][132]: m, l, -, -, o[128]
+    // merge half h holds query columns 4h..4h+3 of every warp: [warp][col & 3][132] floats
+    float* mw = (tq >> 1 ? merge_hi : merge_lo) + (size_t)warp * 4 * kPartialStride;
+    const int c0 = (2 * tq) & 3;
     if (gq == 0) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        mw[(2 * tq + c) * kPartialStride + 0] = m_run[c];
-        mw[(2 * tq + c) * kPartialStride + 1] = l_run[c];
+        mw[(c0 + c) * kPartialStride + 0] = m_run[c];
+        mw[(c0 + c) * kPartialStride + 1] = l_run[c];
       }
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       const int d0 = 16 * gq + 2 * mt;
-      mw[(2 * tq) * kPartialStride + 4 + d0] = o[mt][0];
-      mw[(2 * tq + 1) * kPartialStride + 4 + d0] = o[mt][1];
-      mw[(2 * tq) * kPartialStride + 4 + d0 + 1] = o[mt][2];
-      mw[(2 * tq + 1) * kPartialStride + 4 + d0 + 1] = o[mt][3];
+      mw[c0 * kPartialStride + 4 + d0] = o[mt][0];
+      mw[(c0 + 1) * kPartialStride + 4 + d0] = o[mt][1];
+      mw[c0 * kPartialStride + 4 + d0 + 1] = o[mt][2];
+      mw[(c0 + 1) * kPartialStride + 4 + d0 + 1] = o[mt][3];
     }
     __syncthreads();
     {
@@ -658,17 +733,18 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
                               8 * kPartialStride;
       for (int i = threadIdx.x; i < cols * 130; i += kThreads) {
         const int c = i / 130, e = i % 130;
+        const float* mh = (c >> 2 ? merge_hi : merge_lo) + (c & 3) * kPartialStride;
         float M = -CUDART_INF_F;
 #pragma unroll 4
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, merge[((size_t)w * 8 + c) * kPartialStride]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mh[(size_t)w * 4 * kPartialStride]);
         float acc = 0.f;
         if (M != -CUDART_INF_F) {
           const int src = e == 0 ? -1 : (e == 1 ? 1 : 4 + (e - 2));
 #pragma unroll 4
           for (int w = 0; w < kWarps; ++w) {
-            const float* mwp = merge + ((size_t)w * 8 + c) * kPartialStride;
-            const float sc = exp2f(mwp[0] - M);
-            if (src >= 0) acc += mwp[src] * sc;
+            const float* mwp = mh + (size_t)w * 4 * kPartialStride;
+            const float scale = exp2f(mwp[0] - M);
+            if (src >= 0) acc += mwp[src] * scale;
           }
         }
         if (e == 0) dst[c * kPartialStride] = M;
@@ -763,7 +839,8 @@ static int smem_bytes_for(int bits) {
   int dev = 0, reserved = 0;
   cudaGetDevice(&dev);
   if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) reserved = 0;
-  return (int)(bits == 4 ? smem_layout_end<4>((uint32_t)reserved) : smem_layout_end<3>((uint32_t)reserved));
+  const uint32_t base = (uint32_t)reserved;
+  return (int)((bits == 4 ? smem_plan<4>(base).end : smem_plan<3>(base).end) - base);
 }
 
 size_t attention_smem_bytes() { return (size_t)smem_bytes_for(4) > (size_t)smem_bytes_for(3) ? smem_bytes_for(4) : smem_bytes_for(3); }

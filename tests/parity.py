@@ -38,8 +38,10 @@ def compare_chunks(gpu_pages: np.ndarray, ocache: O.Cache, tokens, margins=None,
         g_ch = gpu_pages[page, h]
         o_ch = ocache.chunk(page, h)
         for kv in (0, 1):
-            lo = (kv * P + off) * vb
-            gb, ob = g_ch[lo:lo + vb], o_ch[lo:lo + vb]
+            if kv == 0:
+                gb, ob = g_ch[off * vb:(off + 1) * vb], o_ch[off * vb:(off + 1) * vb]
+            else:
+                gb, ob = O.v_codes_of(bits, g_ch, P, off), O.v_codes_of(bits, o_ch, P, off)
             compared += 128
             if not np.array_equal(gb, ob):
                 gc, oc = O.unpack(bits, gb), O.unpack(bits, ob)

@@ -43,10 +43,13 @@ def _check_sequence(bn, b, out_gpu):
     diff = np.argwhere(gpu != ora)
     in_band = 0
     for (pg, h, byte) in diff:
-        if byte < 2 * P * vb:
-            kv, rem = divmod(int(byte), P * vb)
-            off = rem // vb
-            norm = False
+        if byte < P * vb:
+            kv, off, norm = 0, int(byte) // vb, False
+        elif byte < 2 * P * vb:
+            o = int(byte) - P * vb   # inside the V-codes section: find the token owning it
+            kv, norm = 1, False
+            off = next(t for t in range(P) for u in range(vb // 8)
+                       if O.v_unit_offset(spec.bits, t, u) <= o < O.v_unit_offset(spec.bits, t, u) + 8)
         else:
             kv, rem = divmod(int(byte) - 2 * P * vb, 2 * P)
             off = rem // 2
@@ -65,8 +68,8 @@ def _check_sequence(bn, b, out_gpu):
             continue
         rot = (wl.rot_k if kv == 0 else wl.rot_v)[h]
         codes, _, margin = O.encode(spec.mode, spec.bits, rot, oc.boundaries, x)
-        lo = (kv * P + off) * vb
-        gc = O.unpack(spec.bits, gpu[pg, h, lo:lo + vb])
+        packed = gpu[pg, h, off * vb:(off + 1) * vb] if kv == 0 else O.v_codes_of(spec.bits, gpu[pg, h], P, off)
+        gc = O.unpack(spec.bits, packed)
         bad = np.nonzero(gc != codes)[0]
         assert np.all(margin[bad] < PT.BOUNDARY_BAND), ("code", b, t, h, kv, bad, margin[bad])
         in_band += len(bad)

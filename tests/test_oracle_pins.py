@@ -278,6 +278,23 @@ def test_pack_round_trip_and_sizes(bits):
     assert O.page_bytes(bits, 64) == 64 * (32 * bits + 4)
 
 
+def test_v_placement_fixture():
+    for bits, off, unit, offset in (map(int, r) for r in _rows("v_layout.txt")):
+        assert O.v_unit_offset(bits, off, unit) == offset, (bits, off, unit)
+
+
+@pytest.mark.parametrize("bits,P", [(4, 16), (4, 64), (3, 16)])
+def test_v_placement_is_a_bijection_onto_the_section(bits, P):
+    vb = O.vector_bytes(bits)
+    seen = set()
+    for off in range(P):
+        for u in range(vb // 8):
+            o = O.v_unit_offset(bits, off, u)
+            assert o % 8 == 0 and 0 <= o < P * vb
+            seen.add(o)
+    assert len(seen) == P * vb // 8
+
+
 def test_savings_printed_on_the_pages():
     for bits, pct in ((int(r[0]), int(r[1])) for r in _rows("savings_vs_fp16.txt")):
         saved = 100.0 * (1 - O.vector_bytes(bits, 128) / (128 * 2)) if bits >= 3 else 100.0 * (1 - bits / 16)
@@ -310,7 +327,7 @@ def test_append_places_codes_and_norms_in_the_chunk(bits):
             ck, nk, _ = O.encode(O.ISO, bits, cache.rot_k[h], cache.boundaries, k[t, h])
             cv, nv, _ = O.encode(O.ISO, bits, cache.rot_v[h], cache.boundaries, v[t, h])
             assert np.array_equal(ch[off * vb:(off + 1) * vb], O.pack(bits, ck))
-            assert np.array_equal(ch[16 * vb + off * vb:16 * vb + (off + 1) * vb], O.pack(bits, cv))
+            assert np.array_equal(O.v_codes_of(bits, ch, 16, off), O.pack(bits, cv))
             norms = ch[32 * vb:].view(np.uint16)
             assert norms[off] == nk and norms[16 + off] == nv
     touched = {(int(s) // 16, h) for s in slots[:2] for h in range(2)}
@@ -333,7 +350,7 @@ def _dequantised(cache, bt, lens):
                 off = t % cache.P
                 norms = ch[2 * cache.P * vb:].view(np.uint16)
                 ck = O.unpack(cache.bits, ch[off * vb:(off + 1) * vb])
-                cv = O.unpack(cache.bits, ch[cache.P * vb + off * vb:cache.P * vb + (off + 1) * vb])
+                cv = O.unpack(cache.bits, O.v_codes_of(cache.bits, ch, cache.P, off))
                 K[b, t, h] = O.dequant(cache.mode, cache.bits, cache.rot_k[h], cache.centroids, ck, norms[off])
                 V[b, t, h] = O.dequant(cache.mode, cache.bits, cache.rot_v[h], cache.centroids, cv,
                                        norms[cache.P + off])
