@@ -160,6 +160,20 @@ int rq_verify_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
                         void *out, int32_t *d_status, void *stream);
 
 /*
+ * Speculative tree-verify attention (a draft tree, e.g. top-k > 1 EAGLE trees): like
+ * rq_verify_attention, except that query row j attends to the prefix, positions
+ * 0 .. seq_lens[b] - T - 1, and to draft i (position seq_lens[b] - T + i) exactly when bit i of
+ * tree_mask[b][j] is set -- usually draft j's ancestors and draft j itself.
+ *   tree_mask  device uint64 [B][T], 1 <= T <= 64
+ * A causal chain is tree_mask[b][j] = 2^(j+1) - 1 and gives rq_verify_attention's result.  A row
+ * that sees nothing (empty prefix and mask 0) gives zeros.  Errors as rq_verify_attention, plus
+ * RQ_ERR_INVALID for T > 64 or a NULL mask.
+ */
+int rq_tree_verify_attention(rq_ctx *ctx, const void *q, int T, const uint64_t *tree_mask, const void *kv_pages,
+                             const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
+                             void *out, int32_t *d_status, void *stream);
+
+/*
  * Decode attention that allocates nothing.  The pages have no counterpart to this entry point:
  * it exists for callers that cannot call cudaMalloc -- for example code running inside a
  * serving engine whose memory pool has already reserved the device's free memory (a raw

@@ -88,6 +88,11 @@ def lib():
                                         P(ctypes.c_uint8), P(ctypes.c_int32), c_int, P(ctypes.c_int32), c_int,
                                         P(c_dbl)]
             L.rqo_attention.restype = c_int
+            L.rqo_tree_attention.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int, P(ctypes.c_float),
+                                             P(ctypes.c_float), P(ctypes.c_float), c_dbl, P(ctypes.c_uint16), c_int,
+                                             P(ctypes.c_uint64), P(ctypes.c_uint8), P(ctypes.c_int32), c_int,
+                                             P(ctypes.c_int32), c_int, P(c_dbl)]
+            L.rqo_tree_attention.restype = c_int
             L.rqo_attention_dense.argtypes = [c_int, c_int, c_int, c_dbl, P(ctypes.c_uint16), c_int,
                                               P(ctypes.c_uint16), P(ctypes.c_uint16), c_int, P(ctypes.c_int32),
                                               c_int, P(c_dbl)]
@@ -284,6 +289,26 @@ class Cache:
                                  _p(sl, ctypes.c_int32), B, _p(out, ctypes.c_double))
         if rc != 0:
             raise MemoryError("oracle attention: allocation failed")
+        return out
+
+    def tree_attention(self, q16, tree_mask, block_table, seq_lens):
+        """Tree verify: q16 fp16 [B][T][Hq][d]; tree_mask uint64 [B][T] (bit i of row j: query j
+        sees draft i, the draft being position len - T + i) -> float64 [B][T][Hq][d]."""
+        q16 = _f16bits(q16)
+        mask = np.ascontiguousarray(tree_mask, np.uint64)
+        bt = np.ascontiguousarray(block_table, np.int32)
+        sl = np.ascontiguousarray(seq_lens, np.int32)
+        B, max_pages = bt.shape
+        T = mask.shape[1]
+        out = np.zeros((B, T, self.hq, self.d), np.float64)
+        rc = lib().rqo_tree_attention(self.mode, self.bits, self.d, self.hq, self.hkv, self.P,
+                                      _p(self.rot_k, ctypes.c_float), _p(self.rot_v, ctypes.c_float),
+                                      _p(self.centroids, ctypes.c_float), self.sm_scale, _p(q16, ctypes.c_uint16), T,
+                                      _p(mask, ctypes.c_uint64), _p(self.pages, ctypes.c_uint8),
+                                      _p(bt, ctypes.c_int32), max_pages, _p(sl, ctypes.c_int32), B,
+                                      _p(out, ctypes.c_double))
+        if rc != 0:
+            raise ValueError("oracle tree attention failed (T must be 1..64)")
         return out
 
     def chunk(self, page: int, head: int) -> np.ndarray:

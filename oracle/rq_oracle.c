@@ -436,14 +436,17 @@ static void load_token(int mode, int bits, int d, int hkv, int page_size, const 
  * Attention over the dequantised cache, in the original (unrotated) space.
  *   q: fp16 [B][T][Hq][d];  out: double [B][T][Hq][d].
  *   Query head hq reads kv head hq / (Hq / Hkv).  seq_lens[b] counts every cached token,
- *   the T query tokens included; query row j attends to positions 0 .. len - T + j.
- *   s_t = sm_scale * <q, k_t>,  o = sum_t softmax(s)_t v_t.  A row that sees no position
- *   (len - T + j < 0) or a sequence with len = 0 gives zeros.
+ *   the T query tokens included (they are the last T positions, the drafts).
+ *   Visibility of position t to query row j:
+ *     chain (tree_mask NULL): t <= len - T + j;
+ *     tree: t < len - T (the prefix), or draft i = t - (len - T) with bit i of tree_mask[b][j].
+ *   s_t = sm_scale * <q, k_t>,  o = sum over visible t of softmax(s)_t v_t.  A row that sees no
+ *   position, or a sequence with len = 0, gives zeros.
  */
-int rqo_attention(int mode, int bits, int d, int hq, int hkv, int page_size,
-                  const float *rot_k, const float *rot_v, const float *centroids, double sm_scale,
-                  const uint16_t *q, int T, const uint8_t *pages, const int32_t *block_table,
-                  int max_pages, const int32_t *seq_lens, int B, double *out) {
+static int attention_impl(int mode, int bits, int d, int hq, int hkv, int page_size,
+                          const float *rot_k, const float *rot_v, const float *centroids, double sm_scale,
+                          const uint16_t *q, int T, const uint64_t *tree_mask, const uint8_t *pages,
+                          const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B, double *out) {
   int group = hq / hkv;
   for (int b = 0; b < B; ++b) {
     int len = seq_lens[b];
@@ -452,39 +455,73 @@ int rqo_attention(int mode, int bits, int d, int hq, int hkv, int page_size,
       double *K = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len : 1) * d);
       double *V = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len : 1) * d);
       double *s = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len : 1));
-      if (!K || !V || !s) { free(K); free(V); free(s); return -1; }
+      char *vis = (char *)malloc((size_t)(len > 0 ? len : 1));
+      if (!K || !V || !s || !vis) { free(K); free(V); free(s); free(vis); return -1; }
       for (int t = 0; t < len; ++t)
         load_token(mode, bits, d, hkv, page_size, rot_k, rot_v, centroids, pages, bt, t, h,
                    K + (size_t)t * d, V + (size_t)t * d);
       for (int j = 0; j < T; ++j) {
-        int last = len - T + j;               /* inclusive */
+        int any = 0;
+        for (int t = 0; t < len; ++t) {
+          if (!tree_mask) {
+            vis[t] = t <= len - T + j;
+          } else {
+            int i = t - (len - T);
+            vis[t] = i < 0 ? 1 : (int)((tree_mask[(size_t)b * T + j] >> i) & 1u);
+          }
+          any |= vis[t];
+        }
         for (int g = 0; g < group; ++g) {
           int head = h * group + g;
           const uint16_t *qv = q + (((size_t)b * T + j) * hq + head) * d;
           double *o = out + (((size_t)b * T + j) * hq + head) * d;
           for (int i = 0; i < d; ++i) o[i] = 0.0;
-          if (len <= 0 || last < 0) continue;
+          if (len <= 0 || !any) continue;
           double qd[1024];
           for (int i = 0; i < d; ++i) qd[i] = rqo_half_to_double(qv[i]);
           double mx = -INFINITY;
-          for (int t = 0; t <= last; ++t) {
+          for (int t = 0; t < len; ++t) {
+            if (!vis[t]) continue;
             double acc = 0.0;
             for (int i = 0; i < d; ++i) acc += qd[i] * K[(size_t)t * d + i];
             s[t] = sm_scale * acc;
             if (s[t] > mx) mx = s[t];
           }
           double denom = 0.0;
-          for (int t = 0; t <= last; ++t) { s[t] = exp(s[t] - mx); denom += s[t]; }
-          for (int t = 0; t <= last; ++t) {
+          for (int t = 0; t < len; ++t) {
+            if (!vis[t]) continue;
+            s[t] = exp(s[t] - mx);
+            denom += s[t];
+          }
+          for (int t = 0; t < len; ++t) {
+            if (!vis[t]) continue;
             double p = s[t] / denom;
             for (int i = 0; i < d; ++i) o[i] += p * V[(size_t)t * d + i];
           }
         }
       }
-      free(K); free(V); free(s);
+      free(K); free(V); free(s); free(vis);
     }
   }
   return 0;
+}
+
+int rqo_attention(int mode, int bits, int d, int hq, int hkv, int page_size,
+                  const float *rot_k, const float *rot_v, const float *centroids, double sm_scale,
+                  const uint16_t *q, int T, const uint8_t *pages, const int32_t *block_table,
+                  int max_pages, const int32_t *seq_lens, int B, double *out) {
+  return attention_impl(mode, bits, d, hq, hkv, page_size, rot_k, rot_v, centroids, sm_scale, q, T, NULL, pages,
+                        block_table, max_pages, seq_lens, B, out);
+}
+
+/* Tree verify: tree_mask uint64 [B][T], bit i of row j = query j sees draft i (T <= 64). */
+int rqo_tree_attention(int mode, int bits, int d, int hq, int hkv, int page_size,
+                       const float *rot_k, const float *rot_v, const float *centroids, double sm_scale,
+                       const uint16_t *q, int T, const uint64_t *tree_mask, const uint8_t *pages,
+                       const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B, double *out) {
+  if (T < 1 || T > 64 || !tree_mask) return -2;
+  return attention_impl(mode, bits, d, hq, hkv, page_size, rot_k, rot_v, centroids, sm_scale, q, T, tree_mask,
+                        pages, block_table, max_pages, seq_lens, B, out);
 }
 
 /* Plain attention over unquantised fp16 K/V given densely as [B][L][Hkv][d] (the fidelity

@@ -259,8 +259,9 @@ int rq_quantize_append(rq_ctx* ctx, const void* k, const void* v, const int32_t*
                                      (cudaStream_t)stream));
 }
 
-int rq_verify_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages, const int32_t* block_table,
-                        int max_pages, const int32_t* seq_lens, int B, void* out, int32_t* d_status, void* stream) {
+static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tree_mask, const void* kv_pages,
+                          const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B, void* out,
+                          int32_t* d_status, void* stream) {
   if (!ctx || B < 0 || T < 1 || max_pages < 1) return RQ_ERR_INVALID;
   if (B == 0) return RQ_OK;
   if (!q || !kv_pages || !block_table || !seq_lens || !out) return RQ_ERR_INVALID;
@@ -279,6 +280,7 @@ int rq_verify_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages,
   a.T = T;
   a.out = out;
   a.status = d_status;
+  a.tree_mask = tree_mask;
   a.ws = ctx->d_ws;
   a.rows = T * ctx->g.group;
   a.n_tiles_n = (a.rows + 7) / 8;
@@ -313,9 +315,21 @@ int rq_verify_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages,
       rq::launch_attention(ctx->g, a, ctx->num_sms, (cudaStream_t)stream, ctx->prof_start, ctx->prof_end));
 }
 
+int rq_verify_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages, const int32_t* block_table,
+                        int max_pages, const int32_t* seq_lens, int B, void* out, int32_t* d_status, void* stream) {
+  return attention_call(ctx, q, T, nullptr, kv_pages, block_table, max_pages, seq_lens, B, out, d_status, stream);
+}
+
+int rq_tree_verify_attention(rq_ctx* ctx, const void* q, int T, const uint64_t* tree_mask, const void* kv_pages,
+                             const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B, void* out,
+                             int32_t* d_status, void* stream) {
+  if (T > 64 || (B > 0 && !tree_mask)) return RQ_ERR_INVALID;
+  return attention_call(ctx, q, T, tree_mask, kv_pages, block_table, max_pages, seq_lens, B, out, d_status, stream);
+}
+
 int rq_decode_attention(rq_ctx* ctx, const void* q, const void* kv_pages, const int32_t* block_table, int max_pages,
                         const int32_t* seq_lens, int B, void* out, int32_t* d_status, void* stream) {
-  return rq_verify_attention(ctx, q, 1, kv_pages, block_table, max_pages, seq_lens, B, out, d_status, stream);
+  return attention_call(ctx, q, 1, nullptr, kv_pages, block_table, max_pages, seq_lens, B, out, d_status, stream);
 }
 
 }  // extern "C"

@@ -495,7 +495,8 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
     // q~ = R_k q * sm_scale * log2(e) for query column gq of this n-tile, the lane's 32 dims.
     uint32_t qf[8][2];
     const int row = it.nt * 8 + gq;  // query row of the kv head: draft j = row / group, head row % group
-    int last_pos[2];                  // last visible position of query columns 2tq, 2tq+1
+    int last_pos[2];                  // last position wholly visible to query columns 2tq, 2tq+1
+    uint64_t draft_mask[2];           // tree verify: the columns' draft visibility bits
     {
       float qv[32];
       if (row < a.rows) {
@@ -543,7 +544,10 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
       for (int c = 0; c < 2; ++c) {
         const int rc = it.nt * 8 + 2 * tq + c;
         const int j = rc < a.rows ? rc / g.group : a.T - 1;
-        last_pos[c] = len - a.T + j;
+        // chain: row j sees positions <= len - T + j; tree: the prefix for sure (the drafts
+        // by their mask bit), so only the prefix counts as wholly visible
+        last_pos[c] = a.tree_mask ? len - a.T - 1 : len - a.T + j;
+        draft_mask[c] = a.tree_mask ? a.tree_mask[(size_t)it.b * a.T + j] : 0ull;
       }
     }
     __syncthreads();  // page ids staged
@@ -627,10 +631,18 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
       // Pairs wholly inside every column's visible range skip the per-element mask.
       const bool interior = __all_sync(0xffffffffu, pos0 + 31 <= min(last_pos[0], last_pos[1]));
       if (!interior) {
+        const int draft0 = len - a.T;  // position of the first draft
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int pos = pos0 + 16 * (e >> 2) + rho<BITS>(gq) + 8 * ((e >> 1) & 1);
-          if (pos > last_pos[e & 1]) sc[e] = -CUDART_INF_F;
+          bool vis;
+          if (a.tree_mask) {
+            const int i = pos - draft0;
+            vis = i < 0 || (i < a.T && ((draft_mask[e & 1] >> i) & 1ull));
+          } else {
+            vis = pos <= last_pos[e & 1];
+          }
+          if (!vis) sc[e] = -CUDART_INF_F;
         }
       }
       float alpha[2];

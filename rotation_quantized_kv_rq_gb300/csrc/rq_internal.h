@@ -43,6 +43,7 @@ struct AttnArgs {
   int pages_per_split;
   int max_splits;            // splits per (b, kv head) the workspace has room for
   int* counters;             // [2] work-item and finished-CTA counters, zero between launches
+  const uint64_t* tree_mask; // [B][T] draft visibility bits (tree verify), or null (causal chain)
 };
 
 constexpr int kPartialStride = 132;   // floats per partial row: m, l, pad, pad, o[128]

@@ -109,6 +109,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   a.T = 1;
   a.out = out;
   a.status = d_status;
+  a.tree_mask = nullptr;
   a.rows = group;
   a.n_tiles_n = (group + 7) / 8;
 

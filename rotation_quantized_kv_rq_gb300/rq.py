@@ -24,7 +24,7 @@ HEAD_DIM = 128
 
 EXPORTS = ["rq_create", "rq_free", "rq_page_bytes", "rq_lloyd_max_codebook", "rq_get_codebook",
            "rq_quantize_append", "rq_decode_attention", "rq_verify_attention", "rq_set_profile_events",
-           "rq_decode_attention_noalloc", "rq_status_string"]
+           "rq_decode_attention_noalloc", "rq_tree_verify_attention", "rq_status_string"]
 
 
 class RQError(RuntimeError):
@@ -71,6 +71,9 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             L.rq_verify_attention.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, vp,
                                               vp]
             L.rq_verify_attention.restype = ctypes.c_int
+            L.rq_tree_verify_attention.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp, ctypes.c_int,
+                                                   vp, vp, vp]
+            L.rq_tree_verify_attention.restype = ctypes.c_int
             L.rq_decode_attention_noalloc.argtypes = [ctypes.POINTER(rq_config), vp, vp, vp, vp, vp, vp,
                                                       ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]
             L.rq_decode_attention_noalloc.restype = ctypes.c_int
@@ -180,6 +183,21 @@ def rq_verify_attention(ctx, q: torch.Tensor, kv_pages: torch.Tensor, block_tabl
     return out
 
 
+def rq_tree_verify_attention(ctx, q: torch.Tensor, tree_mask: torch.Tensor, kv_pages: torch.Tensor,
+                             block_table: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor,
+                             status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q, out: fp16 [B][T][Hq][128]; tree_mask int64/uint64 [B][T] (bit i of row j: draft i visible)."""
+    B, T = q.shape[0], q.shape[1]
+    assert q.dtype == torch.float16 and out.dtype == torch.float16 and q.is_contiguous() and out.is_contiguous()
+    assert tree_mask.dtype in (torch.int64, torch.uint64) and tree_mask.is_contiguous() and tuple(tree_mask.shape) == (B, T)
+    assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32 and block_table.is_contiguous()
+    _check("rq_tree_verify_attention",
+           lib().rq_tree_verify_attention(ctx, _ptr(q), T, _ptr(tree_mask), _ptr(kv_pages), _ptr(block_table),
+                                          block_table.shape[-1], _ptr(seq_lens), B, _ptr(out), _ptr(status),
+                                          _stream(stream, q.device)))
+    return out
+
+
 def rq_decode_attention_noalloc(mode: int, bits: int, num_q_heads: int, num_kv_heads: int, page_size: int,
                                 num_pages: int, d_rot_k: torch.Tensor, d_rot_v: torch.Tensor,
                                 d_centroids: torch.Tensor, q: torch.Tensor, kv_pages: torch.Tensor,
@@ -244,6 +262,12 @@ class KVCache:
         if out is None:
             out = torch.empty_like(q)
         return rq_verify_attention(self.ctx, q, self.pages, block_table, seq_lens, out, self.status, stream)
+
+    def tree_verify(self, q, tree_mask, block_table, seq_lens, out=None, stream=None):
+        if out is None:
+            out = torch.empty_like(q)
+        return rq_tree_verify_attention(self.ctx, q, tree_mask, self.pages, block_table, seq_lens, out, self.status,
+                                        stream)
 
     def close(self):
         if self.ctx is not None:

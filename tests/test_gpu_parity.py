@@ -184,3 +184,48 @@ def test_repeated_calls_are_deterministic():
         again = cache.decode(qd, bt, sl)
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
     cache.close()
+
+
+def _tree_masks(rng, B, T):
+    """Ancestor masks of random draft trees (parent = the prefix or an earlier draft)."""
+    masks = np.zeros((B, T), np.uint64)
+    for b in range(B):
+        parent = [-1] + [int(rng.integers(-1, i)) for i in range(1, T)]
+        for i in range(T):
+            m, j = 0, i
+            while j >= 0:
+                m |= 1 << j
+                j = parent[j]
+            masks[b, i] = m
+    return masks
+
+
+@pytest.mark.parametrize("mode,bits,hq,hkv,P,lens,T", [
+    (ISO, 3, 32, 8, 16, [300, 6, 90], 6),
+    (PLANAR, 4, 64, 8, 16, [513, 40], 8),
+    (ISO, 4, 24, 2, 64, [200, 3], 3),
+])
+def test_tree_verify_matches_oracle(mode, bits, hq, hkv, P, lens, T):
+    wl, kv, q = make_case(mode, bits, hq, hkv, P, lens, T, seed=23)
+    s = wl.spec
+    oc = PT.oracle_cache(wl)
+    cache = rq.KVCache(s.mode, s.bits, s.num_q_heads, s.num_kv_heads, s.page_size, wl.num_pages, wl.rot_k, wl.rot_v,
+                       max_batch=s.batch, max_query_tokens=T, max_pages_per_seq=wl.block_table.shape[1])
+    for b, (k, v) in enumerate(kv):
+        slots = PT.positions_slots(wl, b, 0, k.shape[0])
+        oc.append(k, v, slots)
+        cache.append(PT.to_dev(k), PT.to_dev(v), PT.to_dev(slots))
+    rng = np.random.default_rng(5)
+    masks = _tree_masks(rng, s.batch, T)
+    qd, bt, sl = PT.to_dev(q), PT.to_dev(wl.block_table), PT.to_dev(wl.seq_lens)
+    dmask = torch.from_numpy(masks.view(np.int64)).cuda()
+    got = cache.tree_verify(qd, dmask, bt, sl).cpu().numpy()
+    ref = oc.tree_attention(q, masks, wl.block_table, wl.seq_lens)
+    PT.assert_close(got, ref, "tree verify")
+    chain = torch.tensor([[(1 << (j + 1)) - 1 for j in range(T)]] * s.batch, dtype=torch.int64).cuda()
+    a = cache.tree_verify(qd, chain, bt, sl)
+    b2 = cache.verify(qd, bt, sl)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b2.view(torch.int16))
+    assert int(cache.status.item()) == 0
+    cache.close()

@@ -425,3 +425,44 @@ def test_rotated_space_accumulation_identity():
     once, _ = O.rotate(O.ISO, p_rot, acc, inverse=True)
     each = sum(w[t] * O.dequant(O.ISO, 4, p_rot, cents, codes[t], n16[t]) for t in range(10))
     assert np.allclose(once, each, atol=1e-12)
+
+
+def _random_tree_masks(rng, B, T):
+    """Ancestor masks of random draft trees: draft i's parent is the root (prefix) or an earlier
+    draft; draft i sees itself and its ancestors."""
+    masks = np.zeros((B, T), np.uint64)
+    for b in range(B):
+        parent = [-1] + [int(rng.integers(-1, i)) for i in range(1, T)]
+        for i in range(T):
+            m, j = 0, i
+            while j >= 0:
+                m |= 1 << j
+                j = parent[j]
+            masks[b, i] = m
+    return masks
+
+
+def test_tree_attention_against_sdpa_and_chain():
+    cache, rng = _small_cache(O.PLANAR, 4, num_pages=8)
+    T = 5
+    lens = np.array([37, T], np.int32)
+    bt = np.array([[3, 0, 6], [7, 0, 0]], np.int32)
+    for b, L in enumerate(lens):
+        k = (rng.standard_normal((L, 2, 128)) * 2).astype(np.float16)
+        v = rng.standard_normal((L, 2, 128)).astype(np.float16)
+        pos = np.arange(L)
+        cache.append(k, v, (bt[b, pos // 16] * 16 + pos % 16).astype(np.int32))
+    q = rng.standard_normal((2, T, 8, 128)).astype(np.float16)
+    masks = _random_tree_masks(rng, 2, T)
+    got = cache.tree_attention(q, masks, bt, lens)
+    K, V = _dequantised(cache, bt, lens)
+    for b, L in enumerate(lens):
+        qq = torch.from_numpy(q[b].astype(np.float64)).permute(1, 0, 2)
+        kk = torch.from_numpy(K[b, :L]).permute(1, 0, 2).repeat_interleave(4, 0)
+        vv = torch.from_numpy(V[b, :L]).permute(1, 0, 2).repeat_interleave(4, 0)
+        vis = torch.tensor([[t < L - T or bool((int(masks[b, j]) >> (t - (L - T))) & 1) for t in range(L)]
+                            for j in range(T)])
+        ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=vis)
+        assert np.allclose(got[b], ref.permute(1, 0, 2).numpy(), atol=1e-12)
+    chain = np.array([[(1 << (j + 1)) - 1 for j in range(T)]] * 2, np.uint64)
+    assert np.array_equal(cache.tree_attention(q, chain, bt, lens), cache.attention(q, bt, lens, T=T))
