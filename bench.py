@@ -232,17 +232,26 @@ def measured_peaks():
 
 
 def committed_traffic(kernel_file, workload):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    """DRAM bytes per launch (read + write) from the committed ncu summary
+    profiles/traffic_<workload>.txt ("key: value" lines), if it was taken on the current
+    kernel source (same sha256); None otherwise."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
     src = os.path.join(ROOT, "rotation_quantized_kv_rq_gb300", "csrc", kernel_file)
     if not os.path.exists(p):
         return None
+    d = {}
     with open(p) as f:
-        d = json.load(f)
+        for ln in f:
+            if ":" in ln and not ln.startswith("#"):
+                k, v = ln.split(":", 1)
+                d[k.strip()] = v.strip()
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     if d.get("source_sha256") != sha:
         return None
-    return d.get("dram_bytes_per_launch")
+    try:
+        return float(d["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 # ---------------------------------------------------------------------------------------
