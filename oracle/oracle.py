@@ -24,7 +24,7 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-PLANAR, ISO = 0, 1
+PLANAR, ISO, DENSE = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -77,6 +77,8 @@ def lib():
             L.rqo_dequant.restype = None
             L.rqo_v_unit_offset.argtypes = [c_int, c_int, c_int, c_int]
             L.rqo_v_unit_offset.restype = c_sz
+            L.rqo_v_unit_bytes.argtypes = [c_int, c_int]
+            L.rqo_v_unit_bytes.restype = c_int
             L.rqo_page_bytes.argtypes = [c_int, c_int, c_int]
             L.rqo_page_bytes.restype = c_sz
             L.rqo_append.argtypes = [c_int, c_int, c_int, c_int, c_int, P(ctypes.c_float), P(ctypes.c_float),
@@ -229,12 +231,17 @@ def v_unit_offset(bits: int, off: int, unit: int, d: int = 128) -> int:
     return int(lib().rqo_v_unit_offset(bits, d, off, unit))
 
 
+def v_unit_bytes(bits: int, d: int = 128) -> int:
+    return int(lib().rqo_v_unit_bytes(bits, d))
+
+
 def v_codes_of(bits: int, chunk: np.ndarray, page_size: int, off: int, d: int = 128) -> np.ndarray:
     """The packed codes of V token `off` gathered from a chunk."""
     vb = vector_bytes(bits, d)
+    ub = v_unit_bytes(bits, d)
     base = page_size * vb
-    return np.concatenate([chunk[base + v_unit_offset(bits, off, u, d):base + v_unit_offset(bits, off, u, d) + 8]
-                           for u in range(vb // 8)])
+    return np.concatenate([chunk[base + v_unit_offset(bits, off, u, d):base + v_unit_offset(bits, off, u, d) + ub]
+                           for u in range(vb // ub)])
 
 
 def page_bytes(bits: int, page_size: int, d: int = 128) -> int:
@@ -249,8 +256,9 @@ class Cache:
         self.mode, self.bits = int(mode), int(bits)
         self.hq, self.hkv, self.P, self.d = int(num_q_heads), int(num_kv_heads), int(page_size), int(head_dim)
         self.num_pages = int(num_pages)
-        self.rot_k = np.ascontiguousarray(rot_k, np.float32).reshape(self.hkv, self.d)
-        self.rot_v = np.ascontiguousarray(rot_v, np.float32).reshape(self.hkv, self.d)
+        per_head = self.d * self.d if self.mode == DENSE else self.d
+        self.rot_k = np.ascontiguousarray(rot_k, np.float32).reshape(self.hkv, per_head)
+        self.rot_v = np.ascontiguousarray(rot_v, np.float32).reshape(self.hkv, per_head)
         self.centroids, self.boundaries = codebook(self.bits, self.d)
         self.sm_scale = float(sm_scale) if sm_scale else 1.0 / np.sqrt(self.d)
         self.page_bytes = page_bytes(self.bits, self.P, self.d)

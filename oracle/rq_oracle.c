@@ -157,6 +157,8 @@ void rqo_codebook(int bits, int d, float *centroids, float *boundaries) {
 /*       y_2i = cos*x_2i - sin*x_2i+1,   y_2i+1 = sin*x_2i + cos*x_2i+1                     */
 /*   iso (IsoQuant, 4D quaternion): params [d/4][4] = unit quaternion (a,b,c,d) for block    */
 /*       4i..4i+3, y_blk = q (x) x_blk, the Hamilton product with q on the left.            */
+/*   dense (TurboQuant, "TurboQuant KV Cache Compression" section and "Acknowledgments":    */
+/*       random rotation): params [d][d] = an orthogonal matrix R, row-major, y = R x.       */
 /* The inverse applies the transpose.  Each returns the number of multiply-adds it made.    */
 /* ------------------------------------------------------------------------------------- */
 
@@ -170,6 +172,17 @@ static void quat_left_matrix(const float *q, double L[4][4]) {
 
 long rqo_rotate(int mode, const float *params, int d, const double *x, double *y, int inverse) {
   long fma = 0;
+  if (mode == 2) {
+    for (int r = 0; r < d; ++r) {
+      double acc = 0.0;
+      for (int k = 0; k < d; ++k) {
+        acc += (double)(inverse ? params[(size_t)k * d + r] : params[(size_t)r * d + k]) * x[k];
+        fma += 1;
+      }
+      y[r] = acc;
+    }
+    return fma;
+  }
   if (mode == 0) {
     for (int i = 0; i < d / 2; ++i) {
       double c = params[2 * i], s = params[2 * i + 1];
@@ -205,7 +218,8 @@ long rqo_rotate(int mode, const float *params, int d, const double *x, double *y
 
 /* The same rotation as a dense d x d matrix R (row-major), y = R x. */
 void rqo_rotation_matrix(int mode, const float *params, int d, double *R) {
-  for (int i = 0; i < d * d; ++i) R[i] = 0.0;
+  for (int i = 0; i < d * d; ++i) R[i] = (mode == 2) ? (double)params[i] : 0.0;
+  if (mode == 2) return;
   if (mode == 0) {
     for (int i = 0; i < d / 2; ++i) {
       double c = params[2 * i], s = params[2 * i + 1];
@@ -297,7 +311,11 @@ static uint32_t get_word(const uint8_t *p) {
 }
 
 void rqo_pack(int bits, int d, const uint8_t *codes, uint8_t *out) {
-  if (bits == 4) {
+  if (bits == 2) {
+    for (int j = 0; j < d / 4; ++j)
+      out[j] = (uint8_t)((codes[4 * j] & 3) | ((codes[4 * j + 1] & 3) << 2) | ((codes[4 * j + 2] & 3) << 4) |
+                         ((codes[4 * j + 3] & 3) << 6));
+  } else if (bits == 4) {
     for (int j = 0; j < d / 2; ++j) out[j] = (uint8_t)((codes[2 * j] & 15) | ((codes[2 * j + 1] & 15) << 4));
   } else {
     for (int w = 0; w < d / 32; ++w) {
@@ -316,7 +334,10 @@ void rqo_pack(int bits, int d, const uint8_t *codes, uint8_t *out) {
 }
 
 void rqo_unpack(int bits, int d, const uint8_t *in, uint8_t *codes) {
-  if (bits == 4) {
+  if (bits == 2) {
+    for (int j = 0; j < d / 4; ++j)
+      for (int r = 0; r < 4; ++r) codes[4 * j + r] = (in[j] >> (2 * r)) & 3;
+  } else if (bits == 4) {
     for (int j = 0; j < d / 2; ++j) {
       codes[2 * j] = in[j] & 15;
       codes[2 * j + 1] = in[j] >> 4;
@@ -348,32 +369,45 @@ void rqo_dequant(int mode, int bits, int d, const float *rot, const float *centr
 /* Paged cache.  One chunk per (page, kv head), at byte (page * Hkv + head) * page_bytes:   */
 /*   K codes [P][vb] | V codes [P][vb] | K norms fp16 [P] | V norms fp16 [P]               */
 /* with vb = d * bits / 8.  Slot s holds token offset s % P of page s / P.                 */
-/* K codes, and 3-bit V codes, are stored token after token.  4-bit V codes (d = 128) are   */
-/* stored as token pairs: pair p = tokens (2p, 2p+1) fills 128 bytes; its 8-byte unit for  */
-/* 16-dim group c of token 2p + h sits at byte 16 * (c ^ (2p mod 8)) + 8h of the pair.      */
+/* K codes, and 3-bit V codes, are stored token after token, in units of 8 bytes.  4-bit   */
+/* and 2-bit V codes (d = 128) are stored as token pairs, in units of one 16-dim group      */
+/* (8 bytes at 4 bits, 4 bytes at 2 bits): pair p = tokens (2p, 2p+1) fills 2 * vb bytes,  */
+/* and the unit of group c of token 2p + h sits at byte                                     */
+/*   4-bit:  16 * (c ^ (2p mod 8)) + 8h                                                     */
+/*   2-bit:   8 * (c ^ (4 * ((p >> 1) & 1))) + 4h                                           */
+/* of the pair.                                                                             */
 /* ------------------------------------------------------------------------------------- */
 
-/* Byte offset, inside the V-codes section, of the vb bytes (or the 8-byte unit `unit` of  */
-/* a 4-bit d = 128 vector) of token `off`. */
+static int v_unit_bytes(int bits, int d) { return ((bits == 4 || bits == 2) && d == 128) ? 2 * bits : 8; }
+
+/* Byte offset, inside the V-codes section, of unit `unit` of token `off`. */
 static size_t v_unit_offset(int bits, int d, int off, int unit) {
   size_t vb = rqo_vector_bytes(bits, d);
-  if (bits != 4 || d != 128) return (size_t)off * vb + (size_t)unit * 8;
+  if (d != 128 || bits == 3) return (size_t)off * vb + (size_t)unit * 8;
   int pair = off / 2, h = off % 2;
-  return (size_t)pair * 128 + (size_t)16 * (unit ^ ((2 * pair) % 8)) + (size_t)8 * h;
+  if (bits == 4) return (size_t)pair * 128 + (size_t)16 * (unit ^ ((2 * pair) % 8)) + (size_t)8 * h;
+  return (size_t)pair * 64 + (size_t)8 * (unit ^ (4 * ((pair >> 1) & 1))) + (size_t)4 * h;
 }
 
 static void put_v(int bits, int d, uint8_t *vsec, int off, const uint8_t *packed) {
   size_t vb = rqo_vector_bytes(bits, d);
-  for (size_t u = 0; u < vb / 8; ++u) memcpy(vsec + v_unit_offset(bits, d, off, (int)u), packed + 8 * u, 8);
+  int ub = v_unit_bytes(bits, d);
+  for (size_t u = 0; u < vb / ub; ++u) memcpy(vsec + v_unit_offset(bits, d, off, (int)u), packed + ub * u, ub);
 }
 
 static void get_v(int bits, int d, const uint8_t *vsec, int off, uint8_t *packed) {
   size_t vb = rqo_vector_bytes(bits, d);
-  for (size_t u = 0; u < vb / 8; ++u) memcpy(packed + 8 * u, vsec + v_unit_offset(bits, d, off, (int)u), 8);
+  int ub = v_unit_bytes(bits, d);
+  for (size_t u = 0; u < vb / ub; ++u) memcpy(packed + ub * u, vsec + v_unit_offset(bits, d, off, (int)u), ub);
 }
 
-/* Exposed for tests: byte offset of 8-byte unit `unit` of V token `off` in its section. */
+/* Exposed for tests: byte offset of unit `unit` of V token `off` in its section, and the
+   unit size in bytes. */
 size_t rqo_v_unit_offset(int bits, int d, int off, int unit) { return v_unit_offset(bits, d, off, unit); }
+int rqo_v_unit_bytes(int bits, int d) { return v_unit_bytes(bits, d); }
+
+/* Floats of one head's rotation parameters: d for planar / iso, d * d for dense. */
+static size_t rot_stride(int mode, int d) { return mode == 2 ? (size_t)d * d : (size_t)d; }
 
 size_t rqo_page_bytes(int bits, int page_size, int d) {
   return (size_t)page_size * (2 * rqo_vector_bytes(bits, d) + 4);
@@ -395,10 +429,10 @@ void rqo_append(int mode, int bits, int d, int hkv, int page_size,
       uint8_t *chunk = pages + ((size_t)page * hkv + h) * pb;
       const size_t src = ((size_t)t * hkv + h) * d;
       uint16_t nk, nv;
-      rqo_encode(mode, bits, d, rot_k + (size_t)h * d, boundaries, k + src, codes, &nk,
+      rqo_encode(mode, bits, d, rot_k + (size_t)h * rot_stride(mode, d), boundaries, k + src, codes, &nk,
                  margin_k ? margin_k + src : NULL);
       rqo_pack(bits, d, codes, chunk + off * vb);
-      rqo_encode(mode, bits, d, rot_v + (size_t)h * d, boundaries, v + src, codes, &nv,
+      rqo_encode(mode, bits, d, rot_v + (size_t)h * rot_stride(mode, d), boundaries, v + src, codes, &nv,
                  margin_v ? margin_v + src : NULL);
       uint8_t packed[1024];
       rqo_pack(bits, d, codes, packed);
@@ -425,11 +459,11 @@ static void load_token(int mode, int bits, int d, int hkv, int page_size, const 
   uint16_t nv = (uint16_t)(norms[2 * page_size + 2 * off] | (norms[2 * page_size + 2 * off + 1] << 8));
   uint8_t codes[1024];
   rqo_unpack(bits, d, chunk + off * vb, codes);
-  rqo_dequant(mode, bits, d, rot_k + (size_t)h * d, centroids, codes, nk, kh);
+  rqo_dequant(mode, bits, d, rot_k + (size_t)h * rot_stride(mode, d), centroids, codes, nk, kh);
   uint8_t packed[1024];
   get_v(bits, d, chunk + page_size * vb, off, packed);
   rqo_unpack(bits, d, packed, codes);
-  rqo_dequant(mode, bits, d, rot_v + (size_t)h * d, centroids, codes, nv, vh);
+  rqo_dequant(mode, bits, d, rot_v + (size_t)h * rot_stride(mode, d), centroids, codes, nv, vh);
 }
 
 /*

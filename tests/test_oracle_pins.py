@@ -126,6 +126,25 @@ def test_fma_counts_printed_on_the_pages():
     assert n_dense // n_planar == 64 and n_dense // n_iso == 32
 
 
+def _dense_params(rng, d=128):
+    q, r = np.linalg.qr(rng.standard_normal((d, d)))
+    return (q * np.sign(np.diag(r))[None, :]).astype(np.float32)
+
+
+def test_dense_rotation_cost_matrix_and_inverse():
+    """TurboQuant's dense rotation: 16,384 multiply-adds, equal to its matrix, inverse = transpose."""
+    rng = np.random.default_rng(70)
+    R = _dense_params(rng)
+    x = rng.standard_normal(128)
+    y, n = O.rotate(O.DENSE, R, x)
+    assert n == 16384
+    assert np.allclose(y, R.astype(np.float64) @ x, atol=1e-12)
+    assert np.array_equal(O.rotation_matrix(O.DENSE, R, 128), R.astype(np.float64))
+    back, _ = O.rotate(O.DENSE, R, y, inverse=True)
+    assert np.allclose(back, R.astype(np.float64).T @ y, atol=1e-12)
+    assert np.allclose(back, x, atol=1e-5)
+
+
 def test_planar_is_complex_multiplication():
     """(x_2i + i x_2i+1) * exp(i t): an independent statement of the Givens rotation."""
     rng = np.random.default_rng(2)
@@ -238,6 +257,31 @@ def test_codec_distortion_matches_lloyd_max_mse(bits, mode):
     assert abs(np.mean(errs) - mse) < 0.08 * mse, (np.mean(errs), mse)
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_dense_rotation_spreads_outliers(bits):
+    """The distortion of a dense random rotation (TurboQuant) is an expectation over the draw of
+    the rotation: averaged over fresh rotations, keys with x10 outlier channels code to the
+    Lloyd-Max MSE of N(0,1).  A block-local rotation (iso) cannot move an outlier out of its
+    4-dim block, so the same keys land far above it."""
+    rng = np.random.default_rng(80 + bits)
+    cents, bnds = O.codebook(bits, 128)
+    _, _, mse, _ = O.lloyd_max_normal(1 << bits)
+    dense, local = [], []
+    for _ in range(200):
+        R = _dense_params(rng)
+        p = _iso_params(rng)
+        x = rng.standard_normal(128)
+        x[[3, 40, 77, 101]] *= 10
+        x = x.astype(np.float16)
+        xd = x.astype(np.float64)
+        for mode, rot, errs in ((O.DENSE, R, dense), (O.ISO, p, local)):
+            codes, n16, _ = O.encode(mode, bits, rot, bnds, x)
+            xh = O.dequant(mode, bits, rot, cents, codes, n16)
+            errs.append(np.sum((xd - xh) ** 2) / np.sum(xd ** 2))
+    assert abs(np.mean(dense) - mse) < 0.1 * mse, (np.mean(dense), mse)
+    assert np.mean(local) > 2.5 * mse, (np.mean(local), mse)
+
+
 # ---------------------------------------------------------------------------------------
 # Packing
 # ---------------------------------------------------------------------------------------
@@ -247,6 +291,17 @@ def test_pack_4bit_fixture():
     codes = (np.arange(128) % 16).astype(np.uint8)
     assert np.array_equal(O.pack(4, codes), want)
     assert np.array_equal(O.unpack(4, want), codes)
+
+
+def test_pack_2bit_fixture():
+    rows = _rows("pack_2bit.txt")
+    codes = {"i%4": (np.arange(128) % 4).astype(np.uint8), "3-i%4": (3 - np.arange(128) % 4).astype(np.uint8)}
+    for i in range(0, len(rows), 2):
+        c = codes[rows[i][1]]
+        want = np.array([int(h, 16) for h in rows[i + 1][1:]], np.uint8)
+        assert want.size == 32
+        assert np.array_equal(O.pack(2, c), want)
+        assert np.array_equal(O.unpack(2, want), c)
 
 
 def test_pack_3bit_fixtures():
@@ -266,7 +321,7 @@ def test_pack_3bit_fixtures():
         assert np.array_equal(O.unpack(3, want), codes), parts[0]
 
 
-@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 def test_pack_round_trip_and_sizes(bits):
     rng = np.random.default_rng(30 + bits)
     for _ in range(50):
@@ -283,16 +338,17 @@ def test_v_placement_fixture():
         assert O.v_unit_offset(bits, off, unit) == offset, (bits, off, unit)
 
 
-@pytest.mark.parametrize("bits,P", [(4, 16), (4, 64), (3, 16)])
+@pytest.mark.parametrize("bits,P", [(4, 16), (4, 64), (3, 16), (2, 16), (2, 64)])
 def test_v_placement_is_a_bijection_onto_the_section(bits, P):
     vb = O.vector_bytes(bits)
+    ub = O.v_unit_bytes(bits)
     seen = set()
     for off in range(P):
-        for u in range(vb // 8):
+        for u in range(vb // ub):
             o = O.v_unit_offset(bits, off, u)
-            assert o % 8 == 0 and 0 <= o < P * vb
+            assert o % ub == 0 and 0 <= o < P * vb
             seen.add(o)
-    assert len(seen) == P * vb // 8
+    assert len(seen) == P * vb // ub
 
 
 def test_savings_printed_on_the_pages():
