@@ -294,7 +294,9 @@ static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tre
   // partial write), so pick the split count that minimises that product.
   const int P = ctx->g.page_size;
   const long long units = (long long)B * ctx->g.num_kv_heads * a.n_tiles_n;
-  const int quantum = 256 / P > 0 ? 256 / P : 1;
+  // one round = every warp of a CTA taking one 32-token pair
+  const int round_tokens = rq::kAttnWarps * rq::kAttnPairTokens;
+  const int quantum = round_tokens / P > 0 ? round_tokens / P : 1;
   const long long min_pps = (max_pages + ctx->max_splits - 1) / ctx->max_splits;
   long long best_pps = -1, best_cost = -1;
   for (int ns = 1; ns <= ctx->max_splits; ++ns) {
@@ -305,8 +307,8 @@ static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tre
     const long long nsplit = (max_pages + pps - 1) / pps;
     if (nsplit > ctx->max_splits) continue;
     const long long rounds = (units * nsplit + ctx->num_sms - 1) / ctx->num_sms;
-    const long long tile_rounds = (pps * (P / 16) + 15) / 16;
-    const long long cost = rounds * (tile_rounds + 2);
+    const long long tile_rounds = (pps * P + round_tokens - 1) / round_tokens;
+    const long long cost = rounds * (tile_rounds + 1);
     if (best_cost < 0 || cost < best_cost) best_cost = cost, best_pps = pps;
   }
   if (best_pps < 0) return RQ_ERR_CAPACITY;

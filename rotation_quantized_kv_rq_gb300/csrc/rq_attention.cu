@@ -29,7 +29,7 @@
 namespace rq {
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = kAttnWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr int kLutBytes = 256 * 256;          // 256 index bytes x (2 tables x 32 lanes x 4 B)
 constexpr int kMaxSplitPages = 1024;          // page ids staged per item

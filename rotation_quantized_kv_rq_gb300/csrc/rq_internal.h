@@ -7,6 +7,8 @@
 namespace rq {
 
 constexpr int kHeadDim = 128;
+constexpr int kAttnWarps = 16;      // warps per split-K attention CTA (one CTA per SM)
+constexpr int kAttnPairTokens = 32; // tokens a warp takes per iteration (two 16-token tiles)
 
 // Device-side copy of what every kernel needs to know about a context.
 struct Geometry {

@@ -116,7 +116,9 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   // Split choice as in the context path (whole 256-token rounds, fewest worst-case rounds),
   // restricted to what the scratch array holds.
   const int P = cfg->page_size;
-  const int quantum = 256 / P > 0 ? 256 / P : 1;
+  // one round = every warp of a CTA taking one 32-token pair
+  const int round_tokens = rq::kAttnWarps * rq::kAttnPairTokens;
+  const int quantum = round_tokens / P > 0 ? round_tokens / P : 1;
   long long best_pps = -1, best_cost = -1, best_ns = 0;
   for (int ns = 1; ns <= kMaxSplits; ++ns) {
     long long pps = (max_pages + ns - 1) / ns;
@@ -125,7 +127,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
     const long long nsplit = (max_pages + pps - 1) / pps;
     if (units * nsplit > (long long)kScratchItems) continue;
     const long long rounds = (units * nsplit + slot->num_sms - 1) / slot->num_sms;
-    const long long cost = rounds * ((pps * (P / 16) + 15) / 16 + 2);
+    const long long cost = rounds * ((pps * P + round_tokens - 1) / round_tokens + 1);
     if (best_cost < 0 || cost < best_cost) best_cost = cost, best_pps = pps, best_ns = nsplit;
   }
   if (best_pps < 0) return RQ_ERR_CAPACITY;
