@@ -50,6 +50,10 @@ DESCRIPTIONS = {
             "append 6 drafts + verify",
     "cfg3_prefill": "rq3_iso quantize-append of 65536 tokens x 8 kv heads (K and V), page 16",
     "cfg4": "rq3_planar decode, 64 x 65536 ctx, 64 q / 8 kv heads, head_dim 128, page 64",
+    "tq4_32k": "tq4 (dense rotation) decode, 32 x 32768 ctx, 64 q / 8 kv heads, head_dim 128, page 16",
+    "tq3_32k": "tq3 (dense rotation) decode, 32 x 32768 ctx, 64 q / 8 kv heads, head_dim 128, page 16",
+    "tq2_32k": "tq2 (dense rotation) decode, 32 x 32768 ctx, 64 q / 8 kv heads, head_dim 128, page 16",
+    "tq3_prefill": "tq3 (dense rotation) quantize-append of 65536 tokens x 8 kv heads (K and V), page 16",
 }
 
 
@@ -91,10 +95,8 @@ class Bench:
     def __init__(self, name, device):
         self.name = name
         self.device = device
-        self.prefill_only = name == "cfg3_prefill"
-        spec = synth.SPECS["cfg3" if self.prefill_only else name]
-        if self.prefill_only:
-            spec = synth.scaled(spec, batch=1, ctx=synth.PREFILL_TOKENS, query_tokens=1, appended=synth.PREFILL_TOKENS)
+        self.prefill_only = name in synth.PREFILL
+        spec = synth.prefill_spec(name) if self.prefill_only else synth.SPECS[name]
         self.spec = spec
         self.wl = synth.workload(spec)
         s, wl = spec, self.wl
@@ -145,7 +147,8 @@ class Bench:
 
     def launches_per_step(self):
         n = 1 if self.k_new is not None else 0
-        return n if self.prefill_only else n + 2
+        # split-K + combine, and for a dense rotation the query pre-rotation
+        return n if self.prefill_only else n + 2 + (self.spec.mode == synth.DENSE)
 
     def tokens_per_step(self):
         if self.prefill_only:
@@ -162,7 +165,8 @@ class Bench:
         token-head, the queries, and the block-table entries it reads."""
         s = self.spec
         pages = int(((self.wl.seq_lens + s.page_size - 1) // s.page_size).sum())
-        return self.packed_bytes() + s.batch * s.query_tokens * s.num_q_heads * 256 + pages * 4
+        q_bytes = 512 if s.mode == synth.DENSE else 256  # fp32 pre-rotated rows, or fp16 q
+        return self.packed_bytes() + s.batch * s.query_tokens * s.num_q_heads * q_bytes + pages * 4
 
     def append_algorithmic_bytes(self):
         n = int(self.slots_new.numel()) if self.slots_new is not None else 0
@@ -262,10 +266,8 @@ def oracle_step_rate(name, budget_s=10.0, max_seqs=None):
     packed cache is built first (untimed), then append + attention are timed per sequence
     until the budget is spent.  Returns (tokens/s, description, seconds)."""
     from oracle import oracle as O
-    prefill_only = name == "cfg3_prefill"
-    spec = synth.SPECS["cfg3" if prefill_only else name]
-    if prefill_only:
-        spec = synth.scaled(spec, batch=1, ctx=synth.PREFILL_TOKENS, query_tokens=1, appended=synth.PREFILL_TOKENS)
+    prefill_only = name in synth.PREFILL
+    spec = synth.prefill_spec(name) if prefill_only else synth.SPECS[name]
     wl = synth.workload(spec)
     q = synth.queries(spec).numpy()
     timed, toks, seqs = 0.0, 0, 0
@@ -313,7 +315,6 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     rate, sample, secs = oracle_step_rate(args.workload, budget_s=args.ref_budget)
-    spec_tokens = synth.SPECS.get(args.workload, synth.SPECS["cfg3"])
     line = {
         "impl": "reference", "metric": "decode-attn tokens/s", "value": rate, "unit": "tokens/s", "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,

@@ -4,8 +4,9 @@
  * The method ("SGLang 1-Bit Turbo" README, section "RotorQuant KV Cache Compression", and
  * the TurboQuant section it is compared with): every K and V vector written to the cache
  * keeps its L2 norm, is turned by a fixed data-oblivious rotation -- 2D Givens pairs
- * (PlanarQuant) or 4D unit-quaternion blocks (IsoQuant) -- and each rotated coordinate is
- * coded with a b-bit Lloyd-Max scalar quantizer (modes rq3/rq4 x planar/iso).  Attention
+ * (PlanarQuant), 4D unit-quaternion blocks (IsoQuant) or one dense orthogonal matrix
+ * (TurboQuant) -- and each rotated coordinate is coded with a b-bit Lloyd-Max scalar
+ * quantizer (rq3/rq4 x planar/iso, tq2/tq3/tq4 dense; every mode takes 2, 3 or 4 bits).  Attention
  * reads the packed cache directly: because the rotation is orthogonal, a query is rotated
  * once instead of un-rotating every key, values are summed in the rotated space and the
  * output is rotated back once.
@@ -34,6 +35,9 @@
  *                 tokens are stored as pairs: pair p = tokens (2p, 2p+1) fills 128 bytes and the
  *                 8 bytes of 16-dim group c of token 2p + h sit at 16 * (c ^ (2p mod 8)) + 8h.
  *                 K codes, and 3-bit V codes, are stored token after token.
+ *   2-bit codes : byte j = code[4j] | code[4j+1] << 2 | code[4j+2] << 4 | code[4j+3] << 6.  In
+ *                 the V-codes section, pair p = tokens (2p, 2p+1) fills 64 bytes and the 4 bytes
+ *                 of 16-dim group c of token 2p + h sit at 8 * (c ^ (4 * (p / 2 mod 2))) + 4h.
  *   3-bit codes : per 32-dim group w, 12 bytes at 12w = little-endian words W0, W1, W2:
  *                 W0 bits 2i.. = code[32w+i] & 3, W1 bits 2i.. = code[32w+16+i] & 3
  *                 (i = 0..15), W2 bit p(i) = code[32w+i] >> 2 with i = 16h + 4k + r and
@@ -58,7 +62,7 @@ extern "C" {
 /* Return codes */
 #define RQ_OK 0
 #define RQ_ERR_INVALID 1       /* a NULL pointer, a negative size, inconsistent geometry */
-#define RQ_ERR_UNSUPPORTED 2   /* valid but not built: head_dim != 128, bits not 3/4, ... */
+#define RQ_ERR_UNSUPPORTED 2   /* valid but not built: head_dim != 128, bits not 2/3/4, ... */
 #define RQ_ERR_CUDA 3          /* a CUDA call failed (allocation, copy or launch) */
 #define RQ_ERR_CAPACITY 4      /* batch, query tokens or block-table width above the context's limits */
 
@@ -70,9 +74,10 @@ extern "C" {
 #define RQ_STATUS_TIMEOUT 16   /* an attention kernel's staged page copy did not complete within
                                   its bounded wait (outputs of that call are unspecified) */
 
-/* Rotation families ("--kv-cache-dtype rq{3,4}_{planar,iso}") */
+/* Rotation families ("--kv-cache-dtype rq{3,4}_{planar,iso}", TurboQuant "tq{2,3,4}") */
 #define RQ_PLANAR 0            /* PlanarQuant: 2D Givens rotation per dimension pair */
 #define RQ_ISO 1               /* IsoQuant: unit quaternion per 4-dimension block */
+#define RQ_DENSE 2             /* TurboQuant: one dense orthogonal head_dim x head_dim matrix */
 
 typedef struct rq_ctx rq_ctx;  /* opaque, owned by the library */
 
@@ -80,17 +85,20 @@ typedef struct {
   int head_dim;              /* must be 128 */
   int num_q_heads;           /* Hq, a multiple of num_kv_heads */
   int num_kv_heads;          /* Hkv >= 1 */
-  int bits;                  /* 3 or 4 */
-  int mode;                  /* RQ_PLANAR or RQ_ISO */
+  int bits;                  /* 2, 3 or 4 */
+  int mode;                  /* RQ_PLANAR, RQ_ISO or RQ_DENSE */
   int page_size;             /* P: a multiple of 16, at most 256 */
   int num_pages;             /* pages in the caller's pool */
   int max_batch;             /* largest B of an attention call */
   int max_query_tokens;      /* largest T of a verify call (>= 1) */
   int max_pages_per_seq;     /* largest block-table width (max_pages) of an attention call */
-  /* host float32 [num_kv_heads][head_dim]: planar -> [Hkv][d/2][2] = (cos t, sin t) of the
-     pair (2i, 2i+1), y_2i = c x_2i - s x_2i+1, y_2i+1 = s x_2i + c x_2i+1;
+  /* host float32.  planar -> [Hkv][d/2][2] = (cos t, sin t) of the pair (2i, 2i+1),
+     y_2i = c x_2i - s x_2i+1, y_2i+1 = s x_2i + c x_2i+1;
      iso -> [Hkv][d/4][4] = unit quaternion (a, b, c, d) of block 4i..4i+3, y = q (x) x
-     (Hamilton product, q on the left).  rot_k turns keys and queries, rot_v values. */
+     (Hamilton product, q on the left);
+     dense -> [Hkv][d][d] = row-major R, y_i = sum_j R[i][j] x_j.  R must be orthogonal (the
+     library does not check; decoding multiplies by R^T).
+     rot_k turns keys and queries, rot_v values. */
   const float *rot_k;
   const float *rot_v;
   /* host float32 [2^bits] ascending centroids, or NULL for the Lloyd-Max quantizer of
@@ -182,7 +190,8 @@ int rq_tree_verify_attention(rq_ctx *ctx, const void *q, int T, const uint64_t *
  * everything comes in as arguments:
  *   cfg         host; only head_dim, num_q_heads, num_kv_heads, bits, mode, page_size, num_pages
  *               and sm_scale are read (the max_* limits, host tables, codebook and device are
- *               ignored)
+ *               ignored).  mode RQ_DENSE returns RQ_ERR_UNSUPPORTED (its query rotation needs
+ *               a workspace).
  *   d_rot_k, d_rot_v   device float32 [Hkv][head_dim], laid out as rq_config.rot_k / rot_v
  *   d_centroids        device float32 [2^bits], ascending (e.g. from rq_lloyd_max_codebook)
  *   other arguments    as rq_decode_attention, on the CURRENT device

@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/rq.h: argument validation, the context (device
 // tables and split-K workspace), the default Lloyd-Max codebook and launch planning.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -17,6 +18,9 @@ struct rq_ctx {
   int device;
   int num_sms;
   float* d_tables;        // rot_k | rot_v | centroids | boundaries
+  __half* d_dense16;      // dense: fp16 hi/lo split of R_k and R_v for the append GEMM
+  float* d_dense32;       // dense: fp32 R_k and R_v, row-major, for the append's exact recompute
+  float* d_qrot;          // dense: fp32 R_k q of one attention call [max_batch][max_T][Hq][128]
   float* d_ws;            // split-K partials
   int* d_counters;        // attention work-item counters (2 ints, zero between launches)
   size_t ws_floats;
@@ -88,10 +92,10 @@ int check_geometry(const rq_config* c) {
       c->max_batch <= 0 || c->max_query_tokens <= 0 || c->max_pages_per_seq <= 0)
     return RQ_ERR_INVALID;
   if (c->num_q_heads % c->num_kv_heads != 0) return RQ_ERR_INVALID;
-  if (c->mode != RQ_PLANAR && c->mode != RQ_ISO) return RQ_ERR_INVALID;
+  if (c->mode != RQ_PLANAR && c->mode != RQ_ISO && c->mode != RQ_DENSE) return RQ_ERR_INVALID;
   if (!c->rot_k || !c->rot_v) return RQ_ERR_INVALID;
   if (c->head_dim != rq::kHeadDim) return RQ_ERR_UNSUPPORTED;
-  if (c->bits != 3 && c->bits != 4) return RQ_ERR_UNSUPPORTED;
+  if (c->bits < 2 || c->bits > 4) return RQ_ERR_UNSUPPORTED;
   if (c->page_size % 16 != 0 || c->page_size > 256) return RQ_ERR_UNSUPPORTED;
   if ((long long)c->num_pages * c->page_size > INT32_MAX) return RQ_ERR_UNSUPPORTED;
   if (!(c->sm_scale >= 0.0f) || std::isinf(c->sm_scale)) return RQ_ERR_INVALID;
@@ -164,7 +168,8 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   }
 
   const int hkv = cfg->num_kv_heads, d = cfg->head_dim;
-  const size_t rot = (size_t)hkv * d;
+  const bool dense = cfg->mode == RQ_DENSE;
+  const size_t rot = (size_t)hkv * d * (dense ? d : 1);
   const size_t table_floats = 2 * rot + 256 + 256;
   const int group = cfg->num_q_heads / hkv;
   ctx->max_n_tiles = (cfg->max_query_tokens * group + 7) / 8;
@@ -178,24 +183,63 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   if (e == cudaSuccess) e = cudaMalloc(&ctx->d_ws, ctx->ws_floats * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&ctx->d_counters, 2 * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(ctx->d_counters, 0, 2 * sizeof(int));
+  const size_t dense16_halves = dense ? 2 * rot * 2 : 0;  // [K, V][Hkv][hi, lo][d][d]
+  if (e == cudaSuccess && dense) {
+    e = cudaMalloc(&ctx->d_dense16, dense16_halves * sizeof(__half));
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_dense32, 2 * rot * sizeof(float));
+    if (e == cudaSuccess) e = cudaMemcpy(ctx->d_dense32, cfg->rot_k, rot * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(ctx->d_dense32 + rot, cfg->rot_v, rot * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMalloc(&ctx->d_qrot, (size_t)cfg->max_batch * cfg->max_query_tokens * cfg->num_q_heads * d * sizeof(float));
+  }
   float* host = nullptr;
+  __half* host16 = nullptr;
   if (e == cudaSuccess) {
     host = (float*)std::calloc(table_floats, sizeof(float));
-    if (!host) e = cudaErrorMemoryAllocation;
+    if (dense) host16 = (__half*)std::calloc(dense16_halves, sizeof(__half));
+    if (!host || (dense && !host16)) e = cudaErrorMemoryAllocation;
   }
   if (e == cudaSuccess) {
-    std::memcpy(host, cfg->rot_k, rot * sizeof(float));
-    std::memcpy(host + rot, cfg->rot_v, rot * sizeof(float));
+    if (dense) {
+      // rot_k is kept transposed (the query rotation walks it by columns), rot_v as given, and
+      // both are split into fp16 hi + lo for the append's tensor-core GEMM.
+      for (int h = 0; h < hkv; ++h)
+        for (int i = 0; i < d; ++i)
+          for (int m = 0; m < d; ++m) host[((size_t)h * d + m) * d + i] = cfg->rot_k[((size_t)h * d + i) * d + m];
+      std::memcpy(host + rot, cfg->rot_v, rot * sizeof(float));
+      for (int kind = 0; kind < 2; ++kind) {
+        const float* R = kind ? cfg->rot_v : cfg->rot_k;
+        for (int h = 0; h < hkv; ++h)
+          for (size_t e2 = 0; e2 < (size_t)d * d; ++e2) {
+            const double x = (double)R[(size_t)h * d * d + e2];
+            const __half hi = __double2half(x);
+            const __half lo = __double2half(x - (double)__half2float(hi));
+            __half* dst = host16 + (((size_t)kind * hkv + h) * 2) * d * d;
+            dst[e2] = hi;
+            dst[(size_t)d * d + e2] = lo;
+          }
+      }
+      e = cudaMemcpy(ctx->d_dense16, host16, dense16_halves * sizeof(__half), cudaMemcpyHostToDevice);
+    } else {
+      std::memcpy(host, cfg->rot_k, rot * sizeof(float));
+      std::memcpy(host + rot, cfg->rot_v, rot * sizeof(float));
+    }
     std::memcpy(host + 2 * rot, ctx->centroids, L * sizeof(float));
     std::memcpy(host + 2 * rot + 256, ctx->boundaries, (L - 1) * sizeof(float));
-    e = cudaMemcpy(ctx->d_tables, host, table_floats * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(ctx->d_tables, host, table_floats * sizeof(float), cudaMemcpyHostToDevice);
   }
   std::free(host);
+  std::free(host16);
   if (e == cudaSuccess) e = rq::attention_prepare();
+  if (e == cudaSuccess) e = rq::append_prepare();
   if (e != cudaSuccess) {
     cudaFree(ctx->d_tables);
     cudaFree(ctx->d_ws);
     cudaFree(ctx->d_counters);
+    cudaFree(ctx->d_dense16);
+    cudaFree(ctx->d_dense32);
+    cudaFree(ctx->d_qrot);
     delete ctx;
     return RQ_ERR_CUDA;
   }
@@ -214,6 +258,8 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   g.q_scale = (float)(scale * 1.44269504088896340736);
   g.rot_k = ctx->d_tables;
   g.rot_v = ctx->d_tables + rot;
+  g.dense16 = ctx->d_dense16;
+  g.dense32 = ctx->d_dense32;
   g.centroids = ctx->d_tables + 2 * rot;
   g.boundaries = ctx->d_tables + 2 * rot + 256;
   *out = ctx;
@@ -227,6 +273,9 @@ void rq_free(rq_ctx* ctx) {
     cudaFree(ctx->d_tables);
     cudaFree(ctx->d_ws);
     cudaFree(ctx->d_counters);
+    cudaFree(ctx->d_dense16);
+    cudaFree(ctx->d_dense32);
+    cudaFree(ctx->d_qrot);
   }
   delete ctx;
 }
@@ -253,6 +302,7 @@ int rq_quantize_append(rq_ctx* ctx, const void* k, const void* v, const int32_t*
   if (!ctx || n < 0) return RQ_ERR_INVALID;
   if (n == 0) return RQ_OK;
   if (!k || !v || !slot_mapping || !kv_pages) return RQ_ERR_INVALID;
+  if ((uintptr_t)k % 16 != 0 || (uintptr_t)v % 16 != 0) return RQ_ERR_INVALID;  // 16-byte vector loads
   DeviceScope scope(ctx->device);
   if (!scope.ok()) return RQ_ERR_CUDA;
   return to_status(rq::launch_append(ctx->g, k, v, slot_mapping, n, (uint8_t*)kv_pages, d_status,
@@ -281,6 +331,7 @@ static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tre
   a.out = out;
   a.status = d_status;
   a.tree_mask = tree_mask;
+  a.q_rot = ctx->d_qrot;  // null unless dense
   a.ws = ctx->d_ws;
   a.rows = T * ctx->g.group;
   a.n_tiles_n = (a.rows + 7) / 8;

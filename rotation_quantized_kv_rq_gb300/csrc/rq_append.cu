@@ -1,13 +1,25 @@
 // Fused quantize-pack-append ("SGLang 1-Bit Turbo" README, section "RotorQuant KV Cache
 // Compression": norm, fixed data-oblivious rotation -- 2D Givens pairs or 4D quaternion
-// blocks -- then Lloyd-Max scalar codes, bit-packed into the paged cache).
+// blocks -- then Lloyd-Max scalar codes, bit-packed into the paged cache; section "TurboQuant
+// KV Cache Compression" for the dense random rotation).
 //
-// Work item = one (token, kv head).  A warp takes items in a grid-stride loop: lanes 0-15
-// encode the K vector and lanes 16-31 the V vector.  Lane j of a half owns dimensions
-// 8j..8j+7 -- four whole Givens pairs or two whole quaternion blocks -- so the rotation is
-// lane-local and only the squared norm is reduced (4 xor-shuffles within the half).  Each lane
-// reads 16 bytes, and the next item's 16 bytes are in flight while the current one is coded.
-// The kernel is bound by HBM: 512 bytes of fp16 in, 2 * (16 * bits + 2) bytes out per item.
+// Structured rotations (planar / iso): work item = one (token, kv head).  A warp takes items
+// in a grid-stride loop: lanes 0-15 encode the K vector and lanes 16-31 the V vector.  Lane j
+// of a half owns dimensions 8j..8j+7 -- four whole Givens pairs or two whole quaternion
+// blocks -- so the rotation is lane-local and only the squared norm is reduced (4
+// xor-shuffles within the half).  Each lane reads 16 bytes, and the next item's 16 bytes are
+// in flight while the current one is coded.  The kernel is bound by HBM: 512 bytes of fp16
+// in, 2 * (16 * bits + 2) bytes out per item.
+//
+// Dense rotation: Y = X R^T for a tile of 64 vectors of one (kv head, K or V) is a small GEMM
+// (64 x 128 x 128) on the tensor cores.  X is fp16 and exact as an operand; R (fp32) is split
+// as R = hi + lo with hi = fp16(R), lo = fp16(R - hi), both multiplied into one fp32
+// accumulator.  That carries R to ~6e-8 per entry, but the tensor cores' fp32 accumulation is
+// not correctly rounded, so a coordinate whose u lies within kFixBand of a boundary is
+// recomputed exactly -- a compensated fp32 dot product (error-free products and sums) against
+// the fp32 R, shared by the vector's half-warp -- before it is coded.  Codes then differ from
+// the fp64 definition only as rarely as the structured kernel's.  The coding epilogue is the
+// one the structured kernel uses, on Y staged in shared memory.
 #include <cuda_fp16.h>
 
 #include "rq_internal.h"
@@ -21,22 +33,135 @@ constexpr int kAppendWarps = kAppendThreads / 32;
 
 // Number of boundaries strictly below u (b ascending, in registers): a binary search written as
 // a select tree, one compare per level and no indexed memory.
-__device__ __forceinline__ int code_of(float u, const float (&b)[15], int bits) {
-  if (bits == 3) {
+template <int BITS>
+__device__ __forceinline__ int code_of(float u, const float (&b)[15]) {
+  if constexpr (BITS == 2) {
+    const bool s1 = u > b[1];
+    const bool s0 = u > (s1 ? b[2] : b[0]);
+    return (s1 ? 2 : 0) + (s0 ? 1 : 0);
+  } else if constexpr (BITS == 3) {
     const bool s2 = u > b[3];
     const bool s1 = u > (s2 ? b[5] : b[1]);
     const bool s0 = u > (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
     return (s2 ? 4 : 0) + (s1 ? 2 : 0) + (s0 ? 1 : 0);
+  } else {
+    const bool s3 = u > b[7];
+    const bool s2 = u > (s3 ? b[11] : b[3]);
+    const bool s1 = u > (s3 ? (s2 ? b[13] : b[9]) : (s2 ? b[5] : b[1]));
+    const float m0 = s3 ? (s2 ? (s1 ? b[14] : b[12]) : (s1 ? b[10] : b[8]))
+                        : (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
+    const bool s0 = u > m0;
+    return (s3 ? 8 : 0) + (s2 ? 4 : 0) + (s1 ? 2 : 0) + (s0 ? 1 : 0);
   }
-  const bool s3 = u > b[7];
-  const bool s2 = u > (s3 ? b[11] : b[3]);
-  const bool s1 = u > (s3 ? (s2 ? b[13] : b[9]) : (s2 ? b[5] : b[1]));
-  const float m0 = s3 ? (s2 ? (s1 ? b[14] : b[12]) : (s1 ? b[10] : b[8]))
-                      : (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
-  const bool s0 = u > m0;
-  return (s3 ? 8 : 0) + (s2 ? 4 : 0) + (s1 ? 2 : 0) + (s0 ? 1 : 0);
 }
 
+// code_of that also returns the distance from u to the nearest boundary: the boundaries on
+// either side of u are both among those the search compares against.
+template <int BITS>
+__device__ __forceinline__ int code_of_margin(float u, const float (&b)[15], float& dmin) {
+  if constexpr (BITS == 2) {
+    const bool s1 = u > b[1];
+    const float m0 = s1 ? b[2] : b[0];
+    dmin = fminf(fabsf(u - b[1]), fabsf(u - m0));
+    return (s1 ? 2 : 0) + (u > m0 ? 1 : 0);
+  } else if constexpr (BITS == 3) {
+    const bool s2 = u > b[3];
+    const float m1 = s2 ? b[5] : b[1];
+    const bool s1 = u > m1;
+    const float m0 = s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]);
+    dmin = fminf(fminf(fabsf(u - b[3]), fabsf(u - m1)), fabsf(u - m0));
+    return (s2 ? 4 : 0) + (s1 ? 2 : 0) + (u > m0 ? 1 : 0);
+  } else {
+    const bool s3 = u > b[7];
+    const float m2 = s3 ? b[11] : b[3];
+    const bool s2 = u > m2;
+    const float m1 = s3 ? (s2 ? b[13] : b[9]) : (s2 ? b[5] : b[1]);
+    const bool s1 = u > m1;
+    const float m0 = s3 ? (s2 ? (s1 ? b[14] : b[12]) : (s1 ? b[10] : b[8]))
+                        : (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
+    dmin = fminf(fminf(fabsf(u - b[7]), fabsf(u - m2)), fminf(fabsf(u - m1), fabsf(u - m0)));
+    return (s3 ? 8 : 0) + (s2 ? 4 : 0) + (s1 ? 2 : 0) + (u > m0 ? 1 : 0);
+  }
+}
+
+// Packs the codes of dims 8j..8j+7 (j = lane within its half-warp) of one vector and writes
+// them and the fp16 norm to the vector's place in `chunk` (kind 0 = K, 1 = V; `off` = offset
+// in page).  Every lane of the warp must call it: the 3-bit packing exchanges high bits
+// between lanes j and j ^ 2.  With `store` false nothing is written.
+template <int BITS>
+__device__ __forceinline__ void pack_store(const int (&code)[8], float nrm, uint8_t* chunk, int page_size, int kind,
+                                           int off, int j, bool store, int32_t* status) {
+  constexpr int vb = BITS * 16;
+  uint8_t* dst = chunk + (size_t)kind * page_size * vb + (size_t)off * vb;
+  uint8_t* vsec = chunk + (size_t)page_size * vb;
+  const int pair = off >> 1, hv = off & 1, c = j >> 1;  // V pair placement (2- and 4-bit)
+  if constexpr (BITS == 4) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) word |= (uint32_t)code[e] << (4 * e);
+    if (store) {
+      if (kind == 0) {
+        *reinterpret_cast<uint32_t*>(dst + 4 * j) = word;
+      } else {
+        // V: token pairs (2p, 2p+1) share 128 bytes; the 8-byte unit of 16-dim group c of
+        // token 2p + h sits at 16 * (c ^ (2p mod 8)) + 8h.  Lane j holds half of unit j / 2.
+        *reinterpret_cast<uint32_t*>(vsec + pair * 128 + 16 * (c ^ ((2 * pair) & 7)) + 8 * hv + 4 * (j & 1)) = word;
+      }
+    }
+  } else if constexpr (BITS == 2) {
+    uint32_t half_word = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) half_word |= (uint32_t)code[e] << (2 * e);
+    if (store) {
+      if (kind == 0) {
+        *reinterpret_cast<uint16_t*>(dst + 2 * j) = (uint16_t)half_word;
+      } else {
+        // V: token pairs share 64 bytes; the 4-byte unit of group c of token 2p + h sits at
+        // 8 * (c ^ (4 * (p / 2 mod 2))) + 4h.  Lane j holds half of unit j / 2.
+        *reinterpret_cast<uint16_t*>(vsec + pair * 64 + 8 * (c ^ (4 * ((pair >> 1) & 1))) + 4 * hv + 2 * (j & 1)) =
+            (uint16_t)half_word;
+      }
+    }
+  } else {
+    // Lane j covers dims 8m..8m+7 of 32-dim group w = j/4 (m = j%4).  Its low bits are
+    // bytes 2m, 2m+1 of the group's W0|W1; its high bits fill half of bytes 2(m&1) and
+    // 2(m&1)+1 of W2, shared with lane j^2 (same k, other h).
+    const int w = j >> 2, m = j & 3, hh = m >> 1;
+    uint32_t lo = 0, hib = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      lo |= (uint32_t)(code[e] & 3) << (2 * e);
+      const int r = e & 3, kk = e >> 2;  // dim 8m + e = 16hh + 4(2(m&1) + kk) + r
+      const int off_r = (r < 2) ? 4 + r : r - 2;
+      hib |= (uint32_t)(code[e] >> 2) << (8 * kk + 2 * hh + off_r);
+    }
+    const uint32_t partner = __shfl_xor_sync(0xffffffffu, hib, 2);
+    if (store) {
+      *reinterpret_cast<uint16_t*>(dst + 12 * w + 2 * m) = (uint16_t)lo;
+      if (hh == 0) *reinterpret_cast<uint16_t*>(dst + 12 * w + 8 + 2 * (m & 1)) = (uint16_t)(hib | partner);
+    }
+  }
+  if (store && j == 0) {
+    const __half n16 = __float2half_rn(nrm);
+    uint8_t* nb = chunk + (size_t)2 * page_size * vb + (size_t)kind * 2 * page_size + 2 * off;
+    *reinterpret_cast<__half*>(nb) = n16;
+    if (status && __hisinf(n16)) atomicOr(status, RQ_STATUS_NORM_OVERFLOW);
+  }
+}
+
+// 1 / n, so that u = y / n is formed as y * (1/n): within an ulp of the quotient, so a code can
+// differ from the quotient's only for u within ~1e-7 of a boundary.  n = 0 gives u = 0.
+__device__ __forceinline__ float inv_norm(float nrm) { return nrm > 0.f ? __frcp_rn(nrm) : 0.f; }
+
+template <int BITS>
+__device__ __forceinline__ void load_boundaries(float (&bnd)[15], const float* boundaries) {
+#pragma unroll
+  for (int i = 0; i < 15; ++i) bnd[i] = i < (1 << BITS) - 1 ? __ldg(boundaries + i) : 0.f;
+}
+
+// ---------------------------------------------------------------------------------------
+// Structured rotations
+// ---------------------------------------------------------------------------------------
 struct Item {
   int t, h, slot;
   uint4 raw;  // 8 fp16 of this lane's half (K or V)
@@ -57,8 +182,7 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
               const int32_t* __restrict__ slots, int n, uint8_t* __restrict__ pages,
               int32_t* __restrict__ status) {
   float bnd[15];
-#pragma unroll
-  for (int i = 0; i < 15; ++i) bnd[i] = i < (1 << BITS) - 1 ? __ldg(g.boundaries + i) : 0.f;
+  load_boundaries<BITS>(bnd, g.boundaries);
 
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;        // 0: K, 1: V
@@ -66,7 +190,6 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
   const long long items = (long long)n * g.num_kv_heads;
   const long long stride = (long long)gridDim.x * kAppendWarps;
   const float* rot = half ? g.rot_v : g.rot_k;
-  const int vb = BITS * 16;
   const long long pool_slots = (long long)g.num_pages * g.page_size;
 
   long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
@@ -117,79 +240,294 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
           y[4 * q + 3] = d * xb[0] - c * xb[1] + b * xb[2] + a * xb[3];
         }
       }
-      // u = y / n as y * (1/n): within an ulp of the quotient, so a code can differ from the
-      // quotient's only for u within ~1e-7 of a boundary.
-      const float rcp = nrm > 0.f ? __frcp_rn(nrm) : 0.f;
+      const float rcp = inv_norm(nrm);
       int code[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) code[e] = code_of(y[e] * rcp, bnd, BITS);
-
+      for (int e = 0; e < 8; ++e) code[e] = code_of<BITS>(y[e] * rcp, bnd);
       const int page = slot / g.page_size, off = slot % g.page_size;
       uint8_t* chunk = pages + ((size_t)page * g.num_kv_heads + cur.h) * (size_t)g.page_bytes;
-      uint8_t* dst = chunk + (size_t)half * g.page_size * vb + (size_t)off * vb;
-      if (BITS == 4) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) word |= (uint32_t)code[e] << (4 * e);
-        if (half == 0) {
-          *reinterpret_cast<uint32_t*>(dst + 4 * j) = word;
-        } else {
-          // V: token pairs (2p, 2p+1) share 128 bytes; the 8-byte unit of 16-dim group c of
-          // token 2p + h sits at 16 * (c ^ (2p mod 8)) + 8h.  Lane j holds half of unit j / 2.
-          const int pair = off >> 1, hv = off & 1, c = j >> 1;
-          uint8_t* vsec = chunk + (size_t)g.page_size * vb;
-          *reinterpret_cast<uint32_t*>(vsec + pair * 128 + 16 * (c ^ ((2 * pair) & 7)) + 8 * hv + 4 * (j & 1)) = word;
-        }
-      } else {
-        // Lane j covers dims 8m..8m+7 of 32-dim group w = j/4 (m = j%4).  Its low bits are
-        // bytes 2m, 2m+1 of the group's W0|W1; its high bits fill half of bytes 2(m&1) and
-        // 2(m&1)+1 of W2, shared with lane j^2 (same k, other h).
-        const int w = j >> 2, m = j & 3, hh = m >> 1;
-        uint32_t lo = 0, hib = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          lo |= (uint32_t)(code[e] & 3) << (2 * e);
-          const int r = e & 3, kk = e >> 2;  // dim 8m + e = 16hh + 4(2(m&1) + kk) + r
-          const int off_r = (r < 2) ? 4 + r : r - 2;
-          hib |= (uint32_t)(code[e] >> 2) << (8 * kk + 2 * hh + off_r);
-        }
-        const uint32_t partner = __shfl_xor_sync(0xffffffffu, hib, 2);
-        *reinterpret_cast<uint16_t*>(dst + 12 * w + 2 * m) = (uint16_t)lo;
-        if (hh == 0) *reinterpret_cast<uint16_t*>(dst + 12 * w + 8 + 2 * (m & 1)) = (uint16_t)(hib | partner);
-      }
-      if (j == 0) {
-        const __half n16 = __float2half_rn(nrm);
-        uint8_t* nb = chunk + (size_t)2 * g.page_size * vb + (size_t)half * 2 * g.page_size + 2 * off;
-        *reinterpret_cast<__half*>(nb) = n16;
-        if (status && __hisinf(n16)) atomicOr(status, RQ_STATUS_NORM_OVERFLOW);
-      }
+      pack_store<BITS>(code, nrm, chunk, g.page_size, half, off, j, true, status);
     }
     cur = nxt;
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Dense rotation (tensor cores)
+// ---------------------------------------------------------------------------------------
+constexpr int kDenseRows = 64;                 // vectors per tile
+constexpr int kDenseThreads = 512;             // 16 warps: 4 row tiles x 4 column quarters
+constexpr int kYStride = 136;                  // floats per staged Y row (conflict-free float2 stores)
+constexpr int kSmemR = 0;                      // fp16 [2 (hi, lo)][128][128], 16-byte chunks swizzled
+constexpr int kSmemX = kSmemR + 2 * 128 * 128 * 2;            // fp16 [2 buffers][64][128], swizzled
+constexpr int kSmemY = kSmemX + 2 * kDenseRows * 128 * 2;     // fp32 [64][136]
+constexpr int kSmemR32 = kSmemY + kDenseRows * kYStride * 4;  // fp32 [128][128] R (exact recompute)
+constexpr int kDenseSmem = kSmemR32 + 128 * 128 * 4;           // 198,656 bytes
+// Tensor-core Y is trusted to decide a code when u is farther than this from every boundary.
+// Its error is the hi + lo split (|R - hi - lo| <= 6e-8 per entry, so <= 7e-7 in u by
+// Cauchy-Schwarz) plus the accumulation of 16 fp32 MMA steps (a few fp32 ulps of n each).
+constexpr float kFixBand = 1e-5f;
+
+// A 256-byte row of 16 chunks (8 fp16 each) stores chunk c at position c ^ (row mod 8), so the
+// eight rows one ldmatrix phase reads fall in eight different 16-byte bank groups.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(row * 256 + ((chunk ^ (row & 7)) << 4)); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Tile t covers tokens 64 * (t / (2 Hkv)) .. +63 of kv head hk % Hkv, K (hk < Hkv) or V, with
+// hk = t % (2 Hkv).  Rows past n are zero-filled.
+__device__ __forceinline__ void issue_x(uint32_t xs, long long tile, const Geometry& g, const __half* k,
+                                       const __half* v, int n, uint8_t* xs_generic) {
+  const int hkv = g.num_kv_heads;
+  const int hk = (int)(tile % (2 * hkv));
+  const long long blk = tile / (2 * hkv);
+  const int kind = hk / hkv, h = hk % hkv;
+  const __half* src = kind ? v : k;
+  for (int i = threadIdx.x; i < kDenseRows * 16; i += kDenseThreads) {
+    const int r = i >> 4, c = i & 15;
+    const long long t = blk * kDenseRows + r;
+    if (t < n) {
+      cp_async16(xs + swz(r, c), src + ((size_t)t * hkv + h) * kHeadDim + 8 * c);
+    } else {
+      *reinterpret_cast<uint4*>(xs_generic + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+// y_i = sum_m x_m R[i][m] for one vector, summed exactly enough to be correctly rounded in all
+// but pathological cases: error-free products (fma) and error-free sums (two-sum), the rounding
+// errors carried in a second word.  Lane j of the half-warp holds x[8j..8j+7]; `row` is R's row
+// i in shared memory.  Every lane of the warp calls it (shuffles stay within each half).
+__device__ __forceinline__ float dot_compensated(const float (&x)[8], const float* row, int j) {
+  const float4 r0 = *reinterpret_cast<const float4*>(row + 8 * j);
+  const float4 r1 = *reinterpret_cast<const float4*>(row + 8 * j + 4);
+  const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+  float s = 0.f, c = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float p = x[e] * rr[e];
+    const float pe = fmaf(x[e], rr[e], -p);  // x * r = p + pe exactly
+    const float t = s + p;
+    const float z = t - s;
+    c += ((s - (t - z)) + (p - z)) + pe;     // s + p = t + (that) exactly
+    s = t;
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+    const float t = s + s2;
+    const float z = t - s;
+    c += c2 + ((s - (t - z)) + (s2 - z));
+    s = t;
+  }
+  return s + c;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kDenseThreads, 1)
+append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict__ v,
+                    const int32_t* __restrict__ slots, int n, uint8_t* __restrict__ pages,
+                    int32_t* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem);
+  float* Ys = reinterpret_cast<float*>(smem + kSmemY);
+  float bnd[15];
+  load_boundaries<BITS>(bnd, g.boundaries);
+
+  const int hkv = g.num_kv_heads;
+  const long long nblk = ((long long)n + kDenseRows - 1) / kDenseRows;
+  const long long tiles = 2LL * hkv * nblk;
+  const long long pool_slots = (long long)g.num_pages * g.page_size;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int mt = warp & 3, nq = warp >> 2;  // rows 16mt.., columns 32nq..
+  const int half = lane >> 4, j = lane & 15;
+
+  long long tile = blockIdx.x;
+  if (tile >= tiles) return;
+  int buf = 0, cur_hk = -1;
+  issue_x(base + kSmemX, tile, g, k, v, n, smem + kSmemX);
+  cp_async_commit();
+  for (; tile < tiles; tile += gridDim.x) {
+    const int hk = (int)(tile % (2 * hkv));
+    const long long blk = tile / (2 * hkv);
+    const int kind = hk / hkv, h = hk % hkv;
+    if (hk != cur_hk) {  // stage R of this (K or V, head); the previous tile is done with it
+      const uint4* src = reinterpret_cast<const uint4*>(g.dense16 + ((size_t)kind * hkv + h) * 2 * 128 * 128);
+      for (int i = threadIdx.x; i < 2 * 128 * 16; i += kDenseThreads) {
+        const int hl = i >> 11, row = (i >> 4) & 127, c = i & 15;
+        *reinterpret_cast<uint4*>(smem + kSmemR + hl * 32768 + swz(row, c)) = __ldg(src + i);
+      }
+      const float4* src32 = reinterpret_cast<const float4*>(g.dense32 + ((size_t)kind * hkv + h) * 128 * 128);
+      for (int i = threadIdx.x; i < 128 * 32; i += kDenseThreads)
+        reinterpret_cast<float4*>(smem + kSmemR32)[i] = __ldg(src32 + i);
+      cur_hk = hk;
+    }
+    const long long next = tile + gridDim.x;
+    const uint32_t xs_next = base + kSmemX + (uint32_t)((buf ^ 1) * kDenseRows * 256);
+    if (next < tiles) issue_x(xs_next, next, g, k, v, n, smem + kSmemX + (buf ^ 1) * kDenseRows * 256);
+    cp_async_commit();
+    cp_async_wait1();
+    __syncthreads();  // this tile's X (and R, if restaged) visible to every warp
+
+    const uint32_t xs = base + kSmemX + (uint32_t)(buf * kDenseRows * 256);
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll 2
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t a[4];
+      // matrices: rows 0-7 / 8-15 of the row tile, k chunks 2ks / 2ks+1 -> a0, a1, a2, a3
+      ldsm_x4(a, xs + swz(16 * mt + (lane & 15), 2 * ks + (lane >> 4)));
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        const int nrow = 8 * (4 * nq + 2 * np + (lane >> 4)) + (lane & 7);
+        const int kc = 2 * ks + ((lane >> 3) & 1);
+#pragma unroll
+        for (int hl = 0; hl < 2; ++hl) {
+          uint32_t b[4];  // b0, b1 of n-tile 2np, then of 2np + 1
+          ldsm_x4(b, base + kSmemR + hl * 32768 + swz(nrow, kc));
+          mma16816(acc[2 * np], a, b[0], b[1]);
+          mma16816(acc[2 * np + 1], a, b[2], b[3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int col = 32 * nq + 8 * nt + 2 * tq;
+      *reinterpret_cast<float2*>(Ys + (16 * mt + gq) * kYStride + col) = make_float2(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<float2*>(Ys + (16 * mt + gq + 8) * kYStride + col) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+    __syncthreads();
+
+    // Coding: a half-warp per vector, lane j on dims 8j..8j+7 (32 vectors per pass).
+    const uint8_t* xg = smem + kSmemX + buf * kDenseRows * 256;
+#pragma unroll 1
+    for (int pass = 0; pass < kDenseRows / 32; ++pass) {
+      const int r = 32 * pass + 2 * warp + half;
+      const long long t = blk * kDenseRows + r;
+      int slot = t < n ? __ldg(slots + t) : -1;
+      const bool bad = (long long)slot >= pool_slots;
+      if (bad && j == 0 && status) atomicOr(status, RQ_STATUS_BAD_SLOT);
+      const bool store = slot >= 0 && !bad;
+      if (!store) slot = 0;
+      const uint4 raw = *reinterpret_cast<const uint4*>(xg + swz(r, j));
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float nrm = __fsqrt_rn(ss);
+      const float4 y0 = *reinterpret_cast<const float4*>(Ys + r * kYStride + 8 * j);
+      const float4 y1 = *reinterpret_cast<const float4*>(Ys + r * kYStride + 8 * j + 4);
+      const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+      // Coordinates whose tensor-core u is within kFixBand of a boundary: recompute exactly,
+      // one at a time per half-warp (both halves walk their lists together), then re-code.
+      const float rcp = inv_norm(nrm);
+      uint32_t todo = 0;
+      int code[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float dm;
+        code[e] = code_of_margin<BITS>(y[e] * rcp, bnd, dm);
+        if (dm < kFixBand && store) todo |= 1u << e;
+      }
+      while (__any_sync(0xffffffffu, todo != 0)) {
+        const uint32_t want = __ballot_sync(0xffffffffu, todo != 0) & (half ? 0xffff0000u : 0x0000ffffu);
+        const int leader = want ? __ffs(want) - 1 : (half << 4);  // no work: any lane, result unused
+        const int e_lead = __shfl_sync(0xffffffffu, todo ? __ffs(todo) - 1 : 0, leader);
+        const int i = 8 * (leader & 15) + e_lead;  // the coordinate (dim of y) being recomputed
+        const float yi = dot_compensated(x, reinterpret_cast<const float*>(smem + kSmemR32) + i * 128, j);
+        if (lane == leader && want) {
+          const int c = code_of<BITS>(yi * rcp, bnd);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (e == e_lead) code[e] = c;
+          todo &= ~(1u << e_lead);
+        }
+      }
+      const int page = slot / g.page_size, off = slot % g.page_size;
+      uint8_t* chunk = pages + ((size_t)page * hkv + h) * (size_t)g.page_bytes;
+      pack_store<BITS>(code, nrm, chunk, g.page_size, kind, off, j, store, status);
+    }
+    __syncthreads();  // X buffer and Y free for the next tile
+    buf ^= 1;
+  }
+}
+
+template <int BITS>
+cudaError_t launch_append_bits(const Geometry& g, const __half* k, const __half* v, const int32_t* slots, int n,
+                               uint8_t* pages, int32_t* status, cudaStream_t stream, int sms) {
+  if (g.mode == RQ_DENSE) {
+    const long long tiles = 2LL * g.num_kv_heads * ((n + kDenseRows - 1) / kDenseRows);
+    // whole multiples of the 2 Hkv (K/V, head) groups, so a CTA keeps one R staged
+    int ctas = sms >= 2 * g.num_kv_heads ? sms / (2 * g.num_kv_heads) * (2 * g.num_kv_heads) : sms;
+    if (tiles < ctas) ctas = (int)tiles;
+    append_dense_kernel<BITS><<<ctas, kDenseThreads, kDenseSmem, stream>>>(g, k, v, slots, n, pages, status);
+  } else {
+    const long long items = (long long)n * g.num_kv_heads;
+    long long blocks = (items + kAppendWarps - 1) / kAppendWarps;
+    const long long max_blocks = (long long)sms * (2048 / kAppendThreads);
+    if (blocks > max_blocks) blocks = max_blocks;
+    append_kernel<BITS><<<(unsigned)blocks, kAppendThreads, 0, stream>>>(g, k, v, slots, n, pages, status);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t append_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(append_dense_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(append_dense_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(append_dense_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+  return e;
+}
 
 cudaError_t launch_append(const Geometry& g, const void* k, const void* v, const int32_t* slots, int n,
                           uint8_t* pages, int32_t* status, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  static int max_blocks = 0;
-  if (max_blocks == 0) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    max_blocks = (sms > 0 ? sms : 132) * (2048 / kAppendThreads);
+  static int sms_of[64] = {};  // per device; benign race: every writer stores the same value
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int sms = dev >= 0 && dev < 64 ? sms_of[dev] : 0;
+  if (sms <= 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 132;
+    if (dev >= 0 && dev < 64) sms_of[dev] = sms;
   }
-  const long long items = (long long)n * g.num_kv_heads;
-  long long blocks = (items + kAppendWarps - 1) / kAppendWarps;
-  if (blocks > max_blocks) blocks = max_blocks;
-  if (g.bits == 4)
-    append_kernel<4><<<(unsigned)blocks, kAppendThreads, 0, stream>>>(g, (const __half*)k, (const __half*)v,
-                                                                     slots, n, pages, status);
-  else
-    append_kernel<3><<<(unsigned)blocks, kAppendThreads, 0, stream>>>(g, (const __half*)k, (const __half*)v,
-                                                                     slots, n, pages, status);
-  return cudaGetLastError();
+  const __half* kh = (const __half*)k;
+  const __half* vh = (const __half*)v;
+  if (g.bits == 4) return launch_append_bits<4>(g, kh, vh, slots, n, pages, status, stream, sms);
+  if (g.bits == 3) return launch_append_bits<3>(g, kh, vh, slots, n, pages, status, stream, sms);
+  return launch_append_bits<2>(g, kh, vh, slots, n, pages, status, stream, sms);
 }
 
 }  // namespace rq

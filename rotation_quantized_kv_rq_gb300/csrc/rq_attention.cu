@@ -16,8 +16,11 @@
 //     O^T[128 x 8 q] += V~^T[128 x 16 tok] P^T.  The <= 8 query rows of a kv head (the GQA
 //     group, or group x drafts for verify) are the N = 8 side, so no query padding to 16.
 //   * Codes become fp16 centroids through a lane-replicated shared-memory table: one byte of
-//     codes (two 4-bit codes, or two 3-bit codes assembled from the 3-bit planes) indexes a
-//     half2 entry; each lane reads its own copy of the entry, so lookups never conflict.
+//     codes (two 4-bit codes, two 3-bit codes assembled from the 3-bit planes, or four 2-bit
+//     codes read as two halves) indexes a half2 entry; each lane reads its own copy of the
+//     entry, so lookups never conflict.
+//   * Dense rotations (TurboQuant) change only the two ends: a small kernel forms R_k q for the
+//     whole call first, and the combine applies R_v^T per (sequence, kv head) group.
 //   * P is moved from the S^T accumulator layout to the B-operand layout with movmatrix.
 //   * Scores are kept in base 2 (sm_scale * log2 e folded into q~).
 #include <cuda_fp16.h>
@@ -42,7 +45,7 @@ constexpr int kWaitLimit = 1 << 22;           // bounded mbarrier polling (about
 template <int BITS>
 struct Ring {
   static constexpr int VB = BITS * 16;
-  static constexpr int SB = 32 * VB + 64;     // slot bytes: 2112 (4-bit), 1600 (3-bit)
+  static constexpr int SB = 32 * VB + 64;     // slot bytes: 2112 (4-bit), 1600 (3-bit), 1088 (2-bit)
 };
 constexpr int kSlots = 4;                     // per warp: 2 stages x 2 tiles
 constexpr int kStages = kSlots / 2;
@@ -166,8 +169,10 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
 //   T4 (4-bit):  code_a = e & 15,                       code_b = e >> 4
 //   T1 (3-bit):  code_a = (e & 3) | (e >> 4 & 1) << 2,   code_b = (e >> 2 & 3) | (e >> 5 & 1) << 2
 //   T2 (3-bit):  code_a = (e >> 4 & 3) | (e & 1) << 2,   code_b = (e >> 6 & 3) | (e >> 1 & 1) << 2
+//   U1 (2-bit):  code_a = e & 3,                        code_b = e >> 4 & 3
+//   U2 (2-bit):  code_a = e >> 2 & 3,                   code_b = e >> 6 & 3
 // Row e holds 64 words: word l (l < 32) is the first table's entry for lane l, word 32 + l the
-// second table's (T2 for 3-bit; a copy of T4 for 4-bit).  A lookup address is
+// second table's (T2 for 3-bit, U2 for 2-bit; a copy of T4 for 4-bit).  A lookup address is
 // base + e * 256 + lane * 4 (+ 128 for the second table).
 // ---------------------------------------------------------------------------------------
 template <int BITS>
@@ -180,6 +185,9 @@ __device__ void build_lut(uint32_t* lut, const float* centroids, float* cb) {
     if (BITS == 4) {
       ca = e & 15;
       cbx = e >> 4;
+    } else if (BITS == 2) {
+      ca = second ? (e >> 2) & 3 : e & 3;
+      cbx = second ? (e >> 6) & 3 : (e >> 4) & 3;
     } else if (!second) {
       ca = (e & 3) | ((e >> 4) & 1) << 2;
       cbx = ((e >> 2) & 3) | ((e >> 5) & 1) << 2;
@@ -213,8 +221,8 @@ __device__ __forceinline__ float ex2(float x) {
 
 // ---------------------------------------------------------------------------------------
 // Raw tile data of one lane (lane = 4g + t), read from a staged tile in shared memory.
-// The MMA rows of a tile map to its tokens through rho(r): the identity for 4-bit codes, whose
-// V token pairs are stored swizzled, and r ^ ((r >> 1) & 1) for 3-bit codes, a permutation
+// The MMA rows of a tile map to its tokens through rho(r): the identity for 4- and 2-bit codes,
+// whose V token pairs are stored swizzled, and r ^ ((r >> 1) & 1) for 3-bit codes, a permutation
 // chosen so that the staged reads are conflict-free for K and at most 2-way for V:
 //   K rows g and g+8 -> tokens rho(g), rho(g) + 8, the 32 dims 32t..32t+31 of each;
 //   V k-slots 2t, 2t+1, 2t+8, 2t+9 -> tokens rho(2t), rho(2t+1), rho(2t) + 8, rho(2t+1) + 8,
@@ -225,7 +233,7 @@ __device__ __forceinline__ float ex2(float x) {
 // ---------------------------------------------------------------------------------------
 template <int BITS>
 __device__ __forceinline__ int rho(int r) {
-  return BITS == 4 ? r : (r ^ ((r >> 1) & 1));
+  return BITS == 3 ? (r ^ ((r >> 1) & 1)) : r;
 }
 
 template <int BITS>
@@ -236,6 +244,12 @@ struct Raw<4> {
   uint4 k[2];        // 16 bytes = 32 codes per K row
   uint2 v[4];        // 8 bytes = 16 codes per V token
   uint32_t nk, nv;   // fp16 norms of the two K rows' tokens (low, high)
+};
+template <>
+struct Raw<2> {
+  uint2 k[2];        // 8 bytes = 32 codes per K row
+  uint2 v[2];        // V token pairs (2t, 2t+1) and (2t+8, 2t+9): 4 bytes = 16 codes per token
+  uint32_t nk, nv;
 };
 template <>
 struct Raw<3> {
@@ -262,6 +276,16 @@ __device__ __forceinline__ void load_stage(Raw<BITS>& r, const uint8_t* st, int 
       r.v[2 * i] = make_uint2(u.x, u.y);
       r.v[2 * i + 1] = make_uint2(u.z, u.w);
     }
+  } else if constexpr (BITS == 2) {
+    r.k[0] = *reinterpret_cast<const uint2*>(st + rk * 32 + 8 * t);
+    r.k[1] = *reinterpret_cast<const uint2*>(st + (rk + 8) * 32 + 8 * t);
+    // 64-byte pair rows t and t+4; the 4-byte units of group g of both tokens are adjacent, at
+    // 8 * (g ^ (4 * (pair / 2 mod 2))).
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int pair = t + 4 * i;
+      r.v[i] = *reinterpret_cast<const uint2*>(vbp + pair * 64 + 8 * (g ^ (4 * ((pair >> 1) & 1))));
+    }
   } else {
     const int va = rho<BITS>(2 * t), vbt = rho<BITS>(2 * t + 1);
     const int vt[4] = {va, vbt, va + 8, vbt + 8};
@@ -284,6 +308,8 @@ __device__ __forceinline__ void load_stage(Raw<BITS>& r, const uint8_t* st, int 
 // A operand of S^T = K~ q~^T for k-chunk kc: rows g / g+8 hold the two K rows, k-slots
 // 2t,2t+1 hold dim pair 2kc and 2t+8,2t+9 dim pair 2kc+1 of the lane's 32 dims.
 // 4-bit: pair j is byte j of the row's 16 bytes.
+// 2-bit: byte kc of the row's 8 bytes carries dims 4kc..4kc+3; U1 gives (4kc, 4kc+2) for
+//        k-slots 2t,2t+1 and U2 gives (4kc+1, 4kc+3) for 2t+8,2t+9, and q~ is packed to match.
 // 3-bit: X0 = W0.lo | W2.hi (T1, pairs 2k), X1 = W2.lo | W0.hi (T2, pairs 2k+1),
 //        X2 = W1.lo | (W2>>2).hi (T1, pairs 8+2k), X3 = (W2>>2).lo | W1.hi (T2, pairs 9+2k).
 template <int BITS>
@@ -309,6 +335,19 @@ __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const
         a2 = lut<3, 0>(k0[w], key1, key2);
         a3 = lut<3, 0>(k1[w], key1, key2);
       }
+      if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+      else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+    }
+  } else if constexpr (BITS == 2) {
+    const uint32_t k0[2] = {r.k[0].x, r.k[0].y};
+    const uint32_t k1[2] = {r.k[1].x, r.k[1].y};
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) {
+      const int w = kc >> 2, byte = kc & 3;
+      const uint32_t a0 = lut_dyn<0>(k0[w], byte, key1, key2);
+      const uint32_t a1 = lut_dyn<0>(k1[w], byte, key1, key2);
+      const uint32_t a2 = lut_dyn<1>(k0[w], byte, key1, key2);
+      const uint32_t a3 = lut_dyn<1>(k1[w], byte, key1, key2);
       if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
       else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
     }
@@ -360,6 +399,27 @@ __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, ui
       const uint32_t a1 = lut_dyn<0>(XO[0][w], j, key1, key2);
       const uint32_t a2 = lut_dyn<0>(XE[1][w], j, key1, key2);
       const uint32_t a3 = lut_dyn<0>(XO[1][w], j, key1, key2);
+      mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+  } else if constexpr (BITS == 2) {
+    // Nibble-interleave each token pair: byte k of XE = (dims 4k, 4k+1 of the first token,
+    // the same dims of the second); XO the same for dims 4k+2, 4k+3.  U1 of such a byte is
+    // the k-slot pair of the lower dim, U2 that of the upper one.
+    uint32_t XE[2], XO[2];
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const uint32_t A = r.v[pr].x, B = r.v[pr].y;
+      XE[pr] = bitsel(A, B << 4, 0x0F0F0F0Fu);
+      XO[pr] = bitsel(A >> 4, B, 0x0F0F0F0Fu);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int j = mt >> 1;
+      const uint32_t x0 = (mt & 1) ? XO[0] : XE[0], x1 = (mt & 1) ? XO[1] : XE[1];
+      const uint32_t a0 = lut_dyn<0>(x0, j, key1, key2);
+      const uint32_t a1 = lut_dyn<1>(x0, j, key1, key2);
+      const uint32_t a2 = lut_dyn<0>(x1, j, key1, key2);
+      const uint32_t a3 = lut_dyn<1>(x1, j, key1, key2);
       mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
     }
   } else {
@@ -418,7 +478,65 @@ __device__ __forceinline__ ItemInfo decode_item(int item, const Geometry& g, con
   return it;
 }
 
-template <int BITS>
+// The lane's 32 dims 32tq..32tq+31 of R_k q for query row `row` of kv head h (zeros past the
+// rows): read from the call's pre-rotated buffer for a dense rotation (PRE), else the row's
+// fp16 q turned here -- Givens pairs or quaternion blocks never leave the lane's dims.
+template <bool PRE>
+__device__ __forceinline__ void rotated_query(float (&y)[32], const Geometry& g, const AttnArgs& a, int b, int h,
+                                              int row, int tq) {
+  const int j = row / g.group, head = h * g.group + row % g.group;
+  const size_t qoff = (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim + 32 * tq;
+  if constexpr (PRE) {
+    const float4* src = reinterpret_cast<const float4*>(a.q_rot + qoff);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 f = row < a.rows ? src[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      y[4 * c] = f.x;
+      y[4 * c + 1] = f.y;
+      y[4 * c + 2] = f.z;
+      y[4 * c + 3] = f.w;
+    }
+  } else {
+    float qv[32];
+    if (row < a.rows) {
+      const __half* src = reinterpret_cast<const __half*>(a.q) + qoff;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(src + 8 * c);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          qv[8 * c + 2 * e] = f.x;
+          qv[8 * c + 2 * e + 1] = f.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) qv[i] = 0.f;
+    }
+    const float4* rp = reinterpret_cast<const float4*>(g.rot_k + (size_t)h * kHeadDim + 32 * tq);
+#pragma unroll
+    for (int blk = 0; blk < 8; ++blk) {
+      const float4 p = __ldg(rp + blk);
+      const float* x = qv + 4 * blk;
+      if (g.mode == RQ_PLANAR) {
+        y[4 * blk + 0] = p.x * x[0] - p.y * x[1];
+        y[4 * blk + 1] = p.y * x[0] + p.x * x[1];
+        y[4 * blk + 2] = p.z * x[2] - p.w * x[3];
+        y[4 * blk + 3] = p.w * x[2] + p.z * x[3];
+      } else {
+        y[4 * blk + 0] = p.x * x[0] - p.y * x[1] - p.z * x[2] - p.w * x[3];
+        y[4 * blk + 1] = p.y * x[0] + p.x * x[1] - p.w * x[2] + p.z * x[3];
+        y[4 * blk + 2] = p.z * x[0] + p.w * x[1] + p.x * x[2] - p.y * x[3];
+        y[4 * blk + 3] = p.w * x[0] - p.z * x[1] + p.y * x[2] + p.x * x[3];
+      }
+    }
+  }
+}
+
+// PRE: the queries were rotated before the launch (dense rotation).
+template <int BITS, bool PRE>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_bytes) {
   using R = Ring<BITS>;
@@ -445,7 +563,6 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
   const uint32_t key2 = key1 + 128u;
   const int P = g.page_size;
   const int tiles_per_page = P / 16;
-  const __half* qh = reinterpret_cast<const __half*>(a.q);
   // shared addresses of this warp's slots: stage st uses slots 2st (first tile) and 2st + 1
   auto slot_of = [&](int i) -> uint32_t {
     const int sl = warp * kSlots + i;
@@ -498,47 +615,15 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
     int last_pos[2];                  // last position wholly visible to query columns 2tq, 2tq+1
     uint64_t draft_mask[2];           // tree verify: the columns' draft visibility bits
     {
-      float qv[32];
-      if (row < a.rows) {
-        const int j = row / g.group, head = it.h * g.group + row % g.group;
-        const __half* src = qh + (((size_t)it.b * a.T + j) * g.num_q_heads + head) * kHeadDim + 32 * tq;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(src + 8 * c);
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-            qv[8 * c + 2 * e] = f.x;
-            qv[8 * c + 2 * e + 1] = f.y;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) qv[i] = 0.f;
-      }
-      const float4* rp = reinterpret_cast<const float4*>(g.rot_k + (size_t)it.h * kHeadDim + 32 * tq);
       float y[32];
-#pragma unroll
-      for (int blk = 0; blk < 8; ++blk) {
-        const float4 p = __ldg(rp + blk);
-        const float* x = qv + 4 * blk;
-        if (g.mode == RQ_PLANAR) {
-          y[4 * blk + 0] = p.x * x[0] - p.y * x[1];
-          y[4 * blk + 1] = p.y * x[0] + p.x * x[1];
-          y[4 * blk + 2] = p.z * x[2] - p.w * x[3];
-          y[4 * blk + 3] = p.w * x[2] + p.z * x[3];
-        } else {
-          y[4 * blk + 0] = p.x * x[0] - p.y * x[1] - p.z * x[2] - p.w * x[3];
-          y[4 * blk + 1] = p.y * x[0] + p.x * x[1] - p.w * x[2] + p.z * x[3];
-          y[4 * blk + 2] = p.z * x[0] + p.w * x[1] + p.x * x[2] - p.y * x[3];
-          y[4 * blk + 3] = p.w * x[0] - p.z * x[1] + p.y * x[2] + p.x * x[3];
-        }
-      }
+      rotated_query<PRE>(y, g, a, it.b, it.h, row, tq);
+      // k-slot order of the K operand: dims (4kc, 4kc+1 | 4kc+2, 4kc+3) of the lane's 32, or
+      // (4kc, 4kc+2 | 4kc+1, 4kc+3) for 2-bit codes
+      constexpr int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;
 #pragma unroll
       for (int kc = 0; kc < 8; ++kc) {
-        qf[kc][0] = pack_half2(y[4 * kc] * g.q_scale, y[4 * kc + 1] * g.q_scale);
-        qf[kc][1] = pack_half2(y[4 * kc + 2] * g.q_scale, y[4 * kc + 3] * g.q_scale);
+        qf[kc][0] = pack_half2(y[4 * kc] * g.q_scale, y[4 * kc + s1] * g.q_scale);
+        qf[kc][1] = pack_half2(y[4 * kc + s2] * g.q_scale, y[4 * kc + 3] * g.q_scale);
       }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -781,6 +866,49 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
 }
 
 // ---------------------------------------------------------------------------------------
+// Log-sum-exp merge of one query row's split partials: o~ = sum_s 2^(m_s - M) O_s / L with
+// M = max_s m_s and L = sum_s 2^(m_s - M) l_s, for the lane's dims 4 lane .. 4 lane + 3.  The
+// lanes take the splits' (m, l) one split each, so M and L are warp reductions rather than
+// chains of dependent loads, and the O sum issues its independent loads eight at a time.
+// Zeros for an empty (or invalid) sequence.  All 32 lanes must call it.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float4 merge_splits(const Geometry& g, const AttnArgs& a, int nsplit, int b, int h, int row,
+                                               int lane) {
+  const int nt = row >> 3, col = row & 7;
+  const int P = g.page_size;
+  int len = a.seq_lens[b];
+  const int cap = a.max_pages * P;
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  const int npages = (len + P - 1) / P;
+  const int ns = min(nsplit, (npages + a.pages_per_split - 1) / a.pages_per_split);
+  const size_t stride = (size_t)8 * kPartialStride;  // between splits of one row
+  const float* base = a.ws + (((size_t)b * g.num_kv_heads + h) * a.n_tiles_n + nt) * a.max_splits * stride +
+                      (size_t)col * kPartialStride;
+  float M = -CUDART_INF_F;
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * stride]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M == -CUDART_INF_F || len < a.T) return acc;
+  float L = 0.f;
+  for (int s = lane; s < ns; s += 32) L += base[s * stride + 1] * exp2f(base[s * stride] - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+#pragma unroll 8
+  for (int s = 0; s < ns; ++s) {
+    const float* ps = base + s * stride;
+    const float w = exp2f(ps[0] - M);
+    const float4 v = *reinterpret_cast<const float4*>(ps + 4 + 4 * lane);
+    acc.x += v.x * w;
+    acc.y += v.y * w;
+    acc.z += v.z * w;
+    acc.w += v.w * w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  return make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
+// ---------------------------------------------------------------------------------------
 // Combine: one warp per output row (b, j, query head); lane l owns dims 4l..4l+3.
 //   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  o~ = sum_s O_s 2^(m_s - M) / L,
 //   out = R_v^T o~  (block-local: a Givens pair or a quaternion block per lane).
@@ -796,33 +924,8 @@ attn_combine_kernel(const Geometry g, const AttnArgs a, int nsplit) {
   const int b = warp_global / (g.num_q_heads * a.T);
   const int h = head / g.group;
   const int row = j * g.group + head % g.group;
-  const int nt = row >> 3, col = row & 7;
-  const int P = g.page_size;
-  int len = a.seq_lens[b];
-  const int cap = a.max_pages * P;
-  len = len < 0 ? 0 : (len > cap ? cap : len);
-  const int npages = (len + P - 1) / P;
-  const int ns = min(nsplit, (npages + a.pages_per_split - 1) / a.pages_per_split);
-  const float* base = a.ws + (((size_t)b * g.num_kv_heads + h) * a.n_tiles_n + nt) * a.max_splits * 8 * kPartialStride +
-                      (size_t)col * kPartialStride;
-  float M = -CUDART_INF_F;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, base[(size_t)s * 8 * kPartialStride]);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float L = 0.f;
-  if (M != -CUDART_INF_F && len >= a.T) {
-    for (int s = 0; s < ns; ++s) {
-      const float* ps = base + (size_t)s * 8 * kPartialStride;
-      const float w = exp2f(ps[0] - M);
-      L += ps[1] * w;
-      const float4 v = *reinterpret_cast<const float4*>(ps + 4 + 4 * lane);
-      acc.x += v.x * w;
-      acc.y += v.y * w;
-      acc.z += v.z * w;
-      acc.w += v.w * w;
-    }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const float y[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+  const float4 o = merge_splits(g, a, nsplit, b, h, row, lane);
+  const float y[4] = {o.x, o.y, o.z, o.w};
   const float4 p = __ldg(reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim) + lane);
   float x[4];
   if (g.mode == RQ_PLANAR) {
@@ -843,6 +946,99 @@ attn_combine_kernel(const Geometry g, const AttnArgs a, int nsplit) {
   out[1] = __floats2half2_rn(x[2], x[3]);
 }
 
+// ---------------------------------------------------------------------------------------
+// Dense rotation (TurboQuant): both ends of the call.  The query rows of one kv head -- over
+// every sequence and query token -- are numbered r = (b * T + j) * group + k; a CTA takes 16
+// consecutive rows of one head.  Thread i owns output dim i: per step of the sum it reads
+// four matrix entries (coalesced across threads, L2-resident) and the 16 rows' four inputs as
+// float4 broadcasts from shared memory, 64 FMAs per 20 loads.
+// ---------------------------------------------------------------------------------------
+constexpr int kDenseRows = 16;
+
+constexpr int kDenseSmem = kHeadDim * kHeadDim * 4;  // the 128 x 128 fp32 matrix, staged
+
+// Stages the 64 KB matrix w into shared memory ws: every thread's 32 16-byte copies are in
+// flight at once (one memory round trip instead of one per step of the sum).
+__device__ __forceinline__ void stage_matrix(float* ws, const float* __restrict__ w) {
+  const uint32_t dst = (uint32_t)__cvta_generic_to_shared(ws);
+  for (int c = threadIdx.x; c < kHeadDim * kHeadDim / 4; c += blockDim.x)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * c), "l"(w + 4 * c) : "memory");
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+// out[r][i] = sum_m ws[m * 128 + i] * xs[r][m] for the CTA's rows (thread i).
+__device__ __forceinline__ void dense_rows(float (&acc)[kDenseRows], const float* ws, const float (*xs)[kHeadDim]) {
+#pragma unroll
+  for (int r = 0; r < kDenseRows; ++r) acc[r] = 0.f;
+  const int i = threadIdx.x;
+#pragma unroll 2
+  for (int m = 0; m < kHeadDim; m += 4) {
+    const float w0 = ws[(m + 0) * kHeadDim + i], w1 = ws[(m + 1) * kHeadDim + i];
+    const float w2 = ws[(m + 2) * kHeadDim + i], w3 = ws[(m + 3) * kHeadDim + i];
+#pragma unroll
+    for (int r = 0; r < kDenseRows; ++r) {
+      const float4 x = *reinterpret_cast<const float4*>(&xs[r][m]);
+      acc[r] = fmaf(w0, x.x, fmaf(w1, x.y, fmaf(w2, x.z, fmaf(w3, x.w, acc[r]))));
+    }
+  }
+}
+
+// Query row r of kv head h -> its index in the [B][T][Hq] query / output arrays.
+__device__ __forceinline__ size_t dense_row_index(const Geometry& g, int h, int r) {
+  const int bj = r / g.group, k = r % g.group;
+  return (size_t)bj * g.num_q_heads + h * g.group + k;
+}
+
+// q_rot[b][j][head] = R_k q[b][j][head] (fp32, unscaled); rot_k holds R_k transposed.
+__global__ void __launch_bounds__(kHeadDim)
+rotate_q_dense_kernel(const Geometry g, const AttnArgs a) {
+  __shared__ __align__(16) float qs[kDenseRows][kHeadDim];
+  extern __shared__ __align__(16) float wsm[];
+  const int h = blockIdx.x % g.num_kv_heads;
+  stage_matrix(wsm, g.rot_k + (size_t)h * kHeadDim * kHeadDim);
+  const int r0 = (blockIdx.x / g.num_kv_heads) * kDenseRows;
+  const int nr = min(kDenseRows, a.B * a.T * g.group - r0);
+  const __half* q = reinterpret_cast<const __half*>(a.q);
+  for (int e = threadIdx.x; e < kDenseRows * kHeadDim; e += kHeadDim) {
+    const int r = e / kHeadDim, d = e % kHeadDim;
+    qs[r][d] = r < nr ? __half2float(q[dense_row_index(g, h, r0 + r) * kHeadDim + d]) : 0.f;
+  }
+  __syncthreads();
+  float acc[kDenseRows];
+  dense_rows(acc, wsm, qs);
+#pragma unroll
+  for (int r = 0; r < kDenseRows; ++r)
+    if (r < nr) a.q_rot[dense_row_index(g, h, r0 + r) * kHeadDim + threadIdx.x] = acc[r];
+}
+
+// The log-sum-exp merge of attn_combine_kernel for the CTA's rows, then out = R_v^T o~.
+__global__ void __launch_bounds__(kHeadDim)
+attn_combine_dense_kernel(const Geometry g, const AttnArgs a, int nsplit) {
+  __shared__ __align__(16) float os[kDenseRows][kHeadDim];
+  extern __shared__ __align__(16) float wsm[];
+  const int h = blockIdx.x % g.num_kv_heads;
+  const int r0 = (blockIdx.x / g.num_kv_heads) * kDenseRows;
+  const int nr = min(kDenseRows, a.B * a.T * g.group - r0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  stage_matrix(wsm, g.rot_v + (size_t)h * kHeadDim * kHeadDim);
+  for (int rr = warp; rr < kDenseRows; rr += kHeadDim / 32) {
+    float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (rr < nr) {  // uniform across the warp
+      const int r = r0 + rr, bj = r / g.group;
+      const int b = bj / a.T, j = bj % a.T;
+      res = merge_splits(g, a, nsplit, b, h, j * g.group + r % g.group, lane);
+    }
+    *reinterpret_cast<float4*>(&os[rr][4 * lane]) = res;
+  }
+  __syncthreads();
+  float acc[kDenseRows];
+  dense_rows(acc, wsm, os);
+  __half* out = reinterpret_cast<__half*>(a.out);
+#pragma unroll
+  for (int r = 0; r < kDenseRows; ++r)
+    if (r < nr) out[dense_row_index(g, h, r0 + r) * kHeadDim + threadIdx.x] = __float2half_rn(acc[r]);
+}
+
 }  // namespace
 
 // Dynamic shared memory of a variant: its layout end for a window that starts right after the
@@ -852,36 +1048,79 @@ static int smem_bytes_for(int bits) {
   cudaGetDevice(&dev);
   if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) reserved = 0;
   const uint32_t base = (uint32_t)reserved;
-  return (int)((bits == 4 ? smem_plan<4>(base).end : smem_plan<3>(base).end) - base);
+  const uint32_t end = bits == 4 ? smem_plan<4>(base).end : (bits == 3 ? smem_plan<3>(base).end : smem_plan<2>(base).end);
+  return (int)(end - base);
 }
 
-size_t attention_smem_bytes() { return (size_t)smem_bytes_for(4) > (size_t)smem_bytes_for(3) ? smem_bytes_for(4) : smem_bytes_for(3); }
+size_t attention_smem_bytes() {
+  size_t m = 0;
+  for (int bits = 2; bits <= 4; ++bits)
+    if ((size_t)smem_bytes_for(bits) > m) m = (size_t)smem_bytes_for(bits);
+  return m;
+}
+
+template <int BITS, bool PRE>
+static cudaError_t set_smem_limit() {
+  return cudaFuncSetAttribute(attn_splitk_kernel<BITS, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes_for(BITS));
+}
 
 cudaError_t attention_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(attn_splitk_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for(3));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_splitk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for(4));
+  cudaError_t e = set_smem_limit<2, false>();
+  if (e == cudaSuccess) e = set_smem_limit<3, false>();
+  if (e == cudaSuccess) e = set_smem_limit<4, false>();
+  if (e == cudaSuccess) e = set_smem_limit<2, true>();
+  if (e == cudaSuccess) e = set_smem_limit<3, true>();
+  if (e == cudaSuccess) e = set_smem_limit<4, true>();
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(rotate_q_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_combine_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+  return e;
+}
+
+template <int BITS>
+static void launch_splitk(const Geometry& g, const AttnArgs& a, int grid, int n_items, int smem, cudaStream_t stream) {
+  if (a.q_rot)
+    attn_splitk_kernel<BITS, true><<<grid, kThreads, smem, stream>>>(g, a, n_items, smem);
+  else
+    attn_splitk_kernel<BITS, false><<<grid, kThreads, smem, stream>>>(g, a, n_items, smem);
 }
 
 cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream,
                              cudaEvent_t ev_start, cudaEvent_t ev_end) {
   if (a.B <= 0) return cudaSuccess;
+  const bool dense = g.mode == RQ_DENSE;
+  if (dense != (a.q_rot != nullptr)) return cudaErrorInvalidValue;
   const int nsplit = (a.max_pages + a.pages_per_split - 1) / a.pages_per_split;
   const long long n_items = (long long)a.B * g.num_kv_heads * a.n_tiles_n * nsplit;
+  const long long rows_per_head = (long long)a.B * a.T * g.group;
+  const unsigned groups = (unsigned)(g.num_kv_heads * ((rows_per_head + kDenseRows - 1) / kDenseRows));
+  if (dense) {
+    rotate_q_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (n_items > 0) {
     const int grid = (int)(n_items < num_ctas ? n_items : num_ctas);
     if (ev_start) cudaEventRecord(ev_start, stream);
     const int smem = smem_bytes_for(g.bits);
     if (g.bits == 4)
-      attn_splitk_kernel<4><<<grid, kThreads, smem, stream>>>(g, a, (int)n_items, smem);
+      launch_splitk<4>(g, a, grid, (int)n_items, smem, stream);
+    else if (g.bits == 3)
+      launch_splitk<3>(g, a, grid, (int)n_items, smem, stream);
     else
-      attn_splitk_kernel<3><<<grid, kThreads, smem, stream>>>(g, a, (int)n_items, smem);
+      launch_splitk<2>(g, a, grid, (int)n_items, smem, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev_end) cudaEventRecord(ev_end, stream);
   }
-  const long long rows = (long long)a.B * a.T * g.num_q_heads;
-  attn_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(g, a, nsplit);
+  if (dense) {
+    attn_combine_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a, nsplit);
+  } else {
+    const long long rows = (long long)a.B * a.T * g.num_q_heads;
+    attn_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(g, a, nsplit);
+  }
   return cudaGetLastError();
 }
 

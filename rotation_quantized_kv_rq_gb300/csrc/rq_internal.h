@@ -1,6 +1,7 @@
 // Internal interface between the host API (rq_api.cpp) and the sm_103a kernels (*.cu).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,15 +16,23 @@ struct Geometry {
   int num_q_heads;
   int num_kv_heads;
   int group;           // Hq / Hkv
-  int bits;
-  int mode;            // 0 planar, 1 iso
+  int bits;            // 2, 3 or 4
+  int mode;            // 0 planar, 1 iso, 2 dense
   int page_size;
   int num_pages;
   int vec_bytes;       // head_dim * bits / 8
   int page_bytes;      // page_size * (2 * vec_bytes + 4)
   float q_scale;       // sm_scale * log2(e): scores are kept in base 2
-  const float* rot_k;  // device [Hkv][128]
-  const float* rot_v;  // device [Hkv][128]
+  // planar / iso: device [Hkv][128] rotation parameters.
+  // dense: rot_k = device [Hkv][128][128] R_k TRANSPOSED (query rotation reads it column-wise),
+  //        rot_v = device [Hkv][128][128] R_v (output rotation R_v^T o reads it row-wise).
+  const float* rot_k;
+  const float* rot_v;
+  // dense only: device fp16 [2 (K, V)][Hkv][2 (hi, lo)][128][128], R = hi + lo split for the
+  // tensor-core append (hi = fp16(R), lo = fp16(R - hi)); null otherwise.
+  const __half* dense16;
+  // dense only: device fp32 [2 (K, V)][Hkv][128][128] row-major R (exact recompute in the append)
+  const float* dense32;
   const float* centroids;   // device [2^bits]
   const float* boundaries;  // device [2^bits - 1]
 };
@@ -46,12 +55,14 @@ struct AttnArgs {
   int max_splits;            // splits per (b, kv head) the workspace has room for
   int* counters;             // [2] work-item and finished-CTA counters, zero between launches
   const uint64_t* tree_mask; // [B][T] draft visibility bits (tree verify), or null (causal chain)
+  float* q_rot;              // dense: fp32 [B][T][Hq][128] scratch for R_k q; null otherwise
 };
 
 constexpr int kPartialStride = 132;   // floats per partial row: m, l, pad, pad, o[128]
 
 cudaError_t launch_append(const Geometry& g, const void* k, const void* v, const int32_t* slots,
                           int n, uint8_t* pages, int32_t* status, cudaStream_t stream);
+cudaError_t append_prepare();  // sets the dense append kernel's shared-memory limit
 
 cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream,
                              cudaEvent_t ev_start = nullptr, cudaEvent_t ev_end = nullptr);

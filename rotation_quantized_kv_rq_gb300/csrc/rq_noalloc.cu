@@ -62,10 +62,12 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
                                            int B, void* out, int32_t* d_status, void* stream) {
   if (!cfg || B < 0 || max_pages < 1) return RQ_ERR_INVALID;
   if (cfg->num_q_heads <= 0 || cfg->num_kv_heads <= 0 || cfg->page_size <= 0 || cfg->num_pages <= 0 ||
-      cfg->num_q_heads % cfg->num_kv_heads != 0 || (cfg->mode != RQ_PLANAR && cfg->mode != RQ_ISO) ||
+      cfg->num_q_heads % cfg->num_kv_heads != 0 ||
+      (cfg->mode != RQ_PLANAR && cfg->mode != RQ_ISO && cfg->mode != RQ_DENSE) ||
       !(cfg->sm_scale >= 0.0f) || std::isinf(cfg->sm_scale))
     return RQ_ERR_INVALID;
-  if (cfg->head_dim != rq::kHeadDim || (cfg->bits != 3 && cfg->bits != 4) || cfg->page_size % 16 != 0 ||
+  if (cfg->mode == RQ_DENSE) return RQ_ERR_UNSUPPORTED;  // its query rotation needs a workspace
+  if (cfg->head_dim != rq::kHeadDim || cfg->bits < 2 || cfg->bits > 4 || cfg->page_size % 16 != 0 ||
       cfg->page_size > 256)
     return RQ_ERR_UNSUPPORTED;
   if (B == 0) return RQ_OK;
@@ -96,6 +98,8 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   g.q_scale = (float)(scale * 1.44269504088896340736);
   g.rot_k = d_rot_k;
   g.rot_v = d_rot_v;
+  g.dense16 = nullptr;
+  g.dense32 = nullptr;
   g.centroids = d_centroids;
   g.boundaries = nullptr;  // decode never codes
 
@@ -110,6 +114,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   a.out = out;
   a.status = d_status;
   a.tree_mask = nullptr;
+  a.q_rot = nullptr;
   a.rows = group;
   a.n_tiles_n = (group + 7) / 8;
 

@@ -19,7 +19,7 @@ from . import build as _build
 
 RQ_OK, RQ_ERR_INVALID, RQ_ERR_UNSUPPORTED, RQ_ERR_CUDA, RQ_ERR_CAPACITY = 0, 1, 2, 3, 4
 RQ_STATUS_BAD_PAGE, RQ_STATUS_BAD_SLOT, RQ_STATUS_BAD_LEN, RQ_STATUS_NORM_OVERFLOW, RQ_STATUS_TIMEOUT = 1, 2, 4, 8, 16
-RQ_PLANAR, RQ_ISO = 0, 1
+RQ_PLANAR, RQ_ISO, RQ_DENSE = 0, 1, 2
 HEAD_DIM = 128
 
 EXPORTS = ["rq_create", "rq_free", "rq_page_bytes", "rq_lloyd_max_codebook", "rq_get_codebook",
@@ -119,6 +119,9 @@ def rq_create(mode: int, bits: int, num_q_heads: int, num_kv_heads: int, page_si
               codebook=None, sm_scale: float = 0.0, device: int = -1) -> ctypes.c_void_p:
     rk = np.ascontiguousarray(rot_k, np.float32).reshape(-1)
     rv = np.ascontiguousarray(rot_v, np.float32).reshape(-1)
+    want = num_kv_heads * HEAD_DIM * (HEAD_DIM if mode == RQ_DENSE else 1)
+    if rk.size != want or rv.size != want:  # the library reads exactly `want` floats of each
+        raise RQError("rq_create", RQ_ERR_INVALID)
     cb = None if codebook is None else np.ascontiguousarray(codebook, np.float32)
     fp = ctypes.POINTER(ctypes.c_float)
     cfg = rq_config(HEAD_DIM, num_q_heads, num_kv_heads, bits, mode, page_size, num_pages, max_batch,

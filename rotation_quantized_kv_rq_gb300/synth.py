@@ -16,6 +16,9 @@ Workloads (geometry from the five synthetic decode/verify configurations of this
         step appends the 6 drafts, then verifies.
   cfg3_prefill  quantize-append of 65536 tokens x 8 kv heads (K and V) of one sequence.
   cfg4  rq3 planar decode, 64 x 65536 ctx, 64/8, page 64, permuted pages.
+  tq{2,3,4}_32k  TurboQuant (dense random orthogonal rotation) decode at 2, 3 and 4 bits on
+        the cfg2_32k geometry and data.
+  tq3_prefill  dense-rotation quantize-append of 65536 tokens x 8 kv heads.
 
 Distributions: Q, V ~ N(0, 1); K ~ N(0, 1) with 4 distinct channels per kv head (drawn from
 the seed, fixed for all tokens) multiplied by 10 after sampling; fp16 storage.
@@ -28,7 +31,7 @@ import math
 import numpy as np
 import torch
 
-PLANAR, ISO = 0, 1
+PLANAR, ISO, DENSE = 0, 1, 2
 HEAD_DIM = 128
 
 
@@ -61,8 +64,19 @@ SPECS = {
     "cfg2_32k": Spec("cfg2_32k", ISO, 4, 32, 32768, 64, 8, 16, appended=0, seed=1002),
     "cfg3": Spec("cfg3", ISO, 3, 8, 16384 + 6, 32, 8, 16, query_tokens=6, appended=6, seed=1003),
     "cfg4": Spec("cfg4", PLANAR, 3, 64, 65536, 64, 8, 64, appended=0, seed=1004),
+    # TurboQuant: the cfg2_32k geometry and seed (same K, V and Q), dense rotation
+    "tq4_32k": Spec("tq4_32k", DENSE, 4, 32, 32768, 64, 8, 16, appended=0, seed=1002),
+    "tq3_32k": Spec("tq3_32k", DENSE, 3, 32, 32768, 64, 8, 16, appended=0, seed=1002),
+    "tq2_32k": Spec("tq2_32k", DENSE, 2, 32, 32768, 64, 8, 16, appended=0, seed=1002),
 }
-PREFILL_TOKENS = 65536     # cfg3_prefill: one sequence, all 8 kv heads, K and V
+PREFILL_TOKENS = 65536     # prefill workloads: one sequence, all 8 kv heads, K and V
+PREFILL = {"cfg3_prefill": "cfg3", "tq3_prefill": "tq3_32k"}  # workload -> spec it takes its codec from
+
+
+def prefill_spec(name: str) -> "Spec":
+    """The one-sequence, PREFILL_TOKENS-token append workload `name` (see PREFILL)."""
+    return dataclasses.replace(SPECS[PREFILL[name]], name=name, batch=1, ctx=PREFILL_TOKENS, ragged_min=0,
+                               query_tokens=1, appended=PREFILL_TOKENS)
 
 
 def scaled(spec: Spec, **kw) -> Spec:
@@ -83,11 +97,19 @@ def _rng(spec_seed: int, purpose: str) -> np.random.Generator:
 
 
 def rotation_params(mode: int, num_kv_heads: int, rng: np.random.Generator, head_dim: int = HEAD_DIM):
-    """Random per-head rotation parameters as float32 [Hkv][head_dim].
+    """Random per-head rotation parameters, float32.
 
     planar: [Hkv][head_dim/2][2] = (cos t, sin t), t ~ U[0, 2 pi) per pair per head.
     iso:    [Hkv][head_dim/4][4] = g / |g|, g ~ N(0, I4) per block per head.
+    dense:  [Hkv][head_dim][head_dim], a uniformly (Haar) distributed orthogonal matrix per head:
+            the Q factor of a Gaussian matrix, its columns' signs fixed by diag(R) > 0.
     """
+    if mode == DENSE:
+        out = np.empty((num_kv_heads, head_dim, head_dim), np.float32)
+        for h in range(num_kv_heads):
+            q, r = np.linalg.qr(rng.standard_normal(size=(head_dim, head_dim)))
+            out[h] = q * np.sign(np.diag(r))[None, :]
+        return out
     if mode == PLANAR:
         theta = rng.uniform(0.0, 2.0 * math.pi, size=(num_kv_heads, head_dim // 2))
         p = np.stack([np.cos(theta), np.sin(theta)], axis=-1)
@@ -180,7 +202,7 @@ def queries(spec: Spec, device="cpu", batch=None):
 @dataclasses.dataclass
 class Workload:
     spec: Spec
-    rot_k: np.ndarray        # float32 [Hkv][d]
+    rot_k: np.ndarray        # float32 [Hkv][d] (dense: [Hkv][d][d])
     rot_v: np.ndarray
     seq_lens: np.ndarray     # int32 [B] (after the step's appends)
     block_table: np.ndarray  # int32 [B][max_pages]

@@ -23,13 +23,14 @@ def positions_slots(wl: synth.Workload, b: int, start: int, count: int) -> np.nd
     return synth.slots_for(wl.block_table, b, np.arange(start, start + count), wl.spec.page_size)
 
 
-def compare_chunks(gpu_pages: np.ndarray, ocache: O.Cache, tokens, margins=None, inputs=None):
+def compare_chunks(gpu_pages: np.ndarray, ocache: O.Cache, tokens, margins=None, inputs=None, flips=None):
     """Compare the packed codes and norms of the given (page, offset, head, token-index) tuples.
 
     gpu_pages: uint8 [num_pages][Hkv][page_bytes] copied from the device.  margins: dict
     token-index -> (margin_k [Hkv][d], margin_v [Hkv][d]) from the oracle's append; inputs:
     (K, V) fp16 numpy [n][Hkv][d] indexed by token-index, to locate fp16 rounding midpoints.
-    Returns (n_codes_compared, n_mismatch_in_band).  Raises AssertionError on any mismatch
+    Returns (n_codes_compared, n_mismatch_in_band); `flips`, if a set, receives the
+    (token-index, kv head) of every in-band difference.  Raises AssertionError on any mismatch
     outside the band or any norm mismatch that is not at an fp16 rounding midpoint."""
     bits, P = ocache.bits, ocache.P
     vb = O.vector_bytes(bits)
@@ -50,6 +51,8 @@ def compare_chunks(gpu_pages: np.ndarray, ocache: O.Cache, tokens, margins=None,
                 m = margins[ti][kv][h]
                 assert np.all(m[bad] < BOUNDARY_BAND), (page, off, h, kv, bad, m[bad], gc[bad], oc[bad])
                 in_band += len(bad)
+                if flips is not None:
+                    flips.add((ti, h))
             no = 2 * P * vb + kv * 2 * P + 2 * off
             gn = int(g_ch[no]) | int(g_ch[no + 1]) << 8
             on = int(o_ch[no]) | int(o_ch[no + 1]) << 8
@@ -62,6 +65,8 @@ def compare_chunks(gpu_pages: np.ndarray, ocache: O.Cache, tokens, margins=None,
                 mid = 0.5 * (a + b)
                 assert abs(exact - mid) <= 1e-6 * exact, ("norm mismatch", page, off, h, kv, gn, on, exact)
                 in_band += 1
+                if flips is not None:
+                    flips.add((ti, h))
     return compared, in_band
 
 
@@ -73,6 +78,17 @@ def assert_close(gpu: np.ndarray, ref: np.ndarray, what=""):
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside {ATOL} + {RTOL}|ref|; "
                            f"max abs err {err.max():.3g} at {np.unravel_index(err.argmax(), err.shape)}")
     return float(err.max())
+
+
+def assert_close_except(gpu: np.ndarray, ref: np.ndarray, group: int, allowed, what=""):
+    """assert_close over [B][T][Hq][d], except that (sequence, kv head) groups in `allowed` may
+    miss: there a near-boundary code was decided the other way, also a correct decision, and one
+    such code of a dominant token can move the output by more than the tolerance.  Returns the
+    (sequence, kv head) groups that missed."""
+    miss = np.abs(gpu.astype(np.float64) - ref) > ATOL + RTOL * np.abs(ref)
+    groups = {(int(b), int(hq) // group) for b, _, hq in np.argwhere(miss.any(axis=3))}
+    assert groups <= set(allowed), (what, sorted(groups - set(allowed)))
+    return sorted(groups)
 
 
 def cosine_per_head(a: np.ndarray, b: np.ndarray) -> np.ndarray:

@@ -62,13 +62,15 @@ def _cfg(**over):
 
 @pytest.mark.parametrize("over,code", [
     (dict(head_dim=64), rq.RQ_ERR_UNSUPPORTED),
-    (dict(bits=2), rq.RQ_ERR_UNSUPPORTED),
+    (dict(bits=1), rq.RQ_ERR_UNSUPPORTED),
+    (dict(bits=5), rq.RQ_ERR_UNSUPPORTED),
     (dict(bits=8), rq.RQ_ERR_UNSUPPORTED),
     (dict(page_size=24), rq.RQ_ERR_UNSUPPORTED),
     (dict(page_size=512), rq.RQ_ERR_UNSUPPORTED),
     (dict(num_q_heads=30), rq.RQ_ERR_INVALID),
     (dict(num_kv_heads=0), rq.RQ_ERR_INVALID),
-    (dict(mode=2), rq.RQ_ERR_INVALID),
+    (dict(mode=3), rq.RQ_ERR_INVALID),
+    (dict(mode=-1), rq.RQ_ERR_INVALID),
     (dict(num_pages=0), rq.RQ_ERR_INVALID),
     (dict(max_batch=-1), rq.RQ_ERR_INVALID),
     (dict(sm_scale=-1.0), rq.RQ_ERR_INVALID),
@@ -86,3 +88,16 @@ def test_calls_reject_null_context():
     assert L.rq_quantize_append(None, None, None, None, 1, None, None, None) == rq.RQ_ERR_INVALID
     assert L.rq_decode_attention(None, None, None, None, 1, None, 1, None, None, None) == rq.RQ_ERR_INVALID
     assert L.rq_verify_attention(None, None, 2, None, None, 1, None, 1, None, None, None) == rq.RQ_ERR_INVALID
+
+
+def test_binding_checks_rotation_table_size():
+    """A dense context reads Hkv x 128 x 128 floats per table; the binding refuses a wrong size
+    before the library could read past the caller's array."""
+    rk = np.zeros((8, 128), np.float32)
+    with pytest.raises(rq.RQError) as e:
+        rq.rq_create(rq.RQ_DENSE, 4, 32, 8, 16, 64, rk, rk, max_batch=1)
+    assert e.value.code == rq.RQ_ERR_INVALID
+    dense = np.zeros((8, 128, 128), np.float32)
+    with pytest.raises(rq.RQError) as e:
+        rq.rq_create(rq.RQ_PLANAR, 4, 32, 8, 16, 64, dense, dense, max_batch=1)
+    assert e.value.code == rq.RQ_ERR_INVALID

@@ -1,17 +1,24 @@
-"""Parity at the five workloads' full sizes, in the launch configuration bench.py times.
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
 
 For each workload the whole packed cache is built on the GPU, one bench step runs (append of
 the step's tokens + attention), and sampled sequences are re-encoded by the CPU oracle from
-the same inputs: their packed bytes must match (near-boundary codes excepted and bounded), and
-their attention outputs must agree within 2e-3 + 1e-3|ref|.  Fidelity against attention over
-the unquantised fp16 cache is reported as cosine similarity."""
+the same inputs.  Per sampled sequence:
+  * codes: the packed bytes match the oracle's, except codes within 1e-6 of a bin boundary
+    (counted and bounded);
+  * attention over the same cache: the kernels, run on the oracle's own packed pages of the
+    sequence, agree with the oracle's fp64 attention within 2e-3 + 1e-3|ref|;
+  * end to end: the bench step's output agrees with the oracle's too, except in kv-head
+    groups whose codes hold a near-boundary difference -- there both codes are correct
+    decisions, and one flipped code of a dominant token moves the output by more than the
+    tolerance, so such groups are reported, not failed.
+Fidelity against attention over the unquantised fp16 cache is reported as cosine similarity."""
 import numpy as np
 import pytest
 import torch
 
 import bench
 from oracle import oracle as O
-from rotation_quantized_kv_rq_gb300 import synth
+from rotation_quantized_kv_rq_gb300 import rq, synth
 from tests import parity as PT
 
 pytestmark = pytest.mark.gpu
@@ -42,14 +49,16 @@ def _check_sequence(bn, b, out_gpu):
     vb = 16 * spec.bits
     diff = np.argwhere(gpu != ora)
     in_band = 0
+    flipped_heads = set()   # kv heads of this sequence with a near-boundary code or norm difference
     for (pg, h, byte) in diff:
         if byte < P * vb:
             kv, off, norm = 0, int(byte) // vb, False
         elif byte < 2 * P * vb:
             o = int(byte) - P * vb   # inside the V-codes section: find the token owning it
             kv, norm = 1, False
-            off = next(t for t in range(P) for u in range(vb // 8)
-                       if O.v_unit_offset(spec.bits, t, u) <= o < O.v_unit_offset(spec.bits, t, u) + 8)
+            ub = O.v_unit_bytes(spec.bits)
+            off = next(t for t in range(P) for u in range(vb // ub)
+                       if O.v_unit_offset(spec.bits, t, u) <= o < O.v_unit_offset(spec.bits, t, u) + ub)
         else:
             kv, rem = divmod(int(byte) - 2 * P * vb, 2 * P)
             off = rem // 2
@@ -65,6 +74,7 @@ def _check_sequence(bn, b, out_gpu):
             mid = 0.5 * (O.half_to_double(gn) + O.half_to_double(on))
             assert abs(exact - mid) <= 1e-6 * exact, ("norm", b, t, h, kv)
             in_band += 1
+            flipped_heads.add(int(h))
             continue
         rot = (wl.rot_k if kv == 0 else wl.rot_v)[h]
         codes, _, margin = O.encode(spec.mode, spec.bits, rot, oc.boundaries, x)
@@ -73,21 +83,40 @@ def _check_sequence(bn, b, out_gpu):
         bad = np.nonzero(gc != codes)[0]
         assert np.all(margin[bad] < PT.BOUNDARY_BAND), ("code", b, t, h, kv, bad, margin[bad])
         in_band += len(bad)
+        if len(bad):
+            flipped_heads.add(int(h))
     total_codes = L * spec.num_kv_heads * 2 * 128
     assert in_band <= max(4, total_codes // 200000), (in_band, total_codes)
 
     q = bn.q.cpu().numpy()
-    qb = q[b:b + 1] if spec.query_tokens > 1 else q[b:b + 1, None]
-    ref = oc.attention(qb, np.arange(npg, dtype=np.int32)[None], np.array([L], np.int32), T=spec.query_tokens)
-    got = out_gpu[b:b + 1] if spec.query_tokens > 1 else out_gpu[b:b + 1, None]
-    err = PT.assert_close(got, ref, f"{bn.name} seq {b}")
-    dense = O.attention_dense(qb, k[None], v[None], np.array([L], np.int32), spec.num_q_heads, spec.num_kv_heads,
-                              T=spec.query_tokens)
+    T = spec.query_tokens
+    qb = q[b:b + 1] if T > 1 else q[b:b + 1, None]
+    bt1 = np.arange(npg, dtype=np.int32)[None]
+    len1 = np.array([L], np.int32)
+    ref = oc.attention(qb, bt1, len1, T=T)
+    # the kernels over the oracle's own pages of this sequence: the same dequantised cache
+    one = rq.KVCache(spec.mode, spec.bits, spec.num_q_heads, spec.num_kv_heads, P, npg, wl.rot_k, wl.rot_v,
+                     max_batch=1, max_query_tokens=T, max_pages_per_seq=npg, device=bn.device)
+    one.pages.copy_(torch.from_numpy(oc.pages.reshape(one.pages.shape)))
+    qd, btd, lend = PT.to_dev(qb, bn.device), PT.to_dev(bt1, bn.device), PT.to_dev(len1, bn.device)
+    same = (one.decode(qd[:, 0].contiguous(), btd, lend).unsqueeze(1) if T == 1 else one.verify(qd, btd, lend))
+    same = same.cpu().numpy()
+    assert int(one.status.item()) == 0
+    one.close()
+    err_same = PT.assert_close(same, ref, f"{bn.name} seq {b}, kernels over the oracle's pages")
+    # end to end: only kv-head groups holding a near-boundary code may miss
+    got = out_gpu[b:b + 1] if T > 1 else out_gpu[b:b + 1, None]
+    miss = np.abs(got.astype(np.float64) - ref) > PT.ATOL + PT.RTOL * np.abs(ref)   # [1][T][Hq][d]
+    miss_heads = {int(hq) // spec.group for hq in np.nonzero(miss.any(axis=(0, 1, 3)))[0]}
+    assert miss_heads <= flipped_heads, (bn.name, b, sorted(miss_heads), sorted(flipped_heads))
+    dense = O.attention_dense(qb, k[None], v[None], len1, spec.num_q_heads, spec.num_kv_heads, T=T)
     cos = PT.cosine_per_head(got, dense)
-    return err, in_band, total_codes, float(cos.min()), float(cos.mean())
+    err_e2e = float(np.abs(got.astype(np.float64) - ref).max())
+    return err_same, err_e2e, sorted(miss_heads), in_band, total_codes, float(cos.min()), float(cos.mean())
 
 
-@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg2", "cfg2_32k", "cfg3", "cfg4", "cfg3_prefill"])
+@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg2", "cfg2_32k", "cfg3", "cfg4", "cfg3_prefill", "tq4_32k",
+                                  "tq2_32k", "tq3_prefill"])
 def test_full_size_workload(name, capsys):
     dev = torch.device("cuda", 0)
     bn = bench.Bench(name, dev)
@@ -123,8 +152,9 @@ def test_full_size_workload(name, capsys):
     lens = bn.wl.seq_lens
     samples = sorted({0, B - 1, int(np.argmax(lens))})
     for b in samples:
-        err, in_band, total, cmin, cmean = _check_sequence(bn, b, out)
+        err_same, err_e2e, miss, in_band, total, cmin, cmean = _check_sequence(bn, b, out)
         with capsys.disabled():
-            print(f"\n{name} seq {b} (ctx {int(lens[b])}): max abs err {err:.2e}, near-boundary codes "
-                  f"{in_band}/{total}, cosine vs fp16 attention min {cmin:.5f} mean {cmean:.5f}")
+            print(f"\n{name} seq {b} (ctx {int(lens[b])}): max abs err {err_same:.2e} over the oracle's pages, "
+                  f"{err_e2e:.2e} end to end (kv heads off tolerance: {miss}); near-boundary codes "
+                  f"{in_band}/{total}; cosine vs fp16 attention min {cmin:.5f} mean {cmean:.5f}")
     bn.cache.close()

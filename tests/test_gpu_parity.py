@@ -12,7 +12,8 @@ from tests import parity as PT
 
 pytestmark = pytest.mark.gpu
 
-PLANAR, ISO = synth.PLANAR, synth.ISO
+PLANAR, ISO, DENSE = synth.PLANAR, synth.ISO, synth.DENSE
+MODE_NAMES = {PLANAR: 'planar', ISO: 'iso', DENSE: 'dense'}
 
 
 def make_case(mode, bits, hq, hkv, P, lens, T=1, seed=7, zero_tokens=(), permuted=True):
@@ -43,7 +44,7 @@ def make_case(mode, bits, hq, hkv, P, lens, T=1, seed=7, zero_tokens=(), permute
 def run_both(wl, kv, q):
     s = wl.spec
     oc = PT.oracle_cache(wl)
-    margins, tokens = {}, []
+    margins, tokens, seq_of = {}, [], {}
     flat_k, flat_v, flat_slots = [], [], []
     ti = 0
     for b, (k, v) in enumerate(kv):
@@ -54,6 +55,7 @@ def run_both(wl, kv, q):
         mk, mv = oc.append(k, v, slots, with_margins=True)
         for t in range(L):
             margins[ti + t] = (mk[t], mv[t])
+            seq_of[ti + t] = b
             for h in range(s.num_kv_heads):
                 tokens.append((int(slots[t]) // s.page_size, int(slots[t]) % s.page_size, h, ti + t))
         flat_k.append(k)
@@ -85,7 +87,7 @@ def run_both(wl, kv, q):
     out2 = out2.cpu().numpy()
     cache.close()
     return dict(oc=oc, ref=ref, out=out, out_on_oracle_pages=out2, gpu_pages=gpu_pages, tokens=tokens,
-                margins=margins, inputs=(K, V), status=status)
+                margins=margins, inputs=(K, V), status=status, seq_of=seq_of)
 
 
 CASES = [
@@ -101,19 +103,32 @@ CASES = [
     (PLANAR, 4, 12, 4, 16, [48, 20], 3),
     (ISO, 4, 32, 8, 16, [5000], 1),
     (PLANAR, 3, 32, 8, 128, [700, 129], 2),
+    # 2-bit codes and the dense (TurboQuant) rotation
+    (PLANAR, 2, 32, 8, 16, [200, 33, 1], 1),
+    (ISO, 2, 64, 8, 64, [300, 65], 1),
+    (DENSE, 4, 32, 8, 16, [300, 17, 1024], 1),
+    (DENSE, 3, 64, 8, 16, [129, 1000, 5], 1),
+    (DENSE, 2, 32, 8, 16, [70, 100, 6, 7], 6),
+    (DENSE, 4, 24, 2, 32, [95, 3], 2),
+    (DENSE, 3, 40, 2, 16, [50, 200], 1),
+    (DENSE, 2, 8, 8, 16, [16, 48], 1),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{'iso' if c[0] else 'planar'}{c[1]}_G{c[2] // c[3]}_P{c[4]}_T{c[6]}_n{len(c[5])}")
-def test_append_and_attention_match_oracle(case):
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{MODE_NAMES[c[0]]}{c[1]}_G{c[2] // c[3]}_P{c[4]}_T{c[6]}_n{len(c[5])}")
+def test_append_and_attention_match_oracle(case, capsys):
     mode, bits, hq, hkv, P, lens, T = case
     wl, kv, q = make_case(mode, bits, hq, hkv, P, lens, T, zero_tokens=[(0, 3)])
     r = run_both(wl, kv, q)
     assert r["status"] == 0
-    compared, in_band = PT.compare_chunks(r["gpu_pages"], r["oc"], r["tokens"], r["margins"], r["inputs"])
+    flips = set()
+    compared, in_band = PT.compare_chunks(r["gpu_pages"], r["oc"], r["tokens"], r["margins"], r["inputs"], flips)
+    with capsys.disabled():
+        print(f" [{compared} codes, {in_band} within 1e-6 of a boundary]", end="")
     assert in_band <= max(2, compared // 100000), (in_band, compared)
     PT.assert_close(r["out_on_oracle_pages"], r["ref"], "attention over the oracle's pages")
-    PT.assert_close(r["out"], r["ref"], "append + attention")
+    allowed = {(r["seq_of"][ti], h) for ti, h in flips}
+    PT.assert_close_except(r["out"], r["ref"], hq // hkv, allowed, "append + attention")
 
 
 def test_zero_length_sequences_give_zeros():
