@@ -4,7 +4,8 @@
 
 A step is one pass of the whole hot path over one batch: the quantize-append of the step's
 new tokens, then split-K decode (or chain-verify) attention over the packed cache and the
-log-sum-exp combine.  Inputs are synthetic and seeded (rotation_quantized_kv_rq_gb300.synth);
+log-sum-exp combine.  A decode step that appends one token per sequence (cfg1) runs as one
+rq_decode_step call: the append is folded into the split-K kernel.  Inputs are synthetic and seeded (rotation_quantized_kv_rq_gb300.synth);
 the packed cache is built before timing and stays resident in HBM.
 
 Default workload cfg1: rq3_planar, 16 sequences x 8192 context, 32 q / 8 kv heads, page 16,
@@ -131,11 +132,17 @@ class Bench:
         if s.query_tokens == 1:
             self.q = self.q[:, 0].contiguous()
         self.out = torch.empty_like(self.q)
+        # one token per sequence, then decode: a single rq_decode_step (structured rotations)
+        self.fused_step = (not self.prefill_only and s.appended == 1 and s.query_tokens == 1
+                           and s.mode != synth.DENSE)
         torch.cuda.synchronize(device)
         assert int(self.cache.status.item()) == 0, "range fault while building the cache"
 
     def step(self):
         s = self.spec
+        if self.fused_step:
+            self.cache.decode_step(self.q, self.k_new, self.v_new, self.bt, self.lens, out=self.out)
+            return
         if self.k_new is not None:
             self.cache.append(self.k_new, self.v_new, self.slots_new)
         if self.prefill_only:
@@ -146,6 +153,8 @@ class Bench:
             self.cache.verify(self.q, self.bt, self.lens, out=self.out)
 
     def launches_per_step(self):
+        if self.fused_step:
+            return 2  # split-K with the append folded in, combine
         n = 1 if self.k_new is not None else 0
         # split-K + combine, and for a dense rotation the query pre-rotation
         return n if self.prefill_only else n + 2 + (self.spec.mode == synth.DENSE)
@@ -166,12 +175,13 @@ class Bench:
         s = self.spec
         pages = int(((self.wl.seq_lens + s.page_size - 1) // s.page_size).sum())
         q_bytes = 512 if s.mode == synth.DENSE else 256  # fp32 pre-rotated rows, or fp16 q
-        return self.packed_bytes() + s.batch * s.query_tokens * s.num_q_heads * q_bytes + pages * 4
+        fused = self.append_algorithmic_bytes() if self.fused_step else 0  # the step's tokens, when folded in
+        return self.packed_bytes() + s.batch * s.query_tokens * s.num_q_heads * q_bytes + pages * 4 + fused
 
     def append_algorithmic_bytes(self):
         n = int(self.slots_new.numel()) if self.slots_new is not None else 0
         per_vec = 256 + 16 * self.spec.bits + 2
-        return n * self.spec.num_kv_heads * 2 * per_vec + n * 4
+        return n * self.spec.num_kv_heads * 2 * per_vec + (0 if self.fused_step else n * 4)
 
 
 # ---------------------------------------------------------------------------------------
@@ -383,7 +393,8 @@ def run_ours(args, rank, world, local):
     d_k = torch.empty_like(bench.k_new) if h_k is not None else None
     d_v = torch.empty_like(bench.v_new) if h_k is not None else None
     d_s = torch.empty_like(bench.slots_new) if h_k is not None else None
-    h2d = h_q.numel() * 2 + (h_k.numel() * 2 * 2 + h_s.numel() * 4 if h_k is not None else 0)
+    h2d = h_q.numel() * 2 + (h_k.numel() * 2 * 2 + (0 if bench.fused_step else h_s.numel() * 4)
+                             if h_k is not None else 0)
     d2h = h_out.numel() * 2
     e2e_times = []
     n_e2e = max(3, min(K, 200))
@@ -391,12 +402,18 @@ def run_ours(args, rank, world, local):
         flush.fill_(float(i))
         torch.cuda.synchronize(device)
         t0 = time.perf_counter()
-        if h_k is not None:
+        if bench.fused_step:
+            d_k.copy_(h_k, non_blocking=True)
+            d_v.copy_(h_v, non_blocking=True)
+            d_q.copy_(h_q, non_blocking=True)
+            bench.cache.decode_step(d_q, d_k, d_v, bench.bt, bench.lens, out=bench.out)
+            h_out.copy_(bench.out, non_blocking=True)
+        elif h_k is not None:
             d_k.copy_(h_k, non_blocking=True)
             d_v.copy_(h_v, non_blocking=True)
             d_s.copy_(h_s, non_blocking=True)
             bench.cache.append(d_k, d_v, d_s)
-        if not bench.prefill_only:
+        if not bench.prefill_only and not bench.fused_step:
             d_q.copy_(h_q, non_blocking=True)
             if bench.spec.query_tokens == 1:
                 bench.cache.decode(d_q, bench.bt, bench.lens, out=bench.out)
@@ -436,7 +453,8 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None, "dtype": f"u{s.bits} codes, f16 mma, f32 accumulate", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}", "batch": s.batch,
                    "ctx": int(s.ctx), "query_tokens": s.query_tokens, "bits": s.bits,
-                   "mode": "planar" if s.mode == synth.PLANAR else "iso", "page_size": s.page_size,
+                   "mode": {synth.PLANAR: "planar", synth.ISO: "iso", synth.DENSE: "dense"}[s.mode],
+                   "page_size": s.page_size, "fused_decode_step": bench.fused_step,
                    "packed_kv_bytes": bench.packed_bytes(),
                    "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MB write) outside the per-step events",
                    "parallelism": f"replicas x{world}"},

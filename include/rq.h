@@ -155,6 +155,25 @@ int rq_decode_attention(rq_ctx *ctx, const void *q, const void *kv_pages, const 
                         void *stream);
 
 /*
+ * One decode step in one launch (plus the combine): quantize-append of every sequence's newest
+ * K/V token, folded into rq_decode_attention's split-K kernel, then decode attention over the
+ * cache including that token.
+ *   k_new, v_new  device fp16 [B][Hkv][head_dim]: the token of sequence b, written to position
+ *                 seq_lens[b] - 1 -- page block_table[b][(seq_lens[b] - 1) / P], offset
+ *                 (seq_lens[b] - 1) % P -- exactly as rq_quantize_append would write it
+ *   kv_pages      device page pool (written: the step's tokens; read: everything)
+ *   other arguments as rq_decode_attention; seq_lens[b] counts the new token, and a sequence
+ *   with seq_lens[b] = 0 appends nothing.
+ * The result equals rq_quantize_append of the tokens followed by rq_decode_attention.  A page id
+ * out of range for the new token sets RQ_STATUS_BAD_PAGE and skips its write.  Errors as
+ * rq_decode_attention, plus RQ_ERR_INVALID for a NULL or non-16-byte-aligned k_new / v_new, and
+ * RQ_ERR_UNSUPPORTED for RQ_DENSE (use rq_quantize_append, then rq_decode_attention).
+ */
+int rq_decode_step(rq_ctx *ctx, const void *q, const void *k_new, const void *v_new, void *kv_pages,
+                   const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B, void *out,
+                   int32_t *d_status, void *stream);
+
+/*
  * Speculative chain-verify attention: T query tokens per sequence, the last T cached tokens
  * being the drafts themselves (append them first).  Query row j (0 <= j < T) attends to
  * positions 0 .. seq_lens[b] - T + j (causal over the draft tail).

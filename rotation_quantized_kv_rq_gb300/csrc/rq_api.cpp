@@ -21,10 +21,10 @@ struct rq_ctx {
   __half* d_dense16;      // dense: fp16 hi/lo split of R_k and R_v for the append GEMM
   float* d_dense32;       // dense: fp32 R_k and R_v, row-major, for the append's exact recompute
   float* d_qrot;          // dense: fp32 R_k q of one attention call [max_batch][max_T][Hq][128]
-  float* d_ws;            // split-K partials
-  int* d_counters;        // attention work-item counters (2 ints, zero between launches)
+  float* d_ws;            // fragment partials of the stream-K split
+  int* d_frag;            // first / last CTA of each unit's fragments
   size_t ws_floats;
-  int max_splits;
+  size_t max_units;       // max_batch * Hkv * ceil(max_query_tokens * group / 8)
   int max_n_tiles;        // ceil(max_query_tokens * group / 8)
   cudaEvent_t prof_start; // optional diagnostics events (caller-owned)
   cudaEvent_t prof_end;
@@ -33,9 +33,6 @@ struct rq_ctx {
 };
 
 namespace {
-
-constexpr int kMaxSplitsDefault = 64;
-constexpr int kMaxSplitPages = 1024;  // mirrors the kernel's staging buffer
 
 // Makes `dev` current for the scope and restores the previous device afterwards.
 class DeviceScope {
@@ -98,6 +95,7 @@ int check_geometry(const rq_config* c) {
   if (c->bits < 2 || c->bits > 4) return RQ_ERR_UNSUPPORTED;
   if (c->page_size % 16 != 0 || c->page_size > 256) return RQ_ERR_UNSUPPORTED;
   if ((long long)c->num_pages * c->page_size > INT32_MAX) return RQ_ERR_UNSUPPORTED;
+  if (c->max_batch > rq::kMaxBatch) return RQ_ERR_UNSUPPORTED;
   if (!(c->sm_scale >= 0.0f) || std::isinf(c->sm_scale)) return RQ_ERR_INVALID;
   return RQ_OK;
 }
@@ -173,16 +171,13 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   const size_t table_floats = 2 * rot + 256 + 256;
   const int group = cfg->num_q_heads / hkv;
   ctx->max_n_tiles = (cfg->max_query_tokens * group + 7) / 8;
-  ctx->max_splits = kMaxSplitsDefault;
-  const int need = (cfg->max_pages_per_seq + kMaxSplitPages - 1) / kMaxSplitPages;
-  if (need > ctx->max_splits) ctx->max_splits = need;
-  if (ctx->max_splits > cfg->max_pages_per_seq) ctx->max_splits = cfg->max_pages_per_seq;
-  ctx->ws_floats = (size_t)cfg->max_batch * hkv * ctx->max_n_tiles * ctx->max_splits * 8 * rq::kPartialStride;
+  // one partial slot per fragment: at most units + CTAs of them (stream-K split)
+  ctx->max_units = (size_t)cfg->max_batch * hkv * ctx->max_n_tiles;
+  ctx->ws_floats = (ctx->max_units + (size_t)ctx->num_sms) * 8 * rq::kPartialStride;
 
   cudaError_t e = cudaMalloc(&ctx->d_tables, table_floats * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&ctx->d_ws, ctx->ws_floats * sizeof(float));
-  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_counters, 2 * sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(ctx->d_counters, 0, 2 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_frag, 2 * ctx->max_units * sizeof(int));
   const size_t dense16_halves = dense ? 2 * rot * 2 : 0;  // [K, V][Hkv][hi, lo][d][d]
   if (e == cudaSuccess && dense) {
     e = cudaMalloc(&ctx->d_dense16, dense16_halves * sizeof(__half));
@@ -236,7 +231,7 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   if (e != cudaSuccess) {
     cudaFree(ctx->d_tables);
     cudaFree(ctx->d_ws);
-    cudaFree(ctx->d_counters);
+    cudaFree(ctx->d_frag);
     cudaFree(ctx->d_dense16);
     cudaFree(ctx->d_dense32);
     cudaFree(ctx->d_qrot);
@@ -272,7 +267,7 @@ void rq_free(rq_ctx* ctx) {
     DeviceScope scope(ctx->device);
     cudaFree(ctx->d_tables);
     cudaFree(ctx->d_ws);
-    cudaFree(ctx->d_counters);
+    cudaFree(ctx->d_frag);
     cudaFree(ctx->d_dense16);
     cudaFree(ctx->d_dense32);
     cudaFree(ctx->d_qrot);
@@ -311,7 +306,7 @@ int rq_quantize_append(rq_ctx* ctx, const void* k, const void* v, const int32_t*
 
 static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tree_mask, const void* kv_pages,
                           const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B, void* out,
-                          int32_t* d_status, void* stream) {
+                          int32_t* d_status, void* stream, const void* k_new = nullptr, const void* v_new = nullptr) {
   if (!ctx || B < 0 || T < 1 || max_pages < 1) return RQ_ERR_INVALID;
   if (B == 0) return RQ_OK;
   if (!q || !kv_pages || !block_table || !seq_lens || !out) return RQ_ERR_INVALID;
@@ -332,40 +327,14 @@ static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tre
   a.status = d_status;
   a.tree_mask = tree_mask;
   a.q_rot = ctx->d_qrot;  // null unless dense
+  a.k_new = (const __half*)k_new;
+  a.v_new = (const __half*)v_new;
   a.ws = ctx->d_ws;
   a.rows = T * ctx->g.group;
   a.n_tiles_n = (a.rows + 7) / 8;
-  a.max_splits = ctx->max_splits;
-
-  a.counters = ctx->d_counters;
-
-  // Split planning.  Each split is a whole number of "one 16-token tile per warp" rounds
-  // (256 tokens).  A CTA works through ceil(items / CTAs) items in the worst case, each
-  // costing its tile rounds plus about two rounds of fixed work (query rotation, merge,
-  // partial write), so pick the split count that minimises that product.
-  const int P = ctx->g.page_size;
-  const long long units = (long long)B * ctx->g.num_kv_heads * a.n_tiles_n;
-  // one round = every warp of a CTA taking one 32-token pair
-  const int round_tokens = rq::kAttnWarps * rq::kAttnPairTokens;
-  const int quantum = round_tokens / P > 0 ? round_tokens / P : 1;
-  const long long min_pps = (max_pages + ctx->max_splits - 1) / ctx->max_splits;
-  long long best_pps = -1, best_cost = -1;
-  for (int ns = 1; ns <= ctx->max_splits; ++ns) {
-    long long pps = (max_pages + ns - 1) / ns;
-    pps = (pps + quantum - 1) / quantum * quantum;
-    if (pps < min_pps) pps = (min_pps + quantum - 1) / quantum * quantum;
-    if (pps > kMaxSplitPages) continue;
-    const long long nsplit = (max_pages + pps - 1) / pps;
-    if (nsplit > ctx->max_splits) continue;
-    const long long rounds = (units * nsplit + ctx->num_sms - 1) / ctx->num_sms;
-    const long long tile_rounds = (pps * P + round_tokens - 1) / round_tokens;
-    const long long cost = rounds * (tile_rounds + 1);
-    if (best_cost < 0 || cost < best_cost) best_cost = cost, best_pps = pps;
-  }
-  if (best_pps < 0) return RQ_ERR_CAPACITY;
-  a.pages_per_split = (int)best_pps;
-  return to_status(
-      rq::launch_attention(ctx->g, a, ctx->num_sms, (cudaStream_t)stream, ctx->prof_start, ctx->prof_end));
+  a.frag = ctx->d_frag;
+  a.grid = ctx->num_sms;  // one CTA per SM, each an equal share of the tiles
+  return to_status(rq::launch_attention(ctx->g, a, (cudaStream_t)stream, ctx->prof_start, ctx->prof_end));
 }
 
 int rq_verify_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages, const int32_t* block_table,
@@ -378,6 +347,16 @@ int rq_tree_verify_attention(rq_ctx* ctx, const void* q, int T, const uint64_t* 
                              int32_t* d_status, void* stream) {
   if (T > 64 || (B > 0 && !tree_mask)) return RQ_ERR_INVALID;
   return attention_call(ctx, q, T, tree_mask, kv_pages, block_table, max_pages, seq_lens, B, out, d_status, stream);
+}
+
+int rq_decode_step(rq_ctx* ctx, const void* q, const void* k_new, const void* v_new, void* kv_pages,
+                   const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B, void* out, int32_t* d_status,
+                   void* stream) {
+  if (!ctx) return RQ_ERR_INVALID;
+  if (ctx->g.mode == RQ_DENSE) return RQ_ERR_UNSUPPORTED;  // its append is a GEMM of its own
+  if (B > 0 && (!k_new || !v_new || (uintptr_t)k_new % 16 != 0 || (uintptr_t)v_new % 16 != 0)) return RQ_ERR_INVALID;
+  return attention_call(ctx, q, 1, nullptr, kv_pages, block_table, max_pages, seq_lens, B, out, d_status, stream, k_new,
+                        v_new);
 }
 
 int rq_decode_attention(rq_ctx* ctx, const void* q, const void* kv_pages, const int32_t* block_table, int max_pages,

@@ -7,10 +7,13 @@
 //   sum p v = R_v^T sum p n_v c[code_v]          (sum in rotated space, rotate back once)
 //
 // Kernel design (sm_103a):
-//   * Persistent CTAs of 16 warps; work item = (sequence, kv head, query n-tile, split of
-//     the context).  The CTA stages the split's page ids in shared memory, every warp takes
-//     16-token tiles of the split round-robin, and the warps' (m, l, O) are merged through
-//     shared memory into one partial per item.
+//   * One CTA of 16 warps per SM, stream-K partition: the work of all units (sequence, kv head,
+//     query n-tile), in that order, counted in rounds -- 32 consecutive 16-token tiles, one
+//     pair of tiles per warp -- is cut into gridDim.x equal contiguous ranges, so every SM gets
+//     the same number of rounds whatever the lengths.  The part of a unit that falls in one
+//     CTA's range is a fragment: the CTA stages its page ids in shared memory, the warps take
+//     its tiles two at a time round-robin, and their (m, l, O) are merged through shared
+//     memory into one partial per fragment.
 //   * Per 16-token tile both contractions run on the tensor cores with mma.sync m16n8k16
 //     (fp16 in, fp32 accumulate): S^T[16 tok x 8 q] = K~[16 x 128] q~^T and
 //     O^T[128 x 8 q] += V~^T[128 x 16 tok] P^T.  The <= 8 query rows of a kv head (the GQA
@@ -19,6 +22,9 @@
 //     codes (two 4-bit codes, two 3-bit codes assembled from the 3-bit planes, or four 2-bit
 //     codes read as two halves) indexes a half2 entry; each lane reads its own copy of the
 //     entry, so lookups never conflict.
+//   * A decode step can hand the kernel the step's new K/V token of every sequence: each CTA
+//     quantizes the tokens of the units whose last round it holds into the cache before it
+//     stages their pages, so the step needs no separate append launch.
 //   * Dense rotations (TurboQuant) change only the two ends: a small kernel forms R_k q for the
 //     whole call first, and the combine applies R_v^T per (sequence, kv head) group.
 //   * P is moved from the S^T accumulator layout to the B-operand layout with movmatrix.
@@ -26,6 +32,7 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include "rq_codec.cuh"
 #include "rq_internal.h"
 #include "../../include/rq.h"
 
@@ -56,7 +63,7 @@ constexpr int kMergeHalfBytes = kWarps * 4 * kPartialStride * 4;  // 4 query col
 //   [base, lut)          low slots (as many whole slots as fit), or nothing
 //   [lut, lut + 64 KB)   lookup table; lut = first 64 KB-aligned address >= base
 //   [lut + 64 KB, ...)   the remaining slots, page ids int[1024], mbarriers u64[16][2],
-//                        centroids float[16], item slot int[4]
+//                        centroids float[16], the CTA's position in its tile range (Walk)
 // Between items the two halves of the merge buffer (query columns 0-3 and 4-7) reuse slot
 // space: the low region when it holds a half, else the high slots.
 struct SmemPlan {
@@ -68,6 +75,37 @@ struct SmemPlan {
   uint32_t merge_hi;   // shared address of merge half 1 (columns 4-7)
   uint32_t end;        // one past the last byte used
 };
+constexpr int kRoundTiles = 2 * kWarps;  // a round: one pair of 16-token tiles per warp
+
+// Rounds of one unit of a sequence of len tokens: ceil(tiles / kRoundTiles).
+__host__ __device__ __forceinline__ int unit_rounds(int len) { return ((len + 15) / 16 + kRoundTiles - 1) / kRoundTiles; }
+
+// Where a CTA stands in its range [x, x_end) of rounds: sequence b, whose units' rounds start
+// at cumb.  Kept in shared memory (thread 0 advances it between fragments) so that none of it
+// occupies registers during the tile loop.
+struct Walk {
+  long long x, x_end, cumb;
+  int b;
+};
+
+// The fragment at the walk's position: rounds [r0, r1) of the rb rounds of unit uib of
+// sequence b (uib = kv head * n_tiles_n + n-tile), i.e. its tiles [t0, t1) of tb.
+struct Frag {
+  int tb, rb, uib, r0, r1, t0, t1;
+};
+__device__ __forceinline__ Frag frag_at(const Walk& w, int len) {
+  Frag f;
+  f.tb = (len + 15) / 16;
+  f.rb = unit_rounds(len);
+  const long long off = w.x - w.cumb;
+  f.uib = (int)(off / f.rb);
+  f.r0 = (int)(off % f.rb);
+  f.r1 = (int)min((long long)f.rb, f.r0 + (w.x_end - w.x));
+  f.t0 = f.r0 * kRoundTiles;
+  f.t1 = min(f.tb, f.r1 * kRoundTiles);
+  return f;
+}
+
 template <int BITS>
 __host__ __device__ constexpr SmemPlan smem_plan(uint32_t base) {
   SmemPlan p{};
@@ -82,7 +120,7 @@ __host__ __device__ constexpr SmemPlan smem_plan(uint32_t base) {
   p.merge_hi = lo_merge ? p.hi : p.hi + kMergeHalfBytes;
   const uint32_t hi_need = lo_merge ? kMergeHalfBytes : 2 * kMergeHalfBytes;
   p.tail = p.hi + (hi_bytes > hi_need ? hi_bytes : hi_need);
-  p.end = p.tail + kMaxSplitPages * 4 + kWarps * kStages * 8 + 64 + 16;
+  p.end = p.tail + kMaxSplitPages * 4 + kWarps * kStages * 8 + 64 + 32;
   return p;
 }
 
@@ -461,23 +499,6 @@ __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, ui
 // ---------------------------------------------------------------------------------------
 // The split-K kernel.
 // ---------------------------------------------------------------------------------------
-struct ItemInfo {
-  int b, h, nt, split;
-};
-
-// Items are ordered split-major, so every sequence's full-length splits come before the
-// (shorter or empty) last splits and the dynamic scheduler hands out long items first.
-__device__ __forceinline__ ItemInfo decode_item(int item, const Geometry& g, const AttnArgs& a) {
-  ItemInfo it;
-  it.nt = item % a.n_tiles_n;
-  int rest = item / a.n_tiles_n;
-  it.h = rest % g.num_kv_heads;
-  rest /= g.num_kv_heads;
-  it.b = rest % a.B;
-  it.split = rest / a.B;
-  return it;
-}
-
 // The lane's 32 dims 32tq..32tq+31 of R_k q for query row `row` of kv head h (zeros past the
 // rows): read from the call's pre-rotated buffer for a dense rotation (PRE), else the row's
 // fp16 q turned here -- Givens pairs or quaternion blocks never leave the lane's dims.
@@ -535,10 +556,61 @@ __device__ __forceinline__ void rotated_query(float (&y)[32], const Geometry& g,
   }
 }
 
-// PRE: the queries were rotated before the launch (dense rotation).
-template <int BITS, bool PRE>
+// Moves a walk past the fragment f it stands on (as thread 0 does between fragments).
+__device__ __forceinline__ void walk_advance(Walk& w, const Frag& f, int upb, const AttnArgs& a) {
+  w.x += f.r1 - f.r0;
+  if (f.r1 == f.rb && f.uib == upb - 1) {  // sequence b is done: on to the next one with tiles
+    w.cumb += (long long)f.rb * upb;
+    for (++w.b; w.x < w.x_end && w.b < a.B; ++w.b)
+      if (a.seq_lens[w.b] > 0) break;
+  }
+}
+
+// Decode step: quantizes the newest token (position len - 1) of the kv head of every unit whose
+// last round lies in the CTA's range [w.x, w.x_end), a warp per token (lanes 0-15 K, 16-31 V),
+// into its slot of the cache.  A unit's last round holds its last tile, so no other CTA stages
+// the token's page; n-tiles of one kv head may write the same token from several CTAs, with
+// equal bytes.  The proxy fence orders the writes before the bulk copies this CTA issues after
+// its next barrier.
+template <int BITS>
+__device__ __forceinline__ void step_append(const Geometry& g, const AttnArgs& a, Walk w, int cap, int upb) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, j = lane & 15;
+  float bnd[15];
+  codec::load_boundaries<BITS>(bnd, g.boundaries);
+  int i = 0;
+  while (w.x < w.x_end) {
+    int len = a.seq_lens[w.b];
+    len = len < 0 ? 0 : (len > cap ? cap : len);
+    const Frag f = frag_at(w, len);
+    if (f.r1 == f.rb) {  // warp-uniform
+      if (i % kWarps == warp) {
+        const int h = f.uib / a.n_tiles_n, pos = len - 1;
+        const int page = a.block_table[(size_t)w.b * a.max_pages + pos / g.page_size];
+        const bool ok = page >= 0 && page < g.num_pages;
+        if (!ok && lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
+        const __half* src = (half ? a.v_new : a.k_new) + ((size_t)w.b * g.num_kv_heads + h) * kHeadDim + 8 * j;
+        const float* rot = (half ? g.rot_v : g.rot_k) + (size_t)h * kHeadDim + 8 * j;
+        const float4 p0 = __ldg(reinterpret_cast<const float4*>(rot));
+        const float4 p1 = __ldg(reinterpret_cast<const float4*>(rot + 4));
+        const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        // the cache is the caller's writable pool; the attention arguments carry it read-only
+        uint8_t* chunk = const_cast<uint8_t*>(a.pages) + ((size_t)(ok ? page : 0) * g.num_kv_heads + h) * g.page_bytes;
+        codec::encode_structured<BITS>(*reinterpret_cast<const uint4*>(src), pr, g.mode, bnd, chunk, g.page_size, half,
+                                       pos % g.page_size, j, ok, a.status);
+      }
+      ++i;
+    }
+    walk_advance(w, f, upb, a);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// PRE: the queries were rotated before the launch (dense rotation).  STEP: a decode step that
+// quantizes each sequence's newest token first (a.k_new, a.v_new; structured rotations).
+template <int BITS, bool PRE, bool STEP>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_bytes) {
+attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   using R = Ring<BITS>;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t dyn_base = (uint32_t)__cvta_generic_to_shared(smem);
@@ -552,7 +624,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
   int* page_ids = reinterpret_cast<int*>(at(plan.tail));
   uint64_t* mbar = reinterpret_cast<uint64_t*>(page_ids + kMaxSplitPages);
   float* cb = reinterpret_cast<float*>(mbar + kWarps * kStages);
-  int* s_item = reinterpret_cast<int*>(cb + 16);
+  Walk* walk = reinterpret_cast<Walk*>(cb + 16);
   float* const merge_lo = reinterpret_cast<float*>(at(plan.merge_lo));
   float* const merge_hi = reinterpret_cast<float*>(at(plan.merge_hi));
 
@@ -577,37 +649,78 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
   uint32_t phase = 0;   // bit st: parity of the next completion of stage st
   bool broken = false;  // a staged copy never completed: stop using the ring
 
-  if (threadIdx.x == 0) *s_item = atomicAdd(a.counters, 1);
-  __syncthreads();
-  for (int item = *s_item; item < n_items;) {
-    const ItemInfo it = decode_item(item, g, a);
-    int len = a.seq_lens[it.b];
-    const int cap = a.max_pages * P;
-    if (len < 0 || len > cap || (len > 0 && len < a.T)) {
-      if (threadIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_LEN);
-      len = len < 0 ? 0 : (len > cap ? cap : len);
-    }
-    const int npages = (len + P - 1) / P;
-    const int p0 = it.split * a.pages_per_split;
-    int p1 = p0 + a.pages_per_split;
-    if (p1 > npages) p1 = npages;
-    if (p0 >= p1) {  // uniform across the CTA: the combine never reads this split
-      __syncthreads();
-      if (threadIdx.x == 0) *s_item = atomicAdd(a.counters, 1);
-      __syncthreads();
-      item = *s_item;
-      continue;
-    }
-
-    // Stage the split's page ids (clamped into the pool).
-    for (int i = threadIdx.x; i < p1 - p0; i += kThreads) {
-      int pg = a.block_table[(size_t)it.b * a.max_pages + p0 + i];
-      if (pg < 0 || pg >= g.num_pages) {
-        if (a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
-        pg = 0;
+  // ---- this CTA's range [x, x_end) of rounds in the stream-K partition ----
+  // cum[b] = rounds of all units of sequences < b; built with a block scan in the low slot
+  // region, which the ring does not use before the first fragment.
+  const int upb = g.num_kv_heads * a.n_tiles_n;  // units per sequence
+  const int cap = a.max_pages * P;
+  {
+    long long* cum = reinterpret_cast<long long*>(smem);
+    long long* wsum = reinterpret_cast<long long*>(page_ids);  // [kWarps] scan scratch
+    long long total = 0;
+    for (int c0 = 0; c0 < a.B; c0 += kThreads) {
+      const int bb = c0 + threadIdx.x;
+      long long v = 0;
+      if (bb < a.B) {
+        int len = a.seq_lens[bb];
+        if (len < 0 || len > cap || (len > 0 && len < a.T)) {
+          if (blockIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_LEN);
+          len = len < 0 ? 0 : (len > cap ? cap : len);
+        }
+        v = (long long)unit_rounds(len) * upb;
       }
-      page_ids[i] = pg;
+      long long inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+      }
+      if (lane == 31) wsum[warp] = inc;
+      __syncthreads();
+      if (warp == 0) {
+        long long w = lane < kWarps ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long n = __shfl_up_sync(0xffffffffu, w, o);
+          if (lane >= o) w += n;
+        }
+        if (lane < kWarps) wsum[lane] = w;
+      }
+      __syncthreads();
+      if (bb < a.B) cum[bb + 1] = total + (warp > 0 ? wsum[warp - 1] : 0) + inc;
+      total += wsum[kWarps - 1];
+      __syncthreads();
     }
+    if (threadIdx.x == 0) cum[0] = 0;
+    __syncthreads();
+    // Parts = min(CTAs, rounds), so that every part is non-empty: the combine takes the CTAs
+    // between a unit's first and last fragment to all hold one.  CTAs past the parts idle.
+    const long long parts = min((long long)gridDim.x, total);
+    const long long x0 = blockIdx.x < parts ? total * blockIdx.x / parts : 0;
+    const long long x1 = blockIdx.x < parts ? total * (blockIdx.x + 1) / parts : 0;
+    int lo = 0, hi = a.B;  // the last sequence b with cum[b] <= x0, which skips empty ones
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cum[mid] <= x0) lo = mid;
+      else hi = mid;
+    }
+    if (threadIdx.x == 0) *walk = Walk{x0, x1, cum[lo], lo};
+    __syncthreads();  // the scratch is slot space from here on
+  }
+  if constexpr (STEP) step_append<BITS>(g, a, *walk, cap, upb);
+
+  auto clamped_len = [&](int b) {
+    const int l = a.seq_lens[b];
+    return l < 0 ? 0 : (l > cap ? cap : l);
+  };
+  for (;;) {
+    if (walk->x >= walk->x_end) break;
+    const int len = clamped_len(walk->b);
+    const Frag fr = frag_at(*walk, len);
+    const int t1 = fr.t1;
+    struct {
+      int b, h, nt;
+    } it = {walk->b, fr.uib / a.n_tiles_n, fr.uib % a.n_tiles_n};
 
     // q~ = R_k q * sm_scale * log2(e) for query column gq of this n-tile, the lane's 32 dims.
     uint32_t qf[8][2];
@@ -635,7 +748,6 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
         draft_mask[c] = a.tree_mask ? a.tree_mask[(size_t)it.b * a.T + j] : 0ull;
       }
     }
-    __syncthreads();  // page ids staged
 
     float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
     float l_run[2] = {0.f, 0.f};
@@ -643,10 +755,29 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    // The split's tiles, taken two at a time: pair q = tiles tile0 + 2q and tile0 + 2q + 1
-    // (the second exists unless the split ends on an odd page); warp w takes pairs w + 16k.
-    const int tile0 = p0 * tiles_per_page, tile1 = p1 * tiles_per_page;
+    // The fragment in chunks of at most kMaxSplitPages pages (one chunk unless a CTA's range
+    // is very long); the warps' states carry over from chunk to chunk.
+    for (int tile0 = fr.t0; tile0 < t1;) {
+    const int p0 = tile0 / tiles_per_page;
+    const int tile1 = min(t1, (p0 + kMaxSplitPages) * tiles_per_page);
+    const int p1 = (tile1 + tiles_per_page - 1) / tiles_per_page;
+    __syncthreads();  // every warp is done with the previous chunk's page ids
+    for (int i = threadIdx.x; i < p1 - p0; i += kThreads) {  // stage them, clamped into the pool
+      int pg = a.block_table[(size_t)it.b * a.max_pages + p0 + i];
+      if (pg < 0 || pg >= g.num_pages) {
+        if (a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
+        pg = 0;
+      }
+      page_ids[i] = pg;
+    }
+    __syncthreads();
+
+    // The chunk's tiles, taken two at a time: pair q = tiles tile0 + 2q and tile0 + 2q + 1
+    // (the second exists unless the chunk ends there); warp w takes pairs w + 16k.
     const int n_pairs = (tile1 - tile0 + 1) / 2;
+    // A pair whose second tile lies past the chunk reads a stale slot for it: its positions,
+    // all past pos_lim, are masked like positions past the sequence.
+    const int pos_lim = tile1 * 16 - 1;
     const size_t head_off = (size_t)it.h * g.page_bytes;
     const int n_w = (warp < n_pairs && !broken) ? (n_pairs - 1 - warp) / kWarps + 1 : 0;
     // Lane 0 stages the warp's k-th pair into stage k % 2 (slots 2(k%2), 2(k%2)+1): per tile one
@@ -714,9 +845,9 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
         sc[7] = s[3] * nk3;
       }
       // Pairs wholly inside every column's visible range skip the per-element mask.
-      const bool interior = __all_sync(0xffffffffu, pos0 + 31 <= min(last_pos[0], last_pos[1]));
+      const bool interior = __all_sync(0xffffffffu, pos0 + 31 <= min(min(last_pos[0], last_pos[1]), pos_lim));
       if (!interior) {
-        const int draft0 = len - a.T;  // position of the first draft
+        const int draft0 = last_pos[0] + 1;  // tree: the first draft follows the prefix
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int pos = pos0 + 16 * (e >> 2) + rho<BITS>(gq) + 8 * ((e >> 1) & 1);
@@ -727,7 +858,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
           } else {
             vis = pos <= last_pos[e & 1];
           }
-          if (!vis) sc[e] = -CUDART_INF_F;
+          if (!vis || pos > pos_lim) sc[e] = -CUDART_INF_F;
         }
       }
       float alpha[2];
@@ -794,6 +925,8 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
       for (int k = consumed; k < min(n_w, consumed + kStages); ++k)
         mbar_wait_bounded(mbar_addr + 8 * (k % kStages), (phase >> (k % kStages)) & 1u);
     }
+    tile0 = tile1;
+    }
 
     // ---- merge the warps' partial states of this item ----
     __syncthreads();  // every warp is done with its slots, which the merge buffer reuses
@@ -825,9 +958,16 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
     }
     __syncthreads();
     {
+      // Fragment partials of unit u sit at slots u + c for its CTAs c: slots never collide,
+      // because both the units and the CTAs' ranges follow the same order.
       const int cols = min(8, a.rows - it.nt * 8);
-      float* dst = a.ws + ((((size_t)it.b * g.num_kv_heads + it.h) * a.n_tiles_n + it.nt) * a.max_splits + it.split) *
-                              8 * kPartialStride;
+      const int unit = (it.b * g.num_kv_heads + it.h) * a.n_tiles_n + it.nt;
+      float* dst = a.ws + (size_t)(unit + blockIdx.x) * 8 * kPartialStride;
+      if (threadIdx.x == 0) {
+        const Frag f = frag_at(*walk, clamped_len(it.b));
+        if (f.t0 == 0) a.frag[2 * unit] = blockIdx.x;         // the unit's first CTA
+        if (f.t1 == f.tb) a.frag[2 * unit + 1] = blockIdx.x;  // and its last
+      }
       for (int i = threadIdx.x; i < cols * 130; i += kThreads) {
         const int c = i / 130, e = i % 130;
         const float* mh = (c >> 2 ? merge_hi : merge_lo) + (c & 3) * kPartialStride;
@@ -849,19 +989,13 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
         else dst[c * kPartialStride + 4 + (e - 2)] = acc;
       }
     }
-    __syncthreads();  // merge buffer and page ids are reused by the next item
-    if (threadIdx.x == 0) *s_item = atomicAdd(a.counters, 1);
-    __syncthreads();
-    item = *s_item;
-  }
-  // The last CTA to finish re-arms the work counter for the next launch on this stream.
-  // Nothing waits on it: every CTA has already drawn an out-of-range item.
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(a.counters + 1, 1) == (int)gridDim.x - 1) {
-      atomicExch(a.counters, 0);
-      atomicExch(a.counters + 1, 0);
+    __syncthreads();  // the merge buffer reuses slot space
+    if (threadIdx.x == 0) {
+      Walk w = *walk;
+      walk_advance(w, frag_at(w, clamped_len(w.b)), upb, a);
+      *walk = w;
     }
+    __syncthreads();
   }
 }
 
@@ -872,24 +1006,25 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int n_items, int smem_byt
 // chains of dependent loads, and the O sum issues its independent loads eight at a time.
 // Zeros for an empty (or invalid) sequence.  All 32 lanes must call it.
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ float4 merge_splits(const Geometry& g, const AttnArgs& a, int nsplit, int b, int h, int row,
-                                               int lane) {
+__device__ __forceinline__ float4 merge_splits(const Geometry& g, const AttnArgs& a, int b, int h, int row, int lane) {
   const int nt = row >> 3, col = row & 7;
-  const int P = g.page_size;
   int len = a.seq_lens[b];
-  const int cap = a.max_pages * P;
+  const int cap = a.max_pages * g.page_size;
   len = len < 0 ? 0 : (len > cap ? cap : len);
-  const int npages = (len + P - 1) / P;
-  const int ns = min(nsplit, (npages + a.pages_per_split - 1) / a.pages_per_split);
-  const size_t stride = (size_t)8 * kPartialStride;  // between splits of one row
-  const float* base = a.ws + (((size_t)b * g.num_kv_heads + h) * a.n_tiles_n + nt) * a.max_splits * stride +
-                      (size_t)col * kPartialStride;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (len == 0 || len < a.T) return acc;
+  // the unit's fragments: CTAs first .. last, partials at slots unit + c
+  const int unit = (b * g.num_kv_heads + h) * a.n_tiles_n + nt;
+  const int first = a.frag[2 * unit], last = a.frag[2 * unit + 1];
+  if (first < 0 || last < first || last >= a.grid) return acc;  // a launch that gave up early
+  const int ns = last - first + 1;
+  const size_t stride = (size_t)8 * kPartialStride;  // between consecutive slots
+  const float* base = a.ws + (size_t)(unit + first) * stride + (size_t)col * kPartialStride;
   float M = -CUDART_INF_F;
   for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * stride]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M == -CUDART_INF_F || len < a.T) return acc;
+  if (M == -CUDART_INF_F) return acc;
   float L = 0.f;
   for (int s = lane; s < ns; s += 32) L += base[s * stride + 1] * exp2f(base[s * stride] - M);
 #pragma unroll
@@ -914,7 +1049,7 @@ __device__ __forceinline__ float4 merge_splits(const Geometry& g, const AttnArgs
 //   out = R_v^T o~  (block-local: a Givens pair or a quaternion block per lane).
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
-attn_combine_kernel(const Geometry g, const AttnArgs a, int nsplit) {
+attn_combine_kernel(const Geometry g, const AttnArgs a) {
   const int warp_global = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int total = a.B * a.T * g.num_q_heads;
@@ -924,7 +1059,7 @@ attn_combine_kernel(const Geometry g, const AttnArgs a, int nsplit) {
   const int b = warp_global / (g.num_q_heads * a.T);
   const int h = head / g.group;
   const int row = j * g.group + head % g.group;
-  const float4 o = merge_splits(g, a, nsplit, b, h, row, lane);
+  const float4 o = merge_splits(g, a, b, h, row, lane);
   const float y[4] = {o.x, o.y, o.z, o.w};
   const float4 p = __ldg(reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim) + lane);
   float x[4];
@@ -1013,7 +1148,7 @@ rotate_q_dense_kernel(const Geometry g, const AttnArgs a) {
 
 // The log-sum-exp merge of attn_combine_kernel for the CTA's rows, then out = R_v^T o~.
 __global__ void __launch_bounds__(kHeadDim)
-attn_combine_dense_kernel(const Geometry g, const AttnArgs a, int nsplit) {
+attn_combine_dense_kernel(const Geometry g, const AttnArgs a) {
   __shared__ __align__(16) float os[kDenseRows][kHeadDim];
   extern __shared__ __align__(16) float wsm[];
   const int h = blockIdx.x % g.num_kv_heads;
@@ -1026,7 +1161,7 @@ attn_combine_dense_kernel(const Geometry g, const AttnArgs a, int nsplit) {
     if (rr < nr) {  // uniform across the warp
       const int r = r0 + rr, bj = r / g.group;
       const int b = bj / a.T, j = bj % a.T;
-      res = merge_splits(g, a, nsplit, b, h, j * g.group + r % g.group, lane);
+      res = merge_splits(g, a, b, h, j * g.group + r % g.group, lane);
     }
     *reinterpret_cast<float4*>(&os[rr][4 * lane]) = res;
   }
@@ -1059,19 +1194,24 @@ size_t attention_smem_bytes() {
   return m;
 }
 
-template <int BITS, bool PRE>
+template <int BITS, bool PRE, bool STEP>
 static cudaError_t set_smem_limit() {
-  return cudaFuncSetAttribute(attn_splitk_kernel<BITS, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(attn_splitk_kernel<BITS, PRE, STEP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               smem_bytes_for(BITS));
 }
 
+template <int BITS>
+static cudaError_t set_smem_limits() {
+  cudaError_t e = set_smem_limit<BITS, false, false>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, true, false>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, false, true>();
+  return e;
+}
+
 cudaError_t attention_prepare() {
-  cudaError_t e = set_smem_limit<2, false>();
-  if (e == cudaSuccess) e = set_smem_limit<3, false>();
-  if (e == cudaSuccess) e = set_smem_limit<4, false>();
-  if (e == cudaSuccess) e = set_smem_limit<2, true>();
-  if (e == cudaSuccess) e = set_smem_limit<3, true>();
-  if (e == cudaSuccess) e = set_smem_limit<4, true>();
+  cudaError_t e = set_smem_limits<2>();
+  if (e == cudaSuccess) e = set_smem_limits<3>();
+  if (e == cudaSuccess) e = set_smem_limits<4>();
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(rotate_q_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
   if (e == cudaSuccess)
@@ -1080,20 +1220,21 @@ cudaError_t attention_prepare() {
 }
 
 template <int BITS>
-static void launch_splitk(const Geometry& g, const AttnArgs& a, int grid, int n_items, int smem, cudaStream_t stream) {
+static void launch_splitk(const Geometry& g, const AttnArgs& a, int smem, cudaStream_t stream) {
   if (a.q_rot)
-    attn_splitk_kernel<BITS, true><<<grid, kThreads, smem, stream>>>(g, a, n_items, smem);
+    attn_splitk_kernel<BITS, true, false><<<a.grid, kThreads, smem, stream>>>(g, a, smem);
+  else if (a.k_new)
+    attn_splitk_kernel<BITS, false, true><<<a.grid, kThreads, smem, stream>>>(g, a, smem);
   else
-    attn_splitk_kernel<BITS, false><<<grid, kThreads, smem, stream>>>(g, a, n_items, smem);
+    attn_splitk_kernel<BITS, false, false><<<a.grid, kThreads, smem, stream>>>(g, a, smem);
 }
 
-cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream,
-                             cudaEvent_t ev_start, cudaEvent_t ev_end) {
+cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
+                             cudaEvent_t ev_end) {
   if (a.B <= 0) return cudaSuccess;
   const bool dense = g.mode == RQ_DENSE;
   if (dense != (a.q_rot != nullptr)) return cudaErrorInvalidValue;
-  const int nsplit = (a.max_pages + a.pages_per_split - 1) / a.pages_per_split;
-  const long long n_items = (long long)a.B * g.num_kv_heads * a.n_tiles_n * nsplit;
+  if (a.k_new && (dense || !a.v_new || !g.boundaries || a.T != 1)) return cudaErrorInvalidValue;
   const long long rows_per_head = (long long)a.B * a.T * g.group;
   const unsigned groups = (unsigned)(g.num_kv_heads * ((rows_per_head + kDenseRows - 1) / kDenseRows));
   if (dense) {
@@ -1101,25 +1242,24 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if (n_items > 0) {
-    const int grid = (int)(n_items < num_ctas ? n_items : num_ctas);
+  if (a.grid > 0) {
     if (ev_start) cudaEventRecord(ev_start, stream);
     const int smem = smem_bytes_for(g.bits);
     if (g.bits == 4)
-      launch_splitk<4>(g, a, grid, (int)n_items, smem, stream);
+      launch_splitk<4>(g, a, smem, stream);
     else if (g.bits == 3)
-      launch_splitk<3>(g, a, grid, (int)n_items, smem, stream);
+      launch_splitk<3>(g, a, smem, stream);
     else
-      launch_splitk<2>(g, a, grid, (int)n_items, smem, stream);
+      launch_splitk<2>(g, a, smem, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev_end) cudaEventRecord(ev_end, stream);
   }
   if (dense) {
-    attn_combine_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a, nsplit);
+    attn_combine_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a);
   } else {
     const long long rows = (long long)a.B * a.T * g.num_q_heads;
-    attn_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(g, a, nsplit);
+    attn_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(g, a);
   }
   return cudaGetLastError();
 }

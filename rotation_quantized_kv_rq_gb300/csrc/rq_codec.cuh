@@ -1,0 +1,199 @@
+// Codec device code shared by the append kernels and the decode-step append inside the
+// attention kernel: the code search over the fp32 bin boundaries, and the packing of a
+// vector's codes into the storage contract of include/rq.h (section "RotorQuant KV Cache
+// Compression" of the "SGLang 1-Bit Turbo" README for the method; the bit layout is this
+// library's).  A vector is coded by a half-warp: lane j holds its dims 8j..8j+7.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/rq.h"
+
+namespace rq {
+namespace codec {
+
+// Number of boundaries strictly below u (b ascending, in registers): a binary search written as
+// a select tree, one compare per level and no indexed memory.
+template <int BITS>
+__device__ __forceinline__ int code_of(float u, const float (&b)[15]) {
+  if constexpr (BITS == 2) {
+    const bool s1 = u > b[1];
+    const bool s0 = u > (s1 ? b[2] : b[0]);
+    return (s1 ? 2 : 0) + (s0 ? 1 : 0);
+  } else if constexpr (BITS == 3) {
+    const bool s2 = u > b[3];
+    const bool s1 = u > (s2 ? b[5] : b[1]);
+    const bool s0 = u > (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
+    return (s2 ? 4 : 0) + (s1 ? 2 : 0) + (s0 ? 1 : 0);
+  } else {
+    const bool s3 = u > b[7];
+    const bool s2 = u > (s3 ? b[11] : b[3]);
+    const bool s1 = u > (s3 ? (s2 ? b[13] : b[9]) : (s2 ? b[5] : b[1]));
+    const float m0 = s3 ? (s2 ? (s1 ? b[14] : b[12]) : (s1 ? b[10] : b[8]))
+                        : (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
+    const bool s0 = u > m0;
+    return (s3 ? 8 : 0) + (s2 ? 4 : 0) + (s1 ? 2 : 0) + (s0 ? 1 : 0);
+  }
+}
+
+// code_of that also returns the distance from u to the nearest boundary: the boundaries on
+// either side of u are both among those the search compares against.
+template <int BITS>
+__device__ __forceinline__ int code_of_margin(float u, const float (&b)[15], float& dmin) {
+  if constexpr (BITS == 2) {
+    const bool s1 = u > b[1];
+    const float m0 = s1 ? b[2] : b[0];
+    dmin = fminf(fabsf(u - b[1]), fabsf(u - m0));
+    return (s1 ? 2 : 0) + (u > m0 ? 1 : 0);
+  } else if constexpr (BITS == 3) {
+    const bool s2 = u > b[3];
+    const float m1 = s2 ? b[5] : b[1];
+    const bool s1 = u > m1;
+    const float m0 = s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]);
+    dmin = fminf(fminf(fabsf(u - b[3]), fabsf(u - m1)), fabsf(u - m0));
+    return (s2 ? 4 : 0) + (s1 ? 2 : 0) + (u > m0 ? 1 : 0);
+  } else {
+    const bool s3 = u > b[7];
+    const float m2 = s3 ? b[11] : b[3];
+    const bool s2 = u > m2;
+    const float m1 = s3 ? (s2 ? b[13] : b[9]) : (s2 ? b[5] : b[1]);
+    const bool s1 = u > m1;
+    const float m0 = s3 ? (s2 ? (s1 ? b[14] : b[12]) : (s1 ? b[10] : b[8]))
+                        : (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
+    dmin = fminf(fminf(fabsf(u - b[7]), fabsf(u - m2)), fminf(fabsf(u - m1), fabsf(u - m0)));
+    return (s3 ? 8 : 0) + (s2 ? 4 : 0) + (s1 ? 2 : 0) + (u > m0 ? 1 : 0);
+  }
+}
+
+// Packs the codes of dims 8j..8j+7 (j = lane within its half-warp) of one vector and writes
+// them and the fp16 norm to the vector's place in `chunk` (kind 0 = K, 1 = V; `off` = offset
+// in page).  Every lane of the warp must call it: the 3-bit packing exchanges high bits
+// between lanes j and j ^ 2.  With `store` false nothing is written.
+template <int BITS>
+__device__ __forceinline__ void pack_store(const int (&code)[8], float nrm, uint8_t* chunk, int page_size, int kind,
+                                           int off, int j, bool store, int32_t* status) {
+  constexpr int vb = BITS * 16;
+  uint8_t* dst = chunk + (size_t)kind * page_size * vb + (size_t)off * vb;
+  uint8_t* vsec = chunk + (size_t)page_size * vb;
+  const int pair = off >> 1, hv = off & 1, c = j >> 1;  // V pair placement (2- and 4-bit)
+  if constexpr (BITS == 4) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) word |= (uint32_t)code[e] << (4 * e);
+    if (store) {
+      if (kind == 0) {
+        *reinterpret_cast<uint32_t*>(dst + 4 * j) = word;
+      } else {
+        // V: token pairs (2p, 2p+1) share 128 bytes; the 8-byte unit of 16-dim group c of
+        // token 2p + h sits at 16 * (c ^ (2p mod 8)) + 8h.  Lane j holds half of unit j / 2.
+        *reinterpret_cast<uint32_t*>(vsec + pair * 128 + 16 * (c ^ ((2 * pair) & 7)) + 8 * hv + 4 * (j & 1)) = word;
+      }
+    }
+  } else if constexpr (BITS == 2) {
+    uint32_t half_word = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) half_word |= (uint32_t)code[e] << (2 * e);
+    if (store) {
+      if (kind == 0) {
+        *reinterpret_cast<uint16_t*>(dst + 2 * j) = (uint16_t)half_word;
+      } else {
+        // V: token pairs share 64 bytes; the 4-byte unit of group c of token 2p + h sits at
+        // 8 * (c ^ (4 * (p / 2 mod 2))) + 4h.  Lane j holds half of unit j / 2.
+        *reinterpret_cast<uint16_t*>(vsec + pair * 64 + 8 * (c ^ (4 * ((pair >> 1) & 1))) + 4 * hv + 2 * (j & 1)) =
+            (uint16_t)half_word;
+      }
+    }
+  } else {
+    // Lane j covers dims 8m..8m+7 of 32-dim group w = j/4 (m = j%4).  Its low bits are
+    // bytes 2m, 2m+1 of the group's W0|W1; its high bits fill half of bytes 2(m&1) and
+    // 2(m&1)+1 of W2, shared with lane j^2 (same k, other h).
+    const int w = j >> 2, m = j & 3, hh = m >> 1;
+    uint32_t lo = 0, hib = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      lo |= (uint32_t)(code[e] & 3) << (2 * e);
+      const int r = e & 3, kk = e >> 2;  // dim 8m + e = 16hh + 4(2(m&1) + kk) + r
+      const int off_r = (r < 2) ? 4 + r : r - 2;
+      hib |= (uint32_t)(code[e] >> 2) << (8 * kk + 2 * hh + off_r);
+    }
+    const uint32_t partner = __shfl_xor_sync(0xffffffffu, hib, 2);
+    if (store) {
+      *reinterpret_cast<uint16_t*>(dst + 12 * w + 2 * m) = (uint16_t)lo;
+      if (hh == 0) *reinterpret_cast<uint16_t*>(dst + 12 * w + 8 + 2 * (m & 1)) = (uint16_t)(hib | partner);
+    }
+  }
+  if (store && j == 0) {
+    const __half n16 = __float2half_rn(nrm);
+    uint8_t* nb = chunk + (size_t)2 * page_size * vb + (size_t)kind * 2 * page_size + 2 * off;
+    *reinterpret_cast<__half*>(nb) = n16;
+    if (status && __hisinf(n16)) atomicOr(status, RQ_STATUS_NORM_OVERFLOW);
+  }
+}
+
+// 1 / n, so that u = y / n is formed as y * (1/n): within an ulp of the quotient, so a code can
+// differ from the quotient's only for u within ~1e-7 of a boundary.  n = 0 gives u = 0.
+__device__ __forceinline__ float inv_norm(float nrm) { return nrm > 0.f ? __frcp_rn(nrm) : 0.f; }
+
+template <int BITS>
+__device__ __forceinline__ void load_boundaries(float (&bnd)[15], const float* boundaries) {
+#pragma unroll
+  for (int i = 0; i < 15; ++i) bnd[i] = i < (1 << BITS) - 1 ? __ldg(boundaries + i) : 0.f;
+}
+
+
+// The structured rotation of the lane's 8 dims (dims 8j..8j+7: four Givens pairs or two
+// quaternion blocks), p = the lane's 8 parameters.
+__device__ __forceinline__ void rotate8(float (&y)[8], const float (&x)[8], const float (&p)[8], int mode) {
+  if (mode == RQ_PLANAR) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float c = p[2 * q], s = p[2 * q + 1];
+      y[2 * q] = c * x[2 * q] - s * x[2 * q + 1];
+      y[2 * q + 1] = s * x[2 * q] + c * x[2 * q + 1];
+    }
+  } else {  // Hamilton product (a,b,c,d) (x) (x0,x1,x2,x3)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float a = p[4 * q], b = p[4 * q + 1], c = p[4 * q + 2], d = p[4 * q + 3];
+      const float* xb = x + 4 * q;
+      y[4 * q + 0] = a * xb[0] - b * xb[1] - c * xb[2] - d * xb[3];
+      y[4 * q + 1] = b * xb[0] + a * xb[1] - d * xb[2] + c * xb[3];
+      y[4 * q + 2] = c * xb[0] + d * xb[1] + a * xb[2] - b * xb[3];
+      y[4 * q + 3] = d * xb[0] - c * xb[1] + b * xb[2] + a * xb[3];
+    }
+  }
+}
+
+// Encodes one fp16 vector with a structured rotation and writes it to slot `off` of `chunk`:
+// lane j of the half-warp passes its 16 bytes of x (dims 8j..8j+7) and its rotation
+// parameters.  Every lane of the warp must call it (shuffles); `store` false writes nothing.
+template <int BITS>
+__device__ __forceinline__ void encode_structured(uint4 raw, const float (&p)[8], int mode, const float (&bnd)[15],
+                                                  uint8_t* chunk, int page_size, int kind, int off, int j, bool store,
+                                                  int32_t* status) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  float x[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+    x[2 * e] = f.x;
+    x[2 * e + 1] = f.y;
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float nrm = __fsqrt_rn(ss);
+  float y[8];
+  rotate8(y, x, p, mode);
+  const float rcp = inv_norm(nrm);
+  int code[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) code[e] = code_of<BITS>(y[e] * rcp, bnd);
+  pack_store<BITS>(code, nrm, chunk, page_size, kind, off, j, store, status);
+}
+
+}  // namespace codec
+}  // namespace rq

@@ -48,14 +48,17 @@ struct AttnArgs {
   int T;
   void* out;                 // fp16 [B][T][Hq][128]
   int32_t* status;           // nullable
-  float* ws;                 // split-K partials
+  float* ws;                 // fragment partials: [units + grid][8 rows][kPartialStride] floats
+  int* frag;                 // [units][2]: first and last CTA holding a fragment of each unit
+  int grid;                  // CTAs of the split-K launch (the stream-K partition's parts)
   int rows;                  // T * group: query rows per kv head
   int n_tiles_n;             // ceil(rows / 8)
-  int pages_per_split;
-  int max_splits;            // splits per (b, kv head) the workspace has room for
-  int* counters;             // [2] work-item and finished-CTA counters, zero between launches
   const uint64_t* tree_mask; // [B][T] draft visibility bits (tree verify), or null (causal chain)
   float* q_rot;              // dense: fp32 [B][T][Hq][128] scratch for R_k q; null otherwise
+  // Decode step (planar / iso): fp16 [B][Hkv][128] K and V of each sequence's newest token,
+  // position seq_lens[b] - 1, quantized into the cache by the split-K kernel itself; or null.
+  const __half* k_new;
+  const __half* v_new;
 };
 
 constexpr int kPartialStride = 132;   // floats per partial row: m, l, pad, pad, o[128]
@@ -64,8 +67,12 @@ cudaError_t launch_append(const Geometry& g, const void* k, const void* v, const
                           int n, uint8_t* pages, int32_t* status, cudaStream_t stream);
 cudaError_t append_prepare();  // sets the dense append kernel's shared-memory limit
 
-cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, int num_ctas, cudaStream_t stream,
+cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t stream,
                              cudaEvent_t ev_start = nullptr, cudaEvent_t ev_end = nullptr);
+
+// The split-K kernel's prefix of tiles per sequence lives in its low slot region: at most this
+// many sequences per call.
+constexpr int kMaxBatch = 8000;
 
 // Dynamic shared memory the attention kernel needs (set as the kernel's maximum once).
 size_t attention_smem_bytes();

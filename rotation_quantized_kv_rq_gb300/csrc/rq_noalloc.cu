@@ -1,6 +1,6 @@
 // rq_decode_attention_noalloc: the decode attention of rq_decode_attention for callers that
-// cannot allocate device memory.  Its split-K scratch (the per-split partial states and the
-// two work counters) lives in one file-scope __device__ array instead of a context's
+// cannot allocate device memory.  Its split-K scratch (the fragment partials and the per-unit
+// fragment bounds) lives in one file-scope __device__ array instead of a context's
 // cudaMalloc'd workspace, and the tables come from the caller as device pointers, so the call
 // allocates nothing.  The kernels are the library's own attention kernels.
 #include <cuda_runtime.h>
@@ -13,14 +13,14 @@
 
 namespace {
 
-// Scratch: the two work counters, then split partials of kPartialStride floats per row.
+// Scratch: fragment bounds (2 ints per unit, kFragBytes), then fragment partials of 8 query
+// rows x kPartialStride floats.  A call with U units and G CTAs uses 2U ints and U + G slots.
 constexpr size_t kScratchBytes = (size_t)16 << 20;
-constexpr size_t kCounterBytes = 256;
-constexpr size_t kRowBytes = 8 * rq::kPartialStride * sizeof(float);  // one item: 8 query rows
-constexpr size_t kScratchItems = (kScratchBytes - kCounterBytes) / kRowBytes;
+constexpr size_t kFragBytes = (size_t)64 << 10;
+constexpr size_t kMaxUnits = kFragBytes / (2 * sizeof(int));           // 8,192
+constexpr size_t kSlotBytes = 8 * rq::kPartialStride * sizeof(float);   // one fragment
+constexpr size_t kScratchSlots = (kScratchBytes - kFragBytes) / kSlotBytes;  // 3,956
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSplits = 64;
-constexpr int kMaxSplitPages = 1024;
 
 // Every GPU that loads the library holds this array until the process exits.  Host code must
 // not use its name as an address: the device address comes from cudaGetSymbolAddress.
@@ -76,13 +76,13 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
 
   const int hkv = cfg->num_kv_heads, group = cfg->num_q_heads / hkv;
   const long long units = (long long)B * hkv * ((group + 7) / 8);
-  if (units > (long long)kScratchItems) return RQ_ERR_CAPACITY;  // not even one split fits
-  if ((max_pages + kMaxSplitPages - 1) / kMaxSplitPages > kMaxSplits) return RQ_ERR_CAPACITY;
+  if (B > rq::kMaxBatch || units > (long long)kMaxUnits) return RQ_ERR_CAPACITY;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RQ_ERR_CUDA;
   DeviceSlot* slot = nullptr;
   if (setup_device(dev, &slot) != cudaSuccess) return RQ_ERR_CUDA;
+  if (units + slot->num_sms > (long long)kScratchSlots) return RQ_ERR_CAPACITY;
 
   rq::Geometry g;
   g.num_q_heads = cfg->num_q_heads;
@@ -115,34 +115,14 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   a.status = d_status;
   a.tree_mask = nullptr;
   a.q_rot = nullptr;
+  a.k_new = a.v_new = nullptr;
   a.rows = group;
   a.n_tiles_n = (group + 7) / 8;
 
-  // Split choice as in the context path (whole 256-token rounds, fewest worst-case rounds),
-  // restricted to what the scratch array holds.
-  const int P = cfg->page_size;
-  // one round = every warp of a CTA taking one 32-token pair
-  const int round_tokens = rq::kAttnWarps * rq::kAttnPairTokens;
-  const int quantum = round_tokens / P > 0 ? round_tokens / P : 1;
-  long long best_pps = -1, best_cost = -1, best_ns = 0;
-  for (int ns = 1; ns <= kMaxSplits; ++ns) {
-    long long pps = (max_pages + ns - 1) / ns;
-    pps = (pps + quantum - 1) / quantum * quantum;
-    if (pps > kMaxSplitPages) continue;
-    const long long nsplit = (max_pages + pps - 1) / pps;
-    if (units * nsplit > (long long)kScratchItems) continue;
-    const long long rounds = (units * nsplit + slot->num_sms - 1) / slot->num_sms;
-    const long long cost = rounds * ((pps * P + round_tokens - 1) / round_tokens + 1);
-    if (best_cost < 0 || cost < best_cost) best_cost = cost, best_pps = pps, best_ns = nsplit;
-  }
-  if (best_pps < 0) return RQ_ERR_CAPACITY;
-  a.pages_per_split = (int)best_pps;
-  a.max_splits = (int)best_ns;
-  a.counters = reinterpret_cast<int*>(slot->scratch);
-  a.ws = reinterpret_cast<float*>(slot->scratch + kCounterBytes);
-
-  // The array keeps whatever the last call left: the counters must start every launch at 0.
-  cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemsetAsync(slot->scratch, 0, 2 * sizeof(int), st) != cudaSuccess) return RQ_ERR_CUDA;
-  return rq::launch_attention(g, a, slot->num_sms, st) == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+  a.frag = reinterpret_cast<int*>(slot->scratch);
+  a.ws = reinterpret_cast<float*>(slot->scratch + kFragBytes);
+  a.grid = slot->num_sms;
+  // Nothing in the array needs a starting value: every launch writes the bounds of every unit
+  // with tokens and the partials they point at before its combine reads them.
+  return rq::launch_attention(g, a, (cudaStream_t)stream) == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }

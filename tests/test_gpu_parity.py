@@ -244,3 +244,70 @@ def test_tree_verify_matches_oracle(mode, bits, hq, hkv, P, lens, T):
     assert torch.equal(a.view(torch.int16), b2.view(torch.int16))
     assert int(cache.status.item()) == 0
     cache.close()
+
+
+STEP_CASES = [
+    # mode, bits, Hq, Hkv, P, lens (each sequence's last token arrives with the step)
+    (PLANAR, 3, 32, 8, 16, [300, 17, 1, 64]),
+    (ISO, 4, 64, 8, 64, [200, 129, 64]),
+    (PLANAR, 4, 96, 8, 16, [100, 33]),     # group 12: two n-tiles per kv head write the token
+    (ISO, 2, 32, 8, 16, [50, 16, 2049]),
+]
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: f"{MODE_NAMES[c[0]]}{c[1]}_G{c[2] // c[3]}_P{c[4]}")
+def test_decode_step_appends_then_attends(case, capsys):
+    """rq_decode_step (append folded into the split-K kernel) writes the same bytes as
+    rq_quantize_append and returns the same output as append + rq_decode_attention; both match
+    the oracle."""
+    mode, bits, hq, hkv, P, lens = case
+    wl, kv, q = make_case(mode, bits, hq, hkv, P, lens, seed=17)
+    s = wl.spec
+    oc = PT.oracle_cache(wl)
+    margins, tokens, seq_of, flat = {}, [], {}, ([], [])
+    ti = 0
+    for b, (k, v) in enumerate(kv):
+        L = k.shape[0]
+        slots = PT.positions_slots(wl, b, 0, L)
+        mk, mv = oc.append(k, v, slots, with_margins=True)
+        for t in range(L):
+            margins[ti + t] = (mk[t], mv[t])
+            seq_of[ti + t] = b
+            for h in range(hkv):
+                tokens.append((int(slots[t]) // P, int(slots[t]) % P, h, ti + t))
+        flat[0].append(k)
+        flat[1].append(v)
+        ti += L
+    ref = oc.attention(q, wl.block_table, wl.seq_lens)
+    bt, sl, qd = PT.to_dev(wl.block_table), PT.to_dev(wl.seq_lens), PT.to_dev(q[:, 0])
+    k_new = PT.to_dev(np.stack([k[-1] for k, _ in kv]))
+    v_new = PT.to_dev(np.stack([v[-1] for _, v in kv]))
+
+    outs, pages = [], []
+    for fused in (True, False):
+        cache = rq.KVCache(mode, bits, hq, hkv, P, wl.num_pages, wl.rot_k, wl.rot_v, max_batch=s.batch,
+                           max_pages_per_seq=wl.block_table.shape[1])
+        for b, (k, v) in enumerate(kv):  # everything but the step's token
+            if k.shape[0] > 1:
+                cache.append(PT.to_dev(k[:-1]), PT.to_dev(v[:-1]),
+                             PT.to_dev(PT.positions_slots(wl, b, 0, k.shape[0] - 1)))
+        if fused:
+            out = cache.decode_step(qd, k_new, v_new, bt, sl)
+        else:
+            last = np.array([PT.positions_slots(wl, b, k.shape[0] - 1, 1)[0] for b, (k, _) in enumerate(kv)], np.int32)
+            cache.append(k_new, v_new, PT.to_dev(last))
+            out = cache.decode(qd, bt, sl)
+        torch.cuda.synchronize()
+        assert int(cache.status.item()) == 0
+        outs.append(out.cpu().numpy())
+        pages.append(cache.pages.cpu().numpy())
+        cache.close()
+    assert np.array_equal(pages[0], pages[1]), "decode step and append wrote different bytes"
+    assert np.array_equal(outs[0], outs[1]), "decode step and append + decode differ"
+    flips = set()
+    compared, in_band = PT.compare_chunks(pages[0], oc, tokens, margins,
+                                          (np.concatenate(flat[0]), np.concatenate(flat[1])), flips)
+    with capsys.disabled():
+        print(f" [{compared} codes, {in_band} within 1e-6 of a boundary]", end="")
+    allowed = {(seq_of[t], h) for t, h in flips}
+    PT.assert_close_except(outs[0][:, None], ref, hq // hkv, allowed, "decode step")
