@@ -85,7 +85,7 @@ __host__ __device__ __forceinline__ int unit_rounds(int len) { return ((len + 15
 // occupies registers during the tile loop.
 struct Walk {
   long long x, x_end, cumb;
-  int b;
+  int b, len;  // len: sequence b's tokens, clamped to the block table (> 0 while x < x_end)
 };
 
 // The fragment at the walk's position: rounds [r0, r1) of the rb rounds of unit uib of
@@ -93,13 +93,13 @@ struct Walk {
 struct Frag {
   int tb, rb, uib, r0, r1, t0, t1;
 };
-__device__ __forceinline__ Frag frag_at(const Walk& w, int len) {
+__device__ __forceinline__ Frag frag_at(const Walk& w) {
   Frag f;
-  f.tb = (len + 15) / 16;
-  f.rb = unit_rounds(len);
-  const long long off = w.x - w.cumb;
-  f.uib = (int)(off / f.rb);
-  f.r0 = (int)(off % f.rb);
+  f.tb = (w.len + 15) / 16;
+  f.rb = max(unit_rounds(w.len), 1);          // >= 1 whenever the walk has work left
+  const int off = (int)(w.x - w.cumb);        // < the rounds of one sequence's units
+  f.uib = off / f.rb;
+  f.r0 = off % f.rb;
   f.r1 = (int)min((long long)f.rb, f.r0 + (w.x_end - w.x));
   f.t0 = f.r0 * kRoundTiles;
   f.t1 = min(f.tb, f.r1 * kRoundTiles);
@@ -555,53 +555,63 @@ __device__ __forceinline__ void rotated_query(float (&y)[32], const Geometry& g,
     }
   }
 }
+// Sequence b's tokens, clamped to what its block-table row can hold.
+__device__ __forceinline__ int clamp_len(const AttnArgs& a, int b, int cap) {
+  const int l = a.seq_lens[b];
+  return l < 0 ? 0 : (l > cap ? cap : l);
+}
 
-// Moves a walk past the fragment f it stands on (as thread 0 does between fragments).
-__device__ __forceinline__ void walk_advance(Walk& w, const Frag& f, int upb, const AttnArgs& a) {
+// Moves a walk past the fragment f it stands on (thread 0, between fragments).
+__device__ __forceinline__ void walk_advance(Walk& w, const Frag& f, int upb, const AttnArgs& a, int cap) {
   w.x += f.r1 - f.r0;
   if (f.r1 == f.rb && f.uib == upb - 1) {  // sequence b is done: on to the next one with tiles
     w.cumb += (long long)f.rb * upb;
-    for (++w.b; w.x < w.x_end && w.b < a.B; ++w.b)
-      if (a.seq_lens[w.b] > 0) break;
+    for (++w.b; w.x < w.x_end && w.b < a.B; ++w.b) {
+      w.len = clamp_len(a, w.b, cap);
+      if (w.len > 0) break;
+    }
+    if (w.b >= a.B) w.x = w.x_end;  // nothing left (cannot happen with a consistent prefix)
   }
 }
 
 // Decode step: quantizes the newest token (position len - 1) of the kv head of every unit whose
-// last round lies in the CTA's range [w.x, w.x_end), a warp per token (lanes 0-15 K, 16-31 V),
-// into its slot of the cache.  A unit's last round holds its last tile, so no other CTA stages
-// the token's page; n-tiles of one kv head may write the same token from several CTAs, with
-// equal bytes.  The proxy fence orders the writes before the bulk copies this CTA issues after
-// its next barrier.
+// last round lies in the CTA's range [x0, x1) of rounds -- found from the prefix cum of rounds
+// per sequence -- a warp per token (lanes 0-15 K, 16-31 V), into its slot of the cache.  A
+// unit's last round holds its last tile, so no other CTA stages the token's page; n-tiles of
+// one kv head may write the same token from several CTAs, with equal bytes.  The proxy fence
+// orders the writes before the bulk copies this CTA issues after its next barrier.
 template <int BITS>
-__device__ __forceinline__ void step_append(const Geometry& g, const AttnArgs& a, Walk w, int cap, int upb) {
+__device__ __forceinline__ void step_append(const Geometry& g, const AttnArgs& a, const long long* cum, long long x0,
+                                            long long x1, int b0, int cap, int upb) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, j = lane & 15;
   float bnd[15];
   codec::load_boundaries<BITS>(bnd, g.boundaries);
-  int i = 0;
-  while (w.x < w.x_end) {
-    int len = a.seq_lens[w.b];
-    len = len < 0 ? 0 : (len > cap ? cap : len);
-    const Frag f = frag_at(w, len);
-    if (f.r1 == f.rb) {  // warp-uniform
-      if (i % kWarps == warp) {
-        const int h = f.uib / a.n_tiles_n, pos = len - 1;
-        const int page = a.block_table[(size_t)w.b * a.max_pages + pos / g.page_size];
-        const bool ok = page >= 0 && page < g.num_pages;
-        if (!ok && lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
-        const __half* src = (half ? a.v_new : a.k_new) + ((size_t)w.b * g.num_kv_heads + h) * kHeadDim + 8 * j;
-        const float* rot = (half ? g.rot_v : g.rot_k) + (size_t)h * kHeadDim + 8 * j;
-        const float4 p0 = __ldg(reinterpret_cast<const float4*>(rot));
-        const float4 p1 = __ldg(reinterpret_cast<const float4*>(rot + 4));
-        const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        // the cache is the caller's writable pool; the attention arguments carry it read-only
-        uint8_t* chunk = const_cast<uint8_t*>(a.pages) + ((size_t)(ok ? page : 0) * g.num_kv_heads + h) * g.page_bytes;
-        codec::encode_structured<BITS>(*reinterpret_cast<const uint4*>(src), pr, g.mode, bnd, chunk, g.page_size, half,
-                                       pos % g.page_size, j, ok, a.status);
-      }
-      ++i;
+  int i = 0;  // tokens enumerated so far: token i goes to warp i % kWarps
+  for (int b = b0; b < a.B && cum[b] < x1; ++b) {
+    const long long rounds = cum[b + 1] - cum[b];
+    if (rounds <= 0) continue;
+    const long long rb = rounds / upb;
+    // units whose last round, cum[b] + (u + 1) rb - 1, lies in [x0, x1)
+    const long long u_lo = max(0LL, (x0 - cum[b] + rb) / rb - 1);
+    const long long u_hi = min((long long)upb - 1, (x1 - cum[b]) / rb - 1);
+    for (long long u = u_lo; u <= u_hi; ++u, ++i) {
+      if (i % kWarps != warp) continue;  // warp-uniform
+      const int h = (int)u / a.n_tiles_n;
+      const int len = clamp_len(a, b, cap), pos = len - 1;
+      const int page = a.block_table[(size_t)b * a.max_pages + pos / g.page_size];
+      const bool ok = page >= 0 && page < g.num_pages;
+      if (!ok && lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
+      const __half* src = (half ? a.v_new : a.k_new) + ((size_t)b * g.num_kv_heads + h) * kHeadDim + 8 * j;
+      const float* rot = (half ? g.rot_v : g.rot_k) + (size_t)h * kHeadDim + 8 * j;
+      const float4 p0 = __ldg(reinterpret_cast<const float4*>(rot));
+      const float4 p1 = __ldg(reinterpret_cast<const float4*>(rot + 4));
+      const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      // the cache is the caller's writable pool; the attention arguments carry it read-only
+      uint8_t* chunk = const_cast<uint8_t*>(a.pages) + ((size_t)(ok ? page : 0) * g.num_kv_heads + h) * g.page_bytes;
+      codec::encode_structured<BITS>(*reinterpret_cast<const uint4*>(src), pr, g.mode, bnd, chunk, g.page_size, half,
+                                     pos % g.page_size, j, ok, a.status);
     }
-    walk_advance(w, f, upb, a);
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -704,50 +714,29 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       if (cum[mid] <= x0) lo = mid;
       else hi = mid;
     }
-    if (threadIdx.x == 0) *walk = Walk{x0, x1, cum[lo], lo};
+    if (threadIdx.x == 0) *walk = Walk{x0, x1, cum[lo], lo, clamp_len(a, lo, cap)};
+    if constexpr (STEP) step_append<BITS>(g, a, cum, x0, x1, lo, cap, upb);
     __syncthreads();  // the scratch is slot space from here on
   }
-  if constexpr (STEP) step_append<BITS>(g, a, *walk, cap, upb);
 
-  auto clamped_len = [&](int b) {
-    const int l = a.seq_lens[b];
-    return l < 0 ? 0 : (l > cap ? cap : l);
-  };
-  for (;;) {
+  // Every fragment advances the walk by at least one round, so this bound (the range's rounds)
+  // is never reached; it only guarantees that the loop ends.
+  const long long max_fragments = walk->x_end - walk->x;
+  for (long long n_frag = 0; n_frag < max_fragments; ++n_frag) {
     if (walk->x >= walk->x_end) break;
-    const int len = clamped_len(walk->b);
-    const Frag fr = frag_at(*walk, len);
+    const int len = walk->len;
+    const Frag fr = frag_at(*walk);
     const int t1 = fr.t1;
     struct {
       int b, h, nt;
     } it = {walk->b, fr.uib / a.n_tiles_n, fr.uib % a.n_tiles_n};
 
-    // q~ = R_k q * sm_scale * log2(e) for query column gq of this n-tile, the lane's 32 dims.
+    // q~ = R_k q * sm_scale * log2(e) for query column gq of this n-tile, the lane's 32 dims,
+    // formed once the fragment's first copies are in flight (below).
     uint32_t qf[8][2];
     const int row = it.nt * 8 + gq;  // query row of the kv head: draft j = row / group, head row % group
     int last_pos[2];                  // last position wholly visible to query columns 2tq, 2tq+1
     uint64_t draft_mask[2];           // tree verify: the columns' draft visibility bits
-    {
-      float y[32];
-      rotated_query<PRE>(y, g, a, it.b, it.h, row, tq);
-      // k-slot order of the K operand: dims (4kc, 4kc+1 | 4kc+2, 4kc+3) of the lane's 32, or
-      // (4kc, 4kc+2 | 4kc+1, 4kc+3) for 2-bit codes
-      constexpr int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;
-#pragma unroll
-      for (int kc = 0; kc < 8; ++kc) {
-        qf[kc][0] = pack_half2(y[4 * kc] * g.q_scale, y[4 * kc + s1] * g.q_scale);
-        qf[kc][1] = pack_half2(y[4 * kc + s2] * g.q_scale, y[4 * kc + 3] * g.q_scale);
-      }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int rc = it.nt * 8 + 2 * tq + c;
-        const int j = rc < a.rows ? rc / g.group : a.T - 1;
-        // chain: row j sees positions <= len - T + j; tree: the prefix for sure (the drafts
-        // by their mask bit), so only the prefix counts as wholly visible
-        last_pos[c] = a.tree_mask ? len - a.T - 1 : len - a.T + j;
-        draft_mask[c] = a.tree_mask ? a.tree_mask[(size_t)it.b * a.T + j] : 0ull;
-      }
-    }
 
     float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
     float l_run[2] = {0.f, 0.f};
@@ -806,6 +795,27 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     if (lane == 0 && n_w > 0) {
       fence_proxy_async();
       for (int k = 0; k < min(kStages, n_w); ++k) issue(k);
+    }
+    if (tile0 == fr.t0) {  // the fragment's first chunk: its copies overlap the query's loads
+      float y[32];
+      rotated_query<PRE>(y, g, a, it.b, it.h, row, tq);
+      // k-slot order of the K operand: dims (4kc, 4kc+1 | 4kc+2, 4kc+3) of the lane's 32, or
+      // (4kc, 4kc+2 | 4kc+1, 4kc+3) for 2-bit codes
+      constexpr int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        qf[kc][0] = pack_half2(y[4 * kc] * g.q_scale, y[4 * kc + s1] * g.q_scale);
+        qf[kc][1] = pack_half2(y[4 * kc + s2] * g.q_scale, y[4 * kc + 3] * g.q_scale);
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int rc = it.nt * 8 + 2 * tq + c;
+        const int j = rc < a.rows ? rc / g.group : a.T - 1;
+        // chain: row j sees positions <= len - T + j; tree: the prefix for sure (the drafts
+        // by their mask bit), so only the prefix counts as wholly visible
+        last_pos[c] = a.tree_mask ? len - a.T - 1 : len - a.T + j;
+        draft_mask[c] = a.tree_mask ? a.tree_mask[(size_t)it.b * a.T + j] : 0ull;
+      }
     }
     int consumed = 0;
     for (int k = 0; k < n_w; ++k) {
@@ -964,7 +974,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       const int unit = (it.b * g.num_kv_heads + it.h) * a.n_tiles_n + it.nt;
       float* dst = a.ws + (size_t)(unit + blockIdx.x) * 8 * kPartialStride;
       if (threadIdx.x == 0) {
-        const Frag f = frag_at(*walk, clamped_len(it.b));
+        const Frag f = frag_at(*walk);
         if (f.t0 == 0) a.frag[2 * unit] = blockIdx.x;         // the unit's first CTA
         if (f.t1 == f.tb) a.frag[2 * unit + 1] = blockIdx.x;  // and its last
       }
@@ -992,7 +1002,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     __syncthreads();  // the merge buffer reuses slot space
     if (threadIdx.x == 0) {
       Walk w = *walk;
-      walk_advance(w, frag_at(w, clamped_len(w.b)), upb, a);
+      walk_advance(w, frag_at(w), upb, a, cap);
       *walk = w;
     }
     __syncthreads();
