@@ -76,6 +76,10 @@ struct SmemPlan {
   uint32_t end;        // one past the last byte used
 };
 constexpr int kRoundTiles = 2 * kWarps;  // a round: one pair of 16-token tiles per warp
+// A CTA pays about this many rounds for each extra fragment (prologue, pipeline refill, the
+// barriers and the merge), measured on 16 x 8K-token decode: one whole unit per CTA on 128 of
+// 152 SMs beat 13.5 rounds in two fragments per CTA on all 152.
+constexpr int kFragmentRounds = 3;
 
 // Rounds of one unit of a sequence of len tokens: ceil(tiles / kRoundTiles).
 __host__ __device__ __forceinline__ int unit_rounds(int len) { return ((len + 15) / 16 + kRoundTiles - 1) / kRoundTiles; }
@@ -667,7 +671,10 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   {
     long long* cum = reinterpret_cast<long long*>(smem);
     long long* wsum = reinterpret_cast<long long*>(page_ids);  // [kWarps] scan scratch
+    int* wunits = page_ids + 2 * kWarps;                       // [kWarps]: units with tokens
+    int* wmax = wunits + kWarps;                                // [kWarps]: largest unit (rounds)
     long long total = 0;
+    int n_units = 0, max_rounds = 0;
     for (int c0 = 0; c0 < a.B; c0 += kThreads) {
       const int bb = c0 + threadIdx.x;
       long long v = 0;
@@ -678,6 +685,16 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           len = len < 0 ? 0 : (len > cap ? cap : len);
         }
         v = (long long)unit_rounds(len) * upb;
+      }
+      int nu = v > 0 ? upb : 0, mr = (int)(v / upb);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        nu += __shfl_xor_sync(0xffffffffu, nu, o);
+        mr = max(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+      }
+      if (lane == 0) {
+        wunits[warp] = nu;
+        wmax[warp] = mr;
       }
       long long inc = v;
 #pragma unroll
@@ -699,13 +716,26 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       __syncthreads();
       if (bb < a.B) cum[bb + 1] = total + (warp > 0 ? wsum[warp - 1] : 0) + inc;
       total += wsum[kWarps - 1];
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        n_units += wunits[w];
+        max_rounds = max(max_rounds, wmax[w]);
+      }
       __syncthreads();
     }
     if (threadIdx.x == 0) cum[0] = 0;
     __syncthreads();
     // Parts = min(CTAs, rounds), so that every part is non-empty: the combine takes the CTAs
     // between a unit's first and last fragment to all hold one.  CTAs past the parts idle.
-    const long long parts = min((long long)gridDim.x, total);
+    // When every unit has the same rounds and there are no more units than CTAs, one whole unit
+    // per part is the other candidate: a CTA's cost is its rounds plus kFragmentRounds per
+    // fragment, and equal parts that do not divide the units cost most CTAs two fragments.
+    long long parts = min((long long)gridDim.x, total);
+    if (n_units > 0 && n_units <= (int)gridDim.x && total == (long long)n_units * max_rounds) {
+      const long long per_part = (total + parts - 1) / parts;
+      const long long cost_split = per_part + (max_rounds % per_part == 0 ? 1 : 2) * kFragmentRounds;
+      if (max_rounds + kFragmentRounds <= cost_split) parts = n_units;
+    }
     const long long x0 = blockIdx.x < parts ? total * blockIdx.x / parts : 0;
     const long long x1 = blockIdx.x < parts ? total * (blockIdx.x + 1) / parts : 0;
     int lo = 0, hi = a.B;  // the last sequence b with cum[b] <= x0, which skips empty ones
@@ -938,7 +968,10 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     tile0 = tile1;
     }
 
-    // ---- merge the warps' partial states of this item ----
+    // ---- merge the warps' partial states of this fragment ----
+    // Warp w's O goes to row (w, mt & 3) of merge half mt / 4 as one float4 per lane: rows of
+    // 132 floats, so the writes are contiguous and the column-wise reads hit distinct bank
+    // groups.  m and l go to the page-id array, free until the next fragment.
     __syncthreads();  // every warp is done with its slots, which the merge buffer reuses
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -948,24 +981,18 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       l += __shfl_xor_sync(0xffffffffu, l, 16);
       l_run[c] = l;
     }
-    // merge half h holds query columns 4h..4h+3 of every warp: [warp][col & 3][132] floats
-    float* mw = (tq >> 1 ? merge_hi : merge_lo) + (size_t)warp * 4 * kPartialStride;
-    const int c0 = (2 * tq) & 3;
+    float* const ml = reinterpret_cast<float*>(page_ids);  // [warp][column][m, l]
     if (gq == 0) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        mw[(c0 + c) * kPartialStride + 0] = m_run[c];
-        mw[(c0 + c) * kPartialStride + 1] = l_run[c];
+        ml[(warp * 8 + 2 * tq + c) * 2] = m_run[c];
+        ml[(warp * 8 + 2 * tq + c) * 2 + 1] = l_run[c];
       }
     }
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int d0 = 16 * gq + 2 * mt;
-      mw[c0 * kPartialStride + 4 + d0] = o[mt][0];
-      mw[(c0 + 1) * kPartialStride + 4 + d0] = o[mt][1];
-      mw[c0 * kPartialStride + 4 + d0 + 1] = o[mt][2];
-      mw[(c0 + 1) * kPartialStride + 4 + d0 + 1] = o[mt][3];
-    }
+    for (int mt = 0; mt < 8; ++mt)
+      reinterpret_cast<float4*>((mt < 4 ? merge_lo : merge_hi) + (warp * 4 + (mt & 3)) * kPartialStride)[lane] =
+          make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
     __syncthreads();
     {
       // Fragment partials of unit u sit at slots u + c for its CTAs c: slots never collide,
@@ -978,25 +1005,30 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         if (f.t0 == 0) a.frag[2 * unit] = blockIdx.x;         // the unit's first CTA
         if (f.t1 == f.tb) a.frag[2 * unit + 1] = blockIdx.x;  // and its last
       }
-      for (int i = threadIdx.x; i < cols * 130; i += kThreads) {
-        const int c = i / 130, e = i % 130;
-        const float* mh = (c >> 2 ? merge_hi : merge_lo) + (c & 3) * kPartialStride;
+      // thread (c, gq', mt') merges dims 16 gq' + 2 mt' and +1 of column c: lane 4 gq' + c / 2
+      // of every warp held them, as components (c & 1) and (c & 1) + 2 of its float4 mt'
+      const int c = threadIdx.x >> 6, gm = (threadIdx.x >> 3) & 7, mm = threadIdx.x & 7;
+      if (c < cols) {
         float M = -CUDART_INF_F;
 #pragma unroll 4
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mh[(size_t)w * 4 * kPartialStride]);
-        float acc = 0.f;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 8 + c) * 2]);
+        float acc0 = 0.f, acc1 = 0.f, lsum = 0.f;
         if (M != -CUDART_INF_F) {
-          const int src = e == 0 ? -1 : (e == 1 ? 1 : 4 + (e - 2));
+          const float* half_base = (mm < 4 ? merge_lo : merge_hi) + (mm & 3) * kPartialStride + 4 * (4 * gm + (c >> 1));
 #pragma unroll 4
           for (int w = 0; w < kWarps; ++w) {
-            const float* mwp = mh + (size_t)w * 4 * kPartialStride;
-            const float scale = exp2f(mwp[0] - M);
-            if (src >= 0) acc += mwp[src] * scale;
+            const float scale = exp2f(ml[(w * 8 + c) * 2] - M);
+            const float4 v = *reinterpret_cast<const float4*>(half_base + w * 4 * kPartialStride);
+            acc0 += ((c & 1) ? v.y : v.x) * scale;
+            acc1 += ((c & 1) ? v.w : v.z) * scale;
+            lsum += ml[(w * 8 + c) * 2 + 1] * scale;
           }
         }
-        if (e == 0) dst[c * kPartialStride] = M;
-        else if (e == 1) dst[c * kPartialStride + 1] = acc;
-        else dst[c * kPartialStride + 4 + (e - 2)] = acc;
+        *reinterpret_cast<float2*>(dst + c * kPartialStride + 4 + 16 * gm + 2 * mm) = make_float2(acc0, acc1);
+        if (gm == 0 && mm == 0) {
+          dst[c * kPartialStride] = M;
+          dst[c * kPartialStride + 1] = lsum;
+        }
       }
     }
     __syncthreads();  // the merge buffer reuses slot space
