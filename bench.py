@@ -39,6 +39,7 @@ from rotation_quantized_kv_rq_gb300 import rq, synth  # noqa: E402
 
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TFLOPS_SUSTAINED = 1700.0
 L2_FLUSH_BYTES = 512 << 20
 
 DESCRIPTIONS = {
@@ -55,6 +56,8 @@ DESCRIPTIONS = {
     "tq3_32k": "tq3 (dense rotation) decode, 32 x 32768 ctx, 64 q / 8 kv heads, head_dim 128, page 16",
     "tq2_32k": "tq2 (dense rotation) decode, 32 x 32768 ctx, 64 q / 8 kv heads, head_dim 128, page 16",
     "tq3_prefill": "tq3 (dense rotation) quantize-append of 65536 tokens x 8 kv heads (K and V), page 16",
+    "cfg3_extend": "rq3_iso extend: 8 x (15360 cached + 1024 new) tokens, 32 q / 8 kv heads, head_dim 128, page 16, "
+                   "append the 1024 new tokens + causal extend attention",
 }
 
 
@@ -135,6 +138,7 @@ class Bench:
         # one token per sequence, then decode: a single rq_decode_step (structured rotations)
         self.fused_step = (not self.prefill_only and s.appended == 1 and s.query_tokens == 1
                            and s.mode != synth.DENSE)
+        self.extend = not self.prefill_only and s.query_tokens >= synth.EXTEND_MIN_T
         torch.cuda.synchronize(device)
         assert int(self.cache.status.item()) == 0, "range fault while building the cache"
 
@@ -149,12 +153,16 @@ class Bench:
             return
         if s.query_tokens == 1:
             self.cache.decode(self.q, self.bt, self.lens, out=self.out)
+        elif self.extend:
+            self.cache.extend(self.q, self.bt, self.lens, out=self.out)
         else:
             self.cache.verify(self.q, self.bt, self.lens, out=self.out)
 
     def launches_per_step(self):
         if self.fused_step:
             return 2  # split-K with the append folded in, combine
+        if self.extend:
+            return 2  # append, extend attention
         n = 1 if self.k_new is not None else 0
         # split-K + combine, and for a dense rotation the query pre-rotation
         return n if self.prefill_only else n + 2 + (self.spec.mode == synth.DENSE)
@@ -177,6 +185,16 @@ class Bench:
         q_bytes = 512 if s.mode == synth.DENSE else 256  # fp32 pre-rotated rows, or fp16 q
         fused = self.append_algorithmic_bytes() if self.fused_step else 0  # the step's tokens, when folded in
         return self.packed_bytes() + s.batch * s.query_tokens * s.num_q_heads * q_bytes + pages * 4 + fused
+
+    def extend_flops(self):
+        """Tensor-core FLOPs of the extend kernel per launch: query row j of a sequence of len tokens
+        sees len - T + j + 1 keys; per (row, key) 128 multiply-adds for QK^T and 128 for PV."""
+        s = self.spec
+        T = s.query_tokens
+        total = 0
+        for L in self.wl.seq_lens.astype(np.int64):
+            total += sum(max(0, int(L) - T + j + 1) for j in range(T))
+        return float(total) * s.num_q_heads * 4 * 128
 
     def append_algorithmic_bytes(self):
         n = int(self.slots_new.numel()) if self.slots_new is not None else 0
@@ -243,6 +261,17 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense fp16/bf16 tensor TFLOP/s sustained over a long loop (the kernel runs inside a step
+    loop), measured by cuBLAS bf16 -- fp16 has the same tensor-core rate."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured bf16_tflops_sustained"
+    return FALLBACK_TFLOPS_SUSTAINED, "fallback (1.7 PFLOP/s sustained)"
 
 
 def committed_traffic(kernel_file, workload):
@@ -417,6 +446,8 @@ def run_ours(args, rank, world, local):
             d_q.copy_(h_q, non_blocking=True)
             if bench.spec.query_tokens == 1:
                 bench.cache.decode(d_q, bench.bt, bench.lens, out=bench.out)
+            elif bench.extend:
+                bench.cache.extend(d_q, bench.bt, bench.lens, out=bench.out)
             else:
                 bench.cache.verify(d_q, bench.bt, bench.lens, out=bench.out)
             h_out.copy_(bench.out, non_blocking=True)
@@ -429,18 +460,27 @@ def run_ours(args, rank, world, local):
         return
     peak, peak_kind = measured_peaks()
     kms = statistics.mean(kern_ms)
-    if bench.prefill_only:
-        alg = bench.append_algorithmic_bytes()
-        kname = "append_kernel"
+    if bench.extend:
+        flops = bench.extend_flops()
+        tpeak, tkind = measured_tensor_peak()
+        achieved = flops / (kms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s", "frac": achieved / tpeak,
+                "traffic": committed_traffic("rq_extend.cu", args.workload), "kernel": "extend_kernel",
+                "algorithmic_flops_per_launch": flops, "kernel_ms_mean": kms,
+                "kernel_ms_median": statistics.median(kern_ms), "peak_source": tkind}
     else:
-        alg = bench.attention_algorithmic_bytes()
-        kname = "attn_splitk_kernel"
-    achieved = alg / (kms * 1e-3) / 1e9
-    traffic = committed_traffic("rq_attention.cu" if not bench.prefill_only else "rq_append.cu", args.workload)
-    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": traffic, "kernel": kname, "algorithmic_bytes_per_launch": alg,
-            "kernel_ms_mean": kms, "kernel_ms_median": statistics.median(kern_ms),
-            "peak_source": f"{peak_kind} hbm_gbs", "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
+        if bench.prefill_only:
+            alg = bench.append_algorithmic_bytes()
+            kname = "append_kernel"
+        else:
+            alg = bench.attention_algorithmic_bytes()
+            kname = "attn_splitk_kernel"
+        achieved = alg / (kms * 1e-3) / 1e9
+        traffic = committed_traffic("rq_attention.cu" if not bench.prefill_only else "rq_append.cu", args.workload)
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "kernel": kname, "algorithmic_bytes_per_launch": alg,
+                "kernel_ms_mean": kms, "kernel_ms_median": statistics.median(kern_ms),
+                "peak_source": f"{peak_kind} hbm_gbs", "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rate, sample, secs = oracle_step_rate(args.workload, budget_s=args.cpu_budget)

@@ -155,6 +155,21 @@ int rq_decode_attention(rq_ctx *ctx, const void *q, const void *kv_pages, const 
                         void *stream);
 
 /*
+ * Extend (prefill) attention: T new query tokens per sequence, already appended as the last T
+ * tokens of the cache, each attending to the cached prefix and causally to the new tokens:
+ * query row j (0 <= j < T) sees positions 0 .. seq_lens[b] - T + j -- the same result as
+ * rq_verify_attention, computed by a kernel built for large T (64 query rows share every
+ * dequantized tile of the cache; tensor-core QK^T and PV).  It uses no workspace: T is limited
+ * only by the q / out buffers, not by max_query_tokens.
+ *   q   device fp16 [B][T][Hq][head_dim],   out device fp16 [B][T][Hq][head_dim]
+ * Other arguments as rq_verify_attention.  Errors as rq_verify_attention (except that T above
+ * max_query_tokens is allowed), plus RQ_ERR_UNSUPPORTED for RQ_DENSE.
+ */
+int rq_extend_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages, const int32_t *block_table,
+                        int max_pages, const int32_t *seq_lens, int B, void *out, int32_t *d_status,
+                        void *stream);
+
+/*
  * One decode step in one launch (plus the combine): quantize-append of every sequence's newest
  * K/V token, folded into rq_decode_attention's split-K kernel, then decode attention over the
  * cache including that token.

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "librq.so")
-SOURCES = ["rq_api.cpp", "rq_append.cu", "rq_attention.cu", "rq_noalloc.cu"]
+SOURCES = ["rq_api.cpp", "rq_append.cu", "rq_attention.cu", "rq_extend.cu", "rq_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

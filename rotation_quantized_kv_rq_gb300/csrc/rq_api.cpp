@@ -228,6 +228,7 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   std::free(host16);
   if (e == cudaSuccess) e = rq::attention_prepare();
   if (e == cudaSuccess) e = rq::append_prepare();
+  if (e == cudaSuccess) e = rq::extend_prepare();
   if (e != cudaSuccess) {
     cudaFree(ctx->d_tables);
     cudaFree(ctx->d_ws);
@@ -347,6 +348,30 @@ int rq_tree_verify_attention(rq_ctx* ctx, const void* q, int T, const uint64_t* 
                              int32_t* d_status, void* stream) {
   if (T > 64 || (B > 0 && !tree_mask)) return RQ_ERR_INVALID;
   return attention_call(ctx, q, T, tree_mask, kv_pages, block_table, max_pages, seq_lens, B, out, d_status, stream);
+}
+
+int rq_extend_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages, const int32_t* block_table,
+                        int max_pages, const int32_t* seq_lens, int B, void* out, int32_t* d_status, void* stream) {
+  if (!ctx || B < 0 || T < 1 || max_pages < 1) return RQ_ERR_INVALID;
+  if (B == 0) return RQ_OK;
+  if (!q || !kv_pages || !block_table || !seq_lens || !out) return RQ_ERR_INVALID;
+  if (ctx->g.mode == RQ_DENSE) return RQ_ERR_UNSUPPORTED;
+  if (B > ctx->cfg.max_batch || max_pages > ctx->cfg.max_pages_per_seq) return RQ_ERR_CAPACITY;
+  if ((long long)T * ctx->g.group > INT32_MAX / 2) return RQ_ERR_CAPACITY;
+  DeviceScope scope(ctx->device);
+  if (!scope.ok()) return RQ_ERR_CUDA;
+  rq::AttnArgs a{};
+  a.q = q;
+  a.pages = (const uint8_t*)kv_pages;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.B = B;
+  a.T = T;
+  a.out = out;
+  a.status = d_status;
+  a.rows = T * ctx->g.group;
+  return to_status(rq::launch_extend(ctx->g, a, (cudaStream_t)stream, ctx->prof_start, ctx->prof_end));
 }
 
 int rq_decode_step(rq_ctx* ctx, const void* q, const void* k_new, const void* v_new, void* kv_pages,

@@ -74,6 +74,11 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t 
 // many sequences per call.
 constexpr int kMaxBatch = 8000;
 
+// Extend (prefill) attention: T query tokens per sequence, causal, no workspace.
+cudaError_t launch_extend(const Geometry& g, const AttnArgs& a, cudaStream_t stream, cudaEvent_t ev_start = nullptr,
+                          cudaEvent_t ev_end = nullptr);
+cudaError_t extend_prepare();
+
 // Dynamic shared memory the attention kernel needs (set as the kernel's maximum once).
 size_t attention_smem_bytes();
 cudaError_t attention_prepare();

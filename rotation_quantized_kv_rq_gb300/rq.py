@@ -24,7 +24,7 @@ HEAD_DIM = 128
 
 EXPORTS = ["rq_create", "rq_free", "rq_page_bytes", "rq_lloyd_max_codebook", "rq_get_codebook",
            "rq_quantize_append", "rq_decode_attention", "rq_verify_attention", "rq_set_profile_events",
-           "rq_decode_attention_noalloc", "rq_tree_verify_attention", "rq_decode_step", "rq_status_string"]
+           "rq_decode_attention_noalloc", "rq_tree_verify_attention", "rq_decode_step", "rq_extend_attention", "rq_status_string"]
 
 
 class RQError(RuntimeError):
@@ -70,6 +70,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             L.rq_decode_attention.restype = ctypes.c_int
             L.rq_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]
             L.rq_decode_step.restype = ctypes.c_int
+            L.rq_extend_attention.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]
+            L.rq_extend_attention.restype = ctypes.c_int
             L.rq_verify_attention.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, vp,
                                               vp]
             L.rq_verify_attention.restype = ctypes.c_int
@@ -191,6 +193,19 @@ def rq_decode_step(ctx, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tenso
     return out
 
 
+def rq_extend_attention(ctx, q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
+                        seq_lens: torch.Tensor, out: torch.Tensor, status: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """Extend (prefill) attention: q, out fp16 [B][T][Hq][128]; row j sees positions <= len - T + j."""
+    B, T = q.shape[0], q.shape[1]
+    assert q.dtype == torch.float16 and out.dtype == torch.float16 and q.is_contiguous() and out.is_contiguous()
+    assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32 and block_table.is_contiguous()
+    _check("rq_extend_attention",
+           lib().rq_extend_attention(ctx, _ptr(q), T, _ptr(kv_pages), _ptr(block_table), block_table.shape[-1],
+                                     _ptr(seq_lens), B, _ptr(out), _ptr(status), _stream(stream, q.device)))
+    return out
+
+
 def rq_verify_attention(ctx, q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
                         seq_lens: torch.Tensor, out: torch.Tensor, status: torch.Tensor | None = None,
                         stream=None) -> torch.Tensor:
@@ -283,6 +298,11 @@ class KVCache:
         if out is None:
             out = torch.empty_like(q)
         return rq_decode_step(self.ctx, q, k_new, v_new, self.pages, block_table, seq_lens, out, self.status, stream)
+
+    def extend(self, q, block_table, seq_lens, out=None, stream=None):
+        if out is None:
+            out = torch.empty_like(q)
+        return rq_extend_attention(self.ctx, q, self.pages, block_table, seq_lens, out, self.status, stream)
 
     def verify(self, q, block_table, seq_lens, out=None, stream=None):
         if out is None:

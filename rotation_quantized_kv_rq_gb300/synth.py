@@ -19,6 +19,8 @@ Workloads (geometry from the five synthetic decode/verify configurations of this
   tq{2,3,4}_32k  TurboQuant (dense random orthogonal rotation) decode at 2, 3 and 4 bits on
         the cfg2_32k geometry and data.
   tq3_prefill  dense-rotation quantize-append of 65536 tokens x 8 kv heads.
+  cfg3_extend  extend (chunked prefill): 8 sequences of 15360 cached tokens take 1024 new tokens
+        each, appended then attended causally (rq3 iso, 32/8 heads, page 16).
 
 Distributions: Q, V ~ N(0, 1); K ~ N(0, 1) with 4 distinct channels per kv head (drawn from
 the seed, fixed for all tokens) multiplied by 10 after sampling; fp16 storage.
@@ -68,7 +70,10 @@ SPECS = {
     "tq4_32k": Spec("tq4_32k", DENSE, 4, 32, 32768, 64, 8, 16, appended=0, seed=1002),
     "tq3_32k": Spec("tq3_32k", DENSE, 3, 32, 32768, 64, 8, 16, appended=0, seed=1002),
     "tq2_32k": Spec("tq2_32k", DENSE, 2, 32, 32768, 64, 8, 16, appended=0, seed=1002),
+    # extend: the cfg3 geometry and seed, 1024 new tokens per sequence
+    "cfg3_extend": Spec("cfg3_extend", ISO, 3, 8, 16384, 32, 8, 16, query_tokens=1024, appended=1024, seed=1003),
 }
+EXTEND_MIN_T = 64  # query tokens from which a step attends with the extend kernel
 PREFILL_TOKENS = 65536     # prefill workloads: one sequence, all 8 kv heads, K and V
 PREFILL = {"cfg3_prefill": "cfg3", "tq3_prefill": "tq3_32k"}  # workload -> spec it takes its codec from
 

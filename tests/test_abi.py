@@ -88,6 +88,7 @@ def test_calls_reject_null_context():
     assert L.rq_quantize_append(None, None, None, None, 1, None, None, None) == rq.RQ_ERR_INVALID
     assert L.rq_decode_attention(None, None, None, None, 1, None, 1, None, None, None) == rq.RQ_ERR_INVALID
     assert L.rq_decode_step(None, None, None, None, None, None, 1, None, 1, None, None, None) == rq.RQ_ERR_INVALID
+    assert L.rq_extend_attention(None, None, 2, None, None, 1, None, 1, None, None, None) == rq.RQ_ERR_INVALID
     assert L.rq_verify_attention(None, None, 2, None, None, 1, None, 1, None, None, None) == rq.RQ_ERR_INVALID
 
 

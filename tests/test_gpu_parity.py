@@ -311,3 +311,38 @@ def test_decode_step_appends_then_attends(case, capsys):
         print(f" [{compared} codes, {in_band} within 1e-6 of a boundary]", end="")
     allowed = {(seq_of[t], h) for t, h in flips}
     PT.assert_close_except(outs[0][:, None], ref, hq // hkv, allowed, "decode step")
+
+
+EXTEND_CASES = [
+    # mode, bits, Hq, Hkv, P, lens (after the new tokens), T
+    (PLANAR, 4, 32, 8, 16, [300, 1000], 64),
+    (ISO, 3, 64, 8, 64, [200, 513], 100),
+    (PLANAR, 2, 32, 8, 16, [17, 50, 33], 17),
+    (ISO, 4, 24, 2, 32, [129, 70], 70),      # group 12: 64-row blocks cut through a draft's heads
+    (PLANAR, 3, 8, 8, 16, [2048], 256),
+]
+
+
+@pytest.mark.parametrize("case", EXTEND_CASES, ids=lambda c: f"{MODE_NAMES[c[0]]}{c[1]}_G{c[2] // c[3]}_P{c[4]}_T{c[6]}")
+def test_extend_attention_matches_oracle(case):
+    """rq_extend_attention (causal attention of T new tokens over the packed cache) against the
+    oracle's chain attention over the same pages, and against rq_verify_attention."""
+    mode, bits, hq, hkv, P, lens, T = case
+    wl, kv, q = make_case(mode, bits, hq, hkv, P, lens, T=T, seed=23)
+    s = wl.spec
+    oc = PT.oracle_cache(wl)
+    for b, (k, v) in enumerate(kv):
+        oc.append(k, v, PT.positions_slots(wl, b, 0, k.shape[0]))
+    ref = oc.attention(q, wl.block_table, wl.seq_lens, T=T)
+    cache = rq.KVCache(mode, bits, hq, hkv, P, wl.num_pages, wl.rot_k, wl.rot_v, max_batch=s.batch,
+                       max_query_tokens=T, max_pages_per_seq=wl.block_table.shape[1])
+    cache.pages.copy_(torch.from_numpy(oc.pages.reshape(cache.pages.shape)))  # the oracle's own pages
+    bt, sl, qd = PT.to_dev(wl.block_table), PT.to_dev(wl.seq_lens), PT.to_dev(q)
+    out = cache.extend(qd, bt, sl)
+    ver = cache.verify(qd, bt, sl)
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) == 0
+    out, ver = out.cpu().numpy(), ver.cpu().numpy()
+    cache.close()
+    PT.assert_close(out, ref, "extend attention")
+    PT.assert_close(ver, ref, "verify attention")
