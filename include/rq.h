@@ -134,7 +134,8 @@ int rq_get_codebook(const rq_ctx *ctx, float *centroids, float *boundaries);
  * k[t][h][:] and v[t][h][:] (device fp16 [n][Hkv][head_dim]) into slot slot_mapping[t]
  * (device int32 [n]) of the page pool kv_pages (device, see the storage contract).  A slot
  * < 0 is skipped (padding); a slot >= num_pages * page_size sets RQ_STATUS_BAD_SLOT and is
- * skipped.  Slots within one call must be distinct.  n = 0 is a no-op.
+ * skipped.  Slots within one call must be distinct.  n = 0 is a no-op.  k, v and kv_pages must be
+ * 16-byte aligned (RQ_ERR_INVALID otherwise).
  */
 int rq_quantize_append(rq_ctx *ctx, const void *k, const void *v, const int32_t *slot_mapping,
                        int n, void *kv_pages, int32_t *d_status, void *stream);
@@ -146,8 +147,9 @@ int rq_quantize_append(rq_ctx *ctx, const void *k, const void *v, const int32_t 
  *   block_table device int32 [B][max_pages]
  *   seq_lens    device int32 [B]: tokens of sequence b, all attended (0 gives zeros)
  *   out         device fp16 [B][Hq][head_dim]; head hq reads kv head hq / (Hq / Hkv)
- * out = softmax(sm_scale * q K^T) V over the dequantised cache.  B may be 0.
- * Errors: RQ_ERR_INVALID, RQ_ERR_CAPACITY (B > max_batch, max_pages > max_pages_per_seq),
+ * out = softmax(sm_scale * q K^T) V over the dequantised cache.  B may be 0.  q, kv_pages and
+ * out must be 16-byte aligned (this and every attention entry point below).
+ * Errors: RQ_ERR_INVALID (also a misaligned q, kv_pages or out), RQ_ERR_CAPACITY (B > max_batch, max_pages > max_pages_per_seq),
  * RQ_ERR_CUDA.
  */
 int rq_decode_attention(rq_ctx *ctx, const void *q, const void *kv_pages, const int32_t *block_table,

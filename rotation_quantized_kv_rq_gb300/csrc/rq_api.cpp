@@ -298,12 +298,15 @@ int rq_quantize_append(rq_ctx* ctx, const void* k, const void* v, const int32_t*
   if (!ctx || n < 0) return RQ_ERR_INVALID;
   if (n == 0) return RQ_OK;
   if (!k || !v || !slot_mapping || !kv_pages) return RQ_ERR_INVALID;
-  if ((uintptr_t)k % 16 != 0 || (uintptr_t)v % 16 != 0) return RQ_ERR_INVALID;  // 16-byte vector loads
+  if ((uintptr_t)k % 16 != 0 || (uintptr_t)v % 16 != 0 || (uintptr_t)kv_pages % 16 != 0)
+    return RQ_ERR_INVALID;  // 16-byte vector loads and stores
   DeviceScope scope(ctx->device);
   if (!scope.ok()) return RQ_ERR_CUDA;
   return to_status(rq::launch_append(ctx->g, k, v, slot_mapping, n, (uint8_t*)kv_pages, d_status,
                                      (cudaStream_t)stream));
 }
+
+static bool misaligned16(const void* p) { return (uintptr_t)p % 16 != 0; }
 
 static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tree_mask, const void* kv_pages,
                           const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B, void* out,
@@ -311,6 +314,7 @@ static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tre
   if (!ctx || B < 0 || T < 1 || max_pages < 1) return RQ_ERR_INVALID;
   if (B == 0) return RQ_OK;
   if (!q || !kv_pages || !block_table || !seq_lens || !out) return RQ_ERR_INVALID;
+  if (misaligned16(q) || misaligned16(kv_pages) || misaligned16(out)) return RQ_ERR_INVALID;  // bulk copies, vector I/O
   if (B > ctx->cfg.max_batch || T > ctx->cfg.max_query_tokens || max_pages > ctx->cfg.max_pages_per_seq)
     return RQ_ERR_CAPACITY;
   DeviceScope scope(ctx->device);
@@ -355,6 +359,7 @@ int rq_extend_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages,
   if (!ctx || B < 0 || T < 1 || max_pages < 1) return RQ_ERR_INVALID;
   if (B == 0) return RQ_OK;
   if (!q || !kv_pages || !block_table || !seq_lens || !out) return RQ_ERR_INVALID;
+  if (misaligned16(q) || misaligned16(kv_pages) || misaligned16(out)) return RQ_ERR_INVALID;  // vector loads, stores
   if (ctx->g.mode == RQ_DENSE) return RQ_ERR_UNSUPPORTED;
   if (B > ctx->cfg.max_batch || max_pages > ctx->cfg.max_pages_per_seq) return RQ_ERR_CAPACITY;
   if ((long long)T * ctx->g.group > INT32_MAX / 2) return RQ_ERR_CAPACITY;

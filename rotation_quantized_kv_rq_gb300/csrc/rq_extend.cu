@@ -8,10 +8,12 @@
 //
 // Design (sm_103a): a CTA of 4 warps takes 64 query rows of one (sequence, kv head) -- rows
 // r = j * group + k -- and walks the cache in 32-token tiles up to the last position its rows
-// can see.  Each tile's K and V codes are dequantized once into fp16 shared memory (centroid
-// values; the norms scale the scores and the probabilities), and shared by all 64 rows: every
-// warp computes S = Q~ K~^T for its 16 rows and O~ += P' V~ with mma.sync m16n8k16, reading
-// K~ and V~ with ldmatrix (V~ transposed).  Online softmax in base 2 as in the split-K kernel.
+// can see.  Each thread owns the K and V 32-dim code groups of one (token, group) pair of a
+// tile: it loads the next tile's code words and norms into registers while the current tile's
+// MMAs run, then dequantizes them into fp16 shared memory (centroid values; the norms scale the
+// scores and the probabilities), shared by all 64 rows: every warp computes S = Q~ K~^T for its
+// 16 rows and O~ += P' V~ with mma.sync m16n8k16, reading K~ and V~ with ldmatrix (V~
+// transposed).  Online softmax in base 2 as in the split-K kernel.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -66,45 +68,73 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// The 8 codes of dims 8c..8c+7 of token `off` of a chunk's K (kind 0) or V (kind 1) section,
-// in the storage contract of include/rq.h.  code[e] belongs to dim 8c + e.
+// One (token, 32-dim group) of a K or V vector as stored (include/rq.h): the code words and the
+// token's fp16 norm, loaded from global memory ahead of use.
+struct GroupRaw {
+  uint32_t w[4];  // 4-bit: 4 words (8 codes each); 2-bit: 2 words (16 each); 3-bit: W0, W1, W2
+  uint32_t norm;  // fp16 bits (group 0 only), 0 past the sequence
+};
+
+// Loads group g of token pos of kind (0 K, 1 V) of the (sequence, kv head) whose page table row
+// is bt (npages valid entries); zeros past len.  Page ids outside the pool read page 0 and set
+// RQ_STATUS_BAD_PAGE.
 template <int BITS>
-__device__ __forceinline__ void chunk_codes(int (&code)[8], const uint8_t* chunk, int P, int kind, int off, int c) {
+__device__ __forceinline__ void load_group(GroupRaw& r, const Geometry& g, const AttnArgs& a, const int32_t* bt,
+                                           int h, int pos, int len, int kind, int grp) {
   constexpr int vb = 16 * BITS;
+  r.w[0] = r.w[1] = r.w[2] = r.w[3] = 0u;
+  r.norm = 0u;
+  if (pos >= len) return;
+  const int P = g.page_size;
+  int page = __ldg(bt + pos / P);
+  if (page < 0 || page >= g.num_pages) {
+    if (a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
+    page = 0;
+  }
+  const int off = pos % P;
+  const uint8_t* chunk = a.pages + ((size_t)page * g.num_kv_heads + h) * g.page_bytes;
   const uint8_t* sec = chunk + (size_t)kind * P * vb;
   if constexpr (BITS == 4) {
-    uint32_t w;
     if (kind == 0) {
-      w = *reinterpret_cast<const uint32_t*>(sec + off * vb + 4 * c);
-    } else {  // pair rows: unit c/2 of token 2p + h at 16 (c/2 ^ 2p mod 8) + 8h; half c&1 of it
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(sec + off * vb + 16 * grp));
+      r.w[0] = v.x, r.w[1] = v.y, r.w[2] = v.z, r.w[3] = v.w;
+    } else {  // pair rows: unit u of token 2p + h at 16 (u ^ 2p mod 8) + 8h, units 2 grp, 2 grp + 1
       const int p = off >> 1;
-      w = *reinterpret_cast<const uint32_t*>(sec + p * 128 + 16 * ((c >> 1) ^ ((2 * p) & 7)) + 8 * (off & 1) + 4 * (c & 1));
+      const uint8_t* row = sec + p * 128 + 8 * (off & 1);
+      const uint2 u0 = __ldg(reinterpret_cast<const uint2*>(row + 16 * ((2 * grp) ^ ((2 * p) & 7))));
+      const uint2 u1 = __ldg(reinterpret_cast<const uint2*>(row + 16 * ((2 * grp + 1) ^ ((2 * p) & 7))));
+      r.w[0] = u0.x, r.w[1] = u0.y, r.w[2] = u1.x, r.w[3] = u1.y;
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) code[e] = (w >> (4 * e)) & 15;
   } else if constexpr (BITS == 2) {
-    uint32_t w;
     if (kind == 0) {
-      w = *reinterpret_cast<const uint16_t*>(sec + off * vb + 2 * c);
-    } else {  // pair rows: unit c/2 of token 2p + h at 8 (c/2 ^ 4 (p/2 mod 2)) + 4h; half c&1
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(sec + off * vb + 8 * grp));
+      r.w[0] = v.x, r.w[1] = v.y;
+    } else {  // pair rows: unit u of token 2p + h at 8 (u ^ 4 (p/2 mod 2)) + 4h
       const int p = off >> 1;
-      w = *reinterpret_cast<const uint16_t*>(sec + p * 64 + 8 * ((c >> 1) ^ (4 * ((p >> 1) & 1))) + 4 * (off & 1) + 2 * (c & 1));
+      const uint8_t* row = sec + p * 64 + 4 * (off & 1);
+      r.w[0] = __ldg(reinterpret_cast<const uint32_t*>(row + 8 * ((2 * grp) ^ (4 * ((p >> 1) & 1)))));
+      r.w[1] = __ldg(reinterpret_cast<const uint32_t*>(row + 8 * ((2 * grp + 1) ^ (4 * ((p >> 1) & 1)))));
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) code[e] = (w >> (2 * e)) & 3;
-  } else {
-    // 32-dim group w8 = c / 4 at 12 w8: low bits of dims 8m..8m+7 (m = c % 4) at byte 2m,
-    // high bit of dim i = 16h + 4k + r at bit 8k + 2h + {4,5,0,1}[r] of the word at byte 8
-    const uint8_t* grp = sec + off * vb + 12 * (c >> 2);
-    const int m = c & 3, hh = m >> 1;
-    const uint32_t lo = *reinterpret_cast<const uint16_t*>(grp + 2 * m);
-    const uint32_t w2 = *reinterpret_cast<const uint32_t*>(grp + 8);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int k = 2 * (m & 1) + (e >> 2), r = e & 3;
-      const int bit = 8 * k + 2 * hh + (r < 2 ? 4 + r : r - 2);
-      code[e] = (int)((lo >> (2 * e)) & 3) | (int)(((w2 >> bit) & 1) << 2);
-    }
+  } else {  // 12 bytes of group grp: W0, W1, W2
+    const uint32_t* gw = reinterpret_cast<const uint32_t*>(sec + off * vb + 12 * grp);
+    r.w[0] = __ldg(gw), r.w[1] = __ldg(gw + 1), r.w[2] = __ldg(gw + 2);
+  }
+  if (grp == 0)
+    r.norm = __ldg(reinterpret_cast<const uint16_t*>(chunk + (size_t)2 * P * vb + kind * 2 * P + 2 * off));
+}
+
+// The code of dim i (0..31) of a loaded group.
+template <int BITS>
+__device__ __forceinline__ int group_code(const GroupRaw& r, int i) {
+  if constexpr (BITS == 4) {
+    return (int)((r.w[i >> 3] >> (4 * (i & 7))) & 15u);
+  } else if constexpr (BITS == 2) {
+    return (int)((r.w[i >> 4] >> (2 * (i & 15))) & 3u);
+  } else {  // low bits: W0 (dims 0-15) / W1 (16-31); high bit of i = 16h + 4k + r at 8k + 2h + {4,5,0,1}[r]
+    const int lo = (int)((r.w[i >> 4] >> (2 * (i & 15))) & 3u);
+    const int hh = i >> 4, k = (i >> 2) & 3, rr = i & 3;
+    const int bit = 8 * k + 2 * hh + (rr < 2 ? 4 + rr : rr - 2);
+    return lo | (int)(((r.w[2] >> bit) & 1u) << 2);
   }
 }
 
@@ -179,41 +209,38 @@ extend_kernel(const Geometry g, const AttnArgs a) {
   float o[16][4];
 #pragma unroll
   for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  const size_t head_off = (size_t)h * g.page_bytes;
+  // thread t owns (token t / 4, 32-dim group t % 4) of every tile, for K and for V
+  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
+  const int my_tok = threadIdx.x >> 2, my_grp = threadIdx.x & 3;
+  GroupRaw cur[2], nxt[2];
+  load_group<BITS>(cur[0], g, a, bt, h, my_tok, len, 0, my_grp);
+  load_group<BITS>(cur[1], g, a, bt, h, my_tok, len, 1, my_grp);
 
   for (int t0 = 0; t0 < kv_end; t0 += kXTok) {
-    __syncthreads();  // the previous tile is consumed
-    // ---- dequantize the tile: (token, 8-dim chunk) per step, K then V ----
-    for (int i = threadIdx.x; i < 2 * kXTok * 16; i += kXThreads) {
-      const int kind = i / (kXTok * 16), tok = (i / 16) % kXTok, c = i % 16;
-      const int pos = t0 + tok;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      float nrm = 0.f;
-      if (pos < len) {
-        int page = __ldg(a.block_table + (size_t)b * a.max_pages + pos / P);
-        if (page < 0 || page >= g.num_pages) {
-          if (a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
-          page = 0;
-        }
-        const uint8_t* chunk = a.pages + (size_t)page * g.num_kv_heads * g.page_bytes + head_off;
-        int code[8];
-        chunk_codes<BITS>(code, chunk, P, kind, pos % P, c);
+    __syncthreads();  // the previous tile's K~, V~ are consumed
+    // ---- dequantize this thread's two groups into the fp16 tiles ----
+#pragma unroll
+    for (int kind = 0; kind < 2; ++kind) {
+      uint8_t* tile = smem + (kind ? kXSmemV : kXSmemK);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // 8 dims = one 16-byte chunk of the row
         uint32_t wv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const __half lo = cb16[code[2 * e]], hi = cb16[code[2 * e + 1]];
+          const __half lo = cb16[group_code<BITS>(cur[kind], 8 * q + 2 * e)];
+          const __half hi = cb16[group_code<BITS>(cur[kind], 8 * q + 2 * e + 1)];
           wv[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
         }
-        val = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        if (c == 0) {
-          const uint16_t nb = *reinterpret_cast<const uint16_t*>(chunk + (size_t)2 * P * 16 * BITS + kind * 2 * P + 2 * (pos % P));
-          nrm = __half2float(__ushort_as_half(nb));
-        }
+        *reinterpret_cast<uint4*>(tile + xswz(my_tok, 4 * my_grp + q)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
       }
-      *reinterpret_cast<uint4*>(smem + (kind ? kXSmemV : kXSmemK) + xswz(tok, c)) = val;
-      if (c == 0) (kind ? nv : nk)[tok] = nrm;
+      if (my_grp == 0) (kind ? nv : nk)[my_tok] = __half2float(__ushort_as_half((unsigned short)cur[kind].norm));
     }
     __syncthreads();
+    // ---- the next tile's groups are in flight while this one is multiplied ----
+    if (t0 + kXTok < kv_end) {
+      load_group<BITS>(nxt[0], g, a, bt, h, t0 + kXTok + my_tok, len, 0, my_grp);
+      load_group<BITS>(nxt[1], g, a, bt, h, t0 + kXTok + my_tok, len, 1, my_grp);
+    }
 
     // ---- S = q~ K~^T for the warp's 16 rows x 32 tokens ----
     float s[4][4];
@@ -284,6 +311,8 @@ extend_kernel(const Geometry g, const AttnArgs a) {
         mma16816(o[nd + 1], pa[kk], vb[2], vb[3]);
       }
     }
+    cur[0] = nxt[0];
+    cur[1] = nxt[1];
   }
 
   // ---- normalise, stage, rotate back, store ----

@@ -73,6 +73,8 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   if (B == 0) return RQ_OK;
   if (!d_rot_k || !d_rot_v || !d_centroids || !q || !kv_pages || !block_table || !seq_lens || !out)
     return RQ_ERR_INVALID;
+  if ((uintptr_t)q % 16 != 0 || (uintptr_t)kv_pages % 16 != 0 || (uintptr_t)out % 16 != 0)
+    return RQ_ERR_INVALID;  // bulk copies and vector I/O
 
   const int hkv = cfg->num_kv_heads, group = cfg->num_q_heads / hkv;
   const long long units = (long long)B * hkv * ((group + 7) / 8);

@@ -103,3 +103,16 @@ def test_binding_checks_rotation_table_size():
     with pytest.raises(rq.RQError) as e:
         rq.rq_create(rq.RQ_PLANAR, 4, 32, 8, 16, 64, dense, dense, max_batch=1)
     assert e.value.code == rq.RQ_ERR_INVALID
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host-side check only; fake pointers")
+@pytest.mark.parametrize("which", ["q", "kv_pages", "out"])
+def test_noalloc_rejects_misaligned_pointers_before_cuda(which):
+    """The bulk copies and vector loads of the decode kernel need 16-byte aligned q, kv_pages
+    and out; a misaligned one is refused on the host, before any CUDA call."""
+    cfg, keep = _cfg()
+    ptr = {"q": 0x10000, "kv_pages": 0x20000, "out": 0x30000}
+    ptr[which] += 8
+    rc = rq.lib().rq_decode_attention_noalloc(ctypes.byref(cfg), 0x40000, 0x40000, 0x40000, ptr["q"],
+                                               ptr["kv_pages"], 0x50000, 1, 0x60000, 1, ptr["out"], None, None)
+    assert rc == rq.RQ_ERR_INVALID
