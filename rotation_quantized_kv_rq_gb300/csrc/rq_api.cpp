@@ -95,6 +95,8 @@ int check_geometry(const rq_config* c) {
   if (c->bits < 2 || c->bits > 4) return RQ_ERR_UNSUPPORTED;
   if (c->page_size % 16 != 0 || c->page_size > 256) return RQ_ERR_UNSUPPORTED;
   if ((long long)c->num_pages * c->page_size > INT32_MAX) return RQ_ERR_UNSUPPORTED;
+  // one page's chunks of all kv heads stay below 2^31 bytes (32-bit page strides in the kernels)
+  if ((long long)c->num_kv_heads * c->page_size * (2 * 16 * c->bits + 4) > INT32_MAX) return RQ_ERR_UNSUPPORTED;
   if (c->max_batch > rq::kMaxBatch) return RQ_ERR_UNSUPPORTED;
   if (!(c->sm_scale >= 0.0f) || std::isinf(c->sm_scale)) return RQ_ERR_INVALID;
   return RQ_OK;

@@ -766,7 +766,6 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     uint32_t qf[8][2];
     const int row = it.nt * 8 + gq;  // query row of the kv head: draft j = row / group, head row % group
     int last_pos[2];                  // last position wholly visible to query columns 2tq, 2tq+1
-    uint64_t draft_mask[2];           // tree verify: the columns' draft visibility bits
 
     float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
     float l_run[2] = {0.f, 0.f};
@@ -797,24 +796,30 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     // A pair whose second tile lies past the chunk reads a stale slot for it: its positions,
     // all past pos_lim, are masked like positions past the sequence.
     const int pos_lim = tile1 * 16 - 1;
-    const size_t head_off = (size_t)it.h * g.page_bytes;
     const int n_w = (warp < n_pairs && !broken) ? (n_pairs - 1 - warp) / kWarps + 1 : 0;
-    // Lane 0 stages the warp's k-th pair into stage k % 2 (slots 2(k%2), 2(k%2)+1): per tile one
-    // bulk copy when a page is one tile, else K codes, V codes and the two norm runs.
+    // Lanes 0 and 1 stage tile `lane` of the warp's k-th pair into stage k % 2 (slots 2(k%2),
+    // 2(k%2)+1): one bulk copy when a page is one tile, else K codes, V codes and the two norm
+    // runs.  Lane 0 announces the stage's bytes first.
     auto issue = [&](int k) {
       const int st = k % kStages;
       const int tA = tile0 + 2 * (warp + k * kWarps);
       const int nt_pair = tA + 1 < tile1 ? 2 : 1;
       const uint32_t mb = mbar_addr + 8 * st;
-      mbar_expect_tx(mb, nt_pair * R::SB);
-      for (int h = 0; h < nt_pair; ++h) {
-        const int tile = tA + h;
-        const int pi = tile / tiles_per_page - p0, off = (tile % tiles_per_page) * 16;
-        const uint8_t* chunk = a.pages + (size_t)page_ids[pi] * g.num_kv_heads * g.page_bytes + head_off;
-        const uint32_t dst = st ? (h ? slot3 : slot2) : (h ? slot1 : slot0);
-        if (P == 16) {
-          bulk_g2s(dst, chunk, R::SB, mb);
+      if (lane == 0) mbar_expect_tx(mb, nt_pair * R::SB);
+      __syncwarp(0x3u);
+      if (lane < nt_pair) {
+        const int tile = tA + lane;
+        const uint32_t dst = st ? (lane ? slot3 : slot2) : (lane ? slot1 : slot0);
+        // chunk (page, kv head) at page * Hkv * page_bytes + h * page_bytes: both products stay
+        // below 2^31 per page (checked at creation), so a 32 x 32 -> 64-bit multiply-add forms it
+        const uint32_t page_stride = (uint32_t)(g.num_kv_heads * g.page_bytes);
+        const uint32_t head_off = (uint32_t)(it.h * g.page_bytes);
+        if (P == 16) {  // tile t is page t
+          const uint32_t page = (uint32_t)page_ids[tile - p0];
+          bulk_g2s(dst, a.pages + ((uint64_t)page * page_stride + head_off), R::SB, mb);
         } else {
+          const int pi = tile / tiles_per_page - p0, off = (tile % tiles_per_page) * 16;
+          const uint8_t* chunk = a.pages + ((uint64_t)(uint32_t)page_ids[pi] * page_stride + head_off);
           bulk_g2s(dst, chunk + (size_t)off * R::VB, 16 * R::VB, mb);
           bulk_g2s(dst + 16 * R::VB, chunk + (size_t)(P + off) * R::VB, 16 * R::VB, mb);
           bulk_g2s(dst + 32 * R::VB, chunk + (size_t)2 * P * R::VB + 2 * off, 32, mb);
@@ -822,7 +827,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         }
       }
     };
-    if (lane == 0 && n_w > 0) {
+    if (lane < 2 && n_w > 0) {
       fence_proxy_async();
       for (int k = 0; k < min(kStages, n_w); ++k) issue(k);
     }
@@ -844,7 +849,6 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         // chain: row j sees positions <= len - T + j; tree: the prefix for sure (the drafts
         // by their mask bit), so only the prefix counts as wholly visible
         last_pos[c] = a.tree_mask ? len - a.T - 1 : len - a.T + j;
-        draft_mask[c] = a.tree_mask ? a.tree_mask[(size_t)it.b * a.T + j] : 0ull;
       }
     }
     int consumed = 0;
@@ -888,6 +892,14 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       const bool interior = __all_sync(0xffffffffu, pos0 + 31 <= min(min(last_pos[0], last_pos[1]), pos_lim));
       if (!interior) {
         const int draft0 = last_pos[0] + 1;  // tree: the first draft follows the prefix
+        uint64_t draft_mask[2] = {0ull, 0ull};  // tree: the columns' draft visibility bits (re-read here,
+        if (a.tree_mask) {                      // not held in registers through the loop)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int rc = it.nt * 8 + 2 * tq + c;
+            draft_mask[c] = a.tree_mask[(size_t)it.b * a.T + (rc < a.rows ? rc / g.group : a.T - 1)];
+          }
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int pos = pos0 + 16 * (e >> 2) + rho<BITS>(gq) + 8 * ((e >> 1) & 1);
@@ -951,7 +963,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       load_stage<BITS>(rvA, stA, gq, tq);
       load_stage<BITS>(rvB, stB, gq, tq);
       __syncwarp();
-      if (k + kStages < n_w && lane == 0) {  // refill this stage while the pair is accumulated
+      if (k + kStages < n_w && lane < 2) {  // refill this stage while the pair is accumulated
         fence_proxy_async();
         issue(k + kStages);
       }

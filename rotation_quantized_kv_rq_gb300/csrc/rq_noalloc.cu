@@ -68,7 +68,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
     return RQ_ERR_INVALID;
   if (cfg->mode == RQ_DENSE) return RQ_ERR_UNSUPPORTED;  // its query rotation needs a workspace
   if (cfg->head_dim != rq::kHeadDim || cfg->bits < 2 || cfg->bits > 4 || cfg->page_size % 16 != 0 ||
-      cfg->page_size > 256)
+      cfg->page_size > 256 || (long long)cfg->num_kv_heads * cfg->page_size * (2 * 16 * cfg->bits + 4) > INT32_MAX)
     return RQ_ERR_UNSUPPORTED;
   if (B == 0) return RQ_OK;
   if (!d_rot_k || !d_rot_v || !d_centroids || !q || !kv_pages || !block_table || !seq_lens || !out)
