@@ -3,9 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg1] [--impl ours|reference]
 
 A step is one pass of the whole hot path over one batch: the quantize-append of the step's
-new tokens, then split-K decode (or chain-verify) attention over the packed cache and the
-log-sum-exp combine.  A decode step that appends one token per sequence (cfg1) runs as one
-rq_decode_step call: the append is folded into the split-K kernel.  Inputs are synthetic and seeded (rotation_quantized_kv_rq_gb300.synth);
+new tokens, then split-K decode (or chain-verify) attention over the packed cache with its
+log-sum-exp combine (done inside the split-K kernel for planar / iso rotations, by a second
+kernel that also applies R_v^T for a dense one).  A decode step that appends one token per
+sequence (cfg1) runs as one rq_decode_step call: the append is folded into the split-K kernel.  Inputs are synthetic and seeded (rotation_quantized_kv_rq_gb300.synth);
 the packed cache is built before timing and stays resident in HBM.
 
 Default workload cfg1: rq3_planar, 16 sequences x 8192 context, 32 q / 8 kv heads, page 16,
@@ -160,12 +161,12 @@ class Bench:
 
     def launches_per_step(self):
         if self.fused_step:
-            return 2  # split-K with the append folded in, combine
+            return 1  # split-K with the append folded in and the units finished in-kernel
         if self.extend:
             return 2  # append, extend attention
         n = 1 if self.k_new is not None else 0
-        # split-K + combine, and for a dense rotation the query pre-rotation
-        return n if self.prefill_only else n + 2 + (self.spec.mode == synth.DENSE)
+        # split-K; a dense rotation adds the query pre-rotation and the combine (R_v^T)
+        return n if self.prefill_only else n + 1 + 2 * (self.spec.mode == synth.DENSE)
 
     def tokens_per_step(self):
         if self.prefill_only:

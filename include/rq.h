@@ -232,14 +232,16 @@ int rq_tree_verify_attention(rq_ctx *ctx, const void *q, int T, const uint64_t *
  *   d_centroids        device float32 [2^bits], ascending (e.g. from rq_lloyd_max_codebook)
  *   other arguments    as rq_decode_attention, on the CURRENT device
  * The result equals rq_decode_attention's on the same inputs.
- * Scratch: the split-K partials and work counters live in one file-scope 16 MiB device array
- * that every GPU which loads the library holds until the process exits.  A call whose
- * B * num_kv_heads * ceil(group / 8) exceeds 3,971 (not even one context split per sequence
- * fits) returns RQ_ERR_CAPACITY; so does a block table wider than 65,536 pages.
+ * Scratch: the split-K partials, the per-unit fragment bounds and round counters live in one
+ * file-scope 16 MiB device array that every GPU which loads the library holds until the process
+ * exits.  With U = B * num_kv_heads * ceil(group / 8) work units, a call with U > 8,192, or with
+ * U + (the device's SM count) > 3,948 partial slots, returns RQ_ERR_CAPACITY; so do B > 8,000
+ * and a block table whose max_pages * page_size exceeds INT32_MAX.
  * The first call on a device sets up that device (resolves the array's address, reads the SM
  * count, sets the kernel's shared-memory limit); make that first call before any stream
- * capture.  Every call shares the one array and re-zeroes its counters on `stream`, so calls
- * that overlap on the GPU (different streams, or different host threads) race: serialise them.
+ * capture.  The round counters start at zero (the array is zero-initialised when the library
+ * loads) and every call leaves them at zero.  Every call shares the one array, so calls that
+ * overlap on the GPU (different streams, or different host threads) race: serialise them.
  */
 int rq_decode_attention_noalloc(const rq_config *cfg, const float *d_rot_k, const float *d_rot_v,
                                 const float *d_centroids, const void *q, const void *kv_pages,

@@ -22,7 +22,7 @@ struct rq_ctx {
   float* d_dense32;       // dense: fp32 R_k and R_v, row-major, for the append's exact recompute
   float* d_qrot;          // dense: fp32 R_k q of one attention call [max_batch][max_T][Hq][128]
   float* d_ws;            // fragment partials of the stream-K split
-  int* d_frag;            // first / last CTA of each unit's fragments
+  int* d_frag;            // first / last CTA of each unit's fragments [2 U], then rounds done per unit [U]
   size_t ws_floats;
   size_t max_units;       // max_batch * Hkv * ceil(max_query_tokens * group / 8)
   int max_n_tiles;        // ceil(max_query_tokens * group / 8)
@@ -95,6 +95,7 @@ int check_geometry(const rq_config* c) {
   if (c->bits < 2 || c->bits > 4) return RQ_ERR_UNSUPPORTED;
   if (c->page_size % 16 != 0 || c->page_size > 256) return RQ_ERR_UNSUPPORTED;
   if ((long long)c->num_pages * c->page_size > INT32_MAX) return RQ_ERR_UNSUPPORTED;
+  if ((long long)c->max_pages_per_seq * c->page_size > INT32_MAX) return RQ_ERR_UNSUPPORTED;  // positions are int
   // one page's chunks of all kv heads stay below 2^31 bytes (32-bit page strides in the kernels)
   if ((long long)c->num_kv_heads * c->page_size * (2 * 16 * c->bits + 4) > INT32_MAX) return RQ_ERR_UNSUPPORTED;
   if (c->max_batch > rq::kMaxBatch) return RQ_ERR_UNSUPPORTED;
@@ -179,7 +180,9 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
 
   cudaError_t e = cudaMalloc(&ctx->d_tables, table_floats * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&ctx->d_ws, ctx->ws_floats * sizeof(float));
-  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_frag, 2 * ctx->max_units * sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_frag, 3 * ctx->max_units * sizeof(int));
+  // the per-unit round counters start at zero; every launch leaves them at zero
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_frag, 0, 3 * ctx->max_units * sizeof(int));
   const size_t dense16_halves = dense ? 2 * rot * 2 : 0;  // [K, V][Hkv][hi, lo][d][d]
   if (e == cudaSuccess && dense) {
     e = cudaMalloc(&ctx->d_dense16, dense16_halves * sizeof(__half));
@@ -340,6 +343,7 @@ static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tre
   a.rows = T * ctx->g.group;
   a.n_tiles_n = (a.rows + 7) / 8;
   a.frag = ctx->d_frag;
+  a.cnt = ctx->d_frag + 2 * ctx->max_units;
   a.grid = ctx->num_sms;  // one CTA per SM, each an equal share of the tiles
   return to_status(rq::launch_attention(ctx->g, a, (cudaStream_t)stream, ctx->prof_start, ctx->prof_end));
 }

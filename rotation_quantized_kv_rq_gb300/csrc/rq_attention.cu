@@ -90,6 +90,10 @@ __host__ __device__ __forceinline__ int unit_rounds(int len) { return ((len + 15
 struct Walk {
   long long x, x_end, cumb;
   int b, len;  // len: sequence b's tokens, clamped to the block table (> 0 while x < x_end)
+  // Units whose last-finished fragment was this CTA's (set by thread 0): at most the first and
+  // the last fragment of a CTA's range are partial units, the ones between are whole.
+  int n_fin;
+  int fin[2];
 };
 
 // The fragment at the walk's position: rounds [r0, r1) of the rb rounds of unit uib of
@@ -501,6 +505,115 @@ __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, ui
 }
 
 // ---------------------------------------------------------------------------------------
+// Log-sum-exp merge of one query row's split partials: o~ = sum_s 2^(m_s - M) O_s / L with
+// M = max_s m_s and L = sum_s 2^(m_s - M) l_s, for the lane's dims 4 lane .. 4 lane + 3.  The
+// lanes take the splits' (m, l) one split each, so M and L are warp reductions rather than
+// chains of dependent loads, and the O sum issues its independent loads eight at a time.
+// Zeros for an empty (or invalid) sequence.  All 32 lanes must call it.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float4 merge_splits(const Geometry& g, const AttnArgs& a, int b, int h, int row, int lane) {
+  const int nt = row >> 3, col = row & 7;
+  int len = a.seq_lens[b];
+  const int cap = a.max_pages * g.page_size;
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (len == 0 || len < a.T) return acc;
+  // the unit's fragments: CTAs first .. last, partials at slots unit + c
+  const int unit = (b * g.num_kv_heads + h) * a.n_tiles_n + nt;
+  // written by other CTAs of this launch (or the previous kernel): read through L2
+  const int first = __ldcg(a.frag + 2 * unit), last = __ldcg(a.frag + 2 * unit + 1);
+  if (first < 0 || last < first || last >= a.grid) return acc;  // a launch that gave up early
+  const int ns = last - first + 1;
+  const size_t stride = (size_t)8 * kPartialStride;  // between consecutive slots
+  const float* base = a.ws + (size_t)(unit + first) * stride + (size_t)col * kPartialStride;
+  // (m, l) of the lane's slots, one load each; running max and rescaled sum, then warp-merged
+  float M = -CUDART_INF_F, L = 0.f;
+  for (int s = lane; s < ns; s += 32) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + s * stride));
+    if (ml.x == -CUDART_INF_F) continue;
+    const float m_new = fmaxf(M, ml.x);
+    L = L * exp2f(M - m_new) + ml.y * exp2f(ml.x - m_new);
+    M = m_new;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float M2 = __shfl_xor_sync(0xffffffffu, M, o), L2 = __shfl_xor_sync(0xffffffffu, L, o);
+    const float m_new = fmaxf(M, M2);
+    if (m_new != -CUDART_INF_F) L = (M == -CUDART_INF_F ? 0.f : L * exp2f(M - m_new)) +
+                                    (M2 == -CUDART_INF_F ? 0.f : L2 * exp2f(M2 - m_new));
+    M = m_new;
+  }
+  if (M == -CUDART_INF_F) return acc;
+#pragma unroll 8
+  for (int s = 0; s < ns; ++s) {
+    const float* ps = base + s * stride;
+    const float w = exp2f(__ldcg(ps) - M);
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(ps + 4 + 4 * lane));
+    acc.x += v.x * w;
+    acc.y += v.y * w;
+    acc.z += v.z * w;
+    acc.w += v.w * w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  return make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
+// out = R_v^T o~ for query row `row` of kv head h of sequence b (planar / iso: block-local),
+// the lane's dims 4 lane .. 4 lane + 3, as fp16.  All 32 lanes of the warp call it.
+__device__ __forceinline__ void store_row(const Geometry& g, const AttnArgs& a, int b, int h, int row, int lane,
+                                          float4 o) {
+  const float y[4] = {o.x, o.y, o.z, o.w};
+  const float4 p = __ldg(reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim) + lane);
+  float x[4];
+  if (g.mode == RQ_PLANAR) {
+    x[0] = p.x * y[0] + p.y * y[1];
+    x[1] = -p.y * y[0] + p.x * y[1];
+    x[2] = p.z * y[2] + p.w * y[3];
+    x[3] = -p.w * y[2] + p.z * y[3];
+  } else {  // L(q)^T y
+    const float qa = p.x, qb = p.y, qc = p.z, qd = p.w;
+    x[0] = qa * y[0] + qb * y[1] + qc * y[2] + qd * y[3];
+    x[1] = -qb * y[0] + qa * y[1] + qd * y[2] - qc * y[3];
+    x[2] = -qc * y[0] - qd * y[1] + qa * y[2] + qb * y[3];
+    x[3] = -qd * y[0] + qc * y[1] - qb * y[2] + qa * y[3];
+  }
+  const int j = row / g.group, head = h * g.group + row % g.group;
+  __half2* out = reinterpret_cast<__half2*>(reinterpret_cast<__half*>(a.out) +
+                                            (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim + 4 * lane);
+  out[0] = __floats2half2_rn(x[0], x[1]);
+  out[1] = __floats2half2_rn(x[2], x[3]);
+}
+
+// The same for the two dims d0, d0 + 1 (d0 even) of row `row`, held as (y0, y1) by this lane;
+// with a quaternion rotation the block's other two dims are held by lane ^ 1 (d0 ^ 2).  All 32
+// lanes of the warp call it.
+__device__ __forceinline__ void store_pair(const Geometry& g, const AttnArgs& a, int b, int h, int row, int d0,
+                                           float y0, float y1) {
+  const float* rv = g.rot_v + (size_t)h * kHeadDim;
+  const float z0 = __shfl_xor_sync(0xffffffffu, y0, 1), z1 = __shfl_xor_sync(0xffffffffu, y1, 1);
+  float x0, x1;
+  if (g.mode == RQ_PLANAR) {
+    const float2 p = __ldg(reinterpret_cast<const float2*>(rv + d0));
+    x0 = p.x * y0 + p.y * y1;
+    x1 = -p.y * y0 + p.x * y1;
+  } else {
+    const float4 q = __ldg(reinterpret_cast<const float4*>(rv + (d0 & ~3)));
+    const float qa = q.x, qb = q.y, qc = q.z, qd = q.w;
+    if ((d0 & 2) == 0) {  // own dims 0, 1 of the block; the partner's are 2, 3
+      x0 = qa * y0 + qb * y1 + qc * z0 + qd * z1;
+      x1 = -qb * y0 + qa * y1 + qd * z0 - qc * z1;
+    } else {              // own dims 2, 3; the partner's are 0, 1
+      x0 = -qc * z0 - qd * z1 + qa * y0 + qb * y1;
+      x1 = -qd * z0 + qc * z1 - qb * y0 + qa * y1;
+    }
+  }
+  const int j = row / g.group, head = h * g.group + row % g.group;
+  *reinterpret_cast<__half2*>(reinterpret_cast<__half*>(a.out) +
+                              (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim + d0) =
+      __floats2half2_rn(x0, x1);
+}
+
+// ---------------------------------------------------------------------------------------
 // The split-K kernel.
 // ---------------------------------------------------------------------------------------
 // The lane's 32 dims 32tq..32tq+31 of R_k q for query row `row` of kv head h (zeros past the
@@ -746,6 +859,14 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     }
     if (threadIdx.x == 0) *walk = Walk{x0, x1, cum[lo], lo, clamp_len(a, lo, cap)};
     if constexpr (STEP) step_append<BITS>(g, a, cum, x0, x1, lo, cap, upb);
+    if constexpr (!PRE) {  // a sequence without tokens has no fragments: its rows are zeros
+      for (int bb = blockIdx.x; bb < a.B; bb += gridDim.x) {
+        if (clamp_len(a, bb, cap) != 0) continue;
+        const int n16 = a.T * g.num_q_heads * (kHeadDim / 8);
+        uint4* o16 = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(a.out) + (size_t)bb * a.T * g.num_q_heads * kHeadDim);
+        for (int i = threadIdx.x; i < n16; i += kThreads) o16[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     __syncthreads();  // the scratch is slot space from here on
   }
 
@@ -1008,19 +1129,22 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     __syncthreads();
     {
       // Fragment partials of unit u sit at slots u + c for its CTAs c: slots never collide,
-      // because both the units and the CTAs' ranges follow the same order.
+      // because both the units and the CTAs' ranges follow the same order.  A fragment that is
+      // its unit's whole range finishes the unit right here (structured rotations; a dense one
+      // always hands its partial to the combine kernel, which applies R_v^T).
       const int cols = min(8, a.rows - it.nt * 8);
       const int unit = (it.b * g.num_kv_heads + it.h) * a.n_tiles_n + it.nt;
+      const Frag f = frag_at(*walk);
+      const bool whole = !PRE && f.t0 == 0 && f.t1 == f.tb;  // uniform over the CTA
       float* dst = a.ws + (size_t)(unit + blockIdx.x) * 8 * kPartialStride;
-      if (threadIdx.x == 0) {
-        const Frag f = frag_at(*walk);
+      if (threadIdx.x == 0 && !whole) {
         if (f.t0 == 0) a.frag[2 * unit] = blockIdx.x;         // the unit's first CTA
         if (f.t1 == f.tb) a.frag[2 * unit + 1] = blockIdx.x;  // and its last
       }
       // thread (c, gq', mt') merges dims 16 gq' + 2 mt' and +1 of column c: lane 4 gq' + c / 2
       // of every warp held them, as components (c & 1) and (c & 1) + 2 of its float4 mt'
       const int c = threadIdx.x >> 6, gm = (threadIdx.x >> 3) & 7, mm = threadIdx.x & 7;
-      if (c < cols) {
+      if (c < cols) {  // c is uniform over each warp
         float M = -CUDART_INF_F;
 #pragma unroll 4
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 8 + c) * 2]);
@@ -1036,10 +1160,31 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
             lsum += ml[(w * 8 + c) * 2 + 1] * scale;
           }
         }
-        *reinterpret_cast<float2*>(dst + c * kPartialStride + 4 + 16 * gm + 2 * mm) = make_float2(acc0, acc1);
-        if (gm == 0 && mm == 0) {
-          dst[c * kPartialStride] = M;
-          dst[c * kPartialStride + 1] = lsum;
+        if (whole) {
+          const float inv = (lsum > 0.f && len >= a.T) ? 1.f / lsum : 0.f;
+          store_pair(g, a, it.b, it.h, it.nt * 8 + c, 16 * gm + 2 * mm, acc0 * inv, acc1 * inv);
+        } else {
+          *reinterpret_cast<float2*>(dst + c * kPartialStride + 4 + 16 * gm + 2 * mm) = make_float2(acc0, acc1);
+          if (gm == 0 && mm == 0) {
+            dst[c * kPartialStride] = M;
+            dst[c * kPartialStride + 1] = lsum;
+          }
+        }
+      }
+      if (!PRE && !whole) {
+        // Publish the partial and count the unit's finished rounds: the barrier orders every
+        // thread's partial before thread 0's fence and add.  The CTA whose rounds complete the
+        // unit merges all its partials once its own range is done (no CTA waits for another)
+        // and puts the counter back to zero for the next launch.
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          const int n = f.r1 - f.r0;
+          __threadfence();
+          if (atomicAdd(a.cnt + unit, n) + n >= f.rb) {
+            a.cnt[unit] = 0;
+            if (walk->n_fin < 2) walk->fin[walk->n_fin++] = unit;
+            else if (a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);  // cannot happen (see Walk)
+          }
         }
       }
     }
@@ -1051,88 +1196,21 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     }
     __syncthreads();
   }
-}
 
-// ---------------------------------------------------------------------------------------
-// Log-sum-exp merge of one query row's split partials: o~ = sum_s 2^(m_s - M) O_s / L with
-// M = max_s m_s and L = sum_s 2^(m_s - M) l_s, for the lane's dims 4 lane .. 4 lane + 3.  The
-// lanes take the splits' (m, l) one split each, so M and L are warp reductions rather than
-// chains of dependent loads, and the O sum issues its independent loads eight at a time.
-// Zeros for an empty (or invalid) sequence.  All 32 lanes must call it.
-// ---------------------------------------------------------------------------------------
-__device__ __forceinline__ float4 merge_splits(const Geometry& g, const AttnArgs& a, int b, int h, int row, int lane) {
-  const int nt = row >> 3, col = row & 7;
-  int len = a.seq_lens[b];
-  const int cap = a.max_pages * g.page_size;
-  len = len < 0 ? 0 : (len > cap ? cap : len);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (len == 0 || len < a.T) return acc;
-  // the unit's fragments: CTAs first .. last, partials at slots unit + c
-  const int unit = (b * g.num_kv_heads + h) * a.n_tiles_n + nt;
-  const int first = a.frag[2 * unit], last = a.frag[2 * unit + 1];
-  if (first < 0 || last < first || last >= a.grid) return acc;  // a launch that gave up early
-  const int ns = last - first + 1;
-  const size_t stride = (size_t)8 * kPartialStride;  // between consecutive slots
-  const float* base = a.ws + (size_t)(unit + first) * stride + (size_t)col * kPartialStride;
-  float M = -CUDART_INF_F;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * stride]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (M == -CUDART_INF_F) return acc;
-  float L = 0.f;
-  for (int s = lane; s < ns; s += 32) L += base[s * stride + 1] * exp2f(base[s * stride] - M);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-#pragma unroll 8
-  for (int s = 0; s < ns; ++s) {
-    const float* ps = base + s * stride;
-    const float w = exp2f(ps[0] - M);
-    const float4 v = *reinterpret_cast<const float4*>(ps + 4 + 4 * lane);
-    acc.x += v.x * w;
-    acc.y += v.y * w;
-    acc.z += v.z * w;
-    acc.w += v.w * w;
+  if constexpr (!PRE) {
+    // Finish the units this CTA completed: a warp per query row of the unit.
+    if (threadIdx.x == 0 && walk->n_fin > 0) __threadfence();  // after the adds that saw them done
+    __syncthreads();
+    const int ntn = a.n_tiles_n;
+    for (int k = 0; k < walk->n_fin; ++k) {
+      const int unit = walk->fin[k];
+      const int nt = unit % ntn, h = (unit / ntn) % g.num_kv_heads, b = unit / (ntn * g.num_kv_heads);
+      if (warp < min(8, a.rows - nt * 8)) {
+        const int row = nt * 8 + warp;
+        store_row(g, a, b, h, row, lane, merge_splits(g, a, b, h, row, lane));
+      }
+    }
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  return make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-}
-
-// ---------------------------------------------------------------------------------------
-// Combine: one warp per output row (b, j, query head); lane l owns dims 4l..4l+3.
-//   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  o~ = sum_s O_s 2^(m_s - M) / L,
-//   out = R_v^T o~  (block-local: a Givens pair or a quaternion block per lane).
-// ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
-attn_combine_kernel(const Geometry g, const AttnArgs a) {
-  const int warp_global = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int total = a.B * a.T * g.num_q_heads;
-  if (warp_global >= total) return;
-  const int head = warp_global % g.num_q_heads;
-  const int j = (warp_global / g.num_q_heads) % a.T;
-  const int b = warp_global / (g.num_q_heads * a.T);
-  const int h = head / g.group;
-  const int row = j * g.group + head % g.group;
-  const float4 o = merge_splits(g, a, b, h, row, lane);
-  const float y[4] = {o.x, o.y, o.z, o.w};
-  const float4 p = __ldg(reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim) + lane);
-  float x[4];
-  if (g.mode == RQ_PLANAR) {
-    x[0] = p.x * y[0] + p.y * y[1];
-    x[1] = -p.y * y[0] + p.x * y[1];
-    x[2] = p.z * y[2] + p.w * y[3];
-    x[3] = -p.w * y[2] + p.z * y[3];
-  } else {  // L(q)^T y
-    const float qa = p.x, qb = p.y, qc = p.z, qd = p.w;
-    x[0] = qa * y[0] + qb * y[1] + qc * y[2] + qd * y[3];
-    x[1] = -qb * y[0] + qa * y[1] + qd * y[2] - qc * y[3];
-    x[2] = -qc * y[0] - qd * y[1] + qa * y[2] + qb * y[3];
-    x[3] = -qd * y[0] + qc * y[1] - qb * y[2] + qa * y[3];
-  }
-  __half2* out = reinterpret_cast<__half2*>(reinterpret_cast<__half*>(a.out) +
-                                            (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim + 4 * lane);
-  out[0] = __floats2half2_rn(x[0], x[1]);
-  out[1] = __floats2half2_rn(x[2], x[3]);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1200,7 +1278,7 @@ rotate_q_dense_kernel(const Geometry g, const AttnArgs a) {
     if (r < nr) a.q_rot[dense_row_index(g, h, r0 + r) * kHeadDim + threadIdx.x] = acc[r];
 }
 
-// The log-sum-exp merge of attn_combine_kernel for the CTA's rows, then out = R_v^T o~.
+// The log-sum-exp merge of merge_splits for the CTA's rows, then out = R_v^T o~.
 __global__ void __launch_bounds__(kHeadDim)
 attn_combine_dense_kernel(const Geometry g, const AttnArgs a) {
   __shared__ __align__(16) float os[kDenseRows][kHeadDim];
@@ -1309,12 +1387,8 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t 
     if (e != cudaSuccess) return e;
     if (ev_end) cudaEventRecord(ev_end, stream);
   }
-  if (dense) {
-    attn_combine_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a);
-  } else {
-    const long long rows = (long long)a.B * a.T * g.num_q_heads;
-    attn_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(g, a);
-  }
+  // planar / iso: the split-K kernel finishes every unit itself
+  if (dense) attn_combine_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a);
   return cudaGetLastError();
 }
 

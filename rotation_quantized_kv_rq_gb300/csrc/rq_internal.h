@@ -50,6 +50,7 @@ struct AttnArgs {
   int32_t* status;           // nullable
   float* ws;                 // fragment partials: [units + grid][8 rows][kPartialStride] floats
   int* frag;                 // [units][2]: first and last CTA holding a fragment of each unit
+  int* cnt;                  // [units]: rounds finished per unit; zero between launches
   int grid;                  // CTAs of the split-K launch (the stream-K partition's parts)
   int rows;                  // T * group: query rows per kv head
   int n_tiles_n;             // ceil(rows / 8)

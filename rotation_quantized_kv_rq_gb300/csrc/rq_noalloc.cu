@@ -1,6 +1,6 @@
 // rq_decode_attention_noalloc: the decode attention of rq_decode_attention for callers that
-// cannot allocate device memory.  Its split-K scratch (the fragment partials and the per-unit
-// fragment bounds) lives in one file-scope __device__ array instead of a context's
+// cannot allocate device memory.  Its split-K scratch (the fragment partials, the per-unit
+// fragment bounds and round counters) lives in one file-scope __device__ array instead of a context's
 // cudaMalloc'd workspace, and the tables come from the caller as device pointers, so the call
 // allocates nothing.  The kernels are the library's own attention kernels.
 #include <cuda_runtime.h>
@@ -13,13 +13,15 @@
 
 namespace {
 
-// Scratch: fragment bounds (2 ints per unit, kFragBytes), then fragment partials of 8 query
-// rows x kPartialStride floats.  A call with U units and G CTAs uses 2U ints and U + G slots.
+// Scratch: fragment bounds (2 ints per unit), round counters (1 int per unit), then fragment
+// partials of 8 query rows x kPartialStride floats.  A call with U units and G CTAs uses
+// 3U ints and U + G slots.
 constexpr size_t kScratchBytes = (size_t)16 << 20;
-constexpr size_t kFragBytes = (size_t)64 << 10;
-constexpr size_t kMaxUnits = kFragBytes / (2 * sizeof(int));           // 8,192
+constexpr size_t kMaxUnits = 8192;
+constexpr size_t kFragBytes = kMaxUnits * 2 * sizeof(int);              // 64 KiB
+constexpr size_t kCntBytes = kMaxUnits * sizeof(int);                   // 32 KiB
 constexpr size_t kSlotBytes = 8 * rq::kPartialStride * sizeof(float);   // one fragment
-constexpr size_t kScratchSlots = (kScratchBytes - kFragBytes) / kSlotBytes;  // 3,956
+constexpr size_t kScratchSlots = (kScratchBytes - kFragBytes - kCntBytes) / kSlotBytes;  // 3,948
 constexpr int kMaxDevices = 64;
 
 // Every GPU that loads the library holds this array until the process exits.  Host code must
@@ -79,6 +81,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   const int hkv = cfg->num_kv_heads, group = cfg->num_q_heads / hkv;
   const long long units = (long long)B * hkv * ((group + 7) / 8);
   if (B > rq::kMaxBatch || units > (long long)kMaxUnits) return RQ_ERR_CAPACITY;
+  if ((long long)max_pages * cfg->page_size > INT32_MAX) return RQ_ERR_CAPACITY;  // positions are int
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RQ_ERR_CUDA;
@@ -122,9 +125,11 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   a.n_tiles_n = (group + 7) / 8;
 
   a.frag = reinterpret_cast<int*>(slot->scratch);
-  a.ws = reinterpret_cast<float*>(slot->scratch + kFragBytes);
+  a.cnt = reinterpret_cast<int*>(slot->scratch + kFragBytes);
+  a.ws = reinterpret_cast<float*>(slot->scratch + kFragBytes + kCntBytes);
   a.grid = slot->num_sms;
-  // Nothing in the array needs a starting value: every launch writes the bounds of every unit
-  // with tokens and the partials they point at before its combine reads them.
+  // Only the round counters need a starting value: zero, as the array is zero-initialised when
+  // the module loads, and every launch that runs to its end leaves them at zero again.  The
+  // bounds and partials are written by each launch before they are read.
   return rq::launch_attention(g, a, (cudaStream_t)stream) == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }
