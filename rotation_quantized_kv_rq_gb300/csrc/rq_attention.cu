@@ -225,8 +225,11 @@ template <int BITS>
 __device__ void build_lut(uint32_t* lut, const float* centroids, float* cb) {
   if (threadIdx.x < (1 << BITS)) cb[threadIdx.x] = centroids[threadIdx.x];
   __syncthreads();
-  for (int i = threadIdx.x; i < 256 * 64; i += kThreads) {
-    const int e = i >> 6, second = (i >> 5) & 1;
+  // Each row holds 2 distinct words, each 32 times: 16-byte stores of 4 copies, a warp writing
+  // 512 consecutive bytes (two rows) per store, free of bank conflicts.
+  uint4* lut4 = reinterpret_cast<uint4*>(lut);
+  for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
+    const int e = i >> 4, second = (i >> 3) & 1;
     int ca, cbx;
     if (BITS == 4) {
       ca = e & 15;
@@ -241,7 +244,8 @@ __device__ void build_lut(uint32_t* lut, const float* centroids, float* cb) {
       ca = ((e >> 4) & 3) | (e & 1) << 2;
       cbx = ((e >> 6) & 3) | ((e >> 1) & 1) << 2;
     }
-    lut[i] = pack_half2(cb[ca], cb[cbx]);
+    const uint32_t w = pack_half2(cb[ca], cb[cbx]);
+    lut4[i] = make_uint4(w, w, w, w);
   }
 }
 
