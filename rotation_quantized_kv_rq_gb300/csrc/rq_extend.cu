@@ -6,14 +6,19 @@
 // hundreds or thousands, where the split-K kernel (which re-reads the cache for every 8 query
 // rows) stops paying.
 //
-// Design (sm_103a): a CTA of 4 warps takes 64 query rows of one (sequence, kv head) -- rows
-// r = j * group + k -- and walks the cache in 32-token tiles up to the last position its rows
-// can see.  Each thread owns the K and V 32-dim code groups of one (token, group) pair of a
-// tile: it loads the next tile's code words and norms into registers while the current tile's
-// MMAs run, then dequantizes them into fp16 shared memory (centroid values; the norms scale the
-// scores and the probabilities), shared by all 64 rows: every warp computes S = Q~ K~^T for its
-// 16 rows and O~ += P' V~ with mma.sync m16n8k16, reading K~ and V~ with ldmatrix (V~
-// transposed).  Online softmax in base 2 as in the split-K kernel.
+// Design (sm_103a, 5th-generation tensor cores): a CTA of 4 warps takes 128 query rows of one
+// (sequence, kv head) -- rows r = j * group + k, thread i owning row i -- and walks the cache
+// in 64-token tiles up to the last position its rows can see.  Per tile the threads
+// dequantize K~ (token-major) and V~^T (dim-major) into shared memory as fp16 centroid values
+// in the K-major 128-byte-swizzled operand layout; one thread issues S = Q~ K~^T
+// (tcgen05.mma, M 128 x N 64 x K 128) into tensor memory; every thread reads its row of S
+// (tcgen05.ld), scales it by the key norms, masks it and runs the online softmax in base 2
+// with no cross-thread reduction, then writes P' = p * n_v as fp16; one thread issues
+// O~ += P' V~ (M 128 x N 128 x K 64), accumulated in tensor memory.  The next tile's K~ is
+// dequantized while P'V~ runs and its V~ while the next S runs; two CTAs share an SM (tensor
+// memory 2 x 256 columns, shared memory 2 x 83.5 KB) and fill each other's gaps.  Every wait
+// is bounded: a wait that runs out sets RQ_STATUS_TIMEOUT, the CTA stops, waits (bounded)
+// for the MMAs it issued and frees its tensor memory.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -23,41 +28,87 @@
 namespace rq {
 namespace {
 
-constexpr int kXWarps = 4;
-constexpr int kXThreads = 32 * kXWarps;
-constexpr int kXRows = 16 * kXWarps;  // query rows per CTA
-constexpr int kXTok = 32;             // tokens per K/V tile
-constexpr int kXOStride = 132;        // floats per staged output row
-// shared memory: K~ and V~ tiles fp16 [32][128] (16-byte chunks XOR-swizzled by row), the
-// tile's norms, the fp16 centroids, then the query staging (fp16 [64][128]) that the output
-// staging (fp32 [64][132]) later reuses
-constexpr int kXSmemK = 0;
-constexpr int kXSmemV = kXSmemK + kXTok * 256;
-constexpr int kXSmemNk = kXSmemV + kXTok * 256;
-constexpr int kXSmemNv = kXSmemNk + kXTok * 4;
-constexpr int kXSmemCb = kXSmemNv + kXTok * 4;
-constexpr int kXSmemQ = kXSmemCb + 64;
-constexpr int kXSmem = kXSmemQ + kXRows * kXOStride * 4;  // 50,496 bytes
+constexpr int kXThreads = 128;  // thread i owns query row i of the CTA's block
+constexpr int kXRows = 128;     // M of both MMAs
+constexpr int kXTok = 64;       // tokens per K/V tile: N of S, K of P'V~
+// Shared memory, from a 1024-byte-aligned base.  MMA operands are K-major with the 128-byte
+// swizzle: 128-byte rows (64 fp16 of K), 16-byte chunk c of row r stored at chunk c ^ (r % 8),
+// 8-row groups 1024 bytes apart, a second 64-wide K atom after all rows of the first.
+constexpr int kXQ = 0;                    // q~: 128 rows x 128 dims, two atoms of 16 KB
+constexpr int kXK = kXQ + 32768;          // K~: 64 tokens x 128 dims, two atoms of 8 KB
+constexpr int kXV = kXK + 16384;          // V~^T: 128 dims x 64 tokens
+constexpr int kXP = kXV + 16384;          // P': 128 rows x 64 tokens
+constexpr int kXNk = kXP + 16384;         // the tile's K norms, f32 [64]
+constexpr int kXNv = kXNk + 256;          // the tile's V norms, f32 [64]
+constexpr int kXCb = kXNv + 256;          // centroids, fp16 [16]
+constexpr int kXBar = kXCb + 32;          // mbarriers: S done, P'V~ done
+constexpr int kXTmemSlot = kXBar + 16;    // tensor-memory address from tcgen05.alloc
+constexpr int kXSmem = kXTmemSlot + 16 + 1024;  // + alignment slack: 83,520 bytes (> 1/3 of the SM)
+constexpr uint32_t kXTmemCols = 256;      // O~ in columns [0, 128), S in [128, 192)
+constexpr int kXWaitLimit = 1 << 22;      // bounded mbarrier polling (about a second)
 
-__device__ __forceinline__ uint32_t xswz(int row, int chunk) { return (uint32_t)(row * 256 + ((chunk ^ (row & 7)) << 4)); }
+__device__ __forceinline__ uint32_t xswz(int row, int chunk) { return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4)); }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
+// Shared-memory matrix descriptor of a K-major 128-byte-swizzled operand starting at saddr:
+// start address >> 4 (bits 0-13), leading offset 16 B (unused by this layout), stride 1024 B
+// between 8-row groups (bits 32-45), descriptor version 1 (bits 46-47), swizzle mode 2 =
+// 128-byte (bits 61-63).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+// Instruction descriptor, kind::f16: f32 accumulator (bits 4-5 = 1), f16 A and B (bits 7-12 =
+// 0), both K-major (bits 15, 16 = 0), N / 8 at bits 17-22, M / 16 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) { return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24); }
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id, uint32_t accumulate) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(id), "r"(accumulate));
 }
+// The mbarrier completes once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
+  for (int i = 0; i < kXWaitLimit; ++i) {
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(ok)
+                 : "r"(addr), "r"(parity)
+                 : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+// 16 consecutive tensor-memory columns of the warp's 32 lanes (thread = lane), and back.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -66,6 +117,9 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_hh(__half lo, __half hi) {
+  return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
 // One (token, 32-dim group) of a K or V vector as stored (include/rq.h): the code words and the
@@ -139,221 +193,321 @@ __device__ __forceinline__ int group_code(const GroupRaw& r, int i) {
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kXThreads)
+__global__ void __launch_bounds__(kXThreads, 2)
 extend_kernel(const Geometry g, const AttnArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
-  float* nk = reinterpret_cast<float*>(smem + kXSmemNk);
-  float* nv = reinterpret_cast<float*>(smem + kXSmemNv);
-  __half* cb16 = reinterpret_cast<__half*>(smem + kXSmemCb);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const sm = smem_raw + (base - raw);
+  float* const nk = reinterpret_cast<float*>(sm + kXNk);
+  float* const nv = reinterpret_cast<float*>(sm + kXNv);
+  __half* const cb16 = reinterpret_cast<__half*>(sm + kXCb);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_rb = (a.rows + kXRows - 1) / kXRows;
-  const int rb = blockIdx.x % n_rb;
+  const int rb = n_rb - 1 - (int)(blockIdx.x % n_rb);  // latest rows (longest reach) first
   const int h = (blockIdx.x / n_rb) % g.num_kv_heads;
   const int b = blockIdx.x / (n_rb * g.num_kv_heads);
-  const int P = g.page_size;
-  const int cap = a.max_pages * P;
+  const int cap = a.max_pages * g.page_size;
   int len = a.seq_lens[b];
   if (len < 0 || len > cap || (len > 0 && len < a.T)) {
-    if (rb == 0 && h == 0 && threadIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_LEN);
+    if (rb == n_rb - 1 && h == 0 && tid == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_LEN);
     len = len < 0 ? 0 : (len > cap ? cap : len);
   }
-  if (threadIdx.x < (1 << BITS)) cb16[threadIdx.x] = __float2half_rn(g.centroids[threadIdx.x]);
-
-  // ---- q~ = R_k q * sm_scale * log2(e) of the CTA's 64 rows, fp16, staged for ldmatrix ----
-  const __half* qh = reinterpret_cast<const __half*>(a.q);
-  for (int i = threadIdx.x; i < kXRows * 32; i += kXThreads) {
-    const int rr = i >> 5, quad = i & 31;  // row, dims 4 quad .. 4 quad + 3
-    const int r = rb * kXRows + rr;
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-    if (r < a.rows) {
-      const int j = r / g.group, head = h * g.group + r % g.group;
-      const uint2 raw = *reinterpret_cast<const uint2*>(qh + (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim + 4 * quad);
-      const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-      const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-      const float4 p = __ldg(reinterpret_cast<const float4*>(g.rot_k + (size_t)h * kHeadDim) + quad);
-      if (g.mode == RQ_PLANAR) {
-        y[0] = p.x * x01.x - p.y * x01.y;
-        y[1] = p.y * x01.x + p.x * x01.y;
-        y[2] = p.z * x23.x - p.w * x23.y;
-        y[3] = p.w * x23.x + p.z * x23.y;
-      } else {  // Hamilton product (a,b,c,d) (x) x
-        y[0] = p.x * x01.x - p.y * x01.y - p.z * x23.x - p.w * x23.y;
-        y[1] = p.y * x01.x + p.x * x01.y - p.w * x23.x + p.z * x23.y;
-        y[2] = p.z * x01.x + p.w * x01.y + p.x * x23.x - p.y * x23.y;
-        y[3] = p.w * x01.x - p.z * x01.y + p.y * x23.x + p.x * x23.y;
-      }
-    }
-    const uint2 v = make_uint2(pack_h2(y[0] * g.q_scale, y[1] * g.q_scale), pack_h2(y[2] * g.q_scale, y[3] * g.q_scale));
-    *reinterpret_cast<uint2*>(smem + kXSmemQ + xswz(rr, quad >> 1) + 8 * (quad & 1)) = v;
+  if (tid < (1 << BITS)) cb16[tid] = __float2half_rn(g.centroids[tid]);
+  const uint32_t bar_s = base + kXBar, bar_o = base + kXBar + 8;
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_s) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_o) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
-  uint32_t qa[8][4];  // A fragments of the warp's 16 rows, k-steps of 16 dims
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-    ldsm_x4(qa[ks], sbase + kXSmemQ + xswz(16 * warp + (lane & 15), 2 * ks + (lane >> 4)));
-
-  // rows g and g + 8 of the warp: their last visible position (-1: none, or not a row)
-  int qpos[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int r = rb * kXRows + 16 * warp + gq + 8 * i;
-    qpos[i] = r < a.rows ? len - a.T + r / g.group : -1;
+  __syncwarp();  // tcgen05.alloc is warp-collective
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + kXTmemSlot),
+                 "r"(kXTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  const int r_last = min(a.rows, (rb + 1) * kXRows) - 1;
-  const int kv_end = min(len, len - a.T + r_last / g.group + 1);  // positions any row here sees
 
-  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
-  float l_run[2] = {0.f, 0.f};
-  float o[16][4];
+  // ---- q~ = R_k q * sm_scale * log2(e) of row r, fp16, into the A operand of S ----
+  const int r = rb * kXRows + tid;
+  {
+    const bool valid = r < a.rows;
+    const int j = valid ? r / g.group : 0, head = h * g.group + (valid ? r % g.group : 0);
+    const uint4* qrow = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(a.q) +
+                                                       (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
+    const float4* rk = reinterpret_cast<const float4*>(g.rot_k + (size_t)h * kHeadDim);
+#pragma unroll 4
+    for (int c = 0; c < 16; ++c) {  // dims 8c .. 8c + 7: two rotation blocks of 4
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      if (valid) {
+        const uint4 raw8 = __ldg(qrow + c);
+        const uint32_t hw[4] = {raw8.x, raw8.y, raw8.z, raw8.w};
 #pragma unroll
-  for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  // thread t owns (token t / 4, 32-dim group t % 4) of every tile, for K and for V
-  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
-  const int my_tok = threadIdx.x >> 2, my_grp = threadIdx.x & 3;
-  GroupRaw cur[2], nxt[2];
-  load_group<BITS>(cur[0], g, a, bt, h, my_tok, len, 0, my_grp);
-  load_group<BITS>(cur[1], g, a, bt, h, my_tok, len, 1, my_grp);
-
-  for (int t0 = 0; t0 < kv_end; t0 += kXTok) {
-    __syncthreads();  // the previous tile's K~, V~ are consumed
-    // ---- dequantize this thread's two groups into the fp16 tiles ----
-#pragma unroll
-    for (int kind = 0; kind < 2; ++kind) {
-      uint8_t* tile = smem + (kind ? kXSmemV : kXSmemK);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {  // 8 dims = one 16-byte chunk of the row
-        uint32_t wv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half lo = cb16[group_code<BITS>(cur[kind], 8 * q + 2 * e)];
-          const __half hi = cb16[group_code<BITS>(cur[kind], 8 * q + 2 * e + 1)];
-          wv[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+        for (int blk = 0; blk < 2; ++blk) {
+          const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * blk]));
+          const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * blk + 1]));
+          const float4 p = __ldg(rk + 2 * c + blk);
+          float y[4];
+          if (g.mode == RQ_PLANAR) {
+            y[0] = p.x * x01.x - p.y * x01.y;
+            y[1] = p.y * x01.x + p.x * x01.y;
+            y[2] = p.z * x23.x - p.w * x23.y;
+            y[3] = p.w * x23.x + p.z * x23.y;
+          } else {  // Hamilton product (a,b,c,d) (x) x
+            y[0] = p.x * x01.x - p.y * x01.y - p.z * x23.x - p.w * x23.y;
+            y[1] = p.y * x01.x + p.x * x01.y - p.w * x23.x + p.z * x23.y;
+            y[2] = p.z * x01.x + p.w * x01.y + p.x * x23.x - p.y * x23.y;
+            y[3] = p.w * x01.x - p.z * x01.y + p.y * x23.x + p.x * x23.y;
+          }
+          w[2 * blk] = pack_h2(y[0] * g.q_scale, y[1] * g.q_scale);
+          w[2 * blk + 1] = pack_h2(y[2] * g.q_scale, y[3] * g.q_scale);
         }
-        *reinterpret_cast<uint4*>(tile + xswz(my_tok, 4 * my_grp + q)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
       }
-      if (my_grp == 0) (kind ? nv : nk)[my_tok] = __half2float(__ushort_as_half((unsigned short)cur[kind].norm));
+      *reinterpret_cast<uint4*>(sm + kXQ + (c >> 3) * 16384 + xswz(tid, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+  }
+
+  // row r sees positions <= qpos (-1: nothing, or not a row); the block's rows see < kv_end
+  const int qpos = r < a.rows ? len - a.T + r / g.group : -1;
+  const int r_last = min(a.rows, (rb + 1) * kXRows) - 1;
+  const int kv_end = min(len, len - a.T + r_last / g.group + 1);
+  const int n_tiles = kv_end > 0 ? (kv_end + kXTok - 1) / kXTok : 0;
+  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
+
+  // K~ of tile t0: thread (token tid % 64, dims 64 (tid / 64) ..) -> 8 16-byte chunks of a row
+  auto dequant_k = [&](int t0) {
+    const int tok = tid & 63, half = tid >> 6;
+    GroupRaw g0, g1;
+    load_group<BITS>(g0, g, a, bt, h, t0 + tok, len, 0, 2 * half);
+    load_group<BITS>(g1, g, a, bt, h, t0 + tok, len, 0, 2 * half + 1);
+    uint8_t* const atom = sm + kXK + half * 8192;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const GroupRaw& gr = c < 4 ? g0 : g1;
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = pack_hh(cb16[group_code<BITS>(gr, 8 * (c & 3) + 2 * e)], cb16[group_code<BITS>(gr, 8 * (c & 3) + 2 * e + 1)]);
+      *reinterpret_cast<uint4*>(atom + xswz(tok, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (half == 0) nk[tok] = __half2float(__ushort_as_half((unsigned short)g0.norm));
+  };
+  // V~^T of tile t0: warp w takes dims 32w .. 32w + 31 (code group w), lane p the token pair
+  // (2p, 2p + 1), stored as one half2 per dim row -- a warp writes 128 consecutive bytes a row
+  auto dequant_v = [&](int t0) {
+    const int grp = warp, p = lane;
+    GroupRaw v0, v1;
+    load_group<BITS>(v0, g, a, bt, h, t0 + 2 * p, len, 1, grp);
+    load_group<BITS>(v1, g, a, bt, h, t0 + 2 * p + 1, len, 1, grp);
+    uint8_t* const atom = sm + kXV;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int row = 32 * grp + i;
+      *reinterpret_cast<uint32_t*>(atom + row * 128 + (((p >> 2) ^ (row & 7)) << 4) + 4 * (p & 3)) =
+          pack_hh(cb16[group_code<BITS>(v0, i)], cb16[group_code<BITS>(v1, i)]);
+    }
+    if (grp == 0) {
+      nv[2 * p] = __half2float(__ushort_as_half((unsigned short)v0.norm));
+      nv[2 * p + 1] = __half2float(__ushort_as_half((unsigned short)v1.norm));
+    }
+  };
+
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();  // q~, centroids, barriers and the tensor-memory address are in place
+  fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kXTmemSlot);
+  const uint32_t tmem_o = tmem, tmem_s = tmem + 128;
+  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;  // the warp's 32 lanes of tensor memory
+  const uint32_t id_s = idesc_f16(kXRows, kXTok), id_o = idesc_f16(kXRows, kHeadDim);
+  int n_s = 0, n_o = 0;        // MMA groups issued (thread 0) ...
+  int seen_s = 0, seen_o = 0;  // ... and seen complete
+  bool alive = true;
+
+  auto issue_s = [&]() {  // S = q~ K~^T: 8 K-steps of 16 dims (4 per atom, 32 bytes apart)
+    if (tid == 0) {
+      fence_after_sync();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        umma_f16(tmem_s, sdesc(base + kXQ + (ks >> 2) * 16384 + (ks & 3) * 32),
+                 sdesc(base + kXK + (ks >> 2) * 8192 + (ks & 3) * 32), id_s, ks > 0);
+      umma_commit(bar_s);
+      ++n_s;
+    }
+  };
+  auto issue_o = [&](bool accumulate) {  // O~ += P' V~: 4 K-steps of 16 tokens
+    if (tid == 0) {
+      fence_after_sync();
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_f16(tmem_o, sdesc(base + kXP + ks * 32), sdesc(base + kXV + ks * 32), id_o, accumulate || ks > 0);
+      umma_commit(bar_o);
+      ++n_o;
+    }
+  };
+  // thread 0 waits for the next completion of a barrier; the result reaches every thread at
+  // the following __syncthreads_and
+  auto wait_next = [&](uint32_t bar, int& seen) -> bool {
+    if (tid != 0) return true;
+    const bool ok = mbar_wait_bounded(bar, (uint32_t)(seen & 1));
+    if (ok) ++seen;
+    return ok;
+  };
+
+  float m_run = -CUDART_INF_F, l_run = 0.f;
+  if (n_tiles > 0) {
+    dequant_k(0);
+    fence_async_smem();
     __syncthreads();
-    // ---- the next tile's groups are in flight while this one is multiplied ----
-    if (t0 + kXTok < kv_end) {
-      load_group<BITS>(nxt[0], g, a, bt, h, t0 + kXTok + my_tok, len, 0, my_grp);
-      load_group<BITS>(nxt[1], g, a, bt, h, t0 + kXTok + my_tok, len, 1, my_grp);
+    issue_s();
+  }
+  for (int t = 0; t < n_tiles; ++t) {
+    const int t0 = t * kXTok;
+    bool ok = t == 0 || wait_next(bar_o, seen_o);  // P'V~ of the previous tile done: V~, P', O~ free
+    if (!__syncthreads_and(ok)) {
+      alive = false;
+      break;
     }
+    fence_after_sync();
+    dequant_v(t0);
+    ok = wait_next(bar_s, seen_s);  // S of this tile done
+    if (!__syncthreads_and(ok)) {   // (also: the V norms are visible)
+      alive = false;
+      break;
+    }
+    fence_after_sync();
 
-    // ---- S = q~ K~^T for the warp's 16 rows x 32 tokens ----
-    float s[4][4];
+    // ---- this row's scores: scale by the key norms, mask, online softmax (base 2) ----
+    float s[kXTok];
 #pragma unroll
-    for (int nn = 0; nn < 4; ++nn) s[nn][0] = s[nn][1] = s[nn][2] = s[nn][3] = 0.f;
+    for (int c = 0; c < kXTok / 16; ++c) {
+      float v[16];
+      tmem_ld16(tmem_s + lane_off + 16 * c, v);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
+      for (int i = 0; i < 16; ++i) s[16 * c + i] = v[i];
+    }
+    tmem_wait_ld();
+    float tmax = -CUDART_INF_F;
 #pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        uint32_t kb[4];  // b0, b1 of token n-tile 2np, then of 2np + 1
-        ldsm_x4(kb, sbase + kXSmemK + xswz(8 * (2 * np + (lane >> 4)) + (lane & 7), 2 * ks + ((lane >> 3) & 1)));
-        mma16816(s[2 * np], qa[ks], kb[0], kb[1]);
-        mma16816(s[2 * np + 1], qa[ks], kb[2], kb[3]);
+    for (int c = 0; c < kXTok / 4; ++c) {
+      const float4 n4 = reinterpret_cast<const float4*>(nk)[c];
+      const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int jj = 4 * c + i;
+        const float v = t0 + jj > qpos ? -CUDART_INF_F : s[jj] * nn[i];
+        s[jj] = v;
+        tmax = fmaxf(tmax, v);
       }
     }
-    // scale by the key norms, mask, online softmax (rows g: elements 0,1; g + 8: elements 2,3)
-    float tmax[2] = {-CUDART_INF_F, -CUDART_INF_F};
+    const float m_new = fmaxf(m_run, tmax);
+    const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+    const float alpha = ex2(m_run - m_use);
+    float lsum = 0.f;
 #pragma unroll
-    for (int nn = 0; nn < 4; ++nn) {
+    for (int c = 0; c < kXTok / 4; ++c) {
+      const float4 n4 = reinterpret_cast<const float4*>(nv)[c];
+      const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = 8 * nn + 2 * tq + (e & 1);
-        float v = s[nn][e] * nk[tok];
-        if (t0 + tok > qpos[e >> 1]) v = -CUDART_INF_F;
-        s[nn][e] = v;
-        tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
+      for (int i = 0; i < 4; ++i) {
+        const float pr = ex2(s[4 * c + i] - m_use);  // masked: +0
+        lsum += pr;
+        s[4 * c + i] = pr * nn[i];
       }
     }
-    float alpha[2], m_use[2];
+    l_run = l_run * alpha + lsum;
+    m_run = m_new;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 1));
-      tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 2));
-      const float m_new = fmaxf(m_run[i], tmax[i]);
-      m_use[i] = m_new == -CUDART_INF_F ? 0.f : m_new;
-      alpha[i] = ex2(m_run[i] - m_use[i]);
-      m_run[i] = m_new;
-      l_run[i] *= alpha[i];
-    }
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(sm + kXP + xswz(tid, c)) =
+          make_uint4(pack_h2(s[8 * c], s[8 * c + 1]), pack_h2(s[8 * c + 2], s[8 * c + 3]),
+                     pack_h2(s[8 * c + 4], s[8 * c + 5]), pack_h2(s[8 * c + 6], s[8 * c + 7]));
+    // O~ *= alpha where some row's running max moved (never before the first P'V~)
+    if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+      for (int c = 0; c < kHeadDim / 16; ++c) {
+        float v[16];
+        tmem_ld16(tmem_o + lane_off + 16 * c, v);
+        tmem_wait_ld();
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      o[nd][0] *= alpha[0];
-      o[nd][1] *= alpha[0];
-      o[nd][2] *= alpha[1];
-      o[nd][3] *= alpha[1];
-    }
-    uint32_t pa[2][4];  // P' = p * n_v as A fragments of two 16-token k-steps
-#pragma unroll
-    for (int nn = 0; nn < 4; ++nn) {
-      float pv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p = ex2(s[nn][e] - m_use[e >> 1]);  // masked: +0
-        l_run[e >> 1] += p;
-        pv[e] = p * nv[8 * nn + 2 * tq + (e & 1)];
+        for (int i = 0; i < 16; ++i) v[i] *= alpha;
+        tmem_st16(tmem_o + lane_off + 16 * c, v);
       }
-      pa[nn >> 1][2 * (nn & 1)] = pack_h2(pv[0], pv[1]);      // row g
-      pa[nn >> 1][2 * (nn & 1) + 1] = pack_h2(pv[2], pv[3]);  // row g + 8
+      tmem_wait_st();
     }
-    // ---- O~ += P' V~ ----
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-      for (int nd = 0; nd < 16; nd += 2) {
-        uint32_t vb[4];  // b0, b1 of dim n-tile nd, then of nd + 1
-        ldsm_x4_t(vb, sbase + kXSmemV + xswz(16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7), nd + (lane >> 4)));
-        mma16816(o[nd], pa[kk], vb[0], vb[1]);
-        mma16816(o[nd + 1], pa[kk], vb[2], vb[3]);
-      }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();  // P', V~ written; S read; O~ rescaled
+    issue_o(t > 0);
+    if (t + 1 < n_tiles) {  // the next K~ while P'V~ runs (S is read, K~ and the K norms free)
+      dequant_k(t0 + kXTok);
+      fence_async_smem();
+      __syncthreads();
+      issue_s();
     }
-    cur[0] = nxt[0];
-    cur[1] = nxt[1];
   }
 
-  // ---- normalise, stage, rotate back, store ----
+  // ---- epilogue: wait for the last P'V~, normalise, rotate back, store ----
+  bool ok = alive && (n_o == 0 || tid != 0 || wait_next(bar_o, seen_o));
+  if (tid == 0 && alive && n_tiles > 0 && n_o != seen_o) ok = false;
+  ok = __syncthreads_and(ok) && alive;
+  if (!ok) {
+    if (tid == 0) {
+      if (a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
+      // never free tensor memory under an MMA still running: wait (bounded) for every group
+      while (seen_s < n_s && mbar_wait_bounded(bar_s, (uint32_t)(seen_s & 1))) ++seen_s;
+      while (seen_o < n_o && mbar_wait_bounded(bar_o, (uint32_t)(seen_o & 1))) ++seen_o;
+    }
+  } else {
+    fence_after_sync();
+    // the tensor-memory loads are warp-collective: every lane takes part, valid rows store
+    const bool store = r < a.rows;
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    const int j = store ? r / g.group : 0, head = h * g.group + (store ? r % g.group : 0);
+    uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(a.out) +
+                                           (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
+    const float4* rv = reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim);
+#pragma unroll 1
+    for (int c = 0; c < kHeadDim / 16; ++c) {  // dims 16c .. 16c + 15
+      float y[16];
+      __syncwarp();       // the previous stores diverged by row
+      if (n_tiles > 0) {  // uniform over the CTA
+        tmem_ld16(tmem_o + lane_off + 16 * c, y);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 1);
-    l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 2);
-  }
-  const float inv0 = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f, inv1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
-  __syncthreads();  // everyone is done with the query staging, which the output staging reuses
-  float* os = reinterpret_cast<float*>(smem + kXSmemQ);
+        for (int i = 0; i < 16; ++i) y[i] = 0.f;
+      }
+      if (store) {
+        uint32_t w[8];
 #pragma unroll
-  for (int nd = 0; nd < 16; ++nd) {
-    const int d = 8 * nd + 2 * tq;
-    *reinterpret_cast<float2*>(os + (16 * warp + gq) * kXOStride + d) = make_float2(o[nd][0] * inv0, o[nd][1] * inv0);
-    *reinterpret_cast<float2*>(os + (16 * warp + gq + 8) * kXOStride + d) = make_float2(o[nd][2] * inv1, o[nd][3] * inv1);
+        for (int blk = 0; blk < 4; ++blk) {
+          const float4 p = __ldg(rv + 4 * c + blk);
+          const float y0 = y[4 * blk] * inv, y1 = y[4 * blk + 1] * inv, y2 = y[4 * blk + 2] * inv, y3 = y[4 * blk + 3] * inv;
+          float x[4];
+          if (g.mode == RQ_PLANAR) {
+            x[0] = p.x * y0 + p.y * y1;
+            x[1] = -p.y * y0 + p.x * y1;
+            x[2] = p.z * y2 + p.w * y3;
+            x[3] = -p.w * y2 + p.z * y3;
+          } else {  // L(q)^T y
+            x[0] = p.x * y0 + p.y * y1 + p.z * y2 + p.w * y3;
+            x[1] = -p.y * y0 + p.x * y1 + p.w * y2 - p.z * y3;
+            x[2] = -p.z * y0 - p.w * y1 + p.x * y2 + p.y * y3;
+            x[3] = -p.w * y0 + p.z * y1 - p.y * y2 + p.x * y3;
+          }
+          w[2 * blk] = pack_h2(x[0], x[1]);
+          w[2 * blk + 1] = pack_h2(x[2], x[3]);
+        }
+        orow[2 * c] = make_uint4(w[0], w[1], w[2], w[3]);
+        orow[2 * c + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
   }
+  fence_before_sync();
   __syncthreads();
-  __half* out = reinterpret_cast<__half*>(a.out);
-  for (int i = threadIdx.x; i < kXRows * 32; i += kXThreads) {
-    const int rr = i >> 5, quad = i & 31;
-    const int r = rb * kXRows + rr;
-    if (r >= a.rows) continue;
-    const float4 yv = *reinterpret_cast<const float4*>(os + rr * kXOStride + 4 * quad);
-    const float4 p = __ldg(reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim) + quad);
-    float x[4];
-    if (g.mode == RQ_PLANAR) {
-      x[0] = p.x * yv.x + p.y * yv.y;
-      x[1] = -p.y * yv.x + p.x * yv.y;
-      x[2] = p.z * yv.z + p.w * yv.w;
-      x[3] = -p.w * yv.z + p.z * yv.w;
-    } else {  // L(q)^T y
-      x[0] = p.x * yv.x + p.y * yv.y + p.z * yv.z + p.w * yv.w;
-      x[1] = -p.y * yv.x + p.x * yv.y + p.w * yv.z - p.z * yv.w;
-      x[2] = -p.z * yv.x - p.w * yv.y + p.x * yv.z + p.y * yv.w;
-      x[3] = -p.w * yv.x + p.z * yv.y - p.y * yv.z + p.x * yv.w;
-    }
-    const int j = r / g.group, head = h * g.group + r % g.group;
-    *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim + 4 * quad) =
-        make_uint2(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]));
-  }
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kXTmemCols) : "memory");
 }
 
 }  // namespace

@@ -320,6 +320,7 @@ EXTEND_CASES = [
     (PLANAR, 2, 32, 8, 16, [17, 50, 33], 17),
     (ISO, 4, 24, 2, 32, [129, 70], 70),      # group 12: 64-row blocks cut through a draft's heads
     (PLANAR, 3, 8, 8, 16, [2048], 256),
+    (ISO, 2, 32, 8, 16, [0, 130, 64], 64),  # an empty sequence (zeros) and one of only new tokens
 ]
 
 
