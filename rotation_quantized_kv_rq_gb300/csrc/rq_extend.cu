@@ -15,10 +15,11 @@
 // (tcgen05.ld), scales it by the key norms, masks it and runs the online softmax in base 2
 // with no cross-thread reduction, then writes P' = p * n_v as fp16; one thread issues
 // O~ += P' V~ (M 128 x N 128 x K 64), accumulated in tensor memory.  The next tile's K~ is
-// dequantized while P'V~ runs and its V~ while the next S runs; two CTAs share an SM (tensor
-// memory 2 x 256 columns, shared memory 2 x 83.5 KB) and fill each other's gaps.  Every wait
-// is bounded: a wait that runs out sets RQ_STATUS_TIMEOUT, the CTA stops, waits (bounded)
-// for the MMAs it issued and frees its tensor memory.
+// dequantized while P'V~ runs and its V~ while the next S runs, from code words loaded a tile
+// ahead; two CTAs share an SM (tensor memory 2 x 256 columns, shared memory 2 x 83.5 KB) and
+// fill each other's gaps.  Every wait is bounded: a wait that runs out sets
+// RQ_STATUS_TIMEOUT, the CTA stops, waits (bounded) for the MMAs it issued and frees its
+// tensor memory.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -274,41 +275,46 @@ extend_kernel(const Geometry g, const AttnArgs a) {
   const int n_tiles = kv_end > 0 ? (kv_end + kXTok - 1) / kXTok : 0;
   const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
 
-  // K~ of tile t0: thread (token tid % 64, dims 64 (tid / 64) ..) -> 8 16-byte chunks of a row
-  auto dequant_k = [&](int t0) {
+  // K~ of a tile: thread (token tid % 64, dims 64 (tid / 64) ..) -> 8 16-byte chunks of a row.
+  // V~^T of a tile: warp w takes dims 32w .. 32w + 31 (code group w), lane p the token pair
+  // (2p, 2p + 1), stored as one half2 per dim row -- a warp writes 128 consecutive bytes a row.
+  // The code words are loaded into registers a tile ahead of their dequantisation.
+  GroupRaw kr0, kr1, vr0, vr1;
+  auto load_k = [&](int t0) {
     const int tok = tid & 63, half = tid >> 6;
-    GroupRaw g0, g1;
-    load_group<BITS>(g0, g, a, bt, h, t0 + tok, len, 0, 2 * half);
-    load_group<BITS>(g1, g, a, bt, h, t0 + tok, len, 0, 2 * half + 1);
+    load_group<BITS>(kr0, g, a, bt, h, t0 + tok, len, 0, 2 * half);
+    load_group<BITS>(kr1, g, a, bt, h, t0 + tok, len, 0, 2 * half + 1);
+  };
+  auto load_v = [&](int t0) {
+    load_group<BITS>(vr0, g, a, bt, h, t0 + 2 * lane, len, 1, warp);
+    load_group<BITS>(vr1, g, a, bt, h, t0 + 2 * lane + 1, len, 1, warp);
+  };
+  auto store_k = [&]() {
+    const int tok = tid & 63, half = tid >> 6;
     uint8_t* const atom = sm + kXK + half * 8192;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const GroupRaw& gr = c < 4 ? g0 : g1;
+      const GroupRaw& gr = c < 4 ? kr0 : kr1;
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         w[e] = pack_hh(cb16[group_code<BITS>(gr, 8 * (c & 3) + 2 * e)], cb16[group_code<BITS>(gr, 8 * (c & 3) + 2 * e + 1)]);
       *reinterpret_cast<uint4*>(atom + xswz(tok, c)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    if (half == 0) nk[tok] = __half2float(__ushort_as_half((unsigned short)g0.norm));
+    if (half == 0) nk[tok] = __half2float(__ushort_as_half((unsigned short)kr0.norm));
   };
-  // V~^T of tile t0: warp w takes dims 32w .. 32w + 31 (code group w), lane p the token pair
-  // (2p, 2p + 1), stored as one half2 per dim row -- a warp writes 128 consecutive bytes a row
-  auto dequant_v = [&](int t0) {
+  auto store_v = [&]() {
     const int grp = warp, p = lane;
-    GroupRaw v0, v1;
-    load_group<BITS>(v0, g, a, bt, h, t0 + 2 * p, len, 1, grp);
-    load_group<BITS>(v1, g, a, bt, h, t0 + 2 * p + 1, len, 1, grp);
     uint8_t* const atom = sm + kXV;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int row = 32 * grp + i;
       *reinterpret_cast<uint32_t*>(atom + row * 128 + (((p >> 2) ^ (row & 7)) << 4) + 4 * (p & 3)) =
-          pack_hh(cb16[group_code<BITS>(v0, i)], cb16[group_code<BITS>(v1, i)]);
+          pack_hh(cb16[group_code<BITS>(vr0, i)], cb16[group_code<BITS>(vr1, i)]);
     }
     if (grp == 0) {
-      nv[2 * p] = __half2float(__ushort_as_half((unsigned short)v0.norm));
-      nv[2 * p + 1] = __half2float(__ushort_as_half((unsigned short)v1.norm));
+      nv[2 * p] = __half2float(__ushort_as_half((unsigned short)vr0.norm));
+      nv[2 * p + 1] = __half2float(__ushort_as_half((unsigned short)vr1.norm));
     }
   };
 
@@ -356,10 +362,13 @@ extend_kernel(const Geometry g, const AttnArgs a) {
 
   float m_run = -CUDART_INF_F, l_run = 0.f;
   if (n_tiles > 0) {
-    dequant_k(0);
+    load_k(0);
+    load_v(0);
+    store_k();
     fence_async_smem();
     __syncthreads();
     issue_s();
+    if (n_tiles > 1) load_k(kXTok);
   }
   for (int t = 0; t < n_tiles; ++t) {
     const int t0 = t * kXTok;
@@ -369,7 +378,8 @@ extend_kernel(const Geometry g, const AttnArgs a) {
       break;
     }
     fence_after_sync();
-    dequant_v(t0);
+    store_v();
+    if (t + 1 < n_tiles) load_v(t0 + kXTok);
     ok = wait_next(bar_s, seen_s);  // S of this tile done
     if (!__syncthreads_and(ok)) {   // (also: the V norms are visible)
       alive = false;
@@ -440,7 +450,8 @@ extend_kernel(const Geometry g, const AttnArgs a) {
     __syncthreads();  // P', V~ written; S read; O~ rescaled
     issue_o(t > 0);
     if (t + 1 < n_tiles) {  // the next K~ while P'V~ runs (S is read, K~ and the K norms free)
-      dequant_k(t0 + kXTok);
+      store_k();
+      if (t + 2 < n_tiles) load_k(t0 + 2 * kXTok);
       fence_async_smem();
       __syncthreads();
       issue_s();
