@@ -33,6 +33,7 @@
 #include <math_constants.h>
 
 #include "rq_codec.cuh"
+#include "rq_lut.cuh"
 #include "rq_internal.h"
 #include "../../include/rq.h"
 
@@ -41,7 +42,7 @@ namespace {
 
 constexpr int kWarps = kAttnWarps;
 constexpr int kThreads = kWarps * 32;
-constexpr int kLutBytes = 256 * 256;          // 256 index bytes x (2 tables x 32 lanes x 4 B)
+constexpr int kLutBytes = lut::kBytes;
 constexpr int kMaxSplitPages = 1024;          // page ids staged per item
 constexpr int kWaitLimit = 1 << 22;           // bounded mbarrier polling (about a second)
 
@@ -210,56 +211,25 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Code tables.  Entry e of a table is the half2 (c[code_a], c[code_b]) of the two codes an
-// index byte e carries:
-//   T4 (4-bit):  code_a = e & 15,                       code_b = e >> 4
-//   T1 (3-bit):  code_a = (e & 3) | (e >> 4 & 1) << 2,   code_b = (e >> 2 & 3) | (e >> 5 & 1) << 2
-//   T2 (3-bit):  code_a = (e >> 4 & 3) | (e & 1) << 2,   code_b = (e >> 6 & 3) | (e >> 1 & 1) << 2
-//   U1 (2-bit):  code_a = e & 3,                        code_b = e >> 4 & 3
-//   U2 (2-bit):  code_a = e >> 2 & 3,                   code_b = e >> 6 & 3
-// Row e holds 64 words: word l (l < 32) is the first table's entry for lane l, word 32 + l the
-// second table's (T2 for 3-bit, U2 for 2-bit; a copy of T4 for 4-bit).  A lookup address is
-// base + e * 256 + lane * 4 (+ 128 for the second table).
+// Code tables (rq_lut.cuh): T4 / T1 + T2 / U1 + U2 turn an index byte of two codes into the
+// half2 of their centroids with one shared load.
 // ---------------------------------------------------------------------------------------
 template <int BITS>
-__device__ void build_lut(uint32_t* lut, const float* centroids, float* cb) {
+__device__ void build_lut(uint32_t* table, const float* centroids, float* cb) {
   if (threadIdx.x < (1 << BITS)) cb[threadIdx.x] = centroids[threadIdx.x];
   __syncthreads();
-  // Each row holds 2 distinct words, each 32 times: 16-byte stores of 4 copies, a warp writing
-  // 512 consecutive bytes (two rows) per store, free of bank conflicts.
-  uint4* lut4 = reinterpret_cast<uint4*>(lut);
-  for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
-    const int e = i >> 4, second = (i >> 3) & 1;
-    int ca, cbx;
-    if (BITS == 4) {
-      ca = e & 15;
-      cbx = e >> 4;
-    } else if (BITS == 2) {
-      ca = second ? (e >> 2) & 3 : e & 3;
-      cbx = second ? (e >> 6) & 3 : (e >> 4) & 3;
-    } else if (!second) {
-      ca = (e & 3) | ((e >> 4) & 1) << 2;
-      cbx = ((e >> 2) & 3) | ((e >> 5) & 1) << 2;
-    } else {
-      ca = ((e >> 4) & 3) | (e & 1) << 2;
-      cbx = ((e >> 6) & 3) | ((e >> 1) & 1) << 2;
-    }
-    const uint32_t w = pack_half2(cb[ca], cb[cbx]);
-    lut4[i] = make_uint4(w, w, w, w);
-  }
+  lut::fill<BITS>(table, cb, threadIdx.x, kThreads);
 }
 
-// Half2 of the two codes in byte J of index word x (SECOND selects the second table).
-// The table starts at a 64 KB-aligned shared address A, so an entry's address
-// A + e * 256 + lane * 4 (+ 128) has byte 0 = lane * 4 (+ 128), byte 1 = e and bytes 2-3 = A's:
-// one byte permute of (x, key) with key = A | lane * 4 (+ 128) forms it, with no add.
+// Half2 of the two codes in byte J of index word x (SECOND selects the second table); key1 /
+// key2 are the lane's table keys (lut::key).
 template <int J, int SECOND>
-__device__ __forceinline__ uint32_t lut(uint32_t x, uint32_t key1, uint32_t key2) {
-  return lds32(prmt(x, SECOND ? key2 : key1, 0x7604u | (J << 4)));
+__device__ __forceinline__ uint32_t lut_at(uint32_t x, uint32_t key1, uint32_t key2) {
+  return lut::get(x, J, SECOND ? key2 : key1);
 }
 template <int SECOND>
 __device__ __forceinline__ uint32_t lut_dyn(uint32_t x, int j, uint32_t key1, uint32_t key2) {
-  return lds32(prmt(x, SECOND ? key2 : key1, 0x7604u | (j << 4)));
+  return lut::get(x, j, SECOND ? key2 : key1);
 }
 
 // 2^x on the SFU (x = -inf gives +0, which masked scores rely on).
@@ -375,15 +345,15 @@ __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const
       const int w = kc >> 1, j0 = (2 * kc) & 3;
       uint32_t a0, a1, a2, a3;
       if (j0 == 0) {
-        a0 = lut<0, 0>(k0[w], key1, key2);
-        a1 = lut<0, 0>(k1[w], key1, key2);
-        a2 = lut<1, 0>(k0[w], key1, key2);
-        a3 = lut<1, 0>(k1[w], key1, key2);
+        a0 = lut_at<0, 0>(k0[w], key1, key2);
+        a1 = lut_at<0, 0>(k1[w], key1, key2);
+        a2 = lut_at<1, 0>(k0[w], key1, key2);
+        a3 = lut_at<1, 0>(k1[w], key1, key2);
       } else {
-        a0 = lut<2, 0>(k0[w], key1, key2);
-        a1 = lut<2, 0>(k1[w], key1, key2);
-        a2 = lut<3, 0>(k0[w], key1, key2);
-        a3 = lut<3, 0>(k1[w], key1, key2);
+        a0 = lut_at<2, 0>(k0[w], key1, key2);
+        a1 = lut_at<2, 0>(k1[w], key1, key2);
+        a2 = lut_at<3, 0>(k0[w], key1, key2);
+        a3 = lut_at<3, 0>(k1[w], key1, key2);
       }
       if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
       else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);

@@ -6,47 +6,77 @@
 // hundreds or thousands, where the split-K kernel (which re-reads the cache for every 8 query
 // rows) stops paying.
 //
-// Design (sm_103a, 5th-generation tensor cores): a CTA of 4 warps takes 128 query rows of one
-// (sequence, kv head) -- rows r = j * group + k, thread i owning row i -- and walks the cache
-// in 64-token tiles up to the last position its rows can see.  Per tile the threads
-// dequantize K~ (token-major) and V~^T (dim-major) into shared memory as fp16 centroid values
-// in the K-major 128-byte-swizzled operand layout; one thread issues S = Q~ K~^T
-// (tcgen05.mma, M 128 x N 64 x K 128) into tensor memory; every thread reads its row of S
-// (tcgen05.ld), scales it by the key norms, masks it and runs the online softmax in base 2
-// with no cross-thread reduction, then writes P' = p * n_v as fp16; one thread issues
-// O~ += P' V~ (M 128 x N 128 x K 64), accumulated in tensor memory.  The next tile's K~ is
-// dequantized while P'V~ runs and its V~ while the next S runs, from code words loaded a tile
-// ahead; two CTAs share an SM (tensor memory 2 x 256 columns, shared memory 2 x 83.5 KB) and
-// fill each other's gaps.  Every wait is bounded: a wait that runs out sets
-// RQ_STATUS_TIMEOUT, the CTA stops, waits (bounded) for the MMAs it issued and frees its
+// Design (sm_103a, 5th-generation tensor cores): one CTA per SM, 8 warps, takes 256 query rows
+// of one (sequence, kv head) -- rows r = j * group + k, thread i owning row i, in two blocks of
+// 128 (warps 0-3 and 4-7) -- and walks the cache in 64-token tiles up to the last position its
+// rows can see.  Per tile the 256 threads dequantize K~ (token-major) and V~^T (dim-major) once
+// for both blocks, into shared memory as fp16 centroid values in the K-major 128-byte-swizzled
+// operand layout: code bytes index a lane-replicated table of centroid pairs (rq_lut.cuh), one
+// shared load per two values.  One thread issues S_b = Q~_b K~^T (tcgen05.mma, M 128 x N 64 x
+// K 128) for both blocks into tensor memory; every thread reads its row of S (tcgen05.ld),
+// scales it by the key norms, masks it and runs the online softmax in base 2 with no
+// cross-thread reduction, then writes P' = p * n_v as fp16; one thread issues
+// O~_b += P'_b V~ (M 128 x N 128 x K 64), accumulated in tensor memory (all 512 columns: O~_0,
+// O~_1, S_0, S_1).  The next tile's K~ is dequantized while P'V~ runs and its V~ while the next
+// S runs, from code words loaded a tile ahead.  Every wait is bounded: a wait that runs out
+// sets RQ_STATUS_TIMEOUT, the CTA stops, waits (bounded) for the MMAs it issued and frees its
 // tensor memory.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "rq_internal.h"
+#include "rq_lut.cuh"
 #include "../../include/rq.h"
 
 namespace rq {
 namespace {
 
-constexpr int kXThreads = 128;  // thread i owns query row i of the CTA's block
-constexpr int kXRows = 128;     // M of both MMAs
+constexpr int kXThreads = 256;  // thread i owns query row i of the CTA's 256
+constexpr int kXBlock = 128;    // rows per block: M of every MMA
+constexpr int kXRows = 2 * kXBlock;
 constexpr int kXTok = 64;       // tokens per K/V tile: N of S, K of P'V~
-// Shared memory, from a 1024-byte-aligned base.  MMA operands are K-major with the 128-byte
-// swizzle: 128-byte rows (64 fp16 of K), 16-byte chunk c of row r stored at chunk c ^ (r % 8),
-// 8-row groups 1024 bytes apart, a second 64-wide K atom after all rows of the first.
-constexpr int kXQ = 0;                    // q~: 128 rows x 128 dims, two atoms of 16 KB
-constexpr int kXK = kXQ + 32768;          // K~: 64 tokens x 128 dims, two atoms of 8 KB
-constexpr int kXV = kXK + 16384;          // V~^T: 128 dims x 64 tokens
-constexpr int kXP = kXV + 16384;          // P': 128 rows x 64 tokens
-constexpr int kXNk = kXP + 16384;         // the tile's K norms, f32 [64]
-constexpr int kXNv = kXNk + 256;          // the tile's V norms, f32 [64]
-constexpr int kXCb = kXNv + 256;          // centroids, fp16 [16]
-constexpr int kXBar = kXCb + 32;          // mbarriers: S done, P'V~ done
-constexpr int kXTmemSlot = kXBar + 16;    // tensor-memory address from tcgen05.alloc
-constexpr int kXSmem = kXTmemSlot + 16 + 1024;  // + alignment slack: 83,520 bytes (> 1/3 of the SM)
-constexpr uint32_t kXTmemCols = 256;      // O~ in columns [0, 128), S in [128, 192)
-constexpr int kXWaitLimit = 1 << 22;      // bounded mbarrier polling (about a second)
+// Shared memory: the 64 KB code table at the first 64 KB-aligned address of the window, the
+// buffers (1024-aligned) below it where they fit, else above it.  MMA operands are K-major with
+// the 128-byte swizzle: 128-byte rows (64 fp16 of K), 16-byte chunk c of row r stored at chunk
+// c ^ (r % 8), 8-row groups 1024 bytes apart, a second 64-wide K atom after all rows of the first.
+constexpr uint32_t kXQBytes = 32768;   // q~ of a block: 128 rows x 128 dims, two atoms
+constexpr uint32_t kXKBytes = 16384;   // K~: 64 tokens x 128 dims, two atoms of 8 KB
+constexpr uint32_t kXVBytes = 16384;   // V~^T: 128 dims x 64 tokens
+constexpr uint32_t kXPBytes = 16384;   // P' of a block: 128 rows x 64 tokens
+constexpr uint32_t kXMiscBytes = 1024; // K norms f32[64], V norms f32[64], centroids f32[16],
+                                       // two mbarriers, the tensor-memory address
+constexpr int kXSmem = 232448;         // the whole opt-in window (one CTA per SM)
+constexpr uint32_t kXTmemCols = 512;   // O~_0 [0,128), O~_1 [128,256), S_0 [256,320), S_1 [320,384)
+constexpr int kXWaitLimit = 1 << 22;   // bounded mbarrier polling (about a second)
+
+struct XPlan {
+  uint32_t lut, q[2], k, v, p[2], misc, end;  // shared addresses
+};
+__device__ __forceinline__ XPlan x_plan(uint32_t raw) {
+  XPlan pl;
+  pl.lut = (raw + 0xFFFFu) & ~0xFFFFu;
+  uint32_t lo = (raw + 1023u) & ~1023u, hi = pl.lut + (uint32_t)lut::kBytes;
+  auto place = [&](uint32_t bytes) {
+    uint32_t at;
+    if (lo + bytes <= pl.lut) {
+      at = lo;
+      lo += bytes;
+    } else {
+      at = hi;
+      hi += bytes;
+    }
+    return at;
+  };
+  pl.q[0] = place(kXQBytes);
+  pl.q[1] = place(kXQBytes);
+  pl.k = place(kXKBytes);
+  pl.v = place(kXVBytes);
+  pl.p[0] = place(kXPBytes);
+  pl.p[1] = place(kXPBytes);
+  pl.misc = place(kXMiscBytes);
+  pl.end = hi;
+  return pl;
+}
 
 __device__ __forceinline__ uint32_t xswz(int row, int chunk) { return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4)); }
 
@@ -60,7 +90,9 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
 }
 // Instruction descriptor, kind::f16: f32 accumulator (bits 4-5 = 1), f16 A and B (bits 7-12 =
 // 0), both K-major (bits 15, 16 = 0), N / 8 at bits 17-22, M / 16 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) { return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24); }
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id, uint32_t accumulate) {
   asm volatile(
@@ -119,9 +151,14 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ uint32_t pack_hh(__half lo, __half hi) {
-  return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+template <uint32_t LUT3>
+__device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, %4;" : "=r"(d) : "r"(a), "r"(b), "r"(c), "n"(LUT3));
+  return d;
 }
+// (a & c) | (b & ~c)
+__device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t c) { return lop3<0xE4>(a, b, c); }
 
 // One (token, 32-dim group) of a K or V vector as stored (include/rq.h): the code words and the
 // token's fp16 norm, loaded from global memory ahead of use.
@@ -178,32 +215,106 @@ __device__ __forceinline__ void load_group(GroupRaw& r, const Geometry& g, const
     r.norm = __ldg(reinterpret_cast<const uint16_t*>(chunk + (size_t)2 * P * vb + kind * 2 * P + 2 * off));
 }
 
-// The code of dim i (0..31) of a loaded group.
+// ---- K~ rows: one token's 32-dim group -> four 16-byte chunks of 8 fp16 ----
+// Chunk q holds dims 8q .. 8q + 7 of the group, as the half2 of dim pairs.  4-bit: byte j of
+// word q is the pair (8q + 2j, 8q + 2j + 1).  3-bit: X0 = W0.lo | W2.hi and X1 = W2.lo | W0.hi
+// give pairs 2k (T1) and 2k + 1 (T2) from byte k, X2 = W1.lo | (W2 >> 2).hi and X3 =
+// (W2 >> 2).lo | W1.hi pairs 8 + 2k and 9 + 2k.  2-bit: byte j of word q >> 1 carries dims
+// 4j' .. 4j' + 3; U1 gives (4j', 4j' + 2) and U2 (4j' + 1, 4j' + 3), so within every 4-dim
+// block the stored order is 0, 2, 1, 3 -- and q~ is stored in the same order.
 template <int BITS>
-__device__ __forceinline__ int group_code(const GroupRaw& r, int i) {
+__device__ __forceinline__ void k_chunks(uint4 (&ch)[4], const GroupRaw& r, uint32_t key1, uint32_t key2) {
   if constexpr (BITS == 4) {
-    return (int)((r.w[i >> 3] >> (4 * (i & 7))) & 15u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      ch[q] = make_uint4(lut::get(r.w[q], 0, key1), lut::get(r.w[q], 1, key1), lut::get(r.w[q], 2, key1),
+                         lut::get(r.w[q], 3, key1));
   } else if constexpr (BITS == 2) {
-    return (int)((r.w[i >> 4] >> (2 * (i & 15))) & 3u);
-  } else {  // low bits: W0 (dims 0-15) / W1 (16-31); high bit of i = 16h + 4k + r at 8k + 2h + {4,5,0,1}[r]
-    const int lo = (int)((r.w[i >> 4] >> (2 * (i & 15))) & 3u);
-    const int hh = i >> 4, k = (i >> 2) & 3, rr = i & 3;
-    const int bit = 8 * k + 2 * hh + (rr < 2 ? 4 + rr : rr - 2);
-    return lo | (int)(((r.w[2] >> bit) & 1u) << 2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t w = r.w[q >> 1];
+      const int j0 = 2 * (q & 1);
+      ch[q] = make_uint4(lut::get(w, j0, key1), lut::get(w, j0, key2), lut::get(w, j0 + 1, key1),
+                         lut::get(w, j0 + 1, key2));
+    }
+  } else {
+    const uint32_t w2s = r.w[2] >> 2;
+    const uint32_t X0 = bitsel(r.w[0], r.w[2], 0x0F0F0F0Fu), X1 = bitsel(r.w[2], r.w[0], 0x0F0F0F0Fu);
+    const uint32_t X2 = bitsel(r.w[1], w2s, 0x0F0F0F0Fu), X3 = bitsel(w2s, r.w[1], 0x0F0F0F0Fu);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t xe = q < 2 ? X0 : X2, xo = q < 2 ? X1 : X3;
+      const int j0 = 2 * (q & 1);
+      ch[q] = make_uint4(lut::get(xe, j0, key1), lut::get(xo, j0, key2), lut::get(xe, j0 + 1, key1),
+                         lut::get(xo, j0 + 1, key2));
+    }
+  }
+}
+
+// ---- V~^T rows: 16 dims (half hh of a 32-dim group) of a token pair (A, B) -> 16 half2 ----
+// out[i] = (c[A's code of dim 16 hh + i], c[B's]).  Index bytes interleave the two tokens' codes
+// of one dim.  4-bit: XE = A | B << 4 per nibble pair gives dims 2k (T4), XO dims 2k + 1.
+// 2-bit: XE byte k gives dims 4k (U1) and 4k + 1 (U2), XO dims 4k + 2, 4k + 3.  3-bit: with E / O
+// the two tokens' low bits of even / odd dims and M / M2 their high bits, XE1 (T1), XO1 (T1), XE2
+// (T2), XO2 (T2) byte k give dims 4k, 4k + 1, 4k + 2, 4k + 3.
+template <int BITS>
+__device__ __forceinline__ void v_pairs(uint32_t (&out)[16], const GroupRaw& A, const GroupRaw& B, int hh,
+                                        uint32_t key1, uint32_t key2) {
+  if constexpr (BITS == 4) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t a = A.w[2 * hh + u], b = B.w[2 * hh + u];
+      const uint32_t XE = bitsel(a, b << 4, 0x0F0F0F0Fu), XO = bitsel(a >> 4, b, 0x0F0F0F0Fu);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        out[8 * u + 2 * k] = lut::get(XE, k, key1);
+        out[8 * u + 2 * k + 1] = lut::get(XO, k, key1);
+      }
+    }
+  } else if constexpr (BITS == 2) {
+    const uint32_t a = A.w[hh], b = B.w[hh];
+    const uint32_t XE = bitsel(a, b << 4, 0x0F0F0F0Fu), XO = bitsel(a >> 4, b, 0x0F0F0F0Fu);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      out[4 * k] = lut::get(XE, k, key1);
+      out[4 * k + 1] = lut::get(XE, k, key2);
+      out[4 * k + 2] = lut::get(XO, k, key1);
+      out[4 * k + 3] = lut::get(XO, k, key2);
+    }
+  } else {
+    const int sh = 2 * hh;
+    const uint32_t a = A.w[hh], b = B.w[hh], a2 = A.w[2], b2 = B.w[2];
+    const uint32_t E = bitsel(a, b << 2, 0x33333333u), O = bitsel(a >> 2, b, 0x33333333u);
+    const uint32_t M = bitsel(a2, b2 << 1, 0x55555555u) >> sh, M2 = bitsel(a2 >> 1, b2, 0x55555555u) >> sh;
+    const uint32_t XE1 = bitsel(E, M, 0x0F0F0F0Fu), XE2 = bitsel(M, E, 0x0F0F0F0Fu);
+    const uint32_t XO1 = bitsel(O, M2, 0x0F0F0F0Fu), XO2 = bitsel(M2, O, 0x0F0F0F0Fu);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      out[4 * k] = lut::get(XE1, k, key1);
+      out[4 * k + 1] = lut::get(XO1, k, key1);
+      out[4 * k + 2] = lut::get(XE2, k, key2);
+      out[4 * k + 3] = lut::get(XO2, k, key2);
+    }
   }
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kXThreads, 2)
-extend_kernel(const Geometry g, const AttnArgs a) {
+__global__ void __launch_bounds__(kXThreads, 1)
+extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* const sm = smem_raw + (base - raw);
-  float* const nk = reinterpret_cast<float*>(sm + kXNk);
-  float* const nv = reinterpret_cast<float*>(sm + kXNv);
-  __half* const cb16 = reinterpret_cast<__half*>(sm + kXCb);
+  const XPlan pl = x_plan(raw);
+  if (pl.end - raw > (uint32_t)smem_bytes) {  // unexpected reserved shared memory
+    if (threadIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
+    return;
+  }
+  auto at = [&](uint32_t addr) { return smem_raw + (addr - raw); };
+  float* const nk = reinterpret_cast<float*>(at(pl.misc));
+  float* const nv = nk + 64;
+  float* const cb = nk + 128;
+  const uint32_t bar_s = pl.misc + 576, bar_o = pl.misc + 584, tmem_slot = pl.misc + 592;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int blk = warp >> 2;  // row block of this thread
   const int n_rb = (a.rows + kXRows - 1) / kXRows;
   const int rb = n_rb - 1 - (int)(blockIdx.x % n_rb);  // latest rows (longest reach) first
   const int h = (blockIdx.x / n_rb) % g.num_kv_heads;
@@ -214,8 +325,7 @@ extend_kernel(const Geometry g, const AttnArgs a) {
     if (rb == n_rb - 1 && h == 0 && tid == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_LEN);
     len = len < 0 ? 0 : (len > cap ? cap : len);
   }
-  if (tid < (1 << BITS)) cb16[tid] = __float2half_rn(g.centroids[tid]);
-  const uint32_t bar_s = base + kXBar, bar_o = base + kXBar + 8;
+  if (tid < (1 << BITS)) cb[tid] = g.centroids[tid];
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_s) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_o) : "memory");
@@ -223,13 +333,12 @@ extend_kernel(const Geometry g, const AttnArgs a) {
   }
   __syncwarp();  // tcgen05.alloc is warp-collective
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + kXTmemSlot),
-                 "r"(kXTmemCols)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(kXTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
 
-  // ---- q~ = R_k q * sm_scale * log2(e) of row r, fp16, into the A operand of S ----
+  // ---- q~ = R_k q * sm_scale * log2(e) of row r, fp16, into the A operand of its block ----
   const int r = rb * kXRows + tid;
   {
     const bool valid = r < a.rows;
@@ -237,6 +346,8 @@ extend_kernel(const Geometry g, const AttnArgs a) {
     const uint4* qrow = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(a.q) +
                                                        (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
     const float4* rk = reinterpret_cast<const float4*>(g.rot_k + (size_t)h * kHeadDim);
+    uint8_t* const qs = at(blk ? pl.q[1] : pl.q[0]);
+    const int row = tid & (kXBlock - 1);
 #pragma unroll 4
     for (int c = 0; c < 16; ++c) {  // dims 8c .. 8c + 7: two rotation blocks of 4
       uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -244,10 +355,10 @@ extend_kernel(const Geometry g, const AttnArgs a) {
         const uint4 raw8 = __ldg(qrow + c);
         const uint32_t hw[4] = {raw8.x, raw8.y, raw8.z, raw8.w};
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * blk]));
-          const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * blk + 1]));
-          const float4 p = __ldg(rk + 2 * c + blk);
+        for (int bk = 0; bk < 2; ++bk) {
+          const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * bk]));
+          const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * bk + 1]));
+          const float4 p = __ldg(rk + 2 * c + bk);
           float y[4];
           if (g.mode == RQ_PLANAR) {
             y[0] = p.x * x01.x - p.y * x01.y;
@@ -260,59 +371,55 @@ extend_kernel(const Geometry g, const AttnArgs a) {
             y[2] = p.z * x01.x + p.w * x01.y + p.x * x23.x - p.y * x23.y;
             y[3] = p.w * x01.x - p.z * x01.y + p.y * x23.x + p.x * x23.y;
           }
-          w[2 * blk] = pack_h2(y[0] * g.q_scale, y[1] * g.q_scale);
-          w[2 * blk + 1] = pack_h2(y[2] * g.q_scale, y[3] * g.q_scale);
+          const int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;  // the K~ order of a 4-dim block
+          w[2 * bk] = pack_h2(y[0] * g.q_scale, y[s1] * g.q_scale);
+          w[2 * bk + 1] = pack_h2(y[s2] * g.q_scale, y[3] * g.q_scale);
         }
       }
-      *reinterpret_cast<uint4*>(sm + kXQ + (c >> 3) * 16384 + xswz(tid, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + xswz(row, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+  __syncthreads();  // the centroids are staged
+  lut::fill<BITS>(reinterpret_cast<uint32_t*>(at(pl.lut)), cb, tid, kXThreads);
+  const uint32_t key1 = lut::key(pl.lut, lane, 0), key2 = lut::key(pl.lut, lane, 1);
 
-  // row r sees positions <= qpos (-1: nothing, or not a row); the block's rows see < kv_end
+  // row r sees positions <= qpos (-1: nothing, or not a row); the CTA's rows see < kv_end
   const int qpos = r < a.rows ? len - a.T + r / g.group : -1;
   const int r_last = min(a.rows, (rb + 1) * kXRows) - 1;
   const int kv_end = min(len, len - a.T + r_last / g.group + 1);
   const int n_tiles = kv_end > 0 ? (kv_end + kXTok - 1) / kXTok : 0;
   const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
 
-  // K~ of a tile: thread (token tid % 64, dims 64 (tid / 64) ..) -> 8 16-byte chunks of a row.
-  // V~^T of a tile: warp w takes dims 32w .. 32w + 31 (code group w), lane p the token pair
-  // (2p, 2p + 1), stored as one half2 per dim row -- a warp writes 128 consecutive bytes a row.
-  // The code words are loaded into registers a tile ahead of their dequantisation.
-  GroupRaw kr0, kr1, vr0, vr1;
-  auto load_k = [&](int t0) {
-    const int tok = tid & 63, half = tid >> 6;
-    load_group<BITS>(kr0, g, a, bt, h, t0 + tok, len, 0, 2 * half);
-    load_group<BITS>(kr1, g, a, bt, h, t0 + tok, len, 0, 2 * half + 1);
-  };
+  // K~ of a tile: thread (token tid % 64, code group tid / 64) -> 4 chunks of a row.  V~^T:
+  // warp w takes dims 16w .. 16w + 15 (half w % 2 of code group w / 2), lane p the token pair
+  // (2p, 2p + 1), one half2 per dim row -- a warp writes 128 consecutive bytes a row.  Code
+  // words are loaded into registers a tile ahead of their dequantisation.
+  const int ktok = tid & 63, kgrp = tid >> 6;
+  GroupRaw kr, vr0, vr1;
+  auto load_k = [&](int t0) { load_group<BITS>(kr, g, a, bt, h, t0 + ktok, len, 0, kgrp); };
   auto load_v = [&](int t0) {
-    load_group<BITS>(vr0, g, a, bt, h, t0 + 2 * lane, len, 1, warp);
-    load_group<BITS>(vr1, g, a, bt, h, t0 + 2 * lane + 1, len, 1, warp);
+    load_group<BITS>(vr0, g, a, bt, h, t0 + 2 * lane, len, 1, warp >> 1);
+    load_group<BITS>(vr1, g, a, bt, h, t0 + 2 * lane + 1, len, 1, warp >> 1);
   };
   auto store_k = [&]() {
-    const int tok = tid & 63, half = tid >> 6;
-    uint8_t* const atom = sm + kXK + half * 8192;
+    uint4 ch[4];
+    k_chunks<BITS>(ch, kr, key1, key2);
+    uint8_t* const atom = at(pl.k) + (kgrp >> 1) * 8192;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const GroupRaw& gr = c < 4 ? kr0 : kr1;
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        w[e] = pack_hh(cb16[group_code<BITS>(gr, 8 * (c & 3) + 2 * e)], cb16[group_code<BITS>(gr, 8 * (c & 3) + 2 * e + 1)]);
-      *reinterpret_cast<uint4*>(atom + xswz(tok, c)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    if (half == 0) nk[tok] = __half2float(__ushort_as_half((unsigned short)kr0.norm));
+    for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(atom + xswz(ktok, 4 * (kgrp & 1) + q)) = ch[q];
+    if (kgrp == 0) nk[ktok] = __half2float(__ushort_as_half((unsigned short)kr.norm));
   };
   auto store_v = [&]() {
-    const int grp = warp, p = lane;
-    uint8_t* const atom = sm + kXV;
+    uint32_t pv[16];
+    v_pairs<BITS>(pv, vr0, vr1, warp & 1, key1, key2);
+    uint8_t* const vt = at(pl.v);
+    const int p = lane;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int row = 32 * grp + i;
-      *reinterpret_cast<uint32_t*>(atom + row * 128 + (((p >> 2) ^ (row & 7)) << 4) + 4 * (p & 3)) =
-          pack_hh(cb16[group_code<BITS>(vr0, i)], cb16[group_code<BITS>(vr1, i)]);
+    for (int i = 0; i < 16; ++i) {
+      const int row = 16 * warp + i;
+      *reinterpret_cast<uint32_t*>(vt + row * 128 + (((p >> 2) ^ (row & 7)) << 4) + 4 * (p & 3)) = pv[i];
     }
-    if (grp == 0) {
+    if (warp == 0) {
       nv[2 * p] = __half2float(__ushort_as_half((unsigned short)vr0.norm));
       nv[2 * p + 1] = __half2float(__ushort_as_half((unsigned short)vr1.norm));
     }
@@ -320,33 +427,38 @@ extend_kernel(const Geometry g, const AttnArgs a) {
 
   fence_async_smem();
   fence_before_sync();
-  __syncthreads();  // q~, centroids, barriers and the tensor-memory address are in place
+  __syncthreads();  // q~, the code table, barriers and the tensor-memory address are in place
   fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kXTmemSlot);
-  const uint32_t tmem_o = tmem, tmem_s = tmem + 128;
-  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;  // the warp's 32 lanes of tensor memory
-  const uint32_t id_s = idesc_f16(kXRows, kXTok), id_o = idesc_f16(kXRows, kHeadDim);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(at(tmem_slot));
+  const uint32_t tmem_o = tmem + 128 * blk, tmem_s = tmem + 256 + 64 * blk;  // this thread's block
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;              // the warp's 32 lanes
+  const uint32_t id_s = idesc_f16(kXBlock, kXTok), id_o = idesc_f16(kXBlock, kHeadDim);
   int n_s = 0, n_o = 0;        // MMA groups issued (thread 0) ...
   int seen_s = 0, seen_o = 0;  // ... and seen complete
   bool alive = true;
 
-  auto issue_s = [&]() {  // S = q~ K~^T: 8 K-steps of 16 dims (4 per atom, 32 bytes apart)
+  auto issue_s = [&]() {  // S_b = q~_b K~^T: 8 K-steps of 16 dims (4 per atom, 32 bytes apart)
     if (tid == 0) {
       fence_after_sync();
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        umma_f16(tmem_s, sdesc(base + kXQ + (ks >> 2) * 16384 + (ks & 3) * 32),
-                 sdesc(base + kXK + (ks >> 2) * 8192 + (ks & 3) * 32), id_s, ks > 0);
+      for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_f16(tmem + 256 + 64 * bb, sdesc((bb ? pl.q[1] : pl.q[0]) + (ks >> 2) * 16384 + (ks & 3) * 32),
+                   sdesc(pl.k + (ks >> 2) * 8192 + (ks & 3) * 32), id_s, ks > 0);
       umma_commit(bar_s);
       ++n_s;
     }
   };
-  auto issue_o = [&](bool accumulate) {  // O~ += P' V~: 4 K-steps of 16 tokens
+  auto issue_o = [&](bool accumulate) {  // O~_b += P'_b V~: 4 K-steps of 16 tokens
     if (tid == 0) {
       fence_after_sync();
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma_f16(tmem_o, sdesc(base + kXP + ks * 32), sdesc(base + kXV + ks * 32), id_o, accumulate || ks > 0);
+      for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_f16(tmem + 128 * bb, sdesc((bb ? pl.p[1] : pl.p[0]) + ks * 32), sdesc(pl.v + ks * 32), id_o,
+                   accumulate || ks > 0);
       umma_commit(bar_o);
       ++n_o;
     }
@@ -397,6 +509,7 @@ extend_kernel(const Geometry g, const AttnArgs a) {
       for (int i = 0; i < 16; ++i) s[16 * c + i] = v[i];
     }
     tmem_wait_ld();
+    const bool interior = t0 + kXTok - 1 <= qpos;  // no masked position in this row's tile
     float tmax = -CUDART_INF_F;
 #pragma unroll
     for (int c = 0; c < kXTok / 4; ++c) {
@@ -405,7 +518,8 @@ extend_kernel(const Geometry g, const AttnArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int jj = 4 * c + i;
-        const float v = t0 + jj > qpos ? -CUDART_INF_F : s[jj] * nn[i];
+        float v = s[jj] * nn[i];
+        if (!interior && t0 + jj > qpos) v = -CUDART_INF_F;
         s[jj] = v;
         tmax = fmaxf(tmax, v);
       }
@@ -427,9 +541,10 @@ extend_kernel(const Geometry g, const AttnArgs a) {
     }
     l_run = l_run * alpha + lsum;
     m_run = m_new;
+    uint8_t* const ps = at(blk ? pl.p[1] : pl.p[0]);
 #pragma unroll
     for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(sm + kXP + xswz(tid, c)) =
+      *reinterpret_cast<uint4*>(ps + xswz(tid & (kXBlock - 1), c)) =
           make_uint4(pack_h2(s[8 * c], s[8 * c + 1]), pack_h2(s[8 * c + 2], s[8 * c + 3]),
                      pack_h2(s[8 * c + 4], s[8 * c + 5]), pack_h2(s[8 * c + 6], s[8 * c + 7]));
     // O~ *= alpha where some row's running max moved (never before the first P'V~)
@@ -492,9 +607,9 @@ extend_kernel(const Geometry g, const AttnArgs a) {
       if (store) {
         uint32_t w[8];
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          const float4 p = __ldg(rv + 4 * c + blk);
-          const float y0 = y[4 * blk] * inv, y1 = y[4 * blk + 1] * inv, y2 = y[4 * blk + 2] * inv, y3 = y[4 * blk + 3] * inv;
+        for (int bk = 0; bk < 4; ++bk) {
+          const float4 p = __ldg(rv + 4 * c + bk);
+          const float y0 = y[4 * bk] * inv, y1 = y[4 * bk + 1] * inv, y2 = y[4 * bk + 2] * inv, y3 = y[4 * bk + 3] * inv;
           float x[4];
           if (g.mode == RQ_PLANAR) {
             x[0] = p.x * y0 + p.y * y1;
@@ -507,8 +622,8 @@ extend_kernel(const Geometry g, const AttnArgs a) {
             x[2] = -p.z * y0 - p.w * y1 + p.x * y2 + p.y * y3;
             x[3] = -p.w * y0 + p.z * y1 - p.y * y2 + p.x * y3;
           }
-          w[2 * blk] = pack_h2(x[0], x[1]);
-          w[2 * blk + 1] = pack_h2(x[2], x[3]);
+          w[2 * bk] = pack_h2(x[0], x[1]);
+          w[2 * bk + 1] = pack_h2(x[2], x[3]);
         }
         orow[2 * c] = make_uint4(w[0], w[1], w[2], w[3]);
         orow[2 * c + 1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -538,11 +653,11 @@ cudaError_t launch_extend(const Geometry& g, const AttnArgs& a, cudaStream_t str
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (ev_start) cudaEventRecord(ev_start, stream);
   if (g.bits == 4)
-    extend_kernel<4><<<(unsigned)ctas, kXThreads, kXSmem, stream>>>(g, a);
+    extend_kernel<4><<<(unsigned)ctas, kXThreads, kXSmem, stream>>>(g, a, kXSmem);
   else if (g.bits == 3)
-    extend_kernel<3><<<(unsigned)ctas, kXThreads, kXSmem, stream>>>(g, a);
+    extend_kernel<3><<<(unsigned)ctas, kXThreads, kXSmem, stream>>>(g, a, kXSmem);
   else
-    extend_kernel<2><<<(unsigned)ctas, kXThreads, kXSmem, stream>>>(g, a);
+    extend_kernel<2><<<(unsigned)ctas, kXThreads, kXSmem, stream>>>(g, a, kXSmem);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess && ev_end) cudaEventRecord(ev_end, stream);
   return e;
