@@ -41,16 +41,16 @@ constexpr int kXTok = 64;       // tokens per K/V tile: N of S, K of P'V~
 // c ^ (r % 8), 8-row groups 1024 bytes apart, a second 64-wide K atom after all rows of the first.
 constexpr uint32_t kXQBytes = 32768;   // q~ of a block: 128 rows x 128 dims, two atoms
 constexpr uint32_t kXKBytes = 16384;   // K~: 64 tokens x 128 dims, two atoms of 8 KB
-constexpr uint32_t kXVBytes = 16384;   // V~^T: 128 dims x 64 tokens
+constexpr uint32_t kXVBytes = 16384;   // V~^T: 128 dims x 64 tokens (two: tiles alternate)
 constexpr uint32_t kXPBytes = 16384;   // P' of a block: 128 rows x 64 tokens
-constexpr uint32_t kXMiscBytes = 1024; // K norms f32[64], V norms f32[64], centroids f32[16],
-                                       // two mbarriers, the tensor-memory address
+constexpr uint32_t kXMiscBytes = 2048; // K norms f32[2][64], V norms f32[2][64] (tiles alternate),
+                                       // centroids f32[16], two mbarriers, the tensor-memory address
 constexpr int kXSmem = 232448;         // the whole opt-in window (one CTA per SM)
-constexpr uint32_t kXTmemCols = 512;   // O~_0 [0,128), O~_1 [128,256), S_0 [256,320), S_1 [320,384)
+constexpr uint32_t kXTmemCols = 512;   // O~_b at [128 b, 128 b + 128); S_b of tile t at 256 + 128 (t % 2) + 64 b
 constexpr int kXWaitLimit = 1 << 22;   // bounded mbarrier polling (about a second)
 
 struct XPlan {
-  uint32_t lut, q[2], k, v, p[2], misc, end;  // shared addresses
+  uint32_t lut, q[2], k, v[2], p[2], misc, end;  // shared addresses
 };
 __device__ __forceinline__ XPlan x_plan(uint32_t raw) {
   XPlan pl;
@@ -70,7 +70,8 @@ __device__ __forceinline__ XPlan x_plan(uint32_t raw) {
   pl.q[0] = place(kXQBytes);
   pl.q[1] = place(kXQBytes);
   pl.k = place(kXKBytes);
-  pl.v = place(kXVBytes);
+  pl.v[0] = place(kXVBytes);
+  pl.v[1] = place(kXVBytes);
   pl.p[0] = place(kXPBytes);
   pl.p[1] = place(kXPBytes);
   pl.misc = place(kXMiscBytes);
@@ -262,8 +263,8 @@ __device__ __forceinline__ void v_pairs(uint32_t (&out)[16], const GroupRaw& A, 
                                         uint32_t key1, uint32_t key2) {
   if constexpr (BITS == 4) {
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const uint32_t a = A.w[2 * hh + u], b = B.w[2 * hh + u];
+    for (int u = 0; u < 2; ++u) {  // (selects, not a runtime index: the words stay in registers)
+      const uint32_t a = hh ? A.w[2 + u] : A.w[u], b = hh ? B.w[2 + u] : B.w[u];
       const uint32_t XE = bitsel(a, b << 4, 0x0F0F0F0Fu), XO = bitsel(a >> 4, b, 0x0F0F0F0Fu);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -272,7 +273,7 @@ __device__ __forceinline__ void v_pairs(uint32_t (&out)[16], const GroupRaw& A, 
       }
     }
   } else if constexpr (BITS == 2) {
-    const uint32_t a = A.w[hh], b = B.w[hh];
+    const uint32_t a = hh ? A.w[1] : A.w[0], b = hh ? B.w[1] : B.w[0];
     const uint32_t XE = bitsel(a, b << 4, 0x0F0F0F0Fu), XO = bitsel(a >> 4, b, 0x0F0F0F0Fu);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -283,7 +284,7 @@ __device__ __forceinline__ void v_pairs(uint32_t (&out)[16], const GroupRaw& A, 
     }
   } else {
     const int sh = 2 * hh;
-    const uint32_t a = A.w[hh], b = B.w[hh], a2 = A.w[2], b2 = B.w[2];
+    const uint32_t a = hh ? A.w[1] : A.w[0], b = hh ? B.w[1] : B.w[0], a2 = A.w[2], b2 = B.w[2];
     const uint32_t E = bitsel(a, b << 2, 0x33333333u), O = bitsel(a >> 2, b, 0x33333333u);
     const uint32_t M = bitsel(a2, b2 << 1, 0x55555555u) >> sh, M2 = bitsel(a2 >> 1, b2, 0x55555555u) >> sh;
     const uint32_t XE1 = bitsel(E, M, 0x0F0F0F0Fu), XE2 = bitsel(M, E, 0x0F0F0F0Fu);
@@ -309,10 +310,10 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     return;
   }
   auto at = [&](uint32_t addr) { return smem_raw + (addr - raw); };
-  float* const nk = reinterpret_cast<float*>(at(pl.misc));
-  float* const nv = nk + 64;
-  float* const cb = nk + 128;
-  const uint32_t bar_s = pl.misc + 576, bar_o = pl.misc + 584, tmem_slot = pl.misc + 592;
+  float* const nk2 = reinterpret_cast<float*>(at(pl.misc));  // [tile % 2][64]
+  float* const nv2 = nk2 + 128;                                // [tile % 2][64]
+  float* const cb = nk2 + 256;
+  const uint32_t bar_s = pl.misc + 1088, bar_o = pl.misc + 1096, tmem_slot = pl.misc + 1104;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int blk = warp >> 2;  // row block of this thread
   const int n_rb = (a.rows + kXRows - 1) / kXRows;
@@ -401,18 +402,18 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     load_group<BITS>(vr0, g, a, bt, h, t0 + 2 * lane, len, 1, warp >> 1);
     load_group<BITS>(vr1, g, a, bt, h, t0 + 2 * lane + 1, len, 1, warp >> 1);
   };
-  auto store_k = [&]() {
+  auto store_k = [&](int t) {
     uint4 ch[4];
     k_chunks<BITS>(ch, kr, key1, key2);
     uint8_t* const atom = at(pl.k) + (kgrp >> 1) * 8192;
 #pragma unroll
     for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(atom + xswz(ktok, 4 * (kgrp & 1) + q)) = ch[q];
-    if (kgrp == 0) nk[ktok] = __half2float(__ushort_as_half((unsigned short)kr.norm));
+    if (kgrp == 0) nk2[64 * (t & 1) + ktok] = __half2float(__ushort_as_half((unsigned short)kr.norm));
   };
-  auto store_v = [&]() {
+  auto store_v = [&](int t) {
     uint32_t pv[16];
     v_pairs<BITS>(pv, vr0, vr1, warp & 1, key1, key2);
-    uint8_t* const vt = at(pl.v);
+    uint8_t* const vt = at((t & 1) ? pl.v[1] : pl.v[0]);
     const int p = lane;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -420,8 +421,8 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       *reinterpret_cast<uint32_t*>(vt + row * 128 + (((p >> 2) ^ (row & 7)) << 4) + 4 * (p & 3)) = pv[i];
     }
     if (warp == 0) {
-      nv[2 * p] = __half2float(__ushort_as_half((unsigned short)vr0.norm));
-      nv[2 * p + 1] = __half2float(__ushort_as_half((unsigned short)vr1.norm));
+      nv2[64 * (t & 1) + 2 * p] = __half2float(__ushort_as_half((unsigned short)vr0.norm));
+      nv2[64 * (t & 1) + 2 * p + 1] = __half2float(__ushort_as_half((unsigned short)vr1.norm));
     }
   };
 
@@ -430,35 +431,36 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   __syncthreads();  // q~, the code table, barriers and the tensor-memory address are in place
   fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(at(tmem_slot));
-  const uint32_t tmem_o = tmem + 128 * blk, tmem_s = tmem + 256 + 64 * blk;  // this thread's block
+  const uint32_t tmem_o = tmem + 128 * blk, tmem_s = tmem + 256 + 64 * blk;  // this thread's block (S: + 128 (t % 2))
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;              // the warp's 32 lanes
   const uint32_t id_s = idesc_f16(kXBlock, kXTok), id_o = idesc_f16(kXBlock, kHeadDim);
   int n_s = 0, n_o = 0;        // MMA groups issued (thread 0) ...
   int seen_s = 0, seen_o = 0;  // ... and seen complete
   bool alive = true;
 
-  auto issue_s = [&]() {  // S_b = q~_b K~^T: 8 K-steps of 16 dims (4 per atom, 32 bytes apart)
+  auto issue_s = [&](int t) {  // S_b = q~_b K~^T: 8 K-steps of 16 dims (4 per atom, 32 bytes apart)
     if (tid == 0) {
       fence_after_sync();
 #pragma unroll
       for (int bb = 0; bb < 2; ++bb)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_f16(tmem + 256 + 64 * bb, sdesc((bb ? pl.q[1] : pl.q[0]) + (ks >> 2) * 16384 + (ks & 3) * 32),
+          umma_f16(tmem + 256 + 128 * (t & 1) + 64 * bb, sdesc((bb ? pl.q[1] : pl.q[0]) + (ks >> 2) * 16384 + (ks & 3) * 32),
                    sdesc(pl.k + (ks >> 2) * 8192 + (ks & 3) * 32), id_s, ks > 0);
       umma_commit(bar_s);
       ++n_s;
     }
   };
-  auto issue_o = [&](bool accumulate) {  // O~_b += P'_b V~: 4 K-steps of 16 tokens
+  auto issue_o = [&](int t) {  // O~_b += P'_b V~: 4 K-steps of 16 tokens
     if (tid == 0) {
       fence_after_sync();
+      const uint32_t vt = (t & 1) ? pl.v[1] : pl.v[0];
 #pragma unroll
       for (int bb = 0; bb < 2; ++bb)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_f16(tmem + 128 * bb, sdesc((bb ? pl.p[1] : pl.p[0]) + ks * 32), sdesc(pl.v + ks * 32), id_o,
-                   accumulate || ks > 0);
+          umma_f16(tmem + 128 * bb, sdesc((bb ? pl.p[1] : pl.p[0]) + ks * 32), sdesc(vt + ks * 32), id_o,
+                   t > 0 || ks > 0);
       umma_commit(bar_o);
       ++n_o;
     }
@@ -472,39 +474,46 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     return ok;
   };
 
+  // Per tile t: S(t) was issued before tile t - 1's softmax; now K~(t + 1) and V~(t) are
+  // dequantized, S(t + 1) is issued into the other S columns and runs under this tile's softmax;
+  // P'V~(t - 1) must have finished before P' and O~ are touched; then P'V~(t) is issued.
   float m_run = -CUDART_INF_F, l_run = 0.f;
   if (n_tiles > 0) {
     load_k(0);
     load_v(0);
-    store_k();
+    store_k(0);
     fence_async_smem();
     __syncthreads();
-    issue_s();
+    issue_s(0);
     if (n_tiles > 1) load_k(kXTok);
   }
   for (int t = 0; t < n_tiles; ++t) {
     const int t0 = t * kXTok;
-    bool ok = t == 0 || wait_next(bar_o, seen_o);  // P'V~ of the previous tile done: V~, P', O~ free
+    bool ok = wait_next(bar_s, seen_s);  // S(t) done: K~ free, S(t) readable
     if (!__syncthreads_and(ok)) {
       alive = false;
       break;
     }
     fence_after_sync();
-    store_v();
-    if (t + 1 < n_tiles) load_v(t0 + kXTok);
-    ok = wait_next(bar_s, seen_s);  // S of this tile done
-    if (!__syncthreads_and(ok)) {   // (also: the V norms are visible)
-      alive = false;
-      break;
+    if (t + 1 < n_tiles) {
+      store_k(t + 1);
+      if (t + 2 < n_tiles) load_k(t0 + 2 * kXTok);
     }
-    fence_after_sync();
+    store_v(t);  // into V~^T buffer t % 2, last read by P'V~(t - 2)
+    if (t + 1 < n_tiles) load_v(t0 + kXTok);
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();  // K~(t + 1), V~(t) and the norms in place
+    if (t + 1 < n_tiles) issue_s(t + 1);
 
     // ---- this row's scores: scale by the key norms, mask, online softmax (base 2) ----
+    const float* const nk = nk2 + 64 * (t & 1);
+    const float* const nv = nv2 + 64 * (t & 1);
     float s[kXTok];
 #pragma unroll
     for (int c = 0; c < kXTok / 16; ++c) {
       float v[16];
-      tmem_ld16(tmem_s + lane_off + 16 * c, v);
+      tmem_ld16(tmem_s + 128 * (t & 1) + lane_off + 16 * c, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) s[16 * c + i] = v[i];
     }
@@ -541,6 +550,13 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     }
     l_run = l_run * alpha + lsum;
     m_run = m_new;
+
+    ok = t == 0 || wait_next(bar_o, seen_o);  // P'V~(t - 1) done: P' and O~ free
+    if (!__syncthreads_and(ok)) {
+      alive = false;
+      break;
+    }
+    fence_after_sync();
     uint8_t* const ps = at(blk ? pl.p[1] : pl.p[0]);
 #pragma unroll
     for (int c = 0; c < 8; ++c)
@@ -562,15 +578,8 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     }
     fence_async_smem();
     fence_before_sync();
-    __syncthreads();  // P', V~ written; S read; O~ rescaled
-    issue_o(t > 0);
-    if (t + 1 < n_tiles) {  // the next K~ while P'V~ runs (S is read, K~ and the K norms free)
-      store_k();
-      if (t + 2 < n_tiles) load_k(t0 + 2 * kXTok);
-      fence_async_smem();
-      __syncthreads();
-      issue_s();
-    }
+    __syncthreads();  // P' written, S(t) read, O~ rescaled
+    issue_o(t);
   }
 
   // ---- epilogue: wait for the last P'V~, normalise, rotate back, store ----
