@@ -519,7 +519,10 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     }
     tmem_wait_ld();
     const bool interior = t0 + kXTok - 1 <= qpos;  // no masked position in this row's tile
-    float tmax = -CUDART_INF_F;
+    // max and sum in 8 independent partial chains (few warps per SM: latency, not issue, bounds)
+    float tm[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tm[i] = -CUDART_INF_F;
 #pragma unroll
     for (int c = 0; c < kXTok / 4; ++c) {
       const float4 n4 = reinterpret_cast<const float4*>(nk)[c];
@@ -530,24 +533,29 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         float v = s[jj] * nn[i];
         if (!interior && t0 + jj > qpos) v = -CUDART_INF_F;
         s[jj] = v;
-        tmax = fmaxf(tmax, v);
+        tm[jj & 7] = fmaxf(tm[jj & 7], v);
       }
     }
+    const float tmax = fmaxf(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])), fmaxf(fmaxf(tm[4], tm[5]), fmaxf(tm[6], tm[7])));
     const float m_new = fmaxf(m_run, tmax);
     const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
     const float alpha = ex2(m_run - m_use);
-    float lsum = 0.f;
+    float ls[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ls[i] = 0.f;
 #pragma unroll
     for (int c = 0; c < kXTok / 4; ++c) {
       const float4 n4 = reinterpret_cast<const float4*>(nv)[c];
       const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float pr = ex2(s[4 * c + i] - m_use);  // masked: +0
-        lsum += pr;
-        s[4 * c + i] = pr * nn[i];
+        const int jj = 4 * c + i;
+        const float pr = ex2(s[jj] - m_use);  // masked: +0
+        ls[jj & 7] += pr;
+        s[jj] = pr * nn[i];
       }
     }
+    const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
     l_run = l_run * alpha + lsum;
     m_run = m_new;
 
