@@ -9,18 +9,18 @@
 // Design (sm_103a, 5th-generation tensor cores): one CTA per SM, 8 warps, takes 256 query rows
 // of one (sequence, kv head) -- rows r = j * group + k, thread i owning row i, in two blocks of
 // 128 (warps 0-3 and 4-7) -- and walks the cache in 64-token tiles up to the last position its
-// rows can see.  Per tile the 256 threads dequantize K~ (token-major) and V~^T (dim-major) once
-// for both blocks, into shared memory as fp16 centroid values in the K-major 128-byte-swizzled
-// operand layout: code bytes index a lane-replicated table of centroid pairs (rq_lut.cuh), one
-// shared load per two values.  One thread issues S_b = Q~_b K~^T (tcgen05.mma, M 128 x N 64 x
-// K 128) for both blocks into tensor memory; every thread reads its row of S (tcgen05.ld),
-// scales it by the key norms, masks it and runs the online softmax in base 2 with no
-// cross-thread reduction, then writes P' = p * n_v as fp16; one thread issues
-// O~_b += P'_b V~ (M 128 x N 128 x K 64), accumulated in tensor memory (all 512 columns: O~_0,
-// O~_1, S_0, S_1).  The next tile's K~ is dequantized while P'V~ runs and its V~ while the next
-// S runs, from code words loaded a tile ahead.  Every wait is bounded: a wait that runs out
-// sets RQ_STATUS_TIMEOUT, the CTA stops, waits (bounded) for the MMAs it issued and frees its
-// tensor memory.
+// rows can see.  Per tile the 256 threads dequantize K~ (token-major, centroid values) and
+// V~^T (dim-major, centroid values times the token's value norm) once for both blocks, into
+// shared memory as fp16 in the K-major 128-byte-swizzled operand layout: code bytes index a
+// lane-replicated table of centroid pairs (rq_lut.cuh), one shared load per two values.  One
+// thread issues S_b = Q~_b K~^T (tcgen05.mma, M 128 x N 64 x K 128) for both blocks into
+// tensor memory; every thread reads its row of S (tcgen05.ld), scales it by the key norms,
+// masks it and runs the online softmax in base 2 with no cross-thread reduction, then writes
+// p as fp16; one thread issues O~_b += P_b V~ (M 128 x N 128 x K 64), accumulated in tensor
+// memory (all 512 columns: O~_0, O~_1 and two tiles' S_0, S_1).  S of the next tile runs under
+// this tile's softmax; the next K~ and this V~ are dequantized from code words loaded a tile
+// ahead.  Every wait is bounded: a wait that runs out sets RQ_STATUS_TIMEOUT, the CTA stops,
+// waits (bounded) for the MMAs it issued and frees its tensor memory.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -34,7 +34,7 @@ namespace {
 constexpr int kXThreads = 256;  // thread i owns query row i of the CTA's 256
 constexpr int kXBlock = 128;    // rows per block: M of every MMA
 constexpr int kXRows = 2 * kXBlock;
-constexpr int kXTok = 64;       // tokens per K/V tile: N of S, K of P'V~
+constexpr int kXTok = 64;       // tokens per K/V tile: N of S, K of PV~
 // Shared memory: the 64 KB code table at the first 64 KB-aligned address of the window, the
 // buffers (1024-aligned) below it where they fit, else above it.  MMA operands are K-major with
 // the 128-byte swizzle: 128-byte rows (64 fp16 of K), 16-byte chunk c of row r stored at chunk
@@ -42,12 +42,13 @@ constexpr int kXTok = 64;       // tokens per K/V tile: N of S, K of P'V~
 constexpr uint32_t kXQBytes = 32768;   // q~ of a block: 128 rows x 128 dims, two atoms
 constexpr uint32_t kXKBytes = 16384;   // K~: 64 tokens x 128 dims, two atoms of 8 KB
 constexpr uint32_t kXVBytes = 16384;   // V~^T: 128 dims x 64 tokens (two: tiles alternate)
-constexpr uint32_t kXPBytes = 16384;   // P' of a block: 128 rows x 64 tokens
-constexpr uint32_t kXMiscBytes = 2048; // K norms f32[2][64], V norms f32[2][64] (tiles alternate),
-                                       // centroids f32[16], two mbarriers, the tensor-memory address
+constexpr uint32_t kXPBytes = 16384;   // P of a block: 128 rows x 64 tokens
+constexpr uint32_t kXMiscBytes = 2048; // K norms f32[2][64] (tiles alternate), centroids f32[16] at
+                                       // 1024, two mbarriers, the tensor-memory address
 constexpr int kXSmem = 232448;         // the whole opt-in window (one CTA per SM)
 constexpr uint32_t kXTmemCols = 512;   // O~_b at [128 b, 128 b + 128); S_b of tile t at 256 + 128 (t % 2) + 64 b
 constexpr int kXWaitLimit = 1 << 22;   // bounded mbarrier polling (about a second)
+constexpr float kLazyMax = 8.f;        // running-max slack of the online softmax (log2 units)
 
 struct XPlan {
   uint32_t lut, q[2], k, v[2], p[2], misc, end;  // shared addresses
@@ -165,7 +166,7 @@ __device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t c) {
 // token's fp16 norm, loaded from global memory ahead of use.
 struct GroupRaw {
   uint32_t w[4];  // 4-bit: 4 words (8 codes each); 2-bit: 2 words (16 each); 3-bit: W0, W1, W2
-  uint32_t norm;  // fp16 bits (group 0 only), 0 past the sequence
+  uint32_t norm;  // the token's fp16 norm (bits), 0 past the sequence
 };
 
 // Loads group g of token pos of kind (0 K, 1 V) of the (sequence, kv head) whose page table row
@@ -212,8 +213,7 @@ __device__ __forceinline__ void load_group(GroupRaw& r, const Geometry& g, const
     const uint32_t* gw = reinterpret_cast<const uint32_t*>(sec + off * vb + 12 * grp);
     r.w[0] = __ldg(gw), r.w[1] = __ldg(gw + 1), r.w[2] = __ldg(gw + 2);
   }
-  if (grp == 0)
-    r.norm = __ldg(reinterpret_cast<const uint16_t*>(chunk + (size_t)2 * P * vb + kind * 2 * P + 2 * off));
+  r.norm = __ldg(reinterpret_cast<const uint16_t*>(chunk + (size_t)2 * P * vb + kind * 2 * P + 2 * off));
 }
 
 // ---- K~ rows: one token's 32-dim group -> four 16-byte chunks of 8 fp16 ----
@@ -311,7 +311,6 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   }
   auto at = [&](uint32_t addr) { return smem_raw + (addr - raw); };
   float* const nk2 = reinterpret_cast<float*>(at(pl.misc));  // [tile % 2][64]
-  float* const nv2 = nk2 + 128;                                // [tile % 2][64]
   float* const cb = nk2 + 256;
   const uint32_t bar_s = pl.misc + 1088, bar_o = pl.misc + 1096, tmem_slot = pl.misc + 1104;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -410,19 +409,18 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(atom + xswz(ktok, 4 * (kgrp & 1) + q)) = ch[q];
     if (kgrp == 0) nk2[64 * (t & 1) + ktok] = __half2float(__ushort_as_half((unsigned short)kr.norm));
   };
-  auto store_v = [&](int t) {
+  auto store_v = [&](int t) {  // V~ = n_v * centroid: the norms ride in V~, P = p
     uint32_t pv[16];
     v_pairs<BITS>(pv, vr0, vr1, warp & 1, key1, key2);
     uint8_t* const vt = at((t & 1) ? pl.v[1] : pl.v[0]);
     const int p = lane;
+    const uint32_t nbits = (vr0.norm & 0xFFFFu) | (vr1.norm << 16);
+    const __half2 n2 = *reinterpret_cast<const __half2*>(&nbits);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int row = 16 * warp + i;
-      *reinterpret_cast<uint32_t*>(vt + row * 128 + (((p >> 2) ^ (row & 7)) << 4) + 4 * (p & 3)) = pv[i];
-    }
-    if (warp == 0) {
-      nv2[64 * (t & 1) + 2 * p] = __half2float(__ushort_as_half((unsigned short)vr0.norm));
-      nv2[64 * (t & 1) + 2 * p + 1] = __half2float(__ushort_as_half((unsigned short)vr1.norm));
+      const __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&pv[i]), n2);
+      *reinterpret_cast<__half2*>(vt + row * 128 + (((p >> 2) ^ (row & 7)) << 4) + 4 * (p & 3)) = x;
     }
   };
 
@@ -451,7 +449,7 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       ++n_s;
     }
   };
-  auto issue_o = [&](int t) {  // O~_b += P'_b V~: 4 K-steps of 16 tokens
+  auto issue_o = [&](int t) {  // O~_b += P_b V~: 4 K-steps of 16 tokens
     if (tid == 0) {
       fence_after_sync();
       const uint32_t vt = (t & 1) ? pl.v[1] : pl.v[0];
@@ -476,7 +474,7 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
 
   // Per tile t: S(t) was issued before tile t - 1's softmax; now K~(t + 1) and V~(t) are
   // dequantized, S(t + 1) is issued into the other S columns and runs under this tile's softmax;
-  // P'V~(t - 1) must have finished before P' and O~ are touched; then P'V~(t) is issued.
+  // PV~(t - 1) must have finished before P and O~ are touched; then PV~(t) is issued.
   float m_run = -CUDART_INF_F, l_run = 0.f;
   if (n_tiles > 0) {
     load_k(0);
@@ -499,7 +497,7 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       store_k(t + 1);
       if (t + 2 < n_tiles) load_k(t0 + 2 * kXTok);
     }
-    store_v(t);  // into V~^T buffer t % 2, last read by P'V~(t - 2)
+    store_v(t);  // into V~^T buffer t % 2, last read by PV~(t - 2)
     if (t + 1 < n_tiles) load_v(t0 + kXTok);
     fence_async_smem();
     fence_before_sync();
@@ -508,7 +506,6 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
 
     // ---- this row's scores: scale by the key norms, mask, online softmax (base 2) ----
     const float* const nk = nk2 + 64 * (t & 1);
-    const float* const nv = nv2 + 64 * (t & 1);
     float s[kXTok];
 #pragma unroll
     for (int c = 0; c < kXTok / 16; ++c) {
@@ -537,29 +534,28 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       }
     }
     const float tmax = fmaxf(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])), fmaxf(fmaxf(tm[4], tm[5]), fmaxf(tm[6], tm[7])));
-    const float m_new = fmaxf(m_run, tmax);
-    const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-    const float alpha = ex2(m_run - m_use);
+    // The running max moves only when the tile's max passes it by more than kLazyMax (log2
+    // units): p = 2^(s - m) then stays <= 2^kLazyMax, exact in fp16 and f32, and O~ is rescaled
+    // rarely instead of on most tiles.
+    float alpha = 1.f;
+    if (tmax > m_run + kLazyMax) {
+      alpha = ex2(m_run - tmax);  // 0 while nothing was seen yet
+      m_run = tmax;
+    }
+    const float m_use = m_run == -CUDART_INF_F ? 0.f : m_run;
     float ls[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) ls[i] = 0.f;
 #pragma unroll
-    for (int c = 0; c < kXTok / 4; ++c) {
-      const float4 n4 = reinterpret_cast<const float4*>(nv)[c];
-      const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int jj = 4 * c + i;
-        const float pr = ex2(s[jj] - m_use);  // masked: +0
-        ls[jj & 7] += pr;
-        s[jj] = pr * nn[i];
-      }
+    for (int jj = 0; jj < kXTok; ++jj) {
+      const float pr = ex2(s[jj] - m_use);  // masked: +0
+      ls[jj & 7] += pr;
+      s[jj] = pr;
     }
     const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
     l_run = l_run * alpha + lsum;
-    m_run = m_new;
 
-    ok = t == 0 || wait_next(bar_o, seen_o);  // P'V~(t - 1) done: P' and O~ free
+    ok = t == 0 || wait_next(bar_o, seen_o);  // PV~(t - 1) done: P and O~ free
     if (!__syncthreads_and(ok)) {
       alive = false;
       break;
@@ -571,7 +567,7 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       *reinterpret_cast<uint4*>(ps + xswz(tid & (kXBlock - 1), c)) =
           make_uint4(pack_h2(s[8 * c], s[8 * c + 1]), pack_h2(s[8 * c + 2], s[8 * c + 3]),
                      pack_h2(s[8 * c + 4], s[8 * c + 5]), pack_h2(s[8 * c + 6], s[8 * c + 7]));
-    // O~ *= alpha where some row's running max moved (never before the first P'V~)
+    // O~ *= alpha where some row's running max moved (never before the first PV~)
     if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
       for (int c = 0; c < kHeadDim / 16; ++c) {
@@ -586,11 +582,11 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     }
     fence_async_smem();
     fence_before_sync();
-    __syncthreads();  // P' written, S(t) read, O~ rescaled
+    __syncthreads();  // P written, S(t) read, O~ rescaled
     issue_o(t);
   }
 
-  // ---- epilogue: wait for the last P'V~, normalise, rotate back, store ----
+  // ---- epilogue: wait for the last PV~, normalise, rotate back, store ----
   bool ok = alive && (n_o == 0 || tid != 0 || wait_next(bar_o, seen_o));
   if (tid == 0 && alive && n_tiles > 0 && n_o != seen_o) ok = false;
   ok = __syncthreads_and(ok) && alive;
