@@ -6,21 +6,25 @@
 // hundreds or thousands, where the split-K kernel (which re-reads the cache for every 8 query
 // rows) stops paying.
 //
-// Design (sm_103a, 5th-generation tensor cores): one CTA per SM, 8 warps, takes 256 query rows
-// of one (sequence, kv head) -- rows r = j * group + k, thread i owning row i, in two blocks of
-// 128 (warps 0-3 and 4-7) -- and walks the cache in 64-token tiles up to the last position its
-// rows can see.  Per tile the 256 threads dequantize K~ (token-major, centroid values) and
-// V~^T (dim-major, centroid values times the token's value norm) once for both blocks, into
-// shared memory as fp16 in the K-major 128-byte-swizzled operand layout: code bytes index a
-// lane-replicated table of centroid pairs (rq_lut.cuh), one shared load per two values.  One
-// thread issues S_b = Q~_b K~^T (tcgen05.mma, M 128 x N 64 x K 128) for both blocks into
-// tensor memory; every thread reads its row of S (tcgen05.ld), scales it by the key norms,
-// masks it and runs the online softmax in base 2 with no cross-thread reduction, then writes
-// p as fp16; one thread issues O~_b += P_b V~ (M 128 x N 128 x K 64), accumulated in tensor
-// memory (all 512 columns: O~_0, O~_1 and two tiles' S_0, S_1).  S of the next tile runs under
-// this tile's softmax; the next K~ and this V~ are dequantized from code words loaded a tile
-// ahead.  Every wait is bounded: a wait that runs out sets RQ_STATUS_TIMEOUT, the CTA stops,
-// waits (bounded) for the MMAs it issued and frees its tensor memory.
+// Design (sm_103a, 5th-generation tensor cores): one CTA per SM takes 256 query rows of one
+// (sequence, kv head) -- rows r = j * group + k, in two blocks of 128 -- and walks the cache in
+// 64-token tiles up to the last position its rows can see, with warps specialised by role and
+// coupled only through mbarriers:
+//   dequant (4 warps): per tile, K~ (token-major, centroid, with the key norms beside it; two
+//     stages, a tile ahead) and V~^T (dim-major, centroid times value norm; one buffer) as fp16 in the
+//     K-major 128-byte-swizzled operand layout; code bytes index a lane-replicated table of
+//     centroid pairs (rq_lut.cuh), one shared load per two values; code words load ahead;
+//   MMA (one thread): S_b = Q~_b K~^T (tcgen05.mma, M 128 x N 64 x K 128) for both blocks into
+//     tensor memory one tile ahead, and O~_b += P_b V~ (M 128 x N 128 x K 64) when block b's
+//     P is ready, accumulated in tensor memory (all 512 columns: O~_0, O~_1 and two tiles'
+//     S_0, S_1);
+//   softmax (8 warps, one thread per row, block b = warps 4b .. 4b + 3): reads its row of S
+//     (tcgen05.ld), scales it by the key norms (f32), masks it, runs the online softmax in base
+//     2 with no cross-thread reduction
+//     and writes p as fp16; the running max moves only past a margin, so O~ is rarely
+//     rescaled; at the end it normalises, rotates back and stores its row.
+// Every wait is bounded: one that runs out sets RQ_STATUS_TIMEOUT and an abort flag every role
+// polls; the MMA thread drains what it issued before the tensor memory is freed.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -31,7 +35,11 @@
 namespace rq {
 namespace {
 
-constexpr int kXThreads = 256;  // thread i owns query row i of the CTA's 256
+constexpr int kXSoftWarps = 8;   // warps 0-7: softmax, thread i = row i of the CTA's 256
+constexpr int kXDeqWarps = 4;    // warps 8-11: dequantisation
+constexpr int kXThreads = 32 * (kXSoftWarps + kXDeqWarps + 1);  // + warp 12: MMA issue
+constexpr int kXSoftThreads = 32 * kXSoftWarps, kXDeqThreads = 32 * kXDeqWarps;
+constexpr int kXStages = 2;      // K~ ring (V~^T has one buffer: the shared-memory window)
 constexpr int kXBlock = 128;    // rows per block: M of every MMA
 constexpr int kXRows = 2 * kXBlock;
 constexpr int kXTok = 64;       // tokens per K/V tile: N of S, K of PV~
@@ -41,17 +49,17 @@ constexpr int kXTok = 64;       // tokens per K/V tile: N of S, K of PV~
 // c ^ (r % 8), 8-row groups 1024 bytes apart, a second 64-wide K atom after all rows of the first.
 constexpr uint32_t kXQBytes = 32768;   // q~ of a block: 128 rows x 128 dims, two atoms
 constexpr uint32_t kXKBytes = 16384;   // K~: 64 tokens x 128 dims, two atoms of 8 KB
-constexpr uint32_t kXVBytes = 16384;   // V~^T: 128 dims x 64 tokens (two: tiles alternate)
+constexpr uint32_t kXVBytes = 16384;   // V~^T: 128 dims x 64 tokens
 constexpr uint32_t kXPBytes = 16384;   // P of a block: 128 rows x 64 tokens
-constexpr uint32_t kXMiscBytes = 2048; // K norms f32[2][64] (tiles alternate), centroids f32[16] at
-                                       // 1024, two mbarriers, the tensor-memory address
+constexpr uint32_t kXMiscBytes = 1024; // centroids f32[16], the mbarriers, the tensor-memory
+                                       // address, the abort flag; K norms f32[2][64] at 512
 constexpr int kXSmem = 232448;         // the whole opt-in window (one CTA per SM)
 constexpr uint32_t kXTmemCols = 512;   // O~_b at [128 b, 128 b + 128); S_b of tile t at 256 + 128 (t % 2) + 64 b
 constexpr int kXWaitLimit = 1 << 22;   // bounded mbarrier polling (about a second)
 constexpr float kLazyMax = 8.f;        // running-max slack of the online softmax (log2 units)
 
 struct XPlan {
-  uint32_t lut, q[2], k, v[2], p[2], misc, end;  // shared addresses
+  uint32_t lut, q[2], k[2], v, p[2], misc, end;  // shared addresses
 };
 __device__ __forceinline__ XPlan x_plan(uint32_t raw) {
   XPlan pl;
@@ -70,15 +78,28 @@ __device__ __forceinline__ XPlan x_plan(uint32_t raw) {
   };
   pl.q[0] = place(kXQBytes);
   pl.q[1] = place(kXQBytes);
-  pl.k = place(kXKBytes);
-  pl.v[0] = place(kXVBytes);
-  pl.v[1] = place(kXVBytes);
+  pl.k[0] = place(kXKBytes);
+  pl.k[1] = place(kXKBytes);
+  pl.v = place(kXVBytes);
   pl.p[0] = place(kXPBytes);
   pl.p[1] = place(kXPBytes);
   pl.misc = place(kXMiscBytes);
   pl.end = hi;
   return pl;
 }
+
+// mbarriers in the misc area (arrival counts in brackets)
+constexpr uint32_t kBarKFull = 64;     // [2] K~ stage filled (128 dequant threads)
+constexpr uint32_t kBarKEmpty = 80;    // [2] K~ stage read by S (MMA commit); its norms are read
+                                       // once both blocks have released the tile's S (kBarSEmpty)
+constexpr uint32_t kBarVFull = 208;    // V~^T filled (128 dequant threads)
+constexpr uint32_t kBarVEmpty = 216;   // V~^T read by PV~ (MMA commit)
+constexpr uint32_t kBarSFull = 96;     // [block][2] S ready (MMA commit)
+constexpr uint32_t kBarSEmpty = 128;   // [block][2] S read (128 softmax threads of the block)
+constexpr uint32_t kBarPFull = 160;    // [block] P written, O~ rescaled (128 softmax threads)
+constexpr uint32_t kBarODone = 176;    // [block] PV~ done (MMA commit)
+constexpr uint32_t kBarDrain = 192;    // everything the MMA thread issued is done
+constexpr uint32_t kTmemSlot = 200, kAbortFlag = 204, kKNorms = 512;
 
 __device__ __forceinline__ uint32_t xswz(int row, int chunk) { return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4)); }
 
@@ -109,7 +130,15 @@ __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fenc
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
+__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t addr) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// A role's wait: bounded, and it gives up early once another role has raised the abort flag.
+// Returns false on either; the first to run out raises the flag.
+__device__ __forceinline__ bool role_wait(uint32_t addr, uint32_t parity, volatile int* abort_flag) {
   for (int i = 0; i < kXWaitLimit; ++i) {
     uint32_t ok;
     asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
@@ -117,7 +146,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity
                  : "r"(addr), "r"(parity)
                  : "memory");
     if (ok) return true;
+    if ((i & 255) == 255 && *abort_flag) return false;
   }
+  *abort_flag = 1;
   return false;
 }
 
@@ -310,11 +341,11 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     return;
   }
   auto at = [&](uint32_t addr) { return smem_raw + (addr - raw); };
-  float* const nk2 = reinterpret_cast<float*>(at(pl.misc));  // [tile % 2][64]
-  float* const cb = nk2 + 256;
-  const uint32_t bar_s = pl.misc + 1088, bar_o = pl.misc + 1096, tmem_slot = pl.misc + 1104;
+  float* const cb = reinterpret_cast<float*>(at(pl.misc));
+  float* const knorm = reinterpret_cast<float*>(at(pl.misc + kKNorms));  // [stage][64]
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(at(pl.misc + kAbortFlag));
+  const uint32_t mb = pl.misc;  // barrier base
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int blk = warp >> 2;  // row block of this thread
   const int n_rb = (a.rows + kXRows - 1) / kXRows;
   const int rb = n_rb - 1 - (int)(blockIdx.x % n_rb);  // latest rows (longest reach) first
   const int h = (blockIdx.x / n_rb) % g.num_kv_heads;
@@ -327,27 +358,47 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   }
   if (tid < (1 << BITS)) cb[tid] = g.centroids[tid];
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_s) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_o) : "memory");
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(mb + kBarKFull + 8 * i, kXDeqThreads);
+      mbar_init(mb + kBarKEmpty + 8 * i, 1);
+      mbar_init(mb + kBarPFull + 8 * i, kXBlock);
+      mbar_init(mb + kBarODone + 8 * i, 1);
+      for (int j = 0; j < 2; ++j) {
+        mbar_init(mb + kBarSFull + 16 * i + 8 * j, 1);
+        mbar_init(mb + kBarSEmpty + 16 * i + 8 * j, kXBlock);
+      }
+    }
+    mbar_init(mb + kBarDrain, 1);
+    mbar_init(mb + kBarVFull, kXDeqThreads);
+    mbar_init(mb + kBarVEmpty, 1);
+    *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();  // tcgen05.alloc is warp-collective
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(kXTmemCols)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(mb + kTmemSlot),
+                 "r"(kXTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
 
+  // row r sees positions <= qpos (-1: nothing, or not a row); the CTA's rows see < kv_end
+  const int r_last = min(a.rows, (rb + 1) * kXRows) - 1;
+  const int kv_end = min(len, len - a.T + r_last / g.group + 1);
+  const int n_tiles = kv_end > 0 ? (kv_end + kXTok - 1) / kXTok : 0;
+  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
+  const int blk = (warp >> 2) & 1;                    // softmax: row block
+  const int brow = 32 * (warp & 3) + lane;            // softmax: row within the block (= lane of tensor memory)
+  const int r = rb * kXRows + kXBlock * blk + brow;   // softmax: query row
+
   // ---- q~ = R_k q * sm_scale * log2(e) of row r, fp16, into the A operand of its block ----
-  const int r = rb * kXRows + tid;
-  {
+  if (warp < kXSoftWarps) {
     const bool valid = r < a.rows;
     const int j = valid ? r / g.group : 0, head = h * g.group + (valid ? r % g.group : 0);
     const uint4* qrow = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(a.q) +
                                                        (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
     const float4* rk = reinterpret_cast<const float4*>(g.rot_k + (size_t)h * kHeadDim);
     uint8_t* const qs = at(blk ? pl.q[1] : pl.q[0]);
-    const int row = tid & (kXBlock - 1);
 #pragma unroll 4
     for (int c = 0; c < 16; ++c) {  // dims 8c .. 8c + 7: two rotation blocks of 4
       uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -376,272 +427,289 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           w[2 * bk + 1] = pack_h2(y[s2] * g.q_scale, y[3] * g.q_scale);
         }
       }
-      *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + xswz(row, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + xswz(brow, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
-  __syncthreads();  // the centroids are staged
+  __syncthreads();  // the centroids are staged, the barriers initialised
   lut::fill<BITS>(reinterpret_cast<uint32_t*>(at(pl.lut)), cb, tid, kXThreads);
   const uint32_t key1 = lut::key(pl.lut, lane, 0), key2 = lut::key(pl.lut, lane, 1);
-
-  // row r sees positions <= qpos (-1: nothing, or not a row); the CTA's rows see < kv_end
-  const int qpos = r < a.rows ? len - a.T + r / g.group : -1;
-  const int r_last = min(a.rows, (rb + 1) * kXRows) - 1;
-  const int kv_end = min(len, len - a.T + r_last / g.group + 1);
-  const int n_tiles = kv_end > 0 ? (kv_end + kXTok - 1) / kXTok : 0;
-  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
-
-  // K~ of a tile: thread (token tid % 64, code group tid / 64) -> 4 chunks of a row.  V~^T:
-  // warp w takes dims 16w .. 16w + 15 (half w % 2 of code group w / 2), lane p the token pair
-  // (2p, 2p + 1), one half2 per dim row -- a warp writes 128 consecutive bytes a row.  Code
-  // words are loaded into registers a tile ahead of their dequantisation.
-  const int ktok = tid & 63, kgrp = tid >> 6;
-  GroupRaw kr, vr0, vr1;
-  auto load_k = [&](int t0) { load_group<BITS>(kr, g, a, bt, h, t0 + ktok, len, 0, kgrp); };
-  auto load_v = [&](int t0) {
-    load_group<BITS>(vr0, g, a, bt, h, t0 + 2 * lane, len, 1, warp >> 1);
-    load_group<BITS>(vr1, g, a, bt, h, t0 + 2 * lane + 1, len, 1, warp >> 1);
-  };
-  auto store_k = [&](int t) {
-    uint4 ch[4];
-    k_chunks<BITS>(ch, kr, key1, key2);
-    uint8_t* const atom = at(pl.k) + (kgrp >> 1) * 8192;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(atom + xswz(ktok, 4 * (kgrp & 1) + q)) = ch[q];
-    if (kgrp == 0) nk2[64 * (t & 1) + ktok] = __half2float(__ushort_as_half((unsigned short)kr.norm));
-  };
-  auto store_v = [&](int t) {  // V~ = n_v * centroid: the norms ride in V~, P = p
-    uint32_t pv[16];
-    v_pairs<BITS>(pv, vr0, vr1, warp & 1, key1, key2);
-    uint8_t* const vt = at((t & 1) ? pl.v[1] : pl.v[0]);
-    const int p = lane;
-    const uint32_t nbits = (vr0.norm & 0xFFFFu) | (vr1.norm << 16);
-    const __half2 n2 = *reinterpret_cast<const __half2*>(&nbits);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int row = 16 * warp + i;
-      const __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&pv[i]), n2);
-      *reinterpret_cast<__half2*>(vt + row * 128 + (((p >> 2) ^ (row & 7)) << 4) + 4 * (p & 3)) = x;
-    }
-  };
-
   fence_async_smem();
   fence_before_sync();
-  __syncthreads();  // q~, the code table, barriers and the tensor-memory address are in place
+  __syncthreads();  // q~, the code table and the tensor-memory address are in place
   fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(at(tmem_slot));
-  const uint32_t tmem_o = tmem + 128 * blk, tmem_s = tmem + 256 + 64 * blk;  // this thread's block (S: + 128 (t % 2))
-  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;              // the warp's 32 lanes
-  const uint32_t id_s = idesc_f16(kXBlock, kXTok), id_o = idesc_f16(kXBlock, kHeadDim);
-  int n_s = 0, n_o = 0;        // MMA groups issued (thread 0) ...
-  int seen_s = 0, seen_o = 0;  // ... and seen complete
-  bool alive = true;
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(at(mb + kTmemSlot));
 
-  auto issue_s = [&](int t) {  // S_b = q~_b K~^T: 8 K-steps of 16 dims (4 per atom, 32 bytes apart)
-    if (tid == 0) {
+  if (warp < kXSoftWarps) {
+    // ================= softmax: one thread per row of block blk =================
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t tmem_o = tmem + lane_off + 128 * blk;
+    const int qpos = r < a.rows ? len - a.T + r / g.group : -1;
+    float m_run = -CUDART_INF_F, l_run = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n_tiles && ok; ++t) {
+      const int t0 = t * kXTok, i = t & 1;
+      ok = __all_sync(0xffffffffu, role_wait(mb + kBarSFull + 16 * blk + 8 * i, (uint32_t)((t >> 1) & 1), abort_flag));
+      if (!ok) break;
       fence_after_sync();
+      float s[kXTok];
 #pragma unroll
-      for (int bb = 0; bb < 2; ++bb)
+      for (int c = 0; c < kXTok / 16; ++c) {
+        float v[16];
+        tmem_ld16(tmem + lane_off + 256 + 128 * i + 64 * blk + 16 * c, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) s[16 * c + k] = v[k];
+      }
+      tmem_wait_ld();
+      {  // key norms of the tile (stage t % 2)
+        const float4* n4 = reinterpret_cast<const float4*>(knorm + 64 * (t % kXStages));
+#pragma unroll
+        for (int c = 0; c < kXTok / 4; ++c) {
+          const float4 nn = n4[c];
+          s[4 * c] *= nn.x;
+          s[4 * c + 1] *= nn.y;
+          s[4 * c + 2] *= nn.z;
+          s[4 * c + 3] *= nn.w;
+        }
+      }
+      fence_before_sync();
+      mbar_arrive(mb + kBarSEmpty + 16 * blk + 8 * i);  // this S buffer and the tile's norms may be reused
+      if (!(t0 + kXTok - 1 <= qpos)) {  // mask what the row may not see
+#pragma unroll
+        for (int jj = 0; jj < kXTok; ++jj)
+          if (t0 + jj > qpos) s[jj] = -CUDART_INF_F;
+      }
+      float tm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) tm[k] = s[k];
+#pragma unroll
+      for (int jj = 8; jj < kXTok; ++jj) tm[jj & 7] = fmaxf(tm[jj & 7], s[jj]);
+      const float tmax = fmaxf(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])), fmaxf(fmaxf(tm[4], tm[5]), fmaxf(tm[6], tm[7])));
+      // The running max moves only when the tile's max passes it by more than kLazyMax (log2
+      // units): p = 2^(s - m) then stays <= 2^kLazyMax, exact in fp16 and f32, and O~ is
+      // rescaled rarely instead of on most tiles.
+      float alpha = 1.f;
+      if (tmax > m_run + kLazyMax) {
+        alpha = ex2(m_run - tmax);  // 0 while nothing was seen yet
+        m_run = tmax;
+      }
+      const float m_use = m_run == -CUDART_INF_F ? 0.f : m_run;
+      float ls[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < kXTok; ++jj) {
+        const float pr = ex2(s[jj] - m_use);  // masked: +0
+        ls[jj & 7] += pr;
+        s[jj] = pr;
+      }
+      l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+      if (t > 0) {  // PV~(t - 1) of this block done: P free, O~ stable
+        ok = __all_sync(0xffffffffu, role_wait(mb + kBarODone + 8 * blk, (uint32_t)((t - 1) & 1), abort_flag));
+        if (!ok) break;
+        fence_after_sync();
+      }
+      uint8_t* const ps = at(blk ? pl.p[1] : pl.p[0]);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(ps + xswz(brow, c)) =
+            make_uint4(pack_h2(s[8 * c], s[8 * c + 1]), pack_h2(s[8 * c + 2], s[8 * c + 3]),
+                       pack_h2(s[8 * c + 4], s[8 * c + 5]), pack_h2(s[8 * c + 6], s[8 * c + 7]));
+      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // O~ *= alpha (the warp's rows)
+#pragma unroll 1
+        for (int c = 0; c < kHeadDim / 16; ++c) {
+          float v[16];
+          tmem_ld16(tmem_o + 16 * c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] *= alpha;
+          tmem_st16(tmem_o + 16 * c, v);
+        }
+        tmem_wait_st();
+      }
+      fence_async_smem();
+      fence_before_sync();
+      mbar_arrive(mb + kBarPFull + 8 * blk);
+    }
+    // ---- normalise, rotate back, store ----
+    if (ok && n_tiles > 0) {
+      ok = __all_sync(0xffffffffu, role_wait(mb + kBarODone + 8 * blk, (uint32_t)((n_tiles - 1) & 1), abort_flag));
+      if (ok) fence_after_sync();
+    }
+    if (ok) {
+      const bool store = r < a.rows;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const int j = store ? r / g.group : 0, head = h * g.group + (store ? r % g.group : 0);
+      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(a.out) +
+                                             (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
+      const float4* rv = reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim);
+#pragma unroll 1
+      for (int c = 0; c < kHeadDim / 16; ++c) {  // dims 16c .. 16c + 15
+        float y[16];
+        __syncwarp();       // the previous stores diverged by row
+        if (n_tiles > 0) {  // uniform over the CTA
+          tmem_ld16(tmem_o + 16 * c, y);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) y[k] = 0.f;
+        }
+        if (store) {
+          uint32_t w[8];
+#pragma unroll
+          for (int bk = 0; bk < 4; ++bk) {
+            const float4 p = __ldg(rv + 4 * c + bk);
+            const float y0 = y[4 * bk] * inv, y1 = y[4 * bk + 1] * inv, y2 = y[4 * bk + 2] * inv, y3 = y[4 * bk + 3] * inv;
+            float x[4];
+            if (g.mode == RQ_PLANAR) {
+              x[0] = p.x * y0 + p.y * y1;
+              x[1] = -p.y * y0 + p.x * y1;
+              x[2] = p.z * y2 + p.w * y3;
+              x[3] = -p.w * y2 + p.z * y3;
+            } else {  // L(q)^T y
+              x[0] = p.x * y0 + p.y * y1 + p.z * y2 + p.w * y3;
+              x[1] = -p.y * y0 + p.x * y1 + p.w * y2 - p.z * y3;
+              x[2] = -p.z * y0 - p.w * y1 + p.x * y2 + p.y * y3;
+              x[3] = -p.w * y0 + p.z * y1 - p.y * y2 + p.x * y3;
+            }
+            w[2 * bk] = pack_h2(x[0], x[1]);
+            w[2 * bk + 1] = pack_h2(x[2], x[3]);
+          }
+          orow[2 * c] = make_uint4(w[0], w[1], w[2], w[3]);
+          orow[2 * c + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+    }
+    if (!ok && lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
+  } else if (warp < kXSoftWarps + kXDeqWarps) {
+    // ================= dequantisation: K~ a tile ahead of V~^T =================
+    // K~: thread (token dt % 64, code groups dt / 64 and dt / 64 + 2) -> 4 chunks of a row each.
+    // V~^T: warp dw takes dims 32 dw .. 32 dw + 31 (code group dw), lane p the token pair
+    // (2p, 2p + 1), one half2 per dim row -- a warp writes 128 consecutive bytes a row.
+    // Order: K(0); then per tile t: K(t + 1) (stage free once S(t - 1) is done), V(t) (buffer
+    // free once PV~(t - 1) is done) -- so S never waits for a PV~.
+    const int dt = tid - kXSoftThreads, dw = dt >> 5;
+    const int ktok = dt & 63, kg0 = dt >> 6;
+    GroupRaw k0, k1, va, vb;
+    auto load_k = [&](int t0) {
+      load_group<BITS>(k0, g, a, bt, h, t0 + ktok, len, 0, kg0);
+      load_group<BITS>(k1, g, a, bt, h, t0 + ktok, len, 0, kg0 + 2);
+    };
+    auto load_v = [&](int t0) {
+      load_group<BITS>(va, g, a, bt, h, t0 + 2 * lane, len, 1, dw);
+      load_group<BITS>(vb, g, a, bt, h, t0 + 2 * lane + 1, len, 1, dw);
+    };
+    auto produce_k = [&](int t) -> bool {  // K~(t) (centroids) into stage t % 2, its norms beside it
+      const int st = t % kXStages;
+      if (t >= kXStages) {  // S(t - 2) done, and both blocks have read its S and norms
+        const uint32_t par = (uint32_t)((t / kXStages - 1) & 1);
+        bool w = role_wait(mb + kBarKEmpty + 8 * st, par, abort_flag);
+        w = w && role_wait(mb + kBarSEmpty + 8 * st, par, abort_flag);
+        w = w && role_wait(mb + kBarSEmpty + 16 + 8 * st, par, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) return false;
+      }
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+        const int grp = kg0 + 2 * gi;
+        uint4 ch[4];
+        k_chunks<BITS>(ch, gi ? k1 : k0, key1, key2);
+        uint8_t* const atom = at(st ? pl.k[1] : pl.k[0]) + (grp >> 1) * 8192;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(atom + xswz(ktok, 4 * (grp & 1) + q)) = ch[q];
+      }
+      if (dt < 64) knorm[64 * st + ktok] = __half2float(__ushort_as_half((unsigned short)k0.norm));
+      if (t + 1 < n_tiles) load_k((t + 1) * kXTok);
+      fence_async_smem();
+      mbar_arrive(mb + kBarKFull + 8 * st);
+      return true;
+    };
+    auto produce_v = [&](int t) -> bool {  // V~(t)^T = n_v * centroid
+      if (t >= 1 && !__all_sync(0xffffffffu, role_wait(mb + kBarVEmpty, (uint32_t)((t - 1) & 1), abort_flag)))
+        return false;
+      const uint32_t nbits = (va.norm & 0xFFFFu) | (vb.norm << 16);
+      const __half2 n2 = *reinterpret_cast<const __half2*>(&nbits);
+      uint8_t* const vt = at(pl.v);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pv[16];
+        v_pairs<BITS>(pv, va, vb, hh, key1, key2);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int row = 32 * dw + 16 * hh + i;
+          const __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&pv[i]), n2);
+          *reinterpret_cast<__half2*>(vt + row * 128 + (((lane >> 2) ^ (row & 7)) << 4) + 4 * (lane & 3)) = x;
+        }
+      }
+      if (t + 1 < n_tiles) load_v((t + 1) * kXTok);
+      fence_async_smem();
+      mbar_arrive(mb + kBarVFull);
+      return true;
+    };
+    bool ok = true;
+    if (n_tiles > 0) {
+      load_k(0);
+      load_v(0);
+      ok = produce_k(0);
+    }
+    for (int t = 0; t < n_tiles && ok; ++t) {
+      if (t + 1 < n_tiles && !(ok = produce_k(t + 1))) break;
+      ok = produce_v(t);
+    }
+    if (!ok && lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
+  } else if (lane == 0) {
+    // ================= MMA issue (one thread) =================
+    const uint32_t id_s = idesc_f16(kXBlock, kXTok), id_o = idesc_f16(kXBlock, kHeadDim);
+    bool ok = true;
+    int issued = 0;
+    auto issue_s = [&](int t) -> bool {  // S_b(t) = q~_b K~(t)^T into S columns of tile parity t % 2
+      const int st = t % kXStages, i = t & 1;
+      if (!role_wait(mb + kBarKFull + 8 * st, (uint32_t)((t / kXStages) & 1), abort_flag)) return false;
+      const uint32_t kb = st ? pl.k[1] : pl.k[0];
+#pragma unroll 1
+      for (int bb = 0; bb < 2; ++bb) {
+        if (t >= 2 && !role_wait(mb + kBarSEmpty + 16 * bb + 8 * i, (uint32_t)(((t >> 1) - 1) & 1), abort_flag))
+          return false;
+        fence_after_sync();
+        const uint32_t qb = bb ? pl.q[1] : pl.q[0];
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_f16(tmem + 256 + 128 * (t & 1) + 64 * bb, sdesc((bb ? pl.q[1] : pl.q[0]) + (ks >> 2) * 16384 + (ks & 3) * 32),
-                   sdesc(pl.k + (ks >> 2) * 8192 + (ks & 3) * 32), id_s, ks > 0);
-      umma_commit(bar_s);
-      ++n_s;
-    }
-  };
-  auto issue_o = [&](int t) {  // O~_b += P_b V~: 4 K-steps of 16 tokens
-    if (tid == 0) {
-      fence_after_sync();
-      const uint32_t vt = (t & 1) ? pl.v[1] : pl.v[0];
-#pragma unroll
-      for (int bb = 0; bb < 2; ++bb)
+          umma_f16(tmem + 256 + 128 * i + 64 * bb, sdesc(qb + (ks >> 2) * 16384 + (ks & 3) * 32),
+                   sdesc(kb + (ks >> 2) * 8192 + (ks & 3) * 32), id_s, ks > 0);
+        umma_commit(mb + kBarSFull + 16 * bb + 8 * i);
+        ++issued;
+      }
+      umma_commit(mb + kBarKEmpty + 8 * st);  // the stage's K~ has been read
+      return true;
+    };
+    if (n_tiles > 0) ok = issue_s(0);
+    for (int t = 0; t < n_tiles && ok; ++t) {
+      if (t + 1 < n_tiles && !(ok = issue_s(t + 1))) break;  // S(t + 1) runs under softmax(t)
+      if (!(ok = role_wait(mb + kBarVFull, (uint32_t)(t & 1), abort_flag))) break;
+      const uint32_t vb = pl.v;
+#pragma unroll 1
+      for (int bb = 0; bb < 2; ++bb) {
+        if (!(ok = role_wait(mb + kBarPFull + 8 * bb, (uint32_t)(t & 1), abort_flag))) break;
+        fence_after_sync();
+        const uint32_t pb = bb ? pl.p[1] : pl.p[0];
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_f16(tmem + 128 * bb, sdesc((bb ? pl.p[1] : pl.p[0]) + ks * 32), sdesc(vt + ks * 32), id_o,
-                   t > 0 || ks > 0);
-      umma_commit(bar_o);
-      ++n_o;
+          umma_f16(tmem + 128 * bb, sdesc(pb + ks * 32), sdesc(vb + ks * 32), id_o, t > 0 || ks > 0);
+        umma_commit(mb + kBarODone + 8 * bb);
+        ++issued;
+      }
+      if (ok) umma_commit(mb + kBarVEmpty);  // V~^T has been read
     }
-  };
-  // thread 0 waits for the next completion of a barrier; the result reaches every thread at
-  // the following __syncthreads_and
-  auto wait_next = [&](uint32_t bar, int& seen) -> bool {
-    if (tid != 0) return true;
-    const bool ok = mbar_wait_bounded(bar, (uint32_t)(seen & 1));
-    if (ok) ++seen;
-    return ok;
-  };
-
-  // Per tile t: S(t) was issued before tile t - 1's softmax; now K~(t + 1) and V~(t) are
-  // dequantized, S(t + 1) is issued into the other S columns and runs under this tile's softmax;
-  // PV~(t - 1) must have finished before P and O~ are touched; then PV~(t) is issued.
-  float m_run = -CUDART_INF_F, l_run = 0.f;
-  if (n_tiles > 0) {
-    load_k(0);
-    load_v(0);
-    store_k(0);
-    fence_async_smem();
-    __syncthreads();
-    issue_s(0);
-    if (n_tiles > 1) load_k(kXTok);
-  }
-  for (int t = 0; t < n_tiles; ++t) {
-    const int t0 = t * kXTok;
-    bool ok = wait_next(bar_s, seen_s);  // S(t) done: K~ free, S(t) readable
-    if (!__syncthreads_and(ok)) {
-      alive = false;
-      break;
-    }
-    fence_after_sync();
-    if (t + 1 < n_tiles) {
-      store_k(t + 1);
-      if (t + 2 < n_tiles) load_k(t0 + 2 * kXTok);
-    }
-    store_v(t);  // into V~^T buffer t % 2, last read by PV~(t - 2)
-    if (t + 1 < n_tiles) load_v(t0 + kXTok);
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();  // K~(t + 1), V~(t) and the norms in place
-    if (t + 1 < n_tiles) issue_s(t + 1);
-
-    // ---- this row's scores: scale by the key norms, mask, online softmax (base 2) ----
-    const float* const nk = nk2 + 64 * (t & 1);
-    float s[kXTok];
-#pragma unroll
-    for (int c = 0; c < kXTok / 16; ++c) {
-      float v[16];
-      tmem_ld16(tmem_s + 128 * (t & 1) + lane_off + 16 * c, v);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) s[16 * c + i] = v[i];
-    }
-    tmem_wait_ld();
-    const bool interior = t0 + kXTok - 1 <= qpos;  // no masked position in this row's tile
-    // max and sum in 8 independent partial chains (few warps per SM: latency, not issue, bounds)
-    float tm[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) tm[i] = -CUDART_INF_F;
-#pragma unroll
-    for (int c = 0; c < kXTok / 4; ++c) {
-      const float4 n4 = reinterpret_cast<const float4*>(nk)[c];
-      const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int jj = 4 * c + i;
-        float v = s[jj] * nn[i];
-        if (!interior && t0 + jj > qpos) v = -CUDART_INF_F;
-        s[jj] = v;
-        tm[jj & 7] = fmaxf(tm[jj & 7], v);
+    if (issued > 0) {  // drain: nothing may be running when the tensor memory is freed
+      umma_commit(mb + kBarDrain);
+      for (int i = 0; i < kXWaitLimit; ++i) {
+        uint32_t done;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+                     : "=r"(done)
+                     : "r"(mb + kBarDrain), "r"(0u)
+                     : "memory");
+        if (done) break;
       }
     }
-    const float tmax = fmaxf(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])), fmaxf(fmaxf(tm[4], tm[5]), fmaxf(tm[6], tm[7])));
-    // The running max moves only when the tile's max passes it by more than kLazyMax (log2
-    // units): p = 2^(s - m) then stays <= 2^kLazyMax, exact in fp16 and f32, and O~ is rescaled
-    // rarely instead of on most tiles.
-    float alpha = 1.f;
-    if (tmax > m_run + kLazyMax) {
-      alpha = ex2(m_run - tmax);  // 0 while nothing was seen yet
-      m_run = tmax;
-    }
-    const float m_use = m_run == -CUDART_INF_F ? 0.f : m_run;
-    float ls[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ls[i] = 0.f;
-#pragma unroll
-    for (int jj = 0; jj < kXTok; ++jj) {
-      const float pr = ex2(s[jj] - m_use);  // masked: +0
-      ls[jj & 7] += pr;
-      s[jj] = pr;
-    }
-    const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-    l_run = l_run * alpha + lsum;
-
-    ok = t == 0 || wait_next(bar_o, seen_o);  // PV~(t - 1) done: P and O~ free
-    if (!__syncthreads_and(ok)) {
-      alive = false;
-      break;
-    }
-    fence_after_sync();
-    uint8_t* const ps = at(blk ? pl.p[1] : pl.p[0]);
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(ps + xswz(tid & (kXBlock - 1), c)) =
-          make_uint4(pack_h2(s[8 * c], s[8 * c + 1]), pack_h2(s[8 * c + 2], s[8 * c + 3]),
-                     pack_h2(s[8 * c + 4], s[8 * c + 5]), pack_h2(s[8 * c + 6], s[8 * c + 7]));
-    // O~ *= alpha where some row's running max moved (never before the first PV~)
-    if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-      for (int c = 0; c < kHeadDim / 16; ++c) {
-        float v[16];
-        tmem_ld16(tmem_o + lane_off + 16 * c, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] *= alpha;
-        tmem_st16(tmem_o + lane_off + 16 * c, v);
-      }
-      tmem_wait_st();
-    }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();  // P written, S(t) read, O~ rescaled
-    issue_o(t);
-  }
-
-  // ---- epilogue: wait for the last PV~, normalise, rotate back, store ----
-  bool ok = alive && (n_o == 0 || tid != 0 || wait_next(bar_o, seen_o));
-  if (tid == 0 && alive && n_tiles > 0 && n_o != seen_o) ok = false;
-  ok = __syncthreads_and(ok) && alive;
-  if (!ok) {
-    if (tid == 0) {
-      if (a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
-      // never free tensor memory under an MMA still running: wait (bounded) for every group
-      while (seen_s < n_s && mbar_wait_bounded(bar_s, (uint32_t)(seen_s & 1))) ++seen_s;
-      while (seen_o < n_o && mbar_wait_bounded(bar_o, (uint32_t)(seen_o & 1))) ++seen_o;
-    }
-  } else {
-    fence_after_sync();
-    // the tensor-memory loads are warp-collective: every lane takes part, valid rows store
-    const bool store = r < a.rows;
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    const int j = store ? r / g.group : 0, head = h * g.group + (store ? r % g.group : 0);
-    uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(a.out) +
-                                           (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
-    const float4* rv = reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim);
-#pragma unroll 1
-    for (int c = 0; c < kHeadDim / 16; ++c) {  // dims 16c .. 16c + 15
-      float y[16];
-      __syncwarp();       // the previous stores diverged by row
-      if (n_tiles > 0) {  // uniform over the CTA
-        tmem_ld16(tmem_o + lane_off + 16 * c, y);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = 0.f;
-      }
-      if (store) {
-        uint32_t w[8];
-#pragma unroll
-        for (int bk = 0; bk < 4; ++bk) {
-          const float4 p = __ldg(rv + 4 * c + bk);
-          const float y0 = y[4 * bk] * inv, y1 = y[4 * bk + 1] * inv, y2 = y[4 * bk + 2] * inv, y3 = y[4 * bk + 3] * inv;
-          float x[4];
-          if (g.mode == RQ_PLANAR) {
-            x[0] = p.x * y0 + p.y * y1;
-            x[1] = -p.y * y0 + p.x * y1;
-            x[2] = p.z * y2 + p.w * y3;
-            x[3] = -p.w * y2 + p.z * y3;
-          } else {  // L(q)^T y
-            x[0] = p.x * y0 + p.y * y1 + p.z * y2 + p.w * y3;
-            x[1] = -p.y * y0 + p.x * y1 + p.w * y2 - p.z * y3;
-            x[2] = -p.z * y0 - p.w * y1 + p.x * y2 + p.y * y3;
-            x[3] = -p.w * y0 + p.z * y1 - p.y * y2 + p.x * y3;
-          }
-          w[2 * bk] = pack_h2(x[0], x[1]);
-          w[2 * bk + 1] = pack_h2(x[2], x[3]);
-        }
-        orow[2 * c] = make_uint4(w[0], w[1], w[2], w[3]);
-        orow[2 * c + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-    }
+    if (!ok && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
   }
   fence_before_sync();
   __syncthreads();
