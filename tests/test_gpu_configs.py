@@ -11,7 +11,9 @@ the same inputs.  Per sampled sequence:
     groups whose codes hold a near-boundary difference -- there both codes are correct
     decisions, and one flipped code of a dominant token moves the output by more than the
     tolerance, so such groups are reported, not failed.
-Fidelity against attention over the unquantised fp16 cache is reported as cosine similarity."""
+Fidelity against attention over the unquantised fp16 cache is reported as cosine similarity.
+The extend workload (1,024 query rows per sequence) is checked on sampled rows: row j of an
+extend is a decode over the first seq_len - T + j + 1 tokens."""
 import numpy as np
 import pytest
 import torch
@@ -93,30 +95,48 @@ def _check_sequence(bn, b, out_gpu):
     qb = q[b:b + 1] if T > 1 else q[b:b + 1, None]
     bt1 = np.arange(npg, dtype=np.int32)[None]
     len1 = np.array([L], np.int32)
-    ref = oc.attention(qb, bt1, len1, T=T)
+    if bn.extend:
+        # Extend: query row j sees positions 0 .. L - T + j -- a decode over the first L - T + j + 1
+        # tokens -- so the oracle is evaluated on sampled rows only, each as that decode.
+        rows = sorted({0, T // 2, T - 1})
+        ref = np.concatenate([oc.attention(qb[:, j:j + 1], bt1, np.array([L - T + j + 1], np.int32), T=1)
+                              for j in rows], axis=1)
+    else:
+        rows = list(range(T))
+        ref = oc.attention(qb, bt1, len1, T=T)
     # the kernels over the oracle's own pages of this sequence: the same dequantised cache
     one = rq.KVCache(spec.mode, spec.bits, spec.num_q_heads, spec.num_kv_heads, P, npg, wl.rot_k, wl.rot_v,
                      max_batch=1, max_query_tokens=T, max_pages_per_seq=npg, device=bn.device)
     one.pages.copy_(torch.from_numpy(oc.pages.reshape(one.pages.shape)))
     qd, btd, lend = PT.to_dev(qb, bn.device), PT.to_dev(bt1, bn.device), PT.to_dev(len1, bn.device)
-    same = (one.decode(qd[:, 0].contiguous(), btd, lend).unsqueeze(1) if T == 1 else one.verify(qd, btd, lend))
-    same = same.cpu().numpy()
+    if T == 1:
+        same = one.decode(qd[:, 0].contiguous(), btd, lend).unsqueeze(1)
+    elif bn.extend:
+        same = one.extend(qd, btd, lend)
+    else:
+        same = one.verify(qd, btd, lend)
+    same = same.cpu().numpy()[:, rows]
     assert int(one.status.item()) == 0
     one.close()
     err_same = PT.assert_close(same, ref, f"{bn.name} seq {b}, kernels over the oracle's pages")
     # end to end: only kv-head groups holding a near-boundary code may miss
-    got = out_gpu[b:b + 1] if T > 1 else out_gpu[b:b + 1, None]
-    miss = np.abs(got.astype(np.float64) - ref) > PT.ATOL + PT.RTOL * np.abs(ref)   # [1][T][Hq][d]
+    got = (out_gpu[b:b + 1] if T > 1 else out_gpu[b:b + 1, None])[:, rows]
+    miss = np.abs(got.astype(np.float64) - ref) > PT.ATOL + PT.RTOL * np.abs(ref)   # [1][rows][Hq][d]
     miss_heads = {int(hq) // spec.group for hq in np.nonzero(miss.any(axis=(0, 1, 3)))[0]}
     assert miss_heads <= flipped_heads, (bn.name, b, sorted(miss_heads), sorted(flipped_heads))
-    dense = O.attention_dense(qb, k[None], v[None], len1, spec.num_q_heads, spec.num_kv_heads, T=T)
+    if bn.extend:
+        dense = np.concatenate([O.attention_dense(qb[:, j:j + 1], k[None, :L - T + j + 1], v[None, :L - T + j + 1],
+                                                  np.array([L - T + j + 1], np.int32), spec.num_q_heads,
+                                                  spec.num_kv_heads, T=1) for j in rows], axis=1)
+    else:
+        dense = O.attention_dense(qb, k[None], v[None], len1, spec.num_q_heads, spec.num_kv_heads, T=T)
     cos = PT.cosine_per_head(got, dense)
     err_e2e = float(np.abs(got.astype(np.float64) - ref).max())
     return err_same, err_e2e, sorted(miss_heads), in_band, total_codes, float(cos.min()), float(cos.mean())
 
 
 @pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg2", "cfg2_32k", "cfg3", "cfg4", "cfg3_prefill", "tq4_32k",
-                                  "tq2_32k", "tq3_prefill"])
+                                  "tq2_32k", "tq3_prefill", "cfg3_extend"])
 def test_full_size_workload(name, capsys):
     dev = torch.device("cuda", 0)
     bn = bench.Bench(name, dev)
