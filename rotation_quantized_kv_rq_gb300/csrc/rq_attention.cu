@@ -22,9 +22,9 @@
 //     codes (two 4-bit codes, two 3-bit codes assembled from the 3-bit planes, or four 2-bit
 //     codes read as two halves) indexes a half2 entry; each lane reads its own copy of the
 //     entry, so lookups never conflict.
-//   * A decode step can hand the kernel the step's new K/V token of every sequence: each CTA
-//     quantizes the tokens of the units whose last round it holds into the cache before it
-//     stages their pages, so the step needs no separate append launch.
+//   * A decode step can hand the kernel the step's new K/V token of every sequence: the warp
+//     that stages a unit's last tile quantizes the token into the cache before it copies that
+//     tile, so the step needs no separate append launch.
 //   * Dense rotations (TurboQuant) change only the two ends: a small kernel forms R_k q for the
 //     whole call first, and the combine applies R_v^T per (sequence, kv head) group.
 //   * P is moved from the S^T accumulator layout to the B-operand layout with movmatrix.
@@ -96,6 +96,9 @@ struct Walk {
   int n_fin;
   int fin[2];
 };
+constexpr int kWalkBytes = (int)((sizeof(Walk) + 15) / 16 * 16);
+// The tail of the window: page ids, the warps' mbarriers, the centroids and the walk.
+constexpr int kTailBytes = kMaxSplitPages * 4 + kWarps * kStages * 8 + 64 + kWalkBytes;
 
 // The fragment at the walk's position: rounds [r0, r1) of the rb rounds of unit uib of
 // sequence b (uib = kv head * n_tiles_n + n-tile), i.e. its tiles [t0, t1) of tb.
@@ -129,19 +132,13 @@ __host__ __device__ constexpr SmemPlan smem_plan(uint32_t base) {
   p.merge_hi = lo_merge ? p.hi : p.hi + kMergeHalfBytes;
   const uint32_t hi_need = lo_merge ? kMergeHalfBytes : 2 * kMergeHalfBytes;
   p.tail = p.hi + (hi_bytes > hi_need ? hi_bytes : hi_need);
-  p.end = p.tail + kMaxSplitPages * 4 + kWarps * kStages * 8 + 64 + 32;
+  p.end = p.tail + kTailBytes;
   return p;
 }
 
 // ---------------------------------------------------------------------------------------
 // PTX helpers
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
 template <uint32_t LUT>
 __device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -150,12 +147,6 @@ __device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
 }
 // (a & c) | (b & ~c)
 __device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t c) { return lop3<0xE4>(a, b, c); }
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -214,13 +205,6 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
 // Code tables (rq_lut.cuh): T4 / T1 + T2 / U1 + U2 turn an index byte of two codes into the
 // half2 of their centroids with one shared load.
 // ---------------------------------------------------------------------------------------
-template <int BITS>
-__device__ void build_lut(uint32_t* table, const float* centroids, float* cb) {
-  if (threadIdx.x < (1 << BITS)) cb[threadIdx.x] = centroids[threadIdx.x];
-  __syncthreads();
-  lut::fill<BITS>(table, cb, threadIdx.x, kThreads);
-}
-
 // Half2 of the two codes in byte J of index word x (SECOND selects the second table); key1 /
 // key2 are the lane's table keys (lut::key).
 template <int J, int SECOND>
@@ -532,12 +516,18 @@ __device__ __forceinline__ float4 merge_splits(const Geometry& g, const AttnArgs
   return make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
+// The four R_v entries of kv head h for dims d0 & ~3 .. (d0 & ~3) + 3: a Givens pair's (c, s)
+// twice, or the block's quaternion.  Loaded ahead of the merge that needs them.
+__device__ __forceinline__ float4 rot_v_block(const Geometry& g, int h, int d0) {
+  return __ldg(reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim + (d0 & ~3)));
+}
+
 // out = R_v^T o~ for query row `row` of kv head h of sequence b (planar / iso: block-local),
-// the lane's dims 4 lane .. 4 lane + 3, as fp16.  All 32 lanes of the warp call it.
+// the lane's dims 4 lane .. 4 lane + 3, as fp16; p = rot_v_block(g, h, 4 lane).  All 32 lanes of
+// the warp call it.
 __device__ __forceinline__ void store_row(const Geometry& g, const AttnArgs& a, int b, int h, int row, int lane,
-                                          float4 o) {
+                                          float4 o, float4 p) {
   const float y[4] = {o.x, o.y, o.z, o.w};
-  const float4 p = __ldg(reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim) + lane);
   float x[4];
   if (g.mode == RQ_PLANAR) {
     x[0] = p.x * y[0] + p.y * y[1];
@@ -559,20 +549,18 @@ __device__ __forceinline__ void store_row(const Geometry& g, const AttnArgs& a, 
 }
 
 // The same for the two dims d0, d0 + 1 (d0 even) of row `row`, held as (y0, y1) by this lane;
-// with a quaternion rotation the block's other two dims are held by lane ^ 1 (d0 ^ 2).  All 32
-// lanes of the warp call it.
+// with a quaternion rotation the block's other two dims are held by lane ^ 1 (d0 ^ 2).
+// r = rot_v_block(g, h, d0).  All 32 lanes of the warp call it.
 __device__ __forceinline__ void store_pair(const Geometry& g, const AttnArgs& a, int b, int h, int row, int d0,
-                                           float y0, float y1) {
-  const float* rv = g.rot_v + (size_t)h * kHeadDim;
+                                           float y0, float y1, float4 r) {
   const float z0 = __shfl_xor_sync(0xffffffffu, y0, 1), z1 = __shfl_xor_sync(0xffffffffu, y1, 1);
   float x0, x1;
-  if (g.mode == RQ_PLANAR) {
-    const float2 p = __ldg(reinterpret_cast<const float2*>(rv + d0));
-    x0 = p.x * y0 + p.y * y1;
-    x1 = -p.y * y0 + p.x * y1;
+  if (g.mode == RQ_PLANAR) {  // the pair's (c, s): first or second half of the block
+    const float c = (d0 & 2) ? r.z : r.x, sn = (d0 & 2) ? r.w : r.y;
+    x0 = c * y0 + sn * y1;
+    x1 = -sn * y0 + c * y1;
   } else {
-    const float4 q = __ldg(reinterpret_cast<const float4*>(rv + (d0 & ~3)));
-    const float qa = q.x, qb = q.y, qc = q.z, qd = q.w;
+    const float qa = r.x, qb = r.y, qc = r.z, qd = r.w;
     if ((d0 & 2) == 0) {  // own dims 0, 1 of the block; the partner's are 2, 3
       x0 = qa * y0 + qb * y1 + qc * z0 + qd * z1;
       x1 = -qb * y0 + qa * y1 + qd * z0 - qc * z1;
@@ -646,6 +634,32 @@ __device__ __forceinline__ void rotated_query(float (&y)[32], const Geometry& g,
     }
   }
 }
+// The stream-K partition: CTA `cta` of `grid` gets rounds [x0, x1) of `total`.  Parts =
+// min(CTAs, rounds), so that every part is non-empty: the combine takes the CTAs between a
+// unit's first and last fragment to all hold one.  CTAs past the parts idle.  When every unit
+// has the same rounds and there are no more units than CTAs, one whole unit per part is the
+// other candidate: a CTA's cost is its rounds plus kFragmentRounds per fragment, and equal parts
+// that do not divide the units cost most CTAs two fragments.  I is uint32_t whenever
+// total * grid fits it (every practical launch: the 64-bit division is a long software
+// sequence), else long long.
+template <typename I>
+__device__ __forceinline__ void partition(I total, I n_units, I max_rounds, I grid, I cta, long long& x0,
+                                          long long& x1) {
+  I parts = min(grid, total);
+  if (n_units > 0 && n_units <= grid && total == n_units * max_rounds) {
+    const I per_part = (total + parts - 1) / parts;
+    const I cost_split = per_part + (max_rounds % per_part == 0 ? 1 : 2) * (I)kFragmentRounds;
+    if (max_rounds + (I)kFragmentRounds <= cost_split) parts = n_units;
+  }
+  x0 = cta < parts ? (long long)(total * cta / parts) : 0;
+  x1 = cta < parts ? (long long)(total * (cta + 1) / parts) : 0;
+}
+
+// Starts an L2 fill of line `line` (128 bytes) of [p, p + lines * 128), if it exists.
+__device__ __forceinline__ void prefetch_line_l2(const void* p, uint32_t lines, uint32_t line) {
+  if (line < lines) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p) + (size_t)line * 128));
+}
+
 // Sequence b's tokens, clamped to what its block-table row can hold.
 __device__ __forceinline__ int clamp_len(const AttnArgs& a, int b, int cap) {
   const int l = a.seq_lens[b];
@@ -655,6 +669,7 @@ __device__ __forceinline__ int clamp_len(const AttnArgs& a, int b, int cap) {
 // Moves a walk past the fragment f it stands on (thread 0, between fragments).
 __device__ __forceinline__ void walk_advance(Walk& w, const Frag& f, int upb, const AttnArgs& a, int cap) {
   w.x += f.r1 - f.r0;
+  if (w.x >= w.x_end) return;  // the range is done: no next sequence to look up
   if (f.r1 == f.rb && f.uib == upb - 1) {  // sequence b is done: on to the next one with tiles
     w.cumb += (long long)f.rb * upb;
     for (++w.b; w.x < w.x_end && w.b < a.B; ++w.b) {
@@ -665,46 +680,31 @@ __device__ __forceinline__ void walk_advance(Walk& w, const Frag& f, int upb, co
   }
 }
 
-// Decode step: quantizes the newest token (position len - 1) of the kv head of every unit whose
-// last round lies in the CTA's range [x0, x1) of rounds -- found from the prefix cum of rounds
-// per sequence -- a warp per token (lanes 0-15 K, 16-31 V), into its slot of the cache.  A
-// unit's last round holds its last tile, so no other CTA stages the token's page; n-tiles of
-// one kv head may write the same token from several CTAs, with equal bytes.  The proxy fence
-// orders the writes before the bulk copies this CTA issues after its next barrier.
+// Decode step: quantizes the newest token (position len - 1) of sequence b, kv head h into its
+// slot of the cache, one warp (lanes 0-15 K, 16-31 V, 8 dims each).  The caller is the warp that
+// stages the unit's last tile, which holds the token, and issues that tile's copy only after
+// this returns: the proxy fence and the warp barrier order the writes before it.  n-tiles of one
+// kv head may write the same token from several CTAs, with equal bytes.
 template <int BITS>
-__device__ __forceinline__ void step_append(const Geometry& g, const AttnArgs& a, const long long* cum, long long x0,
-                                            long long x1, int b0, int cap, int upb) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, j = lane & 15;
+__device__ __forceinline__ void append_token(const Geometry& g, const AttnArgs& a, int b, int h, int len) {
+  const int lane = threadIdx.x & 31, half = lane >> 4, j = lane & 15;
   float bnd[15];
   codec::load_boundaries<BITS>(bnd, g.boundaries);
-  int i = 0;  // tokens enumerated so far: token i goes to warp i % kWarps
-  for (int b = b0; b < a.B && cum[b] < x1; ++b) {
-    const long long rounds = cum[b + 1] - cum[b];
-    if (rounds <= 0) continue;
-    const long long rb = rounds / upb;
-    // units whose last round, cum[b] + (u + 1) rb - 1, lies in [x0, x1)
-    const long long u_lo = max(0LL, (x0 - cum[b] + rb) / rb - 1);
-    const long long u_hi = min((long long)upb - 1, (x1 - cum[b]) / rb - 1);
-    for (long long u = u_lo; u <= u_hi; ++u, ++i) {
-      if (i % kWarps != warp) continue;  // warp-uniform
-      const int h = (int)u / a.n_tiles_n;
-      const int len = clamp_len(a, b, cap), pos = len - 1;
-      const int page = a.block_table[(size_t)b * a.max_pages + pos / g.page_size];
-      const bool ok = page >= 0 && page < g.num_pages;
-      if (!ok && lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
-      const __half* src = (half ? a.v_new : a.k_new) + ((size_t)b * g.num_kv_heads + h) * kHeadDim + 8 * j;
-      const float* rot = (half ? g.rot_v : g.rot_k) + (size_t)h * kHeadDim + 8 * j;
-      const float4 p0 = __ldg(reinterpret_cast<const float4*>(rot));
-      const float4 p1 = __ldg(reinterpret_cast<const float4*>(rot + 4));
-      const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-      // the cache is the caller's writable pool; the attention arguments carry it read-only
-      uint8_t* chunk = const_cast<uint8_t*>(a.pages) + ((size_t)(ok ? page : 0) * g.num_kv_heads + h) * g.page_bytes;
-      codec::encode_structured<BITS>(*reinterpret_cast<const uint4*>(src), pr, g.mode, bnd, chunk, g.page_size, half,
-                                     pos % g.page_size, j, ok, a.status);
-    }
-  }
+  const int pos = len - 1;
+  const int page = a.block_table[(size_t)b * a.max_pages + pos / g.page_size];
+  const bool ok = page >= 0 && page < g.num_pages;
+  if (!ok && lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
+  const __half* src = (half ? a.v_new : a.k_new) + ((size_t)b * g.num_kv_heads + h) * kHeadDim + 8 * j;
+  const float* rot = (half ? g.rot_v : g.rot_k) + (size_t)h * kHeadDim + 8 * j;
+  const float4 p0 = __ldg(reinterpret_cast<const float4*>(rot));
+  const float4 p1 = __ldg(reinterpret_cast<const float4*>(rot + 4));
+  const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  // the cache is the caller's writable pool; the attention arguments carry it read-only
+  uint8_t* chunk = const_cast<uint8_t*>(a.pages) + ((size_t)(ok ? page : 0) * g.num_kv_heads + h) * g.page_bytes;
+  codec::encode_structured<BITS>(*reinterpret_cast<const uint4*>(src), pr, g.mode, bnd, chunk, g.page_size, half,
+                                 pos % g.page_size, j, ok, a.status);
   asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
 }
 
 // PRE: the queries were rotated before the launch (dense rotation).  STEP: a decode step that
@@ -729,7 +729,27 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   float* const merge_lo = reinterpret_cast<float*>(at(plan.merge_lo));
   float* const merge_hi = reinterpret_cast<float*>(at(plan.merge_hi));
 
-  build_lut<BITS>(lut_words, g.centroids, cb);  // ends with the centroids staged; synced below
+  // The small inputs that CTAs read once their partition is known -- block table, queries,
+  // rotation parameters, a decode step's new tokens -- start filling L2 now, a line per thread
+  // of the grid, so those reads hit L2 instead of queueing behind the first bulk copies.
+  {  // line counts stay far below 2^32 (sizes are bounded at creation)
+    const uint32_t line = threadIdx.x * gridDim.x + blockIdx.x;
+    prefetch_line_l2(a.block_table, (uint32_t)(((size_t)a.B * a.max_pages * 4 + 127) / 128), line);
+    if constexpr (!PRE) {
+      const uint32_t rot_lines = (uint32_t)g.num_kv_heads * kHeadDim * 4 / 128;
+      prefetch_line_l2(a.q, (uint32_t)(((size_t)a.B * a.T * g.num_q_heads * kHeadDim * 2) / 128), line);
+      prefetch_line_l2(g.rot_k, rot_lines, line);
+      prefetch_line_l2(g.rot_v, rot_lines, line);
+    }
+    if constexpr (STEP) {
+      const uint32_t new_lines = (uint32_t)a.B * g.num_kv_heads * kHeadDim * 2 / 128;
+      prefetch_line_l2(a.k_new, new_lines, line);
+      prefetch_line_l2(a.v_new, new_lines, line);
+    }
+  }
+  // The centroids' load is in flight with the lengths' below; the table is filled once the
+  // first fragment's copies are issued, in their shadow.
+  const float cb_val = threadIdx.x < (1 << BITS) ? g.centroids[threadIdx.x] : 0.f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const uint32_t key1 = plan.lut | ((uint32_t)lane * 4u);
@@ -751,12 +771,14 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   bool broken = false;  // a staged copy never completed: stop using the ring
 
   // ---- this CTA's range [x, x_end) of rounds in the stream-K partition ----
-  // cum[b] = rounds of all units of sequences < b; built with a block scan in the low slot
-  // region, which the ring does not use before the first fragment.
+  // cum[b] = rounds of all units of sequences < b and lens[b] = sequence b's clamped tokens,
+  // built with a block scan at the start of the window: slots and table, unused before the
+  // first fragment (at most 8001 x 8 + 8000 x 4 bytes; the table and the 64 slots span more).
   const int upb = g.num_kv_heads * a.n_tiles_n;  // units per sequence
   const int cap = a.max_pages * P;
   {
     long long* cum = reinterpret_cast<long long*>(smem);
+    int* lens = reinterpret_cast<int*>(cum + a.B + 1);
     long long* wsum = reinterpret_cast<long long*>(page_ids);  // [kWarps] scan scratch
     int* wunits = page_ids + 2 * kWarps;                       // [kWarps]: units with tokens
     int* wmax = wunits + kWarps;                                // [kWarps]: largest unit (rounds)
@@ -772,6 +794,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           len = len < 0 ? 0 : (len > cap ? cap : len);
         }
         v = (long long)unit_rounds(len) * upb;
+        lens[bb] = len;
       }
       int nu = v > 0 ? upb : 0, mr = (int)(v / upb);
 #pragma unroll
@@ -812,36 +835,28 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     }
     if (threadIdx.x == 0) cum[0] = 0;
     __syncthreads();
-    // Parts = min(CTAs, rounds), so that every part is non-empty: the combine takes the CTAs
-    // between a unit's first and last fragment to all hold one.  CTAs past the parts idle.
-    // When every unit has the same rounds and there are no more units than CTAs, one whole unit
-    // per part is the other candidate: a CTA's cost is its rounds plus kFragmentRounds per
-    // fragment, and equal parts that do not divide the units cost most CTAs two fragments.
-    long long parts = min((long long)gridDim.x, total);
-    if (n_units > 0 && n_units <= (int)gridDim.x && total == (long long)n_units * max_rounds) {
-      const long long per_part = (total + parts - 1) / parts;
-      const long long cost_split = per_part + (max_rounds % per_part == 0 ? 1 : 2) * kFragmentRounds;
-      if (max_rounds + kFragmentRounds <= cost_split) parts = n_units;
-    }
-    const long long x0 = blockIdx.x < parts ? total * blockIdx.x / parts : 0;
-    const long long x1 = blockIdx.x < parts ? total * (blockIdx.x + 1) / parts : 0;
+    long long x0, x1;
+    if (total * gridDim.x < (1LL << 32))
+      partition<uint32_t>((uint32_t)total, n_units, max_rounds, gridDim.x, blockIdx.x, x0, x1);
+    else
+      partition<long long>(total, n_units, max_rounds, gridDim.x, blockIdx.x, x0, x1);
     int lo = 0, hi = a.B;  // the last sequence b with cum[b] <= x0, which skips empty ones
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (cum[mid] <= x0) lo = mid;
       else hi = mid;
     }
-    if (threadIdx.x == 0) *walk = Walk{x0, x1, cum[lo], lo, clamp_len(a, lo, cap)};
-    if constexpr (STEP) step_append<BITS>(g, a, cum, x0, x1, lo, cap, upb);
+    if (threadIdx.x == 0) *walk = Walk{x0, x1, cum[lo], lo, a.B > 0 ? lens[lo] : 0};
     if constexpr (!PRE) {  // a sequence without tokens has no fragments: its rows are zeros
       for (int bb = blockIdx.x; bb < a.B; bb += gridDim.x) {
-        if (clamp_len(a, bb, cap) != 0) continue;
+        if (cum[bb + 1] != cum[bb]) continue;
         const int n16 = a.T * g.num_q_heads * (kHeadDim / 8);
         uint4* o16 = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(a.out) + (size_t)bb * a.T * g.num_q_heads * kHeadDim);
         for (int i = threadIdx.x; i < n16; i += kThreads) o16[i] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    __syncthreads();  // the scratch is slot space from here on
+    if (threadIdx.x < (1 << BITS)) cb[threadIdx.x] = cb_val;
+    __syncthreads();  // the scratch is slot and table space from here on
   }
 
   // Every fragment advances the walk by at least one round, so this bound (the range's rounds)
@@ -922,9 +937,25 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         }
       }
     };
-    if (lane < 2 && n_w > 0) {
+    // A decode step's token lies in the unit's last tile, which ends the chunk's last pair when
+    // the chunk ends the unit: the warp that stages that pair (its last) writes the token first,
+    // deferring the pair's copy when it is one of the first stages.
+    const bool appends = STEP && tile1 == fr.tb && warp == (n_pairs - 1) % kWarps;
+    const int n_first = min(kStages, n_w) - (appends && n_w <= kStages ? 1 : 0);
+    if (lane < 2 && n_first > 0) {
       fence_proxy_async();
-      for (int k = 0; k < min(kStages, n_w); ++k) issue(k);
+      for (int k = 0; k < n_first; ++k) issue(k);
+    }
+    const bool first_chunk = n_frag == 0 && tile0 == fr.t0;  // uniform over the CTA
+    if (first_chunk) lut::fill<BITS>(lut_words, cb, threadIdx.x, kThreads);
+    if constexpr (STEP) {
+      if (appends) {
+        append_token<BITS>(g, a, it.b, it.h, len);
+        if (n_w > 0 && n_w <= kStages && lane < 2) {
+          fence_proxy_async();
+          issue(n_w - 1);
+        }
+      }
     }
     if (tile0 == fr.t0) {  // the fragment's first chunk: its copies overlap the query's loads
       float y[32];
@@ -946,6 +977,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         last_pos[c] = a.tree_mask ? len - a.T - 1 : len - a.T + j;
       }
     }
+    if (first_chunk) __syncthreads();  // the table is complete
     int consumed = 0;
     for (int k = 0; k < n_w; ++k) {
       const int st = k % kStages;
@@ -1118,6 +1150,8 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       // thread (c, gq', mt') merges dims 16 gq' + 2 mt' and +1 of column c: lane 4 gq' + c / 2
       // of every warp held them, as components (c & 1) and (c & 1) + 2 of its float4 mt'
       const int c = threadIdx.x >> 6, gm = (threadIdx.x >> 3) & 7, mm = threadIdx.x & 7;
+      // a whole unit's R_v entries, loaded while the partials are summed
+      const float4 rv = (whole && c < cols) ? rot_v_block(g, it.h, 16 * gm + 2 * mm) : make_float4(0.f, 0.f, 0.f, 0.f);
       if (c < cols) {  // c is uniform over each warp
         float M = -CUDART_INF_F;
 #pragma unroll 4
@@ -1136,7 +1170,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         }
         if (whole) {
           const float inv = (lsum > 0.f && len >= a.T) ? 1.f / lsum : 0.f;
-          store_pair(g, a, it.b, it.h, it.nt * 8 + c, 16 * gm + 2 * mm, acc0 * inv, acc1 * inv);
+          store_pair(g, a, it.b, it.h, it.nt * 8 + c, 16 * gm + 2 * mm, acc0 * inv, acc1 * inv, rv);
         } else {
           *reinterpret_cast<float2*>(dst + c * kPartialStride + 4 + 16 * gm + 2 * mm) = make_float2(acc0, acc1);
           if (gm == 0 && mm == 0) {
@@ -1181,7 +1215,8 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       const int nt = unit % ntn, h = (unit / ntn) % g.num_kv_heads, b = unit / (ntn * g.num_kv_heads);
       if (warp < min(8, a.rows - nt * 8)) {
         const int row = nt * 8 + warp;
-        store_row(g, a, b, h, row, lane, merge_splits(g, a, b, h, row, lane));
+        const float4 rv = rot_v_block(g, h, 4 * lane);
+        store_row(g, a, b, h, row, lane, merge_splits(g, a, b, h, row, lane), rv);
       }
     }
   }

@@ -66,49 +66,33 @@ __device__ __forceinline__ int code_of_margin(float u, const float (&b)[15], flo
   }
 }
 
-// Packs the codes of dims 8j..8j+7 (j = lane within its half-warp) of one vector and writes
-// them and the fp16 norm to the vector's place in `chunk` (kind 0 = K, 1 = V; `off` = offset
-// in page).  Every lane of the warp must call it: the 3-bit packing exchanges high bits
-// between lanes j and j ^ 2.  With `store` false nothing is written.
+// A lane's share of one coded vector: its packed codes (see pack_codes) and the vector's fp16
+// norm (bits).
+struct Packed {
+  uint32_t codes;
+  uint32_t norm;
+};
+
+// Packs the codes of dims 8j..8j+7 (j = lane within its half-warp) of one vector: 4-bit, eight
+// nibbles; 2-bit, 16 bits; 3-bit, the low bits (16) | the high-bit bytes (16) that lanes j and
+// j ^ 2 share, exchanged here.  Every lane of the warp must call it.
 template <int BITS>
-__device__ __forceinline__ void pack_store(const int (&code)[8], float nrm, uint8_t* chunk, int page_size, int kind,
-                                           int off, int j, bool store, int32_t* status) {
-  constexpr int vb = BITS * 16;
-  uint8_t* dst = chunk + (size_t)kind * page_size * vb + (size_t)off * vb;
-  uint8_t* vsec = chunk + (size_t)page_size * vb;
-  const int pair = off >> 1, hv = off & 1, c = j >> 1;  // V pair placement (2- and 4-bit)
+__device__ __forceinline__ uint32_t pack_codes(const int (&code)[8], int j) {
   if constexpr (BITS == 4) {
     uint32_t word = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) word |= (uint32_t)code[e] << (4 * e);
-    if (store) {
-      if (kind == 0) {
-        *reinterpret_cast<uint32_t*>(dst + 4 * j) = word;
-      } else {
-        // V: token pairs (2p, 2p+1) share 128 bytes; the 8-byte unit of 16-dim group c of
-        // token 2p + h sits at 16 * (c ^ (2p mod 8)) + 8h.  Lane j holds half of unit j / 2.
-        *reinterpret_cast<uint32_t*>(vsec + pair * 128 + 16 * (c ^ ((2 * pair) & 7)) + 8 * hv + 4 * (j & 1)) = word;
-      }
-    }
+    return word;
   } else if constexpr (BITS == 2) {
     uint32_t half_word = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) half_word |= (uint32_t)code[e] << (2 * e);
-    if (store) {
-      if (kind == 0) {
-        *reinterpret_cast<uint16_t*>(dst + 2 * j) = (uint16_t)half_word;
-      } else {
-        // V: token pairs share 64 bytes; the 4-byte unit of group c of token 2p + h sits at
-        // 8 * (c ^ (4 * (p / 2 mod 2))) + 4h.  Lane j holds half of unit j / 2.
-        *reinterpret_cast<uint16_t*>(vsec + pair * 64 + 8 * (c ^ (4 * ((pair >> 1) & 1))) + 4 * hv + 2 * (j & 1)) =
-            (uint16_t)half_word;
-      }
-    }
+    return half_word;
   } else {
     // Lane j covers dims 8m..8m+7 of 32-dim group w = j/4 (m = j%4).  Its low bits are
     // bytes 2m, 2m+1 of the group's W0|W1; its high bits fill half of bytes 2(m&1) and
     // 2(m&1)+1 of W2, shared with lane j^2 (same k, other h).
-    const int w = j >> 2, m = j & 3, hh = m >> 1;
+    const int m = j & 3, hh = m >> 1;
     uint32_t lo = 0, hib = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -118,17 +102,57 @@ __device__ __forceinline__ void pack_store(const int (&code)[8], float nrm, uint
       hib |= (uint32_t)(code[e] >> 2) << (8 * kk + 2 * hh + off_r);
     }
     const uint32_t partner = __shfl_xor_sync(0xffffffffu, hib, 2);
-    if (store) {
-      *reinterpret_cast<uint16_t*>(dst + 12 * w + 2 * m) = (uint16_t)lo;
-      if (hh == 0) *reinterpret_cast<uint16_t*>(dst + 12 * w + 8 + 2 * (m & 1)) = (uint16_t)(hib | partner);
-    }
+    return lo | (hib | partner) << 16;
   }
-  if (store && j == 0) {
-    const __half n16 = __float2half_rn(nrm);
+}
+
+// Writes a lane's packed codes and (lane j == 0) the norm to the vector's place in `chunk`
+// (kind 0 = K, 1 = V; `off` = offset in page).  No shuffles: any subset of lanes may call it.
+// A non-null status gets RQ_STATUS_NORM_OVERFLOW for an infinite norm.
+template <int BITS>
+__device__ __forceinline__ void store_packed(Packed pk, uint8_t* chunk, int page_size, int kind, int off, int j,
+                                             int32_t* status) {
+  constexpr int vb = BITS * 16;
+  uint8_t* dst = chunk + (size_t)kind * page_size * vb + (size_t)off * vb;
+  uint8_t* vsec = chunk + (size_t)page_size * vb;
+  const int pair = off >> 1, hv = off & 1, c = j >> 1;  // V pair placement (2- and 4-bit)
+  if constexpr (BITS == 4) {
+    if (kind == 0) {
+      *reinterpret_cast<uint32_t*>(dst + 4 * j) = pk.codes;
+    } else {
+      // V: token pairs (2p, 2p+1) share 128 bytes; the 8-byte unit of 16-dim group c of
+      // token 2p + h sits at 16 * (c ^ (2p mod 8)) + 8h.  Lane j holds half of unit j / 2.
+      *reinterpret_cast<uint32_t*>(vsec + pair * 128 + 16 * (c ^ ((2 * pair) & 7)) + 8 * hv + 4 * (j & 1)) = pk.codes;
+    }
+  } else if constexpr (BITS == 2) {
+    if (kind == 0) {
+      *reinterpret_cast<uint16_t*>(dst + 2 * j) = (uint16_t)pk.codes;
+    } else {
+      // V: token pairs share 64 bytes; the 4-byte unit of group c of token 2p + h sits at
+      // 8 * (c ^ (4 * (p / 2 mod 2))) + 4h.  Lane j holds half of unit j / 2.
+      *reinterpret_cast<uint16_t*>(vsec + pair * 64 + 8 * (c ^ (4 * ((pair >> 1) & 1))) + 4 * hv + 2 * (j & 1)) =
+          (uint16_t)pk.codes;
+    }
+  } else {
+    const int w = j >> 2, m = j & 3, hh = m >> 1;
+    *reinterpret_cast<uint16_t*>(dst + 12 * w + 2 * m) = (uint16_t)pk.codes;
+    if (hh == 0) *reinterpret_cast<uint16_t*>(dst + 12 * w + 8 + 2 * (m & 1)) = (uint16_t)(pk.codes >> 16);
+  }
+  if (j == 0) {
+    const __half n16 = __ushort_as_half((unsigned short)pk.norm);
     uint8_t* nb = chunk + (size_t)2 * page_size * vb + (size_t)kind * 2 * page_size + 2 * off;
     *reinterpret_cast<__half*>(nb) = n16;
     if (status && __hisinf(n16)) atomicOr(status, RQ_STATUS_NORM_OVERFLOW);
   }
+}
+
+// pack_codes + store_packed: the vector's codes and fp16 norm to its place in `chunk`.  Every
+// lane of the warp must call it; with `store` false nothing is written.
+template <int BITS>
+__device__ __forceinline__ void pack_store(const int (&code)[8], float nrm, uint8_t* chunk, int page_size, int kind,
+                                           int off, int j, bool store, int32_t* status) {
+  const Packed pk{pack_codes<BITS>(code, j), (uint32_t)__half_as_ushort(__float2half_rn(nrm))};
+  if (store) store_packed<BITS>(pk, chunk, page_size, kind, off, j, status);
 }
 
 // 1 / n, so that u = y / n is formed as y * (1/n): within an ulp of the quotient, so a code can
@@ -165,13 +189,12 @@ __device__ __forceinline__ void rotate8(float (&y)[8], const float (&x)[8], cons
   }
 }
 
-// Encodes one fp16 vector with a structured rotation and writes it to slot `off` of `chunk`:
-// lane j of the half-warp passes its 16 bytes of x (dims 8j..8j+7) and its rotation
-// parameters.  Every lane of the warp must call it (shuffles); `store` false writes nothing.
+// Codes one fp16 vector with a structured rotation: lane j of the half-warp passes its 16 bytes
+// of x (dims 8j..8j+7) and its rotation parameters, and gets its share of the result.  Every
+// lane of the warp must call it (shuffles).
 template <int BITS>
-__device__ __forceinline__ void encode_structured(uint4 raw, const float (&p)[8], int mode, const float (&bnd)[15],
-                                                  uint8_t* chunk, int page_size, int kind, int off, int j, bool store,
-                                                  int32_t* status) {
+__device__ __forceinline__ Packed encode_packed(uint4 raw, const float (&p)[8], int mode, const float (&bnd)[15],
+                                                int j) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
   float x[8];
 #pragma unroll
@@ -192,7 +215,16 @@ __device__ __forceinline__ void encode_structured(uint4 raw, const float (&p)[8]
   int code[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) code[e] = code_of<BITS>(y[e] * rcp, bnd);
-  pack_store<BITS>(code, nrm, chunk, page_size, kind, off, j, store, status);
+  return Packed{pack_codes<BITS>(code, j), (uint32_t)__half_as_ushort(__float2half_rn(nrm))};
+}
+
+// encode_packed, written to slot `off` of `chunk` (`store` false writes nothing).
+template <int BITS>
+__device__ __forceinline__ void encode_structured(uint4 raw, const float (&p)[8], int mode, const float (&bnd)[15],
+                                                  uint8_t* chunk, int page_size, int kind, int off, int j, bool store,
+                                                  int32_t* status) {
+  const Packed pk = encode_packed<BITS>(raw, p, mode, bnd, j);
+  if (store) store_packed<BITS>(pk, chunk, page_size, kind, off, j, status);
 }
 
 }  // namespace codec
