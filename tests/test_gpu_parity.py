@@ -252,6 +252,9 @@ STEP_CASES = [
     (ISO, 4, 64, 8, 64, [200, 129, 64]),
     (PLANAR, 4, 96, 8, 16, [100, 33]),     # group 12: two n-tiles per kv head write the token
     (ISO, 2, 32, 8, 16, [50, 16, 2049]),
+    # 344 rounds over the CTAs: ranges cross unit boundaries, so tokens land in a CTA's second
+    # fragment and in units split across CTAs
+    (PLANAR, 3, 32, 8, 16, [5000, 3000, 777, 12345]),
 ]
 
 
