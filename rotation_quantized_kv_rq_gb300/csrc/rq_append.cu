@@ -42,10 +42,10 @@ struct Item {
   uint4 raw;  // 8 fp16 of this lane's half (K or V)
 };
 
-__device__ __forceinline__ void fetch(Item& it, long long item, const Geometry& g, const __half* src_k,
+__device__ __forceinline__ void fetch(Item& it, int t, int h, const Geometry& g, const __half* src_k,
                                       const __half* src_v, const int32_t* slots, int half, int j) {
-  it.t = (int)(item / g.num_kv_heads);
-  it.h = (int)(item % g.num_kv_heads);
+  it.t = t;
+  it.h = h;
   it.slot = __ldg(slots + it.t);
   const __half* src = (half ? src_v : src_k) + ((size_t)it.t * g.num_kv_heads + it.h) * kHeadDim + 8 * j;
   it.raw = __ldg(reinterpret_cast<const uint4*>(src));
@@ -69,10 +69,21 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
 
   long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
   if (item >= items) return;
+  // item = t * Hkv + h: divided once, then advanced by the stride without dividing (a 64-bit
+  // division is a long instruction sequence, comparable to coding the vectors)
+  const int hkv = g.num_kv_heads;
+  int t = (int)(item / hkv), h = (int)(item % hkv);
+  const int stride_t = (int)(stride / hkv), stride_h = (int)(stride % hkv);
   Item cur, nxt;
-  fetch(cur, item, g, k, v, slots, half, j);
+  fetch(cur, t, h, g, k, v, slots, half, j);
   for (; item < items; item += stride) {
-    if (item + stride < items) fetch(nxt, item + stride, g, k, v, slots, half, j);
+    t += stride_t;
+    h += stride_h;
+    if (h >= hkv) {
+      h -= hkv;
+      ++t;
+    }
+    if (item + stride < items) fetch(nxt, t, h, g, k, v, slots, half, j);
 
     const int slot = cur.slot;
     const bool bad = (long long)slot >= pool_slots;
@@ -129,14 +140,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// Tile t covers tokens 64 * (t / (2 Hkv)) .. +63 of kv head hk % Hkv, K (hk < Hkv) or V, with
-// hk = t % (2 Hkv).  Rows past n are zero-filled.
-__device__ __forceinline__ void issue_x(uint32_t xs, long long tile, const Geometry& g, const __half* k,
+// Tile t covers tokens 64 blk .. 64 blk + 63 of kv head hk % Hkv, K (hk < Hkv) or V, with
+// hk = t % (2 Hkv) and blk = t / (2 Hkv).  Rows past n are zero-filled.
+__device__ __forceinline__ void issue_x(uint32_t xs, int hk, long long blk, const Geometry& g, const __half* k,
                                        const __half* v, int n, uint8_t* xs_generic) {
   const int hkv = g.num_kv_heads;
-  const int hk = (int)(tile % (2 * hkv));
-  const long long blk = tile / (2 * hkv);
-  const int kind = hk / hkv, h = hk % hkv;
+  const int kind = hk >= hkv, h = kind ? hk - hkv : hk;
   const __half* src = kind ? v : k;
   for (int i = threadIdx.x; i < kDenseRows * 16; i += kDenseThreads) {
     const int r = i >> 4, c = i & 15;
@@ -201,13 +210,25 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
 
   long long tile = blockIdx.x;
   if (tile >= tiles) return;
+  // (hk, blk) of the tile, advanced by the grid stride without dividing
+  const int h2 = 2 * hkv;
+  int hk = (int)(tile % h2);
+  long long blk = tile / h2;
+  const int stride_hk = (int)(gridDim.x % h2);
+  const long long stride_blk = gridDim.x / h2;
+  auto advance = [&](int& a, long long& b) {
+    a += stride_hk;
+    b += stride_blk;
+    if (a >= h2) {
+      a -= h2;
+      ++b;
+    }
+  };
   int buf = 0, cur_hk = -1;
-  issue_x(base + kSmemX, tile, g, k, v, n, smem + kSmemX);
+  issue_x(base + kSmemX, hk, blk, g, k, v, n, smem + kSmemX);
   cp_async_commit();
   for (; tile < tiles; tile += gridDim.x) {
-    const int hk = (int)(tile % (2 * hkv));
-    const long long blk = tile / (2 * hkv);
-    const int kind = hk / hkv, h = hk % hkv;
+    const int kind = hk >= hkv, h = kind ? hk - hkv : hk;
     if (hk != cur_hk) {  // stage R of this (K or V, head); the previous tile is done with it
       const uint4* src = reinterpret_cast<const uint4*>(g.dense16 + ((size_t)kind * hkv + h) * 2 * 128 * 128);
       for (int i = threadIdx.x; i < 2 * 128 * 16; i += kDenseThreads) {
@@ -220,8 +241,11 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
       cur_hk = hk;
     }
     const long long next = tile + gridDim.x;
+    int hk_next = hk;
+    long long blk_next = blk;
+    advance(hk_next, blk_next);
     const uint32_t xs_next = base + kSmemX + (uint32_t)((buf ^ 1) * kDenseRows * 256);
-    if (next < tiles) issue_x(xs_next, next, g, k, v, n, smem + kSmemX + (buf ^ 1) * kDenseRows * 256);
+    if (next < tiles) issue_x(xs_next, hk_next, blk_next, g, k, v, n, smem + kSmemX + (buf ^ 1) * kDenseRows * 256);
     cp_async_commit();
     cp_async_wait1();
     __syncthreads();  // this tile's X (and R, if restaged) visible to every warp
@@ -316,6 +340,8 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
     }
     __syncthreads();  // X buffer and Y free for the next tile
     buf ^= 1;
+    hk = hk_next;
+    blk = blk_next;
   }
 }
 
