@@ -34,6 +34,27 @@ using namespace codec;
 constexpr int kAppendThreads = 256;
 constexpr int kAppendWarps = kAppendThreads / 32;
 
+// slot -> (page, offset): a shift and a mask for the usual power-of-two page sizes (decided once
+// per thread; the division is a longer instruction sequence), else a division.
+struct PageSplit {
+  int P, shift;  // shift < 0: P is not a power of two
+  __device__ explicit PageSplit(int page_size) : P(page_size), shift(-1) {
+    if ((page_size & (page_size - 1)) == 0) {  // page sizes are at most 256
+      shift = 0;
+      while ((1 << shift) < page_size) ++shift;
+    }
+  }
+  __device__ __forceinline__ void operator()(int slot, int& page, int& off) const {
+    if (shift >= 0) {
+      page = slot >> shift;
+      off = slot & (P - 1);
+    } else {
+      page = slot / P;
+      off = slot - page * P;
+    }
+  }
+};
+
 // ---------------------------------------------------------------------------------------
 // Structured rotations
 // ---------------------------------------------------------------------------------------
@@ -66,6 +87,7 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
   const long long stride = (long long)gridDim.x * kAppendWarps;
   const float* rot = half ? g.rot_v : g.rot_k;
   const long long pool_slots = (long long)g.num_pages * g.page_size;
+  const PageSplit split(g.page_size);
 
   long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
   if (item >= items) return;
@@ -92,7 +114,8 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
       const float4 p0 = __ldg(reinterpret_cast<const float4*>(rot + (size_t)cur.h * kHeadDim + 8 * j));
       const float4 p1 = __ldg(reinterpret_cast<const float4*>(rot + (size_t)cur.h * kHeadDim + 8 * j + 4));
       const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-      const int page = slot / g.page_size, off = slot % g.page_size;
+      int page, off;
+      split(slot, page, off);
       uint8_t* chunk = pages + ((size_t)page * g.num_kv_heads + cur.h) * (size_t)g.page_bytes;
       encode_structured<BITS>(cur.raw, pr, g.mode, bnd, chunk, g.page_size, half, off, j, true, status);
     }
@@ -203,6 +226,7 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
   const long long nblk = ((long long)n + kDenseRows - 1) / kDenseRows;
   const long long tiles = 2LL * hkv * nblk;
   const long long pool_slots = (long long)g.num_pages * g.page_size;
+  const PageSplit split(g.page_size);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int mt = warp & 3, nq = warp >> 2;  // rows 16mt.., columns 32nq..
@@ -334,7 +358,8 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
           todo &= ~(1u << e_lead);
         }
       }
-      const int page = slot / g.page_size, off = slot % g.page_size;
+      int page, off;
+      split(slot, page, off);
       uint8_t* chunk = pages + ((size_t)page * hkv + h) * (size_t)g.page_bytes;
       pack_store<BITS>(code, nrm, chunk, g.page_size, kind, off, j, store, status);
     }

@@ -103,6 +103,7 @@ CASES = [
     (PLANAR, 4, 12, 4, 16, [48, 20], 3),
     (ISO, 4, 32, 8, 16, [5000], 1),
     (PLANAR, 3, 32, 8, 128, [700, 129], 2),
+    (PLANAR, 3, 32, 8, 48, [100, 47, 200], 1),  # a page size that is not a power of two
     # 2-bit codes and the dense (TurboQuant) rotation
     (PLANAR, 2, 32, 8, 16, [200, 33, 1], 1),
     (ISO, 2, 64, 8, 64, [300, 65], 1),
@@ -112,6 +113,7 @@ CASES = [
     (DENSE, 4, 24, 2, 32, [95, 3], 2),
     (DENSE, 3, 40, 2, 16, [50, 200], 1),
     (DENSE, 2, 8, 8, 16, [16, 48], 1),
+    (DENSE, 4, 32, 8, 48, [130, 49], 1),
 ]
 
 
