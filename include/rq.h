@@ -172,9 +172,9 @@ int rq_extend_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
                         void *stream);
 
 /*
- * One decode step in one launch (plus the combine): quantize-append of every sequence's newest
- * K/V token, folded into rq_decode_attention's split-K kernel, then decode attention over the
- * cache including that token.
+ * One decode step in one kernel launch: quantize-append of every sequence's newest K/V token,
+ * folded into rq_decode_attention's split-K kernel, then decode attention over the cache
+ * including that token (the combine of split partials runs in the same kernel).
  *   k_new, v_new  device fp16 [B][Hkv][head_dim]: the token of sequence b, written to position
  *                 seq_lens[b] - 1 -- page block_table[b][(seq_lens[b] - 1) / P], offset
  *                 (seq_lens[b] - 1) % P -- exactly as rq_quantize_append would write it
