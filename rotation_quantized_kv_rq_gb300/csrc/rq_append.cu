@@ -11,8 +11,9 @@
 // in flight while the current one is coded.  The kernel is bound by HBM: 512 bytes of fp16
 // in, 2 * (16 * bits + 2) bytes out per item.
 //
-// Dense rotation: Y = X R^T for a tile of 64 vectors of one (kv head, K or V) is a small GEMM
-// (64 x 128 x 128) on the tensor cores.  X is fp16 and exact as an operand; R (fp32) is split
+// Dense rotation: Y = X R^T for a tile of 32 vectors of one (kv head, K or V) is a small GEMM
+// (32 x 128 x 128) on the tensor cores, two CTAs per SM so that one's GEMM overlaps the other's
+// coding.  X is fp16 and exact as an operand; R (fp32) is split
 // as R = hi + lo with hi = fp16(R), lo = fp16(R - hi), both multiplied into one fp32
 // accumulator.  That carries R to ~6e-8 per entry, but the tensor cores' fp32 accumulation is
 // not correctly rounded, so a coordinate whose u lies within kFixBand of a boundary is
@@ -126,14 +127,18 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
 // ---------------------------------------------------------------------------------------
 // Dense rotation (tensor cores)
 // ---------------------------------------------------------------------------------------
-constexpr int kDenseRows = 64;                 // vectors per tile
-constexpr int kDenseThreads = 512;             // 16 warps: 4 row tiles x 4 column quarters
+// Two CTAs per SM, so that one CTA's GEMM overlaps the other's coding (each CTA alternates the
+// two with barriers in between).
+constexpr int kDenseRows = 32;                 // vectors per tile
+constexpr int kDenseThreads = 256;             // 8 warps: 2 row tiles x 4 column quarters
+constexpr int kDenseWarps = kDenseThreads / 32;
+constexpr int kDenseCtasPerSm = 2;
 constexpr int kYStride = 136;                  // floats per staged Y row (conflict-free float2 stores)
 constexpr int kSmemR = 0;                      // fp16 [2 (hi, lo)][128][128], 16-byte chunks swizzled
-constexpr int kSmemX = kSmemR + 2 * 128 * 128 * 2;            // fp16 [2 buffers][64][128], swizzled
-constexpr int kSmemY = kSmemX + 2 * kDenseRows * 128 * 2;     // fp32 [64][136]
-constexpr int kSmemR32 = kSmemY + kDenseRows * kYStride * 4;  // fp32 [128][128] R (exact recompute)
-constexpr int kDenseSmem = kSmemR32 + 128 * 128 * 4;           // 198,656 bytes
+constexpr int kSmemX = kSmemR + 2 * 128 * 128 * 2;            // fp16 [2 buffers][32][128], swizzled
+constexpr int kSmemY = kSmemX + 2 * kDenseRows * 128 * 2;     // fp32 [32][136]
+constexpr int kDenseSmem = kSmemY + kDenseRows * kYStride * 4;  // 99,328 bytes; the fp32 R of the
+                                                                // exact recompute is read from L2
 // Tensor-core Y is trusted to decide a code when u is farther than this from every boundary.
 // Its error is the hi + lo split (|R - hi - lo| <= 6e-8 per entry, so <= 7e-7 in u by
 // Cauchy-Schwarz) plus the accumulation of 16 fp32 MMA steps (a few fp32 ulps of n each).
@@ -163,7 +168,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// Tile t covers tokens 64 blk .. 64 blk + 63 of kv head hk % Hkv, K (hk < Hkv) or V, with
+// Tile t covers tokens kDenseRows * blk .. + kDenseRows - 1 of kv head hk % Hkv, K (hk < Hkv) or V, with
 // hk = t % (2 Hkv) and blk = t / (2 Hkv).  Rows past n are zero-filled.
 __device__ __forceinline__ void issue_x(uint32_t xs, int hk, long long blk, const Geometry& g, const __half* k,
                                        const __half* v, int n, uint8_t* xs_generic) {
@@ -184,10 +189,11 @@ __device__ __forceinline__ void issue_x(uint32_t xs, int hk, long long blk, cons
 // y_i = sum_m x_m R[i][m] for one vector, summed exactly enough to be correctly rounded in all
 // but pathological cases: error-free products (fma) and error-free sums (two-sum), the rounding
 // errors carried in a second word.  Lane j of the half-warp holds x[8j..8j+7]; `row` is R's row
-// i in shared memory.  Every lane of the warp calls it (shuffles stay within each half).
+// i in global memory (rarely read: L2).  Every lane of the warp calls it (shuffles stay within
+// each half).
 __device__ __forceinline__ float dot_compensated(const float (&x)[8], const float* row, int j) {
-  const float4 r0 = *reinterpret_cast<const float4*>(row + 8 * j);
-  const float4 r1 = *reinterpret_cast<const float4*>(row + 8 * j + 4);
+  const float4 r0 = __ldg(reinterpret_cast<const float4*>(row + 8 * j));
+  const float4 r1 = __ldg(reinterpret_cast<const float4*>(row + 8 * j + 4));
   const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
   float s = 0.f, c = 0.f;
 #pragma unroll
@@ -212,7 +218,7 @@ __device__ __forceinline__ float dot_compensated(const float (&x)[8], const floa
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kDenseThreads, 1)
+__global__ void __launch_bounds__(kDenseThreads, kDenseCtasPerSm)
 append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict__ v,
                     const int32_t* __restrict__ slots, int n, uint8_t* __restrict__ pages,
                     int32_t* __restrict__ status) {
@@ -229,7 +235,7 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
   const PageSplit split(g.page_size);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const int mt = warp & 3, nq = warp >> 2;  // rows 16mt.., columns 32nq..
+  const int mt = warp & 1, nq = warp >> 1;  // rows 16mt.., columns 32nq..
   const int half = lane >> 4, j = lane & 15;
 
   long long tile = blockIdx.x;
@@ -253,15 +259,13 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
   cp_async_commit();
   for (; tile < tiles; tile += gridDim.x) {
     const int kind = hk >= hkv, h = kind ? hk - hkv : hk;
+    const float* r32 = g.dense32 + ((size_t)kind * hkv + h) * 128 * 128;  // fp32 R rows (exact recompute)
     if (hk != cur_hk) {  // stage R of this (K or V, head); the previous tile is done with it
       const uint4* src = reinterpret_cast<const uint4*>(g.dense16 + ((size_t)kind * hkv + h) * 2 * 128 * 128);
       for (int i = threadIdx.x; i < 2 * 128 * 16; i += kDenseThreads) {
         const int hl = i >> 11, row = (i >> 4) & 127, c = i & 15;
         *reinterpret_cast<uint4*>(smem + kSmemR + hl * 32768 + swz(row, c)) = __ldg(src + i);
       }
-      const float4* src32 = reinterpret_cast<const float4*>(g.dense32 + ((size_t)kind * hkv + h) * 128 * 128);
-      for (int i = threadIdx.x; i < 128 * 32; i += kDenseThreads)
-        reinterpret_cast<float4*>(smem + kSmemR32)[i] = __ldg(src32 + i);
       cur_hk = hk;
     }
     const long long next = tile + gridDim.x;
@@ -304,11 +308,11 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
     }
     __syncthreads();
 
-    // Coding: a half-warp per vector, lane j on dims 8j..8j+7 (32 vectors per pass).
+    // Coding: a half-warp per vector, lane j on dims 8j..8j+7 (2 kDenseWarps vectors per pass).
     const uint8_t* xg = smem + kSmemX + buf * kDenseRows * 256;
 #pragma unroll 1
-    for (int pass = 0; pass < kDenseRows / 32; ++pass) {
-      const int r = 32 * pass + 2 * warp + half;
+    for (int pass = 0; pass < kDenseRows / (2 * kDenseWarps); ++pass) {
+      const int r = 2 * kDenseWarps * pass + 2 * warp + half;
       const long long t = blk * kDenseRows + r;
       int slot = t < n ? __ldg(slots + t) : -1;
       const bool bad = (long long)slot >= pool_slots;
@@ -349,7 +353,7 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
         const int leader = want ? __ffs(want) - 1 : (half << 4);  // no work: any lane, result unused
         const int e_lead = __shfl_sync(0xffffffffu, todo ? __ffs(todo) - 1 : 0, leader);
         const int i = 8 * (leader & 15) + e_lead;  // the coordinate (dim of y) being recomputed
-        const float yi = dot_compensated(x, reinterpret_cast<const float*>(smem + kSmemR32) + i * 128, j);
+        const float yi = dot_compensated(x, r32 + i * 128, j);
         if (lane == leader && want) {
           const int c = code_of<BITS>(yi * rcp, bnd);
 #pragma unroll
@@ -376,7 +380,8 @@ cudaError_t launch_append_bits(const Geometry& g, const __half* k, const __half*
   if (g.mode == RQ_DENSE) {
     const long long tiles = 2LL * g.num_kv_heads * ((n + kDenseRows - 1) / kDenseRows);
     // whole multiples of the 2 Hkv (K/V, head) groups, so a CTA keeps one R staged
-    int ctas = sms >= 2 * g.num_kv_heads ? sms / (2 * g.num_kv_heads) * (2 * g.num_kv_heads) : sms;
+    const int resident = kDenseCtasPerSm * sms;
+    int ctas = resident >= 2 * g.num_kv_heads ? resident / (2 * g.num_kv_heads) * (2 * g.num_kv_heads) : resident;
     if (tiles < ctas) ctas = (int)tiles;
     append_dense_kernel<BITS><<<ctas, kDenseThreads, kDenseSmem, stream>>>(g, k, v, slots, n, pages, status);
   } else {
