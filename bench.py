@@ -28,6 +28,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -216,7 +217,9 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples go to a scratch file; the JSON line carries their summary
+        self.path = os.path.join(os.environ.get("RQ_BENCH_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"rq_bench_clocks_rank{gpu_index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -247,6 +250,10 @@ class ClockSampler:
                 parts = [p.strip() for p in ln.split(",")]
                 if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
                     rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         sm = [float(r[1]) for r in rows]
