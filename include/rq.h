@@ -27,7 +27,7 @@
  *     index is clamped so no access leaves its buffer, and the outputs of the affected
  *     sequence are unspecified.  The library never clears *d_status.
  *
- * Storage contract (the pages fix none of it; see the design doc for the readings):
+ * Storage contract (the method's description fixes none of it; this library's choice):
  *   page pool   : device bytes [num_pages][num_kv_heads][page_bytes]; the chunk of
  *                 (page, kv head) is   K codes [P][vb] | V codes [P][vb] | K norms fp16 [P] |
  *                 V norms fp16 [P],  vb = head_dim * bits / 8, page_bytes = P * (2 vb + 4).

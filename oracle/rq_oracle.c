@@ -13,7 +13,7 @@
  *   - the scalar quantizer is Lloyd-Max (credited to TurboQuant: random rotation + Lloyd-Max
  *     scalar quantization).
  * The pages do not fix norm handling, codebook scaling, pairing, bit layout, page layout or
- * attention; the readings taken here are listed in the design doc and restated at each function.
+ * attention; the reading taken for each is stated at the function that uses it.
  *
  * Everything is computed in double precision, one vector or one (sequence, head) at a time,
  * with no blocking or fusion.  The one decision taken in single precision is the scalar code:
