@@ -1,7 +1,9 @@
 /*
  * rq.h -- C ABI of the rotation-quantized KV cache library (librq.so), GB300 / sm_103a.
  *
- * The method ("SGLang 1-Bit Turbo" README, section "RotorQuant KV Cache Compression", and
+ * The method (the README "SGLang 1-Bit Turbo -- AMD ROCm Inference with PrismML Quantization +
+ * Speculative Decoding Support", called "the README" below; its section "RotorQuant KV Cache
+ * Compression", and
  * the TurboQuant section it is compared with): every K and V vector written to the cache
  * keeps its L2 norm, is turned by a fixed data-oblivious rotation -- 2D Givens pairs
  * (PlanarQuant), 4D unit-quaternion blocks (IsoQuant) or one dense orthogonal matrix
@@ -74,7 +76,9 @@ extern "C" {
 #define RQ_STATUS_TIMEOUT 16   /* an attention kernel's staged page copy did not complete within
                                   its bounded wait (outputs of that call are unspecified) */
 
-/* Rotation families ("--kv-cache-dtype rq{3,4}_{planar,iso}", TurboQuant "tq{2,3,4}") */
+/* Rotation families.  Source: README, CLI Reference > KV Cache Compression Flags (--kv-cache-dtype
+   rq{3,4}_{planar,iso}, tq{2,3,4}) and the two mode tables under Core Features (RotorQuant: 2D
+   Givens or 4D quaternion; TurboQuant: dense random rotation). */
 #define RQ_PLANAR 0            /* PlanarQuant: 2D Givens rotation per dimension pair */
 #define RQ_ISO 1               /* IsoQuant: unit quaternion per 4-dimension block */
 #define RQ_DENSE 2             /* TurboQuant: one dense orthogonal head_dim x head_dim matrix */
@@ -108,28 +112,39 @@ typedef struct {
   int device;                /* CUDA device ordinal the context lives on; -1 = current */
 } rq_config;
 
-/* Validates cfg, copies the rotation tables and codebook to the device and allocates the
-   split-K workspace on cfg->device.  On success *out is a new context; on failure *out is
-   NULL and nothing stays allocated.  Errors: RQ_ERR_INVALID, RQ_ERR_UNSUPPORTED, RQ_ERR_CUDA. */
+/* Source: this library (the constructor of the context that rq_free releases); the tables it holds
+   are the rotations of README > Core Features > RotorQuant / TurboQuant KV Cache Compression and
+   the Lloyd-Max codebook named in its Acknowledgments (TurboQuant entry). Validates cfg, copies the
+   rotation tables and codebook to the device and allocates the split-K workspace on cfg->device.
+   On success *out is a new context; on failure *out is NULL and nothing stays allocated.  Errors:
+   RQ_ERR_INVALID, RQ_ERR_UNSUPPORTED, RQ_ERR_CUDA. */
 int rq_create(rq_ctx **out, const rq_config *cfg);
 
-/* Releases everything rq_create allocated.  NULL-safe.  The caller must make sure no work of
-   this context is still running (synchronise its stream first). */
+/* Source: this library.  Releases everything rq_create allocated.  NULL-safe.  The caller must make
+   sure no work of this context is still running (synchronise its stream first). */
 void rq_free(rq_ctx *ctx);
 
-/* Bytes of one (page, kv head) chunk: page_size * (2 * head_dim * bits / 8 + 4).  0 for NULL. */
+/* Source: this library's storage contract (above).  Bytes of one (page, kv head) chunk: page_size *
+   (2 * head_dim * bits / 8 + 4).  0 for NULL. */
 size_t rq_page_bytes(const rq_ctx *ctx);
 
-/* Host only (no GPU needed): the default codebook -- ascending centroids of the Lloyd-Max
-   quantizer of N(0,1) with 2^bits levels, divided by sqrt(head_dim), rounded to float32 --
-   into centroids[2^bits].  bits in 1..8, head_dim >= 1.  Returns RQ_OK or RQ_ERR_INVALID. */
+/* Source: README, Acknowledgments (TurboQuant entry: "Lloyd-Max scalar quantization"), read as the
+   Lloyd-Max quantizer of the N(0, 1/head_dim) coordinates of a rotated unit vector. Host only (no
+   GPU needed): the default codebook -- ascending centroids of the Lloyd-Max quantizer of N(0,1)
+   with 2^bits levels, divided by sqrt(head_dim), rounded to float32 -- into centroids[2^bits].
+   bits in 1..8, head_dim >= 1.  Returns RQ_OK or RQ_ERR_INVALID. */
 int rq_lloyd_max_codebook(int bits, int head_dim, float *centroids);
 
-/* Host copies of the context's centroids [2^bits] and bin boundaries [2^bits - 1] (float32;
-   boundary j = float((centroid_j + centroid_{j+1}) / 2) computed in double).  Either may be NULL. */
+/* Source: this library.  Host copies of the context's centroids [2^bits] and bin boundaries
+   [2^bits - 1] (float32; boundary j = float((centroid_j + centroid_{j+1}) / 2) computed in
+   double).  Either may be NULL. */
 int rq_get_codebook(const rq_ctx *ctx, float *centroids, float *boundaries);
 
 /*
+ * Source: README > Core Features > RotorQuant KV Cache Compression (a fixed, data-oblivious 2D
+ * Givens or 4D quaternion rotation, 3- or 4-bit codes) and > TurboQuant KV Cache Compression (a
+ * dense random rotation, 2-4 bits), with Acknowledgments (rotation, then Lloyd-Max scalar
+ * quantization).  The norm and the packing are this library's storage contract.
  * Quantize-on-append (one fused kernel): for token t < n and kv head h, encode
  * k[t][h][:] and v[t][h][:] (device fp16 [n][Hkv][head_dim]) into slot slot_mapping[t]
  * (device int32 [n]) of the page pool kv_pages (device, see the storage contract).  A slot
@@ -141,6 +156,10 @@ int rq_quantize_append(rq_ctx *ctx, const void *k, const void *v, const int32_t 
                        int n, void *kv_pages, int32_t *d_status, void *stream);
 
 /*
+ * Source: README > RDNA2 Crash Fixes, rows 6 and 10 (decode attention over a paged cache addressed
+ * through kv_indices, the page table), read over the packed cache of Core
+ * Features > RotorQuant KV Cache Compression: the query is rotated once, values are summed in
+ * the rotated space and the output is rotated back once (the rotation is orthogonal).
  * GQA decode attention over the packed cache (split-K flash-decode + log-sum-exp combine).
  *   q           device fp16 [B][Hq][head_dim]
  *   kv_pages    device page pool
@@ -157,6 +176,8 @@ int rq_decode_attention(rq_ctx *ctx, const void *q, const void *kv_pages, const 
                         void *stream);
 
 /*
+ * Source: README > RDNA2 Crash Fixes, row 5 (extend attention over partial tiles) and row 9a (the
+ * extend path), over the packed cache of Core Features > RotorQuant KV Cache Compression.
  * Extend (prefill) attention: T new query tokens per sequence, already appended as the last T
  * tokens of the cache, each attending to the cached prefix and causally to the new tokens:
  * query row j (0 <= j < T) sees positions 0 .. seq_lens[b] - T + j -- the same result as
@@ -172,6 +193,8 @@ int rq_extend_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
                         void *stream);
 
 /*
+ * Source: this library -- rq_quantize_append of one token per sequence followed by
+ * rq_decode_attention, in one launch.
  * One decode step in one kernel launch: quantize-append of every sequence's newest K/V token,
  * folded into rq_decode_attention's split-K kernel, then decode attention over the cache
  * including that token (the combine of split partials runs in the same kernel).
@@ -191,6 +214,9 @@ int rq_decode_step(rq_ctx *ctx, const void *q, const void *k_new, const void *v_
                    int32_t *d_status, void *stream);
 
 /*
+ * Source: README > Core Features > EAGLE3 / P-EAGLE Speculative Decoding (the target model
+ * verifies the draft tokens) and RDNA2 Crash Fixes rows 9b and 11 (verify extends seq_lens by the
+ * drafts); a chain is a top-1 draft.
  * Speculative chain-verify attention: T query tokens per sequence, the last T cached tokens
  * being the drafts themselves (append them first).  Query row j (0 <= j < T) attends to
  * positions 0 .. seq_lens[b] - T + j (causal over the draft tail).
@@ -204,6 +230,8 @@ int rq_verify_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
                         void *out, int32_t *d_status, void *stream);
 
 /*
+ * Source: README > Core Features > EAGLE3 / P-EAGLE Speculative Decoding (probabilistic tree
+ * sampling of drafts): verify over a draft tree.
  * Speculative tree-verify attention (a draft tree, e.g. top-k > 1 EAGLE trees): like
  * rq_verify_attention, except that query row j attends to the prefix, positions
  * 0 .. seq_lens[b] - T - 1, and to draft i (position seq_lens[b] - T + i) exactly when bit i of
@@ -248,12 +276,12 @@ int rq_decode_attention_noalloc(const rq_config *cfg, const float *d_rot_k, cons
                                 const int32_t *block_table, int max_pages, const int32_t *seq_lens,
                                 int B, void *out, int32_t *d_status, void *stream);
 
-/* Diagnostics.  While set, every attention call records ev_start on its stream just before
-   its split-K kernel and ev_end just after it (both cudaEvent_t created by the caller, who
-   reads the elapsed time); NULL, NULL stops recording.  Costs nothing when unset. */
+/* Source: this library.  Diagnostics.  While set, every attention call records ev_start on its
+   stream just before its split-K kernel and ev_end just after it (both cudaEvent_t created by the
+   caller, who reads the elapsed time); NULL, NULL stops recording.  Costs nothing when unset. */
 int rq_set_profile_events(rq_ctx *ctx, void *ev_start, void *ev_end);
 
-/* Static English text for a return code (never NULL). */
+/* Source: this library.  Static English text for a return code (never NULL). */
 const char *rq_status_string(int status);
 
 #ifdef __cplusplus

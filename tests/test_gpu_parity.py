@@ -81,13 +81,19 @@ def run_both(wl, kv, q):
     status = int(cache.status.item())
     out = out.cpu().numpy()
 
+    # the oracle's attention over the GPU's own packed bytes: whatever codes the GPU decided,
+    # its attention over them must match this strictly
+    og = PT.oracle_cache(wl)
+    og.pages[:] = gpu_pages.reshape(-1)
+    ref_own = og.attention(q, wl.block_table, wl.seq_lens, T=T)
+
     # decode alone, over the oracle's own packed bytes
     cache.pages.copy_(torch.from_numpy(oc.pages.reshape(cache.pages.shape)))
     out2 = (cache.decode(qd[:, 0].contiguous(), bt, sl).unsqueeze(1) if T == 1 else cache.verify(qd, bt, sl))
     out2 = out2.cpu().numpy()
     cache.close()
-    return dict(oc=oc, ref=ref, out=out, out_on_oracle_pages=out2, gpu_pages=gpu_pages, tokens=tokens,
-                margins=margins, inputs=(K, V), status=status, seq_of=seq_of)
+    return dict(oc=oc, ref=ref, ref_own=ref_own, out=out, out_on_oracle_pages=out2, gpu_pages=gpu_pages,
+                tokens=tokens, margins=margins, inputs=(K, V), status=status, seq_of=seq_of)
 
 
 CASES = [
@@ -129,8 +135,41 @@ def test_append_and_attention_match_oracle(case, capsys):
         print(f" [{compared} codes, {in_band} within 1e-6 of a boundary]", end="")
     assert in_band <= max(2, compared // 100000), (in_band, compared)
     PT.assert_close(r["out_on_oracle_pages"], r["ref"], "attention over the oracle's pages")
+    PT.assert_close(r["out"], r["ref_own"], "append + attention, against the oracle over the GPU's own pages")
     allowed = {(r["seq_of"][ti], h) for ti, h in flips}
     PT.assert_close_except(r["out"], r["ref"], hq // hkv, allowed, "append + attention")
+
+
+@pytest.mark.parametrize("plant", ["rot_v", "rot_k", "boundary", "centroid"])
+def test_negative_control_planted_in_the_oracle(plant):
+    """The comparison has teeth: with one mistake planted in the ORACLE (on the CPU) -- a rotation
+    parameter of one head nudged, one bin boundary moved, one centroid changed -- the GPU's
+    output or codes must fail the same checks that pass against the faithful oracle."""
+    wl, kv, q = make_case(ISO, 4, 32, 8, 16, [300, 129], 1, seed=31)
+    r = run_both(wl, kv, q)
+    assert r["status"] == 0
+    bad = PT.oracle_cache(wl)
+    bad.rot_k, bad.rot_v = bad.rot_k.copy(), bad.rot_v.copy()  # the cache views the workload's tables
+    if plant == "rot_v":
+        bad.rot_v[3, 8:12] = bad.rot_v[3, [9, 8, 11, 10]]  # one quaternion block of head 3, permuted
+    elif plant == "rot_k":
+        bad.rot_k[0, 1:4] = -bad.rot_k[0, 1:4]            # one block of head 0: the inverse rotation
+    elif plant == "boundary":
+        j = len(bad.boundaries) // 2 + 2
+        bad.boundaries[j] = np.float32((bad.boundaries[j] + bad.boundaries[j + 1]) / 2)
+    else:
+        bad.centroids[5] = np.float32(bad.centroids[5] * 1.02)
+    if plant == "boundary":
+        # the codes: re-encoding with the planted boundary disagrees with the GPU's bytes
+        for b, (k, v) in enumerate(kv):
+            bad.append(k, v, PT.positions_slots(wl, b, 0, k.shape[0]))
+        with pytest.raises(AssertionError):
+            PT.compare_chunks(r["gpu_pages"], bad, r["tokens"])
+        return
+    bad.pages[:] = r["gpu_pages"].reshape(-1)
+    ref_bad = bad.attention(q, wl.block_table, wl.seq_lens)
+    with pytest.raises(AssertionError):
+        PT.assert_close(r["out"], ref_bad, "planted")
 
 
 def test_zero_length_sequences_give_zeros():
@@ -314,6 +353,9 @@ def test_decode_step_appends_then_attends(case, capsys):
                                           (np.concatenate(flat[0]), np.concatenate(flat[1])), flips)
     with capsys.disabled():
         print(f" [{compared} codes, {in_band} within 1e-6 of a boundary]", end="")
+    og = PT.oracle_cache(wl)
+    og.pages[:] = pages[0].reshape(-1)
+    PT.assert_close(outs[0][:, None], og.attention(q, wl.block_table, wl.seq_lens), "decode step, over its own pages")
     allowed = {(seq_of[t], h) for t, h in flips}
     PT.assert_close_except(outs[0][:, None], ref, hq // hkv, allowed, "decode step")
 
