@@ -262,9 +262,10 @@ int rq_tree_verify_attention(rq_ctx *ctx, const void *q, int T, const uint64_t *
  * The result equals rq_decode_attention's on the same inputs.
  * Scratch: the split-K partials, the per-unit fragment bounds and round counters live in one
  * file-scope 16 MiB device array that every GPU which loads the library holds until the process
- * exits.  With U = B * num_kv_heads * ceil(group / 8) work units, a call with U > 8,192, or with
- * U + (the device's SM count) > 3,948 partial slots, returns RQ_ERR_CAPACITY; so do B > 8,000
- * and a block table whose max_pages * page_size exceeds INT32_MAX.
+ * exits.  With n = ceil(group / 8) tiles of 8 query rows per kv head, m = min(n, 3) of them per
+ * work unit and U = B * num_kv_heads * ceil(n / m) work units, a call with U > 8,192, or with
+ * (U + the device's SM count) * m > 3,948 partial slots, returns RQ_ERR_CAPACITY; so do
+ * B > 8,000 and a block table whose max_pages * page_size exceeds INT32_MAX.
  * The first call on a device sets up that device (resolves the array's address, reads the SM
  * count, sets the kernel's shared-memory limit); make that first call before any stream
  * capture.  The round counters start at zero (the array is zero-initialised when the library

@@ -24,7 +24,7 @@ struct rq_ctx {
   float* d_ws;            // fragment partials of the stream-K split
   int* d_frag;            // first / last CTA of each unit's fragments [2 U], then rounds done per unit [U]
   size_t ws_floats;
-  size_t max_units;       // max_batch * Hkv * ceil(max_query_tokens * group / 8)
+  size_t max_units;       // most split-K units of a call: max_batch * Hkv * ceil(max_query_tokens * group / 8)
   int max_n_tiles;        // ceil(max_query_tokens * group / 8)
   cudaEvent_t prof_start; // optional diagnostics events (caller-owned)
   cudaEvent_t prof_end;
@@ -174,9 +174,18 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   const size_t table_floats = 2 * rot + 256 + 256;
   const int group = cfg->num_q_heads / hkv;
   ctx->max_n_tiles = (cfg->max_query_tokens * group + 7) / 8;
-  // one partial slot per fragment: at most units + CTAs of them (stream-K split)
-  ctx->max_units = (size_t)cfg->max_batch * hkv * ctx->max_n_tiles;
-  ctx->ws_floats = (ctx->max_units + (size_t)ctx->num_sms) * 8 * rq::kPartialStride;
+  // one partial slot per fragment: at most units + CTAs of them (stream-K split); a unit covers
+  // up to 3 n-tiles of a kv head, so the largest workspace is taken over every T the context
+  // allows (and over the one-n-tile units of a decode step)
+  ctx->max_units = 0;
+  ctx->ws_floats = 0;
+  for (int nt = 1; nt <= ctx->max_n_tiles; ++nt)
+    for (int step = 0; step < 2; ++step) {
+      long long units = 0, floats = 0;
+      rq::attention_workspace(cfg->max_batch, hkv, nt, step != 0, ctx->num_sms, &units, &floats);
+      if ((size_t)units > ctx->max_units) ctx->max_units = (size_t)units;
+      if ((size_t)floats > ctx->ws_floats) ctx->ws_floats = (size_t)floats;
+    }
 
   cudaError_t e = cudaMalloc(&ctx->d_tables, table_floats * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&ctx->d_ws, ctx->ws_floats * sizeof(float));
@@ -342,6 +351,7 @@ static int attention_call(rq_ctx* ctx, const void* q, int T, const uint64_t* tre
   a.ws = ctx->d_ws;
   a.rows = T * ctx->g.group;
   a.n_tiles_n = (a.rows + 7) / 8;
+  a.nt = rq::attention_unit_tiles(a.n_tiles_n, k_new != nullptr);
   a.frag = ctx->d_frag;
   a.cnt = ctx->d_frag + 2 * ctx->max_units;
   a.grid = ctx->num_sms;  // one CTA per SM, each an equal share of the tiles

@@ -40,11 +40,14 @@
 namespace rq {
 namespace {
 
-constexpr int kWarps = kAttnWarps;
-constexpr int kThreads = kWarps * 32;
 constexpr int kLutBytes = lut::kBytes;
 constexpr int kMaxSplitPages = 1024;          // page ids staged per item
 constexpr int kWaitLimit = 1 << 22;           // bounded mbarrier polling (about a second)
+// The running softmax max of the split-K kernel moves only when a score passes it by more than
+// this (base 2): p = 2^(s - m) <= 2^8 in between, so most pairs need no warp reduction and no
+// rescale.  Pairs holding a value norm >= 2^8 take the exact path (p <= 1) so that the fp16
+// operand P' = p * n_v cannot overflow.
+constexpr float kLazyMargin = 8.f;
 
 // Staged tiles.  A slot holds one 16-token tile exactly as a 16-token page chunk is laid out:
 // K codes [16][vb] | V codes [16][vb] | K norms fp16 [16] | V norms fp16 [16].  Each warp owns
@@ -55,15 +58,32 @@ struct Ring {
   static constexpr int VB = BITS * 16;
   static constexpr int SB = 32 * VB + 64;     // slot bytes: 2112 (4-bit), 1600 (3-bit), 1088 (2-bit)
 };
-constexpr int kSlots = 4;                     // per warp: 2 stages x 2 tiles
-constexpr int kStages = kSlots / 2;
-constexpr int kSlotsTotal = kWarps * kSlots;  // 64
-constexpr int kMergeHalfBytes = kWarps * 4 * kPartialStride * 4;  // 4 query columns of all warps
+constexpr int kSlotsTotal = 64;               // staged tiles per CTA, whatever its warp count
+
+// A unit of work covers NT n-tiles (8 query rows each) of one kv head: a warp then shares every
+// dequantised K~ and V~ fragment between NT MMAs, so a verify of T drafts x G heads (e.g. 24
+// rows) unpacks the cache once, not once per 8 rows.  Registers decide the warp count: 16 warps
+// at 128 registers for NT = 1 (decode), 8 warps at up to 255 for NT = 2, 3, whose accumulators
+// (NT x 32 floats of O, NT x 16 registers of queries) need them; the 64 staged tiles are then 4
+// stages per warp instead of 2, so the bytes in flight per SM stay the same.
+template <int NT>
+struct Shape {
+  static constexpr int kWarps = NT == 1 ? kAttnWarps : kAttnWarps / 2;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kSlots = kSlotsTotal / kWarps;  // per warp
+  static constexpr int kStages = kSlots / 2;           // pairs of tiles in flight per warp
+  static constexpr int kRoundTiles = 2 * kWarps;       // a round: one pair of 16-token tiles per warp
+  // A CTA pays about 96 tiles' worth of work (3 rounds of 16 warps) for each extra fragment
+  // (prologue, pipeline refill, the barriers and the merge), measured on 16 x 8K-token decode:
+  // one whole unit per CTA on 128 of 152 SMs beat 13.5 rounds in two fragments per CTA on all 152.
+  static constexpr int kFragmentRounds = 96 / kRoundTiles;
+  static constexpr int kMergeHalfBytes = kWarps * 4 * kPartialStride * 4;  // 4 query columns of all warps
+};
 
 // Shared-memory plan for a CTA whose dynamic window starts at shared address `base`:
-//   [base, lut)          low slots (as many whole slots as fit), or nothing
+//   [base, lut)          low slots (as many whole pairs of slots as fit), or nothing
 //   [lut, lut + 64 KB)   lookup table; lut = first 64 KB-aligned address >= base
-//   [lut + 64 KB, ...)   the remaining slots, page ids int[1024], mbarriers u64[16][2],
+//   [lut + 64 KB, ...)   the remaining slots, page ids int[1024], mbarriers u64[64 / 2],
 //                        centroids float[16], the CTA's position in its tile range (Walk)
 // Between items the two halves of the merge buffer (query columns 0-3 and 4-7) reuse slot
 // space: the low region when it holds a half, else the high slots.
@@ -76,14 +96,12 @@ struct SmemPlan {
   uint32_t merge_hi;   // shared address of merge half 1 (columns 4-7)
   uint32_t end;        // one past the last byte used
 };
-constexpr int kRoundTiles = 2 * kWarps;  // a round: one pair of 16-token tiles per warp
-// A CTA pays about this many rounds for each extra fragment (prologue, pipeline refill, the
-// barriers and the merge), measured on 16 x 8K-token decode: one whole unit per CTA on 128 of
-// 152 SMs beat 13.5 rounds in two fragments per CTA on all 152.
-constexpr int kFragmentRounds = 3;
 
 // Rounds of one unit of a sequence of len tokens: ceil(tiles / kRoundTiles).
-__host__ __device__ __forceinline__ int unit_rounds(int len) { return ((len + 15) / 16 + kRoundTiles - 1) / kRoundTiles; }
+template <int NT>
+__host__ __device__ __forceinline__ int unit_rounds(int len) {
+  return ((len + 15) / 16 + Shape<NT>::kRoundTiles - 1) / Shape<NT>::kRoundTiles;
+}
 
 // Where a CTA stands in its range [x, x_end) of rounds: sequence b, whose units' rounds start
 // at cumb.  Kept in shared memory (thread 0 advances it between fragments) so that none of it
@@ -97,40 +115,43 @@ struct Walk {
   int fin[2];
 };
 constexpr int kWalkBytes = (int)((sizeof(Walk) + 15) / 16 * 16);
-// The tail of the window: page ids, the warps' mbarriers, the centroids and the walk.
-constexpr int kTailBytes = kMaxSplitPages * 4 + kWarps * kStages * 8 + 64 + kWalkBytes;
+// The tail of the window: page ids, the warps' mbarriers (one per stage: kSlotsTotal / 2), the
+// centroids and the walk.
+constexpr int kTailBytes = kMaxSplitPages * 4 + (kSlotsTotal / 2) * 8 + 64 + kWalkBytes;
 
 // The fragment at the walk's position: rounds [r0, r1) of the rb rounds of unit uib of
-// sequence b (uib = kv head * n_tiles_n + n-tile), i.e. its tiles [t0, t1) of tb.
+// sequence b (uib = kv head * units per head + unit of the head), i.e. its tiles [t0, t1) of tb.
 struct Frag {
   int tb, rb, uib, r0, r1, t0, t1;
 };
+template <int NT>
 __device__ __forceinline__ Frag frag_at(const Walk& w) {
   Frag f;
   f.tb = (w.len + 15) / 16;
-  f.rb = max(unit_rounds(w.len), 1);          // >= 1 whenever the walk has work left
+  f.rb = max(unit_rounds<NT>(w.len), 1);      // >= 1 whenever the walk has work left
   const int off = (int)(w.x - w.cumb);        // < the rounds of one sequence's units
   f.uib = off / f.rb;
   f.r0 = off % f.rb;
   f.r1 = (int)min((long long)f.rb, f.r0 + (w.x_end - w.x));
-  f.t0 = f.r0 * kRoundTiles;
-  f.t1 = min(f.tb, f.r1 * kRoundTiles);
+  f.t0 = f.r0 * Shape<NT>::kRoundTiles;
+  f.t1 = min(f.tb, f.r1 * Shape<NT>::kRoundTiles);
   return f;
 }
 
-template <int BITS>
+template <int BITS, int NT>
 __host__ __device__ constexpr SmemPlan smem_plan(uint32_t base) {
+  constexpr uint32_t merge_half = Shape<NT>::kMergeHalfBytes;
   SmemPlan p{};
   p.lut = (base + 0xFFFFu) & ~0xFFFFu;
-  int n_lo = (int)((p.lut - base) / Ring<BITS>::SB);
+  int n_lo = (int)((p.lut - base) / Ring<BITS>::SB) & ~1;  // whole pairs: a warp's slots 2s, 2s+1 adjoin
   if (n_lo > kSlotsTotal) n_lo = kSlotsTotal;
   p.n_lo = n_lo;
   p.hi = p.lut + kLutBytes;
   const uint32_t hi_bytes = (uint32_t)(kSlotsTotal - n_lo) * Ring<BITS>::SB;
-  const bool lo_merge = (uint32_t)n_lo * Ring<BITS>::SB >= (uint32_t)kMergeHalfBytes;
+  const bool lo_merge = (uint32_t)n_lo * Ring<BITS>::SB >= merge_half;
   p.merge_lo = lo_merge ? base : p.hi;
-  p.merge_hi = lo_merge ? p.hi : p.hi + kMergeHalfBytes;
-  const uint32_t hi_need = lo_merge ? kMergeHalfBytes : 2 * kMergeHalfBytes;
+  p.merge_hi = lo_merge ? p.hi : p.hi + merge_half;
+  const uint32_t hi_need = lo_merge ? merge_half : 2 * merge_half;
   p.tail = p.hi + (hi_bytes > hi_need ? hi_bytes : hi_need);
   p.end = p.tail + kTailBytes;
   return p;
@@ -316,11 +337,23 @@ __device__ __forceinline__ void load_stage(Raw<BITS>& r, const uint8_t* st, int 
 //        k-slots 2t,2t+1 and U2 gives (4kc+1, 4kc+3) for 2t+8,2t+9, and q~ is packed to match.
 // 3-bit: X0 = W0.lo | W2.hi (T1, pairs 2k), X1 = W2.lo | W0.hi (T2, pairs 2k+1),
 //        X2 = W1.lo | (W2>>2).hi (T1, pairs 8+2k), X3 = (W2>>2).lo | W1.hi (T2, pairs 9+2k).
-template <int BITS>
-__device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const uint32_t (&qf)[8][2],
+// With NT n-tiles, each A fragment feeds NT MMAs (one per n-tile's queries); with one, the even
+// and odd k-chunks accumulate in two chains for the MMAs' latency.
+template <int BITS, int NT>
+__device__ __forceinline__ void qk_tile(float (&s)[NT][4], const Raw<BITS>& r, const uint32_t (&qf)[NT][8][2],
                                         uint32_t key1, uint32_t key2) {
-  s[0] = s[1] = s[2] = s[3] = 0.f;
+#pragma unroll
+  for (int i = 0; i < NT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
   float s2[4] = {0.f, 0.f, 0.f, 0.f};
+  auto mma_all = [&](int kc, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+    if constexpr (NT == 1) {
+      if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[0][kc][0], qf[0][kc][1]);
+      else mma16816(s[0], a0, a1, a2, a3, qf[0][kc][0], qf[0][kc][1]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < NT; ++i) mma16816(s[i], a0, a1, a2, a3, qf[i][kc][0], qf[i][kc][1]);
+    }
+  };
   if constexpr (BITS == 4) {
     const uint32_t k0[4] = {r.k[0].x, r.k[0].y, r.k[0].z, r.k[0].w};
     const uint32_t k1[4] = {r.k[1].x, r.k[1].y, r.k[1].z, r.k[1].w};
@@ -339,8 +372,7 @@ __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const
         a2 = lut_at<3, 0>(k0[w], key1, key2);
         a3 = lut_at<3, 0>(k1[w], key1, key2);
       }
-      if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
-      else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+      mma_all(kc, a0, a1, a2, a3);
     }
   } else if constexpr (BITS == 2) {
     const uint32_t k0[2] = {r.k[0].x, r.k[0].y};
@@ -352,8 +384,7 @@ __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const
       const uint32_t a1 = lut_dyn<0>(k1[w], byte, key1, key2);
       const uint32_t a2 = lut_dyn<1>(k0[w], byte, key1, key2);
       const uint32_t a3 = lut_dyn<1>(k1[w], byte, key1, key2);
-      if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
-      else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+      mma_all(kc, a0, a1, a2, a3);
     }
   } else {
     uint32_t X[2][4];
@@ -372,20 +403,26 @@ __device__ __forceinline__ void qk_tile(float (&s)[4], const Raw<BITS>& r, const
       const uint32_t a1 = lut_dyn<0>(X[1][2 * hi], byte, key1, key2);
       const uint32_t a2 = lut_dyn<1>(X[0][2 * hi + 1], byte, key1, key2);
       const uint32_t a3 = lut_dyn<1>(X[1][2 * hi + 1], byte, key1, key2);
-      if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
-      else mma16816(s, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+      mma_all(kc, a0, a1, a2, a3);
     }
   }
+  if constexpr (NT == 1) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) s[i] += s2[i];
+    for (int i = 0; i < 4; ++i) s[0][i] += s2[i];
+  }
 }
 
 // A operand of O^T += V~^T P^T for m-tile mt: rows g / g+8 hold dims 16g+2mt / 16g+2mt+1,
 // k-slots 2t,2t+1 and 2t+8,2t+9 the lane's two V token pairs.  Index bytes carry one
 // dim of two tokens, so the two tokens' code words are interleaved first.
-template <int BITS>
-__device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, uint32_t pb0, uint32_t pb1,
+// Each A fragment feeds NT MMAs, one per n-tile's P^T (pb[i] = its two B registers).
+template <int BITS, int NT>
+__device__ __forceinline__ void pv_tile(float (&o)[NT][8][4], const Raw<BITS>& r, const uint32_t (&pb)[NT][2],
                                         uint32_t key1, uint32_t key2, int g) {
+  auto mma_all = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+#pragma unroll
+    for (int i = 0; i < NT; ++i) mma16816(o[i][mt], a0, a1, a2, a3, pb[i][0], pb[i][1]);
+  };
   if constexpr (BITS == 4) {
     uint32_t XE[2][2], XO[2][2];  // [token pair][word]
 #pragma unroll
@@ -403,7 +440,7 @@ __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, ui
       const uint32_t a1 = lut_dyn<0>(XO[0][w], j, key1, key2);
       const uint32_t a2 = lut_dyn<0>(XE[1][w], j, key1, key2);
       const uint32_t a3 = lut_dyn<0>(XO[1][w], j, key1, key2);
-      mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+      mma_all(mt, a0, a1, a2, a3);
     }
   } else if constexpr (BITS == 2) {
     // Nibble-interleave each token pair: byte k of XE = (dims 4k, 4k+1 of the first token,
@@ -424,7 +461,7 @@ __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, ui
       const uint32_t a1 = lut_dyn<1>(x0, j, key1, key2);
       const uint32_t a2 = lut_dyn<0>(x1, j, key1, key2);
       const uint32_t a3 = lut_dyn<1>(x1, j, key1, key2);
-      mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+      mma_all(mt, a0, a1, a2, a3);
     }
   } else {
     const int sh = 2 * (g & 1);
@@ -457,7 +494,7 @@ __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, ui
         a2 = lut_dyn<1>(XE2[1], j, key1, key2);
         a3 = lut_dyn<1>(XO2[1], j, key1, key2);
       }
-      mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+      mma_all(mt, a0, a1, a2, a3);
     }
   }
 }
@@ -470,19 +507,20 @@ __device__ __forceinline__ void pv_tile(float (&o)[8][4], const Raw<BITS>& r, ui
 // Zeros for an empty (or invalid) sequence.  All 32 lanes must call it.
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ float4 merge_splits(const Geometry& g, const AttnArgs& a, int b, int h, int row, int lane) {
-  const int nt = row >> 3, col = row & 7;
+  const int rows_u = 8 * a.nt;  // query rows per unit
+  const int ug = row / rows_u, col = row - ug * rows_u;
   int len = a.seq_lens[b];
   const int cap = a.max_pages * g.page_size;
   len = len < 0 ? 0 : (len > cap ? cap : len);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (len == 0 || len < a.T) return acc;
   // the unit's fragments: CTAs first .. last, partials at slots unit + c
-  const int unit = (b * g.num_kv_heads + h) * a.n_tiles_n + nt;
+  const int unit = (b * g.num_kv_heads + h) * ((a.n_tiles_n + a.nt - 1) / a.nt) + ug;
   // written by other CTAs of this launch (or the previous kernel): read through L2
   const int first = __ldcg(a.frag + 2 * unit), last = __ldcg(a.frag + 2 * unit + 1);
   if (first < 0 || last < first || last >= a.grid) return acc;  // a launch that gave up early
   const int ns = last - first + 1;
-  const size_t stride = (size_t)8 * kPartialStride;  // between consecutive slots
+  const size_t stride = (size_t)rows_u * kPartialStride;  // between consecutive slots
   const float* base = a.ws + (size_t)(unit + first) * stride + (size_t)col * kPartialStride;
   // (m, l) of the lane's slots, one load each; running max and rescaled sum, then warp-merged
   float M = -CUDART_INF_F, L = 0.f;
@@ -638,18 +676,18 @@ __device__ __forceinline__ void rotated_query(float (&y)[32], const Geometry& g,
 // min(CTAs, rounds), so that every part is non-empty: the combine takes the CTAs between a
 // unit's first and last fragment to all hold one.  CTAs past the parts idle.  When every unit
 // has the same rounds and there are no more units than CTAs, one whole unit per part is the
-// other candidate: a CTA's cost is its rounds plus kFragmentRounds per fragment, and equal parts
+// other candidate: a CTA's cost is its rounds plus frag_rounds per fragment, and equal parts
 // that do not divide the units cost most CTAs two fragments.  I is uint32_t whenever
 // total * grid fits it (every practical launch: the 64-bit division is a long software
 // sequence), else long long.
 template <typename I>
-__device__ __forceinline__ void partition(I total, I n_units, I max_rounds, I grid, I cta, long long& x0,
-                                          long long& x1) {
+__device__ __forceinline__ void partition(I total, I n_units, I max_rounds, I grid, I cta, I frag_rounds,
+                                          long long& x0, long long& x1) {
   I parts = min(grid, total);
   if (n_units > 0 && n_units <= grid && total == n_units * max_rounds) {
     const I per_part = (total + parts - 1) / parts;
-    const I cost_split = per_part + (max_rounds % per_part == 0 ? 1 : 2) * (I)kFragmentRounds;
-    if (max_rounds + (I)kFragmentRounds <= cost_split) parts = n_units;
+    const I cost_split = per_part + (max_rounds % per_part == 0 ? 1 : 2) * frag_rounds;
+    if (max_rounds + frag_rounds <= cost_split) parts = n_units;
   }
   x0 = cta < parts ? (long long)(total * cta / parts) : 0;
   x1 = cta < parts ? (long long)(total * (cta + 1) / parts) : 0;
@@ -683,8 +721,8 @@ __device__ __forceinline__ void walk_advance(Walk& w, const Frag& f, int upb, co
 // Decode step: quantizes the newest token (position len - 1) of sequence b, kv head h into its
 // slot of the cache, one warp (lanes 0-15 K, 16-31 V, 8 dims each).  The caller is the warp that
 // stages the unit's last tile, which holds the token, and issues that tile's copy only after
-// this returns: the proxy fence and the warp barrier order the writes before it.  n-tiles of one
-// kv head may write the same token from several CTAs, with equal bytes.
+// this returns: the proxy fence and the warp barrier order the writes before it.  The units of
+// one kv head (more than 3 n-tiles) may write the same token from several CTAs, with equal bytes.
 template <int BITS>
 __device__ __forceinline__ void append_token(const Geometry& g, const AttnArgs& a, int b, int h, int len) {
   const int lane = threadIdx.x & 31, half = lane >> 4, j = lane & 15;
@@ -709,14 +747,19 @@ __device__ __forceinline__ void append_token(const Geometry& g, const AttnArgs& 
 
 // PRE: the queries were rotated before the launch (dense rotation).  STEP: a decode step that
 // quantizes each sequence's newest token first (a.k_new, a.v_new; structured rotations).
-template <int BITS, bool PRE, bool STEP>
-__global__ void __launch_bounds__(kThreads, 1)
+// NT: query n-tiles per unit (Shape), each warp carrying all NT of them through every tile.
+template <int BITS, bool PRE, bool STEP, int NT>
+__global__ void __launch_bounds__(Shape<NT>::kThreads, 1)
 attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   using R = Ring<BITS>;
+  constexpr int kWarps = Shape<NT>::kWarps;
+  constexpr int kThreads = Shape<NT>::kThreads;
+  constexpr int kSlots = Shape<NT>::kSlots;
+  constexpr int kStages = Shape<NT>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t dyn_base = (uint32_t)__cvta_generic_to_shared(smem);
-  const SmemPlan plan = smem_plan<BITS>(dyn_base);
-  if (plan.end - dyn_base > (uint32_t)smem_bytes) {  // unexpected reserved shared memory
+  const SmemPlan plan = smem_plan<BITS, NT>(dyn_base);
+  if (plan.end - dyn_base > (uint32_t)smem_bytes || a.nt != NT) {  // unexpected reserved shared memory
     if (threadIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
     return;
   }
@@ -724,7 +767,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   uint32_t* lut_words = reinterpret_cast<uint32_t*>(at(plan.lut));
   int* page_ids = reinterpret_cast<int*>(at(plan.tail));
   uint64_t* mbar = reinterpret_cast<uint64_t*>(page_ids + kMaxSplitPages);
-  float* cb = reinterpret_cast<float*>(mbar + kWarps * kStages);
+  float* cb = reinterpret_cast<float*>(mbar + kSlotsTotal / 2);
   Walk* walk = reinterpret_cast<Walk*>(cb + 16);
   float* const merge_lo = reinterpret_cast<float*>(at(plan.merge_lo));
   float* const merge_hi = reinterpret_cast<float*>(at(plan.merge_hi));
@@ -756,12 +799,24 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   const uint32_t key2 = key1 + 128u;
   const int P = g.page_size;
   const int tiles_per_page = P / 16;
-  // shared addresses of this warp's slots: stage st uses slots 2st (first tile) and 2st + 1
-  auto slot_of = [&](int i) -> uint32_t {
-    const int sl = warp * kSlots + i;
-    return sl < plan.n_lo ? dyn_base + (uint32_t)(sl * R::SB) : plan.hi + (uint32_t)((sl - plan.n_lo) * R::SB);
+  // tiles per page as a shift when it is a power of two (page sizes 16, 32, 64, 128, 256)
+  const int tpp_shift = (tiles_per_page & (tiles_per_page - 1)) == 0 ? __ffs(tiles_per_page) - 1 : -1;
+  const int n_issue = P == 16 ? 2 : 8;                 // lanes that issue a pair's bulk copies
+  const uint32_t issue_mask = P == 16 ? 0x3u : 0xFFu;
+  // Shared address of this warp's stage st: slots 2st (first tile) and 2st + 1 (second tile,
+  // SB bytes after the first: the slot plan keeps a warp's pairs of slots on one side of the table).
+  const int sl0 = warp * kSlots;
+  const uint32_t slot0 = sl0 < plan.n_lo ? dyn_base + (uint32_t)(sl0 * R::SB) : plan.hi + (uint32_t)((sl0 - plan.n_lo) * R::SB);
+  const uint32_t slot2 = sl0 + 2 < plan.n_lo ? dyn_base + (uint32_t)((sl0 + 2) * R::SB)
+                                             : plan.hi + (uint32_t)((sl0 + 2 - plan.n_lo) * R::SB);
+  auto stage_slot = [&](int st) -> uint32_t {
+    if constexpr (kStages == 2) {
+      return st ? slot2 : slot0;
+    } else {
+      const int sl = sl0 + 2 * st;
+      return sl < plan.n_lo ? dyn_base + (uint32_t)(sl * R::SB) : plan.hi + (uint32_t)((sl - plan.n_lo) * R::SB);
+    }
   };
-  const uint32_t slot0 = slot_of(0), slot1 = slot_of(1), slot2 = slot_of(2), slot3 = slot_of(3);
   const uint32_t mbar_addr = (uint32_t)__cvta_generic_to_shared(mbar + warp * kStages);
   if (lane == 0) {
     for (int st = 0; st < kStages; ++st) mbar_init(mbar_addr + 8 * st, 1);
@@ -774,7 +829,8 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   // cum[b] = rounds of all units of sequences < b and lens[b] = sequence b's clamped tokens,
   // built with a block scan at the start of the window: slots and table, unused before the
   // first fragment (at most 8001 x 8 + 8000 x 4 bytes; the table and the 64 slots span more).
-  const int upb = g.num_kv_heads * a.n_tiles_n;  // units per sequence
+  const int n_ug = (a.n_tiles_n + NT - 1) / NT;  // units per kv head
+  const int upb = g.num_kv_heads * n_ug;          // units per sequence
   const int cap = a.max_pages * P;
   {
     long long* cum = reinterpret_cast<long long*>(smem);
@@ -793,7 +849,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           if (blockIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_LEN);
           len = len < 0 ? 0 : (len > cap ? cap : len);
         }
-        v = (long long)unit_rounds(len) * upb;
+        v = (long long)unit_rounds<NT>(len) * upb;
         lens[bb] = len;
       }
       int nu = v > 0 ? upb : 0, mr = (int)(v / upb);
@@ -837,9 +893,10 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     __syncthreads();
     long long x0, x1;
     if (total * gridDim.x < (1LL << 32))
-      partition<uint32_t>((uint32_t)total, n_units, max_rounds, gridDim.x, blockIdx.x, x0, x1);
+      partition<uint32_t>((uint32_t)total, n_units, max_rounds, gridDim.x, blockIdx.x, Shape<NT>::kFragmentRounds,
+                          x0, x1);
     else
-      partition<long long>(total, n_units, max_rounds, gridDim.x, blockIdx.x, x0, x1);
+      partition<long long>(total, n_units, max_rounds, gridDim.x, blockIdx.x, Shape<NT>::kFragmentRounds, x0, x1);
     int lo = 0, hi = a.B;  // the last sequence b with cum[b] <= x0, which skips empty ones
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -865,23 +922,26 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   for (long long n_frag = 0; n_frag < max_fragments; ++n_frag) {
     if (walk->x >= walk->x_end) break;
     const int len = walk->len;
-    const Frag fr = frag_at(*walk);
+    const Frag fr = frag_at<NT>(*walk);
     const int t1 = fr.t1;
     struct {
-      int b, h, nt;
-    } it = {walk->b, fr.uib / a.n_tiles_n, fr.uib % a.n_tiles_n};
+      int b, h, nt0;
+    } it = {walk->b, fr.uib / n_ug, (fr.uib % n_ug) * NT};
 
-    // q~ = R_k q * sm_scale * log2(e) for query column gq of this n-tile, the lane's 32 dims,
-    // formed once the fragment's first copies are in flight (below).
-    uint32_t qf[8][2];
-    const int row = it.nt * 8 + gq;  // query row of the kv head: draft j = row / group, head row % group
-    int last_pos[2];                  // last position wholly visible to query columns 2tq, 2tq+1
+    // q~ = R_k q * sm_scale * log2(e) for query column gq of each of the unit's n-tiles, the
+    // lane's 32 dims, formed once the fragment's first copies are in flight (below).
+    uint32_t qf[NT][8][2];
+    int last_pos[NT][2];  // last position wholly visible to query columns 2tq, 2tq+1 of each n-tile
 
-    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
-    float l_run[2] = {0.f, 0.f};
-    float o[8][4];
+    float m_run[NT][2], l_run[NT][2];
+    float o[NT][8][4];
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    for (int i = 0; i < NT; ++i) {
+      m_run[i][0] = m_run[i][1] = -CUDART_INF_F;
+      l_run[i][0] = l_run[i][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) o[i][mt][0] = o[i][mt][1] = o[i][mt][2] = o[i][mt][3] = 0.f;
+    }
 
     // The fragment in chunks of at most kMaxSplitPages pages (one chunk unless a CTA's range
     // is very long); the warps' states carry over from chunk to chunk.
@@ -901,39 +961,47 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     __syncthreads();
 
     // The chunk's tiles, taken two at a time: pair q = tiles tile0 + 2q and tile0 + 2q + 1
-    // (the second exists unless the chunk ends there); warp w takes pairs w + 16k.
+    // (the second exists unless the chunk ends there); warp w takes pairs w + kWarps k.
     const int n_pairs = (tile1 - tile0 + 1) / 2;
     // A pair whose second tile lies past the chunk reads a stale slot for it: its positions,
     // all past pos_lim, are masked like positions past the sequence.
     const int pos_lim = tile1 * 16 - 1;
     const int n_w = (warp < n_pairs && !broken) ? (n_pairs - 1 - warp) / kWarps + 1 : 0;
-    // Lanes 0 and 1 stage tile `lane` of the warp's k-th pair into stage k % 2 (slots 2(k%2),
-    // 2(k%2)+1): one bulk copy when a page is one tile, else K codes, V codes and the two norm
-    // runs.  Lane 0 announces the stage's bytes first.
+    // A page-sized tile (P = 16) is one bulk copy: lanes 0 and 1 stage tile `lane` of the warp's
+    // k-th pair into stage k % kStages.  A tile of a larger page is four copies (K codes, V codes
+    // and the two norm runs): lanes 0-3 copy the first tile's, 4-7 the second's, one each.
+    // Lane 0 announces the stage's bytes first.
     auto issue = [&](int k) {
       const int st = k % kStages;
       const int tA = tile0 + 2 * (warp + k * kWarps);
       const int nt_pair = tA + 1 < tile1 ? 2 : 1;
       const uint32_t mb = mbar_addr + 8 * st;
       if (lane == 0) mbar_expect_tx(mb, nt_pair * R::SB);
-      __syncwarp(0x3u);
-      if (lane < nt_pair) {
-        const int tile = tA + lane;
-        const uint32_t dst = st ? (lane ? slot3 : slot2) : (lane ? slot1 : slot0);
-        // chunk (page, kv head) at page * Hkv * page_bytes + h * page_bytes: both products stay
-        // below 2^31 per page (checked at creation), so a 32 x 32 -> 64-bit multiply-add forms it
-        const uint32_t page_stride = (uint32_t)(g.num_kv_heads * g.page_bytes);
-        const uint32_t head_off = (uint32_t)(it.h * g.page_bytes);
-        if (P == 16) {  // tile t is page t
-          const uint32_t page = (uint32_t)page_ids[tile - p0];
-          bulk_g2s(dst, a.pages + ((uint64_t)page * page_stride + head_off), R::SB, mb);
-        } else {
-          const int pi = tile / tiles_per_page - p0, off = (tile % tiles_per_page) * 16;
-          const uint8_t* chunk = a.pages + ((uint64_t)(uint32_t)page_ids[pi] * page_stride + head_off);
-          bulk_g2s(dst, chunk + (size_t)off * R::VB, 16 * R::VB, mb);
-          bulk_g2s(dst + 16 * R::VB, chunk + (size_t)(P + off) * R::VB, 16 * R::VB, mb);
-          bulk_g2s(dst + 32 * R::VB, chunk + (size_t)2 * P * R::VB + 2 * off, 32, mb);
-          bulk_g2s(dst + 32 * R::VB + 32, chunk + (size_t)2 * P * R::VB + 2 * P + 2 * off, 32, mb);
+      __syncwarp(issue_mask);
+      // chunk (page, kv head) at page * Hkv * page_bytes + h * page_bytes: both products stay
+      // below 2^31 per page (checked at creation), so a 32 x 32 -> 64-bit multiply-add forms it
+      const uint32_t page_stride = (uint32_t)(g.num_kv_heads * g.page_bytes);
+      const uint32_t head_off = (uint32_t)(it.h * g.page_bytes);
+      const uint32_t sbase = stage_slot(st);
+      if (P == 16) {  // tile t is page t
+        if (lane < nt_pair) {
+          const uint32_t page = (uint32_t)page_ids[tA + lane - p0];
+          bulk_g2s(sbase + (lane ? (uint32_t)R::SB : 0u), a.pages + ((uint64_t)page * page_stride + head_off), R::SB,
+                   mb);
+        }
+      } else {
+        const int which = lane >> 2, sec = lane & 3;
+        if (which < nt_pair) {
+          const int tile = tA + which;
+          const int pq = tpp_shift >= 0 ? tile >> tpp_shift : tile / tiles_per_page;
+          const int off = (tile - pq * tiles_per_page) * 16;
+          const uint8_t* chunk = a.pages + ((uint64_t)(uint32_t)page_ids[pq - p0] * page_stride + head_off);
+          const uint32_t dst = sbase + (which ? (uint32_t)R::SB : 0u) +
+                               (sec == 0 ? 0u : sec == 1 ? 16u * R::VB : 32u * R::VB + (sec == 3 ? 32u : 0u));
+          const size_t src = sec == 0 ? (size_t)off * R::VB
+                           : sec == 1 ? (size_t)(P + off) * R::VB
+                                      : (size_t)2 * P * R::VB + (sec == 3 ? 2 * P : 0) + 2 * off;
+          bulk_g2s(dst, chunk + src, sec < 2 ? 16u * R::VB : 32u, mb);
         }
       }
     };
@@ -942,7 +1010,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     // deferring the pair's copy when it is one of the first stages.
     const bool appends = STEP && tile1 == fr.tb && warp == (n_pairs - 1) % kWarps;
     const int n_first = min(kStages, n_w) - (appends && n_w <= kStages ? 1 : 0);
-    if (lane < 2 && n_first > 0) {
+    if (lane < n_issue && n_first > 0) {
       fence_proxy_async();
       for (int k = 0; k < n_first; ++k) issue(k);
     }
@@ -951,30 +1019,34 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     if constexpr (STEP) {
       if (appends) {
         append_token<BITS>(g, a, it.b, it.h, len);
-        if (n_w > 0 && n_w <= kStages && lane < 2) {
+        if (n_w > 0 && n_w <= kStages && lane < n_issue) {
           fence_proxy_async();
           issue(n_w - 1);
         }
       }
     }
     if (tile0 == fr.t0) {  // the fragment's first chunk: its copies overlap the query's loads
-      float y[32];
-      rotated_query<PRE>(y, g, a, it.b, it.h, row, tq);
       // k-slot order of the K operand: dims (4kc, 4kc+1 | 4kc+2, 4kc+3) of the lane's 32, or
       // (4kc, 4kc+2 | 4kc+1, 4kc+3) for 2-bit codes
       constexpr int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;
 #pragma unroll
-      for (int kc = 0; kc < 8; ++kc) {
-        qf[kc][0] = pack_half2(y[4 * kc] * g.q_scale, y[4 * kc + s1] * g.q_scale);
-        qf[kc][1] = pack_half2(y[4 * kc + s2] * g.q_scale, y[4 * kc + 3] * g.q_scale);
-      }
+      for (int i = 0; i < NT; ++i) {
+        float y[32];
+        // query row of the kv head: draft j = row / group, head row % group
+        rotated_query<PRE>(y, g, a, it.b, it.h, (it.nt0 + i) * 8 + gq, tq);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int rc = it.nt * 8 + 2 * tq + c;
-        const int j = rc < a.rows ? rc / g.group : a.T - 1;
-        // chain: row j sees positions <= len - T + j; tree: the prefix for sure (the drafts
-        // by their mask bit), so only the prefix counts as wholly visible
-        last_pos[c] = a.tree_mask ? len - a.T - 1 : len - a.T + j;
+        for (int kc = 0; kc < 8; ++kc) {
+          qf[i][kc][0] = pack_half2(y[4 * kc] * g.q_scale, y[4 * kc + s1] * g.q_scale);
+          qf[i][kc][1] = pack_half2(y[4 * kc + s2] * g.q_scale, y[4 * kc + 3] * g.q_scale);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int rc = (it.nt0 + i) * 8 + 2 * tq + c;
+          const int j = rc < a.rows ? rc / g.group : a.T - 1;
+          // chain: row j sees positions <= len - T + j; tree: the prefix for sure (the drafts
+          // by their mask bit), so only the prefix counts as wholly visible
+          last_pos[i][c] = a.tree_mask ? len - a.T - 1 : len - a.T + j;
+        }
       }
     }
     if (first_chunk) __syncthreads();  // the table is complete
@@ -988,114 +1060,160 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       }
       phase ^= 1u << st;
       consumed = k + 1;
-      const uint8_t* stA = at(st ? slot2 : slot0);
-      const uint8_t* stB = at(st ? slot3 : slot1);
+      const uint8_t* stA = at(stage_slot(st));
+      const uint8_t* stB = stA + R::SB;
       const int pos0 = (tile0 + 2 * (warp + k * kWarps)) * 16;  // first token of the pair
 
       // ---- scores (base 2) of the lane's four K rows (two per tile) for columns 2tq, 2tq+1
-      float sc[8];  // [tile][row][col]
+      // of each n-tile.  The running max moves lazily: only when some score of the pair lies
+      // more than kLazyMargin above it (or the pair holds a value norm that could overflow the
+      // fp16 P' = p * n_v) does the warp reduce the pair's exact max and rescale; otherwise
+      // p = 2^(s - m_run) <= 2^kLazyMargin and nothing is reduced or rescaled.
+      float sc[NT][8];  // [n-tile][tile][row][col]: the scores, then p
       uint32_t nv_bits[2];
       {
         Raw<BITS> rk;
-        float s[4];
+        float s[NT][4];
         load_stage<BITS>(rk, stA, gq, tq);
-        qk_tile<BITS>(s, rk, qf, key1, key2);
+        qk_tile<BITS, NT>(s, rk, qf, key1, key2);
         nv_bits[0] = rk.nv;
         const float nk0 = half_bits_to_float(rk.nk & 0xffffu), nk1 = half_bits_to_float(rk.nk >> 16);
-        sc[0] = s[0] * nk0;
-        sc[1] = s[1] * nk0;
-        sc[2] = s[2] * nk1;
-        sc[3] = s[3] * nk1;
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          sc[i][0] = s[i][0] * nk0;
+          sc[i][1] = s[i][1] * nk0;
+          sc[i][2] = s[i][2] * nk1;
+          sc[i][3] = s[i][3] * nk1;
+        }
         load_stage<BITS>(rk, stB, gq, tq);
-        qk_tile<BITS>(s, rk, qf, key1, key2);
+        qk_tile<BITS, NT>(s, rk, qf, key1, key2);
         nv_bits[1] = rk.nv;
         const float nk2 = half_bits_to_float(rk.nk & 0xffffu), nk3 = half_bits_to_float(rk.nk >> 16);
-        sc[4] = s[0] * nk2;
-        sc[5] = s[1] * nk2;
-        sc[6] = s[2] * nk3;
-        sc[7] = s[3] * nk3;
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          sc[i][4] = s[i][0] * nk2;
+          sc[i][5] = s[i][1] * nk2;
+          sc[i][6] = s[i][2] * nk3;
+          sc[i][7] = s[i][3] * nk3;
+        }
       }
       // Pairs wholly inside every column's visible range skip the per-element mask.
-      const bool interior = __all_sync(0xffffffffu, pos0 + 31 <= min(min(last_pos[0], last_pos[1]), pos_lim));
+      int vis_min = pos_lim;
+#pragma unroll
+      for (int i = 0; i < NT; ++i) vis_min = min(vis_min, min(last_pos[i][0], last_pos[i][1]));
+      const bool interior = __all_sync(0xffffffffu, pos0 + 31 <= vis_min);
       if (!interior) {
-        const int draft0 = last_pos[0] + 1;  // tree: the first draft follows the prefix
-        uint64_t draft_mask[2] = {0ull, 0ull};  // tree: the columns' draft visibility bits (re-read here,
-        if (a.tree_mask) {                      // not held in registers through the loop)
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          const int draft0 = last_pos[i][0] + 1;  // tree: the first draft follows the prefix
+          uint64_t draft_mask[2] = {0ull, 0ull};  // tree: the columns' draft visibility bits (re-read here,
+          if (a.tree_mask) {                      // not held in registers through the loop)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int rc = (it.nt0 + i) * 8 + 2 * tq + c;
+              draft_mask[c] = a.tree_mask[(size_t)it.b * a.T + (rc < a.rows ? rc / g.group : a.T - 1)];
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int pos = pos0 + 16 * (e >> 2) + rho<BITS>(gq) + 8 * ((e >> 1) & 1);
+            bool vis;
+            if (a.tree_mask) {
+              const int d = pos - draft0;
+              vis = d < 0 || (d < a.T && ((draft_mask[e & 1] >> d) & 1ull));
+            } else {
+              vis = pos <= last_pos[i][e & 1];
+            }
+            if (!vis || pos > pos_lim) sc[i][e] = -CUDART_INF_F;
+          }
+        }
+      }
+      // (with no max yet, m_run = -inf, any visible score passes the test: the exact path)
+      float cmax[NT][2];
+      bool grow = false;
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        cmax[i][0] = fmaxf(fmaxf(sc[i][0], sc[i][2]), fmaxf(sc[i][4], sc[i][6]));
+        cmax[i][1] = fmaxf(fmaxf(sc[i][1], sc[i][3]), fmaxf(sc[i][5], sc[i][7]));
+        grow = grow || cmax[i][0] > m_run[i][0] + kLazyMargin || cmax[i][1] > m_run[i][1] + kLazyMargin;
+      }
+      // fp16 norms at or above 2^8 (bits >= 0x5C00) take the exact path, where p <= 1
+      const uint32_t nv_hi = max(max(nv_bits[0] & 0xffffu, nv_bits[0] >> 16), max(nv_bits[1] & 0xffffu, nv_bits[1] >> 16));
+      float m_use[NT][2];
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        m_use[i][0] = m_run[i][0];
+        m_use[i][1] = m_run[i][1];
+      }
+      if (__any_sync(0xffffffffu, grow || nv_hi >= 0x5C00u)) {
+        float alpha[NT][2];
+        bool moved = false;
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            const int rc = it.nt * 8 + 2 * tq + c;
-            draft_mask[c] = a.tree_mask[(size_t)it.b * a.T + (rc < a.rows ? rc / g.group : a.T - 1)];
+            float tmax = cmax[i][c];
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+            const float m_new = fmaxf(m_run[i][c], tmax);
+            m_use[i][c] = m_new == -CUDART_INF_F ? 0.f : m_new;
+            alpha[i][c] = ex2(m_run[i][c] - m_use[i][c]);  // 0 when there was no max yet
+            l_run[i][c] *= alpha[i][c];
+            m_run[i][c] = m_new;
+            moved = moved || alpha[i][c] != 1.f;
           }
         }
+        if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int pos = pos0 + 16 * (e >> 2) + rho<BITS>(gq) + 8 * ((e >> 1) & 1);
-          bool vis;
-          if (a.tree_mask) {
-            const int i = pos - draft0;
-            vis = i < 0 || (i < a.T && ((draft_mask[e & 1] >> i) & 1ull));
-          } else {
-            vis = pos <= last_pos[e & 1];
-          }
-          if (!vis || pos > pos_lim) sc[e] = -CUDART_INF_F;
-        }
-      }
-      float alpha[2];
+          for (int i = 0; i < NT; ++i)
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float tmax = fmaxf(fmaxf(sc[c], sc[c + 2]), fmaxf(sc[c + 4], sc[c + 6]));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-        const float m_new = fmaxf(m_run[c], tmax);
-        const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-        alpha[c] = ex2(m_run[c] - m_use);
-        float lsum = 0.f;
-#pragma unroll
-        for (int e = c; e < 8; e += 2) {
-          sc[e] = ex2(sc[e] - m_use);  // now p; masked entries give 0
-          lsum += sc[e];
-        }
-        l_run[c] = l_run[c] * alpha[c] + lsum;
-        m_run[c] = m_new;
-      }
-      // Rescale the accumulators only when some column's running max moved (rare after the
-      // first pairs); alpha is exactly 1 otherwise, so skipping changes nothing.
-      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][0] *= alpha[0];
-          o[mt][2] *= alpha[0];
-          o[mt][1] *= alpha[1];
-          o[mt][3] *= alpha[1];
+            for (int mt = 0; mt < 8; ++mt) {
+              o[i][mt][0] *= alpha[i][0];
+              o[i][mt][2] *= alpha[i][0];
+              o[i][mt][1] *= alpha[i][1];
+              o[i][mt][3] *= alpha[i][1];
+            }
         }
       }
       // P' = p * n_v, zero for masked tokens whatever their stored norm; to the B layout.
-      uint32_t pb[2][2];
+      uint32_t pb[2][NT][2];  // [tile][n-tile]
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float nva = half_bits_to_float(nv_bits[h] & 0xffffu), nvb = half_bits_to_float(nv_bits[h] >> 16);
-        float q0 = sc[4 * h + 0] * nva, q1 = sc[4 * h + 1] * nva, q2 = sc[4 * h + 2] * nvb, q3 = sc[4 * h + 3] * nvb;
-        if (!interior) {
-          q0 = sc[4 * h + 0] == 0.f ? 0.f : q0;
-          q1 = sc[4 * h + 1] == 0.f ? 0.f : q1;
-          q2 = sc[4 * h + 2] == 0.f ? 0.f : q2;
-          q3 = sc[4 * h + 3] == 0.f ? 0.f : q3;
+      for (int i = 0; i < NT; ++i) {
+        float ls[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // two short chains per column
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          sc[i][e] = ex2(sc[i][e] - m_use[i][e & 1]);  // now p; masked entries give 0
+          ls[e >> 2][e & 1] += sc[i][e];
         }
-        pb[h][0] = movmatrix_t(pack_half2(q0, q1));
-        pb[h][1] = movmatrix_t(pack_half2(q2, q3));
+        l_run[i][0] += ls[0][0] + ls[1][0];
+        l_run[i][1] += ls[0][1] + ls[1][1];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float nva = half_bits_to_float(nv_bits[h] & 0xffffu), nvb = half_bits_to_float(nv_bits[h] >> 16);
+          float q0 = sc[i][4 * h + 0] * nva, q1 = sc[i][4 * h + 1] * nva;
+          float q2 = sc[i][4 * h + 2] * nvb, q3 = sc[i][4 * h + 3] * nvb;
+          if (!interior) {
+            q0 = sc[i][4 * h + 0] == 0.f ? 0.f : q0;
+            q1 = sc[i][4 * h + 1] == 0.f ? 0.f : q1;
+            q2 = sc[i][4 * h + 2] == 0.f ? 0.f : q2;
+            q3 = sc[i][4 * h + 3] == 0.f ? 0.f : q3;
+          }
+          pb[h][i][0] = movmatrix_t(pack_half2(q0, q1));
+          pb[h][i][1] = movmatrix_t(pack_half2(q2, q3));
+        }
       }
       // ---- values: read both tiles' V codes, hand the stage back, accumulate
       Raw<BITS> rvA, rvB;
       load_stage<BITS>(rvA, stA, gq, tq);
       load_stage<BITS>(rvB, stB, gq, tq);
       __syncwarp();
-      if (k + kStages < n_w && lane < 2) {  // refill this stage while the pair is accumulated
+      if (k + kStages < n_w && lane < n_issue) {  // refill this stage while the pair is accumulated
         fence_proxy_async();
         issue(k + kStages);
       }
-      pv_tile<BITS>(o, rvA, pb[0][0], pb[0][1], key1, key2, gq);
-      pv_tile<BITS>(o, rvB, pb[1][0], pb[1][1], key1, key2, gq);
+      pv_tile<BITS, NT>(o, rvA, pb[0], key1, key2, gq);
+      pv_tile<BITS, NT>(o, rvB, pb[1], key1, key2, gq);
     }
     if (broken) {
       // A copy never landed: flag it, wait (bounded) for the copies still in flight so none
@@ -1107,99 +1225,106 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     tile0 = tile1;
     }
 
-    // ---- merge the warps' partial states of this fragment ----
+    // ---- merge the warps' partial states of this fragment, one n-tile at a time ----
     // Warp w's O goes to row (w, mt & 3) of merge half mt / 4 as one float4 per lane: rows of
     // 132 floats, so the writes are contiguous and the column-wise reads hit distinct bank
-    // groups.  m and l go to the page-id array, free until the next fragment.
-    __syncthreads();  // every warp is done with its slots, which the merge buffer reuses
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float l = l_run[c];
-      l += __shfl_xor_sync(0xffffffffu, l, 4);
-      l += __shfl_xor_sync(0xffffffffu, l, 8);
-      l += __shfl_xor_sync(0xffffffffu, l, 16);
-      l_run[c] = l;
+    // groups.  m and l go to the page-id array, free until the next fragment.  Fragment
+    // partials of unit u sit at slots u + c for its CTAs c (8 NT rows each): slots never
+    // collide, because both the units and the CTAs' ranges follow the same order.  A fragment
+    // that is its unit's whole range finishes the unit right here (structured rotations; a
+    // dense one always hands its partial to the combine kernel, which applies R_v^T).
+    const int unit = (it.b * g.num_kv_heads + it.h) * n_ug + it.nt0 / NT;
+    const Frag f = frag_at<NT>(*walk);
+    const bool whole = !PRE && f.t0 == 0 && f.t1 == f.tb;  // uniform over the CTA
+    float* dst = a.ws + (size_t)(unit + blockIdx.x) * (8 * NT) * kPartialStride;
+    if (threadIdx.x == 0 && !whole) {
+      if (f.t0 == 0) a.frag[2 * unit] = blockIdx.x;         // the unit's first CTA
+      if (f.t1 == f.tb) a.frag[2 * unit + 1] = blockIdx.x;  // and its last
     }
     float* const ml = reinterpret_cast<float*>(page_ids);  // [warp][column][m, l]
-    if (gq == 0) {
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      __syncthreads();  // every warp is done with its slots (or the previous n-tile's merge)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        ml[(warp * 8 + 2 * tq + c) * 2] = m_run[c];
-        ml[(warp * 8 + 2 * tq + c) * 2 + 1] = l_run[c];
+        float l = l_run[i][c];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        l_run[i][c] = l;
       }
-    }
+      if (gq == 0) {
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-      reinterpret_cast<float4*>((mt < 4 ? merge_lo : merge_hi) + (warp * 4 + (mt & 3)) * kPartialStride)[lane] =
-          make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
-    __syncthreads();
-    {
-      // Fragment partials of unit u sit at slots u + c for its CTAs c: slots never collide,
-      // because both the units and the CTAs' ranges follow the same order.  A fragment that is
-      // its unit's whole range finishes the unit right here (structured rotations; a dense one
-      // always hands its partial to the combine kernel, which applies R_v^T).
-      const int cols = min(8, a.rows - it.nt * 8);
-      const int unit = (it.b * g.num_kv_heads + it.h) * a.n_tiles_n + it.nt;
-      const Frag f = frag_at(*walk);
-      const bool whole = !PRE && f.t0 == 0 && f.t1 == f.tb;  // uniform over the CTA
-      float* dst = a.ws + (size_t)(unit + blockIdx.x) * 8 * kPartialStride;
-      if (threadIdx.x == 0 && !whole) {
-        if (f.t0 == 0) a.frag[2 * unit] = blockIdx.x;         // the unit's first CTA
-        if (f.t1 == f.tb) a.frag[2 * unit + 1] = blockIdx.x;  // and its last
+        for (int c = 0; c < 2; ++c) {
+          ml[(warp * 8 + 2 * tq + c) * 2] = m_run[i][c];
+          ml[(warp * 8 + 2 * tq + c) * 2 + 1] = l_run[i][c];
+        }
       }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+        reinterpret_cast<float4*>((mt < 4 ? merge_lo : merge_hi) + (warp * 4 + (mt & 3)) * kPartialStride)[lane] =
+            make_float4(o[i][mt][0], o[i][mt][1], o[i][mt][2], o[i][mt][3]);
+      __syncthreads();
+      const int nt = it.nt0 + i;
+      const int cols = min(8, a.rows - nt * 8);
       // thread (c, gq', mt') merges dims 16 gq' + 2 mt' and +1 of column c: lane 4 gq' + c / 2
       // of every warp held them, as components (c & 1) and (c & 1) + 2 of its float4 mt'
-      const int c = threadIdx.x >> 6, gm = (threadIdx.x >> 3) & 7, mm = threadIdx.x & 7;
-      // a whole unit's R_v entries, loaded while the partials are summed
-      const float4 rv = (whole && c < cols) ? rot_v_block(g, it.h, 16 * gm + 2 * mm) : make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c < cols) {  // c is uniform over each warp
-        float M = -CUDART_INF_F;
+#pragma unroll
+      for (int idx0 = 0; idx0 < 512; idx0 += kThreads) {
+        const int idx = idx0 + threadIdx.x;
+        const int c = idx >> 6, gm = (idx >> 3) & 7, mm = idx & 7;
+        // a whole unit's R_v entries, loaded while the partials are summed
+        const float4 rv = (whole && c < cols) ? rot_v_block(g, it.h, 16 * gm + 2 * mm) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < cols) {  // c is uniform over each warp
+          float M = -CUDART_INF_F;
 #pragma unroll 4
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 8 + c) * 2]);
-        float acc0 = 0.f, acc1 = 0.f, lsum = 0.f;
-        if (M != -CUDART_INF_F) {
-          const float* half_base = (mm < 4 ? merge_lo : merge_hi) + (mm & 3) * kPartialStride + 4 * (4 * gm + (c >> 1));
+          for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 8 + c) * 2]);
+          float acc0 = 0.f, acc1 = 0.f, lsum = 0.f;
+          if (M != -CUDART_INF_F) {
+            const float* half_base = (mm < 4 ? merge_lo : merge_hi) + (mm & 3) * kPartialStride + 4 * (4 * gm + (c >> 1));
 #pragma unroll 4
-          for (int w = 0; w < kWarps; ++w) {
-            const float scale = exp2f(ml[(w * 8 + c) * 2] - M);
-            const float4 v = *reinterpret_cast<const float4*>(half_base + w * 4 * kPartialStride);
-            acc0 += ((c & 1) ? v.y : v.x) * scale;
-            acc1 += ((c & 1) ? v.w : v.z) * scale;
-            lsum += ml[(w * 8 + c) * 2 + 1] * scale;
+            for (int w = 0; w < kWarps; ++w) {
+              const float scale = exp2f(ml[(w * 8 + c) * 2] - M);
+              const float4 v = *reinterpret_cast<const float4*>(half_base + w * 4 * kPartialStride);
+              acc0 += ((c & 1) ? v.y : v.x) * scale;
+              acc1 += ((c & 1) ? v.w : v.z) * scale;
+              lsum += ml[(w * 8 + c) * 2 + 1] * scale;
+            }
           }
-        }
-        if (whole) {
-          const float inv = (lsum > 0.f && len >= a.T) ? 1.f / lsum : 0.f;
-          store_pair(g, a, it.b, it.h, it.nt * 8 + c, 16 * gm + 2 * mm, acc0 * inv, acc1 * inv, rv);
-        } else {
-          *reinterpret_cast<float2*>(dst + c * kPartialStride + 4 + 16 * gm + 2 * mm) = make_float2(acc0, acc1);
-          if (gm == 0 && mm == 0) {
-            dst[c * kPartialStride] = M;
-            dst[c * kPartialStride + 1] = lsum;
+          if (whole) {
+            const float inv = (lsum > 0.f && len >= a.T) ? 1.f / lsum : 0.f;
+            store_pair(g, a, it.b, it.h, nt * 8 + c, 16 * gm + 2 * mm, acc0 * inv, acc1 * inv, rv);
+          } else {
+            float* drow = dst + (i * 8 + c) * kPartialStride;
+            *reinterpret_cast<float2*>(drow + 4 + 16 * gm + 2 * mm) = make_float2(acc0, acc1);
+            if (gm == 0 && mm == 0) {
+              drow[0] = M;
+              drow[1] = lsum;
+            }
           }
         }
       }
-      if (!PRE && !whole) {
-        // Publish the partial and count the unit's finished rounds: the barrier orders every
-        // thread's partial before thread 0's fence and add.  The CTA whose rounds complete the
-        // unit merges all its partials once its own range is done (no CTA waits for another)
-        // and puts the counter back to zero for the next launch.
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          const int n = f.r1 - f.r0;
-          __threadfence();
-          if (atomicAdd(a.cnt + unit, n) + n >= f.rb) {
-            a.cnt[unit] = 0;
-            if (walk->n_fin < 2) walk->fin[walk->n_fin++] = unit;
-            else if (a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);  // cannot happen (see Walk)
-          }
+    }
+    if (!PRE && !whole) {
+      // Publish the partial and count the unit's finished rounds: the barrier orders every
+      // thread's partial before thread 0's fence and add.  The CTA whose rounds complete the
+      // unit merges all its partials once its own range is done (no CTA waits for another)
+      // and puts the counter back to zero for the next launch.
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const int n = f.r1 - f.r0;
+        __threadfence();
+        if (atomicAdd(a.cnt + unit, n) + n >= f.rb) {
+          a.cnt[unit] = 0;
+          if (walk->n_fin < 2) walk->fin[walk->n_fin++] = unit;
+          else if (a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);  // cannot happen (see Walk)
         }
       }
     }
     __syncthreads();  // the merge buffer reuses slot space
     if (threadIdx.x == 0) {
       Walk w = *walk;
-      walk_advance(w, frag_at(w), upb, a, cap);
+      walk_advance(w, frag_at<NT>(w), upb, a, cap);
       *walk = w;
     }
     __syncthreads();
@@ -1209,15 +1334,12 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     // Finish the units this CTA completed: a warp per query row of the unit.
     if (threadIdx.x == 0 && walk->n_fin > 0) __threadfence();  // after the adds that saw them done
     __syncthreads();
-    const int ntn = a.n_tiles_n;
     for (int k = 0; k < walk->n_fin; ++k) {
       const int unit = walk->fin[k];
-      const int nt = unit % ntn, h = (unit / ntn) % g.num_kv_heads, b = unit / (ntn * g.num_kv_heads);
-      if (warp < min(8, a.rows - nt * 8)) {
-        const int row = nt * 8 + warp;
-        const float4 rv = rot_v_block(g, h, 4 * lane);
-        store_row(g, a, b, h, row, lane, merge_splits(g, a, b, h, row, lane), rv);
-      }
+      const int ug = unit % n_ug, h = (unit / n_ug) % g.num_kv_heads, b = unit / (n_ug * g.num_kv_heads);
+      const int row0 = ug * 8 * NT, nrows = min(8 * NT, a.rows - row0);
+      const float4 rv = rot_v_block(g, h, 4 * lane);
+      for (int r = warp; r < nrows; r += kWarps) store_row(g, a, b, h, row0 + r, lane, merge_splits(g, a, b, h, row0 + r, lane), rv);
     }
   }
 }
@@ -1319,33 +1441,49 @@ attn_combine_dense_kernel(const Geometry g, const AttnArgs a) {
 
 // Dynamic shared memory of a variant: its layout end for a window that starts right after the
 // driver's reserved shared memory (the kernels declare no static shared memory).
-static int smem_bytes_for(int bits) {
+template <int NT>
+static int smem_bytes_nt(int bits) {
   int dev = 0, reserved = 0;
   cudaGetDevice(&dev);
   if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) reserved = 0;
   const uint32_t base = (uint32_t)reserved;
-  const uint32_t end = bits == 4 ? smem_plan<4>(base).end : (bits == 3 ? smem_plan<3>(base).end : smem_plan<2>(base).end);
+  const uint32_t end = bits == 4 ? smem_plan<4, NT>(base).end
+                                 : (bits == 3 ? smem_plan<3, NT>(base).end : smem_plan<2, NT>(base).end);
   return (int)(end - base);
+}
+static int smem_bytes_for(int bits, int nt) {
+  return nt == 1 ? smem_bytes_nt<1>(bits) : (nt == 2 ? smem_bytes_nt<2>(bits) : smem_bytes_nt<3>(bits));
 }
 
 size_t attention_smem_bytes() {
   size_t m = 0;
   for (int bits = 2; bits <= 4; ++bits)
-    if ((size_t)smem_bytes_for(bits) > m) m = (size_t)smem_bytes_for(bits);
+    for (int nt = 1; nt <= 3; ++nt)
+      if ((size_t)smem_bytes_for(bits, nt) > m) m = (size_t)smem_bytes_for(bits, nt);
   return m;
 }
 
-template <int BITS, bool PRE, bool STEP>
+// The n-tiles a unit carries for a call whose kv heads have n_tiles n-tiles of 8 query rows:
+// all of them up to 3.
+int attention_unit_tiles(int n_tiles, bool) { return n_tiles < 3 ? n_tiles : 3; }
+
+template <int BITS, bool PRE, bool STEP, int NT>
 static cudaError_t set_smem_limit() {
-  return cudaFuncSetAttribute(attn_splitk_kernel<BITS, PRE, STEP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem_bytes_for(BITS));
+  return cudaFuncSetAttribute(attn_splitk_kernel<BITS, PRE, STEP, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes_for(BITS, NT));
 }
 
 template <int BITS>
 static cudaError_t set_smem_limits() {
-  cudaError_t e = set_smem_limit<BITS, false, false>();
-  if (e == cudaSuccess) e = set_smem_limit<BITS, true, false>();
-  if (e == cudaSuccess) e = set_smem_limit<BITS, false, true>();
+  cudaError_t e = set_smem_limit<BITS, false, false, 1>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, false, false, 2>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, false, false, 3>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, true, false, 1>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, true, false, 2>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, true, false, 3>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, false, true, 1>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, false, true, 2>();
+  if (e == cudaSuccess) e = set_smem_limit<BITS, false, true, 3>();
   return e;
 }
 
@@ -1360,14 +1498,26 @@ cudaError_t attention_prepare() {
   return e;
 }
 
-template <int BITS>
-static void launch_splitk(const Geometry& g, const AttnArgs& a, int smem, cudaStream_t stream) {
+template <int BITS, int NT>
+static void launch_splitk_nt(const Geometry& g, const AttnArgs& a, cudaStream_t stream) {
+  const int smem = smem_bytes_for(BITS, NT);
+  constexpr int threads = Shape<NT>::kThreads;
   if (a.q_rot)
-    attn_splitk_kernel<BITS, true, false><<<a.grid, kThreads, smem, stream>>>(g, a, smem);
+    attn_splitk_kernel<BITS, true, false, NT><<<a.grid, threads, smem, stream>>>(g, a, smem);
   else if (a.k_new)
-    attn_splitk_kernel<BITS, false, true><<<a.grid, kThreads, smem, stream>>>(g, a, smem);
+    attn_splitk_kernel<BITS, false, true, NT><<<a.grid, threads, smem, stream>>>(g, a, smem);
   else
-    attn_splitk_kernel<BITS, false, false><<<a.grid, kThreads, smem, stream>>>(g, a, smem);
+    attn_splitk_kernel<BITS, false, false, NT><<<a.grid, threads, smem, stream>>>(g, a, smem);
+}
+
+template <int BITS>
+static void launch_splitk(const Geometry& g, const AttnArgs& a, cudaStream_t stream) {
+  if (a.nt == 1)
+    launch_splitk_nt<BITS, 1>(g, a, stream);
+  else if (a.nt == 2)
+    launch_splitk_nt<BITS, 2>(g, a, stream);
+  else
+    launch_splitk_nt<BITS, 3>(g, a, stream);
 }
 
 cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
@@ -1376,6 +1526,7 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t 
   const bool dense = g.mode == RQ_DENSE;
   if (dense != (a.q_rot != nullptr)) return cudaErrorInvalidValue;
   if (a.k_new && (dense || !a.v_new || !g.boundaries || a.T != 1)) return cudaErrorInvalidValue;
+  if (a.nt != attention_unit_tiles(a.n_tiles_n, a.k_new != nullptr)) return cudaErrorInvalidValue;
   const long long rows_per_head = (long long)a.B * a.T * g.group;
   const unsigned groups = (unsigned)(g.num_kv_heads * ((rows_per_head + kDenseRows - 1) / kDenseRows));
   if (dense) {
@@ -1385,13 +1536,12 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t 
   }
   if (a.grid > 0) {
     if (ev_start) cudaEventRecord(ev_start, stream);
-    const int smem = smem_bytes_for(g.bits);
     if (g.bits == 4)
-      launch_splitk<4>(g, a, smem, stream);
+      launch_splitk<4>(g, a, stream);
     else if (g.bits == 3)
-      launch_splitk<3>(g, a, smem, stream);
+      launch_splitk<3>(g, a, stream);
     else
-      launch_splitk<2>(g, a, smem, stream);
+      launch_splitk<2>(g, a, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev_end) cudaEventRecord(ev_end, stream);

@@ -48,12 +48,14 @@ struct AttnArgs {
   int T;
   void* out;                 // fp16 [B][T][Hq][128]
   int32_t* status;           // nullable
-  float* ws;                 // fragment partials: [units + grid][8 rows][kPartialStride] floats
+  // A unit is (sequence, kv head, group of nt n-tiles): units = B * Hkv * ceil(n_tiles_n / nt).
+  float* ws;                 // fragment partials: [units + grid][8 nt rows][kPartialStride] floats
   int* frag;                 // [units][2]: first and last CTA holding a fragment of each unit
   int* cnt;                  // [units]: rounds finished per unit; zero between launches
   int grid;                  // CTAs of the split-K launch (the stream-K partition's parts)
   int rows;                  // T * group: query rows per kv head
   int n_tiles_n;             // ceil(rows / 8)
+  int nt;                    // n-tiles per unit: attention_unit_tiles(n_tiles_n, k_new != null)
   const uint64_t* tree_mask; // [B][T] draft visibility bits (tree verify), or null (causal chain)
   float* q_rot;              // dense: fp32 [B][T][Hq][128] scratch for R_k q; null otherwise
   // Decode step (planar / iso): fp16 [B][Hkv][128] K and V of each sequence's newest token,
@@ -79,6 +81,19 @@ constexpr int kMaxBatch = 8000;
 cudaError_t launch_extend(const Geometry& g, const AttnArgs& a, cudaStream_t stream, cudaEvent_t ev_start = nullptr,
                           cudaEvent_t ev_end = nullptr);
 cudaError_t extend_prepare();
+
+// n-tiles of 8 query rows a split-K unit carries, for kv heads of n_tiles n-tiles: min(n_tiles,
+// 3), for decode, verify and a decode step alike (`step` is kept for the workspace sizing).
+int attention_unit_tiles(int n_tiles, bool step);
+
+// Split-K workspace of a call with B sequences, Hkv kv heads, n_tiles n-tiles per kv head and
+// `grid` CTAs: units, partial floats ((units + grid) slots of 8 nt rows).
+inline void attention_workspace(long long B, int hkv, int n_tiles, bool step, int grid, long long* units,
+                                long long* partial_floats) {
+  const int nt = attention_unit_tiles(n_tiles, step);
+  *units = B * hkv * ((n_tiles + nt - 1) / nt);
+  *partial_floats = (*units + grid) * 8LL * nt * kPartialStride;
+}
 
 // Dynamic shared memory the attention kernel needs (set as the kernel's maximum once).
 size_t attention_smem_bytes();

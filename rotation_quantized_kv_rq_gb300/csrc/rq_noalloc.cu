@@ -14,13 +14,13 @@
 namespace {
 
 // Scratch: fragment bounds (2 ints per unit), round counters (1 int per unit), then fragment
-// partials of 8 query rows x kPartialStride floats.  A call with U units and G CTAs uses
-// 3U ints and U + G slots.
+// partials of 8 query rows x kPartialStride floats per n-tile of a unit.  A call with U units
+// and G CTAs uses 3U ints and (U + G) x (n-tiles per unit) 8-row slots.
 constexpr size_t kScratchBytes = (size_t)16 << 20;
 constexpr size_t kMaxUnits = 8192;
 constexpr size_t kFragBytes = kMaxUnits * 2 * sizeof(int);              // 64 KiB
 constexpr size_t kCntBytes = kMaxUnits * sizeof(int);                   // 32 KiB
-constexpr size_t kSlotBytes = 8 * rq::kPartialStride * sizeof(float);   // one fragment
+constexpr size_t kSlotBytes = 8 * rq::kPartialStride * sizeof(float);   // 8 query rows of one fragment
 constexpr size_t kScratchSlots = (kScratchBytes - kFragBytes - kCntBytes) / kSlotBytes;  // 3,948
 constexpr int kMaxDevices = 64;
 
@@ -79,7 +79,10 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
     return RQ_ERR_INVALID;  // bulk copies and vector I/O
 
   const int hkv = cfg->num_kv_heads, group = cfg->num_q_heads / hkv;
-  const long long units = (long long)B * hkv * ((group + 7) / 8);
+  const int n_tiles = (group + 7) / 8;
+  long long units = 0, partial_floats = 0;
+  rq::attention_workspace(B, hkv, n_tiles, false, 0, &units, &partial_floats);
+  const int nt = rq::attention_unit_tiles(n_tiles, false);
   if (B > rq::kMaxBatch || units > (long long)kMaxUnits) return RQ_ERR_CAPACITY;
   if ((long long)max_pages * cfg->page_size > INT32_MAX) return RQ_ERR_CAPACITY;  // positions are int
 
@@ -87,7 +90,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RQ_ERR_CUDA;
   DeviceSlot* slot = nullptr;
   if (setup_device(dev, &slot) != cudaSuccess) return RQ_ERR_CUDA;
-  if (units + slot->num_sms > (long long)kScratchSlots) return RQ_ERR_CAPACITY;
+  if ((units + slot->num_sms) * nt > (long long)kScratchSlots) return RQ_ERR_CAPACITY;
 
   rq::Geometry g;
   g.num_q_heads = cfg->num_q_heads;
@@ -122,7 +125,8 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   a.q_rot = nullptr;
   a.k_new = a.v_new = nullptr;
   a.rows = group;
-  a.n_tiles_n = (group + 7) / 8;
+  a.n_tiles_n = n_tiles;
+  a.nt = nt;
 
   a.frag = reinterpret_cast<int*>(slot->scratch);
   a.cnt = reinterpret_cast<int*>(slot->scratch + kFragBytes);

@@ -120,6 +120,13 @@ CASES = [
     (DENSE, 3, 40, 2, 16, [50, 200], 1),
     (DENSE, 2, 8, 8, 16, [16, 48], 1),
     (DENSE, 4, 32, 8, 48, [130, 49], 1),
+    # units of several n-tiles: group 16 decode (2 n-tiles per unit), 6 drafts x group 8 verify
+    # (48 rows: two units of 3 n-tiles per kv head) with a sequence long enough to split units
+    # across CTAs, and a dense 2-n-tile verify
+    (ISO, 4, 128, 8, 16, [300, 1500], 1),
+    (PLANAR, 3, 64, 8, 16, [400, 9000, 7], 6),
+    (ISO, 2, 48, 8, 64, [3000, 65], 4),
+    (DENSE, 3, 64, 8, 16, [700, 33], 2),
 ]
 
 
