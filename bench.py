@@ -64,6 +64,10 @@ DESCRIPTIONS = {
     "tq3_prefill": "tq3 (dense rotation) quantize-append of 65536 tokens x 8 kv heads (K and V), page 16",
     "cfg3_extend": "rq3_iso extend: 8 x (15360 cached + 1024 new) tokens, 32 q / 8 kv heads, head_dim 128, page 16, "
                    "append the 1024 new tokens + causal extend attention",
+    "tq3_extend": "tq3 (dense rotation) extend: 8 x (15360 cached + 1024 new) tokens, 32 q / 8 kv heads, head_dim 128, "
+                  "page 16, append the 1024 new tokens + causal extend attention",
+    "tq3_step": "tq3 (dense rotation) decode step, 16 x 8192 ctx, 32 q / 8 kv heads, head_dim 128, page 16, "
+                "permuted pages, append 1 token per sequence + decode",
 }
 
 
@@ -141,9 +145,8 @@ class Bench:
         if s.query_tokens == 1:
             self.q = self.q[:, 0].contiguous()
         self.out = torch.empty_like(self.q)
-        # one token per sequence, then decode: a single rq_decode_step (structured rotations)
-        self.fused_step = (not self.prefill_only and s.appended == 1 and s.query_tokens == 1
-                           and s.mode != synth.DENSE)
+        # one token per sequence, then decode: a single rq_decode_step
+        self.fused_step = not self.prefill_only and s.appended == 1 and s.query_tokens == 1
         self.extend = not self.prefill_only and s.query_tokens >= synth.EXTEND_MIN_T
         torch.cuda.synchronize(device)
         assert int(self.cache.status.item()) == 0, "range fault while building the cache"
@@ -165,10 +168,11 @@ class Bench:
             self.cache.verify(self.q, self.bt, self.lens, out=self.out)
 
     def launches_per_step(self):
-        if self.fused_step:
-            return 1  # split-K with the append folded in and the units finished in-kernel
+        dense = self.spec.mode == synth.DENSE
+        if self.fused_step:  # split-K with the append folded in and the units finished in-kernel; a
+            return 3 if dense else 1  # dense rotation: the prologue (queries + tokens), split-K, combine
         if self.extend:
-            return 2  # append, extend attention
+            return 3 if dense else 2  # append, (dense: the query rotation,) extend attention
         n = 1 if self.k_new is not None else 0
         # split-K; a dense rotation adds the query pre-rotation and the combine (R_v^T)
         return n if self.prefill_only else n + 1 + 2 * (self.spec.mode == synth.DENSE)
@@ -189,7 +193,8 @@ class Bench:
         s = self.spec
         pages = int(((self.wl.seq_lens + s.page_size - 1) // s.page_size).sum())
         q_bytes = 512 if s.mode == synth.DENSE else 256  # fp32 pre-rotated rows, or fp16 q
-        fused = self.append_algorithmic_bytes() if self.fused_step else 0  # the step's tokens, when folded in
+        # the step's tokens, when the split-K kernel itself appends them (structured rotations)
+        fused = self.append_algorithmic_bytes() if self.fused_step and s.mode != synth.DENSE else 0
         return self.packed_bytes() + s.batch * s.query_tokens * s.num_q_heads * q_bytes + pages * 4 + fused
 
     def extend_flops(self):
@@ -497,7 +502,7 @@ def config_of(name, world):
     s = synth.prefill_spec(name) if name in synth.PREFILL else synth.SPECS[name]
     wl = synth.workload(s)
     packed = int(wl.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * (32 * s.bits + 4)
-    fused = (name not in synth.PREFILL and s.appended == 1 and s.query_tokens == 1 and s.mode != synth.DENSE)
+    fused = name not in synth.PREFILL and s.appended == 1 and s.query_tokens == 1
     return {"workload": f"{name}: {DESCRIPTIONS[name]}", "batch": s.batch, "ctx": int(s.ctx),
             "query_tokens": s.query_tokens, "bits": s.bits,
             "mode": {synth.PLANAR: "planar", synth.ISO: "iso", synth.DENSE: "dense"}[s.mode],

@@ -181,12 +181,14 @@ int rq_decode_attention(rq_ctx *ctx, const void *q, const void *kv_pages, const 
  * Extend (prefill) attention: T new query tokens per sequence, already appended as the last T
  * tokens of the cache, each attending to the cached prefix and causally to the new tokens:
  * query row j (0 <= j < T) sees positions 0 .. seq_lens[b] - T + j -- the same result as
- * rq_verify_attention, computed by a kernel built for large T (64 query rows share every
- * dequantized tile of the cache; tensor-core QK^T and PV).  It uses no workspace: T is limited
- * only by the q / out buffers, not by max_query_tokens.
+ * rq_verify_attention, computed by a kernel built for large T (256 query rows share every
+ * dequantized tile of the cache; tensor-core QK^T and PV).  Planar and iso rotations use no
+ * workspace: T is limited only by the q / out buffers, not by max_query_tokens.  A dense rotation
+ * (RQ_DENSE) rotates the queries into the context's workspace first, so there T must not exceed
+ * max_query_tokens (RQ_ERR_CAPACITY otherwise).
  *   q   device fp16 [B][T][Hq][head_dim],   out device fp16 [B][T][Hq][head_dim]
  * Other arguments as rq_verify_attention.  Errors as rq_verify_attention (except that T above
- * max_query_tokens is allowed), plus RQ_ERR_UNSUPPORTED for RQ_DENSE.
+ * max_query_tokens is allowed for planar and iso rotations).
  */
 int rq_extend_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages, const int32_t *block_table,
                         int max_pages, const int32_t *seq_lens, int B, void *out, int32_t *d_status,
@@ -195,8 +197,8 @@ int rq_extend_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
 /*
  * Source: this library -- rq_quantize_append of one token per sequence followed by
  * rq_decode_attention, in one launch.
- * One decode step in one kernel launch: quantize-append of every sequence's newest K/V token,
- * folded into rq_decode_attention's split-K kernel, then decode attention over the cache
+ * One decode step in one kernel launch (planar, iso): quantize-append of every sequence's newest
+ * K/V token, folded into rq_decode_attention's split-K kernel, then decode attention over the cache
  * including that token (the combine of split partials runs in the same kernel).
  *   k_new, v_new  device fp16 [B][Hkv][head_dim]: the token of sequence b, written to position
  *                 seq_lens[b] - 1 -- page block_table[b][(seq_lens[b] - 1) / P], offset
@@ -204,10 +206,12 @@ int rq_extend_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
  *   kv_pages      device page pool (written: the step's tokens; read: everything)
  *   other arguments as rq_decode_attention; seq_lens[b] counts the new token, and a sequence
  *   with seq_lens[b] = 0 appends nothing.
- * The result equals rq_quantize_append of the tokens followed by rq_decode_attention.  A page id
- * out of range for the new token sets RQ_STATUS_BAD_PAGE and skips its write.  Errors as
- * rq_decode_attention, plus RQ_ERR_INVALID for a NULL or non-16-byte-aligned k_new / v_new, and
- * RQ_ERR_UNSUPPORTED for RQ_DENSE (use rq_quantize_append, then rq_decode_attention).
+ * The result equals rq_quantize_append of the tokens followed by rq_decode_attention (the same
+ * bytes written, the same output).  A dense rotation (RQ_DENSE) codes the new tokens in the
+ * launch that rotates the queries, before the split-K kernel: three launches with the output
+ * rotation, instead of four.  A page id out of range for the new token sets RQ_STATUS_BAD_PAGE
+ * and skips its write.  Errors as rq_decode_attention, plus RQ_ERR_INVALID for a NULL or
+ * non-16-byte-aligned k_new / v_new.
  */
 int rq_decode_step(rq_ctx *ctx, const void *q, const void *k_new, const void *v_new, void *kv_pages,
                    const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B, void *out,

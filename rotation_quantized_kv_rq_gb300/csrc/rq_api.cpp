@@ -30,6 +30,7 @@ struct rq_ctx {
   cudaEvent_t prof_end;
   float centroids[256];
   float boundaries[255];
+  double c_scale;         // the attention kernels' centroid scale (Geometry::out_scale)
 };
 
 namespace {
@@ -82,6 +83,28 @@ void lloyd_max_positive_half(int levels, double* out_ascending) {
     out_ascending[K + k] = y[k];
     out_ascending[K - 1 - k] = -y[k];
   }
+}
+
+// The scale S in [1, 2) for which the fp16 images of c_j / S, times S, are closest to the
+// centroids c_j (largest relative error over j, smallest over a grid of 2^16 candidates).  fp16
+// keeps 11 significant bits; with 2 to 8 distinct magnitudes a common scale brings them much
+// closer to exact than S = 1, which the attention kernels then undo in fp32 for free.
+double centroid_scale(const float* c, int L) {
+  double best_s = 1.0, best_err = 1e30;
+  for (int k = 0; k < (1 << 16); ++k) {
+    const double s = 1.0 + k / 65536.0;
+    double err = 0.0;
+    for (int j = 0; j < L && err < best_err; ++j) {
+      if (c[j] == 0.f) continue;
+      const double h = (double)__half2float(__float2half_rn((float)((double)c[j] / s)));
+      err = std::fmax(err, std::fabs(h * s - (double)c[j]) / std::fabs((double)c[j]));
+    }
+    if (err < best_err) {
+      best_err = err;
+      best_s = s;
+    }
+  }
+  return best_s;
 }
 
 int check_geometry(const rq_config* c) {
@@ -234,7 +257,8 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
       std::memcpy(host, cfg->rot_k, rot * sizeof(float));
       std::memcpy(host + rot, cfg->rot_v, rot * sizeof(float));
     }
-    std::memcpy(host + 2 * rot, ctx->centroids, L * sizeof(float));
+    ctx->c_scale = centroid_scale(ctx->centroids, L);
+    for (int j = 0; j < L; ++j) host[2 * rot + j] = (float)((double)ctx->centroids[j] / ctx->c_scale);
     std::memcpy(host + 2 * rot + 256, ctx->boundaries, (L - 1) * sizeof(float));
     if (e == cudaSuccess) e = cudaMemcpy(ctx->d_tables, host, table_floats * sizeof(float), cudaMemcpyHostToDevice);
   }
@@ -265,12 +289,13 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   g.vec_bytes = d * cfg->bits / 8;
   g.page_bytes = cfg->page_size * (2 * g.vec_bytes + 4);
   const float scale = cfg->sm_scale > 0.f ? cfg->sm_scale : (float)(1.0 / std::sqrt((double)d));
-  g.q_scale = (float)(scale * 1.44269504088896340736);
+  g.q_scale = (float)(scale * 1.44269504088896340736 * ctx->c_scale);
+  g.out_scale = (float)ctx->c_scale;
   g.rot_k = ctx->d_tables;
   g.rot_v = ctx->d_tables + rot;
   g.dense16 = ctx->d_dense16;
   g.dense32 = ctx->d_dense32;
-  g.centroids = ctx->d_tables + 2 * rot;
+  g.centroids = ctx->d_tables + 2 * rot;  // c / c_scale
   g.boundaries = ctx->d_tables + 2 * rot + 256;
   *out = ctx;
   return RQ_OK;
@@ -376,8 +401,9 @@ int rq_extend_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages,
   if (B == 0) return RQ_OK;
   if (!q || !kv_pages || !block_table || !seq_lens || !out) return RQ_ERR_INVALID;
   if (misaligned16(q) || misaligned16(kv_pages) || misaligned16(out)) return RQ_ERR_INVALID;  // vector loads, stores
-  if (ctx->g.mode == RQ_DENSE) return RQ_ERR_UNSUPPORTED;
   if (B > ctx->cfg.max_batch || max_pages > ctx->cfg.max_pages_per_seq) return RQ_ERR_CAPACITY;
+  // a dense rotation's queries are rotated into the context's workspace first
+  if (ctx->g.mode == RQ_DENSE && T > ctx->cfg.max_query_tokens) return RQ_ERR_CAPACITY;
   if ((long long)T * ctx->g.group > INT32_MAX / 2) return RQ_ERR_CAPACITY;
   DeviceScope scope(ctx->device);
   if (!scope.ok()) return RQ_ERR_CUDA;
@@ -392,6 +418,7 @@ int rq_extend_attention(rq_ctx* ctx, const void* q, int T, const void* kv_pages,
   a.out = out;
   a.status = d_status;
   a.rows = T * ctx->g.group;
+  a.q_rot = ctx->d_qrot;  // null unless dense
   return to_status(rq::launch_extend(ctx->g, a, (cudaStream_t)stream, ctx->prof_start, ctx->prof_end));
 }
 
@@ -399,7 +426,6 @@ int rq_decode_step(rq_ctx* ctx, const void* q, const void* k_new, const void* v_
                    const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B, void* out, int32_t* d_status,
                    void* stream) {
   if (!ctx) return RQ_ERR_INVALID;
-  if (ctx->g.mode == RQ_DENSE) return RQ_ERR_UNSUPPORTED;  // its append is a GEMM of its own
   if (B > 0 && (!k_new || !v_new || (uintptr_t)k_new % 16 != 0 || (uintptr_t)v_new % 16 != 0)) return RQ_ERR_INVALID;
   return attention_call(ctx, q, 1, nullptr, kv_pages, block_table, max_pages, seq_lens, B, out, d_status, stream, k_new,
                         v_new);

@@ -139,10 +139,6 @@ constexpr int kSmemX = kSmemR + 2 * 128 * 128 * 2;            // fp16 [2 buffers
 constexpr int kSmemY = kSmemX + 2 * kDenseRows * 128 * 2;     // fp32 [32][136]
 constexpr int kDenseSmem = kSmemY + kDenseRows * kYStride * 4;  // 99,328 bytes; the fp32 R of the
                                                                 // exact recompute is read from L2
-// Tensor-core Y is trusted to decide a code when u is farther than this from every boundary.
-// Its error is the hi + lo split (|R - hi - lo| <= 6e-8 per entry, so <= 7e-7 in u by
-// Cauchy-Schwarz) plus the accumulation of 16 fp32 MMA steps (a few fp32 ulps of n each).
-constexpr float kFixBand = 1e-5f;
 
 // A 256-byte row of 16 chunks (8 fp16 each) stores chunk c at position c ^ (row mod 8), so the
 // eight rows one ldmatrix phase reads fall in eight different 16-byte bank groups.
@@ -184,37 +180,6 @@ __device__ __forceinline__ void issue_x(uint32_t xs, int hk, long long blk, cons
       *reinterpret_cast<uint4*>(xs_generic + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
-}
-
-// y_i = sum_m x_m R[i][m] for one vector, summed exactly enough to be correctly rounded in all
-// but pathological cases: error-free products (fma) and error-free sums (two-sum), the rounding
-// errors carried in a second word.  Lane j of the half-warp holds x[8j..8j+7]; `row` is R's row
-// i in global memory (rarely read: L2).  Every lane of the warp calls it (shuffles stay within
-// each half).
-__device__ __forceinline__ float dot_compensated(const float (&x)[8], const float* row, int j) {
-  const float4 r0 = __ldg(reinterpret_cast<const float4*>(row + 8 * j));
-  const float4 r1 = __ldg(reinterpret_cast<const float4*>(row + 8 * j + 4));
-  const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-  float s = 0.f, c = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float p = x[e] * rr[e];
-    const float pe = fmaf(x[e], rr[e], -p);  // x * r = p + pe exactly
-    const float t = s + p;
-    const float z = t - s;
-    c += ((s - (t - z)) + (p - z)) + pe;     // s + p = t + (that) exactly
-    s = t;
-  }
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) {
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
-    const float t = s + s2;
-    const float z = t - s;
-    c += c2 + ((s - (t - z)) + (s2 - z));
-    s = t;
-  }
-  return s + c;
 }
 
 template <int BITS>
@@ -320,48 +285,15 @@ append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __re
       const bool store = slot >= 0 && !bad;
       if (!store) slot = 0;
       const uint4 raw = *reinterpret_cast<const uint4*>(xg + swz(r, j));
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-        x[2 * e] = f.x;
-        x[2 * e + 1] = f.y;
+      float y[8];
+      {
+        const float4 y0 = *reinterpret_cast<const float4*>(Ys + r * kYStride + 8 * j);
+        const float4 y1 = *reinterpret_cast<const float4*>(Ys + r * kYStride + 8 * j + 4);
+        y[0] = y0.x, y[1] = y0.y, y[2] = y0.z, y[3] = y0.w, y[4] = y1.x, y[5] = y1.y, y[6] = y1.z, y[7] = y1.w;
       }
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float nrm = __fsqrt_rn(ss);
-      const float4 y0 = *reinterpret_cast<const float4*>(Ys + r * kYStride + 8 * j);
-      const float4 y1 = *reinterpret_cast<const float4*>(Ys + r * kYStride + 8 * j + 4);
-      const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-      // Coordinates whose tensor-core u is within kFixBand of a boundary: recompute exactly,
-      // one at a time per half-warp (both halves walk their lists together), then re-code.
-      const float rcp = inv_norm(nrm);
-      uint32_t todo = 0;
       int code[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float dm;
-        code[e] = code_of_margin<BITS>(y[e] * rcp, bnd, dm);
-        if (dm < kFixBand && store) todo |= 1u << e;
-      }
-      while (__any_sync(0xffffffffu, todo != 0)) {
-        const uint32_t want = __ballot_sync(0xffffffffu, todo != 0) & (half ? 0xffff0000u : 0x0000ffffu);
-        const int leader = want ? __ffs(want) - 1 : (half << 4);  // no work: any lane, result unused
-        const int e_lead = __shfl_sync(0xffffffffu, todo ? __ffs(todo) - 1 : 0, leader);
-        const int i = 8 * (leader & 15) + e_lead;  // the coordinate (dim of y) being recomputed
-        const float yi = dot_compensated(x, r32 + i * 128, j);
-        if (lane == leader && want) {
-          const int c = code_of<BITS>(yi * rcp, bnd);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (e == e_lead) code[e] = c;
-          todo &= ~(1u << e_lead);
-        }
-      }
+      float nrm;
+      dense_codes<BITS>(code, nrm, raw, y, bnd, r32, store, lane);
       int page, off;
       split(slot, page, off);
       uint8_t* chunk = pages + ((size_t)page * hkv + h) * (size_t)g.page_bytes;

@@ -550,7 +550,7 @@ __device__ __forceinline__ float4 merge_splits(const Geometry& g, const AttnArgs
     acc.z += v.z * w;
     acc.w += v.w * w;
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float inv = L > 0.f ? g.out_scale / L : 0.f;
   return make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
@@ -1139,11 +1139,13 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       }
       // fp16 norms at or above 2^8 (bits >= 0x5C00) take the exact path, where p <= 1
       const uint32_t nv_hi = max(max(nv_bits[0] & 0xffffu, nv_bits[0] >> 16), max(nv_bits[1] & 0xffffu, nv_bits[1] >> 16));
+      // (a column with no visible score yet keeps m_run = -inf: its masked scores must give
+      // p = 2^(-inf - 0) = 0, not 2^(-inf + inf))
       float m_use[NT][2];
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
-        m_use[i][0] = m_run[i][0];
-        m_use[i][1] = m_run[i][1];
+        m_use[i][0] = m_run[i][0] == -CUDART_INF_F ? 0.f : m_run[i][0];
+        m_use[i][1] = m_run[i][1] == -CUDART_INF_F ? 0.f : m_run[i][1];
       }
       if (__any_sync(0xffffffffu, grow || nv_hi >= 0x5C00u)) {
         float alpha[NT][2];
@@ -1292,7 +1294,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
             }
           }
           if (whole) {
-            const float inv = (lsum > 0.f && len >= a.T) ? 1.f / lsum : 0.f;
+            const float inv = (lsum > 0.f && len >= a.T) ? g.out_scale / lsum : 0.f;
             store_pair(g, a, it.b, it.h, nt * 8 + c, 16 * gm + 2 * mm, acc0 * inv, acc1 * inv, rv);
           } else {
             float* drow = dst + (i * 8 + c) * kPartialStride;
@@ -1387,26 +1389,105 @@ __device__ __forceinline__ size_t dense_row_index(const Geometry& g, int h, int 
   return (size_t)bj * g.num_q_heads + h * g.group + k;
 }
 
-// q_rot[b][j][head] = R_k q[b][j][head] (fp32, unscaled); rot_k holds R_k transposed.
+// The dense rotation's work before the split-K kernel, one launch:
+//   * CTAs [0, q_ctas): q_rot[b][j][head] = R_k q[b][j][head] (fp32, unscaled); rot_k holds R_k
+//     transposed.  Each kv head's rows, in groups of 16, are shared out over q_ctas / Hkv CTAs,
+//     which stage the matrix once and take every (q_ctas / Hkv)-th group.
+//   * a decode step (a.k_new) adds 2 Hkv ceil(B / 16) CTAs, each coding 16 sequences' newest K
+//     (R_k) or V (R_v) vector of one kv head and writing it at position seq_lens[b] - 1: the
+//     fp32 R x of dense_rows decides every code farther than kFixBand from a boundary and the
+//     compensated dot product the others -- the decisions rq_quantize_append makes, so the two
+//     write the same bytes.
+template <int BITS>
 __global__ void __launch_bounds__(kHeadDim)
-rotate_q_dense_kernel(const Geometry g, const AttnArgs a) {
+dense_prologue_kernel(const Geometry g, const AttnArgs a, int q_ctas) {
   __shared__ __align__(16) float qs[kDenseRows][kHeadDim];
+  __shared__ __align__(16) float ys[kDenseRows][kHeadDim];
   extern __shared__ __align__(16) float wsm[];
-  const int h = blockIdx.x % g.num_kv_heads;
-  stage_matrix(wsm, g.rot_k + (size_t)h * kHeadDim * kHeadDim);
-  const int r0 = (blockIdx.x / g.num_kv_heads) * kDenseRows;
-  const int nr = min(kDenseRows, a.B * a.T * g.group - r0);
-  const __half* q = reinterpret_cast<const __half*>(a.q);
+  const int hkv = g.num_kv_heads;
+  if ((int)blockIdx.x < q_ctas) {
+    const int h = blockIdx.x % hkv, per_head = q_ctas / hkv;
+    stage_matrix(wsm, g.rot_k + (size_t)h * kHeadDim * kHeadDim);
+    const int rows = a.B * a.T * g.group;
+    const __half* q = reinterpret_cast<const __half*>(a.q);
+    for (int r0 = (blockIdx.x / hkv) * kDenseRows; r0 < rows; r0 += per_head * kDenseRows) {
+      const int nr = min(kDenseRows, rows - r0);
+      __syncthreads();  // the previous group's rows are read
+      for (int e = threadIdx.x; e < kDenseRows * kHeadDim; e += kHeadDim) {
+        const int r = e / kHeadDim, d = e % kHeadDim;
+        qs[r][d] = r < nr ? __half2float(q[dense_row_index(g, h, r0 + r) * kHeadDim + d]) : 0.f;
+      }
+      __syncthreads();
+      float acc[kDenseRows];
+      dense_rows(acc, wsm, qs);
+#pragma unroll
+      for (int r = 0; r < kDenseRows; ++r)
+        if (r < nr) a.q_rot[dense_row_index(g, h, r0 + r) * kHeadDim + threadIdx.x] = acc[r];
+    }
+    return;
+  }
+  // ---- the decode step's new tokens ----
+  const int c = blockIdx.x - q_ctas;
+  const int h = c % hkv, kind = (c / hkv) & 1, b0 = (c / (2 * hkv)) * kDenseRows;
+  const int i = threadIdx.x;
+  if (kind == 0) {
+    stage_matrix(wsm, g.rot_k + (size_t)h * kHeadDim * kHeadDim);  // [m][i] = R_k[i][m]
+  } else {  // [m][i] = R_v[i][m]: thread i copies row i of R_v into column i (conflict-free stores)
+    const float4* row = reinterpret_cast<const float4*>(g.rot_v + ((size_t)h * kHeadDim + i) * kHeadDim);
+#pragma unroll 4
+    for (int m4 = 0; m4 < kHeadDim / 4; ++m4) {
+      const float4 v = __ldg(row + m4);
+      wsm[(4 * m4) * kHeadDim + i] = v.x;
+      wsm[(4 * m4 + 1) * kHeadDim + i] = v.y;
+      wsm[(4 * m4 + 2) * kHeadDim + i] = v.z;
+      wsm[(4 * m4 + 3) * kHeadDim + i] = v.w;
+    }
+  }
+  const __half* src = kind ? a.v_new : a.k_new;
   for (int e = threadIdx.x; e < kDenseRows * kHeadDim; e += kHeadDim) {
-    const int r = e / kHeadDim, d = e % kHeadDim;
-    qs[r][d] = r < nr ? __half2float(q[dense_row_index(g, h, r0 + r) * kHeadDim + d]) : 0.f;
+    const int r = e / kHeadDim, d = e % kHeadDim, b = b0 + r;
+    qs[r][d] = b < a.B ? __half2float(src[((size_t)b * hkv + h) * kHeadDim + d]) : 0.f;
   }
   __syncthreads();
-  float acc[kDenseRows];
-  dense_rows(acc, wsm, qs);
+  {
+    float acc[kDenseRows];
+    dense_rows(acc, wsm, qs);
 #pragma unroll
-  for (int r = 0; r < kDenseRows; ++r)
-    if (r < nr) a.q_rot[dense_row_index(g, h, r0 + r) * kHeadDim + threadIdx.x] = acc[r];
+    for (int r = 0; r < kDenseRows; ++r) ys[r][i] = acc[r];
+  }
+  __syncthreads();
+  float bnd[15];
+  codec::load_boundaries<BITS>(bnd, g.boundaries);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, j = lane & 15;
+  const float* r32 = g.dense32 + ((size_t)kind * hkv + h) * kHeadDim * kHeadDim;  // fp32 R rows
+  const int cap = a.max_pages * g.page_size;
+#pragma unroll 1
+  for (int pass = 0; pass < kDenseRows / 8; ++pass) {  // a half-warp per vector, 8 per pass
+    const int r = 8 * pass + 2 * warp + half, b = b0 + r;
+    bool store = false;
+    int page = 0, off = 0;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (b < a.B) {
+      const int len = a.seq_lens[b];  // an out-of-range length is flagged by the split-K kernel
+      if (len >= 1 && len <= cap) {
+        const int pos = len - 1;
+        page = a.block_table[(size_t)b * a.max_pages + pos / g.page_size];
+        off = pos % g.page_size;
+        store = page >= 0 && page < g.num_pages;
+        if (!store && j == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_PAGE);
+        if (!store) page = 0;
+      }
+      raw = *reinterpret_cast<const uint4*>(src + ((size_t)b * hkv + h) * kHeadDim + 8 * j);
+    }
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = ys[r][8 * j + e];
+    int code[8];
+    float nrm;
+    codec::dense_codes<BITS>(code, nrm, raw, y, bnd, r32, store, lane);
+    uint8_t* chunk = const_cast<uint8_t*>(a.pages) + ((size_t)page * hkv + h) * (size_t)g.page_bytes;
+    codec::pack_store<BITS>(code, nrm, chunk, g.page_size, kind, off, j, store, a.status);
+  }
 }
 
 // The log-sum-exp merge of merge_splits for the CTA's rows, then out = R_v^T o~.
@@ -1492,7 +1573,11 @@ cudaError_t attention_prepare() {
   if (e == cudaSuccess) e = set_smem_limits<3>();
   if (e == cudaSuccess) e = set_smem_limits<4>();
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(rotate_q_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+    e = cudaFuncSetAttribute(dense_prologue_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dense_prologue_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dense_prologue_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(attn_combine_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
   return e;
@@ -1520,18 +1605,41 @@ static void launch_splitk(const Geometry& g, const AttnArgs& a, cudaStream_t str
     launch_splitk_nt<BITS, 3>(g, a, stream);
 }
 
+// The dense rotation's prologue launch: query rows, plus a decode step's new tokens.  A kv
+// head's 16-row groups go to at most kDenseQCtasPerHead CTAs (the 64 KB matrix is staged once
+// per CTA, so few rows per CTA would be bound by the staging).
+constexpr int kDenseQCtasPerHead = 64;
+static cudaError_t launch_dense_prologue(const Geometry& g, const AttnArgs& a, cudaStream_t stream) {
+  const long long rows_per_head = (long long)a.B * a.T * g.group;
+  const long long groups = (rows_per_head + kDenseRows - 1) / kDenseRows;
+  const long long q_ctas = (long long)g.num_kv_heads * (groups < kDenseQCtasPerHead ? groups : kDenseQCtasPerHead);
+  const long long step_ctas = a.k_new ? 2LL * g.num_kv_heads * ((a.B + kDenseRows - 1) / kDenseRows) : 0;
+  if (q_ctas + step_ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const unsigned ctas = (unsigned)(q_ctas + step_ctas);
+  if (g.bits == 4)
+    dense_prologue_kernel<4><<<ctas, kHeadDim, kDenseSmem, stream>>>(g, a, (int)q_ctas);
+  else if (g.bits == 3)
+    dense_prologue_kernel<3><<<ctas, kHeadDim, kDenseSmem, stream>>>(g, a, (int)q_ctas);
+  else
+    dense_prologue_kernel<2><<<ctas, kHeadDim, kDenseSmem, stream>>>(g, a, (int)q_ctas);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dense_rotate_q(const Geometry& g, const AttnArgs& a, cudaStream_t stream) {
+  if (a.B <= 0) return cudaSuccess;
+  if (g.mode != RQ_DENSE || !a.q_rot || a.k_new) return cudaErrorInvalidValue;
+  return launch_dense_prologue(g, a, stream);
+}
+
 cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
                              cudaEvent_t ev_end) {
   if (a.B <= 0) return cudaSuccess;
   const bool dense = g.mode == RQ_DENSE;
   if (dense != (a.q_rot != nullptr)) return cudaErrorInvalidValue;
-  if (a.k_new && (dense || !a.v_new || !g.boundaries || a.T != 1)) return cudaErrorInvalidValue;
+  if (a.k_new && (!a.v_new || !g.boundaries || a.T != 1 || (dense && !g.dense32))) return cudaErrorInvalidValue;
   if (a.nt != attention_unit_tiles(a.n_tiles_n, a.k_new != nullptr)) return cudaErrorInvalidValue;
-  const long long rows_per_head = (long long)a.B * a.T * g.group;
-  const unsigned groups = (unsigned)(g.num_kv_heads * ((rows_per_head + kDenseRows - 1) / kDenseRows));
-  if (dense) {
-    rotate_q_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a);
-    cudaError_t e = cudaGetLastError();
+  if (dense) {  // R_k q (and a decode step's new tokens) first; the split-K kernel reads them
+    cudaError_t e = launch_dense_prologue(g, a, stream);
     if (e != cudaSuccess) return e;
   }
   if (a.grid > 0) {
@@ -1547,7 +1655,11 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t 
     if (ev_end) cudaEventRecord(ev_end, stream);
   }
   // planar / iso: the split-K kernel finishes every unit itself
-  if (dense) attn_combine_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a);
+  if (dense) {
+    const long long rows_per_head = (long long)a.B * a.T * g.group;
+    const unsigned groups = (unsigned)(g.num_kv_heads * ((rows_per_head + kDenseRows - 1) / kDenseRows));
+    attn_combine_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a);
+  }
   return cudaGetLastError();
 }
 

@@ -218,6 +218,92 @@ __device__ __forceinline__ Packed encode_packed(uint4 raw, const float (&p)[8], 
   return Packed{pack_codes<BITS>(code, j), (uint32_t)__half_as_ushort(__float2half_rn(nrm))};
 }
 
+// y_i = sum_m x_m R[i][m] for one vector, summed exactly enough to be correctly rounded in all
+// but pathological cases: error-free products (fma) and error-free sums (two-sum), the rounding
+// errors carried in a second word.  Lane j of the half-warp holds x[8j..8j+7]; `row` is R's row
+// i in global memory (rarely read: L2).  Every lane of the warp calls it (shuffles stay within
+// each half).
+__device__ __forceinline__ float dot_compensated(const float (&x)[8], const float* row, int j) {
+  const float4 r0 = __ldg(reinterpret_cast<const float4*>(row + 8 * j));
+  const float4 r1 = __ldg(reinterpret_cast<const float4*>(row + 8 * j + 4));
+  const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+  float s = 0.f, c = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float p = x[e] * rr[e];
+    const float pe = fmaf(x[e], rr[e], -p);  // x * r = p + pe exactly
+    const float t = s + p;
+    const float z = t - s;
+    c += ((s - (t - z)) + (p - z)) + pe;     // s + p = t + (that) exactly
+    s = t;
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+    const float t = s + s2;
+    const float z = t - s;
+    c += c2 + ((s - (t - z)) + (s2 - z));
+    s = t;
+  }
+  return s + c;
+}
+
+// A dense rotation's y = R x is computed approximately (tensor cores, or an fp32 multiply-add
+// chain) and trusted to decide a code when u is farther than this from every boundary.  The
+// tensor-core error is the hi + lo split (|R - hi - lo| <= 6e-8 per entry, so <= 7e-7 in u by
+// Cauchy-Schwarz) plus the accumulation of 16 fp32 MMA steps (a few fp32 ulps of n each); an fp32
+// chain of 128 multiply-adds stays well inside it too.
+constexpr float kFixBand = 1e-5f;
+
+// Codes of one vector under a dense rotation, a half-warp per vector (lane j: dims 8j..8j+7):
+// raw = the lane's 16 bytes of x (fp16), y = its 8 coordinates of the approximate R x.  Each
+// coordinate whose u lies within kFixBand of a boundary is recomputed with dot_compensated from
+// the fp32 rows of R (r32, row-major), one at a time per half-warp (both halves walk their lists
+// together), and re-coded; so the codes are those of the correctly rounded y, whichever
+// approximation gave y.  Also returns the fp32 norm.  Every lane of the warp must call it.
+template <int BITS>
+__device__ __forceinline__ void dense_codes(int (&code)[8], float& nrm, uint4 raw, const float (&y)[8],
+                                            const float (&bnd)[15], const float* r32, bool store, int lane) {
+  const int half = lane >> 4, j = lane & 15;
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  float x[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+    x[2 * e] = f.x;
+    x[2 * e + 1] = f.y;
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  nrm = __fsqrt_rn(ss);
+  const float rcp = inv_norm(nrm);
+  uint32_t todo = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float dm;
+    code[e] = code_of_margin<BITS>(y[e] * rcp, bnd, dm);
+    if (dm < kFixBand && store) todo |= 1u << e;
+  }
+  while (__any_sync(0xffffffffu, todo != 0)) {
+    const uint32_t want = __ballot_sync(0xffffffffu, todo != 0) & (half ? 0xffff0000u : 0x0000ffffu);
+    const int leader = want ? __ffs(want) - 1 : (half << 4);  // no work: any lane, result unused
+    const int e_lead = __shfl_sync(0xffffffffu, todo ? __ffs(todo) - 1 : 0, leader);
+    const int i = 8 * (leader & 15) + e_lead;  // the coordinate (dim of y) being recomputed
+    const float yi = dot_compensated(x, r32 + i * 128, j);
+    if (lane == leader && want) {
+      const int c = code_of<BITS>(yi * rcp, bnd);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (e == e_lead) code[e] = c;
+      todo &= ~(1u << e_lead);
+    }
+  }
+}
+
 // encode_packed, written to slot `off` of `chunk` (`store` false writes nothing).
 template <int BITS>
 __device__ __forceinline__ void encode_structured(uint4 raw, const float (&p)[8], int mode, const float (&bnd)[15],

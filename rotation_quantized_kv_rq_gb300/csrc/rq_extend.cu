@@ -330,7 +330,10 @@ __device__ __forceinline__ void v_pairs(uint32_t (&out)[16], const GroupRaw& A, 
   }
 }
 
-template <int BITS>
+// DENSE: a dense rotation (TurboQuant): the queries come pre-rotated in a.q_rot (fp32), and the
+// output rotation R_v^T is a 128 x 128 matrix-vector product per row, done once every role is
+// finished with R_v staged in the code table's 64 KB.
+template <int BITS, bool DENSE>
 __global__ void __launch_bounds__(kXThreads, 1)
 extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -399,10 +402,22 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
                                                        (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
     const float4* rk = reinterpret_cast<const float4*>(g.rot_k + (size_t)h * kHeadDim);
     uint8_t* const qs = at(blk ? pl.q[1] : pl.q[0]);
+    const float4* qrot = DENSE ? reinterpret_cast<const float4*>(a.q_rot + (((size_t)b * a.T + j) * g.num_q_heads + head) *
+                                                                              kHeadDim)
+                               : nullptr;
 #pragma unroll 4
     for (int c = 0; c < 16; ++c) {  // dims 8c .. 8c + 7: two rotation blocks of 4
       uint32_t w[4] = {0u, 0u, 0u, 0u};
-      if (valid) {
+      if (DENSE && valid) {  // R_k q, formed before the launch
+#pragma unroll
+        for (int bk = 0; bk < 2; ++bk) {
+          const float4 yv = __ldg(qrot + 2 * c + bk);
+          const float y[4] = {yv.x, yv.y, yv.z, yv.w};
+          const int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;  // the K~ order of a 4-dim block
+          w[2 * bk] = pack_h2(y[0] * g.q_scale, y[s1] * g.q_scale);
+          w[2 * bk + 1] = pack_h2(y[s2] * g.q_scale, y[3] * g.q_scale);
+        }
+      } else if (valid) {
         const uint4 raw8 = __ldg(qrow + c);
         const uint32_t hw[4] = {raw8.x, raw8.y, raw8.z, raw8.w};
 #pragma unroll
@@ -439,6 +454,8 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(at(mb + kTmemSlot));
 
+  float soft_inv = 0.f;   // dense: the row's 1 / l, for the epilogue after every role is done
+  bool soft_ok = false;
   if (warp < kXSoftWarps) {
     // ================= softmax: one thread per row of block blk =================
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -535,9 +552,12 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       ok = __all_sync(0xffffffffu, role_wait(mb + kBarODone + 8 * blk, (uint32_t)((n_tiles - 1) & 1), abort_flag));
       if (ok) fence_after_sync();
     }
-    if (ok) {
+    if (DENSE) {
+      soft_ok = ok;
+      soft_inv = l_run > 0.f ? g.out_scale / l_run : 0.f;
+    } else if (ok) {
       const bool store = r < a.rows;
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv = l_run > 0.f ? g.out_scale / l_run : 0.f;
       const int j = store ? r / g.group : 0, head = h * g.group + (store ? r % g.group : 0);
       uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(a.out) +
                                              (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
@@ -711,6 +731,59 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     }
     if (!ok && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
   }
+  if constexpr (DENSE) {
+    // ---- normalise, rotate back (out = R_v^T o~, a full matrix), store ----
+    fence_before_sync();
+    __syncthreads();  // every role is done: the code table is free and O~ is final
+    fence_after_sync();
+    float4* const rvs = reinterpret_cast<float4*>(at(pl.lut));  // R_v row-major: [m][i / 4]
+    const float4* rsrc = reinterpret_cast<const float4*>(g.rot_v + (size_t)h * kHeadDim * kHeadDim);
+    for (int c = tid; c < kHeadDim * kHeadDim / 4; c += kXThreads) rvs[c] = __ldg(rsrc + c);
+    __syncthreads();
+    if (warp < kXSoftWarps && soft_ok) {  // soft_ok is uniform over each warp
+      const uint32_t tmem_o = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128 * blk;
+      const bool store = r < a.rows;
+      const int j = store ? r / g.group : 0, head = h * g.group + (store ? r % g.group : 0);
+      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(a.out) +
+                                             (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
+#pragma unroll 1
+      for (int ic = 0; ic < kHeadDim / 32; ++ic) {  // outputs 32 ic .. 32 ic + 31
+        float acc[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+#pragma unroll 1
+        for (int mc = 0; mc < kHeadDim / 16; ++mc) {  // o~ dims 16 mc .. 16 mc + 15
+          float v[16];
+          if (n_tiles > 0) {  // uniform over the CTA
+            tmem_ld16(tmem_o + 16 * mc, v);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float om = v[k] * soft_inv;
+            const float4* wrow = rvs + (16 * mc + k) * (kHeadDim / 4) + 8 * ic;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 w = wrow[q];
+              acc[4 * q] = fmaf(w.x, om, acc[4 * q]);
+              acc[4 * q + 1] = fmaf(w.y, om, acc[4 * q + 1]);
+              acc[4 * q + 2] = fmaf(w.z, om, acc[4 * q + 2]);
+              acc[4 * q + 3] = fmaf(w.w, om, acc[4 * q + 3]);
+            }
+          }
+        }
+        if (store) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            orow[4 * ic + q] = make_uint4(pack_h2(acc[8 * q], acc[8 * q + 1]), pack_h2(acc[8 * q + 2], acc[8 * q + 3]),
+                                          pack_h2(acc[8 * q + 4], acc[8 * q + 5]), pack_h2(acc[8 * q + 6], acc[8 * q + 7]));
+        }
+      }
+    }
+  }
   fence_before_sync();
   __syncthreads();
   if (warp == 0)
@@ -719,26 +792,48 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
 
 }  // namespace
 
-cudaError_t extend_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(extend_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(extend_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(extend_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
+template <bool DENSE>
+static cudaError_t extend_prepare_flag() {
+  cudaError_t e = cudaFuncSetAttribute(extend_kernel<2, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(extend_kernel<3, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(extend_kernel<4, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
   return e;
+}
+
+cudaError_t extend_prepare() {
+  cudaError_t e = extend_prepare_flag<false>();
+  if (e == cudaSuccess) e = extend_prepare_flag<true>();
+  return e;
+}
+
+template <bool DENSE>
+static void launch_extend_flag(const Geometry& g, const AttnArgs& a, unsigned ctas, cudaStream_t stream) {
+  if (g.bits == 4)
+    extend_kernel<4, DENSE><<<ctas, kXThreads, kXSmem, stream>>>(g, a, kXSmem);
+  else if (g.bits == 3)
+    extend_kernel<3, DENSE><<<ctas, kXThreads, kXSmem, stream>>>(g, a, kXSmem);
+  else
+    extend_kernel<2, DENSE><<<ctas, kXThreads, kXSmem, stream>>>(g, a, kXSmem);
 }
 
 cudaError_t launch_extend(const Geometry& g, const AttnArgs& a, cudaStream_t stream, cudaEvent_t ev_start,
                           cudaEvent_t ev_end) {
   if (a.B <= 0) return cudaSuccess;
-  if (g.mode == RQ_DENSE) return cudaErrorInvalidValue;
+  const bool dense = g.mode == RQ_DENSE;
+  if (dense != (a.q_rot != nullptr)) return cudaErrorInvalidValue;
   const long long ctas = (long long)a.B * g.num_kv_heads * ((a.rows + kXRows - 1) / kXRows);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (dense) {  // R_k q of every row first
+    cudaError_t e = launch_dense_rotate_q(g, a, stream);
+    if (e != cudaSuccess) return e;
+  }
   if (ev_start) cudaEventRecord(ev_start, stream);
-  if (g.bits == 4)
-    extend_kernel<4><<<(unsigned)ctas, kXThreads, kXSmem, stream>>>(g, a, kXSmem);
-  else if (g.bits == 3)
-    extend_kernel<3><<<(unsigned)ctas, kXThreads, kXSmem, stream>>>(g, a, kXSmem);
+  if (dense)
+    launch_extend_flag<true>(g, a, (unsigned)ctas, stream);
   else
-    extend_kernel<2><<<(unsigned)ctas, kXThreads, kXSmem, stream>>>(g, a, kXSmem);
+    launch_extend_flag<false>(g, a, (unsigned)ctas, stream);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess && ev_end) cudaEventRecord(ev_end, stream);
   return e;

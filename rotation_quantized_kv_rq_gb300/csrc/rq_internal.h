@@ -22,7 +22,11 @@ struct Geometry {
   int num_pages;
   int vec_bytes;       // head_dim * bits / 8
   int page_bytes;      // page_size * (2 * vec_bytes + 4)
-  float q_scale;       // sm_scale * log2(e): scores are kept in base 2
+  // The attention kernels multiply fp16 centroids c' = c / out_scale (the table `centroids`),
+  // out_scale chosen so that the codebook's fp16 images are as exact as possible; q_scale and
+  // the final normalisation carry it back, so the results are those of c.
+  float q_scale;       // sm_scale * log2(e) * out_scale: scores are kept in base 2
+  float out_scale;     // multiplies every attention output row (with its 1 / sum of p)
   // planar / iso: device [Hkv][128] rotation parameters.
   // dense: rot_k = device [Hkv][128][128] R_k TRANSPOSED (query rotation reads it column-wise),
   //        rot_v = device [Hkv][128][128] R_v (output rotation R_v^T o reads it row-wise).
@@ -33,7 +37,7 @@ struct Geometry {
   const __half* dense16;
   // dense only: device fp32 [2 (K, V)][Hkv][128][128] row-major R (exact recompute in the append)
   const float* dense32;
-  const float* centroids;   // device [2^bits]
+  const float* centroids;   // device [2^bits]: c / out_scale, the fp16 operands' source
   const float* boundaries;  // device [2^bits - 1]
 };
 
@@ -58,8 +62,9 @@ struct AttnArgs {
   int nt;                    // n-tiles per unit: attention_unit_tiles(n_tiles_n, k_new != null)
   const uint64_t* tree_mask; // [B][T] draft visibility bits (tree verify), or null (causal chain)
   float* q_rot;              // dense: fp32 [B][T][Hq][128] scratch for R_k q; null otherwise
-  // Decode step (planar / iso): fp16 [B][Hkv][128] K and V of each sequence's newest token,
-  // position seq_lens[b] - 1, quantized into the cache by the split-K kernel itself; or null.
+  // Decode step: fp16 [B][Hkv][128] K and V of each sequence's newest token, position
+  // seq_lens[b] - 1, quantized into the cache by the split-K kernel itself (planar / iso) or by
+  // the dense prologue kernel (dense); or null.
   const __half* k_new;
   const __half* v_new;
 };
@@ -77,7 +82,11 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t 
 // many sequences per call.
 constexpr int kMaxBatch = 8000;
 
-// Extend (prefill) attention: T query tokens per sequence, causal, no workspace.
+// Dense rotation: a.q_rot = R_k q for every query row of the call (fp32), one launch.
+cudaError_t launch_dense_rotate_q(const Geometry& g, const AttnArgs& a, cudaStream_t stream);
+
+// Extend (prefill) attention: T query tokens per sequence, causal; a dense rotation's queries
+// come pre-rotated in a.q_rot (launch_dense_rotate_q), other rotations need no workspace.
 cudaError_t launch_extend(const Geometry& g, const AttnArgs& a, cudaStream_t stream, cudaEvent_t ev_start = nullptr,
                           cudaEvent_t ev_end = nullptr);
 cudaError_t extend_prepare();

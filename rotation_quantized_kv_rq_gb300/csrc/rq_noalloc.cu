@@ -104,6 +104,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   g.page_bytes = cfg->page_size * (2 * g.vec_bytes + 4);
   const float scale = cfg->sm_scale > 0.f ? cfg->sm_scale : (float)(1.0 / std::sqrt((double)rq::kHeadDim));
   g.q_scale = (float)(scale * 1.44269504088896340736);
+  g.out_scale = 1.f;  // the caller's centroids, unscaled
   g.rot_k = d_rot_k;
   g.rot_v = d_rot_v;
   g.dense16 = nullptr;

@@ -21,6 +21,8 @@ Workloads (geometry from the five synthetic decode/verify configurations of this
   tq3_prefill  dense-rotation quantize-append of 65536 tokens x 8 kv heads.
   cfg3_extend  extend (chunked prefill): 8 sequences of 15360 cached tokens take 1024 new tokens
         each, appended then attended causally (rq3 iso, 32/8 heads, page 16).
+  tq3_extend  cfg3_extend with the dense rotation.
+  tq3_step  cfg1 (a decode step of 16 x 8K, 1 new token per sequence) with the dense rotation.
 
 Distributions: Q, V ~ N(0, 1); K ~ N(0, 1) with 4 distinct channels per kv head (drawn from
 the seed, fixed for all tokens) multiplied by 10 after sampling; fp16 storage.
@@ -72,6 +74,9 @@ SPECS = {
     "tq2_32k": Spec("tq2_32k", DENSE, 2, 32, 32768, 64, 8, 16, appended=0, seed=1002),
     # extend: the cfg3 geometry and seed, 1024 new tokens per sequence
     "cfg3_extend": Spec("cfg3_extend", ISO, 3, 8, 16384, 32, 8, 16, query_tokens=1024, appended=1024, seed=1003),
+    # TurboQuant on the same geometries: an extend, and a decode step (cfg1's)
+    "tq3_extend": Spec("tq3_extend", DENSE, 3, 8, 16384, 32, 8, 16, query_tokens=1024, appended=1024, seed=1003),
+    "tq3_step": Spec("tq3_step", DENSE, 3, 16, 8192, 32, 8, 16, k_offset_var=0.5, appended=1, seed=1001),
 }
 EXTEND_MIN_T = 64  # query tokens from which a step attends with the extend kernel
 PREFILL_TOKENS = 65536     # prefill workloads: one sequence, all 8 kv heads, K and V

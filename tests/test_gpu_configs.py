@@ -149,7 +149,7 @@ def _check_sequence(bn, b, out_gpu):
 
 
 @pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg2", "cfg2_32k", "cfg3", "cfg4", "cfg3_prefill", "tq4_32k",
-                                  "tq2_32k", "tq3_prefill", "cfg3_extend"])
+                                  "tq2_32k", "tq3_prefill", "cfg3_extend", "tq3_extend", "tq3_step"])
 def test_full_size_workload(name, capsys):
     dev = torch.device("cuda", 0)
     bn = bench.Bench(name, dev)

@@ -303,6 +303,10 @@ STEP_CASES = [
     # 344 rounds over the CTAs: ranges cross unit boundaries, so tokens land in a CTA's second
     # fragment and in units split across CTAs
     (PLANAR, 3, 32, 8, 16, [5000, 3000, 777, 12345]),
+    # dense rotation: the tokens are coded by the launch that rotates the queries
+    (DENSE, 3, 32, 8, 16, [300, 17, 1, 64]),
+    (DENSE, 4, 64, 8, 64, [200, 2049, 129]),
+    (DENSE, 2, 96, 8, 16, [100, 33]),
 ]
 
 
@@ -375,6 +379,10 @@ EXTEND_CASES = [
     (ISO, 4, 24, 2, 32, [129, 70], 70),      # group 12: 64-row blocks cut through a draft's heads
     (PLANAR, 3, 8, 8, 16, [2048], 256),
     (ISO, 2, 32, 8, 16, [0, 130, 64], 64),  # an empty sequence (zeros) and one of only new tokens
+    # dense rotation: queries rotated before the launch, R_v^T per row at the end
+    (DENSE, 3, 32, 8, 16, [300, 1000], 64),
+    (DENSE, 2, 64, 8, 64, [200, 513], 100),
+    (DENSE, 4, 24, 2, 32, [0, 129, 70], 70),
 ]
 
 
