@@ -105,12 +105,19 @@ def max_over_ranks(x, world):
 # ---------------------------------------------------------------------------------------
 # workload setup
 # ---------------------------------------------------------------------------------------
+def spec_of(name, batch=None):
+    """The workload's Spec; `batch` (profiling a smaller case of the same kernel) keeps its
+    first `batch` sequences."""
+    s = synth.prefill_spec(name) if name in synth.PREFILL else synth.SPECS[name]
+    return synth.scaled(s, batch=batch) if batch else s
+
+
 class Bench:
-    def __init__(self, name, device):
+    def __init__(self, name, device, batch=None):
         self.name = name
         self.device = device
         self.prefill_only = name in synth.PREFILL
-        spec = synth.prefill_spec(name) if self.prefill_only else synth.SPECS[name]
+        spec = spec_of(name, batch)
         self.spec = spec
         self.wl = synth.workload(spec)
         s, wl = spec, self.wl
@@ -497,9 +504,9 @@ def host_cores():
 TARGET_WORKLOAD = "cfg2_32k"  # the long-context decode the roofline target is stated at
 
 
-def config_of(name, world):
+def config_of(name, world, batch=None):
     """The `config` object of a workload's JSON line (the same on both arms)."""
-    s = synth.prefill_spec(name) if name in synth.PREFILL else synth.SPECS[name]
+    s = spec_of(name, batch)
     wl = synth.workload(s)
     packed = int(wl.seq_lens.astype(np.int64).sum()) * s.num_kv_heads * (32 * s.bits + 4)
     fused = name not in synth.PREFILL and s.appended == 1 and s.query_tokens == 1
@@ -631,7 +638,7 @@ def attention_roofline(bench, kern_ms, peak, peak_kind, workload):
 def run_ours(args, rank, world, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    bench = Bench(args.workload, device)
+    bench = Bench(args.workload, device, args.batch)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     K = args.steps
@@ -707,7 +714,7 @@ def run_ours(args, rank, world, local):
     # ---- the long-context decode the roofline target is stated at (32 x 32K rq4 iso), timed
     # the same way in the same process, after the headline workload's own measurement
     target = None
-    if not args.no_target and args.workload != TARGET_WORKLOAD:
+    if not args.no_target and args.workload != TARGET_WORKLOAD and not args.batch:
         bench.cache.close()
         del bench
         torch.cuda.empty_cache()
@@ -728,19 +735,19 @@ def run_ours(args, rank, world, local):
         del tb
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not args.batch:
         rate, sample, secs, cores = oracle_step_rate(args.workload, budget_s=args.cpu_budget, threads=host_cores())
         rate1, sample1, secs1, _ = oracle_step_rate(args.workload, budget_s=args.cpu_budget / 2, threads=1)
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": round(secs, 2),
                "one_core": {"value": rate1, "sample": sample1, "seconds": round(secs1, 2)}}
-    s = synth.prefill_spec(args.workload) if args.workload in synth.PREFILL else synth.SPECS[args.workload]
-    packed = config_of(args.workload, world)["packed_kv_bytes"]
+    s = spec_of(args.workload, args.batch)
+    packed = config_of(args.workload, world, args.batch)["packed_kv_bytes"]
     line = {
         "metric": "decode-attn tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": f"u{s.bits} codes, f16 mma, f32 accumulate", "data": "synthetic",
-        "config": config_of(args.workload, world),
+        "config": config_of(args.workload, world, args.batch),
         "packed_kv_gbs": packed / (ms * 1e-3) / 1e9,
         "roofline": roof,
         "target_32k": target,
@@ -767,6 +774,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-target", action="store_true",
                     help="skip the 32 x 32K decode sub-record timed after the workload")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="profiling: the workload's first BATCH sequences only (no baseline or target legs)")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":

@@ -1366,11 +1366,11 @@ __device__ __forceinline__ void stage_matrix(float* ws, const float* __restrict_
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
-// out[r][i] = sum_m ws[m * 128 + i] * xs[r][m] for the CTA's rows (thread i).
-__device__ __forceinline__ void dense_rows(float (&acc)[kDenseRows], const float* ws, const float (*xs)[kHeadDim]) {
+// out[r][i] = sum_m ws[m * 128 + i] * xs[r][m] for 16 rows (the calling thread's dim i).
+__device__ __forceinline__ void dense_rows(float (&acc)[kDenseRows], const float* ws, const float (*xs)[kHeadDim],
+                                           int i) {
 #pragma unroll
   for (int r = 0; r < kDenseRows; ++r) acc[r] = 0.f;
-  const int i = threadIdx.x;
 #pragma unroll 2
   for (int m = 0; m < kHeadDim; m += 4) {
     const float w0 = ws[(m + 0) * kHeadDim + i], w1 = ws[(m + 1) * kHeadDim + i];
@@ -1389,50 +1389,57 @@ __device__ __forceinline__ size_t dense_row_index(const Geometry& g, int h, int 
   return (size_t)bj * g.num_q_heads + h * g.group + k;
 }
 
-// The dense rotation's work before the split-K kernel, one launch:
+// The dense rotation's work before the split-K kernel, one launch of 512-thread CTAs (four
+// 128-thread slices; thread i of a slice owns output dim i):
 //   * CTAs [0, q_ctas): q_rot[b][j][head] = R_k q[b][j][head] (fp32, unscaled); rot_k holds R_k
 //     transposed.  Each kv head's rows, in groups of 16, are shared out over q_ctas / Hkv CTAs,
-//     which stage the matrix once and take every (q_ctas / Hkv)-th group.
+//     which stage the matrix once; the four slices take four groups at a time.
 //   * a decode step (a.k_new) adds 2 Hkv ceil(B / 16) CTAs, each coding 16 sequences' newest K
-//     (R_k) or V (R_v) vector of one kv head and writing it at position seq_lens[b] - 1: the
-//     fp32 R x of dense_rows decides every code farther than kFixBand from a boundary and the
-//     compensated dot product the others -- the decisions rq_quantize_append makes, so the two
-//     write the same bytes.
+//     (R_k) or V (R_v) vector of one kv head and writing it at position seq_lens[b] - 1 (slice
+//     0 computes): the fp32 R x of dense_rows decides every code farther than kFixBand from a
+//     boundary and the compensated dot product the others -- the decisions rq_quantize_append
+//     makes, so the two write the same bytes.
+constexpr int kDenseSlices = 4;
+constexpr int kDenseThreads = kDenseSlices * kHeadDim;
 template <int BITS>
-__global__ void __launch_bounds__(kHeadDim)
+__global__ void __launch_bounds__(kDenseThreads, 2)
 dense_prologue_kernel(const Geometry g, const AttnArgs a, int q_ctas) {
-  __shared__ __align__(16) float qs[kDenseRows][kHeadDim];
-  __shared__ __align__(16) float ys[kDenseRows][kHeadDim];
+  __shared__ __align__(16) float qs[kDenseSlices][kDenseRows][kHeadDim];
   extern __shared__ __align__(16) float wsm[];
   const int hkv = g.num_kv_heads;
+  const int slice = threadIdx.x / kHeadDim, i = threadIdx.x % kHeadDim;
   if ((int)blockIdx.x < q_ctas) {
     const int h = blockIdx.x % hkv, per_head = q_ctas / hkv;
     stage_matrix(wsm, g.rot_k + (size_t)h * kHeadDim * kHeadDim);
     const int rows = a.B * a.T * g.group;
+    const int groups = (rows + kDenseRows - 1) / kDenseRows;
     const __half* q = reinterpret_cast<const __half*>(a.q);
-    for (int r0 = (blockIdx.x / hkv) * kDenseRows; r0 < rows; r0 += per_head * kDenseRows) {
-      const int nr = min(kDenseRows, rows - r0);
-      __syncthreads();  // the previous group's rows are read
-      for (int e = threadIdx.x; e < kDenseRows * kHeadDim; e += kHeadDim) {
+    // (the loop bound is uniform over the CTA: every thread reaches every barrier)
+    for (int g0 = (blockIdx.x / hkv) * kDenseSlices; g0 < groups; g0 += per_head * kDenseSlices) {
+      const int r0 = (g0 + slice) * kDenseRows;
+      const int nr = max(0, min(kDenseRows, rows - r0));
+      __syncthreads();  // the previous groups' rows are read
+      for (int e = i; e < kDenseRows * kHeadDim; e += kHeadDim) {
         const int r = e / kHeadDim, d = e % kHeadDim;
-        qs[r][d] = r < nr ? __half2float(q[dense_row_index(g, h, r0 + r) * kHeadDim + d]) : 0.f;
+        qs[slice][r][d] = r < nr ? __half2float(q[dense_row_index(g, h, r0 + r) * kHeadDim + d]) : 0.f;
       }
       __syncthreads();
-      float acc[kDenseRows];
-      dense_rows(acc, wsm, qs);
+      if (nr > 0) {
+        float acc[kDenseRows];
+        dense_rows(acc, wsm, qs[slice], i);
 #pragma unroll
-      for (int r = 0; r < kDenseRows; ++r)
-        if (r < nr) a.q_rot[dense_row_index(g, h, r0 + r) * kHeadDim + threadIdx.x] = acc[r];
+        for (int r = 0; r < kDenseRows; ++r)
+          if (r < nr) a.q_rot[dense_row_index(g, h, r0 + r) * kHeadDim + i] = acc[r];
+      }
     }
     return;
   }
-  // ---- the decode step's new tokens ----
+  // ---- the decode step's new tokens (slice 0; every thread stages and reaches the barriers) ----
   const int c = blockIdx.x - q_ctas;
   const int h = c % hkv, kind = (c / hkv) & 1, b0 = (c / (2 * hkv)) * kDenseRows;
-  const int i = threadIdx.x;
   if (kind == 0) {
     stage_matrix(wsm, g.rot_k + (size_t)h * kHeadDim * kHeadDim);  // [m][i] = R_k[i][m]
-  } else {  // [m][i] = R_v[i][m]: thread i copies row i of R_v into column i (conflict-free stores)
+  } else if (slice == 0) {  // [m][i] = R_v[i][m]: thread i copies row i of R_v into column i
     const float4* row = reinterpret_cast<const float4*>(g.rot_v + ((size_t)h * kHeadDim + i) * kHeadDim);
 #pragma unroll 4
     for (int m4 = 0; m4 < kHeadDim / 4; ++m4) {
@@ -1444,18 +1451,21 @@ dense_prologue_kernel(const Geometry g, const AttnArgs a, int q_ctas) {
     }
   }
   const __half* src = kind ? a.v_new : a.k_new;
-  for (int e = threadIdx.x; e < kDenseRows * kHeadDim; e += kHeadDim) {
-    const int r = e / kHeadDim, d = e % kHeadDim, b = b0 + r;
-    qs[r][d] = b < a.B ? __half2float(src[((size_t)b * hkv + h) * kHeadDim + d]) : 0.f;
+  if (slice == 0) {
+    for (int e = i; e < kDenseRows * kHeadDim; e += kHeadDim) {
+      const int r = e / kHeadDim, d = e % kHeadDim, b = b0 + r;
+      qs[0][r][d] = b < a.B ? __half2float(src[((size_t)b * hkv + h) * kHeadDim + d]) : 0.f;
+    }
   }
   __syncthreads();
-  {
+  if (slice == 0) {
     float acc[kDenseRows];
-    dense_rows(acc, wsm, qs);
+    dense_rows(acc, wsm, qs[0], i);
 #pragma unroll
-    for (int r = 0; r < kDenseRows; ++r) ys[r][i] = acc[r];
+    for (int r = 0; r < kDenseRows; ++r) qs[1][r][i] = acc[r];  // y, beside x
   }
   __syncthreads();
+  if (slice != 0) return;  // no barrier follows
   float bnd[15];
   codec::load_boundaries<BITS>(bnd, g.boundaries);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, j = lane & 15;
@@ -1481,7 +1491,7 @@ dense_prologue_kernel(const Geometry g, const AttnArgs a, int q_ctas) {
     }
     float y[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = ys[r][8 * j + e];
+    for (int e = 0; e < 8; ++e) y[e] = qs[1][r][8 * j + e];
     int code[8];
     float nrm;
     codec::dense_codes<BITS>(code, nrm, raw, y, bnd, r32, store, lane);
@@ -1511,7 +1521,7 @@ attn_combine_dense_kernel(const Geometry g, const AttnArgs a) {
   }
   __syncthreads();
   float acc[kDenseRows];
-  dense_rows(acc, wsm, os);
+  dense_rows(acc, wsm, os, threadIdx.x);
   __half* out = reinterpret_cast<__half*>(a.out);
 #pragma unroll
   for (int r = 0; r < kDenseRows; ++r)
@@ -1606,22 +1616,22 @@ static void launch_splitk(const Geometry& g, const AttnArgs& a, cudaStream_t str
 }
 
 // The dense rotation's prologue launch: query rows, plus a decode step's new tokens.  A kv
-// head's 16-row groups go to at most kDenseQCtasPerHead CTAs (the 64 KB matrix is staged once
-// per CTA, so few rows per CTA would be bound by the staging).
-constexpr int kDenseQCtasPerHead = 64;
+// head's 16-row groups go to at most kDenseQCtasPerHead CTAs, four groups at a time (the 64 KB
+// matrix is staged once per CTA, so few rows per CTA would be bound by the staging).
+constexpr int kDenseQCtasPerHead = 32;
 static cudaError_t launch_dense_prologue(const Geometry& g, const AttnArgs& a, cudaStream_t stream) {
   const long long rows_per_head = (long long)a.B * a.T * g.group;
-  const long long groups = (rows_per_head + kDenseRows - 1) / kDenseRows;
-  const long long q_ctas = (long long)g.num_kv_heads * (groups < kDenseQCtasPerHead ? groups : kDenseQCtasPerHead);
+  const long long quads = (rows_per_head + kDenseSlices * kDenseRows - 1) / (kDenseSlices * kDenseRows);
+  const long long q_ctas = (long long)g.num_kv_heads * (quads < kDenseQCtasPerHead ? quads : kDenseQCtasPerHead);
   const long long step_ctas = a.k_new ? 2LL * g.num_kv_heads * ((a.B + kDenseRows - 1) / kDenseRows) : 0;
   if (q_ctas + step_ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned ctas = (unsigned)(q_ctas + step_ctas);
   if (g.bits == 4)
-    dense_prologue_kernel<4><<<ctas, kHeadDim, kDenseSmem, stream>>>(g, a, (int)q_ctas);
+    dense_prologue_kernel<4><<<ctas, kDenseThreads, kDenseSmem, stream>>>(g, a, (int)q_ctas);
   else if (g.bits == 3)
-    dense_prologue_kernel<3><<<ctas, kHeadDim, kDenseSmem, stream>>>(g, a, (int)q_ctas);
+    dense_prologue_kernel<3><<<ctas, kDenseThreads, kDenseSmem, stream>>>(g, a, (int)q_ctas);
   else
-    dense_prologue_kernel<2><<<ctas, kHeadDim, kDenseSmem, stream>>>(g, a, (int)q_ctas);
+    dense_prologue_kernel<2><<<ctas, kDenseThreads, kDenseSmem, stream>>>(g, a, (int)q_ctas);
   return cudaGetLastError();
 }
 
