@@ -3,13 +3,13 @@
 // blocks -- then Lloyd-Max scalar codes, bit-packed into the paged cache; section "TurboQuant
 // KV Cache Compression" for the dense random rotation).
 //
-// Structured rotations (planar / iso): work item = one (token, kv head).  A warp takes items
-// in a grid-stride loop: lanes 0-15 encode the K vector and lanes 16-31 the V vector.  Lane j
-// of a half owns dimensions 8j..8j+7 -- four whole Givens pairs or two whole quaternion
-// blocks -- so the rotation is lane-local and only the squared norm is reduced (4
-// xor-shuffles within the half).  Each lane reads 16 bytes, and the next item's 16 bytes are
-// in flight while the current one is coded.  The kernel is bound by HBM: 512 bytes of fp16
-// in, 2 * (16 * bits + 2) bytes out per item.
+// Structured rotations (planar / iso): work item = one (token, kv head).  A half-warp takes
+// items in a grid-stride loop: its lanes 0-7 encode the K vector and lanes 8-15 the V vector,
+// lane l owning dimensions 16l..16l+15 -- eight whole Givens pairs or four whole quaternion
+// blocks -- so the rotation is lane-local and only the squared norm is reduced (xor-shuffles
+// within the eight lanes).  Each lane reads 32 bytes, the next item's loaded while the current
+// one is coded, and writes its share of the packed codes in one store.  Per item: 512 bytes of
+// fp16 in, 2 * (16 * bits + 2) bytes out.
 //
 // Dense rotation: Y = X R^T for a tile of 32 vectors of one (kv head, K or V) is a small GEMM
 // (32 x 128 x 128) on the tensor cores, two CTAs per SM so that one's GEMM overlaps the other's
@@ -33,7 +33,7 @@ namespace {
 using namespace codec;
 
 constexpr int kAppendThreads = 256;
-constexpr int kAppendWarps = kAppendThreads / 32;
+constexpr int kAppendCtasPerSm = 3;  // 85 registers a thread: a lane's 16 parameters, inputs and outputs
 
 // slot -> (page, offset): a shift and a mask for the usual power-of-two page sizes (decided once
 // per thread; the division is a longer instruction sequence), else a division.
@@ -59,68 +59,196 @@ struct PageSplit {
 // ---------------------------------------------------------------------------------------
 // Structured rotations
 // ---------------------------------------------------------------------------------------
-struct Item {
-  int t, h, slot;
-  uint4 raw;  // 8 fp16 of this lane's half (K or V)
-};
+// A half-warp takes one item (token t, kv head h) at a time: lanes 0-7 of the half code its K
+// vector and lanes 8-15 its V vector, lane l owning dims 16l .. 16l + 15 (eight Givens pairs or
+// four quaternion blocks, so the rotation stays lane-local).  Per vector: one 3-step shuffle
+// reduction of the squared norm, then each lane codes its 16 dims and writes its share of the
+// packed bytes as one store: 4-bit, the 8-byte unit of its 16-dim group (K: bytes 8l.., V: the
+// unit's token-pair slot); 2-bit, its 4-byte unit likewise; 3-bit, the low-bit word of half l & 1
+// of 32-dim group l >> 1, with the group's high-bit word W2 assembled from the two lanes of the
+// group by one shuffle and stored by the even lane.
 
-__device__ __forceinline__ void fetch(Item& it, int t, int h, const Geometry& g, const __half* src_k,
-                                      const __half* src_v, const int32_t* slots, int half, int j) {
-  it.t = t;
-  it.h = h;
-  it.slot = __ldg(slots + it.t);
-  const __half* src = (half ? src_v : src_k) + ((size_t)it.t * g.num_kv_heads + it.h) * kHeadDim + 8 * j;
-  it.raw = __ldg(reinterpret_cast<const uint4*>(src));
+// The 16 codes of a lane, from its rotated coordinates y and 1 / norm, as the words it stores:
+// 4-bit, w0 = dims 0-7 and w1 = dims 8-15 as nibbles; 2-bit, w0 = 16 two-bit fields; 3-bit,
+// w0 = the 16 low-bit fields and w1 = the lane's high bits at their W2 positions for half hh.
+// The code is the select-tree search of code_of, whose decisions are the code's bits (most
+// significant first); each decision is set straight into its packed position.
+template <int BITS>
+__device__ __forceinline__ void code16(const float (&y)[16], float rcp, const float (&b)[15], int hh,
+                                       uint32_t& w0, uint32_t& w1) {
+  w0 = 0u;
+  w1 = 0u;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float u = y[i] * rcp;
+    if constexpr (BITS == 4) {
+      const bool s3 = u > b[7];
+      const bool s2 = u > (s3 ? b[11] : b[3]);
+      const bool s1 = u > (s3 ? (s2 ? b[13] : b[9]) : (s2 ? b[5] : b[1]));
+      const float m0 = s3 ? (s2 ? (s1 ? b[14] : b[12]) : (s1 ? b[10] : b[8]))
+                          : (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
+      const bool s0 = u > m0;
+      uint32_t& w = i < 8 ? w0 : w1;
+      const int sh = 4 * (i & 7);
+      if (s0) w |= 1u << sh;
+      if (s1) w |= 2u << sh;
+      if (s2) w |= 4u << sh;
+      if (s3) w |= 8u << sh;
+    } else if constexpr (BITS == 2) {
+      const bool s1 = u > b[1];
+      const bool s0 = u > (s1 ? b[2] : b[0]);
+      if (s0) w0 |= 1u << (2 * i);
+      if (s1) w0 |= 2u << (2 * i);
+    } else {
+      // dim 16 hh + i with i = 4k + r: low bits at 2i of W_hh, high bit at 8k + 2hh + {4,5,0,1}[r]
+      const int k = i >> 2, r = i & 3;
+      const int pos = 8 * k + 2 * hh + (r < 2 ? 4 + r : r - 2);
+      const bool s2 = u > b[3];
+      const bool s1 = u > (s2 ? b[5] : b[1]);
+      const bool s0 = u > (s2 ? (s1 ? b[6] : b[4]) : (s1 ? b[2] : b[0]));
+      if (s0) w0 |= 1u << (2 * i);
+      if (s1) w0 |= 2u << (2 * i);
+      if (s2) w1 |= 1u << pos;
+    }
+  }
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kAppendThreads)
+__global__ void __launch_bounds__(kAppendThreads, kAppendCtasPerSm)
 append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict__ v,
               const int32_t* __restrict__ slots, int n, uint8_t* __restrict__ pages,
               int32_t* __restrict__ status) {
+  constexpr int vb = BITS * 16;
   float bnd[15];
   load_boundaries<BITS>(bnd, g.boundaries);
 
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;        // 0: K, 1: V
-  const int j = lane & 15;           // dims 8j..8j+7
-  const long long items = (long long)n * g.num_kv_heads;
-  const long long stride = (long long)gridDim.x * kAppendWarps;
-  const float* rot = half ? g.rot_v : g.rot_k;
+  const int kind = (lane >> 3) & 1;  // 0: K, 1: V
+  const int l = lane & 7;            // dims 16l .. 16l + 15
+  const int hkv = g.num_kv_heads;
+  const long long items = (long long)n * hkv;
+  const long long halves = (long long)gridDim.x * (kAppendThreads / 16);  // half-warps of the grid
+  const float* rot = kind ? g.rot_v : g.rot_k;
   const long long pool_slots = (long long)g.num_pages * g.page_size;
   const PageSplit split(g.page_size);
 
-  long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
-  if (item >= items) return;
-  // item = t * Hkv + h: divided once, then advanced by the stride without dividing (a 64-bit
-  // division is a long instruction sequence, comparable to coding the vectors)
-  const int hkv = g.num_kv_heads;
+  long long item = (long long)blockIdx.x * (kAppendThreads / 16) + (threadIdx.x >> 4);
+  // item = t * Hkv + h: divided once, then advanced by the stride without dividing; when the
+  // stride is a multiple of Hkv the half-warp's head never changes and its rotation parameters
+  // are loaded once
   int t = (int)(item / hkv), h = (int)(item % hkv);
-  const int stride_t = (int)(stride / hkv), stride_h = (int)(stride % hkv);
-  Item cur, nxt;
-  fetch(cur, t, h, g, k, v, slots, half, j);
-  for (; item < items; item += stride) {
+  const int stride_t = (int)(halves / hkv), stride_h = (int)(halves % hkv);
+  float pr[16];
+  auto load_params = [&](int hh) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 p4 = __ldg(reinterpret_cast<const float4*>(rot + (size_t)hh * kHeadDim + 16 * l + 4 * q));
+      pr[4 * q] = p4.x, pr[4 * q + 1] = p4.y, pr[4 * q + 2] = p4.z, pr[4 * q + 3] = p4.w;
+    }
+  };
+  load_params(h);
+  // every lane of the warp runs every iteration (shuffles): an item past the end stores nothing
+  const long long first = (long long)blockIdx.x * (kAppendThreads / 16) + (threadIdx.x & ~31) / 16;
+  const long long iters = first < items ? (items - first + halves - 1) / halves : 0;
+  // the item's slot and 32 bytes, loaded an iteration ahead
+  int slot_n = -1;
+  uint4 raw0_n = make_uint4(0u, 0u, 0u, 0u), raw1_n = raw0_n;
+  auto fetch = [&](long long itm, int tt, int hh) {
+    slot_n = -1;
+    if (itm < items) {
+      slot_n = __ldg(slots + tt);
+      const uint4* src = reinterpret_cast<const uint4*>((kind ? v : k) + ((size_t)tt * hkv + hh) * kHeadDim + 16 * l);
+      raw0_n = __ldg(src);
+      raw1_n = __ldg(src + 1);
+    }
+  };
+  fetch(item, t, h);
+  for (long long it = 0; it < iters; ++it, item += halves) {
+    const bool live = item < items;
+    const int slot = slot_n;
+    const uint4 raw0 = raw0_n, raw1 = raw1_n;
+    if (stride_h != 0 && it > 0 && live) load_params(h);
+    const int h_cur = h;
     t += stride_t;
     h += stride_h;
     if (h >= hkv) {
       h -= hkv;
       ++t;
     }
-    if (item + stride < items) fetch(nxt, t, h, g, k, v, slots, half, j);
+    fetch(item + halves, t, h);
 
-    const int slot = cur.slot;
     const bool bad = (long long)slot >= pool_slots;
-    if (bad && lane == 0 && status) atomicOr(status, RQ_STATUS_BAD_SLOT);
-    if (slot >= 0 && !bad) {  // uniform across the warp
-      const float4 p0 = __ldg(reinterpret_cast<const float4*>(rot + (size_t)cur.h * kHeadDim + 8 * j));
-      const float4 p1 = __ldg(reinterpret_cast<const float4*>(rot + (size_t)cur.h * kHeadDim + 8 * j + 4));
-      const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    if (bad && l == 0 && kind == 0 && status) atomicOr(status, RQ_STATUS_BAD_SLOT);
+    const bool store = live && slot >= 0 && !bad;
+    float x[16];
+    {
+      const uint32_t w[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+      }
+    }
+    // The squared norm in the order of the 16-lane codec (rq_codec.cuh, which the decode step's
+    // append uses): this lane's halves are that codec's lanes 2l and 2l + 1, whose butterfly
+    // pairs lanes 8, 4, 2 and then 1 apart -- here lanes 4, 2, 1 apart for each half, then the
+    // two halves -- so both write bitwise the same norm.
+    float sa = 0.f, sb = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sa += x[e] * x[e];
+      sb += x[8 + e] * x[8 + e];
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      sa += __shfl_xor_sync(0xffffffffu, sa, o);
+      sb += __shfl_xor_sync(0xffffffffu, sb, o);
+    }
+    const float nrm = __fsqrt_rn(sa + sb);
+    float y[16];
+    {
+      float y8[8], x8[8], p8[8];
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          x8[e] = x[8 * hv + e];
+          p8[e] = pr[8 * hv + e];
+        }
+        rotate8(y8, x8, p8, g.mode);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[8 * hv + e] = y8[e];
+      }
+    }
+    uint32_t w0, w1;
+    code16<BITS>(y, inv_norm(nrm), bnd, l & 1, w0, w1);
+    uint32_t w2 = 0u;
+    if constexpr (BITS == 3) w2 = w1 | __shfl_xor_sync(0xffffffffu, w1, 1);  // the group's high bits
+    if (store) {
       int page, off;
       split(slot, page, off);
-      uint8_t* chunk = pages + ((size_t)page * g.num_kv_heads + cur.h) * (size_t)g.page_bytes;
-      encode_structured<BITS>(cur.raw, pr, g.mode, bnd, chunk, g.page_size, half, off, j, true, status);
+      uint8_t* chunk = pages + ((size_t)page * hkv + h_cur) * (size_t)g.page_bytes;
+      uint8_t* dst = chunk + (size_t)kind * g.page_size * vb + (size_t)off * vb;
+      const int pair = off >> 1, hvt = off & 1;
+      if constexpr (BITS == 4) {
+        uint8_t* at = kind == 0 ? dst + 8 * l
+                                : chunk + (size_t)g.page_size * vb + pair * 128 + 16 * (l ^ ((2 * pair) & 7)) + 8 * hvt;
+        *reinterpret_cast<uint2*>(at) = make_uint2(w0, w1);
+      } else if constexpr (BITS == 2) {
+        uint8_t* at = kind == 0 ? dst + 4 * l
+                                : chunk + (size_t)g.page_size * vb + pair * 64 + 8 * (l ^ (4 * ((pair >> 1) & 1))) + 4 * hvt;
+        *reinterpret_cast<uint32_t*>(at) = w0;
+      } else {
+        *reinterpret_cast<uint32_t*>(dst + 12 * (l >> 1) + 4 * (l & 1)) = w0;
+        if ((l & 1) == 0) *reinterpret_cast<uint32_t*>(dst + 12 * (l >> 1) + 8) = w2;
+      }
+      if (l == 0) {
+        const __half n16 = __float2half_rn(nrm);
+        *reinterpret_cast<__half*>(chunk + (size_t)2 * g.page_size * vb + (size_t)kind * 2 * g.page_size + 2 * off) = n16;
+        if (status && __hisinf(n16)) atomicOr(status, RQ_STATUS_NORM_OVERFLOW);
+      }
     }
-    cur = nxt;
   }
 }
 
@@ -318,8 +446,8 @@ cudaError_t launch_append_bits(const Geometry& g, const __half* k, const __half*
     append_dense_kernel<BITS><<<ctas, kDenseThreads, kDenseSmem, stream>>>(g, k, v, slots, n, pages, status);
   } else {
     const long long items = (long long)n * g.num_kv_heads;
-    long long blocks = (items + kAppendWarps - 1) / kAppendWarps;
-    const long long max_blocks = (long long)sms * (2048 / kAppendThreads);
+    long long blocks = (items + kAppendThreads / 16 - 1) / (kAppendThreads / 16);  // an item per half-warp
+    const long long max_blocks = (long long)sms * kAppendCtasPerSm;
     if (blocks > max_blocks) blocks = max_blocks;
     append_kernel<BITS><<<(unsigned)blocks, kAppendThreads, 0, stream>>>(g, k, v, slots, n, pages, status);
   }
