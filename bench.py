@@ -4,8 +4,8 @@
 
 A step is one pass of the whole hot path over one batch: the quantize-append of the step's
 new tokens, then split-K decode (or chain-verify) attention over the packed cache with its
-log-sum-exp combine (done inside the split-K kernel for planar / iso rotations, by a second
-kernel that also applies R_v^T for a dense one).  A decode step that appends one token per
+log-sum-exp combine and inverse rotation done inside the split-K kernel (a dense rotation adds
+one launch before it that rotates the queries).  A decode step that appends one token per
 sequence (cfg1) runs as one rq_decode_step call: the append is folded into the split-K kernel.
 Inputs are synthetic and seeded (rotation_quantized_kv_rq_gb300.synth); the packed cache is
 built before timing and stays resident in HBM.
@@ -177,12 +177,12 @@ class Bench:
     def launches_per_step(self):
         dense = self.spec.mode == synth.DENSE
         if self.fused_step:  # split-K with the append folded in and the units finished in-kernel; a
-            return 3 if dense else 1  # dense rotation: the prologue (queries + tokens), split-K, combine
+            return 2 if dense else 1  # dense rotation: the prologue (queries + tokens), then split-K
         if self.extend:
             return 3 if dense else 2  # append, (dense: the query rotation,) extend attention
         n = 1 if self.k_new is not None else 0
-        # split-K; a dense rotation adds the query pre-rotation and the combine (R_v^T)
-        return n if self.prefill_only else n + 1 + 2 * (self.spec.mode == synth.DENSE)
+        # split-K (it finishes every unit, R_v^T included); a dense rotation adds the query rotation
+        return n if self.prefill_only else n + 1 + (self.spec.mode == synth.DENSE)
 
     def tokens_per_step(self):
         if self.prefill_only:

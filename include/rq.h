@@ -208,8 +208,8 @@ int rq_extend_attention(rq_ctx *ctx, const void *q, int T, const void *kv_pages,
  *   with seq_lens[b] = 0 appends nothing.
  * The result equals rq_quantize_append of the tokens followed by rq_decode_attention (the same
  * bytes written, the same output).  A dense rotation (RQ_DENSE) codes the new tokens in the
- * launch that rotates the queries, before the split-K kernel: three launches with the output
- * rotation, instead of four.  A page id out of range for the new token sets RQ_STATUS_BAD_PAGE
+ * launch that rotates the queries, before the split-K kernel (which applies the output
+ * rotation itself): two launches instead of four.  A page id out of range for the new token sets RQ_STATUS_BAD_PAGE
  * and skips its write.  Errors as rq_decode_attention, plus RQ_ERR_INVALID for a NULL or
  * non-16-byte-aligned k_new / v_new.
  */

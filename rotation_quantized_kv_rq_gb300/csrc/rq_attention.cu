@@ -26,7 +26,7 @@
 //     that stages a unit's last tile quantizes the token into the cache before it copies that
 //     tile, so the step needs no separate append launch.
 //   * Dense rotations (TurboQuant) change only the two ends: a small kernel forms R_k q for the
-//     whole call first, and the combine applies R_v^T per (sequence, kv head) group.
+//     whole call first, and the CTA that finishes a unit applies the full R_v^T to its rows.
 //   * P is moved from the S^T accumulator layout to the B-operand layout with movmatrix.
 //   * Scores are kept in base 2 (sm_scale * log2 e folded into q~).
 #include <cuda_fp16.h>
@@ -94,8 +94,10 @@ struct SmemPlan {
   uint32_t tail;       // shared address of the page-id array
   uint32_t merge_lo;   // shared address of merge half 0 (columns 0-3)
   uint32_t merge_hi;   // shared address of merge half 1 (columns 4-7)
+  uint32_t obuf;       // dense rotation: 8 normalised output rows [8][128] f32 before R_v^T
   uint32_t end;        // one past the last byte used
 };
+constexpr int kObufBytes = 8 * 128 * 4;
 
 // Rounds of one unit of a sequence of len tokens: ceil(tiles / kRoundTiles).
 template <int NT>
@@ -153,7 +155,8 @@ __host__ __device__ constexpr SmemPlan smem_plan(uint32_t base) {
   p.merge_hi = lo_merge ? p.hi : p.hi + merge_half;
   const uint32_t hi_need = lo_merge ? merge_half : 2 * merge_half;
   p.tail = p.hi + (hi_bytes > hi_need ? hi_bytes : hi_need);
-  p.end = p.tail + kTailBytes;
+  p.obuf = p.tail + kTailBytes;
+  p.end = p.obuf + kObufBytes;
   return p;
 }
 
@@ -745,6 +748,41 @@ __device__ __forceinline__ void append_token(const Geometry& g, const AttnArgs& 
   __syncwarp();
 }
 
+// Dense rotation: out = R_v^T o~ for nrows (<= 8) query rows row0 .. of kv head h of sequence b,
+// whose normalised o~ (already times out_scale / l) are in ob[r][128] (shared memory).  Every
+// thread of the CTA calls it: thread (rp, i) of 128-thread groups rp owns output dim i of rows
+// rp, rp + groups, ...; R_v is read from L2 (each entry once per group of 128 threads).
+template <int THREADS>
+__device__ __forceinline__ void dense_finish_rows(const Geometry& g, const AttnArgs& a, int b, int h, int row0,
+                                                  int nrows, const float (*ob)[kHeadDim]) {
+  constexpr int kGroups = THREADS / kHeadDim, kPer = 8 / kGroups;
+  const int i = threadIdx.x % kHeadDim, rp = threadIdx.x / kHeadDim;
+  float acc[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) acc[q] = 0.f;
+  const float* rv = g.rot_v + (size_t)h * kHeadDim * kHeadDim + i;  // R_v[m][i], row-major
+  // 32 independent loads in flight per round trip to L2 (the column is read once per thread)
+#pragma unroll 1
+  for (int m0 = 0; m0 < kHeadDim; m0 += 32) {
+    float w[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) w[e] = __ldg(rv + (size_t)(m0 + e) * kHeadDim);
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) acc[q] = fmaf(w[e], ob[rp + kGroups * q][m0 + e], acc[q]);
+  }
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int r = rp + kGroups * q;
+    if (r < nrows) {
+      const int row = row0 + r, j = row / g.group, head = h * g.group + row % g.group;
+      reinterpret_cast<__half*>(a.out)[(((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim + i] =
+          __float2half_rn(acc[q]);
+    }
+  }
+}
+
 // PRE: the queries were rotated before the launch (dense rotation).  STEP: a decode step that
 // quantizes each sequence's newest token first (a.k_new, a.v_new; structured rotations).
 // NT: query n-tiles per unit (Shape), each warp carrying all NT of them through every tile.
@@ -904,7 +942,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       else hi = mid;
     }
     if (threadIdx.x == 0) *walk = Walk{x0, x1, cum[lo], lo, a.B > 0 ? lens[lo] : 0};
-    if constexpr (!PRE) {  // a sequence without tokens has no fragments: its rows are zeros
+    {  // a sequence without tokens has no fragments: its rows are zeros
       for (int bb = blockIdx.x; bb < a.B; bb += gridDim.x) {
         if (cum[bb + 1] != cum[bb]) continue;
         const int n16 = a.T * g.num_q_heads * (kHeadDim / 8);
@@ -1233,11 +1271,12 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     // groups.  m and l go to the page-id array, free until the next fragment.  Fragment
     // partials of unit u sit at slots u + c for its CTAs c (8 NT rows each): slots never
     // collide, because both the units and the CTAs' ranges follow the same order.  A fragment
-    // that is its unit's whole range finishes the unit right here (structured rotations; a
-    // dense one always hands its partial to the combine kernel, which applies R_v^T).
+    // that is its unit's whole range finishes the unit right here (a dense rotation through
+    // the normalised rows staged in obuf and dense_finish_rows).
     const int unit = (it.b * g.num_kv_heads + it.h) * n_ug + it.nt0 / NT;
     const Frag f = frag_at<NT>(*walk);
-    const bool whole = !PRE && f.t0 == 0 && f.t1 == f.tb;  // uniform over the CTA
+    const bool whole = f.t0 == 0 && f.t1 == f.tb;  // uniform over the CTA
+    float (*const obuf)[kHeadDim] = reinterpret_cast<float (*)[kHeadDim]>(at(plan.obuf));
     float* dst = a.ws + (size_t)(unit + blockIdx.x) * (8 * NT) * kPartialStride;
     if (threadIdx.x == 0 && !whole) {
       if (f.t0 == 0) a.frag[2 * unit] = blockIdx.x;         // the unit's first CTA
@@ -1276,7 +1315,8 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         const int idx = idx0 + threadIdx.x;
         const int c = idx >> 6, gm = (idx >> 3) & 7, mm = idx & 7;
         // a whole unit's R_v entries, loaded while the partials are summed
-        const float4 rv = (whole && c < cols) ? rot_v_block(g, it.h, 16 * gm + 2 * mm) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 rv = (!PRE && whole && c < cols) ? rot_v_block(g, it.h, 16 * gm + 2 * mm)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
         if (c < cols) {  // c is uniform over each warp
           float M = -CUDART_INF_F;
 #pragma unroll 4
@@ -1295,7 +1335,11 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           }
           if (whole) {
             const float inv = (lsum > 0.f && len >= a.T) ? g.out_scale / lsum : 0.f;
-            store_pair(g, a, it.b, it.h, nt * 8 + c, 16 * gm + 2 * mm, acc0 * inv, acc1 * inv, rv);
+            if constexpr (PRE) {
+              *reinterpret_cast<float2*>(&obuf[c][16 * gm + 2 * mm]) = make_float2(acc0 * inv, acc1 * inv);
+            } else {
+              store_pair(g, a, it.b, it.h, nt * 8 + c, 16 * gm + 2 * mm, acc0 * inv, acc1 * inv, rv);
+            }
           } else {
             float* drow = dst + (i * 8 + c) * kPartialStride;
             *reinterpret_cast<float2*>(drow + 4 + 16 * gm + 2 * mm) = make_float2(acc0, acc1);
@@ -1306,8 +1350,12 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           }
         }
       }
+      if (PRE && whole) {  // uniform over the CTA
+        __syncthreads();
+        dense_finish_rows<kThreads>(g, a, it.b, it.h, nt * 8, cols, obuf);
+      }
     }
-    if (!PRE && !whole) {
+    if (!whole) {
       // Publish the partial and count the unit's finished rounds: the barrier orders every
       // thread's partial before thread 0's fence and add.  The CTA whose rounds complete the
       // unit merges all its partials once its own range is done (no CTA waits for another)
@@ -1332,26 +1380,38 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     __syncthreads();
   }
 
-  if constexpr (!PRE) {
-    // Finish the units this CTA completed: a warp per query row of the unit.
-    if (threadIdx.x == 0 && walk->n_fin > 0) __threadfence();  // after the adds that saw them done
-    __syncthreads();
-    for (int k = 0; k < walk->n_fin; ++k) {
-      const int unit = walk->fin[k];
-      const int ug = unit % n_ug, h = (unit / n_ug) % g.num_kv_heads, b = unit / (n_ug * g.num_kv_heads);
-      const int row0 = ug * 8 * NT, nrows = min(8 * NT, a.rows - row0);
+  // Finish the units this CTA completed: a warp per query row of the unit (a dense rotation:
+  // 8 rows at a time, staged in obuf for dense_finish_rows).
+  if (threadIdx.x == 0 && walk->n_fin > 0) __threadfence();  // after the adds that saw them done
+  __syncthreads();
+  for (int k = 0; k < walk->n_fin; ++k) {
+    const int unit = walk->fin[k];
+    const int ug = unit % n_ug, h = (unit / n_ug) % g.num_kv_heads, b = unit / (n_ug * g.num_kv_heads);
+    const int row0 = ug * 8 * NT, nrows = min(8 * NT, a.rows - row0);
+    if constexpr (PRE) {
+      float (*const obuf)[kHeadDim] = reinterpret_cast<float (*)[kHeadDim]>(at(plan.obuf));
+      for (int r0 = 0; r0 < nrows; r0 += 8) {  // uniform over the CTA
+        if (warp < min(8, nrows - r0)) {
+          const float4 v = merge_splits(g, a, b, h, row0 + r0 + warp, lane);
+          *reinterpret_cast<float4*>(&obuf[warp][4 * lane]) = v;
+        }
+        __syncthreads();
+        dense_finish_rows<kThreads>(g, a, b, h, row0 + r0, min(8, nrows - r0), obuf);
+        __syncthreads();
+      }
+    } else {
       const float4 rv = rot_v_block(g, h, 4 * lane);
-      for (int r = warp; r < nrows; r += kWarps) store_row(g, a, b, h, row0 + r, lane, merge_splits(g, a, b, h, row0 + r, lane), rv);
+      for (int r = warp; r < nrows; r += kWarps)
+        store_row(g, a, b, h, row0 + r, lane, merge_splits(g, a, b, h, row0 + r, lane), rv);
     }
   }
 }
 
 // ---------------------------------------------------------------------------------------
-// Dense rotation (TurboQuant): both ends of the call.  The query rows of one kv head -- over
-// every sequence and query token -- are numbered r = (b * T + j) * group + k; a CTA takes 16
-// consecutive rows of one head.  Thread i owns output dim i: per step of the sum it reads
-// four matrix entries (coalesced across threads, L2-resident) and the 16 rows' four inputs as
-// float4 broadcasts from shared memory, 64 FMAs per 20 loads.
+// Dense rotation (TurboQuant): the queries' end of the call.  The query rows of one kv head --
+// over every sequence and query token -- are numbered r = (b * T + j) * group + k, in groups of
+// 16.  Thread i owns output dim i: per step of the sum it reads four entries of the staged
+// matrix and the 16 rows' four inputs as float4 broadcasts from shared memory.
 // ---------------------------------------------------------------------------------------
 constexpr int kDenseRows = 16;
 
@@ -1500,34 +1560,6 @@ dense_prologue_kernel(const Geometry g, const AttnArgs a, int q_ctas) {
   }
 }
 
-// The log-sum-exp merge of merge_splits for the CTA's rows, then out = R_v^T o~.
-__global__ void __launch_bounds__(kHeadDim)
-attn_combine_dense_kernel(const Geometry g, const AttnArgs a) {
-  __shared__ __align__(16) float os[kDenseRows][kHeadDim];
-  extern __shared__ __align__(16) float wsm[];
-  const int h = blockIdx.x % g.num_kv_heads;
-  const int r0 = (blockIdx.x / g.num_kv_heads) * kDenseRows;
-  const int nr = min(kDenseRows, a.B * a.T * g.group - r0);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  stage_matrix(wsm, g.rot_v + (size_t)h * kHeadDim * kHeadDim);
-  for (int rr = warp; rr < kDenseRows; rr += kHeadDim / 32) {
-    float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (rr < nr) {  // uniform across the warp
-      const int r = r0 + rr, bj = r / g.group;
-      const int b = bj / a.T, j = bj % a.T;
-      res = merge_splits(g, a, b, h, j * g.group + r % g.group, lane);
-    }
-    *reinterpret_cast<float4*>(&os[rr][4 * lane]) = res;
-  }
-  __syncthreads();
-  float acc[kDenseRows];
-  dense_rows(acc, wsm, os, threadIdx.x);
-  __half* out = reinterpret_cast<__half*>(a.out);
-#pragma unroll
-  for (int r = 0; r < kDenseRows; ++r)
-    if (r < nr) out[dense_row_index(g, h, r0 + r) * kHeadDim + threadIdx.x] = __float2half_rn(acc[r]);
-}
-
 }  // namespace
 
 // Dynamic shared memory of a variant: its layout end for a window that starts right after the
@@ -1588,8 +1620,7 @@ cudaError_t attention_prepare() {
     e = cudaFuncSetAttribute(dense_prologue_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dense_prologue_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_combine_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+
   return e;
 }
 
@@ -1664,12 +1695,7 @@ cudaError_t launch_attention(const Geometry& g, const AttnArgs& a, cudaStream_t 
     if (e != cudaSuccess) return e;
     if (ev_end) cudaEventRecord(ev_end, stream);
   }
-  // planar / iso: the split-K kernel finishes every unit itself
-  if (dense) {
-    const long long rows_per_head = (long long)a.B * a.T * g.group;
-    const unsigned groups = (unsigned)(g.num_kv_heads * ((rows_per_head + kDenseRows - 1) / kDenseRows));
-    attn_combine_dense_kernel<<<groups, kHeadDim, kDenseSmem, stream>>>(g, a);
-  }
+  // the split-K kernel finishes every unit itself (normalise, R_v^T, store)
   return cudaGetLastError();
 }
 
