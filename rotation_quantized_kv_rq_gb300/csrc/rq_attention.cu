@@ -49,10 +49,16 @@ constexpr int kWaitLimit = 1 << 22;           // bounded mbarrier polling (about
 // operand P' = p * n_v cannot overflow.
 constexpr float kLazyMargin = 8.f;
 
-// Staged tiles.  A slot holds one 16-token tile exactly as a 16-token page chunk is laid out:
-// K codes [16][vb] | V codes [16][vb] | K norms fp16 [16] | V norms fp16 [16].  Each warp owns
-// kSlots slots used as kSlots/2 stages of two consecutive tiles (32 tokens); one mbarrier per
-// stage.  The slots sit on both sides of the 64 KB-aligned lookup table (see smem_plan).
+// Staged tiles.  Each warp owns kSlots slots of SB bytes used as kSlots/2 stages of two
+// consecutive tiles (32 tokens); one mbarrier per stage.  A stage holds its pair in one of two
+// layouts, fixed by the page size:
+//   * tile by tile (16-token pages, whose pair spans two pages, and pages of an odd number of
+//     tiles): each slot is one tile as a 16-token page chunk is laid out, K codes [16][vb] |
+//     V codes [16][vb] | K norms fp16 [16] | V norms fp16 [16];
+//   * section by section (an even number of tiles per page, so a pair lies in one page):
+//     K codes [32][vb] | V codes [32][vb] | K norms [32] | V norms [32], the four runs of the
+//     page that the pair covers, so the pair is four bulk copies.
+// The slots sit on both sides of the 64 KB-aligned lookup table (see smem_plan).
 template <int BITS>
 struct Ring {
   static constexpr int VB = BITS * 16;
@@ -203,8 +209,10 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t addr, uint32_t parity
   return ok;
 }
 // Polls an mbarrier phase at most kWaitLimit times; false if it never completed.
+// (try_wait itself suspends the thread for a while, so the first poll nearly always succeeds.)
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
-  for (int i = 0; i < kWaitLimit; ++i)
+  if (mbar_try_wait(addr, parity)) return true;
+  for (int i = 1; i < kWaitLimit; ++i)
     if (mbar_try_wait(addr, parity)) return true;
   return false;
 }
@@ -215,6 +223,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// True in one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t is_leader;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}" : "=r"(is_leader));
+  return is_leader != 0;
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
@@ -286,11 +300,10 @@ struct Raw<3> {
   uint32_t nk, nv;
 };
 
+// Tile data at: st its K code rows, vbp its V code rows, nkb / nvb its K / V norms.
 template <int BITS>
-__device__ __forceinline__ void load_stage(Raw<BITS>& r, const uint8_t* st, int g, int t) {
-  constexpr int vb = BITS * 16;
-  const uint8_t* vbp = st + 16 * vb;
-  const uint8_t* nb = st + 32 * vb;
+__device__ __forceinline__ void load_stage(Raw<BITS>& r, const uint8_t* st, const uint8_t* vbp, const uint8_t* nkb,
+                                           const uint8_t* nvb, int g, int t) {
   const int rk = rho<BITS>(g);
   if constexpr (BITS == 4) {
     r.k[0] = *reinterpret_cast<const uint4*>(st + rk * 64 + 16 * t);
@@ -328,9 +341,10 @@ __device__ __forceinline__ void load_stage(Raw<BITS>& r, const uint8_t* st, int 
       r.v[i][1] = *reinterpret_cast<const uint32_t*>(vbp + vt[i] * 48 + 12 * (g >> 1) + 8);
     }
   }
-  const uint16_t* n16 = reinterpret_cast<const uint16_t*>(nb);
-  r.nk = (uint32_t)n16[rk] | ((uint32_t)n16[rk + 8] << 16);
-  r.nv = (uint32_t)n16[16 + rk] | ((uint32_t)n16[16 + rk + 8] << 16);
+  const uint16_t* nk16 = reinterpret_cast<const uint16_t*>(nkb);
+  const uint16_t* nv16 = reinterpret_cast<const uint16_t*>(nvb);
+  r.nk = (uint32_t)nk16[rk] | ((uint32_t)nk16[rk + 8] << 16);
+  r.nv = (uint32_t)nv16[rk] | ((uint32_t)nv16[rk + 8] << 16);
 }
 
 // A operand of S^T = K~ q~^T for k-chunk kc: rows g / g+8 hold the two K rows, k-slots
@@ -837,10 +851,15 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   const uint32_t key2 = key1 + 128u;
   const int P = g.page_size;
   const int tiles_per_page = P / 16;
-  // tiles per page as a shift when it is a power of two (page sizes 16, 32, 64, 128, 256)
-  const int tpp_shift = (tiles_per_page & (tiles_per_page - 1)) == 0 ? __ffs(tiles_per_page) - 1 : -1;
-  const int n_issue = P == 16 ? 2 : 8;                 // lanes that issue a pair's bulk copies
-  const uint32_t issue_mask = P == 16 ? 0x3u : 0xFFu;
+  // Stage layout (see Ring): section by section when a pair always lies in one page.
+  const bool by_section = (tiles_per_page & 1) == 0;
+  // Offsets in a stage of tile A's (first) and tile B's K rows, V rows, K norms and V norms.
+  const uint32_t st_kB = by_section ? 16u * R::VB : (uint32_t)R::SB;
+  const uint32_t st_vA = by_section ? 32u * R::VB : 16u * R::VB;
+  const uint32_t st_vB = by_section ? 48u * R::VB : (uint32_t)R::SB + 16u * R::VB;
+  const uint32_t st_nA = by_section ? 64u * R::VB : 32u * R::VB;
+  const uint32_t st_nB = by_section ? 64u * R::VB + 32u : (uint32_t)R::SB + 32u * R::VB;
+  const uint32_t st_nv = by_section ? 64u : 32u;  // V norms after K norms
   // Shared address of this warp's stage st: slots 2st (first tile) and 2st + 1 (second tile,
   // SB bytes after the first: the slot plan keeps a warp's pairs of slots on one side of the table).
   const int sl0 = warp * kSlots;
@@ -1005,41 +1024,72 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     // all past pos_lim, are masked like positions past the sequence.
     const int pos_lim = tile1 * 16 - 1;
     const int n_w = (warp < n_pairs && !broken) ? (n_pairs - 1 - warp) / kWarps + 1 : 0;
-    // A page-sized tile (P = 16) is one bulk copy: lanes 0 and 1 stage tile `lane` of the warp's
-    // k-th pair into stage k % kStages.  A tile of a larger page is four copies (K codes, V codes
-    // and the two norm runs): lanes 0-3 copy the first tile's, 4-7 the second's, one each.
-    // Lane 0 announces the stage's bytes first.
+    // The warp's k-th pair is tiles tA = tA0 + 2 kWarps k and tA + 1 (if it exists); all lanes
+    // take part and one elected lane announces the stage's bytes and issues its bulk copies from
+    // warp-uniform addresses.  A 16-token page is one copy per tile; a pair inside one page
+    // (section by section) is four, one per run; other pairs are four per tile.  When the tiles
+    // per page divide 2 kWarps (every power-of-two page size) the pair's position in its page is
+    // the same for every k and its page-id entry moves by 2 kWarps / tiles_per_page per pair.
+    const int tA0 = tile0 + 2 * warp;
+    const bool cp_regular = (2 * kWarps) % tiles_per_page == 0;
+    const int cp_step = cp_regular ? 2 * kWarps / tiles_per_page : 0;
+    const int cp_pid0 = tA0 / tiles_per_page - p0;                  // page-id entry of pair 0
+    const int cp_off0 = (tA0 - (cp_pid0 + p0) * tiles_per_page) * 16;  // its first token in the page
+    // chunk (page, kv head) at page * Hkv * page_bytes + h * page_bytes: both products stay
+    // below 2^31 per page (checked at creation), so a 32 x 32 -> 64-bit multiply-add forms it
+    const uint32_t page_stride = (uint32_t)(g.num_kv_heads * g.page_bytes);
+    const uint8_t* const head_base = a.pages + (size_t)it.h * g.page_bytes;
+    auto chunk_of = [&](int pid) {  // the chunk of page-id entry pid (the same in every lane)
+      const uint32_t page = (uint32_t)__shfl_sync(0xffffffffu, page_ids[pid], 0);
+      return head_base + (uint64_t)page * page_stride;
+    };
     auto issue = [&](int k) {
       const int st = k % kStages;
-      const int tA = tile0 + 2 * (warp + k * kWarps);
-      const int nt_pair = tA + 1 < tile1 ? 2 : 1;
+      const int tA = tA0 + 2 * kWarps * k;
+      const bool two = tA + 1 < tile1;  // the pair's second tile exists
       const uint32_t mb = mbar_addr + 8 * st;
-      if (lane == 0) mbar_expect_tx(mb, nt_pair * R::SB);
-      __syncwarp(issue_mask);
-      // chunk (page, kv head) at page * Hkv * page_bytes + h * page_bytes: both products stay
-      // below 2^31 per page (checked at creation), so a 32 x 32 -> 64-bit multiply-add forms it
-      const uint32_t page_stride = (uint32_t)(g.num_kv_heads * g.page_bytes);
-      const uint32_t head_off = (uint32_t)(it.h * g.page_bytes);
-      const uint32_t sbase = stage_slot(st);
-      if (P == 16) {  // tile t is page t
-        if (lane < nt_pair) {
-          const uint32_t page = (uint32_t)page_ids[tA + lane - p0];
-          bulk_g2s(sbase + (lane ? (uint32_t)R::SB : 0u), a.pages + ((uint64_t)page * page_stride + head_off), R::SB,
-                   mb);
+      const uint32_t dst = stage_slot(st);
+      int pid = cp_pid0 + cp_step * k, off = cp_off0;
+      if (!cp_regular) {
+        const int pq = tA / tiles_per_page;
+        pid = pq - p0;
+        off = (tA - pq * tiles_per_page) * 16;
+      }
+      if (P == 16) {
+        const uint8_t* cA = chunk_of(pid);
+        const uint8_t* cB = chunk_of(two ? pid + 1 : pid);
+        if (elect_one()) {
+          mbar_expect_tx(mb, two ? 2 * R::SB : R::SB);
+          bulk_g2s(dst, cA, R::SB, mb);
+          if (two) bulk_g2s(dst + R::SB, cB, R::SB, mb);
         }
-      } else {
-        const int which = lane >> 2, sec = lane & 3;
-        if (which < nt_pair) {
-          const int tile = tA + which;
-          const int pq = tpp_shift >= 0 ? tile >> tpp_shift : tile / tiles_per_page;
-          const int off = (tile - pq * tiles_per_page) * 16;
-          const uint8_t* chunk = a.pages + ((uint64_t)(uint32_t)page_ids[pq - p0] * page_stride + head_off);
-          const uint32_t dst = sbase + (which ? (uint32_t)R::SB : 0u) +
-                               (sec == 0 ? 0u : sec == 1 ? 16u * R::VB : 32u * R::VB + (sec == 3 ? 32u : 0u));
-          const size_t src = sec == 0 ? (size_t)off * R::VB
-                           : sec == 1 ? (size_t)(P + off) * R::VB
-                                      : (size_t)2 * P * R::VB + (sec == 3 ? 2 * P : 0) + 2 * off;
-          bulk_g2s(dst, chunk + src, sec < 2 ? 16u * R::VB : 32u, mb);
+      } else if (by_section) {
+        const uint8_t* c = chunk_of(pid);
+        const uint32_t n = two ? 32u : 16u;
+        if (elect_one()) {
+          mbar_expect_tx(mb, two ? 2 * R::SB : R::SB);
+          bulk_g2s(dst, c + off * R::VB, n * R::VB, mb);
+          bulk_g2s(dst + 32u * R::VB, c + (P + off) * R::VB, n * R::VB, mb);
+          bulk_g2s(dst + 64u * R::VB, c + 2 * P * R::VB + 2 * off, 2 * n, mb);
+          bulk_g2s(dst + 64u * R::VB + 64u, c + 2 * P * R::VB + 2 * P + 2 * off, 2 * n, mb);
+        }
+      } else {  // an odd number of tiles per page: tile by tile, the second maybe in the next page
+        const bool next = off + 16 == P;  // tile A ends its page
+        const uint8_t* cA = chunk_of(pid);
+        const uint8_t* cB = chunk_of(two && next ? pid + 1 : pid);
+        const int offB = next ? 0 : off + 16;
+        if (elect_one()) {
+          mbar_expect_tx(mb, two ? 2 * R::SB : R::SB);
+#pragma unroll 1
+          for (int t = 0; t < (two ? 2 : 1); ++t) {
+            const uint8_t* c = t ? cB : cA;
+            const int o = t ? offB : off;
+            const uint32_t d = dst + (t ? (uint32_t)R::SB : 0u);
+            bulk_g2s(d, c + o * R::VB, 16u * R::VB, mb);
+            bulk_g2s(d + 16u * R::VB, c + (P + o) * R::VB, 16u * R::VB, mb);
+            bulk_g2s(d + 32u * R::VB, c + 2 * P * R::VB + 2 * o, 32u, mb);
+            bulk_g2s(d + 32u * R::VB + 32u, c + 2 * P * R::VB + 2 * P + 2 * o, 32u, mb);
+          }
         }
       }
     };
@@ -1048,7 +1098,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     // deferring the pair's copy when it is one of the first stages.
     const bool appends = STEP && tile1 == fr.tb && warp == (n_pairs - 1) % kWarps;
     const int n_first = min(kStages, n_w) - (appends && n_w <= kStages ? 1 : 0);
-    if (lane < n_issue && n_first > 0) {
+    if (n_first > 0) {
       fence_proxy_async();
       for (int k = 0; k < n_first; ++k) issue(k);
     }
@@ -1057,7 +1107,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     if constexpr (STEP) {
       if (appends) {
         append_token<BITS>(g, a, it.b, it.h, len);
-        if (n_w > 0 && n_w <= kStages && lane < n_issue) {
+        if (n_w > 0 && n_w <= kStages) {
           fence_proxy_async();
           issue(n_w - 1);
         }
@@ -1098,8 +1148,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       }
       phase ^= 1u << st;
       consumed = k + 1;
-      const uint8_t* stA = at(stage_slot(st));
-      const uint8_t* stB = stA + R::SB;
+      const uint8_t* const sp = at(stage_slot(st));
       const int pos0 = (tile0 + 2 * (warp + k * kWarps)) * 16;  // first token of the pair
 
       // ---- scores (base 2) of the lane's four K rows (two per tile) for columns 2tq, 2tq+1
@@ -1112,7 +1161,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       {
         Raw<BITS> rk;
         float s[NT][4];
-        load_stage<BITS>(rk, stA, gq, tq);
+        load_stage<BITS>(rk, sp, sp + st_vA, sp + st_nA, sp + st_nA + st_nv, gq, tq);
         qk_tile<BITS, NT>(s, rk, qf, key1, key2);
         nv_bits[0] = rk.nv;
         const float nk0 = half_bits_to_float(rk.nk & 0xffffu), nk1 = half_bits_to_float(rk.nk >> 16);
@@ -1123,7 +1172,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           sc[i][2] = s[i][2] * nk1;
           sc[i][3] = s[i][3] * nk1;
         }
-        load_stage<BITS>(rk, stB, gq, tq);
+        load_stage<BITS>(rk, sp + st_kB, sp + st_vB, sp + st_nB, sp + st_nB + st_nv, gq, tq);
         qk_tile<BITS, NT>(s, rk, qf, key1, key2);
         nv_bits[1] = rk.nv;
         const float nk2 = half_bits_to_float(rk.nk & 0xffffu), nk3 = half_bits_to_float(rk.nk >> 16);
@@ -1245,10 +1294,10 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       }
       // ---- values: read both tiles' V codes, hand the stage back, accumulate
       Raw<BITS> rvA, rvB;
-      load_stage<BITS>(rvA, stA, gq, tq);
-      load_stage<BITS>(rvB, stB, gq, tq);
+      load_stage<BITS>(rvA, sp, sp + st_vA, sp + st_nA, sp + st_nA + st_nv, gq, tq);
+      load_stage<BITS>(rvB, sp + st_kB, sp + st_vB, sp + st_nB, sp + st_nB + st_nv, gq, tq);
       __syncwarp();
-      if (k + kStages < n_w && lane < n_issue) {  // refill this stage while the pair is accumulated
+      if (k + kStages < n_w) {  // refill this stage while the pair is accumulated
         fence_proxy_async();
         issue(k + kStages);
       }
