@@ -990,7 +990,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     uint32_t qf[NT][8][2];
     int last_pos[NT][2];  // last position wholly visible to query columns 2tq, 2tq+1 of each n-tile
 
-    float m_run[NT][2], l_run[NT][2];
+    float m_run[NT][2], l_run[NT][2];  // m_run: -inf before the column's first visible score
     float o[NT][8][4];
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
@@ -1151,12 +1151,24 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       const uint8_t* const sp = at(stage_slot(st));
       const int pos0 = (tile0 + 2 * (warp + k * kWarps)) * 16;  // first token of the pair
 
-      // ---- scores (base 2) of the lane's four K rows (two per tile) for columns 2tq, 2tq+1
-      // of each n-tile.  The running max moves lazily: only when some score of the pair lies
-      // more than kLazyMargin above it (or the pair holds a value norm that could overflow the
-      // fp16 P' = p * n_v) does the warp reduce the pair's exact max and rescale; otherwise
-      // p = 2^(s - m_run) <= 2^kLazyMargin and nothing is reduced or rescaled.
-      float sc[NT][8];  // [n-tile][tile][row][col]: the scores, then p
+      // ---- shifted scores t = s - m_use (base 2) of the lane's four K rows (two per tile) for
+      // columns 2tq, 2tq+1 of each n-tile, one FMA each from the dot product and the key norm.
+      // The running max moves lazily: only when some t exceeds kLazyMargin (or the pair holds
+      // a value norm that could overflow the fp16 P' = p * n_v, or the column has no max yet)
+      // does the warp reduce the pair's exact max, rescale and re-shift; otherwise
+      // p = 2^t <= 2^kLazyMargin and nothing is reduced or rescaled.
+      // m_use: the max the exponents are taken against (m_run, or 0 while m_run is -inf); thr:
+      // the t above which the pair takes the exact path (kLazyMargin, or -inf before a max).
+      float m_use[NT][2], thr[NT][2];
+#pragma unroll
+      for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const bool none = m_run[i][c] == -CUDART_INF_F;
+          m_use[i][c] = none ? 0.f : m_run[i][c];
+          thr[i][c] = none ? -CUDART_INF_F : kLazyMargin;
+        }
+      float sc[NT][8];  // [n-tile][tile][row][col]: t, then p
       uint32_t nv_bits[2];
       {
         Raw<BITS> rk;
@@ -1167,10 +1179,10 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         const float nk0 = half_bits_to_float(rk.nk & 0xffffu), nk1 = half_bits_to_float(rk.nk >> 16);
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
-          sc[i][0] = s[i][0] * nk0;
-          sc[i][1] = s[i][1] * nk0;
-          sc[i][2] = s[i][2] * nk1;
-          sc[i][3] = s[i][3] * nk1;
+          sc[i][0] = fmaf(s[i][0], nk0, -m_use[i][0]);
+          sc[i][1] = fmaf(s[i][1], nk0, -m_use[i][1]);
+          sc[i][2] = fmaf(s[i][2], nk1, -m_use[i][0]);
+          sc[i][3] = fmaf(s[i][3], nk1, -m_use[i][1]);
         }
         load_stage<BITS>(rk, sp + st_kB, sp + st_vB, sp + st_nB, sp + st_nB + st_nv, gq, tq);
         qk_tile<BITS, NT>(s, rk, qf, key1, key2);
@@ -1178,10 +1190,10 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         const float nk2 = half_bits_to_float(rk.nk & 0xffffu), nk3 = half_bits_to_float(rk.nk >> 16);
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
-          sc[i][4] = s[i][0] * nk2;
-          sc[i][5] = s[i][1] * nk2;
-          sc[i][6] = s[i][2] * nk3;
-          sc[i][7] = s[i][3] * nk3;
+          sc[i][4] = fmaf(s[i][0], nk2, -m_use[i][0]);
+          sc[i][5] = fmaf(s[i][1], nk2, -m_use[i][1]);
+          sc[i][6] = fmaf(s[i][2], nk3, -m_use[i][0]);
+          sc[i][7] = fmaf(s[i][3], nk3, -m_use[i][1]);
         }
       }
       // Pairs wholly inside every column's visible range skip the per-element mask.
@@ -1215,27 +1227,20 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           }
         }
       }
-      // (with no max yet, m_run = -inf, any visible score passes the test: the exact path)
       float cmax[NT][2];
       bool grow = false;
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
         cmax[i][0] = fmaxf(fmaxf(sc[i][0], sc[i][2]), fmaxf(sc[i][4], sc[i][6]));
         cmax[i][1] = fmaxf(fmaxf(sc[i][1], sc[i][3]), fmaxf(sc[i][5], sc[i][7]));
-        grow = grow || cmax[i][0] > m_run[i][0] + kLazyMargin || cmax[i][1] > m_run[i][1] + kLazyMargin;
+        grow = grow || cmax[i][0] > thr[i][0] || cmax[i][1] > thr[i][1];
       }
-      // fp16 norms at or above 2^8 (bits >= 0x5C00) take the exact path, where p <= 1
-      const uint32_t nv_hi = max(max(nv_bits[0] & 0xffffu, nv_bits[0] >> 16), max(nv_bits[1] & 0xffffu, nv_bits[1] >> 16));
-      // (a column with no visible score yet keeps m_run = -inf: its masked scores must give
-      // p = 2^(-inf - 0) = 0, not 2^(-inf + inf))
-      float m_use[NT][2];
-#pragma unroll
-      for (int i = 0; i < NT; ++i) {
-        m_use[i][0] = m_run[i][0] == -CUDART_INF_F ? 0.f : m_run[i][0];
-        m_use[i][1] = m_run[i][1] == -CUDART_INF_F ? 0.f : m_run[i][1];
-      }
-      if (__any_sync(0xffffffffu, grow || nv_hi >= 0x5C00u)) {
-        float alpha[NT][2];
+      // fp16 norms at or above 2^8 (bits >= 0x5C00; norms are >= 0, so a half has no sign bit
+      // and adding 0x2400 to it carries into its bit 15 exactly then) take the exact path,
+      // where p <= 1
+      const bool nv_big = (((nv_bits[0] + 0x24002400u) | (nv_bits[1] + 0x24002400u)) & 0x80008000u) != 0u;
+      if (__any_sync(0xffffffffu, grow || nv_big)) {
+        float alpha[NT][2], shift[NT][2];
         bool moved = false;
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
@@ -1245,13 +1250,18 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-            const float m_new = fmaxf(m_run[i][c], tmax);
-            m_use[i][c] = m_new == -CUDART_INF_F ? 0.f : m_new;
-            alpha[i][c] = ex2(m_run[i][c] - m_use[i][c]);  // 0 when there was no max yet
+            // (a column with no visible score yet keeps m_run = -inf and m_use = 0: its masked
+            // scores must give p = 2^(-inf) = 0)
+            const float m_new = fmaxf(m_run[i][c], tmax + m_use[i][c]);
+            const float mu = m_new == -CUDART_INF_F ? 0.f : m_new;
+            alpha[i][c] = ex2(m_run[i][c] - mu);  // 0 when there was no max yet
+            shift[i][c] = m_use[i][c] - mu;
             l_run[i][c] *= alpha[i][c];
             m_run[i][c] = m_new;
             moved = moved || alpha[i][c] != 1.f;
           }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sc[i][e] += shift[i][e & 1];
         }
         if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
@@ -1269,14 +1279,11 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       uint32_t pb[2][NT][2];  // [tile][n-tile]
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
-        float ls[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // two short chains per column
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          sc[i][e] = ex2(sc[i][e] - m_use[i][e & 1]);  // now p; masked entries give 0
-          ls[e >> 2][e & 1] += sc[i][e];
+          sc[i][e] = ex2(sc[i][e]);  // now p; masked entries give 0
+          l_run[i][e & 1] += sc[i][e];
         }
-        l_run[i][0] += ls[0][0] + ls[1][0];
-        l_run[i][1] += ls[0][1] + ls[1][1];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float nva = half_bits_to_float(nv_bits[h] & 0xffffu), nvb = half_bits_to_float(nv_bits[h] >> 16);
