@@ -187,6 +187,16 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = A B with a zero accumulator (C given as constant zeros, so no register needs clearing).
+__device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
@@ -359,16 +369,20 @@ __device__ __forceinline__ void load_stage(Raw<BITS>& r, const uint8_t* st, cons
 template <int BITS, int NT>
 __device__ __forceinline__ void qk_tile(float (&s)[NT][4], const Raw<BITS>& r, const uint32_t (&qf)[NT][8][2],
                                         uint32_t key1, uint32_t key2) {
-#pragma unroll
-  for (int i = 0; i < NT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-  float s2[4] = {0.f, 0.f, 0.f, 0.f};
+  float s2[4];
+  // (the first MMA of each chain starts from zero: kc 0 and 1 with one n-tile, kc 0 with more)
   auto mma_all = [&](int kc, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
     if constexpr (NT == 1) {
-      if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[0][kc][0], qf[0][kc][1]);
+      if (kc == 0) mma16816_z(s[0], a0, a1, a2, a3, qf[0][kc][0], qf[0][kc][1]);
+      else if (kc == 1) mma16816_z(s2, a0, a1, a2, a3, qf[0][kc][0], qf[0][kc][1]);
+      else if (kc & 1) mma16816(s2, a0, a1, a2, a3, qf[0][kc][0], qf[0][kc][1]);
       else mma16816(s[0], a0, a1, a2, a3, qf[0][kc][0], qf[0][kc][1]);
     } else {
 #pragma unroll
-      for (int i = 0; i < NT; ++i) mma16816(s[i], a0, a1, a2, a3, qf[i][kc][0], qf[i][kc][1]);
+      for (int i = 0; i < NT; ++i) {
+        if (kc == 0) mma16816_z(s[i], a0, a1, a2, a3, qf[i][kc][0], qf[i][kc][1]);
+        else mma16816(s[i], a0, a1, a2, a3, qf[i][kc][0], qf[i][kc][1]);
+      }
     }
   };
   if constexpr (BITS == 4) {
