@@ -10,19 +10,22 @@
 // (sequence, kv head) -- rows r = j * group + k, in two blocks of 128 -- and walks the cache in
 // 64-token tiles up to the last position its rows can see, with warps specialised by role and
 // coupled only through mbarriers:
-//   dequant (4 warps): per tile, K~ (token-major, centroid, with the key norms beside it; two
-//     stages, a tile ahead) and V~^T (dim-major, centroid times value norm; one buffer) as fp16 in the
-//     K-major 128-byte-swizzled operand layout; code bytes index a lane-replicated table of
-//     centroid pairs (rq_lut.cuh), one shared load per two values; code words load ahead;
-//   MMA (one thread): S_b = Q~_b K~^T (tcgen05.mma, M 128 x N 64 x K 128) for both blocks into
-//     tensor memory one tile ahead, and O~_b += P_b V~ (M 128 x N 128 x K 64) when block b's
-//     P is ready, accumulated in tensor memory (all 512 columns: O~_0, O~_1 and two tiles'
-//     S_0, S_1);
+//   dequant (4 warps): per tile, K~ (token-major, centroid, with the key norms beside it) and
+//     V~^T (dim-major, centroid times value norm), two stages each, as fp16 in the K-major
+//     128-byte-swizzled operand layout; code bytes index a lane-replicated table of centroid
+//     pairs (rq_lut.cuh), one shared load per two values; code words load ahead;
+//   MMA (one thread): all operands of the row side live in tensor memory -- q~_b (A of S),
+//     S_b and, over S_b's first 32 columns once the softmax has read it, P_b (A of PV~) -- and
+//     the cache side comes from shared memory.  When block b's P(t) is ready it issues
+//     O~_b += P_b V~(t) (M 128 x N 128 x K 64) and right behind it S_b(t + 1) = q~_b K~(t + 1)^T
+//     (M 128 x N 64 x K 128): the tensor core runs one block's MMAs while the other block's
+//     softmax runs, and S_b reuses its columns only after the PV~ that read them (one thread's
+//     MMAs run in order);
 //   softmax (8 warps, one thread per row, block b = warps 4b .. 4b + 3): reads its row of S
 //     (tcgen05.ld), scales it by the key norms (f32), masks it, runs the online softmax in base
-//     2 with no cross-thread reduction
-//     and writes p as fp16; the running max moves only past a margin, so O~ is rarely
-//     rescaled; at the end it normalises, rotates back and stores its row.
+//     2 with no cross-thread reduction and writes p as fp16 over the row's S (tcgen05.st); the
+//     running max moves only past a margin, so O~ is rarely rescaled (S(t) complete means the
+//     PV~ before it is too); at the end it normalises, rotates back and stores its row.
 // Every wait is bounded: one that runs out sets RQ_STATUS_TIMEOUT and an abort flag every role
 // polls; the MMA thread drains what it issued before the tensor memory is freed.
 #include <cuda_fp16.h>
@@ -39,27 +42,28 @@ constexpr int kXSoftWarps = 8;   // warps 0-7: softmax, thread i = row i of the 
 constexpr int kXDeqWarps = 4;    // warps 8-11: dequantisation
 constexpr int kXThreads = 32 * (kXSoftWarps + kXDeqWarps + 1);  // + warp 12: MMA issue
 constexpr int kXSoftThreads = 32 * kXSoftWarps, kXDeqThreads = 32 * kXDeqWarps;
-constexpr int kXStages = 2;      // K~ ring (V~^T has one buffer: the shared-memory window)
+constexpr int kXStages = 2;      // K~ and V~^T rings
 constexpr int kXBlock = 128;    // rows per block: M of every MMA
 constexpr int kXRows = 2 * kXBlock;
 constexpr int kXTok = 64;       // tokens per K/V tile: N of S, K of PV~
 // Shared memory: the 64 KB code table at the first 64 KB-aligned address of the window, the
-// buffers (1024-aligned) below it where they fit, else above it.  MMA operands are K-major with
+// buffers (1024-aligned) below it where they fit, else above it.  The shared-memory MMA operands
+// (K~, V~^T) are K-major with
 // the 128-byte swizzle: 128-byte rows (64 fp16 of K), 16-byte chunk c of row r stored at chunk
 // c ^ (r % 8), 8-row groups 1024 bytes apart, a second 64-wide K atom after all rows of the first.
-constexpr uint32_t kXQBytes = 32768;   // q~ of a block: 128 rows x 128 dims, two atoms
 constexpr uint32_t kXKBytes = 16384;   // K~: 64 tokens x 128 dims, two atoms of 8 KB
 constexpr uint32_t kXVBytes = 16384;   // V~^T: 128 dims x 64 tokens
-constexpr uint32_t kXPBytes = 16384;   // P of a block: 128 rows x 64 tokens
 constexpr uint32_t kXMiscBytes = 1024; // centroids f32[16], the mbarriers, the tensor-memory
                                        // address, the abort flag; K norms f32[2][64] at 512
 constexpr int kXSmem = 232448;         // the whole opt-in window (one CTA per SM)
-constexpr uint32_t kXTmemCols = 512;   // O~_b at [128 b, 128 b + 128); S_b of tile t at 256 + 128 (t % 2) + 64 b
+constexpr uint32_t kXTmemCols = 512;   // O~_b at [128 b, 128 b + 128); q~_b (fp16 pairs) at
+constexpr uint32_t kXColQ = 256;       //   256 + 64 b; S_b at 384 + 64 b, P_b (fp16 pairs) over
+constexpr uint32_t kXColS = 384;       //   its first 32 columns
 constexpr int kXWaitLimit = 1 << 22;   // bounded mbarrier polling (about a second)
 constexpr float kLazyMax = 8.f;        // running-max slack of the online softmax (log2 units)
 
 struct XPlan {
-  uint32_t lut, q[2], k[2], v, p[2], misc, end;  // shared addresses
+  uint32_t lut, k[2], v[2], misc, end;  // shared addresses
 };
 __device__ __forceinline__ XPlan x_plan(uint32_t raw) {
   XPlan pl;
@@ -76,13 +80,10 @@ __device__ __forceinline__ XPlan x_plan(uint32_t raw) {
     }
     return at;
   };
-  pl.q[0] = place(kXQBytes);
-  pl.q[1] = place(kXQBytes);
   pl.k[0] = place(kXKBytes);
   pl.k[1] = place(kXKBytes);
-  pl.v = place(kXVBytes);
-  pl.p[0] = place(kXPBytes);
-  pl.p[1] = place(kXPBytes);
+  pl.v[0] = place(kXVBytes);
+  pl.v[1] = place(kXVBytes);
   pl.misc = place(kXMiscBytes);
   pl.end = hi;
   return pl;
@@ -92,11 +93,11 @@ __device__ __forceinline__ XPlan x_plan(uint32_t raw) {
 constexpr uint32_t kBarKFull = 64;     // [2] K~ stage filled (128 dequant threads)
 constexpr uint32_t kBarKEmpty = 80;    // [2] K~ stage read by S (MMA commit); its norms are read
                                        // once both blocks have released the tile's S (kBarSEmpty)
-constexpr uint32_t kBarVFull = 208;    // V~^T filled (128 dequant threads)
-constexpr uint32_t kBarVEmpty = 216;   // V~^T read by PV~ (MMA commit)
-constexpr uint32_t kBarSFull = 96;     // [block][2] S ready (MMA commit)
-constexpr uint32_t kBarSEmpty = 128;   // [block][2] S read (128 softmax threads of the block)
-constexpr uint32_t kBarPFull = 160;    // [block] P written, O~ rescaled (128 softmax threads)
+constexpr uint32_t kBarVFull = 224;    // [2] V~^T stage filled (128 dequant threads)
+constexpr uint32_t kBarVEmpty = 240;   // [2] V~^T stage read by PV~ (MMA commit)
+constexpr uint32_t kBarSFull = 96;     // [block] S ready (MMA commit)
+constexpr uint32_t kBarSEmpty = 128;   // [block][stage] S and the stage's key norms read (128 softmax threads)
+constexpr uint32_t kBarPFull = 160;    // [block] P written to tensor memory, O~ rescaled (128 softmax threads)
 constexpr uint32_t kBarODone = 176;    // [block] PV~ done (MMA commit)
 constexpr uint32_t kBarDrain = 192;    // everything the MMA thread issued is done
 constexpr uint32_t kTmemSlot = 200, kAbortFlag = 204, kKNorms = 512;
@@ -117,10 +118,15 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id, uint32_t accumulate) {
+// D (tensor memory) = A B (+ D if accumulate), kind::f16: A read from tensor memory at tmem_a (M
+// rows in lanes, K along columns, two fp16 per 32-bit column), B from the shared-memory
+// descriptor b.
+__device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t id,
+                                            uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(id), "r"(accumulate));
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+          tmem_d),
+      "r"(tmem_a), "l"(b), "r"(id), "r"(accumulate));
 }
 // The mbarrier completes once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t mbar) {
@@ -170,6 +176,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
       "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
       "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -366,14 +379,14 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       mbar_init(mb + kBarKEmpty + 8 * i, 1);
       mbar_init(mb + kBarPFull + 8 * i, kXBlock);
       mbar_init(mb + kBarODone + 8 * i, 1);
-      for (int j = 0; j < 2; ++j) {
-        mbar_init(mb + kBarSFull + 16 * i + 8 * j, 1);
-        mbar_init(mb + kBarSEmpty + 16 * i + 8 * j, kXBlock);
-      }
+      mbar_init(mb + kBarSFull + 8 * i, 1);
+      for (int j = 0; j < 2; ++j) mbar_init(mb + kBarSEmpty + 16 * i + 8 * j, kXBlock);
     }
     mbar_init(mb + kBarDrain, 1);
-    mbar_init(mb + kBarVFull, kXDeqThreads);
-    mbar_init(mb + kBarVEmpty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(mb + kBarVFull + 8 * i, kXDeqThreads);
+      mbar_init(mb + kBarVEmpty + 8 * i, 1);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -394,65 +407,78 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   const int brow = 32 * (warp & 3) + lane;            // softmax: row within the block (= lane of tensor memory)
   const int r = rb * kXRows + kXBlock * blk + brow;   // softmax: query row
 
-  // ---- q~ = R_k q * sm_scale * log2(e) of row r, fp16, into the A operand of its block ----
+  __syncthreads();  // the centroids are staged, the barriers initialised
+  lut::fill<BITS>(reinterpret_cast<uint32_t*>(at(pl.lut)), cb, tid, kXThreads);
+  const uint32_t key1 = lut::key(pl.lut, lane, 0), key2 = lut::key(pl.lut, lane, 1);
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();  // the code table and the tensor-memory address are in place
+  fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(at(mb + kTmemSlot));
+
+  // ---- q~ = R_k q * sm_scale * log2(e) of row r, fp16 pairs, into the A operand of its block
+  // (tensor memory: the thread's lane, columns kXColQ + 64 blk + k / 2 for the operand's K order) ----
   if (warp < kXSoftWarps) {
     const bool valid = r < a.rows;
     const int j = valid ? r / g.group : 0, head = h * g.group + (valid ? r % g.group : 0);
     const uint4* qrow = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(a.q) +
                                                        (((size_t)b * a.T + j) * g.num_q_heads + head) * kHeadDim);
     const float4* rk = reinterpret_cast<const float4*>(g.rot_k + (size_t)h * kHeadDim);
-    uint8_t* const qs = at(blk ? pl.q[1] : pl.q[0]);
     const float4* qrot = DENSE ? reinterpret_cast<const float4*>(a.q_rot + (((size_t)b * a.T + j) * g.num_q_heads + head) *
                                                                               kHeadDim)
                                : nullptr;
-#pragma unroll 4
-    for (int c = 0; c < 16; ++c) {  // dims 8c .. 8c + 7: two rotation blocks of 4
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-      if (DENSE && valid) {  // R_k q, formed before the launch
+    const uint32_t q_cols = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kXColQ + 64 * blk;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {  // dims 32 cc .. 32 cc + 31: 16 columns
+      uint32_t qw[16];
 #pragma unroll
-        for (int bk = 0; bk < 2; ++bk) {
-          const float4 yv = __ldg(qrot + 2 * c + bk);
-          const float y[4] = {yv.x, yv.y, yv.z, yv.w};
-          const int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;  // the K~ order of a 4-dim block
-          w[2 * bk] = pack_h2(y[0] * g.q_scale, y[s1] * g.q_scale);
-          w[2 * bk + 1] = pack_h2(y[s2] * g.q_scale, y[3] * g.q_scale);
-        }
-      } else if (valid) {
-        const uint4 raw8 = __ldg(qrow + c);
-        const uint32_t hw[4] = {raw8.x, raw8.y, raw8.z, raw8.w};
+      for (int c4 = 0; c4 < 4; ++c4) {  // dims 8c .. 8c + 7: two rotation blocks of 4
+        const int c = 4 * cc + c4;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (DENSE && valid) {  // R_k q, formed before the launch
 #pragma unroll
-        for (int bk = 0; bk < 2; ++bk) {
-          const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * bk]));
-          const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * bk + 1]));
-          const float4 p = __ldg(rk + 2 * c + bk);
-          float y[4];
-          if (g.mode == RQ_PLANAR) {
-            y[0] = p.x * x01.x - p.y * x01.y;
-            y[1] = p.y * x01.x + p.x * x01.y;
-            y[2] = p.z * x23.x - p.w * x23.y;
-            y[3] = p.w * x23.x + p.z * x23.y;
-          } else {  // Hamilton product (a,b,c,d) (x) x
-            y[0] = p.x * x01.x - p.y * x01.y - p.z * x23.x - p.w * x23.y;
-            y[1] = p.y * x01.x + p.x * x01.y - p.w * x23.x + p.z * x23.y;
-            y[2] = p.z * x01.x + p.w * x01.y + p.x * x23.x - p.y * x23.y;
-            y[3] = p.w * x01.x - p.z * x01.y + p.y * x23.x + p.x * x23.y;
+          for (int bk = 0; bk < 2; ++bk) {
+            const float4 yv = __ldg(qrot + 2 * c + bk);
+            const float y[4] = {yv.x, yv.y, yv.z, yv.w};
+            const int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;  // the K~ order of a 4-dim block
+            w[2 * bk] = pack_h2(y[0] * g.q_scale, y[s1] * g.q_scale);
+            w[2 * bk + 1] = pack_h2(y[s2] * g.q_scale, y[3] * g.q_scale);
           }
-          const int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;  // the K~ order of a 4-dim block
-          w[2 * bk] = pack_h2(y[0] * g.q_scale, y[s1] * g.q_scale);
-          w[2 * bk + 1] = pack_h2(y[s2] * g.q_scale, y[3] * g.q_scale);
+        } else if (valid) {
+          const uint4 raw8 = __ldg(qrow + c);
+          const uint32_t hw[4] = {raw8.x, raw8.y, raw8.z, raw8.w};
+#pragma unroll
+          for (int bk = 0; bk < 2; ++bk) {
+            const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * bk]));
+            const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * bk + 1]));
+            const float4 p = __ldg(rk + 2 * c + bk);
+            float y[4];
+            if (g.mode == RQ_PLANAR) {
+              y[0] = p.x * x01.x - p.y * x01.y;
+              y[1] = p.y * x01.x + p.x * x01.y;
+              y[2] = p.z * x23.x - p.w * x23.y;
+              y[3] = p.w * x23.x + p.z * x23.y;
+            } else {  // Hamilton product (a,b,c,d) (x) x
+              y[0] = p.x * x01.x - p.y * x01.y - p.z * x23.x - p.w * x23.y;
+              y[1] = p.y * x01.x + p.x * x01.y - p.w * x23.x + p.z * x23.y;
+              y[2] = p.z * x01.x + p.w * x01.y + p.x * x23.x - p.y * x23.y;
+              y[3] = p.w * x01.x - p.z * x01.y + p.y * x23.x + p.x * x23.y;
+            }
+            const int s1 = BITS == 2 ? 2 : 1, s2 = BITS == 2 ? 1 : 2;  // the K~ order of a 4-dim block
+            w[2 * bk] = pack_h2(y[0] * g.q_scale, y[s1] * g.q_scale);
+            w[2 * bk + 1] = pack_h2(y[s2] * g.q_scale, y[3] * g.q_scale);
+          }
         }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) qw[4 * c4 + jj] = w[jj];
       }
-      *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + xswz(brow, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+      tmem_st16u(q_cols + 16 * cc, qw);
     }
+    tmem_wait_st();
   }
-  __syncthreads();  // the centroids are staged, the barriers initialised
-  lut::fill<BITS>(reinterpret_cast<uint32_t*>(at(pl.lut)), cb, tid, kXThreads);
-  const uint32_t key1 = lut::key(pl.lut, lane, 0), key2 = lut::key(pl.lut, lane, 1);
-  fence_async_smem();
   fence_before_sync();
-  __syncthreads();  // q~, the code table and the tensor-memory address are in place
+  __syncthreads();  // q~ is in tensor memory
   fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(at(mb + kTmemSlot));
 
   float soft_inv = 0.f;   // dense: the row's 1 / l, for the epilogue after every role is done
   bool soft_ok = false;
@@ -465,14 +491,16 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     bool ok = true;
     for (int t = 0; t < n_tiles && ok; ++t) {
       const int t0 = t * kXTok, i = t & 1;
-      ok = __all_sync(0xffffffffu, role_wait(mb + kBarSFull + 16 * blk + 8 * i, (uint32_t)((t >> 1) & 1), abort_flag));
+      // S_b(t) complete: so is every MMA issued before it, PV~_b(t - 1) included
+      ok = __all_sync(0xffffffffu, role_wait(mb + kBarSFull + 8 * blk, (uint32_t)(t & 1), abort_flag));
       if (!ok) break;
       fence_after_sync();
+      const uint32_t s_cols = tmem + lane_off + kXColS + 64 * blk;
       float s[kXTok];
 #pragma unroll
       for (int c = 0; c < kXTok / 16; ++c) {
         float v[16];
-        tmem_ld16(tmem + lane_off + 256 + 128 * i + 64 * blk + 16 * c, v);
+        tmem_ld16(s_cols + 16 * c, v);
 #pragma unroll
         for (int k = 0; k < 16; ++k) s[16 * c + k] = v[k];
       }
@@ -489,7 +517,7 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         }
       }
       fence_before_sync();
-      mbar_arrive(mb + kBarSEmpty + 16 * blk + 8 * i);  // this S buffer and the tile's norms may be reused
+      mbar_arrive(mb + kBarSEmpty + 16 * blk + 8 * i);  // the tile's key norms may be reused
       if (!(t0 + kXTok - 1 <= qpos)) {  // mask what the row may not see
 #pragma unroll
         for (int jj = 0; jj < kXTok; ++jj)
@@ -520,17 +548,14 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         s[jj] = pr;
       }
       l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
-      if (t > 0) {  // PV~(t - 1) of this block done: P free, O~ stable
-        ok = __all_sync(0xffffffffu, role_wait(mb + kBarODone + 8 * blk, (uint32_t)((t - 1) & 1), abort_flag));
-        if (!ok) break;
-        fence_after_sync();
-      }
-      uint8_t* const ps = at(blk ? pl.p[1] : pl.p[0]);
+      // P_b(t) as fp16 pairs over the first 32 columns of S_b (already read)
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(ps + xswz(brow, c)) =
-            make_uint4(pack_h2(s[8 * c], s[8 * c + 1]), pack_h2(s[8 * c + 2], s[8 * c + 3]),
-                       pack_h2(s[8 * c + 4], s[8 * c + 5]), pack_h2(s[8 * c + 6], s[8 * c + 7]));
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pw[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) pw[k] = pack_h2(s[32 * c + 2 * k], s[32 * c + 2 * k + 1]);
+        tmem_st16u(s_cols + 16 * c, pw);
+      }
       if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // O~ *= alpha (the warp's rows)
 #pragma unroll 1
         for (int c = 0; c < kHeadDim / 16; ++c) {
@@ -541,9 +566,8 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           for (int k = 0; k < 16; ++k) v[k] *= alpha;
           tmem_st16(tmem_o + 16 * c, v);
         }
-        tmem_wait_st();
       }
-      fence_async_smem();
+      tmem_wait_st();
       fence_before_sync();
       mbar_arrive(mb + kBarPFull + 8 * blk);
     }
@@ -605,8 +629,8 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     // K~: thread (token dt % 64, code groups dt / 64 and dt / 64 + 2) -> 4 chunks of a row each.
     // V~^T: warp dw takes dims 32 dw .. 32 dw + 31 (code group dw), lane p the token pair
     // (2p, 2p + 1), one half2 per dim row -- a warp writes 128 consecutive bytes a row.
-    // Order: K(0); then per tile t: K(t + 1) (stage free once S(t - 1) is done), V(t) (buffer
-    // free once PV~(t - 1) is done) -- so S never waits for a PV~.
+    // Order: K(0); then per tile t: K(t + 1) (stage free once S(t - 1) is done), V(t) (stage
+    // free once PV~(t - 2) is done).
     const int dt = tid - kXSoftThreads, dw = dt >> 5;
     const int ktok = dt & 63, kg0 = dt >> 6;
     GroupRaw k0, k1, va, vb;
@@ -642,12 +666,14 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       mbar_arrive(mb + kBarKFull + 8 * st);
       return true;
     };
-    auto produce_v = [&](int t) -> bool {  // V~(t)^T = n_v * centroid
-      if (t >= 1 && !__all_sync(0xffffffffu, role_wait(mb + kBarVEmpty, (uint32_t)((t - 1) & 1), abort_flag)))
+    auto produce_v = [&](int t) -> bool {  // V~(t)^T = n_v * centroid into stage t % 2
+      const int st = t % kXStages;
+      if (t >= kXStages &&  // PV~(t - 2) has read the stage
+          !__all_sync(0xffffffffu, role_wait(mb + kBarVEmpty + 8 * st, (uint32_t)((t / kXStages - 1) & 1), abort_flag)))
         return false;
       const uint32_t nbits = (va.norm & 0xFFFFu) | (vb.norm << 16);
       const __half2 n2 = *reinterpret_cast<const __half2*>(&nbits);
-      uint8_t* const vt = at(pl.v);
+      uint8_t* const vt = at(st ? pl.v[1] : pl.v[0]);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pv[16];
@@ -661,7 +687,7 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       }
       if (t + 1 < n_tiles) load_v((t + 1) * kXTok);
       fence_async_smem();
-      mbar_arrive(mb + kBarVFull);
+      mbar_arrive(mb + kBarVFull + 8 * st);
       return true;
     };
     bool ok = true;
@@ -680,43 +706,45 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     const uint32_t id_s = idesc_f16(kXBlock, kXTok), id_o = idesc_f16(kXBlock, kHeadDim);
     bool ok = true;
     int issued = 0;
-    auto issue_s = [&](int t) -> bool {  // S_b(t) = q~_b K~(t)^T into S columns of tile parity t % 2
-      const int st = t % kXStages, i = t & 1;
-      if (!role_wait(mb + kBarKFull + 8 * st, (uint32_t)((t / kXStages) & 1), abort_flag)) return false;
-      const uint32_t kb = st ? pl.k[1] : pl.k[0];
-#pragma unroll 1
-      for (int bb = 0; bb < 2; ++bb) {
-        if (t >= 2 && !role_wait(mb + kBarSEmpty + 16 * bb + 8 * i, (uint32_t)(((t >> 1) - 1) & 1), abort_flag))
-          return false;
-        fence_after_sync();
-        const uint32_t qb = bb ? pl.q[1] : pl.q[0];
+    // S_b(t) = q~_b K~(t)^T: A from tensor memory (q~_b), B the K~ stage at kb; into S_b's columns
+    auto s_mmas = [&](int bb, uint32_t kb) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_f16(tmem + 256 + 128 * i + 64 * bb, sdesc(qb + (ks >> 2) * 16384 + (ks & 3) * 32),
-                   sdesc(kb + (ks >> 2) * 8192 + (ks & 3) * 32), id_s, ks > 0);
-        umma_commit(mb + kBarSFull + 16 * bb + 8 * i);
-        ++issued;
-      }
-      umma_commit(mb + kBarKEmpty + 8 * st);  // the stage's K~ has been read
-      return true;
+      for (int ks = 0; ks < 8; ++ks)
+        umma_f16_ts(tmem + kXColS + 64 * bb, tmem + kXColQ + 64 * bb + 8 * ks,
+                    sdesc(kb + (ks >> 2) * 8192 + (ks & 3) * 32), id_s, ks > 0);
+      umma_commit(mb + kBarSFull + 8 * bb);
+      ++issued;
     };
-    if (n_tiles > 0) ok = issue_s(0);
+    auto wait_k = [&](int t) {
+      return role_wait(mb + kBarKFull + 8 * (t % kXStages), (uint32_t)((t / kXStages) & 1), abort_flag);
+    };
+    if (n_tiles > 0 && (ok = wait_k(0))) {
+      fence_after_sync();
+      s_mmas(0, pl.k[0]);
+      s_mmas(1, pl.k[0]);
+      umma_commit(mb + kBarKEmpty);  // stage 0's K~ has been read
+    }
     for (int t = 0; t < n_tiles && ok; ++t) {
-      if (t + 1 < n_tiles && !(ok = issue_s(t + 1))) break;  // S(t + 1) runs under softmax(t)
-      if (!(ok = role_wait(mb + kBarVFull, (uint32_t)(t & 1), abort_flag))) break;
-      const uint32_t vb = pl.v;
+      const int vs = t % kXStages, ks1 = (t + 1) % kXStages;
+      const bool next = t + 1 < n_tiles;
+      if (!(ok = role_wait(mb + kBarVFull + 8 * vs, (uint32_t)((t / kXStages) & 1), abort_flag))) break;
+      if (next && !(ok = wait_k(t + 1))) break;
+      const uint32_t vb = vs ? pl.v[1] : pl.v[0], kb = ks1 ? pl.k[1] : pl.k[0];
 #pragma unroll 1
       for (int bb = 0; bb < 2; ++bb) {
         if (!(ok = role_wait(mb + kBarPFull + 8 * bb, (uint32_t)(t & 1), abort_flag))) break;
         fence_after_sync();
-        const uint32_t pb = bb ? pl.p[1] : pl.p[0];
+        // O~_b += P_b(t) V~(t), P_b from the first 32 columns of S_b
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_f16(tmem + 128 * bb, sdesc(pb + ks * 32), sdesc(vb + ks * 32), id_o, t > 0 || ks > 0);
+          umma_f16_ts(tmem + 128 * bb, tmem + kXColS + 64 * bb + 8 * ks, sdesc(vb + ks * 32), id_o, t > 0 || ks > 0);
         umma_commit(mb + kBarODone + 8 * bb);
         ++issued;
+        if (next) s_mmas(bb, kb);  // S_b(t + 1) over the same columns, behind the PV~ that reads them
       }
-      if (ok) umma_commit(mb + kBarVEmpty);  // V~^T has been read
+      if (!ok) break;
+      umma_commit(mb + kBarVEmpty + 8 * vs);                 // the V~^T stage has been read
+      if (next) umma_commit(mb + kBarKEmpty + 8 * ks1);      // and the next tile's K~ stage
     }
     if (issued > 0) {  // drain: nothing may be running when the tensor memory is freed
       umma_commit(mb + kBarDrain);
