@@ -39,8 +39,8 @@ namespace rq {
 namespace {
 
 constexpr int kXSoftWarps = 8;   // warps 0-7: softmax, thread i = row i of the CTA's 256
-constexpr int kXDeqWarps = 4;    // warps 8-11: dequantisation
-constexpr int kXThreads = 32 * (kXSoftWarps + kXDeqWarps + 1);  // + warp 12: MMA issue
+constexpr int kXDeqWarps = 4;    // warps 8-11: K~ dequantisation, warps 12-15: V~^T dequantisation
+constexpr int kXThreads = 32 * (kXSoftWarps + 2 * kXDeqWarps + 1);  // + warp 16: MMA issue
 constexpr int kXSoftThreads = 32 * kXSoftWarps, kXDeqThreads = 32 * kXDeqWarps;
 constexpr int kXStages = 2;      // K~ and V~^T rings
 constexpr int kXBlock = 128;    // rows per block: M of every MMA
@@ -624,14 +624,15 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       }
     }
     if (!ok && lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
-  } else if (warp < kXSoftWarps + kXDeqWarps) {
-    // ================= dequantisation: K~ a tile ahead of V~^T =================
-    // K~: thread (token dt % 64, code groups dt / 64 and dt / 64 + 2) -> 4 chunks of a row each.
-    // V~^T: warp dw takes dims 32 dw .. 32 dw + 31 (code group dw), lane p the token pair
-    // (2p, 2p + 1), one half2 per dim row -- a warp writes 128 consecutive bytes a row.
-    // Order: K(0); then per tile t: K(t + 1) (stage free once S(t - 1) is done), V(t) (stage
-    // free once PV~(t - 2) is done).
-    const int dt = tid - kXSoftThreads, dw = dt >> 5;
+  } else if (warp < kXSoftWarps + 2 * kXDeqWarps) {
+    // ================= dequantisation: K~ (warps 8-11) and V~^T (warps 12-15) =================
+    // K~: thread (token dt % 64, code groups dt / 64 and dt / 64 + 2) -> 4 chunks of a row each;
+    // a stage is free once S(t - 2) is done.  V~^T: warp dw takes dims 32 dw .. 32 dw + 31 (code
+    // group dw), lane p the token pair (2p, 2p + 1), one half2 per dim row -- a warp writes 128
+    // consecutive bytes a row; a stage is free once PV~(t - 2) is done.  The two run
+    // independently, each loading its next tile's code words while it works on this one.
+    const bool k_role = warp < kXSoftWarps + kXDeqWarps;
+    const int dt = tid - kXSoftThreads - (k_role ? 0 : kXDeqThreads), dw = dt >> 5;
     const int ktok = dt & 63, kg0 = dt >> 6;
     GroupRaw k0, k1, va, vb;
     auto load_k = [&](int t0) {
@@ -691,14 +692,12 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       return true;
     };
     bool ok = true;
-    if (n_tiles > 0) {
-      load_k(0);
-      load_v(0);
-      ok = produce_k(0);
-    }
-    for (int t = 0; t < n_tiles && ok; ++t) {
-      if (t + 1 < n_tiles && !(ok = produce_k(t + 1))) break;
-      ok = produce_v(t);
+    if (k_role) {
+      if (n_tiles > 0) load_k(0);
+      for (int t = 0; t < n_tiles && ok; ++t) ok = produce_k(t);
+    } else {
+      if (n_tiles > 0) load_v(0);
+      for (int t = 0; t < n_tiles && ok; ++t) ok = produce_v(t);
     }
     if (!ok && lane == 0 && a.status) atomicOr(a.status, RQ_STATUS_TIMEOUT);
   } else if (lane == 0) {
