@@ -11,19 +11,18 @@
 // one is coded, and writes its share of the packed codes in one store.  Per item: 512 bytes of
 // fp16 in, 2 * (16 * bits + 2) bytes out.
 //
-// Dense rotation: Y = X R^T for a tile of 32 vectors of one (kv head, K or V) is a small GEMM
-// (32 x 128 x 128) on the tensor cores, two CTAs per SM so that one's GEMM overlaps the other's
-// coding.  X is fp16 and exact as an operand; R (fp32) is split
-// as R = hi + lo with hi = fp16(R), lo = fp16(R - hi), both multiplied into one fp32
-// accumulator.  That carries R to ~6e-8 per entry, but the tensor cores' fp32 accumulation is
-// not correctly rounded, so a coordinate whose u lies within kFixBand of a boundary is
-// recomputed exactly -- a compensated fp32 dot product (error-free products and sums) against
-// the fp32 R, shared by the vector's half-warp -- before it is coded.  Codes then differ from
-// the fp64 definition only as rarely as the structured kernel's.  The coding epilogue is the
-// one the structured kernel uses, on Y staged in shared memory.
+// Dense rotation: Y = X R^T for a tile of 128 vectors of one (kv head, K or V) is a GEMM
+// (128 x 128 x 128) on the 5th-generation tensor cores (tcgen05, f32 accumulators in tensor
+// memory).  X is fp16 and exact as an operand; R (fp32) is split as R = hi + lo with
+// hi = fp16(R), lo = fp16(R - hi), both multiplied into one fp32 accumulator.  That carries R to
+// ~6e-8 per entry, but the tensor cores' fp32 accumulation is not correctly rounded, so a
+// coordinate whose u lies within kFixBand of a boundary is recomputed exactly -- a compensated
+// fp32 dot product (error-free products and sums) against the fp32 R -- before it is coded.
+// Codes then differ from the fp64 definition only as rarely as the structured kernel's.
 #include <cuda_fp16.h>
 
 #include "rq_codec.cuh"
+#include "rq_tc.cuh"
 #include "rq_internal.h"
 #include "../../include/rq.h"
 
@@ -253,197 +252,334 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
 }
 
 // ---------------------------------------------------------------------------------------
-// Dense rotation (tensor cores)
+// Dense rotation on the 5th-generation tensor cores (tcgen05).  A CTA (one per SM) takes
+// 128-vector tiles of one (K or V, kv head), whose R_hi, R_lo it stages once:
+//   * 2 loader warps stage X (fp16, 128 x 128) with cp.async into a two-buffer ring, in the
+//     K-major 128-byte-swizzled operand layout;
+//   * one thread issues Y = X R_hi^T + X R_lo^T (M 128 x N 128 x K 128, f32 accumulate) into
+//     tensor memory, two tiles' Y in 256 columns;
+//   * 8 coding warps: thread (row, half) reads 64 coordinates of its vector's Y from tensor
+//     memory (the lane is the row), forms the norm from X (the partial sums of squares of the
+//     16 eight-dim chunks combined in the half-warp codec's order, so the fp16 norm is the
+//     decode step's bit for bit), codes, and writes its half of the packed vector.  A
+//     coordinate whose u lies within kFixBand of a boundary is recomputed exactly by its whole
+//     warp (a compensated fp32 dot product against R's fp32 row, 4 terms a lane) and re-coded.
 // ---------------------------------------------------------------------------------------
-// Two CTAs per SM, so that one CTA's GEMM overlaps the other's coding (each CTA alternates the
-// two with barriers in between).
-constexpr int kDenseRows = 32;                 // vectors per tile
-constexpr int kDenseThreads = 256;             // 8 warps: 2 row tiles x 4 column quarters
-constexpr int kDenseWarps = kDenseThreads / 32;
-constexpr int kDenseCtasPerSm = 2;
-constexpr int kYStride = 136;                  // floats per staged Y row (conflict-free float2 stores)
-constexpr int kSmemR = 0;                      // fp16 [2 (hi, lo)][128][128], 16-byte chunks swizzled
-constexpr int kSmemX = kSmemR + 2 * 128 * 128 * 2;            // fp16 [2 buffers][32][128], swizzled
-constexpr int kSmemY = kSmemX + 2 * kDenseRows * 128 * 2;     // fp32 [32][136]
-constexpr int kDenseSmem = kSmemY + kDenseRows * kYStride * 4;  // 99,328 bytes; the fp32 R of the
-                                                                // exact recompute is read from L2
+namespace dtc {
+constexpr int kRows = 128;                        // vectors per tile: M of the MMA
+constexpr int kCodeWarps = 8;                     // warps 0-7: coding
+constexpr int kLoadWarps = 2;                     // warps 8-9: X loads
+constexpr int kThreads = 32 * (kCodeWarps + kLoadWarps + 1);  // + warp 10: MMA issue
+constexpr int kCodeThreads = 32 * kCodeWarps, kLoadThreads = 32 * kLoadWarps;
+constexpr uint32_t kR = 0;                        // R_hi, R_lo: fp16 [2][2 atoms of 16 KB]
+constexpr uint32_t kX = 65536;                    // X: fp16 [2 buffers][2 atoms of 16 KB]
+constexpr uint32_t kSS = kX + 65536;              // partial sums of squares: f32 [2][128][16]
+constexpr uint32_t kBar = kSS + 2 * kRows * 16 * 4;
+constexpr uint32_t kBarXFull = 0, kBarXEmpty = 16, kBarYFull = 32, kBarYEmpty = 48, kBarDrain = 64;
+constexpr uint32_t kTmemSlot = 72, kAbort = 76;
+constexpr int kSmem = (int)kBar + 128 + 1024;     // + slack to align the window to 1024 bytes
+constexpr uint32_t kTmemCols = 256;
+}  // namespace dtc
 
-// A 256-byte row of 16 chunks (8 fp16 each) stores chunk c at position c ^ (row mod 8), so the
-// eight rows one ldmatrix phase reads fall in eight different 16-byte bank groups.
-__device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(row * 256 + ((chunk ^ (row & 7)) << 4)); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+__device__ __forceinline__ void cp_async16_tc(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// Tile t covers tokens kDenseRows * blk .. + kDenseRows - 1 of kv head hk % Hkv, K (hk < Hkv) or V, with
-// hk = t % (2 Hkv) and blk = t / (2 Hkv).  Rows past n are zero-filled.
-__device__ __forceinline__ void issue_x(uint32_t xs, int hk, long long blk, const Geometry& g, const __half* k,
-                                       const __half* v, int n, uint8_t* xs_generic) {
-  const int hkv = g.num_kv_heads;
-  const int kind = hk >= hkv, h = kind ? hk - hkv : hk;
-  const __half* src = kind ? v : k;
-  for (int i = threadIdx.x; i < kDenseRows * 16; i += kDenseThreads) {
-    const int r = i >> 4, c = i & 15;
-    const long long t = blk * kDenseRows + r;
-    if (t < n) {
-      cp_async16(xs + swz(r, c), src + ((size_t)t * hkv + h) * kHeadDim + 8 * c);
-    } else {
-      *reinterpret_cast<uint4*>(xs_generic + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
-    }
+// y_i = sum_m x_m R[i][m], exactly enough to be correctly rounded in all but pathological
+// cases (error-free products and sums, errors carried in a second word), by a whole warp: lane
+// l takes dims 4l .. 4l + 3 of x (fp16, row `xrow` of a staged X tile) and of R's fp32 row.
+__device__ __forceinline__ float dot_compensated_warp(const uint8_t* xatoms, int xrow, const float* rrow, int lane) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(xatoms + (lane >> 4) * 16384 + tc::sw128(xrow, (lane >> 1) & 7) +
+                                                    8 * (lane & 1));
+  const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+  const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+  const float x[4] = {x01.x, x01.y, x23.x, x23.y};
+  const float4 r4 = __ldg(reinterpret_cast<const float4*>(rrow + 4 * lane));
+  const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
+  float s = 0.f, c = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float p = x[e] * rr[e];
+    const float pe = fmaf(x[e], rr[e], -p);  // x * r = p + pe exactly
+    const float t = s + p;
+    const float z = t - s;
+    c += ((s - (t - z)) + (p - z)) + pe;     // s + p = t + (that) exactly
+    s = t;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+    const float t = s + s2;
+    const float z = t - s;
+    c += c2 + ((s - (t - z)) + (s2 - z));
+    s = t;
+  }
+  return s + c;
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kDenseThreads, kDenseCtasPerSm)
-append_dense_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict__ v,
-                    const int32_t* __restrict__ slots, int n, uint8_t* __restrict__ pages,
-                    int32_t* __restrict__ status) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem);
-  float* Ys = reinterpret_cast<float*>(smem + kSmemY);
-  float bnd[15];
-  load_boundaries<BITS>(bnd, g.boundaries);
-
-  const int hkv = g.num_kv_heads;
-  const long long nblk = ((long long)n + kDenseRows - 1) / kDenseRows;
-  const long long tiles = 2LL * hkv * nblk;
-  const long long pool_slots = (long long)g.num_pages * g.page_size;
-  const PageSplit split(g.page_size);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-  const int mt = warp & 1, nq = warp >> 1;  // rows 16mt.., columns 32nq..
-  const int half = lane >> 4, j = lane & 15;
-
-  long long tile = blockIdx.x;
-  if (tile >= tiles) return;
-  // (hk, blk) of the tile, advanced by the grid stride without dividing
-  const int h2 = 2 * hkv;
-  int hk = (int)(tile % h2);
-  long long blk = tile / h2;
-  const int stride_hk = (int)(gridDim.x % h2);
-  const long long stride_blk = gridDim.x / h2;
-  auto advance = [&](int& a, long long& b) {
-    a += stride_hk;
-    b += stride_blk;
-    if (a >= h2) {
-      a -= h2;
-      ++b;
+__global__ void __launch_bounds__(dtc::kThreads, 1)
+append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict__ v,
+                       const int32_t* __restrict__ slots, int n, uint8_t* __restrict__ pages,
+                       int32_t* __restrict__ status) {
+  using namespace dtc;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const sm = smem_raw + (base - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hkv = g.num_kv_heads, npairs = 2 * hkv;
+  const int cpp = (int)gridDim.x / npairs;  // CTAs per (K or V, head): the launch makes it >= 1
+  const int pair = (int)blockIdx.x / cpp, sub = (int)blockIdx.x % cpp;
+  const int nblk = (n + kRows - 1) / kRows;
+  const int my_tiles = (pair < npairs && sub < nblk) ? (nblk - 1 - sub) / cpp + 1 : 0;
+  if (my_tiles == 0) return;  // uniform over the CTA, before any barrier or allocation
+  const int kind = pair >= hkv, h = kind ? pair - hkv : pair;
+  const __half* const src = kind ? v : k;
+  const float* const r32 = g.dense32 + ((size_t)kind * hkv + h) * 128 * 128;  // fp32 R rows (exact recompute)
+  const uint32_t mb = base + kBar;
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sm + kBar + kAbort);
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(mb + kBarXFull + 8 * i, kLoadThreads);
+      tc::mbar_init(mb + kBarXEmpty + 8 * i, kCodeThreads);
+      tc::mbar_init(mb + kBarYFull + 8 * i, 1);
+      tc::mbar_init(mb + kBarYEmpty + 8 * i, kCodeThreads);
     }
-  };
-  int buf = 0, cur_hk = -1;
-  issue_x(base + kSmemX, hk, blk, g, k, v, n, smem + kSmemX);
-  cp_async_commit();
-  for (; tile < tiles; tile += gridDim.x) {
-    const int kind = hk >= hkv, h = kind ? hk - hkv : hk;
-    const float* r32 = g.dense32 + ((size_t)kind * hkv + h) * 128 * 128;  // fp32 R rows (exact recompute)
-    if (hk != cur_hk) {  // stage R of this (K or V, head); the previous tile is done with it
-      const uint4* src = reinterpret_cast<const uint4*>(g.dense16 + ((size_t)kind * hkv + h) * 2 * 128 * 128);
-      for (int i = threadIdx.x; i < 2 * 128 * 16; i += kDenseThreads) {
-        const int hl = i >> 11, row = (i >> 4) & 127, c = i & 15;
-        *reinterpret_cast<uint4*>(smem + kSmemR + hl * 32768 + swz(row, c)) = __ldg(src + i);
-      }
-      cur_hk = hk;
+    tc::mbar_init(mb + kBarDrain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kCodeWarps + kLoadWarps) tc::tmem_alloc(mb + kTmemSlot, kTmemCols);  // whole warp
+  {  // R_hi, R_lo ([2][128][128] row-major fp16) in the K-major swizzled layout, rows = output dims
+    const uint4* rsrc = reinterpret_cast<const uint4*>(g.dense16 + ((size_t)kind * hkv + h) * 2 * 128 * 128);
+    for (int i = tid; i < 2 * 128 * 16; i += kThreads) {
+      const int hl = i >> 11, row = (i >> 4) & 127, c = i & 15;
+      *reinterpret_cast<uint4*>(sm + kR + hl * 32768 + (c >> 3) * 16384 + tc::sw128(row, c & 7)) = __ldg(rsrc + i);
     }
-    const long long next = tile + gridDim.x;
-    int hk_next = hk;
-    long long blk_next = blk;
-    advance(hk_next, blk_next);
-    const uint32_t xs_next = base + kSmemX + (uint32_t)((buf ^ 1) * kDenseRows * 256);
-    if (next < tiles) issue_x(xs_next, hk_next, blk_next, g, k, v, n, smem + kSmemX + (buf ^ 1) * kDenseRows * 256);
-    cp_async_commit();
-    cp_async_wait1();
-    __syncthreads();  // this tile's X (and R, if restaged) visible to every warp
+  }
+  tc::fence_async_smem();  // read by the tensor core (async proxy)
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kBar + kTmemSlot);
 
-    const uint32_t xs = base + kSmemX + (uint32_t)(buf * kDenseRows * 256);
-    float acc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-#pragma unroll 2
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t a[4];
-      // matrices: rows 0-7 / 8-15 of the row tile, k chunks 2ks / 2ks+1 -> a0, a1, a2, a3
-      ldsm_x4(a, xs + swz(16 * mt + (lane & 15), 2 * ks + (lane >> 4)));
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const int nrow = 8 * (4 * nq + 2 * np + (lane >> 4)) + (lane & 7);
-        const int kc = 2 * ks + ((lane >> 3) & 1);
-#pragma unroll
-        for (int hl = 0; hl < 2; ++hl) {
-          uint32_t b[4];  // b0, b1 of n-tile 2np, then of 2np + 1
-          ldsm_x4(b, base + kSmemR + hl * 32768 + swz(nrow, kc));
-          mma16816(acc[2 * np], a, b[0], b[1]);
-          mma16816(acc[2 * np + 1], a, b[2], b[3]);
-        }
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = 32 * nq + 8 * nt + 2 * tq;
-      *reinterpret_cast<float2*>(Ys + (16 * mt + gq) * kYStride + col) = make_float2(acc[nt][0], acc[nt][1]);
-      *reinterpret_cast<float2*>(Ys + (16 * mt + gq + 8) * kYStride + col) = make_float2(acc[nt][2], acc[nt][3]);
-    }
-    __syncthreads();
-
-    // Coding: a half-warp per vector, lane j on dims 8j..8j+7 (2 kDenseWarps vectors per pass).
-    const uint8_t* xg = smem + kSmemX + buf * kDenseRows * 256;
-#pragma unroll 1
-    for (int pass = 0; pass < kDenseRows / (2 * kDenseWarps); ++pass) {
-      const int r = 2 * kDenseWarps * pass + 2 * warp + half;
-      const long long t = blk * kDenseRows + r;
+  if (warp < kCodeWarps) {
+    // ================= coding: thread = (row, half of the dims) =================
+    const int row = 32 * (warp & 3) + lane, ch = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    float bnd[15];
+    load_boundaries<BITS>(bnd, g.boundaries);
+    const PageSplit split(g.page_size);
+    const long long pool_slots = (long long)g.num_pages * g.page_size;
+    constexpr int vb = BITS * 16;
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int b = i & 1;
+      const long long t = (long long)(sub + i * cpp) * kRows + row;
       int slot = t < n ? __ldg(slots + t) : -1;
       const bool bad = (long long)slot >= pool_slots;
-      if (bad && j == 0 && status) atomicOr(status, RQ_STATUS_BAD_SLOT);
+      if (bad && ch == 0 && status) atomicOr(status, RQ_STATUS_BAD_SLOT);
       const bool store = slot >= 0 && !bad;
       if (!store) slot = 0;
-      const uint4 raw = *reinterpret_cast<const uint4*>(xg + swz(r, j));
-      float y[8];
-      {
-        const float4 y0 = *reinterpret_cast<const float4*>(Ys + r * kYStride + 8 * j);
-        const float4 y1 = *reinterpret_cast<const float4*>(Ys + r * kYStride + 8 * j + 4);
-        y[0] = y0.x, y[1] = y0.y, y[2] = y0.z, y[3] = y0.w, y[4] = y1.x, y[5] = y1.y, y[6] = y1.z, y[7] = y1.w;
+      ok = tc::role_wait(mb + kBarXFull + 8 * b, (uint32_t)((i >> 1) & 1), abort_flag) &&
+           tc::role_wait(mb + kBarYFull + 8 * b, (uint32_t)((i >> 1) & 1), abort_flag);
+      {  // agree across the coding warps (they meet at a named barrier below)
+        uint32_t all_ok;
+        asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+                     : "=r"(all_ok)
+                     : "r"((uint32_t)ok), "n"(kCodeThreads)
+                     : "memory");
+        ok = all_ok != 0;
       }
-      int code[8];
-      float nrm;
-      dense_codes<BITS>(code, nrm, raw, y, bnd, r32, store, lane);
-      int page, off;
+      if (!ok) break;
+      tc::fence_after_sync();
+      const uint8_t* const xatoms = sm + kX + b * 32768;
+      // the norm: partial sums of squares of the 8-dim chunks (each in order), combined as the
+      // half-warp codec's butterfly (xor 8, 4, 2, 1) combines its lanes' sums
+      float* const ss = reinterpret_cast<float*>(sm + kSS) + (b * kRows + row) * 16;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 w4 = *reinterpret_cast<const uint4*>(xatoms + ch * 16384 + tc::sw128(row, cc));
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          x[2 * e] = f.x;
+          x[2 * e + 1] = f.y;
+        }
+        float ps = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ps += x[e] * x[e];
+        ss[8 * ch + cc] = ps;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kCodeThreads) : "memory");  // both halves' sums are in
+      float a8[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) a8[jj] = ss[jj] + ss[jj + 8];
+      const float b0 = a8[0] + a8[4], b1 = a8[1] + a8[5], b2 = a8[2] + a8[6], b3 = a8[3] + a8[7];
+      const float nrm = __fsqrt_rn((b0 + b2) + (b1 + b3));
+      const float rcp = inv_norm(nrm);
+
+      int page = 0, off = 0;
       split(slot, page, off);
-      uint8_t* chunk = pages + ((size_t)page * hkv + h) * (size_t)g.page_bytes;
-      pack_store<BITS>(code, nrm, chunk, g.page_size, kind, off, j, store, status);
+      uint8_t* const chunk = pages + ((size_t)page * hkv + h) * (size_t)g.page_bytes;
+      uint8_t* const dst = chunk + (size_t)kind * g.page_size * vb + (size_t)off * vb;
+      uint8_t* const vsec = chunk + (size_t)g.page_size * vb;
+      const int vpair = off >> 1, hv = off & 1;
+      uint32_t w2 = 0u;  // 3-bit: the high bits of the current 32-dim group
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {  // coordinates 64 ch + 16 q .. + 15
+        float y[16];
+        tc::tmem_ld16(tmem + lane_off + 128 * b + 64 * ch + 16 * q, y);
+        tc::tmem_wait_ld();
+        int code[16];
+        uint32_t todo = 0;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float dm;
+          code[e] = code_of_margin<BITS>(y[e] * rcp, bnd, dm);
+          if (dm < kFixBand && store) todo |= 1u << e;
+        }
+        while (__any_sync(0xffffffffu, todo != 0)) {  // exact recompute, one coordinate at a time
+          const uint32_t want = __ballot_sync(0xffffffffu, todo != 0);
+          const int leader = __ffs(want) - 1;
+          const int e_lead = __shfl_sync(0xffffffffu, todo ? __ffs(todo) - 1 : 0, leader);
+          const float yi = dot_compensated_warp(xatoms, 32 * (warp & 3) + leader, r32 + (64 * ch + 16 * q + e_lead) * 128,
+                                                lane);
+          if (lane == leader) {
+            const int c = code_of<BITS>(yi * rcp, bnd);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (e == e_lead) code[e] = c;
+            todo &= ~(1u << e_lead);
+          }
+        }
+        if (store) {
+          const int u = 4 * ch + q;  // 16-dim unit of the vector
+          if constexpr (BITS == 4) {
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              lo |= (uint32_t)code[e] << (4 * e);
+              hi |= (uint32_t)code[8 + e] << (4 * e);
+            }
+            uint8_t* at = kind == 0 ? dst + 8 * u : vsec + vpair * 128 + 16 * (u ^ ((2 * vpair) & 7)) + 8 * hv;
+            *reinterpret_cast<uint2*>(at) = make_uint2(lo, hi);
+          } else if constexpr (BITS == 2) {
+            uint32_t wd = 0;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) wd |= (uint32_t)code[e] << (2 * e);
+            uint8_t* at = kind == 0 ? dst + 4 * u : vsec + vpair * 64 + 8 * (u ^ (4 * ((vpair >> 1) & 1))) + 4 * hv;
+            *reinterpret_cast<uint32_t*>(at) = wd;
+          } else {
+            // group grp = u / 2, half hq = u % 2: the low bits are word hq of the group, the high
+            // bits of dim i = 16 hq + 4 kk + r go to bit 8 kk + 2 hq + {4, 5, 0, 1}[r] of W2
+            const int grp = u >> 1, hq = u & 1;
+            uint32_t lo = 0;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              lo |= (uint32_t)(code[e] & 3) << (2 * e);
+              const int kk = e >> 2, r = e & 3;
+              w2 |= (uint32_t)(code[e] >> 2) << (8 * kk + 2 * hq + (r < 2 ? 4 + r : r - 2));
+            }
+            *reinterpret_cast<uint32_t*>(dst + 12 * grp + 4 * hq) = lo;
+            if (hq == 1) {
+              *reinterpret_cast<uint32_t*>(dst + 12 * grp + 8) = w2;
+              w2 = 0u;
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(mb + kBarYEmpty + 8 * b);  // this tile's Y has been read
+      tc::mbar_arrive(mb + kBarXEmpty + 8 * b);  // and its X (norms, recomputes)
+      if (store && ch == 0) {
+        const __half n16 = __float2half_rn(nrm);
+        *reinterpret_cast<__half*>(chunk + (size_t)2 * g.page_size * vb + (size_t)kind * 2 * g.page_size + 2 * off) = n16;
+        if (status && __hisinf(n16)) atomicOr(status, RQ_STATUS_NORM_OVERFLOW);
+      }
     }
-    __syncthreads();  // X buffer and Y free for the next tile
-    buf ^= 1;
-    hk = hk_next;
-    blk = blk_next;
+    if (!ok && lane == 0 && status) atomicOr(status, RQ_STATUS_TIMEOUT);
+  } else if (warp < kCodeWarps + kLoadWarps) {
+    // ================= X loads: tile i into buffer i % 2 =================
+    const int lt = tid - kCodeThreads;
+    auto issue = [&](int i) {
+      const uint32_t xb = base + kX + (uint32_t)(i & 1) * 32768;
+      const long long t0 = (long long)(sub + i * cpp) * kRows;
+      for (int q = lt; q < kRows * 16; q += kLoadThreads) {
+        const int r = q >> 4, c = q & 15;
+        const long long t = t0 + r;
+        const uint32_t d = xb + (c >> 3) * 16384 + tc::sw128(r, c & 7);
+        if (t < n)
+          cp_async16_tc(d, src + ((size_t)t * hkv + h) * kHeadDim + 8 * c);
+        else
+          *reinterpret_cast<uint4*>(sm + (d - base)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    bool ok = true;
+    issue(0);
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");  // tile i has landed
+      tc::fence_async_smem();
+      tc::mbar_arrive(mb + kBarXFull + 8 * (i & 1));
+      if (i + 1 < my_tiles) {  // the next tile, once tile i - 1 has left its buffer
+        if (i >= 1)
+          ok = __all_sync(0xffffffffu, tc::role_wait(mb + kBarXEmpty + 8 * ((i + 1) & 1), (uint32_t)(((i - 1) >> 1) & 1),
+                                                     abort_flag));
+        if (ok) issue(i + 1);
+      }
+    }
+    if (!ok && lane == 0 && status) atomicOr(status, RQ_STATUS_TIMEOUT);
+  } else if (lane == 0) {
+    // ================= MMA issue (one thread) =================
+    const uint32_t id = tc::idesc_f16(kRows, 128);
+    bool ok = true;
+    int issued = 0;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int b = i & 1;
+      ok = tc::role_wait(mb + kBarXFull + 8 * b, (uint32_t)((i >> 1) & 1), abort_flag) &&
+           (i < 2 || tc::role_wait(mb + kBarYEmpty + 8 * b, (uint32_t)(((i >> 1) - 1) & 1), abort_flag));
+      if (!ok) break;
+      tc::fence_after_sync();
+      const uint32_t xb = base + kX + (uint32_t)b * 32768;
+#pragma unroll
+      for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc::umma_f16_ss(tmem + 128 * b, tc::sdesc(xb + (ks >> 2) * 16384 + (ks & 3) * 32),
+                          tc::sdesc(base + kR + hl * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32), id, hl > 0 || ks > 0);
+      tc::umma_commit(mb + kBarYFull + 8 * b);
+      ++issued;
+    }
+    if (issued > 0) {  // drain: nothing may be running when the tensor memory is freed
+      tc::umma_commit(mb + kBarDrain);
+      for (int i = 0; i < tc::kWaitLimit; ++i)
+        if (tc::mbar_test(mb + kBarDrain, 0u)) break;
+    }
+    if (!ok && status) atomicOr(status, RQ_STATUS_TIMEOUT);
   }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kCodeWarps + kLoadWarps) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int BITS>
 cudaError_t launch_append_bits(const Geometry& g, const __half* k, const __half* v, const int32_t* slots, int n,
                                uint8_t* pages, int32_t* status, cudaStream_t stream, int sms) {
   if (g.mode == RQ_DENSE) {
-    const long long tiles = 2LL * g.num_kv_heads * ((n + kDenseRows - 1) / kDenseRows);
-    // whole multiples of the 2 Hkv (K/V, head) groups, so a CTA keeps one R staged
-    const int resident = kDenseCtasPerSm * sms;
-    int ctas = resident >= 2 * g.num_kv_heads ? resident / (2 * g.num_kv_heads) * (2 * g.num_kv_heads) : resident;
-    if (tiles < ctas) ctas = (int)tiles;
-    append_dense_kernel<BITS><<<ctas, kDenseThreads, kDenseSmem, stream>>>(g, k, v, slots, n, pages, status);
+    // CTAs per (K or V, head): the SMs shared out, at most the head's tiles, at least one
+    const int npairs = 2 * g.num_kv_heads;
+    const long long nblk = ((long long)n + dtc::kRows - 1) / dtc::kRows;
+    long long cpp = sms / npairs;
+    if (cpp > nblk) cpp = nblk;
+    if (cpp < 1) cpp = 1;
+    if ((long long)npairs * cpp > 0x7fffffffLL) return cudaErrorInvalidValue;
+    append_dense_tc_kernel<BITS><<<(unsigned)(npairs * cpp), dtc::kThreads, dtc::kSmem, stream>>>(g, k, v, slots, n, pages,
+                                                                                                 status);
   } else {
     const long long items = (long long)n * g.num_kv_heads;
     long long blocks = (items + kAppendThreads / 16 - 1) / (kAppendThreads / 16);  // an item per half-warp
@@ -457,11 +593,11 @@ cudaError_t launch_append_bits(const Geometry& g, const __half* k, const __half*
 }  // namespace
 
 cudaError_t append_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(append_dense_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+  cudaError_t e = cudaFuncSetAttribute(append_dense_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, dtc::kSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(append_dense_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+    e = cudaFuncSetAttribute(append_dense_tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, dtc::kSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(append_dense_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDenseSmem);
+    e = cudaFuncSetAttribute(append_dense_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, dtc::kSmem);
   return e;
 }
 
