@@ -258,18 +258,20 @@ append_kernel(Geometry g, const __half* __restrict__ k, const __half* __restrict
 //     K-major 128-byte-swizzled operand layout;
 //   * one thread issues Y = X R_hi^T + X R_lo^T (M 128 x N 128 x K 128, f32 accumulate) into
 //     tensor memory, two tiles' Y in 256 columns;
-//   * 8 coding warps: thread (row, half) reads 64 coordinates of its vector's Y from tensor
+//   * 16 coding warps: thread (row, part) reads 32 coordinates of its vector's Y from tensor
 //     memory (the lane is the row), forms the norm from X (the partial sums of squares of the
 //     16 eight-dim chunks combined in the half-warp codec's order, so the fp16 norm is the
-//     decode step's bit for bit), codes, and writes its half of the packed vector.  A
+//     decode step's bit for bit), codes, and writes its part of the packed vector.  A
 //     coordinate whose u lies within kFixBand of a boundary is recomputed exactly by its whole
 //     warp (a compensated fp32 dot product against R's fp32 row, 4 terms a lane) and re-coded.
 // ---------------------------------------------------------------------------------------
 namespace dtc {
 constexpr int kRows = 128;                        // vectors per tile: M of the MMA
-constexpr int kCodeWarps = 8;                     // warps 0-7: coding
-constexpr int kLoadWarps = 2;                     // warps 8-9: X loads
-constexpr int kThreads = 32 * (kCodeWarps + kLoadWarps + 1);  // + warp 10: MMA issue
+constexpr int kCodeWarps = 16;                    // warps 0-15: coding
+constexpr int kParts = kCodeWarps / 4;            // coding threads per vector (row)
+constexpr int kPartDims = 128 / kParts;           // dims each codes
+constexpr int kLoadWarps = 2;                     // warps 16-17: X loads
+constexpr int kThreads = 32 * (kCodeWarps + kLoadWarps + 1);  // + warp 18: MMA issue
 constexpr int kCodeThreads = 32 * kCodeWarps, kLoadThreads = 32 * kLoadWarps;
 constexpr uint32_t kR = 0;                        // R_hi, R_lo: fp16 [2][2 atoms of 16 KB]
 constexpr uint32_t kX = 65536;                    // X: fp16 [2 buffers][2 atoms of 16 KB]
@@ -366,8 +368,8 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kBar + kTmemSlot);
 
   if (warp < kCodeWarps) {
-    // ================= coding: thread = (row, half of the dims) =================
-    const int row = 32 * (warp & 3) + lane, ch = warp >> 2;
+    // ================= coding: thread = (row, part ch of the dims) =================
+    const int row = 32 * (warp & 3) + lane, ch = warp >> 2;  // dims kPartDims ch .. + kPartDims - 1
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     float bnd[15];
     load_boundaries<BITS>(bnd, g.boundaries);
@@ -400,8 +402,9 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
       // half-warp codec's butterfly (xor 8, 4, 2, 1) combines its lanes' sums
       float* const ss = reinterpret_cast<float*>(sm + kSS) + (b * kRows + row) * 16;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint4 w4 = *reinterpret_cast<const uint4*>(xatoms + ch * 16384 + tc::sw128(row, cc));
+      for (int cc0 = 0; cc0 < kPartDims / 8; ++cc0) {
+        const int cc = (kPartDims / 8) * ch + cc0;  // the 8-dim chunk of the vector
+        const uint4 w4 = *reinterpret_cast<const uint4*>(xatoms + (cc >> 3) * 16384 + tc::sw128(row, cc & 7));
         const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
         float x[8];
 #pragma unroll
@@ -413,7 +416,7 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
         float ps = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) ps += x[e] * x[e];
-        ss[8 * ch + cc] = ps;
+        ss[cc] = ps;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kCodeThreads) : "memory");  // both halves' sums are in
       float a8[8];
@@ -431,9 +434,10 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
       const int vpair = off >> 1, hv = off & 1;
       uint32_t w2 = 0u;  // 3-bit: the high bits of the current 32-dim group
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {  // coordinates 64 ch + 16 q .. + 15
+      for (int q0 = 0; q0 < kPartDims / 16; ++q0) {  // coordinates 16 q .. 16 q + 15
+        const int q = (kPartDims / 16) * ch + q0;  // the 16-dim unit of the vector
         float y[16];
-        tc::tmem_ld16(tmem + lane_off + 128 * b + 64 * ch + 16 * q, y);
+        tc::tmem_ld16(tmem + lane_off + 128 * b + 16 * q, y);
         tc::tmem_wait_ld();
         int code[16];
         uint32_t todo = 0;
@@ -447,8 +451,7 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
           const uint32_t want = __ballot_sync(0xffffffffu, todo != 0);
           const int leader = __ffs(want) - 1;
           const int e_lead = __shfl_sync(0xffffffffu, todo ? __ffs(todo) - 1 : 0, leader);
-          const float yi = dot_compensated_warp(xatoms, 32 * (warp & 3) + leader, r32 + (64 * ch + 16 * q + e_lead) * 128,
-                                                lane);
+          const float yi = dot_compensated_warp(xatoms, 32 * (warp & 3) + leader, r32 + (16 * q + e_lead) * 128, lane);
           if (lane == leader) {
             const int c = code_of<BITS>(yi * rcp, bnd);
 #pragma unroll
@@ -458,7 +461,7 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
           }
         }
         if (store) {
-          const int u = 4 * ch + q;  // 16-dim unit of the vector
+          const int u = q;
           if constexpr (BITS == 4) {
             uint32_t lo = 0, hi = 0;
 #pragma unroll
