@@ -419,15 +419,17 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
         for (int k = 0; k < 16; ++k) s[16 * c + k] = v[k];
       }
       tmem_wait_ld();
+      // t = s * n_k - m_use (base 2, one FMA a key), m_use the running max (0 before the first)
+      const float m_use0 = m_run == -CUDART_INF_F ? 0.f : m_run;
       {  // key norms of the tile (stage t % 2)
         const float4* n4 = reinterpret_cast<const float4*>(knorm + 64 * (t % kXStages));
 #pragma unroll
         for (int c = 0; c < kXTok / 4; ++c) {
           const float4 nn = n4[c];
-          s[4 * c] *= nn.x;
-          s[4 * c + 1] *= nn.y;
-          s[4 * c + 2] *= nn.z;
-          s[4 * c + 3] *= nn.w;
+          s[4 * c] = fmaf(s[4 * c], nn.x, -m_use0);
+          s[4 * c + 1] = fmaf(s[4 * c + 1], nn.y, -m_use0);
+          s[4 * c + 2] = fmaf(s[4 * c + 2], nn.z, -m_use0);
+          s[4 * c + 3] = fmaf(s[4 * c + 3], nn.w, -m_use0);
         }
       }
       fence_before_sync();
@@ -444,20 +446,23 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
       for (int jj = 8; jj < kXTok; ++jj) tm[jj & 7] = fmaxf(tm[jj & 7], s[jj]);
       const float tmax = fmaxf(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])), fmaxf(fmaxf(tm[4], tm[5]), fmaxf(tm[6], tm[7])));
       // The running max moves only when the tile's max passes it by more than kLazyMax (log2
-      // units): p = 2^(s - m) then stays <= 2^kLazyMax, exact in fp16 and f32, and O~ is
-      // rescaled rarely instead of on most tiles.
+      // units): p = 2^t then stays <= 2^kLazyMax, exact in fp16 and f32, and O~ is rescaled
+      // rarely instead of on most tiles.  Before the first visible key any visible t moves it.
       float alpha = 1.f;
-      if (tmax > m_run + kLazyMax) {
-        alpha = ex2(m_run - tmax);  // 0 while nothing was seen yet
-        m_run = tmax;
+      if (tmax > (m_run == -CUDART_INF_F ? -CUDART_INF_F : kLazyMax)) {
+        const float m_new = tmax + m_use0;
+        alpha = ex2(m_run - m_new);  // 0 while nothing was seen yet
+        m_run = m_new;
+        const float shift = m_use0 - m_new;
+#pragma unroll
+        for (int jj = 0; jj < kXTok; ++jj) s[jj] += shift;
       }
-      const float m_use = m_run == -CUDART_INF_F ? 0.f : m_run;
       float ls[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) ls[k] = 0.f;
 #pragma unroll
       for (int jj = 0; jj < kXTok; ++jj) {
-        const float pr = ex2(s[jj] - m_use);  // masked: +0
+        const float pr = ex2(s[jj]);  // masked: +0
         ls[jj & 7] += pr;
         s[jj] = pr;
       }

@@ -186,9 +186,10 @@ def test_zero_length_sequences_give_zeros():
     PT.assert_close(r["out"], r["ref"])
 
 
-def test_status_flags_and_clamping():
+@pytest.mark.parametrize("mode", [ISO, DENSE], ids=["iso", "dense"])
+def test_status_flags_and_clamping(mode):
     """Out-of-range inputs set status bits instead of faulting; other sequences are unaffected."""
-    wl, kv, q = make_case(ISO, 3, 32, 8, 16, [40, 40])
+    wl, kv, q = make_case(mode, 3, 32, 8, 16, [40, 40])
     s = wl.spec
     cache = rq.KVCache(s.mode, s.bits, s.num_q_heads, s.num_kv_heads, s.page_size, wl.num_pages, wl.rot_k,
                        wl.rot_v, max_batch=2, max_pages_per_seq=wl.block_table.shape[1])
