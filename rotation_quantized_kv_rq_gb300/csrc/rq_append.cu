@@ -275,7 +275,7 @@ constexpr int kThreads = 32 * (kCodeWarps + kLoadWarps + 1);  // + warp 18: MMA 
 constexpr int kCodeThreads = 32 * kCodeWarps, kLoadThreads = 32 * kLoadWarps;
 constexpr uint32_t kR = 0;                        // R_hi, R_lo: fp16 [2][2 atoms of 16 KB]
 constexpr uint32_t kX = 65536;                    // X: fp16 [2 buffers][2 atoms of 16 KB]
-constexpr uint32_t kSS = kX + 65536;              // partial sums of squares: f32 [2][128][16]
+constexpr uint32_t kSS = kX + 65536;              // partial sums of squares: f32 [2][16 chunks][128 rows]
 constexpr uint32_t kBar = kSS + 2 * kRows * 16 * 4;
 constexpr uint32_t kBarXFull = 0, kBarXEmpty = 16, kBarYFull = 32, kBarYEmpty = 48, kBarDrain = 64;
 constexpr uint32_t kTmemSlot = 72, kAbort = 76;
@@ -400,7 +400,7 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
       const uint8_t* const xatoms = sm + kX + b * 32768;
       // the norm: partial sums of squares of the 8-dim chunks (each in order), combined as the
       // half-warp codec's butterfly (xor 8, 4, 2, 1) combines its lanes' sums
-      float* const ss = reinterpret_cast<float*>(sm + kSS) + (b * kRows + row) * 16;
+      float* const ss = reinterpret_cast<float*>(sm + kSS) + b * 16 * kRows + row;  // chunk c at ss[c * kRows]
 #pragma unroll
       for (int cc0 = 0; cc0 < kPartDims / 8; ++cc0) {
         const int cc = (kPartDims / 8) * ch + cc0;  // the 8-dim chunk of the vector
@@ -416,12 +416,12 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
         float ps = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) ps += x[e] * x[e];
-        ss[cc] = ps;
+        ss[cc * kRows] = ps;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kCodeThreads) : "memory");  // both halves' sums are in
       float a8[8];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) a8[jj] = ss[jj] + ss[jj + 8];
+      for (int jj = 0; jj < 8; ++jj) a8[jj] = ss[jj * kRows] + ss[(jj + 8) * kRows];
       const float b0 = a8[0] + a8[4], b1 = a8[1] + a8[5], b2 = a8[2] + a8[6], b3 = a8[3] + a8[7];
       const float nrm = __fsqrt_rn((b0 + b2) + (b1 + b3));
       const float rcp = inv_norm(nrm);
