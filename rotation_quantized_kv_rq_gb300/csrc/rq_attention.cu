@@ -411,10 +411,9 @@ __device__ __forceinline__ void qk_tile(float (&s)[NT][4], const Raw<BITS>& r, c
 #pragma unroll
     for (int kc = 0; kc < 8; ++kc) {
       const int w = kc >> 2, byte = kc & 3;
-      const uint32_t a0 = lut_dyn<0>(k0[w], byte, key1, key2);
-      const uint32_t a1 = lut_dyn<0>(k1[w], byte, key1, key2);
-      const uint32_t a2 = lut_dyn<1>(k0[w], byte, key1, key2);
-      const uint32_t a3 = lut_dyn<1>(k1[w], byte, key1, key2);
+      uint32_t a0, a1, a2, a3;
+      lut::get2(k0[w], byte, key1, a0, a2);  // (U1, U2) of one index byte: one 8-byte load
+      lut::get2(k1[w], byte, key1, a1, a3);
       mma_all(kc, a0, a1, a2, a3);
     }
   } else {
@@ -488,10 +487,9 @@ __device__ __forceinline__ void pv_tile(float (&o)[NT][8][4], const Raw<BITS>& r
     for (int mt = 0; mt < 8; ++mt) {
       const int j = mt >> 1;
       const uint32_t x0 = (mt & 1) ? XO[0] : XE[0], x1 = (mt & 1) ? XO[1] : XE[1];
-      const uint32_t a0 = lut_dyn<0>(x0, j, key1, key2);
-      const uint32_t a1 = lut_dyn<1>(x0, j, key1, key2);
-      const uint32_t a2 = lut_dyn<0>(x1, j, key1, key2);
-      const uint32_t a3 = lut_dyn<1>(x1, j, key1, key2);
+      uint32_t a0, a1, a2, a3;
+      lut::get2(x0, j, key1, a0, a1);
+      lut::get2(x1, j, key1, a2, a3);
       mma_all(mt, a0, a1, a2, a3);
     }
   } else {
@@ -861,8 +859,8 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   const float cb_val = threadIdx.x < (1 << BITS) ? g.centroids[threadIdx.x] : 0.f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const uint32_t key1 = plan.lut | ((uint32_t)lane * 4u);
-  const uint32_t key2 = key1 + 128u;
+  const uint32_t key1 = lut::key<BITS>(plan.lut, lane, 0);
+  const uint32_t key2 = lut::key<BITS>(plan.lut, lane, 1);
   const int P = g.page_size;
   const int tiles_per_page = P / 16;
   // Stage layout (see Ring): section by section when a pair always lies in one page.

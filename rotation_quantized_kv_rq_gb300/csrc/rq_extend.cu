@@ -196,8 +196,8 @@ __device__ __forceinline__ void k_chunks(uint4 (&ch)[4], const GroupRaw& r, uint
     for (int q = 0; q < 4; ++q) {
       const uint32_t w = r.w[q >> 1];
       const int j0 = 2 * (q & 1);
-      ch[q] = make_uint4(lut::get(w, j0, key1), lut::get(w, j0, key2), lut::get(w, j0 + 1, key1),
-                         lut::get(w, j0 + 1, key2));
+      lut::get2(w, j0, key1, ch[q].x, ch[q].y);  // (U1, U2) of one index byte: one 8-byte load
+      lut::get2(w, j0 + 1, key1, ch[q].z, ch[q].w);
     }
   } else {
     const uint32_t w2s = r.w[2] >> 2;
@@ -238,10 +238,8 @@ __device__ __forceinline__ void v_pairs(uint32_t (&out)[16], const GroupRaw& A, 
     const uint32_t XE = bitsel(a, b << 4, 0x0F0F0F0Fu), XO = bitsel(a >> 4, b, 0x0F0F0F0Fu);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      out[4 * k] = lut::get(XE, k, key1);
-      out[4 * k + 1] = lut::get(XE, k, key2);
-      out[4 * k + 2] = lut::get(XO, k, key1);
-      out[4 * k + 3] = lut::get(XO, k, key2);
+      lut::get2(XE, k, key1, out[4 * k], out[4 * k + 1]);
+      lut::get2(XO, k, key1, out[4 * k + 2], out[4 * k + 3]);
     }
   } else {
     const int sh = 2 * hh;
@@ -323,7 +321,7 @@ extend_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
 
   __syncthreads();  // the centroids are staged, the barriers initialised
   lut::fill<BITS>(reinterpret_cast<uint32_t*>(at(pl.lut)), cb, tid, kXThreads);
-  const uint32_t key1 = lut::key(pl.lut, lane, 0), key2 = lut::key(pl.lut, lane, 1);
+  const uint32_t key1 = lut::key<BITS>(pl.lut, lane, 0), key2 = lut::key<BITS>(pl.lut, lane, 1);
   fence_async_smem();
   fence_before_sync();
   __syncthreads();  // the code table and the tensor-memory address are in place
