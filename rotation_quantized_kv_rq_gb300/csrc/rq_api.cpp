@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "../../include/rq.h"
 #include "rq_internal.h"
@@ -20,6 +21,7 @@ struct rq_ctx {
   float* d_tables;        // rot_k | rot_v | centroids | boundaries
   __half* d_dense16;      // dense: fp16 hi/lo split of R_k and R_v for the append GEMM
   float* d_dense32;       // dense: fp32 R_k and R_v, row-major, for the append's exact recompute
+  uint32_t* d_rotq;       // dense: R_k's fp16 hi / lo in the query rotation's MMA fragment order
   float* d_qrot;          // dense: fp32 R_k q of one attention call [max_batch][max_T][Hq][128]
   float* d_ws;            // fragment partials of the stream-K split
   int* d_frag;            // first / last CTA of each unit's fragments [2 U], then rounds done per unit [U]
@@ -219,6 +221,7 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   if (e == cudaSuccess && dense) {
     e = cudaMalloc(&ctx->d_dense16, dense16_halves * sizeof(__half));
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_dense32, 2 * rot * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_rotq, rot * sizeof(uint32_t));  // 4 words per 4 entries
     if (e == cudaSuccess) e = cudaMemcpy(ctx->d_dense32, cfg->rot_k, rot * sizeof(float), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
       e = cudaMemcpy(ctx->d_dense32 + rot, cfg->rot_v, rot * sizeof(float), cudaMemcpyHostToDevice);
@@ -253,6 +256,26 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
           }
       }
       e = cudaMemcpy(ctx->d_dense16, host16, dense16_halves * sizeof(__half), cudaMemcpyHostToDevice);
+      // the same halves of R_k as the query rotation's MMA B operands: per kv head, k-step ks,
+      // n-tile nt and lane 4g + t, output dim n = 8 nt + g and input dims m = 32t + 4ks .. m + 3
+      std::vector<uint32_t> words(rot);
+      auto half_bits = [&](int part, int h, int n, int m) {
+        uint16_t b;
+        std::memcpy(&b, host16 + (((size_t)h * 2 + part) * d + n) * d + m, 2);
+        return (uint32_t)b;
+      };
+      for (int h = 0; h < hkv; ++h)
+        for (int ks = 0; ks < 8; ++ks)
+          for (int nt = 0; nt < 16; ++nt)
+            for (int lane = 0; lane < 32; ++lane) {
+              const int n = 8 * nt + lane / 4, m = 32 * (lane % 4) + 4 * ks;
+              uint32_t* w = words.data() + ((((size_t)h * 8 + ks) * 16 + nt) * 32 + lane) * 4;
+              for (int part = 0; part < 2; ++part) {
+                w[2 * part] = half_bits(part, h, n, m) | half_bits(part, h, n, m + 1) << 16;
+                w[2 * part + 1] = half_bits(part, h, n, m + 2) | half_bits(part, h, n, m + 3) << 16;
+              }
+            }
+      if (e == cudaSuccess) e = cudaMemcpy(ctx->d_rotq, words.data(), rot * sizeof(uint32_t), cudaMemcpyHostToDevice);
     } else {
       std::memcpy(host, cfg->rot_k, rot * sizeof(float));
       std::memcpy(host + rot, cfg->rot_v, rot * sizeof(float));
@@ -273,6 +296,7 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
     cudaFree(ctx->d_frag);
     cudaFree(ctx->d_dense16);
     cudaFree(ctx->d_dense32);
+    cudaFree(ctx->d_rotq);
     cudaFree(ctx->d_qrot);
     delete ctx;
     return RQ_ERR_CUDA;
@@ -295,6 +319,7 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   g.rot_v = ctx->d_tables + rot;
   g.dense16 = ctx->d_dense16;
   g.dense32 = ctx->d_dense32;
+  g.rotq = ctx->d_rotq;
   g.centroids = ctx->d_tables + 2 * rot;  // c / c_scale
   g.boundaries = ctx->d_tables + 2 * rot + 256;
   *out = ctx;
@@ -310,6 +335,7 @@ void rq_free(rq_ctx* ctx) {
     cudaFree(ctx->d_frag);
     cudaFree(ctx->d_dense16);
     cudaFree(ctx->d_dense32);
+    cudaFree(ctx->d_rotq);
     cudaFree(ctx->d_qrot);
   }
   delete ctx;

@@ -32,6 +32,8 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include <algorithm>
+
 #include "rq_codec.cuh"
 #include "rq_lut.cuh"
 #include "rq_internal.h"
@@ -1478,10 +1480,15 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
 // ---------------------------------------------------------------------------------------
 // Dense rotation (TurboQuant): the queries' end of the call.  The query rows of one kv head --
 // over every sequence and query token -- are numbered r = (b * T + j) * group + k, in groups of
-// 16.  Thread i owns output dim i: per step of the sum it reads four entries of the staged
-// matrix and the 16 rows' four inputs as float4 broadcasts from shared memory.
+// 16.  A warp forms y = R_k q for 16 rows and 32 output dims on the tensor cores: the fp16
+// query times R_k's fp16 hi and lo halves (R_k = hi + lo to about 2^-22), both products into
+// one fp32 accumulator (g.rotq holds the halves in the MMA's fragment order).  A decode step's
+// new tokens take the fp32 path of the append instead (thread i owns output dim i: per step of
+// the sum it reads four entries of the staged matrix and the 16 rows' four inputs as float4
+// broadcasts from shared memory), whose decisions the stored codes must repeat.
 // ---------------------------------------------------------------------------------------
 constexpr int kDenseRows = 16;
+constexpr int kRotqWords = 8 * 16 * 32 * 4;  // a kv head's fragments: [k-step][n-tile][lane][4] u32
 
 constexpr int kDenseSmem = kHeadDim * kHeadDim * 4;  // the 128 x 128 fp32 matrix, staged
 
@@ -1517,16 +1524,51 @@ __device__ __forceinline__ size_t dense_row_index(const Geometry& g, int h, int 
   return (size_t)bj * g.num_q_heads + h * g.group + k;
 }
 
-// The dense rotation's work before the split-K kernel, one launch of 512-thread CTAs (four
-// 128-thread slices; thread i of a slice owns output dim i):
-//   * CTAs [0, q_ctas): q_rot[b][j][head] = R_k q[b][j][head] (fp32, unscaled); rot_k holds R_k
-//     transposed.  Each kv head's rows, in groups of 16, are shared out over q_ctas / Hkv CTAs,
-//     which stage the matrix once; the four slices take four groups at a time.
+// y[16 rows][32 dims] = q R_k^T for rows r0 .. r0 + 15 of kv head h (rows >= rows read as zero and
+// are not stored) and output dims 32 ds .. 32 ds + 31: four n-tiles, eight k-steps, two MMAs
+// (hi, lo) each.  The MMA's k-slots of lane t (2t, 2t+1 | 2t+8, 2t+9) carry input dims 32t + 4ks
+// + (0, 1 | 2, 3), an order g.rotq's words follow too, so each lane reads its row's inputs as
+// 8-byte pieces of one 64-byte span.  frag: the head's fragments in shared memory.
+__device__ __forceinline__ void rotate_rows_tc(const Geometry& g, const AttnArgs& a, const uint4* frag, int h,
+                                               int r0, int rows, int ds, int lane) {
+  const int gq = lane >> 2, tq = lane & 3;
+  const __half* q = reinterpret_cast<const __half*>(a.q);
+  const int ra = r0 + gq, rb = r0 + gq + 8;
+  const uint2* pa = ra < rows ? reinterpret_cast<const uint2*>(q + dense_row_index(g, h, ra) * kHeadDim + 32 * tq) : nullptr;
+  const uint2* pb = rb < rows ? reinterpret_cast<const uint2*>(q + dense_row_index(g, h, rb) * kHeadDim + 32 * tq) : nullptr;
+  float acc[4][4];
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint2 xa = pa ? pa[ks] : make_uint2(0u, 0u), xb = pb ? pb[ks] : make_uint2(0u, 0u);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const uint4 w = frag[(ks * 16 + 4 * ds + nt) * 32 + lane];  // hi b0, hi b1, lo b0, lo b1
+      if (ks == 0)
+        mma16816_z(acc[nt], xa.x, xb.x, xa.y, xb.y, w.x, w.y);
+      else
+        mma16816(acc[nt], xa.x, xb.x, xa.y, xb.y, w.x, w.y);
+      mma16816(acc[nt], xa.x, xb.x, xa.y, xb.y, w.z, w.w);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    const int col = 32 * ds + 8 * nt + 2 * tq;
+    if (pa) *reinterpret_cast<float2*>(a.q_rot + dense_row_index(g, h, ra) * kHeadDim + col) = make_float2(acc[nt][0], acc[nt][1]);
+    if (pb) *reinterpret_cast<float2*>(a.q_rot + dense_row_index(g, h, rb) * kHeadDim + col) = make_float2(acc[nt][2], acc[nt][3]);
+  }
+}
+
+// The dense rotation's work before the split-K kernel, one launch of 512-thread CTAs:
+//   * CTAs [0, q_ctas): q_rot[b][j][head] = R_k q[b][j][head] (fp32, unscaled).  Each kv head's
+//     rows, in groups of 64, are shared out over q_ctas / Hkv CTAs, which stage the head's
+//     fragments (64 KB) once; warp w takes rows 16 (w / 4) .. + 15 and dims 32 (w % 4) .. + 31
+//     of each group (rotate_rows_tc).
 //   * a decode step (a.k_new) adds 2 Hkv ceil(B / 16) CTAs, each coding 16 sequences' newest K
-//     (R_k) or V (R_v) vector of one kv head and writing it at position seq_lens[b] - 1 (slice
-//     0 computes): the fp32 R x of dense_rows decides every code farther than kFixBand from a
-//     boundary and the compensated dot product the others -- the decisions rq_quantize_append
-//     makes, so the two write the same bytes.
+//     (R_k) or V (R_v) vector of one kv head and writing it at position seq_lens[b] - 1 (four
+//     128-thread slices, slice 0 computes; thread i owns output dim i): the fp32 R x of
+//     dense_rows decides every code farther than kFixBand from a boundary and the compensated
+//     dot product the others -- the decisions rq_quantize_append makes, so the two write the
+//     same bytes.
 constexpr int kDenseSlices = 4;
 constexpr int kDenseThreads = kDenseSlices * kHeadDim;
 template <int BITS>
@@ -1538,28 +1580,13 @@ dense_prologue_kernel(const Geometry g, const AttnArgs a, int q_ctas) {
   const int slice = threadIdx.x / kHeadDim, i = threadIdx.x % kHeadDim;
   if ((int)blockIdx.x < q_ctas) {
     const int h = blockIdx.x % hkv, per_head = q_ctas / hkv;
-    stage_matrix(wsm, g.rot_k + (size_t)h * kHeadDim * kHeadDim);
+    stage_matrix(wsm, reinterpret_cast<const float*>(g.rotq) + (size_t)h * kRotqWords);  // 64 KB either way
+    __syncthreads();
+    const uint4* frag = reinterpret_cast<const uint4*>(wsm);
     const int rows = a.B * a.T * g.group;
-    const int groups = (rows + kDenseRows - 1) / kDenseRows;
-    const __half* q = reinterpret_cast<const __half*>(a.q);
-    // (the loop bound is uniform over the CTA: every thread reaches every barrier)
-    for (int g0 = (blockIdx.x / hkv) * kDenseSlices; g0 < groups; g0 += per_head * kDenseSlices) {
-      const int r0 = (g0 + slice) * kDenseRows;
-      const int nr = max(0, min(kDenseRows, rows - r0));
-      __syncthreads();  // the previous groups' rows are read
-      for (int e = i; e < kDenseRows * kHeadDim; e += kHeadDim) {
-        const int r = e / kHeadDim, d = e % kHeadDim;
-        qs[slice][r][d] = r < nr ? __half2float(q[dense_row_index(g, h, r0 + r) * kHeadDim + d]) : 0.f;
-      }
-      __syncthreads();
-      if (nr > 0) {
-        float acc[kDenseRows];
-        dense_rows(acc, wsm, qs[slice], i);
-#pragma unroll
-        for (int r = 0; r < kDenseRows; ++r)
-          if (r < nr) a.q_rot[dense_row_index(g, h, r0 + r) * kHeadDim + i] = acc[r];
-      }
-    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int r0 = (blockIdx.x / hkv) * 64; r0 < rows; r0 += per_head * 64)
+      rotate_rows_tc(g, a, frag, h, r0 + 16 * (warp >> 2), rows, warp & 3, lane);
     return;
   }
   // ---- the decode step's new tokens (slice 0; every thread stages and reaches the barriers) ----
@@ -1715,13 +1742,17 @@ static void launch_splitk(const Geometry& g, const AttnArgs& a, cudaStream_t str
 }
 
 // The dense rotation's prologue launch: query rows, plus a decode step's new tokens.  A kv
-// head's 16-row groups go to at most kDenseQCtasPerHead CTAs, four groups at a time (the 64 KB
-// matrix is staged once per CTA, so few rows per CTA would be bound by the staging).
-constexpr int kDenseQCtasPerHead = 32;
+// head's 64-row groups go to at most as many CTAs as make two per SM over all kv heads (each
+// stages the head's 64 KB of fragments once).
 static cudaError_t launch_dense_prologue(const Geometry& g, const AttnArgs& a, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   const long long rows_per_head = (long long)a.B * a.T * g.group;
-  const long long quads = (rows_per_head + kDenseSlices * kDenseRows - 1) / (kDenseSlices * kDenseRows);
-  const long long q_ctas = (long long)g.num_kv_heads * (quads < kDenseQCtasPerHead ? quads : kDenseQCtasPerHead);
+  const long long groups = (rows_per_head + 63) / 64;
+  const long long cap = std::max(1LL, 2LL * sms / g.num_kv_heads);
+  const long long q_ctas = (long long)g.num_kv_heads * std::min(groups, cap);
   const long long step_ctas = a.k_new ? 2LL * g.num_kv_heads * ((a.B + kDenseRows - 1) / kDenseRows) : 0;
   if (q_ctas + step_ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned ctas = (unsigned)(q_ctas + step_ctas);

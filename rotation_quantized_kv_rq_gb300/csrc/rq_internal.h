@@ -37,6 +37,11 @@ struct Geometry {
   const __half* dense16;
   // dense only: device fp32 [2 (K, V)][Hkv][128][128] row-major R (exact recompute in the append)
   const float* dense32;
+  // dense only: device [Hkv][8 k-steps][16 n-tiles][32 lanes][4] u32, R_k's fp16 hi and lo as the
+  // B operands of the query rotation's m16n8k16 MMAs (lane 4g + t: output dim 8 n-tile + g;
+  // words hi(m, m+1), hi(m+2, m+3), lo(m, m+1), lo(m+2, m+3) with m = 32t + 4 k-step, the lower
+  // dim in the low half); null otherwise.
+  const uint32_t* rotq;
   const float* centroids;   // device [2^bits]: c / out_scale, the fp16 operands' source
   const float* boundaries;  // device [2^bits - 1]
 };

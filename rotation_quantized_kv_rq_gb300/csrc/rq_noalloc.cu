@@ -109,6 +109,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   g.rot_v = d_rot_v;
   g.dense16 = nullptr;
   g.dense32 = nullptr;
+  g.rotq = nullptr;
   g.centroids = d_centroids;
   g.boundaries = nullptr;  // decode never codes
 
