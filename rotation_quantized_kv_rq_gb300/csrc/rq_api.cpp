@@ -20,7 +20,7 @@ struct rq_ctx {
   int num_sms;
   float* d_tables;        // rot_k | rot_v | centroids | boundaries
   __half* d_dense16;      // dense: fp16 hi/lo split of R_k and R_v for the append GEMM
-  float* d_dense32;       // dense: fp32 R_k and R_v, row-major, for the append's exact recompute
+  float* d_dense32;       // dense: fp32 R_k and R_v, row-major, for the append's exact recompute; then R_v^T
   uint32_t* d_rotq;       // dense: R_k's fp16 hi / lo in the query rotation's MMA fragment order
   float* d_qrot;          // dense: fp32 R_k q of one attention call [max_batch][max_T][Hq][128]
   float* d_ws;            // fragment partials of the stream-K split
@@ -220,11 +220,18 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   const size_t dense16_halves = dense ? 2 * rot * 2 : 0;  // [K, V][Hkv][hi, lo][d][d]
   if (e == cudaSuccess && dense) {
     e = cudaMalloc(&ctx->d_dense16, dense16_halves * sizeof(__half));
-    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_dense32, 2 * rot * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->d_dense32, 3 * rot * sizeof(float));  // R_k, R_v, R_v^T
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_rotq, rot * sizeof(uint32_t));  // 4 words per 4 entries
     if (e == cudaSuccess) e = cudaMemcpy(ctx->d_dense32, cfg->rot_k, rot * sizeof(float), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
       e = cudaMemcpy(ctx->d_dense32 + rot, cfg->rot_v, rot * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) {
+      std::vector<float> vt(rot);
+      for (int h = 0; h < hkv; ++h)
+        for (int i = 0; i < d; ++i)
+          for (int m = 0; m < d; ++m) vt[((size_t)h * d + m) * d + i] = cfg->rot_v[((size_t)h * d + i) * d + m];
+      e = cudaMemcpy(ctx->d_dense32 + 2 * rot, vt.data(), rot * sizeof(float), cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess)
       e = cudaMalloc(&ctx->d_qrot, (size_t)cfg->max_batch * cfg->max_query_tokens * cfg->num_q_heads * d * sizeof(float));
   }
@@ -320,6 +327,7 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   g.dense16 = ctx->d_dense16;
   g.dense32 = ctx->d_dense32;
   g.rotq = ctx->d_rotq;
+  g.rot_vt = dense ? ctx->d_dense32 + 2 * rot : nullptr;
   g.centroids = ctx->d_tables + 2 * rot;  // c / c_scale
   g.boundaries = ctx->d_tables + 2 * rot + 256;
   *out = ctx;

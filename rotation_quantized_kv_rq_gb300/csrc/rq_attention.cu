@@ -1502,16 +1502,16 @@ __device__ __forceinline__ void stage_matrix(float* ws, const float* __restrict_
 }
 
 // out[r][i] = sum_m ws[m * 128 + i] * xs[r][m] for 16 rows (the calling thread's dim i).
-__device__ __forceinline__ void dense_rows(float (&acc)[kDenseRows], const float* ws, const float (*xs)[kHeadDim],
-                                           int i) {
+template <int N>
+__device__ __forceinline__ void dense_rows(float (&acc)[N], const float* ws, const float (*xs)[kHeadDim], int i) {
 #pragma unroll
-  for (int r = 0; r < kDenseRows; ++r) acc[r] = 0.f;
+  for (int r = 0; r < N; ++r) acc[r] = 0.f;
 #pragma unroll 2
   for (int m = 0; m < kHeadDim; m += 4) {
     const float w0 = ws[(m + 0) * kHeadDim + i], w1 = ws[(m + 1) * kHeadDim + i];
     const float w2 = ws[(m + 2) * kHeadDim + i], w3 = ws[(m + 3) * kHeadDim + i];
 #pragma unroll
-    for (int r = 0; r < kDenseRows; ++r) {
+    for (int r = 0; r < N; ++r) {
       const float4 x = *reinterpret_cast<const float4*>(&xs[r][m]);
       acc[r] = fmaf(w0, x.x, fmaf(w1, x.y, fmaf(w2, x.z, fmaf(w3, x.w, acc[r]))));
     }
@@ -1564,11 +1564,11 @@ __device__ __forceinline__ void rotate_rows_tc(const Geometry& g, const AttnArgs
 //     fragments (64 KB) once; warp w takes rows 16 (w / 4) .. + 15 and dims 32 (w % 4) .. + 31
 //     of each group (rotate_rows_tc).
 //   * a decode step (a.k_new) adds 2 Hkv ceil(B / 16) CTAs, each coding 16 sequences' newest K
-//     (R_k) or V (R_v) vector of one kv head and writing it at position seq_lens[b] - 1 (four
-//     128-thread slices, slice 0 computes; thread i owns output dim i): the fp32 R x of
-//     dense_rows decides every code farther than kFixBand from a boundary and the compensated
-//     dot product the others -- the decisions rq_quantize_append makes, so the two write the
-//     same bytes.
+//     (R_k) or V (R_v) vector of one kv head and writing it at position seq_lens[b] - 1: R
+//     staged transposed, four 128-thread slices forming y = R x for 4 vectors each (thread i
+//     owns output dim i), then a half-warp per vector codes it.  The fp32 R x of dense_rows
+//     decides every code farther than kFixBand from a boundary and the compensated dot product
+//     the others -- the decisions rq_quantize_append makes, so the two write the same bytes.
 constexpr int kDenseSlices = 4;
 constexpr int kDenseThreads = kDenseSlices * kHeadDim;
 template <int BITS>
@@ -1589,46 +1589,42 @@ dense_prologue_kernel(const Geometry g, const AttnArgs a, int q_ctas) {
       rotate_rows_tc(g, a, frag, h, r0 + 16 * (warp >> 2), rows, warp & 3, lane);
     return;
   }
-  // ---- the decode step's new tokens (slice 0; every thread stages and reaches the barriers) ----
+  // ---- the decode step's new tokens (every thread stages and reaches the barriers) ----
   const int c = blockIdx.x - q_ctas;
   const int h = c % hkv, kind = (c / hkv) & 1, b0 = (c / (2 * hkv)) * kDenseRows;
-  if (kind == 0) {
-    stage_matrix(wsm, g.rot_k + (size_t)h * kHeadDim * kHeadDim);  // [m][i] = R_k[i][m]
-  } else if (slice == 0) {  // [m][i] = R_v[i][m]: thread i copies row i of R_v into column i
-    const float4* row = reinterpret_cast<const float4*>(g.rot_v + ((size_t)h * kHeadDim + i) * kHeadDim);
-#pragma unroll 4
-    for (int m4 = 0; m4 < kHeadDim / 4; ++m4) {
-      const float4 v = __ldg(row + m4);
-      wsm[(4 * m4) * kHeadDim + i] = v.x;
-      wsm[(4 * m4 + 1) * kHeadDim + i] = v.y;
-      wsm[(4 * m4 + 2) * kHeadDim + i] = v.z;
-      wsm[(4 * m4 + 3) * kHeadDim + i] = v.w;
-    }
-  }
+  // [m][i] = R[i][m]: R_k and R_v are both kept transposed for this
+  stage_matrix(wsm, (kind ? g.rot_vt : g.rot_k) + (size_t)h * kHeadDim * kHeadDim);
+  static_assert(kDenseRows == 4 * kDenseSlices && kDenseThreads / 32 >= kDenseRows / 2, "the step's shares");
   const __half* src = kind ? a.v_new : a.k_new;
-  if (slice == 0) {
-    for (int e = i; e < kDenseRows * kHeadDim; e += kHeadDim) {
-      const int r = e / kHeadDim, d = e % kHeadDim, b = b0 + r;
-      qs[0][r][d] = b < a.B ? __half2float(src[((size_t)b * hkv + h) * kHeadDim + d]) : 0.f;
+  for (int e = threadIdx.x; e < kDenseRows * kHeadDim / 8; e += kDenseThreads) {  // 8 fp16 at a time
+    const int r = e >> 4, ch = e & 15, b = b0 + r;
+    float2 f[4] = {};
+    if (b < a.B) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(src + ((size_t)b * hkv + h) * kHeadDim + 8 * ch);
+      f[0] = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+      f[1] = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+      f[2] = __half22float2(*reinterpret_cast<const __half2*>(&raw.z));
+      f[3] = __half22float2(*reinterpret_cast<const __half2*>(&raw.w));
     }
+    reinterpret_cast<float4*>(&qs[0][r][8 * ch])[0] = make_float4(f[0].x, f[0].y, f[1].x, f[1].y);
+    reinterpret_cast<float4*>(&qs[0][r][8 * ch])[1] = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
   }
   __syncthreads();
-  if (slice == 0) {
-    float acc[kDenseRows];
-    dense_rows(acc, wsm, qs[0], i);
+  {  // slice s forms rows 4s .. 4s + 3
+    float acc[kDenseRows / kDenseSlices];
+    dense_rows(acc, wsm, qs[0] + 4 * slice, i);
 #pragma unroll
-    for (int r = 0; r < kDenseRows; ++r) qs[1][r][i] = acc[r];  // y, beside x
+    for (int r = 0; r < kDenseRows / kDenseSlices; ++r) qs[1][4 * slice + r][i] = acc[r];  // y, beside x
   }
   __syncthreads();
-  if (slice != 0) return;  // no barrier follows
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, j = lane & 15;
+  if (warp >= kDenseRows / 2) return;  // a half-warp per vector; no barrier follows
   float bnd[15];
   codec::load_boundaries<BITS>(bnd, g.boundaries);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, j = lane & 15;
   const float* r32 = g.dense32 + ((size_t)kind * hkv + h) * kHeadDim * kHeadDim;  // fp32 R rows
   const int cap = a.max_pages * g.page_size;
-#pragma unroll 1
-  for (int pass = 0; pass < kDenseRows / 8; ++pass) {  // a half-warp per vector, 8 per pass
-    const int r = 8 * pass + 2 * warp + half, b = b0 + r;
+  {
+    const int r = 2 * warp + half, b = b0 + r;
     bool store = false;
     int page = 0, off = 0;
     uint4 raw = make_uint4(0u, 0u, 0u, 0u);

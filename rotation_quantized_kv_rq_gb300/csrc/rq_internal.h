@@ -42,6 +42,9 @@ struct Geometry {
   // words hi(m, m+1), hi(m+2, m+3), lo(m, m+1), lo(m+2, m+3) with m = 32t + 4 k-step, the lower
   // dim in the low half); null otherwise.
   const uint32_t* rotq;
+  // dense only: device fp32 [Hkv][128][128] R_v TRANSPOSED ([m][i] = R_v[i][m]: a decode step's
+  // V coding stages it as it is); null otherwise.
+  const float* rot_vt;
   const float* centroids;   // device [2^bits]: c / out_scale, the fp16 operands' source
   const float* boundaries;  // device [2^bits - 1]
 };

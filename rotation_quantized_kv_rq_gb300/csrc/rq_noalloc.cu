@@ -110,6 +110,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   g.dense16 = nullptr;
   g.dense32 = nullptr;
   g.rotq = nullptr;
+  g.rot_vt = nullptr;
   g.centroids = d_centroids;
   g.boundaries = nullptr;  // decode never codes
 
