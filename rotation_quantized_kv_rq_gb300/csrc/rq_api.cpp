@@ -22,6 +22,7 @@ struct rq_ctx {
   __half* d_dense16;      // dense: fp16 hi/lo split of R_k and R_v for the append GEMM
   float* d_dense32;       // dense: fp32 R_k and R_v, row-major, for the append's exact recompute; then R_v^T
   uint32_t* d_rotq;       // dense: R_k's fp16 hi / lo in the query rotation's MMA fragment order
+  uint32_t* d_codetab;    // the binned code table (rq_internal.h), or null
   float* d_qrot;          // dense: fp32 R_k q of one attention call [max_batch][max_T][Hq][128]
   float* d_ws;            // fragment partials of the stream-K split
   int* d_frag;            // first / last CTA of each unit's fragments [2 U], then rounds done per unit [U]
@@ -153,6 +154,35 @@ int rq_lloyd_max_codebook(int bits, int head_dim, float* centroids) {
   const double s = 1.0 / std::sqrt((double)head_dim);
   for (int j = 0; j < L; ++j) centroids[j] = (float)(c[j] * s);
   return RQ_OK;
+}
+
+// The binned code table of boundaries bnd[0 .. nb - 1] (ascending): bin n = k - kCodeBinHalf
+// holds every u with RNE(u * kCodeBinScale) = n, i.e. u in [(n - 1/2) / scale, (n + 1/2) /
+// scale]; widened by 2e-5 on each side it may hold one boundary at most, else there is no table.
+static bool build_code_table(const float* bnd, int nb, uint32_t* tab) {
+  const double ext = 2e-5;
+  for (int k = 0; k + 1 < rq::kCodeBins; ++k) {
+    const int n = k - rq::kCodeBinHalf;
+    const double lo = (n - 0.5) / rq::kCodeBinScale - ext, hi = (n + 0.5) / rq::kCodeBinScale + ext;
+    uint32_t below = 0;
+    int inside = 0;
+    float near = INFINITY;
+    for (int j = 0; j < nb; ++j) {
+      if ((double)bnd[j] < lo) {
+        ++below;
+      } else if ((double)bnd[j] <= hi) {
+        ++inside;
+        near = bnd[j];
+      }
+    }
+    if (inside > 1) return false;
+    tab[2 * k] = below;
+    std::memcpy(&tab[2 * k + 1], &near, 4);
+  }
+  const float inf = INFINITY;
+  tab[2 * (rq::kCodeBins - 1)] = 0u;
+  std::memcpy(&tab[2 * (rq::kCodeBins - 1) + 1], &inf, 4);
+  return true;
 }
 
 int rq_create(rq_ctx** out, const rq_config* cfg) {
@@ -294,6 +324,14 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   }
   std::free(host);
   std::free(host16);
+  if (e == cudaSuccess) {
+    std::vector<uint32_t> tab(2 * rq::kCodeBins);
+    if (build_code_table(ctx->boundaries, L - 1, tab.data())) {
+      e = cudaMalloc(&ctx->d_codetab, tab.size() * sizeof(uint32_t));
+      if (e == cudaSuccess)
+        e = cudaMemcpy(ctx->d_codetab, tab.data(), tab.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
+    }
+  }
   if (e == cudaSuccess) e = rq::attention_prepare();
   if (e == cudaSuccess) e = rq::append_prepare();
   if (e == cudaSuccess) e = rq::extend_prepare();
@@ -304,6 +342,7 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
     cudaFree(ctx->d_dense16);
     cudaFree(ctx->d_dense32);
     cudaFree(ctx->d_rotq);
+    cudaFree(ctx->d_codetab);
     cudaFree(ctx->d_qrot);
     delete ctx;
     return RQ_ERR_CUDA;
@@ -328,6 +367,7 @@ int rq_create(rq_ctx** out, const rq_config* cfg) {
   g.dense32 = ctx->d_dense32;
   g.rotq = ctx->d_rotq;
   g.rot_vt = dense ? ctx->d_dense32 + 2 * rot : nullptr;
+  g.code_table = ctx->d_codetab;
   g.centroids = ctx->d_tables + 2 * rot;  // c / c_scale
   g.boundaries = ctx->d_tables + 2 * rot + 256;
   *out = ctx;
@@ -344,6 +384,7 @@ void rq_free(rq_ctx* ctx) {
     cudaFree(ctx->d_dense16);
     cudaFree(ctx->d_dense32);
     cudaFree(ctx->d_rotq);
+    cudaFree(ctx->d_codetab);
     cudaFree(ctx->d_qrot);
   }
   delete ctx;

@@ -279,7 +279,8 @@ constexpr uint32_t kSS = kX + 65536;              // partial sums of squares: f3
 constexpr uint32_t kBar = kSS + 2 * kRows * 16 * 4;
 constexpr uint32_t kBarXFull = 0, kBarXEmpty = 16, kBarYFull = 32, kBarYEmpty = 48, kBarDrain = 64;
 constexpr uint32_t kTmemSlot = 72, kAbort = 76;
-constexpr int kSmem = (int)kBar + 128 + 1024;     // + slack to align the window to 1024 bytes
+constexpr uint32_t kTab = kBar + 128;             // the binned code table: u32 [kCodeBins][2]
+constexpr int kSmem = (int)kTab + kCodeBins * 8 + 1024;  // + slack to align the window to 1024 bytes
 constexpr uint32_t kTmemCols = 256;
 }  // namespace dtc
 
@@ -361,6 +362,10 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
       *reinterpret_cast<uint4*>(sm + kR + hl * 32768 + (c >> 3) * 16384 + tc::sw128(row, c & 7)) = __ldg(rsrc + i);
     }
   }
+  const uint2* const tab = g.code_table ? reinterpret_cast<const uint2*>(sm + kTab) : nullptr;
+  if (tab)
+    for (int i = tid; i < kCodeBins; i += kThreads)
+      reinterpret_cast<uint2*>(sm + kTab)[i] = __ldg(reinterpret_cast<const uint2*>(g.code_table) + i);
   tc::fence_async_smem();  // read by the tensor core (async proxy)
   tc::fence_before_sync();
   __syncthreads();
@@ -441,11 +446,20 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
         tc::tmem_wait_ld();
         int code[16];
         uint32_t todo = 0;
+        if (tab) {  // the same codes and the same coordinates to recompute as the select tree
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float dm;
-          code[e] = code_of_margin<BITS>(y[e] * rcp, bnd, dm);
-          if (dm < kFixBand && store) todo |= 1u << e;
+          for (int e = 0; e < 16; ++e) {
+            bool near;
+            code[e] = code_of_table(y[e] * rcp, tab, near);
+            if (near && store) todo |= 1u << e;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float dm;
+            code[e] = code_of_margin<BITS>(y[e] * rcp, bnd, dm);
+            if (dm < kFixBand && store) todo |= 1u << e;
+          }
         }
         while (__any_sync(0xffffffffu, todo != 0)) {  // exact recompute, one coordinate at a time
           const uint32_t want = __ballot_sync(0xffffffffu, todo != 0);

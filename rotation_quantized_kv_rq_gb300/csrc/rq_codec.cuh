@@ -9,6 +9,7 @@
 #include <stdint.h>
 
 #include "../../include/rq.h"
+#include "rq_internal.h"
 
 namespace rq {
 namespace codec {
@@ -255,6 +256,20 @@ __device__ __forceinline__ float dot_compensated(const float (&x)[8], const floa
 // Cauchy-Schwarz) plus the accumulation of 16 fp32 MMA steps (a few fp32 ulps of n each); an fp32
 // chain of 128 multiply-adds stays well inside it too.
 constexpr float kFixBand = 1e-5f;
+
+// code_of through the binned code table in shared memory (rq_internal.h): the bin is
+// RNE(u * kCodeBinScale) (u times a power of two is exact, and adding 1.5 * 2^23 rounds it to an
+// integer in the low mantissa bits), clamped to the out-of-range entry; near = u lies within
+// kFixBand of a boundary.  The bin's one boundary is the only one within 2e-5 of it, so both
+// equal what the select tree and code_of_margin decide, NaN included (code 0, not near).
+__device__ __forceinline__ int code_of_table(float u, const uint2* tab, bool& near) {
+  const float t = fmaf(u, (float)kCodeBinScale, 12582912.f);
+  const uint32_t k = min(__float_as_uint(t) - (0x4B400000u - (uint32_t)kCodeBinHalf), (uint32_t)(kCodeBins - 1));
+  const uint2 e = tab[k];
+  const float b = __uint_as_float(e.y);
+  near = fabsf(u - b) < kFixBand;
+  return (int)e.x + (u > b ? 1 : 0);
+}
 
 // Codes of one vector under a dense rotation, a half-warp per vector (lane j: dims 8j..8j+7):
 // raw = the lane's 16 bytes of x (fp16), y = its 8 coordinates of the approximate R x.  Each

@@ -11,6 +11,16 @@ constexpr int kHeadDim = 128;
 constexpr int kAttnWarps = 16;      // warps per split-K attention CTA (one CTA per SM)
 constexpr int kAttnPairTokens = 32; // tokens a warp takes per iteration (two 16-token tiles)
 
+// Binned code table: u in [-kCodeBinHalf, kCodeBinHalf) / kCodeBinScale falls in bin
+// k = RNE(u * kCodeBinScale) + kCodeBinHalf (bins 1 / kCodeBinScale wide); entry k = {the count
+// of boundaries below the bin, the one boundary within 2e-5 of the bin or +inf}, so that the
+// code is count + (u > boundary) and the boundary is the only one u can lie within 1e-5 of.
+// Entry kCodeBins - 1 takes every u outside the range (none for a unit vector's coordinates)
+// and NaN: code 0, as the boundary count gives.
+constexpr int kCodeBinScale = 2048;
+constexpr int kCodeBinHalf = 2304;
+constexpr int kCodeBins = 2 * kCodeBinHalf + 1;
+
 // Device-side copy of what every kernel needs to know about a context.
 struct Geometry {
   int num_q_heads;
@@ -45,6 +55,9 @@ struct Geometry {
   // dense only: device fp32 [Hkv][128][128] R_v TRANSPOSED ([m][i] = R_v[i][m]: a decode step's
   // V coding stages it as it is); null otherwise.
   const float* rot_vt;
+  // device u32 [kCodeBins][2] (count, boundary bits): the binned code table, or null when two
+  // boundaries are too close for its bins (the select tree decides then)
+  const uint32_t* code_table;
   const float* centroids;   // device [2^bits]: c / out_scale, the fp16 operands' source
   const float* boundaries;  // device [2^bits - 1]
 };

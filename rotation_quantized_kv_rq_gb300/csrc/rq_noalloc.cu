@@ -111,6 +111,7 @@ extern "C" int rq_decode_attention_noalloc(const rq_config* cfg, const float* d_
   g.dense32 = nullptr;
   g.rotq = nullptr;
   g.rot_vt = nullptr;
+  g.code_table = nullptr;
   g.centroids = d_centroids;
   g.boundaries = nullptr;  // decode never codes
 
