@@ -376,6 +376,9 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
     // ================= coding: thread = (row, part ch of the dims) =================
     const int row = 32 * (warp & 3) + lane, ch = warp >> 2;  // dims kPartDims ch .. + kPartDims - 1
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    // the four warps of a lane quarter (warp % 4: the same 32 rows, a quarter of the dims each)
+    // exchange their rows' partial sums of squares at named barrier 1 + warp % 4
+    const uint32_t quarter_bar = 1u + (uint32_t)(warp & 3);
     float bnd[15];
     load_boundaries<BITS>(bnd, g.boundaries);
     const PageSplit split(g.page_size);
@@ -392,11 +395,11 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
       if (!store) slot = 0;
       ok = tc::role_wait(mb + kBarXFull + 8 * b, (uint32_t)((i >> 1) & 1), abort_flag) &&
            tc::role_wait(mb + kBarYFull + 8 * b, (uint32_t)((i >> 1) & 1), abort_flag);
-      {  // agree across the coding warps (they meet at a named barrier below)
+      {  // agree across the quarter's coding warps (they meet at a named barrier below)
         uint32_t all_ok;
-        asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+        asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
                      : "=r"(all_ok)
-                     : "r"((uint32_t)ok), "n"(kCodeThreads)
+                     : "r"((uint32_t)ok), "r"(quarter_bar), "n"(kCodeThreads / 4)
                      : "memory");
         ok = all_ok != 0;
       }
@@ -423,7 +426,7 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
         for (int e = 0; e < 8; ++e) ps += x[e] * x[e];
         ss[cc * kRows] = ps;
       }
-      asm volatile("bar.sync 1, %0;" ::"n"(kCodeThreads) : "memory");  // both halves' sums are in
+      asm volatile("bar.sync %0, %1;" ::"r"(quarter_bar), "n"(kCodeThreads / 4) : "memory");  // the row's sums are in
       float a8[8];
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) a8[jj] = ss[jj * kRows] + ss[(jj + 8) * kRows];
