@@ -441,12 +441,15 @@ append_dense_tc_kernel(Geometry g, const __half* __restrict__ k, const __half* _
       uint8_t* const vsec = chunk + (size_t)g.page_size * vb;
       const int vpair = off >> 1, hv = off & 1;
       uint32_t w2 = 0u;  // 3-bit: the high bits of the current 32-dim group
-#pragma unroll 1
-      for (int q0 = 0; q0 < kPartDims / 16; ++q0) {  // coordinates 16 q .. 16 q + 15
-        const int q = (kPartDims / 16) * ch + q0;  // the 16-dim unit of the vector
-        float y[16];
-        tc::tmem_ld16(tmem + lane_off + 128 * b + 16 * q, y);
-        tc::tmem_wait_ld();
+      static_assert(kPartDims == 32, "two 16-dim units a thread");
+      float yy[2][16];  // both units' y, loaded together (one wait)
+      tc::tmem_ld16(tmem + lane_off + 128 * b + 32 * ch, yy[0]);
+      tc::tmem_ld16(tmem + lane_off + 128 * b + 32 * ch + 16, yy[1]);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int q0 = 0; q0 < 2; ++q0) {  // coordinates 16 q .. 16 q + 15
+        const int q = 2 * ch + q0;       // the 16-dim unit of the vector
+        const float(&y)[16] = yy[q0];
         int code[16];
         uint32_t todo = 0;
         if (tab) {  // the same codes and the same coordinates to recompute as the select tree
