@@ -41,9 +41,19 @@ def make_case(mode, bits, hq, hkv, P, lens, T=1, seed=7, zero_tokens=(), permute
     return wl, kv, q
 
 
-def run_both(wl, kv, q):
+def with_codebook(oc, codebook):
+    """The oracle cache with a caller's codebook instead of the default: its centroids, and the
+    midpoints between them as the boundaries (the nearest-centroid rule)."""
+    if codebook is not None:
+        c = np.asarray(codebook, np.float32)
+        oc.centroids = c.copy()
+        oc.boundaries = (0.5 * (c[:-1].astype(np.float64) + c[1:].astype(np.float64))).astype(np.float32)
+    return oc
+
+
+def run_both(wl, kv, q, codebook=None):
     s = wl.spec
-    oc = PT.oracle_cache(wl)
+    oc = with_codebook(PT.oracle_cache(wl), codebook)
     margins, tokens, seq_of = {}, [], {}
     flat_k, flat_v, flat_slots = [], [], []
     ti = 0
@@ -66,7 +76,8 @@ def run_both(wl, kv, q):
     ref = oc.attention(q, wl.block_table, wl.seq_lens, T=T)
 
     cache = rq.KVCache(s.mode, s.bits, s.num_q_heads, s.num_kv_heads, s.page_size, wl.num_pages, wl.rot_k, wl.rot_v,
-                       max_batch=s.batch, max_query_tokens=T, max_pages_per_seq=wl.block_table.shape[1])
+                       max_batch=s.batch, max_query_tokens=T, max_pages_per_seq=wl.block_table.shape[1],
+                       codebook=codebook)
     K = np.concatenate(flat_k)
     V = np.concatenate(flat_v)
     cache.append(PT.to_dev(K), PT.to_dev(V), PT.to_dev(np.concatenate(flat_slots)))
@@ -83,7 +94,7 @@ def run_both(wl, kv, q):
 
     # the oracle's attention over the GPU's own packed bytes: whatever codes the GPU decided,
     # its attention over them must match this strictly
-    og = PT.oracle_cache(wl)
+    og = with_codebook(PT.oracle_cache(wl), codebook)
     og.pages[:] = gpu_pages.reshape(-1)
     ref_own = og.attention(q, wl.block_table, wl.seq_lens, T=T)
 
@@ -145,6 +156,26 @@ def test_append_and_attention_match_oracle(case, capsys):
     PT.assert_close(r["out"], r["ref_own"], "append + attention, against the oracle over the GPU's own pages")
     allowed = {(r["seq_of"][ti], h) for ti, h in flips}
     PT.assert_close_except(r["out"], r["ref"], hq // hkv, allowed, "append + attention")
+
+
+def test_dense_append_with_boundaries_closer_than_a_table_bin(capsys):
+    """A codebook whose two middle boundaries (0 and 2e-4) fall in one bin of the binned code
+    table (bins 1/2048 wide): the context keeps no table, the dense append decides every code by
+    the select tree, and codes and attention still match the oracle's."""
+    cents, _ = O.codebook(3, 128)
+    c = cents.astype(np.float64)
+    c[3], c[4], c[5] = -1e-4, 1e-4, 3e-4
+    assert np.all(np.diff(c) > 0)
+    wl, kv, q = make_case(DENSE, 3, 32, 8, 16, [300, 77], 1, seed=11)
+    r = run_both(wl, kv, q, codebook=c.astype(np.float32))
+    assert r["status"] == 0
+    flips = set()
+    compared, in_band = PT.compare_chunks(r["gpu_pages"], r["oc"], r["tokens"], r["margins"], r["inputs"], flips)
+    with capsys.disabled():
+        print(f" [{compared} codes, {in_band} within 1e-6 of a boundary]", end="")
+    assert in_band <= max(2, compared // 100000), (in_band, compared)
+    PT.assert_close(r["out_on_oracle_pages"], r["ref"], "attention over the oracle's pages")
+    PT.assert_close(r["out"], r["ref_own"], "append + attention, against the oracle over the GPU's own pages")
 
 
 @pytest.mark.parametrize("plant", ["rot_v", "rot_k", "boundary", "centroid"])
