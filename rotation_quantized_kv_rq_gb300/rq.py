@@ -50,6 +50,8 @@ _lib = None
 def lib(path: str | None = None) -> ctypes.CDLL:
     """Load librq.so (building it with nvcc first if it is missing or stale)."""
     global _lib
+    if _lib is not None and path is None:  # loaded: no lock on the call path
+        return _lib
     with _lock:
         if _lib is None:
             L = ctypes.CDLL(path or _build.build())
@@ -99,16 +101,17 @@ def _check(fn: str, code: int):
 
 
 def _ptr(t):
+    """An address for a c_void_p argument (ctypes converts the int itself)."""
     if t is None:
         return None
     if isinstance(t, torch.Tensor):
-        return ctypes.c_void_p(t.data_ptr())
-    return ctypes.c_void_p(int(t))
+        return t.data_ptr()
+    return int(t)
 
 
-def _stream(stream, device) -> ctypes.c_void_p:
+def _stream(stream, device) -> int:
     s = stream if stream is not None else torch.cuda.current_stream(device)
-    return ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
+    return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
 
 
 def rq_lloyd_max_codebook(bits: int, head_dim: int = HEAD_DIM) -> np.ndarray:
