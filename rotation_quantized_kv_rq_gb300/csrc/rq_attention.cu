@@ -113,8 +113,8 @@ __host__ __device__ __forceinline__ int unit_rounds(int len) {
   return ((len + 15) / 16 + Shape<NT>::kRoundTiles - 1) / Shape<NT>::kRoundTiles;
 }
 
-// Where a CTA stands in its range [x, x_end) of rounds: sequence b, whose units' rounds start
-// at cumb.  Kept in shared memory (thread 0 advances it between fragments) so that none of it
+// Where a CTA stands in its range [x, x_end) of the partition's cost: sequence b, whose units'
+// cost starts at cumb (a unit of rb rounds costs rb + the fragment overhead, see frag_at).  Kept in shared memory (thread 0 advances it between fragments) so that none of it
 // occupies registers during the tile loop.
 struct Walk {
   long long x, x_end, cumb;
@@ -131,18 +131,24 @@ constexpr int kTailBytes = kMaxSplitPages * 4 + (kSlotsTotal / 2) * 8 + 64 + kWa
 
 // The fragment at the walk's position: rounds [r0, r1) of the rb rounds of unit uib of
 // sequence b (uib = kv head * units per head + unit of the head), i.e. its tiles [t0, t1) of tb.
+// The partition splits cost, not rounds: unit u of a sequence covers [cumb + u C, cumb + (u + 1)
+// C) with C = rb + kFragmentRounds, its first kFragmentRounds standing for the work of opening a
+// fragment, the rest for its rounds, so a range that crosses many small units is shorter in
+// rounds.  A range that ends inside a unit's opening part takes none of its rounds (r1 <= r0).
 struct Frag {
   int tb, rb, uib, r0, r1, t0, t1;
 };
 template <int NT>
 __device__ __forceinline__ Frag frag_at(const Walk& w) {
+  constexpr int F = Shape<NT>::kFragmentRounds;
   Frag f;
   f.tb = (w.len + 15) / 16;
   f.rb = max(unit_rounds<NT>(w.len), 1);      // >= 1 whenever the walk has work left
-  const int off = (int)(w.x - w.cumb);        // < the rounds of one sequence's units
-  f.uib = off / f.rb;
-  f.r0 = off % f.rb;
-  f.r1 = (int)min((long long)f.rb, f.r0 + (w.x_end - w.x));
+  const int c = f.rb + F;
+  const long long off = w.x - w.cumb;         // < the cost of one sequence's units
+  f.uib = (int)(off / c);
+  f.r0 = max((int)(off % c) - F, 0);
+  f.r1 = (int)min((long long)f.rb, w.x_end - w.cumb - (long long)f.uib * c - F);
   f.t0 = f.r0 * Shape<NT>::kRoundTiles;
   f.t1 = min(f.tb, f.r1 * Shape<NT>::kRoundTiles);
   return f;
@@ -714,9 +720,12 @@ __device__ __forceinline__ void rotated_query(float (&y)[32], const Geometry& g,
 template <typename I>
 __device__ __forceinline__ void partition(I total, I n_units, I max_rounds, I grid, I cta, I frag_rounds,
                                           long long& x0, long long& x1) {
-  I parts = min(grid, total);
-  if (n_units > 0 && n_units <= grid && total == n_units * max_rounds) {
-    const I per_part = (total + parts - 1) / parts;
+  // total: the cost of all units (rounds + frag_rounds each); whole units, one a CTA, when they
+  // are all alike and that beats splitting the rounds over the grid
+  const I rounds = total - n_units * frag_rounds;
+  I parts = min(grid, rounds);
+  if (n_units > 0 && n_units <= grid && rounds == n_units * max_rounds) {
+    const I per_part = (rounds + parts - 1) / parts;
     const I cost_split = per_part + (max_rounds % per_part == 0 ? 1 : 2) * frag_rounds;
     if (max_rounds + frag_rounds <= cost_split) parts = n_units;
   }
@@ -735,12 +744,15 @@ __device__ __forceinline__ int clamp_len(const AttnArgs& a, int b, int cap) {
   return l < 0 ? 0 : (l > cap ? cap : l);
 }
 
-// Moves a walk past the fragment f it stands on (thread 0, between fragments).
+// Moves a walk past the fragment f it stands on (thread 0, between fragments): to the next
+// unit's cost when f finished its unit, else to the end of the range.
+template <int NT>
 __device__ __forceinline__ void walk_advance(Walk& w, const Frag& f, int upb, const AttnArgs& a, int cap) {
-  w.x += f.r1 - f.r0;
+  const int c = f.rb + Shape<NT>::kFragmentRounds;
+  w.x = f.r1 == f.rb ? w.cumb + (long long)(f.uib + 1) * c : w.x_end;
   if (w.x >= w.x_end) return;  // the range is done: no next sequence to look up
-  if (f.r1 == f.rb && f.uib == upb - 1) {  // sequence b is done: on to the next one with tiles
-    w.cumb += (long long)f.rb * upb;
+  if (f.uib == upb - 1) {  // sequence b is done: on to the next one with tiles
+    w.cumb += (long long)c * upb;
     for (++w.b; w.x < w.x_end && w.b < a.B; ++w.b) {
       w.len = clamp_len(a, w.b, cap);
       if (w.len > 0) break;
@@ -896,8 +908,8 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
   uint32_t phase = 0;   // bit st: parity of the next completion of stage st
   bool broken = false;  // a staged copy never completed: stop using the ring
 
-  // ---- this CTA's range [x, x_end) of rounds in the stream-K partition ----
-  // cum[b] = rounds of all units of sequences < b and lens[b] = sequence b's clamped tokens,
+  // ---- this CTA's range [x, x_end) of cost in the stream-K partition ----
+  // cum[b] = cost of all units of sequences < b (frag_at) and lens[b] = sequence b's clamped tokens,
   // built with a block scan at the start of the window: slots and table, unused before the
   // first fragment (at most 8001 x 8 + 8000 x 4 bytes; the table and the 64 slots span more).
   const int n_ug = (a.n_tiles_n + NT - 1) / NT;  // units per kv head
@@ -920,10 +932,10 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
           if (blockIdx.x == 0 && a.status) atomicOr(a.status, RQ_STATUS_BAD_LEN);
           len = len < 0 ? 0 : (len > cap ? cap : len);
         }
-        v = (long long)unit_rounds<NT>(len) * upb;
+        v = len > 0 ? (long long)(unit_rounds<NT>(len) + Shape<NT>::kFragmentRounds) * upb : 0;
         lens[bb] = len;
       }
-      int nu = v > 0 ? upb : 0, mr = (int)(v / upb);
+      int nu = v > 0 ? upb : 0, mr = v > 0 ? (int)(v / upb) - Shape<NT>::kFragmentRounds : 0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         nu += __shfl_xor_sync(0xffffffffu, nu, o);
@@ -987,13 +999,14 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     __syncthreads();  // the scratch is slot and table space from here on
   }
 
-  // Every fragment advances the walk by at least one round, so this bound (the range's rounds)
-  // is never reached; it only guarantees that the loop ends.
+  // Every fragment advances the walk by at least one unit of cost, so this bound (the range's
+  // cost) is never reached; it only guarantees that the loop ends.
   const long long max_fragments = walk->x_end - walk->x;
   for (long long n_frag = 0; n_frag < max_fragments; ++n_frag) {
     if (walk->x >= walk->x_end) break;
     const int len = walk->len;
     const Frag fr = frag_at<NT>(*walk);
+    if (fr.r1 <= fr.r0) break;  // the range ends inside a unit's opening cost: nothing left
     const int t1 = fr.t1;
     struct {
       int b, h, nt0;
@@ -1444,7 +1457,7 @@ attn_splitk_kernel(const Geometry g, const AttnArgs a, int smem_bytes) {
     __syncthreads();  // the merge buffer reuses slot space
     if (threadIdx.x == 0) {
       Walk w = *walk;
-      walk_advance(w, frag_at<NT>(w), upb, a, cap);
+      walk_advance<NT>(w, frag_at<NT>(w), upb, a, cap);
       *walk = w;
     }
     __syncthreads();
