@@ -9,11 +9,11 @@
 // Kernel design (sm_103a):
 //   * One CTA of 16 warps per SM, stream-K partition: the work of all units (sequence, kv head,
 //     query n-tile), in that order, counted in rounds -- 32 consecutive 16-token tiles, one
-//     pair of tiles per warp -- is cut into gridDim.x equal contiguous ranges, so every SM gets
-//     the same number of rounds whatever the lengths.  The part of a unit that falls in one
-//     CTA's range is a fragment: the CTA stages its page ids in shared memory, the warps take
-//     its tiles two at a time round-robin, and their (m, l, O) are merged through shared
-//     memory into one partial per fragment.
+//     pair of tiles per warp -- plus a fixed cost per unit for opening a fragment on it, is cut
+//     into gridDim.x equal contiguous ranges, so every SM gets about the same work whatever the
+//     lengths.  The part of a unit that falls in one CTA's range is a fragment: the CTA stages
+//     its page ids in shared memory, the warps take its tiles two at a time round-robin, and
+//     their (m, l, O) are merged through shared memory into one partial per fragment.
 //   * Per 16-token tile both contractions run on the tensor cores with mma.sync m16n8k16
 //     (fp16 in, fp32 accumulate): S^T[16 tok x 8 q] = K~[16 x 128] q~^T and
 //     O^T[128 x 8 q] += V~^T[128 x 16 tok] P^T.  The <= 8 query rows of a kv head (the GQA
